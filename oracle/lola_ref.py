@@ -1,0 +1,249 @@
+"""CPU float64 oracle for LoLA hybrid attention -- TEST INFRASTRUCTURE ONLY.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package.  The CUDA library never calls it and shares no code with it.
+
+Source: "LoLA: Low-Rank Linear Attention With Sparse Caching" (arXiv 2505.23666v3),
+Chinese reading notes, sections 2.1-2.7.  Per attention head:
+
+* feature map (section 2.2, Eq. 3; the configured form): ``phi(x) = [softmax(W x), softmax(-W x)]``
+  with ``W`` of shape (D/2, d_k), so ``phi(x)`` is strictly positive and each half sums to 1;
+* linear memory (section 2.2, Eqs. 3-5): ``H += phi(k) v^T``, ``s += phi(k)``, read-out
+  ``H^T phi(q) / (phi(q)^T s)``; only KV actually assigned to the state are added;
+* self-recall error (section 2.3, Eq. 10): ``SRE(k, v | H, s) = || H^T phi(k) / (phi(k)^T s) - v ||_2``
+  (the L2 norm, not its square);
+* per-token allocation (section 2.4, Eqs. 11-13, "score, then write" as in appendix H):
+  the new KV enters the sliding window; once the window holds more than eta entries the
+  oldest one leaves and joins the candidates ``E = G ∪ {evictee}``; if ``|E| <= lambda`` all
+  are kept, otherwise the lambda highest-SRE candidates (scored against the state *before*
+  this step's write) stay in the sparse cache G and the rest are written into (H, s) once;
+* co-normalised output (section 2.5, Eq. 14): one shared denominator over the linear
+  memory, the sparse cache and the window, with ``a = exp(q^T k / sqrt(d_k))``.
+
+Readings taken where the notes are silent (each is listed in the design notes):
+
+* R0: the per-token rule above is the definition; the prefill chunk length C only
+  schedules work and never changes which KV are kept (section 2.6's chunk-granular
+  allocation is a different variant, not this one);
+* the window includes the current token: ``W_t = {max(0, t-eta+1) .. t}``, evictee ``t-eta``;
+* empty-state rule (section 2.6 notes that H = 0, s = 0 makes the SRE division undefined):
+  when ``phi(k)^T s = 0`` the memory predicts 0, so ``SRE = ||v||``;
+* exact capacity with ties broken towards the older token: among equal SREs the smaller
+  position is written; SRE order is compared through SRE^2 (same order);
+* the output is read after this step's write, with H_t, G_t and W_t (so every token
+  <= t is in exactly one of window, cache, state);
+* only the softmax branch carries the 1/sqrt(d_k) temperature; the linear branch is the
+  plain ``phi(q)^T phi(k)``.  The max-subtraction in the output is for range only.
+
+Three formulations live here and in ``lola_inc.c``: ``lola_run`` (running H, s; all
+SREs recomputed from H each step), ``lola_set`` (no running state: H is re-summed from
+the written set every step) and the C incremental form.  Tests check that they agree,
+and pin them to closed forms that the method reduces to.
+"""
+from __future__ import annotations
+
+import math
+from collections import deque
+
+import numpy as np
+
+
+def phi(x: np.ndarray, W: np.ndarray) -> np.ndarray:
+    """Feature map ``[softmax(W x), softmax(-W x)]`` over the last axis of ``x`` (float64)."""
+    z = np.asarray(x, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T
+    out = []
+    for zz in (z, -z):
+        e = np.exp(zz - zz.max(axis=-1, keepdims=True))
+        out.append(e / e.sum(axis=-1, keepdims=True))
+    return np.concatenate(out, axis=-1)
+
+
+def sre_sq(H: np.ndarray, s: np.ndarray, phik: np.ndarray, v: np.ndarray) -> float:
+    """Squared self-recall error of (k, v) against memory (H, s) (section 2.3, Eq. 10).
+
+    Empty-memory reading: if ``phi(k)^T s == 0`` the memory predicts 0 and SRE = ||v||."""
+    den = float(phik @ s)
+    if den == 0.0:
+        return float(v @ v)
+    r = (H.T @ phik) / den - v
+    return float(r @ r)
+
+
+def _output(qt, phiq, exact, K, V, H_num, den_lin, scale):
+    """Co-normalised read (section 2.5, Eq. 14).  ``H_num = H^T phi(q)``, ``den_lin = phi(q)^T s``."""
+    if len(exact):
+        idx = np.fromiter(exact, dtype=np.int64)
+        a = (K[idx] @ qt) * scale
+        m = a.max()
+        w = np.exp(a - m)
+        em = math.exp(-m)
+        num = w @ V[idx] + em * H_num
+        den = w.sum() + em * den_lin
+    else:
+        num, den = H_num, den_lin
+    return num / den
+
+
+def lola_run(q, k, v, W, eta: int, lam: int, replay=None):
+    """Per-token LoLA on one head with a running (H, s); float64.
+
+    ``q, k``: (n, d_k); ``v``: (n, d_v); ``W``: (D/2, d_k).  ``replay``: optional (n,)
+    int array of the position written at each step (-1: none); when given, the oracle
+    follows those decisions instead of its own and reports how far each was from its
+    own best (relative SRE gap).
+
+    Returns a dict with Y (n, d_v), write_pos (n,), write_step (n,), H, s, cache
+    (sorted positions), window (positions), min_gap (smallest relative SRE gap between
+    the best and the second-best candidate over all decisions of a free run), max_gap
+    and mismatches (replay only).
+    """
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n, dk = k.shape
+    dv = v.shape[1]
+    PQ, PK = phi(q, W), phi(k, W)
+    D = PK.shape[1]
+    scale = 1.0 / math.sqrt(dk)
+    H = np.zeros((D, dv))
+    s = np.zeros(D)
+    window: deque[int] = deque()
+    cache: list[int] = []
+    write_pos = np.full(n, -1, np.int64)
+    write_step = np.full(n, -1, np.int64)
+    Y = np.zeros((n, dv))
+    min_gap, max_gap, mismatches = math.inf, 0.0, 0
+    for t in range(n):
+        window.append(t)
+        E = list(cache)
+        if len(window) > eta:
+            E.append(window.popleft())
+        if len(E) <= lam:
+            cache = E
+            if replay is not None and replay[t] != -1:
+                raise ValueError(f"replay writes at step {t} but no write is due")
+        else:
+            sq = {j: sre_sq(H, s, PK[j], v[j]) for j in E}
+            best = min(E, key=lambda j: (sq[j], j))
+            if len(E) > 1:
+                second = min((j for j in E if j != best), key=lambda j: (sq[j], j))
+                sb, s2 = math.sqrt(sq[best]), math.sqrt(sq[second])
+                gap = (s2 - sb) / sb if sb > 0 else (math.inf if s2 > 0 else 0.0)
+                min_gap = min(min_gap, gap)
+            w = best
+            if replay is not None:
+                w = int(replay[t])
+                if w not in sq:
+                    raise ValueError(f"replay writes position {w} at step {t}, not a candidate")
+                if w != best:
+                    mismatches += 1
+                    sb, sw = math.sqrt(sq[best]), math.sqrt(sq[w])
+                    gap = (sw - sb) / sb if sb > 0 else (math.inf if sw > 0 else 0.0)
+                    max_gap = max(max_gap, gap)
+            H += np.outer(PK[w], v[w])
+            s += PK[w]
+            write_pos[t] = w
+            write_step[w] = t
+            cache = [j for j in E if j != w]
+        exact = list(window) + cache
+        Y[t] = _output(q[t], PQ[t], exact, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
+    return dict(Y=Y, write_pos=write_pos, write_step=write_step, H=H, s=s,
+                cache=np.array(sorted(cache), np.int64), window=np.array(list(window), np.int64),
+                min_gap=min_gap, max_gap=max_gap, mismatches=mismatches)
+
+
+def lola_set(q, k, v, W, eta: int, lam: int):
+    """Brute-force LoLA with no running state (small n only).
+
+    Every quantity is summed from explicit sets each step: the memory read-out for a
+    key c is ``sum_{j in S} (phi_c . phi_j) v_j / sum_{j in S} phi_c . phi_j`` over the
+    written set S, and the output's linear terms are ``sum_{j in S} (phi_q . phi_j) v_j``
+    and ``sum_{j in S} phi_q . phi_j``.  Same decisions and outputs as ``lola_run`` in
+    exact arithmetic."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n, dk = k.shape
+    PQ, PK = phi(q, W), phi(k, W)
+    scale = 1.0 / math.sqrt(dk)
+    written: list[int] = []
+    cache: list[int] = []
+    write_pos = np.full(n, -1, np.int64)
+    write_step = np.full(n, -1, np.int64)
+    Y = np.zeros((n, v.shape[1]))
+    for t in range(n):
+        win = list(range(max(0, t - eta + 1), t + 1))
+        E = list(cache)
+        if t - eta >= 0:
+            E.append(t - eta)
+        if len(E) <= lam:
+            cache = E
+        else:
+            def err2(c):
+                g = np.array([PK[c] @ PK[j] for j in written])
+                if len(written) == 0 or g.sum() == 0.0:
+                    return float(v[c] @ v[c])
+                r = (g @ v[written]) / g.sum() - v[c]
+                return float(r @ r)
+            sq = {j: err2(j) for j in E}
+            w = min(E, key=lambda j: (sq[j], j))
+            written.append(w)
+            write_pos[t] = w
+            write_step[w] = t
+            cache = [j for j in E if j != w]
+        gl = np.array([PQ[t] @ PK[j] for j in written]) if written else np.zeros(0)
+        num_lin = gl @ v[written] if written else np.zeros(v.shape[1])
+        Y[t] = _output(q[t], PQ[t], win + cache, k, v, num_lin, float(gl.sum()), scale)
+    return dict(Y=Y, write_pos=write_pos, write_step=write_step,
+                cache=np.array(sorted(cache), np.int64), written=np.array(written, np.int64))
+
+
+# ---------------------------------------------------------------------------
+# Closed forms the method reduces to (used as pins)
+# ---------------------------------------------------------------------------
+
+def causal_softmax_attention(q, k, v):
+    """Textbook causal softmax attention, ``softmax(q k^T / sqrt(d_k))`` over j <= t."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n = q.shape[0]
+    a = (q @ k.T) / math.sqrt(q.shape[1])
+    a = np.where(np.tril(np.ones((n, n), bool)), a, -np.inf)
+    p = np.exp(a - a.max(axis=1, keepdims=True))
+    return (p / p.sum(axis=1, keepdims=True)) @ v
+
+
+def linear_attention(q, k, v, W):
+    """Causal linear attention with the inclusive recurrence of section 2.2 (Eqs. 3-5):
+    ``y_t = sum_{j<=t} (phi_q . phi_j) v_j / sum_{j<=t} phi_q . phi_j``."""
+    PQ, PK = phi(q, W), phi(k, W)
+    A = np.tril(PQ @ PK.T)
+    return (A @ np.asarray(v, np.float64)) / A.sum(axis=1, keepdims=True)
+
+
+def window_plus_linear(q, k, v, W, eta: int):
+    """lambda = 0: softmax over the last eta tokens (inclusive) and the linear state over
+    every token <= t - eta, one shared denominator (the LoLCATs base, section 3.1)."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n = q.shape[0]
+    PQ, PK = phi(q, W), phi(k, W)
+    t = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    in_win = (j <= t) & (j > t - eta)
+    in_state = j <= t - eta
+    a = (q @ k.T) / math.sqrt(q.shape[1])
+    m = np.where(in_win, a, -np.inf).max(axis=1, keepdims=True)
+    m = np.where(np.isfinite(m), m, 0.0)
+    ws = np.where(in_win, np.exp(np.where(in_win, a, 0.0) - m), 0.0)
+    wl = np.where(in_state, PQ @ PK.T, 0.0) * np.exp(-m)
+    wt = ws + wl
+    return (wt @ v) / wt.sum(axis=1, keepdims=True)
+
+
+def state_elements(t: int, dk: int, dv: int, D: int, eta: int, lam: int) -> int:
+    """Per-head element count of the persistent memory (appendix B):
+    ``min{t (d_k + d_v), (eta + lambda)(d_k + d_v) + D d_v + D}``."""
+    return min(t * (dk + dv), (eta + lam) * (dk + dv) + D * dv + D)

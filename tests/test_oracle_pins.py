@@ -1,0 +1,279 @@
+"""Pins of the CPU oracle to facts fixed outside it: hand-derived worked examples,
+closed forms the method reduces to, library routines, invariants and brute force.
+
+Source of every rule: "LoLA: Low-Rank Linear Attention With Sparse Caching"
+(arXiv 2505.23666v3) reading notes, sections 2.2-2.7."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import inc
+from oracle import lola_ref as R
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _load(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        g = json.load(f)
+    return {k: (np.array(v, dtype=np.float64) if isinstance(v, list) and k not in ("derivation",) else v)
+            for k, v in g.items()}
+
+
+def _all_forms(q, k, v, W, eta, lam):
+    """The three oracle formulations on one head (float32 inputs for the C form)."""
+    a = R.lola_run(q, k, v, W, eta, lam)
+    b = R.lola_set(q, k, v, W, eta, lam)
+    c = inc.run(np.asarray(q, np.float32)[None], np.asarray(k, np.float32)[None],
+                np.asarray(v, np.float32)[None], np.asarray(W, np.float32), eta, lam, "f32")
+    c1 = {key: (val[0] if isinstance(val, np.ndarray) and val.ndim >= 1 else val) for key, val in c.items()}
+    return a, b, c1
+
+
+# ---------------------------------------------------------------------------
+# feature map
+# ---------------------------------------------------------------------------
+
+def test_phi_matches_library_softmax():
+    from scipy.special import softmax
+    x = synth.gauss_inputs(1, 1, 17, 16, 12, "f32", seed=3)
+    q = x.q[0, 0].astype(np.float64)
+    W = x.W.astype(np.float64)
+    z = q @ W.T
+    want = np.concatenate([softmax(z, axis=-1), softmax(-z, axis=-1)], axis=-1)
+    got = R.phi(q, W)
+    np.testing.assert_allclose(got, want, rtol=1e-14, atol=0)
+    assert (got > 0).all()
+    np.testing.assert_allclose(got[:, :6].sum(-1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(got[:, 6:].sum(-1), 1.0, rtol=1e-14)
+
+
+def test_phi_zero_weight_is_uniform():
+    got = R.phi(np.random.default_rng(0).normal(size=(5, 8)), np.zeros((4, 8)))
+    np.testing.assert_array_equal(got, np.full((5, 8), 0.25))
+
+
+# ---------------------------------------------------------------------------
+# SRE closed forms
+# ---------------------------------------------------------------------------
+
+def test_sre_zero_for_only_written_key():
+    """A state holding only (k, v) recalls v exactly: H^T phi / phi^T s = v (phi.phi)/(phi.phi)."""
+    rng = np.random.default_rng(1)
+    W = rng.normal(size=(8, 16)) / 8
+    k, v = rng.normal(size=16), rng.normal(size=16)
+    p = R.phi(k, W)
+    assert R.sre_sq(np.outer(p, v), p.copy(), p, v) < 1e-28
+
+
+def test_sre_opposite_values_cancel():
+    """Worked example of section 2.4: two keys with the same features and values +v, -v
+    written together leave H = 0, so the read-out is 0 and each SRE equals ||v||."""
+    rng = np.random.default_rng(2)
+    W = rng.normal(size=(8, 16)) / 8
+    k, v = rng.normal(size=16), rng.normal(size=16)
+    p = R.phi(k, W)
+    H = np.outer(p, v) + np.outer(p, -v)
+    s = 2 * p
+    np.testing.assert_allclose(math.sqrt(R.sre_sq(H, s, p, v)), np.linalg.norm(v), rtol=1e-14)
+    np.testing.assert_allclose(math.sqrt(R.sre_sq(H, s, p, -v)), np.linalg.norm(v), rtol=1e-14)
+
+
+def test_sre_empty_memory_is_value_norm():
+    v = np.array([3.0, 4.0])
+    assert R.sre_sq(np.zeros((4, 2)), np.zeros(4), np.full(4, 0.25), v) == 25.0
+
+
+def test_opposite_values_read_out_zero_in_a_run():
+    """Both keys written (eta = lambda = 0): the linear read-out after step 1 is 0."""
+    rng = np.random.default_rng(4)
+    W = rng.normal(size=(4, 8)) / 8
+    kk, vv = rng.normal(size=8), rng.normal(size=8)
+    q = rng.normal(size=(2, 8))
+    k = np.stack([kk, kk])
+    v = np.stack([vv, -vv])
+    for out in _all_forms(q, k, v, W, 0, 0):
+        np.testing.assert_allclose(out["Y"][1], 0.0, atol=1e-12)
+        assert list(out["write_pos"]) == [0, 1]
+
+
+# ---------------------------------------------------------------------------
+# hand-derived worked examples (tests/golden)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["uniform_phi_mean_memory.json", "tie_breaks_to_older.json"])
+def test_golden_worked_examples(name):
+    g = _load(name)
+    eta, lam = int(g["eta"]), int(g["lambda"])
+    for out in _all_forms(g["q"], g["k"], g["v"], g["W"], eta, lam):
+        assert list(out["write_pos"]) == [int(x) for x in g["write_pos"]]
+        assert sorted(int(x) for x in out["cache"] if x >= 0) == [int(x) for x in g["final_cache"]]
+        np.testing.assert_allclose(out["Y"], g["y"], rtol=1e-13, atol=1e-13)
+        if "H" in g and "H" in out:
+            np.testing.assert_allclose(out["H"], g["H"], rtol=1e-13)
+            np.testing.assert_allclose(out["s"], g["s"], rtol=1e-13)
+
+
+# ---------------------------------------------------------------------------
+# closed forms the method reduces to
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("eta,lam", [(40, 0), (25, 15), (0, 40), (64, 64)])
+def test_no_write_is_causal_softmax_attention(eta, lam):
+    """eta + lambda >= n: nothing is ever written, so the method is full causal softmax
+    attention; checked against torch's scaled_dot_product_attention (float64, CPU)."""
+    import torch
+    x = synth.gauss_inputs(1, 1, 40, 16, 16, "f32", seed=5)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    want = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q)[None], torch.from_numpy(k)[None], torch.from_numpy(v)[None],
+        is_causal=True)[0].numpy()
+    for out in _all_forms(q, k, v, x.W, eta, lam):
+        np.testing.assert_allclose(out["Y"], want, rtol=1e-12, atol=1e-12)
+        assert (out["write_pos"] == -1).all()
+    np.testing.assert_allclose(R.causal_softmax_attention(q, k, v), want, rtol=1e-12, atol=1e-12)
+
+
+def test_zero_budget_is_linear_attention():
+    """eta = lambda = 0: every token is written at its own step, so the output is the
+    inclusive linear-attention recurrence of section 2.2 (Eqs. 3-5), here written as a
+    running sum of outer products independent of the oracle's code."""
+    x = synth.gauss_inputs(1, 1, 33, 8, 12, "f32", seed=6, dv=5)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    PQ, PK = R.phi(q, x.W), R.phi(k, x.W)
+    S = np.cumsum(PK[:, :, None] * v[:, None, :], axis=0)     # H_t, (n, D, dv)
+    z = np.cumsum(PK, axis=0)                                  # s_t
+    want = np.einsum("td,tdv->tv", PQ, S) / np.einsum("td,td->t", PQ, z)[:, None]
+    for out in _all_forms(q, k, v, x.W, 0, 0):
+        np.testing.assert_allclose(out["Y"], want, rtol=1e-10, atol=1e-12)
+        assert list(out["write_pos"]) == list(range(33))
+    np.testing.assert_allclose(R.linear_attention(q, k, v, x.W), want, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("eta", [1, 4, 9])
+def test_zero_cache_is_window_plus_linear(eta):
+    """lambda = 0: sliding-window softmax over the last eta tokens plus a linear state over
+    every token <= t - eta, one shared denominator; each token is written when it leaves."""
+    x = synth.gauss_inputs(1, 1, 30, 8, 8, "f32", seed=7)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    want = R.window_plus_linear(q, k, v, x.W, eta)
+    for out in _all_forms(q, k, v, x.W, eta, 0):
+        np.testing.assert_allclose(out["Y"], want, rtol=1e-12, atol=1e-12)
+        assert list(out["write_pos"]) == [-1] * eta + list(range(30 - eta))
+
+
+# ---------------------------------------------------------------------------
+# invariants and brute force
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("eta,lam", [(0, 0), (0, 3), (2, 0), (3, 2), (1, 5), (4, 4), (7, 1)])
+@pytest.mark.parametrize("seed", [0, 1])
+def test_three_forms_agree_brute_force(eta, lam, seed):
+    """n <= 32: set-based brute force, running state and the incremental C form agree."""
+    x = synth.gauss_inputs(1, 1, 32, 8, 8, "f32", seed=10 + seed, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    a, b, c = _all_forms(q, k, v, x.W, eta, lam)
+    assert np.array_equal(a["write_pos"], b["write_pos"])
+    assert np.array_equal(a["write_pos"], c["write_pos"])
+    np.testing.assert_allclose(b["Y"], a["Y"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(c["Y"], a["Y"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(c["H"], a["H"], rtol=1e-11, atol=1e-12)
+    assert np.array_equal(np.array(sorted(c["cache"][c["cache"] >= 0])), a["cache"])
+
+
+@pytest.mark.parametrize("eta,lam", [(0, 0), (3, 2), (5, 9), (16, 16)])
+def test_exactly_once_accounting(eta, lam):
+    """At every t the window, cache and written set are disjoint, cover {0..t}, the
+    window holds min(t+1, eta) tokens, and (H, s) are the sums over the written set."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=12)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    PK = R.phi(k, x.W)
+    for t in (0, 1, eta, eta + lam, eta + lam + 1, 25, 39):
+        if t >= 40:
+            continue
+        o = R.lola_run(q[:t + 1], k[:t + 1], v[:t + 1], x.W, eta, lam)
+        win, cache = set(o["window"].tolist()), set(o["cache"].tolist())
+        written = set(np.flatnonzero(o["write_step"] >= 0).tolist())
+        assert not (win & cache) and not (win & written) and not (cache & written)
+        assert win | cache | written == set(range(t + 1))
+        assert len(win) == min(t + 1, eta)
+        assert len(cache) <= lam
+        wl = sorted(written)
+        np.testing.assert_allclose(o["H"], PK[wl].T @ v[wl] if wl else 0.0, atol=1e-13)
+        np.testing.assert_allclose(o["s"], PK[wl].sum(0) if wl else 0.0, atol=1e-13)
+
+
+def test_prefix_consistency():
+    """The rule is causal: running n + m tokens repeats the decisions and outputs of the
+    first n (the decode step continues a prefill exactly)."""
+    x = synth.gauss_inputs(2, 2, 200, 16, 16, "bf16", seed=13)
+    full = inc.run(x.q, x.k, x.v, x.W, 8, 8, "bf16")
+    part = inc.run(x.q[:, :, :150], x.k[:, :, :150], x.v[:, :, :150], x.W, 8, 8, "bf16")
+    assert np.array_equal(full["write_pos"][..., :150], part["write_pos"])
+    np.testing.assert_array_equal(full["Y"][..., :150, :], part["Y"])
+
+
+def test_value_scaling_and_shift():
+    """V -> cV scales Y and every SRE by c (decisions unchanged); V -> V + b shifts Y by b
+    and leaves every SRE taken against a non-empty memory unchanged (the co-normalised
+    weights sum to 1).  b is small so the one empty-memory decision keeps its order."""
+    x = synth.gauss_inputs(1, 1, 120, 8, 8, "f32", seed=14)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    base = R.lola_run(q, k, v, x.W, 4, 6)
+    sc = R.lola_run(q, k, 2.5 * v, x.W, 4, 6)
+    assert np.array_equal(base["write_pos"], sc["write_pos"])
+    np.testing.assert_allclose(sc["Y"], 2.5 * base["Y"], rtol=1e-12, atol=1e-12)
+    b = 1e-3 * np.arange(1, 9)
+    sh = R.lola_run(q, k, v + b, x.W, 4, 6)
+    assert np.array_equal(base["write_pos"], sh["write_pos"])
+    np.testing.assert_allclose(sh["Y"], base["Y"] + b, rtol=1e-11, atol=1e-11)
+
+
+def test_bf16_inputs_widen_exactly():
+    x = synth.gauss_inputs(1, 3, 64, 16, 16, "bf16", seed=15)
+    a = inc.run(x.q, x.k, x.v, x.W, 4, 4, "bf16")
+    f = [synth.bf16_bits_to_f32(getattr(x, n)) for n in "qkv"]
+    b = inc.run(*f, x.W, 4, 4, "f32")
+    assert np.array_equal(a["write_pos"], b["write_pos"])
+    np.testing.assert_array_equal(a["Y"], b["Y"])
+
+
+def test_replay_of_own_decisions_and_rejection():
+    x = synth.gauss_inputs(1, 2, 100, 8, 8, "f32", seed=16)
+    o = inc.run(x.q, x.k, x.v, x.W, 5, 5, "f32")
+    r = inc.run(x.q, x.k, x.v, x.W, 5, 5, "f32", replay=o["write_pos"])
+    assert (r["status"] == 0).all() and (r["mismatches"] == 0).all()
+    np.testing.assert_array_equal(r["Y"], o["Y"])
+    bad = o["write_pos"].copy()
+    t = int(np.flatnonzero(bad[0, 0] >= 0)[3])
+    bad[0, 0, t] = t    # token t is in the window at step t, never a candidate (eta = 5)
+    assert inc.run(x.q, x.k, x.v, x.W, 5, 5, "f32", replay=bad)["status"][0, 0] == 1
+    bad = o["write_pos"].copy()
+    bad[0, 1, 0] = 0    # a write before any is due
+    assert inc.run(x.q, x.k, x.v, x.W, 5, 5, "f32", replay=bad)["status"][0, 1] == 2
+
+
+def test_replay_reports_gap_of_a_suboptimal_choice():
+    """Replaying a non-best write reports its relative SRE gap to the best candidate."""
+    x = synth.gauss_inputs(1, 1, 60, 8, 8, "f32", seed=17)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 2, 3)
+    t0 = int(np.flatnonzero(o["write_pos"] >= 0)[0])
+    cand = [j for j in range(t0 + 1) if o["write_step"][j] in (-1,) or o["write_step"][j] >= t0]
+    cand = [j for j in cand if j <= t0 - 2]           # the pool at step t0: cache + evictee
+    alt = [j for j in cand if j != o["write_pos"][t0]][0]
+    rep = o["write_pos"].copy()
+    rep[t0] = alt
+    rep[t0 + 1:] = -2                                 # placeholder, trajectory diverges
+    r = R.lola_run(q[:t0 + 1], k[:t0 + 1], v[:t0 + 1], x.W, 2, 3, replay=rep[:t0 + 1])
+    assert r["mismatches"] == 1 and r["max_gap"] > 0
+
+
+def test_state_element_formula():
+    """Appendix B: min{t(d_k+d_v), (eta+lambda)(d_k+d_v) + D d_v + D}."""
+    assert R.state_elements(10, 64, 64, 64, 64, 64) == 10 * 128
+    assert R.state_elements(4096, 128, 128, 128, 64, 64) == 128 * 256 + 128 * 128 + 128
