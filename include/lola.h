@@ -1,0 +1,163 @@
+/* lola.h -- C ABI of the GB300 LoLA hybrid-attention library (liblola.so).
+ *
+ * The library computes, per attention head, the LoLA memory of "LoLA: Low-Rank Linear
+ * Attention With Sparse Caching" (arXiv 2505.23666v3), reading notes sections 2.1-2.7:
+ *   - a feature map phi(x) = [softmax(W x), softmax(-W x)], W of shape (D/2, d_k)
+ *     (section 2.2, Eq. 3, in the configured form);
+ *   - a linear memory H (D x d_v) and s (D) fed by H += phi(k) v^T, s += phi(k)
+ *     (section 2.2, Eqs. 3-5) with only the KV assigned to it;
+ *   - a sliding window of the eta most recent KV (the current token included) and a
+ *     sparse cache of at most lambda exact KV;
+ *   - per token: the KV leaving the window joins the cache as a candidate; when the
+ *     candidates exceed lambda, the one with the smallest self-recall error
+ *     SRE(k, v | H, s) = || H^T phi(k) / (phi(k)^T s) - v ||_2 (section 2.3, Eq. 10),
+ *     scored against the memory before this step's write (section 2.4, Eqs. 11-13), is
+ *     written into (H, s) and leaves the exact memory for good; ties go to the older
+ *     token; an empty memory predicts 0, so SRE = ||v|| while s = 0;
+ *   - the output y_t = (H^T phi(q) + sum_{G ∪ W} a v) / (phi(q)^T s + sum_{G ∪ W} a)
+ *     with a = exp(q^T k / sqrt(d_k)), read after this step's write (section 2.5, Eq. 14).
+ * The prefill chunk length only schedules the work: it never changes which KV are kept
+ * (the per-token rule above is the definition).
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" point to memory on the current CUDA device; "host" to
+ *     host memory.  The library never allocates device memory in these calls: the caller
+ *     owns every buffer (state, workspace, inputs, outputs).
+ *   - Calls are asynchronous and ordered on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream).  Host-side validation failures return at once
+ *     with nothing enqueued.
+ *   - Return values are lola_status codes.  LOLA_ERR_CUDA means a CUDA runtime call
+ *     failed while enqueueing; the CUDA error text is available from
+ *     lola_last_cuda_error().  Device-side anomalies (a chain whose bookkeeping went out
+ *     of its bounds) are recorded in the per-head status word of the state and read
+ *     with lola_read_status(); the kernels never trap.
+ *   - Calls on distinct states may run concurrently; calls on one state must not overlap.
+ *   - Tensors are dense row-major: Q, K, V and Y are [B, Hh, n, d] with d the innermost
+ *     axis; per-head data of head (b, h) is at head index b * Hh + h.
+ */
+#ifndef LOLA_H
+#define LOLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LOLA_OK = 0,
+    LOLA_ERR_INVALID_ARG = -1,   /* null pointer, non-positive size, misaligned buffer */
+    LOLA_ERR_UNSUPPORTED = -2,   /* valid but outside the shapes this build compiles */
+    LOLA_ERR_WORKSPACE = -3,     /* workspace smaller than lola_prefill_workspace_bytes() */
+    LOLA_ERR_CUDA = -4,          /* a CUDA runtime call failed */
+    LOLA_ERR_DEVICE = -5         /* lola_read_status(): a head reported a device-side error */
+} lola_status;
+
+typedef enum {
+    LOLA_F32 = 0,                /* Q, K, V, Y and the exact KV in float32 */
+    LOLA_BF16 = 1                /* ... in bfloat16; H, s and all scores stay float32 */
+} lola_dtype;
+
+typedef struct {
+    int32_t B;          /* batch */
+    int32_t Hh;         /* heads per layer; every (b, h) is an independent memory */
+    int32_t d_k;        /* query/key width */
+    int32_t d_v;        /* value width */
+    int32_t D;          /* feature width of phi; W has D/2 rows */
+    int32_t eta;        /* window length (>= 0) */
+    int32_t lambda;     /* sparse-cache capacity (>= 0) */
+    int32_t chunk;      /* prefill schedule granularity C; no effect on results */
+    int32_t dtype;      /* lola_dtype */
+} lola_config;
+
+/* Supported by this build: d_k = d_v = D in {64, 128}; lambda <= 1024; eta <= 65536;
+ * chunk a power of two in [16, 256]; B * Hh >= 1. */
+
+/* ---- per-head state layout (the public "checkpoint" format) -----------------------
+ * lola_state_bytes(cfg) = B * Hh * lola_head_state_bytes(cfg).  Head i's record starts
+ * at byte i * lola_head_state_bytes(cfg).  Offsets below are from the record start and
+ * are multiples of 256 bytes; io = float32 or bf16 per cfg->dtype.
+ *   [0]        int32 header[16]: t (tokens consumed), n_cache (live cache entries),
+ *              n_written, status (0 ok; nonzero = device-side error bits), rest 0
+ *   H          float32 [D][d_v]          linear memory
+ *   s          float32 [D]               normaliser
+ *   win_pos    int32   [eta]             window ring: position p sits in entry p % eta
+ *   win_k      io      [eta][d_k]
+ *   win_v      io      [eta][d_v]
+ *   c_pos      int32   [lambda]          cache slots, -1 = empty; after lola_prefill the
+ *                                        live slots come first, sorted by position;
+ *                                        lola_decode_step reuses slots in place
+ *   c_k        io      [lambda][d_k]
+ *   c_v        io      [lambda][d_v]
+ *   c_phi      float32 [lambda][D]       phi(k) of each cached key
+ *   c_N        float32 [lambda][d_v]     H^T phi(k) kept current for each cached key
+ *   c_z        float32 [lambda]          s^T phi(k) kept current for each cached key
+ * The appendix-B element count (eta + lambda)(d_k + d_v) + D d_v + D is the window,
+ * cache, H and s above; c_phi, c_N, c_z, positions and the header are the bookkeeping
+ * that lets a decode step score the cache without recomputing H^T phi(k). */
+
+typedef struct {
+    int64_t head_bytes;
+    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z;
+} lola_state_layout;
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int32_t lola_version(void);
+
+/* Static text for a lola_status value. */
+const char* lola_status_string(int32_t status);
+
+/* Text of the last CUDA error seen by the calling thread in this library ("" if none). */
+const char* lola_last_cuda_error(void);
+
+/* LOLA_OK if cfg is valid and supported, else LOLA_ERR_INVALID_ARG / LOLA_ERR_UNSUPPORTED. */
+int32_t lola_check_config(const lola_config* cfg);
+
+/* Fills *out with the per-head state layout (host). */
+int32_t lola_state_layout_of(const lola_config* cfg, lola_state_layout* out);
+
+/* Bytes of the whole state buffer (all B * Hh heads); 0 if cfg is invalid. */
+size_t lola_state_bytes(const lola_config* cfg);
+
+/* Bytes of device workspace lola_prefill needs for n tokens; 0 if invalid. */
+size_t lola_prefill_workspace_bytes(const lola_config* cfg, int32_t n);
+
+/* Resets every head of `state` (device, lola_state_bytes) to the empty memory: t = 0,
+ * H = 0, s = 0, window and cache empty.  Stream-ordered. */
+int32_t lola_state_init(const lola_config* cfg, void* state, void* stream);
+
+/* Prefill: runs the per-token rule over n tokens of every head from the empty memory
+ * (section 2.4, Eqs. 11-13; output section 2.5, Eq. 14).
+ *   Q, K  device io [B, Hh, n, d_k];  V device io [B, Hh, n, d_v]
+ *   W     device float32 [D/2, d_k] shared by all heads when w_head_stride == 0, else head
+ *         h uses W + h * w_head_stride (elements)
+ *   Y     device io [B, Hh, n, d_v]: the outputs y_0 .. y_{n-1}
+ *   state device, lola_state_bytes(cfg): overwritten with the memory after token n-1,
+ *         ready for lola_decode_step
+ *   write_pos  nullable device int32 [B, Hh, n]: the position written into (H, s) at each
+ *         step, or -1 when the step wrote nothing (the decision log)
+ *   workspace  device, >= lola_prefill_workspace_bytes(cfg, n), 256-byte aligned
+ * n >= 1.  Every device pointer must be 16-byte aligned. */
+int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const void* K,
+                     const void* V, const float* W, int64_t w_head_stride, void* Y, void* state,
+                     int32_t* write_pos, void* workspace, size_t workspace_bytes, void* stream);
+
+/* One decode step for every head: token t = state.t with q, k, v (device io [B, Hh, d])
+ * goes through the same rule as one prefill step; y (device io [B, Hh, d_v]) receives
+ * its output; written_pos (nullable device int32 [B, Hh]) receives the position written
+ * this step or -1.  W as in lola_prefill.  The state advances by one token. */
+int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W,
+                         int64_t w_head_stride, const void* q, const void* k, const void* v,
+                         void* y, int32_t* written_pos, void* stream);
+
+/* Synchronises `stream`, then copies the per-head status words into host_status (host
+ * int32 [B * Hh], nullable).  Returns LOLA_OK if every head is 0, else LOLA_ERR_DEVICE. */
+int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* host_status,
+                         void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LOLA_H */

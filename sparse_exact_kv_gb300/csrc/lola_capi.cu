@@ -1,0 +1,223 @@
+// Host side of the C ABI declared in include/lola.h: argument validation, the state and
+// workspace layouts, and the stream-ordered sequence of kernels of each call.
+#include <cstdio>
+#include <cstring>
+
+#include "lola_internal.cuh"
+
+namespace lola {
+
+int select_cluster_size(int lam);
+
+namespace {
+
+thread_local char g_cuda_error[256] = "";
+
+int32_t cuda_fail(cudaError_t e, const char* where) {
+    snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", where, cudaGetErrorString(e));
+    return LOLA_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int32_t to_dims(const lola_config* c, Dims* d) {
+    if (!c) return LOLA_ERR_INVALID_ARG;
+    if (c->B < 1 || c->Hh < 1 || c->d_k < 1 || c->d_v < 1 || c->D < 2 || (c->D & 1) || c->eta < 0 ||
+        c->lambda < 0 || c->chunk < 1 || (c->dtype != LOLA_F32 && c->dtype != LOLA_BF16))
+        return LOLA_ERR_INVALID_ARG;
+    if ((int64_t)c->B * c->Hh > (1 << 24)) return LOLA_ERR_UNSUPPORTED;
+    const bool dims_ok = (c->d_k == 128 && c->d_v == 128 && c->D == 128) || (c->d_k == 64 && c->d_v == 64 && c->D == 64);
+    if (!dims_ok) return LOLA_ERR_UNSUPPORTED;
+    if (c->lambda > 1024 || c->eta > 8192) return LOLA_ERR_UNSUPPORTED;
+    if (c->chunk < 16 || c->chunk > 256 || (c->chunk & (c->chunk - 1))) return LOLA_ERR_UNSUPPORTED;
+    d->B = c->B;
+    d->Hh = c->Hh;
+    d->BH = c->B * c->Hh;
+    d->dk = c->d_k;
+    d->dv = c->d_v;
+    d->D = c->D;
+    d->eta = c->eta;
+    d->lam = c->lambda;
+    d->chunk = c->chunk;
+    d->dtype = c->dtype;
+    return LOLA_OK;
+}
+
+__global__ void state_init_kernel(char* state, Layout L, int eta, int lam) {
+    char* rec = state + (int64_t)blockIdx.x * L.head_bytes;
+    int32_t* wp = reinterpret_cast<int32_t*>(rec + L.win_pos);
+    int32_t* cp = reinterpret_cast<int32_t*>(rec + L.c_pos);
+    for (int i = threadIdx.x; i < eta; i += blockDim.x) wp[i] = -1;
+    for (int i = threadIdx.x; i < lam; i += blockDim.x) cp[i] = -1;
+}
+
+}  // namespace
+
+Workspace carve_workspace(const Dims& d, int n, void* base) {
+    Workspace w;
+    char* p = static_cast<char*>(base);
+    int64_t o = 0;
+    const int64_t BH = d.BH;
+    w.nck = (n + d.chunk - 1) / d.chunk;
+    auto take = [&](int64_t bytes) {
+        char* r = p ? p + o : nullptr;
+        o = align256(o + bytes);
+        return r;
+    };
+    w.phiK = reinterpret_cast<float*>(take(4 * BH * n * d.D));
+    w.phiQ = reinterpret_cast<float*>(take(4 * BH * n * d.D));
+    w.wstep = reinterpret_cast<int32_t*>(take(4 * BH * n));
+    w.wpos = reinterpret_cast<int32_t*>(take(4 * BH * n));
+    w.snapH = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D * d.dv));
+    w.snapS = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D));
+    w.snapC = reinterpret_cast<int32_t*>(take(4 * BH * w.nck * (int64_t)(d.lam > 0 ? d.lam : 1)));
+    w.slotpos = reinterpret_cast<int32_t*>(take(4 * BH * (int64_t)(d.lam > 0 ? d.lam : 1)));
+    w.bytes = (size_t)o;
+    return w;
+}
+
+cudaError_t launch_state_init(const Dims& d, char* state, const Layout& L, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(state, 0, (size_t)L.head_bytes * d.BH, st);
+    if (e != cudaSuccess) return e;
+    state_init_kernel<<<d.BH, 256, 0, st>>>(state, L, d.eta, d.lam);
+    return cudaGetLastError();
+}
+
+}  // namespace lola
+
+using namespace lola;
+
+extern "C" {
+
+int32_t lola_version(void) { return 100; }
+
+const char* lola_status_string(int32_t s) {
+    switch (s) {
+        case LOLA_OK: return "ok";
+        case LOLA_ERR_INVALID_ARG: return "invalid argument";
+        case LOLA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case LOLA_ERR_WORKSPACE: return "workspace too small";
+        case LOLA_ERR_CUDA: return "CUDA runtime error";
+        case LOLA_ERR_DEVICE: return "device-side error reported in the state";
+        default: return "unknown status";
+    }
+}
+
+const char* lola_last_cuda_error(void) { return g_cuda_error; }
+
+int32_t lola_check_config(const lola_config* cfg) {
+    Dims d;
+    return to_dims(cfg, &d);
+}
+
+int32_t lola_state_layout_of(const lola_config* cfg, lola_state_layout* out) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (!out) return LOLA_ERR_INVALID_ARG;
+    Layout L = make_layout(d);
+    out->head_bytes = L.head_bytes;
+    out->H = L.H;
+    out->s = L.s;
+    out->win_pos = L.win_pos;
+    out->win_k = L.win_k;
+    out->win_v = L.win_v;
+    out->c_pos = L.c_pos;
+    out->c_k = L.c_k;
+    out->c_v = L.c_v;
+    out->c_phi = L.c_phi;
+    out->c_N = L.c_N;
+    out->c_z = L.c_z;
+    return LOLA_OK;
+}
+
+size_t lola_state_bytes(const lola_config* cfg) {
+    Dims d;
+    if (to_dims(cfg, &d) != LOLA_OK) return 0;
+    return (size_t)make_layout(d).head_bytes * d.BH;
+}
+
+size_t lola_prefill_workspace_bytes(const lola_config* cfg, int32_t n) {
+    Dims d;
+    if (to_dims(cfg, &d) != LOLA_OK || n < 1) return 0;
+    return carve_workspace(d, n, nullptr).bytes;
+}
+
+int32_t lola_state_init(const lola_config* cfg, void* state, void* stream) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (!state || !aligned16(state)) return LOLA_ERR_INVALID_ARG;
+    cudaError_t e = launch_state_init(d, static_cast<char*>(state), make_layout(d), (cudaStream_t)stream);
+    return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "lola_state_init");
+}
+
+int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const void* K, const void* V, const float* W,
+                     int64_t w_head_stride, void* Y, void* state, int32_t* write_pos, void* workspace,
+                     size_t workspace_bytes, void* stream) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (n < 1) return LOLA_ERR_INVALID_ARG;
+    if ((int64_t)n * d.BH * d.D > ((int64_t)1 << 40)) return LOLA_ERR_UNSUPPORTED;
+    if (!Q || !K || !V || !W || !Y || !state || !workspace) return LOLA_ERR_INVALID_ARG;
+    if (w_head_stride < 0) return LOLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {Q, K, V, W, Y, state, workspace};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;
+    if (write_pos && (reinterpret_cast<uintptr_t>(write_pos) & 3)) return LOLA_ERR_INVALID_ARG;
+    Workspace ws = carve_workspace(d, n, workspace);
+    if (workspace_bytes < ws.bytes) return LOLA_ERR_WORKSPACE;
+    if (write_pos) ws.wpos = write_pos;
+    const Layout L = make_layout(d);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = launch_state_init(d, static_cast<char*>(state), L, st);
+    if (e != cudaSuccess) return cuda_fail(e, "state init");
+    e = launch_phi(d, n, K, W, w_head_stride, ws.phiK, st);
+    if (e != cudaSuccess) return cuda_fail(e, "phi(K)");
+    e = launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, st);
+    if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
+    e = launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st);
+    if (e != cudaSuccess) return cuda_fail(e, "selection");
+    e = launch_output(d, n, ws, Q, K, V, Y, st);
+    if (e != cudaSuccess) return cuda_fail(e, "output");
+    return LOLA_OK;
+}
+
+int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W, int64_t w_head_stride, const void* q,
+                         const void* k, const void* v, void* y, int32_t* written_pos, void* stream) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (!state || !W || !q || !k || !v || !y || w_head_stride < 0) return LOLA_ERR_INVALID_ARG;
+    const void* ptrs[] = {state, W, q, k, v, y};
+    for (const void* p : ptrs)
+        if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;
+    if (written_pos && (reinterpret_cast<uintptr_t>(written_pos) & 3)) return LOLA_ERR_INVALID_ARG;
+    cudaError_t e = launch_decode(d, static_cast<char*>(state), make_layout(d), W, w_head_stride, q, k, v, y,
+                                  written_pos, (cudaStream_t)stream);
+    return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "decode step");
+}
+
+int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* host_status, void* stream) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (!state) return LOLA_ERR_INVALID_ARG;
+    const Layout L = make_layout(d);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "lola_read_status sync");
+    int32_t bad = 0;
+    for (int i = 0; i < d.BH; ++i) {
+        int32_t w = 0;
+        e = cudaMemcpy(&w, static_cast<const char*>(state) + (int64_t)i * L.head_bytes + 4 * HDR_STATUS, 4,
+                       cudaMemcpyDeviceToHost);
+        if (e != cudaSuccess) return cuda_fail(e, "lola_read_status copy");
+        if (host_status) host_status[i] = w;
+        bad |= w;
+    }
+    return bad ? LOLA_ERR_DEVICE : LOLA_OK;
+}
+
+}  // extern "C"

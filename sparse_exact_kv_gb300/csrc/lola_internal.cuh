@@ -1,0 +1,160 @@
+// Internal declarations shared by the liblola translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "lola.h"
+
+namespace lola {
+
+constexpr int kWarp = 32;
+
+// ---------------------------------------------------------------------------------
+// Sizes and the public per-head state layout (see lola.h)
+// ---------------------------------------------------------------------------------
+struct Dims {
+    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype;
+    int io_bytes() const { return dtype == LOLA_BF16 ? 2 : 4; }
+};
+
+__host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int64_t(255); }
+
+struct Layout {
+    int64_t head_bytes;
+    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z;
+};
+
+inline Layout make_layout(const Dims& d) {
+    Layout L;
+    int64_t o = 256;  // header
+    const int64_t io = d.io_bytes();
+    L.H = o;        o = align256(o + 4ll * d.D * d.dv);
+    L.s = o;        o = align256(o + 4ll * d.D);
+    L.win_pos = o;  o = align256(o + 4ll * d.eta);
+    L.win_k = o;    o = align256(o + io * d.eta * d.dk);
+    L.win_v = o;    o = align256(o + io * d.eta * d.dv);
+    L.c_pos = o;    o = align256(o + 4ll * d.lam);
+    L.c_k = o;      o = align256(o + io * d.lam * d.dk);
+    L.c_v = o;      o = align256(o + io * d.lam * d.dv);
+    L.c_phi = o;    o = align256(o + 4ll * d.lam * d.D);
+    L.c_N = o;      o = align256(o + 4ll * d.lam * d.dv);
+    L.c_z = o;      o = align256(o + 4ll * d.lam);
+    L.head_bytes = o;
+    return L;
+}
+
+// header words of a head record
+enum { HDR_T = 0, HDR_NCACHE = 1, HDR_NWRITTEN = 2, HDR_STATUS = 3, HDR_WORDS = 16 };
+
+// device-side status bits
+enum : int32_t { ST_SLOT_OVERFLOW = 1, ST_BAD_STATE = 2 };
+
+// ---------------------------------------------------------------------------------
+// Prefill workspace: per-head arrays used between the kernels
+// ---------------------------------------------------------------------------------
+struct Workspace {
+    float* phiK;       // [BH][n][D]    phi(k_t), float32 (selection precision)
+    float* phiQ;       // [BH][n][D]    phi(q_t)
+    int32_t* wstep;    // [BH][n]       step at which token j was written, -1 never
+    int32_t* wpos;     // [BH][n]       position written at step t, -1 none
+    float* snapH;      // [BH][nck][D*dv]  H before the first step of each chunk
+    float* snapS;      // [BH][nck][D]
+    int32_t* snapC;    // [BH][nck][lam]   cache slot positions before each chunk (-1 empty)
+    int32_t* slotpos;  // [BH][lam]        final slot positions (export scratch)
+    int nck;
+    size_t bytes;
+};
+
+Workspace carve_workspace(const Dims& d, int n, void* base);
+
+// ---------------------------------------------------------------------------------
+// Element access
+// ---------------------------------------------------------------------------------
+template <typename T> struct IO;
+template <> struct IO<float> {
+    static __device__ __forceinline__ float ld(const float* p, int64_t i) { return p[i]; }
+    static __device__ __forceinline__ void st(float* p, int64_t i, float x) { p[i] = x; }
+};
+template <> struct IO<__nv_bfloat16> {
+    static __device__ __forceinline__ float ld(const __nv_bfloat16* p, int64_t i) {
+        return __bfloat162float(p[i]);
+    }
+    static __device__ __forceinline__ void st(__nv_bfloat16* p, int64_t i, float x) {
+        p[i] = __float2bfloat16_rn(x);
+    }
+};
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+// Candidate order of the allocation rule: smaller SRE^2 first, then the older position.
+__device__ __forceinline__ bool key_less(float a, int pa, float b, int pb) {
+    return a < b || (a == b && pa < pb);
+}
+
+// ---------------------------------------------------------------------------------
+// phi(x) = [softmax(W x), softmax(-W x)] for one row, computed by one warp.
+//   xs: the row x (d_k floats) in shared memory;  Ws: W in shared memory with row
+//   stride DK + 1 (conflict-free column reads).  Lane l returns phi[l + 32 m] in
+//   out[m], m < D / 32.  Fixed operation order, shared by every kernel that needs phi,
+//   so prefill and decode produce identical bits.
+// ---------------------------------------------------------------------------------
+template <int DK, int D>
+__device__ __forceinline__ void phi_warp(const float* xs, const float* Ws, int lane, float (&out)[D / 32]) {
+    constexpr int HM = D / 64;  // z values per lane
+    float z[HM];
+#pragma unroll
+    for (int m = 0; m < HM; ++m) {
+        const float* wr = Ws + (lane + 32 * m) * (DK + 1);
+        float acc = 0.f;
+#pragma unroll 8
+        for (int c = 0; c < DK; ++c) acc = fmaf(wr[c], xs[c], acc);
+        z[m] = acc;
+    }
+    float mx = z[0], mn = z[0];
+#pragma unroll
+    for (int m = 1; m < HM; ++m) { mx = fmaxf(mx, z[m]); mn = fminf(mn, z[m]); }
+    mx = warp_max(mx);
+    mn = -warp_max(-mn);
+    float ep[HM], en[HM], sp = 0.f, sn = 0.f;
+#pragma unroll
+    for (int m = 0; m < HM; ++m) {
+        ep[m] = expf(z[m] - mx);
+        en[m] = expf(mn - z[m]);
+        sp += ep[m];
+        sn += en[m];
+    }
+    sp = warp_sum(sp);
+    sn = warp_sum(sn);
+#pragma unroll
+    for (int m = 0; m < HM; ++m) {
+        out[m] = ep[m] / sp;
+        out[HM + m] = en[m] / sn;
+    }
+}
+
+// ---------------------------------------------------------------------------------
+// Launchers (each returns the launch's cudaError_t)
+// ---------------------------------------------------------------------------------
+cudaError_t launch_phi(const Dims& d, int n, const void* X, const float* W, int64_t w_head_stride,
+                       float* out, cudaStream_t st);
+cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
+                          char* state, const Layout& L, cudaStream_t st);
+cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
+                          const void* V, void* Y, cudaStream_t st);
+cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W,
+                          int64_t w_head_stride, const void* q, const void* k, const void* v, void* y,
+                          int32_t* written_pos, cudaStream_t st);
+cudaError_t launch_state_init(const Dims& d, char* state, const Layout& L, cudaStream_t st);
+
+}  // namespace lola

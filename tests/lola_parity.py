@@ -1,0 +1,73 @@
+"""Helpers for GPU-vs-oracle parity: run the CUDA path through the C ABI, run the oracle
+on the same seeded inputs, and compare under the stated bars.
+
+Bars (the LoLA hot-path contract): float32 runs must reproduce the oracle's decision log
+exactly and outputs within max-abs 1e-4 and rel-L2 1e-4; bfloat16 runs may take another
+decision only where the relative SRE gap to the oracle's best candidate is below 1e-3
+(checked by replaying the GPU's decisions in the oracle), and outputs must be within
+max-abs 2e-2 and rel-L2 1e-2 of the oracle's outputs along the GPU's trajectory."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import inc
+
+TOL = {"f32": dict(max_abs=1e-4, rel_l2=1e-4), "bf16": dict(max_abs=2e-2, rel_l2=1e-2)}
+GAP = 1e-3
+
+
+def to_dev(x, dev, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    if dtype == "bf16":
+        t = t.view(torch.bfloat16)
+    return t.to(dev)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def run_prefill(L, x, eta, lam, chunk, n=None, dev="cuda"):
+    """Prefill through the C ABI; returns (Y float64, write_pos, layer)."""
+    w = x.w
+    dt = w.dtype
+    n = n or x.q.shape[2]
+    lay = L.Lola(w.B, w.Hh, w.d, w.D, eta, lam, chunk=chunk,
+                 dtype=torch.bfloat16 if dt == "bf16" else torch.float32, device=dev)
+    Q, K, V = (to_dev(getattr(x, a)[:, :, :n], dev, dt) for a in "qkv")
+    W = torch.from_numpy(x.W).to(dev)
+    wpos = torch.full((w.B, w.Hh, n), -7, dtype=torch.int32, device=dev)
+    Y = lay.prefill(Q, K, V, W, write_pos=wpos)
+    torch.cuda.synchronize()
+    return to_f64(Y), wpos.cpu().numpy(), lay
+
+
+def err_stats(got, ref):
+    d = got - ref
+    return float(np.abs(d).max()), float(np.linalg.norm(d) / max(np.linalg.norm(ref), 1e-300))
+
+
+def check_outputs(got, ref, dtype, what="Y"):
+    ma, rl = err_stats(got, ref)
+    tol = TOL[dtype]
+    assert ma <= tol["max_abs"] and rl <= tol["rel_l2"], f"{what}: max-abs {ma:.3e}, rel-L2 {rl:.3e} vs {tol}"
+    return ma, rl
+
+
+def check_decisions(x, wpos, eta, lam, n=None, nthreads=None):
+    """Validates the GPU decision log against the oracle; returns the oracle run along the
+    GPU's trajectory (replay) and the free-running oracle."""
+    dt = x.w.dtype
+    n = n or wpos.shape[-1]
+    q, k, v = (getattr(x, a)[..., :n, :] for a in "qkv")
+    free = inc.run(q, k, v, x.W, eta, lam, dt, nthreads=nthreads)
+    if dt == "f32":
+        diff = np.argwhere(free["write_pos"] != wpos)
+        assert diff.size == 0, f"float32 decision log differs at (head..., step) {diff[:5].tolist()}"
+        return free, free
+    rep = inc.run(q, k, v, x.W, eta, lam, dt, replay=wpos, nthreads=nthreads)
+    assert (rep["status"] == 0).all(), f"replay rejected the GPU log: status {np.unique(rep['status'])}"
+    worst = float(np.max(rep["max_gap"]))
+    assert worst < GAP, f"a GPU decision is {worst:.3e} (relative SRE) away from the best candidate"
+    return rep, free

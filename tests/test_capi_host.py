@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU needed): every symbol include/lola.h declares is
+exported by liblola.so, configurations are validated, and the state layout holds the
+appendix-B element count of the LoLA reading notes (arXiv 2505.23666v3)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from sparse_exact_kv_gb300 import _build
+    _build.build()
+    import sparse_exact_kv_gb300 as L
+    return L
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "lola.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^[A-Za-z_][\w \*]*?\b(lola_\w+)\s*\(", src, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert len(names) >= 11, names
+    so = ctypes.CDLL(lib.LIB_PATH)
+    for name in names:
+        assert hasattr(so, name), f"{name} declared in lola.h but not exported"
+    assert sorted(lib.EXPORTS) == names
+
+
+def test_version_and_status_strings(lib):
+    assert lib.lola_version() >= 100
+    assert lib.lola_status_string(0) == "ok"
+    assert "workspace" in lib.lola_status_string(lib.LOLA_ERR_WORKSPACE)
+
+
+@pytest.mark.parametrize("bad", [
+    dict(B=0), dict(Hh=-1), dict(D=63), dict(eta=-1), dict(lam=-2), dict(chunk=0), dict(dtype=7)])
+def test_invalid_configs(lib, bad):
+    kw = dict(B=2, Hh=4, d_k=128, d_v=128, D=128, eta=64, lam=64, chunk=64, dtype="bf16")
+    kw.update(bad)
+    cfg = lib.make_config(kw["B"], kw["Hh"], kw["d_k"], kw["d_v"], kw["D"], kw["eta"], kw["lam"], kw["chunk"],
+                          kw["dtype"])
+    assert lib.lola_check_config(cfg) == lib.LOLA_ERR_INVALID_ARG
+    assert lib.lola_state_bytes(cfg) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(d_k=96, d_v=96, D=96), dict(D=64), dict(lam=2000), dict(chunk=48),
+                                 dict(chunk=512), dict(chunk=8)])
+def test_unsupported_configs(lib, bad):
+    kw = dict(B=1, Hh=1, d_k=128, d_v=128, D=128, eta=64, lam=64, chunk=64, dtype="bf16")
+    kw.update(bad)
+    cfg = lib.make_config(kw["B"], kw["Hh"], kw["d_k"], kw["d_v"], kw["D"], kw["eta"], kw["lam"], kw["chunk"],
+                          kw["dtype"])
+    assert lib.lola_check_config(cfg) == lib.LOLA_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("d,eta,lam,dtype", [(128, 64, 64, "bf16"), (64, 64, 64, "f32"), (128, 512, 512, "bf16"),
+                                             (128, 0, 0, "f32"), (64, 7, 3, "bf16")])
+def test_state_layout_holds_appendix_b_memory(lib, d, eta, lam, dtype):
+    """State bytes >= (eta + lambda)(d_k + d_v) io + (D d_v + D) float32 per head; each
+    region is 256-byte aligned and regions do not overlap."""
+    from oracle.lola_ref import state_elements
+    cfg = lib.make_config(3, 5, d, d, d, eta, lam, 64, dtype)
+    assert lib.lola_check_config(cfg) == 0
+    L = lib.lola_state_layout_of(cfg)
+    io = 2 if dtype == "bf16" else 4
+    kv = (eta + lam) * 2 * d
+    min_bytes = kv * io + (d * d + d) * 4
+    assert state_elements(10 ** 9, d, d, d, eta, lam) == kv + d * d + d
+    assert L.head_bytes >= min_bytes
+    assert lib.lola_state_bytes(cfg) == 15 * L.head_bytes
+    regions = [(L.H, 4 * d * d), (L.s, 4 * d), (L.win_pos, 4 * eta), (L.win_k, io * eta * d), (L.win_v, io * eta * d),
+               (L.c_pos, 4 * lam), (L.c_k, io * lam * d), (L.c_v, io * lam * d), (L.c_phi, 4 * lam * d),
+               (L.c_N, 4 * lam * d), (L.c_z, 4 * lam)]
+    end = 64
+    for off, size in regions:
+        assert off % 256 == 0 and off >= end
+        end = off + size
+    assert end <= L.head_bytes
+
+
+def test_workspace_size_grows_with_n(lib):
+    cfg = lib.make_config(4, 32, 128, 128, 128, 64, 64, 64, "bf16")
+    a = lib.lola_prefill_workspace_bytes(cfg, 1024)
+    b = lib.lola_prefill_workspace_bytes(cfg, 4096)
+    assert 0 < a < b
+    assert lib.lola_prefill_workspace_bytes(cfg, 0) == 0
+
+
+def test_null_and_misaligned_pointers_rejected_before_any_launch(lib):
+    """Validation returns before anything touches the GPU: safe to call without one."""
+    cfg = lib.make_config(1, 1, 64, 64, 64, 4, 4, 16, "f32")
+    so = lib._lib
+    P = ctypes.c_void_p
+    st = so.lola_prefill(ctypes.byref(cfg), 16, None, P(256), P(256), P(256), 0, P(256), P(256), None, P(256),
+                         1 << 30, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG
+    st = so.lola_prefill(ctypes.byref(cfg), 16, P(258), P(256), P(256), P(256), 0, P(256), P(256), None, P(256),
+                         1 << 30, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG
+    st = so.lola_prefill(ctypes.byref(cfg), 0, P(256), P(256), P(256), P(256), 0, P(256), P(256), None, P(256),
+                         1 << 30, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG
+    st = so.lola_prefill(ctypes.byref(cfg), 16, P(256), P(256), P(256), P(256), 0, P(256), P(256), None, P(256),
+                         16, None)
+    assert st == lib.LOLA_ERR_WORKSPACE
+    st = so.lola_decode_step(ctypes.byref(cfg), None, P(256), 0, P(256), P(256), P(256), P(256), None, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG
+    st = so.lola_decode_step(ctypes.byref(cfg), P(256), P(256), -1, P(256), P(256), P(256), P(256), None, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG

@@ -1,0 +1,191 @@
+"""GPU parity of the CUDA path (through the C ABI) against the CPU float64 oracle on the
+same seeded inputs, over several tiles, ragged tails and the method's degenerate cases.
+
+Method: "LoLA: Low-Rank Linear Attention With Sparse Caching" (arXiv 2505.23666v3),
+reading notes sections 2.2-2.6."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import inc
+from oracle import lola_ref as R
+
+from lola_parity import check_decisions, check_outputs, run_prefill, to_dev, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import sparse_exact_kv_gb300 as lib
+    return lib
+
+
+def _final_state_matches(lay, ref, eta, n, dtype):
+    st = lay.read_state()
+    BH = lay.cfg.B * lay.cfg.Hh
+    H_ref = ref["H"].reshape(BH, *ref["H"].shape[-2:])
+    s_ref = ref["s"].reshape(BH, -1)
+    tol = 1e-4 if dtype == "f32" else 2e-3
+    scale = max(1.0, float(np.abs(H_ref).max()))
+    assert np.abs(st["H"] - H_ref).max() <= tol * scale
+    assert np.abs(st["s"] - s_ref).max() <= tol * max(1.0, float(np.abs(s_ref).max()))
+    cache_ref = ref["cache"].reshape(BH, -1)
+    for i in range(BH):
+        live = st["c_pos"][i][st["c_pos"][i] >= 0]
+        assert list(live) == sorted(live), "cache not exported sorted by position"
+        assert list(live) == [p for p in cache_ref[i] if p >= 0]
+        assert st["n_cache"][i] == len(live)
+        want_win = sorted(range(max(0, n - eta), n))
+        got_win = sorted(p for p in st["win_pos"][i] if p >= 0)
+        assert got_win == want_win
+    assert (st["t"] == n).all() and (st["status"] == 0).all()
+
+
+@pytest.mark.parametrize("d,eta,lam,chunk,n", [
+    (64, 0, 0, 16, 100),       # pure linear attention (every token written at its own step)
+    (64, 5, 0, 16, 97),        # window + linear state
+    (64, 0, 7, 32, 130),       # cache only
+    (64, 16, 16, 16, 300),
+    (64, 64, 64, 64, 700),     # the float32 workload's budget, ragged tail
+    (128, 32, 64, 64, 333),
+    (128, 40, 100, 32, 500),   # lambda > 64: a 2-CTA cluster per head
+    (128, 20, 300, 64, 700),   # 8-CTA cluster
+    (64, 200, 0, 64, 150),     # eta >= n: nothing written, full causal softmax
+    (64, 8, 8, 16, 1),         # a single token
+])
+def test_prefill_f32_matches_oracle(L, d, eta, lam, chunk, n):
+    x = synth.gauss_inputs(1, 2, n, d, d, "f32", seed=100 + n + lam)
+    Y, wpos, lay = run_prefill(L, x, eta, lam, chunk)
+    ref, _ = check_decisions(x, wpos, eta, lam)
+    check_outputs(Y, ref["Y"], "f32")
+    _final_state_matches(lay, ref, eta, n, "f32")
+
+
+def test_no_write_prefill_is_causal_softmax(L):
+    x = synth.gauss_inputs(1, 1, 90, 64, 64, "f32", seed=5)
+    Y, wpos, _ = run_prefill(L, x, 60, 40, 32)
+    assert (wpos == -1).all()
+    want = R.causal_softmax_attention(*(x.widened(a)[0, 0] for a in "qkv"))
+    check_outputs(Y[0, 0], want, "f32")
+
+
+def test_zero_budget_prefill_is_linear_attention(L):
+    x = synth.gauss_inputs(1, 1, 150, 64, 64, "f32", seed=6)
+    Y, wpos, _ = run_prefill(L, x, 0, 0, 16)
+    assert list(wpos[0, 0]) == list(range(150))
+    want = R.linear_attention(*(x.widened(a)[0, 0] for a in "qkv"), x.W)
+    check_outputs(Y[0, 0], want, "f32")
+
+
+def test_phi_kernel_matches_oracle_phi(L):
+    """K1 output (left in the prefill workspace) against the float64 feature map."""
+    x = synth.gauss_inputs(2, 3, 77, 128, 128, "bf16", seed=7)
+    _, _, lay = run_prefill(L, x, 8, 8, 16)
+    BH, n, D = 6, 77, 128
+    ws = lay.workspace
+    nb = 4 * BH * n * D
+    phiK = ws[:nb].view(torch.float32).cpu().numpy().reshape(2, 3, n, D)
+    off = (nb + 255) // 256 * 256
+    phiQ = ws[off:off + nb].view(torch.float32).cpu().numpy().reshape(2, 3, n, D)
+    np.testing.assert_allclose(phiK, R.phi(x.widened("k"), x.W), rtol=2e-6, atol=1e-8)
+    np.testing.assert_allclose(phiQ, R.phi(x.widened("q"), x.W), rtol=2e-6, atol=1e-8)
+
+
+@pytest.mark.parametrize("eta,lam,chunk,n", [(16, 16, 16, 400), (64, 64, 64, 1000), (8, 200, 32, 600)])
+def test_prefill_bf16_within_gap_and_tolerance(L, eta, lam, chunk, n):
+    x = synth.gauss_inputs(2, 3, n, 128, 128, "bf16", seed=200 + lam)
+    Y, wpos, lay = run_prefill(L, x, eta, lam, chunk)
+    rep, free = check_decisions(x, wpos, eta, lam)
+    check_outputs(Y, rep["Y"], "bf16")
+
+
+def test_workload1_f32_full(L):
+    """The float32 workload (1 head, n = 1024, d = D = 64, eta = lambda = 64, C = 64): the
+    decision log must equal the oracle's and outputs agree to 1e-4."""
+    w = synth.WORKLOADS["w1_f32_n1024"]
+    x = synth.make_inputs(w)
+    Y, wpos, lay = run_prefill(L, x, w.eta, w.lam, w.chunk)
+    ref, _ = check_decisions(x, wpos, w.eta, w.lam)
+    check_outputs(Y, ref["Y"], "f32")
+    _final_state_matches(lay, ref, w.eta, w.n, "f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_chunk_length_has_no_effect(L, dtype):
+    """C only schedules the work: decision logs are identical and outputs agree."""
+    x = synth.gauss_inputs(1, 2, 777, 128, 128, dtype, seed=9)
+    base_y, base_w = None, None
+    for chunk in (16, 32, 64, 128, 256):
+        Y, wpos, _ = run_prefill(L, x, 24, 40, chunk)
+        if base_y is None:
+            base_y, base_w = Y, wpos
+            continue
+        assert np.array_equal(wpos, base_w)
+        assert np.abs(Y - base_y).max() <= (1e-5 if dtype == "f32" else 1e-2)
+
+
+@pytest.mark.parametrize("dtype,d,eta,lam", [("f32", 64, 16, 24), ("bf16", 128, 32, 64), ("bf16", 128, 8, 130),
+                                             ("f32", 64, 0, 5), ("f32", 64, 6, 0)])
+def test_prefill_then_decode_equals_longer_prefill(L, dtype, d, eta, lam):
+    """prefill(x[:n]) followed by m decode steps reproduces prefill(x[:n+m]): the same
+    decisions, outputs and final memory (the per-token rule is causal)."""
+    n, m = 180, 40
+    x = synth.gauss_inputs(2, 2, n + m, d, d, dtype, seed=300 + lam)
+    Yfull, wfull, layfull = run_prefill(L, x, eta, lam, 32, n=n + m)
+    Yp, wp, lay = run_prefill(L, x, eta, lam, 32, n=n)
+    dev = "cuda"
+    Q, K, V = (to_dev(getattr(x, a), dev, dtype) for a in "qkv")
+    W = torch.from_numpy(x.W).to(dev)
+    ys, ws = [], []
+    for t in range(n, n + m):
+        wpt = torch.empty(2, 2, dtype=torch.int32, device=dev)
+        ys.append(lay.decode_step(Q[:, :, t].contiguous(), K[:, :, t].contiguous(), V[:, :, t].contiguous(), W,
+                                  written_pos=wpt))
+        ws.append(wpt)
+    torch.cuda.synchronize()
+    wdec = torch.stack(ws, -1).cpu().numpy()
+    ydec = to_f64(torch.stack(ys, 2))
+    assert np.array_equal(wp, wfull[..., :n])
+    assert np.array_equal(wdec, wfull[..., n:]), "decode decisions differ from the longer prefill"
+    tol = 2e-5 if dtype == "f32" else 1.6e-2
+    assert np.abs(ydec - Yfull[:, :, n:]).max() <= tol
+    a, b = lay.read_state(), layfull.read_state()
+    assert (a["t"] == n + m).all() and (a["status"] == 0).all()
+    np.testing.assert_array_equal(a["H"], b["H"])
+    np.testing.assert_array_equal(a["s"], b["s"])
+    for i in range(4):
+        assert sorted(p for p in a["c_pos"][i] if p >= 0) == sorted(p for p in b["c_pos"][i] if p >= 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_decode_from_empty_matches_oracle(L, dtype):
+    """Decode steps from the empty memory (no prefill) follow the oracle."""
+    B, Hh, n, d, eta, lam = 1, 3, 120, 64, 8, 12
+    x = synth.gauss_inputs(B, Hh, n, d, d, dtype, seed=17)
+    lay = L.Lola(B, Hh, d, d, eta, lam, chunk=16, dtype=torch.bfloat16 if dtype == "bf16" else torch.float32)
+    Q, K, V = (to_dev(getattr(x, a), "cuda", dtype) for a in "qkv")
+    W = torch.from_numpy(x.W).cuda()
+    ys, ws = [], []
+    for t in range(n):
+        wpt = torch.empty(B, Hh, dtype=torch.int32, device="cuda")
+        ys.append(lay.decode_step(Q[:, :, t].contiguous(), K[:, :, t].contiguous(), V[:, :, t].contiguous(), W,
+                                  written_pos=wpt))
+        ws.append(wpt)
+    torch.cuda.synchronize()
+    wpos = torch.stack(ws, -1).cpu().numpy()
+    Y = to_f64(torch.stack(ys, 2))
+    ref, _ = check_decisions(x, wpos, eta, lam)
+    check_outputs(Y, ref["Y"], dtype)
+    st, words = L.lola_read_status(lay.cfg, lay.state)
+    assert st == 0, words
+
+
+def test_status_words_clear_after_prefill(L):
+    x = synth.gauss_inputs(1, 4, 200, 128, 128, "bf16", seed=19)
+    _, _, lay = run_prefill(L, x, 16, 16, 64)
+    st, words = L.lola_read_status(lay.cfg, lay.state)
+    assert st == 0 and words == [0, 0, 0, 0]
