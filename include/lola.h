@@ -71,7 +71,7 @@ typedef struct {
     int32_t dtype;      /* lola_dtype */
 } lola_config;
 
-/* Supported by this build: d_k = d_v = D in {64, 128}; lambda <= 1024; eta <= 65536;
+/* Supported by this build: d_k = d_v = D in {64, 128}; lambda <= 1024; eta <= 8192;
  * chunk a power of two in [16, 256]; B * Hh >= 1. */
 
 /* ---- per-head state layout (the public "checkpoint" format) -----------------------
