@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="session")
 def lib():
-    from sparse_exact_kv_gb300 import _build
-    _build.build()
+    import __graft_entry__
+    __graft_entry__._build_module().build()
     import sparse_exact_kv_gb300 as L
     return L
 
