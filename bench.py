@@ -1,0 +1,440 @@
+#!/usr/bin/env python
+"""Benchmark of the LoLA hybrid-attention hot path on one GB300 (or N, one process each).
+
+One step = one lola_prefill over the workload the metric is quoted on: 4 sequences x 32
+heads, n = 4096, d = D = 128, eta = lambda = 64, C = 64, bf16 inputs (K rows normalised to
+norm sqrt(128)); inputs (402 MB) exceed the 129 MB L2.  `value` is prefill tokens/s per
+layer (B * n / step time, summed over ranks).  The decode workload (64 x 32 heads, state
+prefilled from a 4096-token prefix, then single-token steps) is timed in the same run and
+reported under "decode".  Each rank runs its own replica (weak scaling, no collective
+on the data path).
+
+--impl reference times the CPU float64 oracle on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "prefill & decode tokens/s per layer on 1 GB300; % of tensor/HBM roofline"
+PREFILL = "w2_bf16_b4h32_n4096"
+DECODE = "w4_bf16_decode_b64h32"
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", default="lola", choices=["lola", "reference"])
+    p.add_argument("--decode-steps", type=int, default=64, help="timed decode steps")
+    p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------------------
+
+class Ranks:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = False
+
+    def init_gpu(self):
+        import torch
+        torch.cuda.set_device(self.local)
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
+            self.pg = True
+
+    def barrier(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------------------
+# clocks and peaks
+# ---------------------------------------------------------------------------------------
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu: int):
+        self.gpu = gpu
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [c.strip() for c in line.split(",")]
+                if len(f) >= 9:
+                    rows.append(f)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        reasons = set()
+        for r in rows:
+            for name, col in (("hw_slowdown", 5), ("hw_thermal_slowdown", 6), ("sw_thermal_slowdown", 7),
+                              ("sw_power_cap", 8)):
+                if r[col].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows), "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+def peaks(sm_count: int):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        src = "measured"
+    else:
+        p = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "sm_max_mhz": 2070.0}
+        src = "fallback"
+    mhz = float(p.get("sm_max_mhz", 2070.0))
+    # float32 CUDA-core peak: SMs x 128 FP32 lanes x 2 flop (FMA) x max SM clock
+    p["fp32_tflops"] = sm_count * 128 * 2 * mhz * 1e6 / 1e12
+    p["source"] = src
+    return p
+
+
+# ---------------------------------------------------------------------------------------
+# algorithmic work (per head-token), stated in the design notes
+# ---------------------------------------------------------------------------------------
+
+def select_flops_per_step(D, dv, lam):
+    """Allocation chain per step (steady state): the evictee's H^T phi (2 D dv), the rank-1
+    write of H (2 D dv), one Gram row phi_w . phi_i (2 lambda D), the N update of every
+    candidate (2 lambda dv) and the SRE of the lambda + 1 candidates (4 (lambda + 1) dv)."""
+    return 2 * D * dv + 2 * D * dv + 2 * lam * D + 2 * lam * dv + 4 * (lam + 1) * dv
+
+
+def output_flops_per_token(dk, dv, D, eta, lam):
+    """Co-normalised read per query: softmax branch over eta + lambda exact keys
+    (2 (eta + lambda)(dk + dv)) and the linear read H^T phi(q), phi(q)^T s (2 D dv + 2 D)."""
+    return 2 * (eta + lam) * (dk + dv) + 2 * D * dv + 2 * D
+
+
+def decode_bytes_per_head(d, D, eta, lam, io=2):
+    """Algorithmic HBM bytes of one decode step of one head: H read + write, s read + write,
+    the eta + lambda exact KV read, q, k, v in and y out, and the new KV written."""
+    return 2 * 4 * D * d + 2 * 4 * D + (eta + lam) * 2 * d * io + 4 * d * io + 2 * d * io
+
+
+# ---------------------------------------------------------------------------------------
+# the CUDA path
+# ---------------------------------------------------------------------------------------
+
+def dev_tensor(a, dtype: str, dev):
+    import numpy as np
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype == "bf16":
+        t = t.view(torch.bfloat16)
+    return t.to(dev)
+
+
+def time_loop(fn, steps, stream):
+    import torch
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def kernel_times(L, names):
+    out = {}
+    for k in names:
+        ms, cnt = L.lola_kernel_time(k)
+        if cnt:
+            out[k] = {"launches": cnt, "total_ms": ms, "avg_ms": ms / cnt}
+    return out
+
+
+def run_prefill(L, R, args, pk):
+    import torch
+    import synth
+    w = synth.WORKLOADS[PREFILL]
+    x = synth.make_inputs(w)
+    dev = torch.device("cuda", R.local)
+    Q, K, V = (dev_tensor(getattr(x, a), w.dtype, dev) for a in "qkv")
+    W = torch.from_numpy(x.W).to(dev)
+    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev)
+    ws = lay.workspace_for(w.n)
+    Y = torch.empty_like(V)
+    wpos = torch.empty(w.B, w.Hh, w.n, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        L.lola_prefill(lay.cfg, w.n, Q, K, V, W, 0, Y, lay.state, wpos, ws, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with Clocks(R.local) as clk:
+        L.lola_kernel_timing(True)
+        R.barrier()
+        ms = time_loop(step, args.steps, stream)
+        R.barrier()
+        L.lola_kernel_timing(False)
+        kt = kernel_times(L, ["state_init", "phi", "select", "output"])
+    ms = R.max(ms) / args.steps
+    tokens = w.B * w.n
+    res = {"workload": w, "ms": ms, "value": R.world * tokens / (ms / 1e3), "kernels": kt, "clocks": clk.summary(),
+           "launches": sum(v["launches"] for v in kt.values())}
+    heads = w.B * w.Hh
+    sel = kt.get("select")
+    if sel:
+        fl = heads * w.n * select_flops_per_step(w.D, w.d, w.lam)
+        ach = fl / (sel["avg_ms"] / 1e3) / 1e12
+        res["roofline"] = {"kernel": "select", "bound": "alu", "achieved": ach, "peak": pk["fp32_tflops"],
+                           "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"], "traffic": None,
+                           "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+    out = kt.get("output")
+    if out:
+        fl = heads * w.n * output_flops_per_token(w.d, w.d, w.D, w.eta, w.lam)
+        ach = fl / (out["avg_ms"] / 1e3) / 1e12
+        out["achieved_tflops"] = ach
+        out["frac_of_bf16_peak"] = ach / pk["bf16_tflops"]
+    phi = kt.get("phi")
+    if phi:
+        byts = heads * w.n * (w.d * 2 + w.D * 4)
+        phi["achieved_gbs"] = byts / (phi["avg_ms"] / 1e3) / 1e9
+    # end to end: pinned host inputs in, Y back to pinned host memory, every step
+    if not args.no_e2e:
+        hq, hk, hv = (t.cpu().pin_memory() for t in (Q, K, V))
+        hy = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+
+        def e2e_step():
+            Q.copy_(hq, non_blocking=True)
+            K.copy_(hk, non_blocking=True)
+            V.copy_(hv, non_blocking=True)
+            step()
+            hy.copy_(Y, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        R.barrier()
+        ems = R.max(time_loop(e2e_step, args.steps, stream)) / args.steps
+        res["e2e"] = {"value": R.world * tokens / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+                      "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(),
+                      "d2h_bytes_per_step": Y.numel() * Y.element_size()}
+    res["x"] = x
+    return res
+
+
+def run_decode(L, R, args, pk):
+    import torch
+    import synth
+    w = synth.WORKLOADS[DECODE]
+    x = synth.make_inputs(w)
+    dev = torch.device("cuda", R.local)
+    steps = min(args.decode_steps, w.decode_steps - args.warmup)
+    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev)
+    W = torch.from_numpy(x.W).to(dev)
+    P = [dev_tensor(getattr(x, a)[:, :, :w.n], w.dtype, dev) for a in "qkv"]
+    lay.prefill(*P, W)
+    del P
+    lay.workspace = None
+    nt = args.warmup + steps
+    dq, dk, dv = (dev_tensor(getattr(x, a)[:, :, w.n:w.n + nt].transpose(2, 0, 1, 3), w.dtype, dev) for a in "qkv")
+    y = torch.empty(w.B, w.Hh, w.d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+    it = [0]
+
+    def step():
+        i = it[0]
+        L.lola_decode_step(lay.cfg, lay.state, W, 0, dq[i], dk[i], dv[i], y, None, stream)
+        it[0] += 1
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    with Clocks(R.local) as clk:
+        L.lola_kernel_timing(True)
+        R.barrier()
+        ms = time_loop(step, steps, stream)
+        R.barrier()
+        L.lola_kernel_timing(False)
+        kt = kernel_times(L, ["decode"])
+    ms = R.max(ms) / steps
+    heads = w.B * w.Hh
+    res = {"metric": "decode tokens/s per layer", "value": R.world * w.B / (ms / 1e3), "unit": "tokens/s",
+           "ms_per_step": ms, "steps": steps,
+           "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "d": w.d, "D": w.D, "eta": w.eta, "lambda": w.lam,
+                      "prefix": w.n, "state_bytes": lola_state_bytes(L, lay)},
+           "kernels": kt, "clocks": clk.summary(), "gpu_launches": sum(v["launches"] for v in kt.values())}
+    dk_ = kt.get("decode")
+    if dk_:
+        byts = heads * decode_bytes_per_head(w.d, w.D, w.eta, w.lam)
+        ach = byts / (dk_["avg_ms"] / 1e3) / 1e9
+        res["roofline"] = {"kernel": "decode", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": ach / pk["hbm_gbs"], "traffic": None,
+                           "algorithmic_bytes_per_launch": byts}
+    return res
+
+
+def lola_state_bytes(L, lay):
+    return L.lola_state_bytes(lay.cfg)
+
+
+# ---------------------------------------------------------------------------------------
+# the CPU oracle
+# ---------------------------------------------------------------------------------------
+
+def oracle_sample(x, w, heads: int):
+    """Runs the oracle on the first `heads` heads of the workload; returns (seconds, tokens, threads)."""
+    from oracle import inc
+    BH = w.B * w.Hh
+    heads = min(heads, BH)
+    sl = lambda a: a.reshape(BH, *a.shape[2:])[:heads]  # noqa: E731
+    t0 = time.perf_counter()
+    out = inc.run(sl(x.q), sl(x.k), sl(x.v), x.W, w.eta, w.lam, w.dtype)
+    dt = time.perf_counter() - t0
+    return dt, heads * w.n / w.Hh, out["threads"]
+
+
+def cpu_baseline(x, w):
+    heads = min(w.B * w.Hh, 2 * (os.cpu_count() or 1))
+    dt, tokens, threads = oracle_sample(x, w, heads)
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {heads} of {w.B * w.Hh} heads of {w.name}, full n={w.n} "
+                      f"({tokens:g} token-equivalents in {dt:.2f} s)"}
+
+
+def run_reference(args):
+    R = Ranks()
+    if R.rank != 0:
+        return 0
+    import synth
+    w = synth.WORKLOADS[PREFILL]
+    x = synth.make_inputs(w, B=1)         # one sequence's 32 heads: the sample is drawn from them
+    heads = min(w.Hh, max(1, os.cpu_count() or 1))
+    for _ in range(args.warmup):
+        oracle_sample(x, x.w, heads)
+    times = []
+    tokens = threads = 0
+    for _ in range(args.steps):
+        dt, tokens, threads = oracle_sample(x, x.w, heads)
+        times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = tokens / (ms / 1e3)
+    sample = f"each step: {heads} of {w.B * w.Hh} heads of {w.name}, full n={w.n}"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta,
+                       "lambda": w.lam, "chunk": w.chunk},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    import torch
+    import sparse_exact_kv_gb300 as L
+    R = Ranks()
+    R.init_gpu()
+    props = torch.cuda.get_device_properties(R.local)
+    pk = peaks(props.multi_processor_count)
+    pre = run_prefill(L, R, args, pk)
+    w = pre["workload"]
+    dec = None if args.no_decode else run_decode(L, R, args, pk)
+    cpu = None
+    if R.rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(pre["x"], w)
+    if R.rank == 0:
+        launches = pre["launches"] * 1
+        line = {
+            "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": R.world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": pre["ms"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta,
+                       "lambda": w.lam, "chunk": w.chunk, "l2": "inputs 402 MB > 129 MB L2, no flush",
+                       "parallelism": f"replicas x{R.world}"},
+            "roofline": pre.get("roofline"), "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
+            "clocks": pre["clocks"], "kernels": pre["kernels"], "peaks": {k: pk[k] for k in
+                                                                        ("hbm_gbs", "bf16_tflops", "fp32_tflops",
+                                                                         "source")},
+            "decode": dec,
+        }
+        print(json.dumps(line))
+    R.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

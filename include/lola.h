@@ -156,6 +156,30 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W,
 int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* host_status,
                          void* stream);
 
+/* ---- tracing: per-kernel device time of the library's own launches --------------------
+ * When enabled, every kernel launch of lola_prefill / lola_decode_step / lola_state_init is
+ * bracketed by two CUDA events on the call's stream (a few microseconds of overhead per
+ * launch, no device memory).  Kernel ids: */
+typedef enum {
+    LOLA_KERNEL_STATE_INIT = 0,  /* state reset */
+    LOLA_KERNEL_PHI = 1,         /* feature map of Q and K */
+    LOLA_KERNEL_SELECT = 2,      /* allocation chain: SRE scoring, argmin, (H, s) write */
+    LOLA_KERNEL_OUTPUT = 3,      /* co-normalised output of every query */
+    LOLA_KERNEL_DECODE = 4,      /* one decode step */
+    LOLA_KERNEL_COUNT = 5
+} lola_kernel_id;
+
+/* enable != 0: clear the totals and start recording (process-wide); 0: stop recording. */
+int32_t lola_kernel_timing(int32_t enable);
+
+/* Waits for the recorded events of kernel `id`, then returns in *total_ms and *launches
+ * the summed device time and number of launches recorded since lola_kernel_timing(1).
+ * Either output may be NULL. */
+int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches);
+
+/* Static name of a kernel id ("" if out of range). */
+const char* lola_kernel_name(int32_t id);
+
 #ifdef __cplusplus
 }
 #endif

@@ -29,7 +29,9 @@ LOLA_BF16 = 1
 # every symbol include/lola.h declares
 EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_check_config",
            "lola_state_layout_of", "lola_state_bytes", "lola_prefill_workspace_bytes", "lola_state_init",
-           "lola_prefill", "lola_decode_step", "lola_read_status")
+           "lola_prefill", "lola_decode_step", "lola_read_status", "lola_kernel_timing", "lola_kernel_time",
+           "lola_kernel_name")
+KERNELS = ("state_init", "phi", "select", "output", "decode")
 
 
 class lola_config(ctypes.Structure):
@@ -72,6 +74,10 @@ def _load():
                          ctypes.c_int32),
         "lola_decode_step": ([C, P, P, ctypes.c_int64, P, P, P, P, P, P], ctypes.c_int32),
         "lola_read_status": ([C, P, P, P], ctypes.c_int32),
+        "lola_kernel_timing": ([ctypes.c_int32], ctypes.c_int32),
+        "lola_kernel_time": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)],
+                             ctypes.c_int32),
+        "lola_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -156,6 +162,22 @@ def lola_read_status(cfg: lola_config, state, stream=None):
     return st, list(buf)
 
 
+def lola_kernel_timing(enable: bool) -> None:
+    _check(_lib.lola_kernel_timing(1 if enable else 0), "lola_kernel_timing")
+
+
+def lola_kernel_time(kernel) -> tuple[float, int]:
+    """(total device ms, launches) of a kernel id or name since timing was enabled."""
+    kid = KERNELS.index(kernel) if isinstance(kernel, str) else int(kernel)
+    ms, cnt = ctypes.c_double(), ctypes.c_int64()
+    _check(_lib.lola_kernel_time(kid, ctypes.byref(ms), ctypes.byref(cnt)), "lola_kernel_time")
+    return ms.value, cnt.value
+
+
+def lola_kernel_name(kid: int) -> str:
+    return _lib.lola_kernel_name(kid).decode()
+
+
 # ---------------------------------------------------------------------------------------
 # Convenience: buffers allocated through torch, then the C ABI
 # ---------------------------------------------------------------------------------------
@@ -209,16 +231,17 @@ class Lola:
         def f(off, count, dt, size):
             return np.ascontiguousarray(raw[:, off: off + count * size]).view(dt)
 
+        BH = c.B * c.Hh
         hdr = f(0, 16, np.int32, 4)
         return dict(t=hdr[:, 0], n_cache=hdr[:, 1], n_written=hdr[:, 2], status=hdr[:, 3],
-                    H=f(L.H, c.D * c.d_v, np.float32, 4).reshape(-1, c.D, c.d_v),
+                    H=f(L.H, c.D * c.d_v, np.float32, 4).reshape(BH, c.D, c.d_v),
                     s=f(L.s, c.D, np.float32, 4),
                     win_pos=f(L.win_pos, c.eta, np.int32, 4),
-                    win_k=f(L.win_k, c.eta * c.d_k, io, isz).reshape(-1, c.eta, c.d_k),
-                    win_v=f(L.win_v, c.eta * c.d_v, io, isz).reshape(-1, c.eta, c.d_v),
+                    win_k=f(L.win_k, c.eta * c.d_k, io, isz).reshape(BH, c.eta, c.d_k),
+                    win_v=f(L.win_v, c.eta * c.d_v, io, isz).reshape(BH, c.eta, c.d_v),
                     c_pos=f(L.c_pos, c.lambda_, np.int32, 4),
-                    c_k=f(L.c_k, c.lambda_ * c.d_k, io, isz).reshape(-1, c.lambda_, c.d_k),
-                    c_v=f(L.c_v, c.lambda_ * c.d_v, io, isz).reshape(-1, c.lambda_, c.d_v),
-                    c_phi=f(L.c_phi, c.lambda_ * c.D, np.float32, 4).reshape(-1, c.lambda_, c.D),
-                    c_N=f(L.c_N, c.lambda_ * c.d_v, np.float32, 4).reshape(-1, c.lambda_, c.d_v),
+                    c_k=f(L.c_k, c.lambda_ * c.d_k, io, isz).reshape(BH, c.lambda_, c.d_k),
+                    c_v=f(L.c_v, c.lambda_ * c.d_v, io, isz).reshape(BH, c.lambda_, c.d_v),
+                    c_phi=f(L.c_phi, c.lambda_ * c.D, np.float32, 4).reshape(BH, c.lambda_, c.D),
+                    c_N=f(L.c_N, c.lambda_ * c.d_v, np.float32, 4).reshape(BH, c.lambda_, c.d_v),
                     c_z=f(L.c_z, c.lambda_, np.float32, 4))

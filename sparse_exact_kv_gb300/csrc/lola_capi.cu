@@ -2,6 +2,8 @@
 // workspace layouts, and the stream-ordered sequence of kernels of each call.
 #include <cstdio>
 #include <cstring>
+#include <mutex>
+#include <vector>
 
 #include "lola_internal.cuh"
 
@@ -51,6 +53,58 @@ __global__ void state_init_kernel(char* state, Layout L, int eta, int lam) {
     for (int i = threadIdx.x; i < lam; i += blockDim.x) cp[i] = -1;
 }
 
+// ---- tracing: CUDA events around each launch ----
+struct TimedLaunch {
+    int id;
+    cudaEvent_t start, stop;
+};
+std::mutex g_trace_mu;
+bool g_trace_on = false;
+std::vector<TimedLaunch> g_pending;
+double g_total_ms[LOLA_KERNEL_COUNT];
+int64_t g_launches[LOLA_KERNEL_COUNT];
+
+// Runs `launch` (returning cudaError_t) bracketed by events when tracing is on.
+template <typename F>
+cudaError_t traced(int id, cudaStream_t st, F&& launch) {
+    bool on;
+    {
+        std::lock_guard<std::mutex> g(g_trace_mu);
+        on = g_trace_on;
+    }
+    if (!on) return launch();
+    TimedLaunch r{id, nullptr, nullptr};
+    cudaError_t e = cudaEventCreate(&r.start);
+    if (e == cudaSuccess) e = cudaEventCreate(&r.stop);
+    if (e == cudaSuccess) e = cudaEventRecord(r.start, st);
+    if (e != cudaSuccess) return e;
+    e = launch();
+    if (e != cudaSuccess) return e;
+    e = cudaEventRecord(r.stop, st);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    g_pending.push_back(r);
+    return cudaSuccess;
+}
+
+void drain_pending(int id) {
+    std::vector<TimedLaunch> keep;
+    for (auto& r : g_pending) {
+        if (id >= 0 && r.id != id) {
+            keep.push_back(r);
+            continue;
+        }
+        float ms = 0.f;
+        if (cudaEventSynchronize(r.stop) == cudaSuccess && cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+            g_total_ms[r.id] += ms;
+            g_launches[r.id] += 1;
+        }
+        cudaEventDestroy(r.start);
+        cudaEventDestroy(r.stop);
+    }
+    g_pending.swap(keep);
+}
+
 }  // namespace
 
 Workspace carve_workspace(const Dims& d, int n, void* base) {
@@ -77,10 +131,12 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
 }
 
 cudaError_t launch_state_init(const Dims& d, char* state, const Layout& L, cudaStream_t st) {
-    cudaError_t e = cudaMemsetAsync(state, 0, (size_t)L.head_bytes * d.BH, st);
-    if (e != cudaSuccess) return e;
-    state_init_kernel<<<d.BH, 256, 0, st>>>(state, L, d.eta, d.lam);
-    return cudaGetLastError();
+    return traced(LOLA_KERNEL_STATE_INIT, st, [&]() {
+        cudaError_t e = cudaMemsetAsync(state, 0, (size_t)L.head_bytes * d.BH, st);
+        if (e != cudaSuccess) return e;
+        state_init_kernel<<<d.BH, 256, 0, st>>>(state, L, d.eta, d.lam);
+        return cudaGetLastError();
+    });
 }
 
 }  // namespace lola
@@ -173,13 +229,14 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = launch_state_init(d, static_cast<char*>(state), L, st);
     if (e != cudaSuccess) return cuda_fail(e, "state init");
-    e = launch_phi(d, n, K, W, w_head_stride, ws.phiK, st);
+    e = traced(LOLA_KERNEL_PHI, st, [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(K)");
-    e = launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, st);
+    e = traced(LOLA_KERNEL_PHI, st, [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
-    e = launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st);
+    e = traced(LOLA_KERNEL_SELECT, st,
+               [&]() { return launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st); });
     if (e != cudaSuccess) return cuda_fail(e, "selection");
-    e = launch_output(d, n, ws, Q, K, V, Y, st);
+    e = traced(LOLA_KERNEL_OUTPUT, st, [&]() { return launch_output(d, n, ws, Q, K, V, Y, st); });
     if (e != cudaSuccess) return cuda_fail(e, "output");
     return LOLA_OK;
 }
@@ -194,8 +251,11 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W, in
     for (const void* p : ptrs)
         if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;
     if (written_pos && (reinterpret_cast<uintptr_t>(written_pos) & 3)) return LOLA_ERR_INVALID_ARG;
-    cudaError_t e = launch_decode(d, static_cast<char*>(state), make_layout(d), W, w_head_stride, q, k, v, y,
-                                  written_pos, (cudaStream_t)stream);
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = traced(LOLA_KERNEL_DECODE, st, [&]() {
+        return launch_decode(d, static_cast<char*>(state), make_layout(d), W, w_head_stride, q, k, v, y, written_pos,
+                             st);
+    });
     return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "decode step");
 }
 
@@ -218,6 +278,33 @@ int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* hos
         bad |= w;
     }
     return bad ? LOLA_ERR_DEVICE : LOLA_OK;
+}
+
+int32_t lola_kernel_timing(int32_t enable) {
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    if (enable) {
+        drain_pending(-1);
+        for (int i = 0; i < LOLA_KERNEL_COUNT; ++i) {
+            g_total_ms[i] = 0.0;
+            g_launches[i] = 0;
+        }
+    }
+    g_trace_on = enable != 0;
+    return LOLA_OK;
+}
+
+int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches) {
+    if (id < 0 || id >= LOLA_KERNEL_COUNT) return LOLA_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> g(g_trace_mu);
+    drain_pending(id);
+    if (total_ms) *total_ms = g_total_ms[id];
+    if (launches) *launches = g_launches[id];
+    return LOLA_OK;
+}
+
+const char* lola_kernel_name(int32_t id) {
+    static const char* names[LOLA_KERNEL_COUNT] = {"state_init", "phi", "select", "output", "decode"};
+    return (id >= 0 && id < LOLA_KERNEL_COUNT) ? names[id] : "";
 }
 
 }  // extern "C"
