@@ -98,6 +98,13 @@ __device__ __forceinline__ float4 ld_cluster(uint32_t addr) {
     return v;
 }
 
+__device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
 // entry i (0..PD-1) of lane `sub` of a slot: float4 chunks interleaved across the 8 lanes
 __device__ __forceinline__ int slot_dim(int sub, int i) { return 4 * sub + 32 * (i >> 2) + (i & 3); }
 
@@ -114,8 +121,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
     constexpr int EW = D + DV;                     // phi and v of one candidate
     static_assert(PD % 4 == 0 && PV % 4 == 0 && kSelThreads % DV == 0 && D % NRG == 0, "shape");
 
-    __shared__ __align__(16) float xbuf[2][kSelWarps][EW];  // warp-best phi/v (speculative)
-    __shared__ __align__(16) float ebuf[4][EW];             // evictee phi/v, by step & 3
+    extern __shared__ __align__(16) float dyn_sm[];
+    float (*xbuf)[kSelWarps][EW] = reinterpret_cast<float (*)[kSelWarps][EW]>(dyn_sm);  // [2] warp-best phi/v
+    constexpr int PF = 4;                                   // evictee prefetch distance (steps)
+    constexpr int NEB = 8;                                  // ring of evictee buffers, by step & 7
+    constexpr int VCH = DV * (int)sizeof(T) / 16;           // 16-byte chunks of one value row
+    __shared__ __align__(16) float ebuf[NEB][EW];           // evictee phi and v (float32)
+    __shared__ __align__(16) T evraw[NEB][DV];              // value row as stored (cp.async target)
     __shared__ __align__(16) float wbuf[EW];                // winner phi/v copied from a peer
     __shared__ __align__(16) float red[NRG][DV];            // N_e partial sums
     __shared__ __align__(16) float s_sm[D];
@@ -157,15 +169,33 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
     if (rank == 0)
         for (int i = tid; i < n; i += kSelThreads) wstep[i] = -1;
 
+    // Evictee rows arrive by cp.async PF steps ahead: threads [0, D/4) copy phi(k_e),
+    // threads [D/4, D/4 + VCH) copy v_e; each step commits one group (possibly empty).
     auto prefetch = [&](int step) {
         const int e = step - eta;
         if (step < n && e >= 0) {
-            float* eb = ebuf[step & 3];
-            if (tid < D) eb[tid] = phiK[(int64_t)e * D + tid];
-            else if (tid < D + DV) eb[tid] = ldio<T>(a.V, (vrow0 + e) * DV + (tid - D));
+            if (tid < D / 4) cp_async16(&ebuf[step & (NEB - 1)][4 * tid], phiK + (int64_t)e * D + 4 * tid);
+            else if (tid < D / 4 + VCH)
+                cp_async16(reinterpret_cast<char*>(evraw[step & (NEB - 1)]) + 16 * (tid - D / 4),
+                           reinterpret_cast<const char*>(static_cast<const T*>(a.V) + (vrow0 + e) * DV) +
+                               16 * (tid - D / 4));
+        }
+        cp_async_commit();
+    };
+    // After this thread's copies for `step` have landed: widen its value chunk to float32.
+    auto finish = [&](int step) {
+        if (step < n && step - eta >= 0 && tid >= D / 4 && tid < D / 4 + VCH) {
+            constexpr int PER = 16 / (int)sizeof(T);
+            const int c = tid - D / 4;
+            const T* src = &evraw[step & (NEB - 1)][c * PER];
+            float* dst = &ebuf[step & (NEB - 1)][D + c * PER];
+#pragma unroll
+            for (int i = 0; i < PER; ++i) dst[i] = IO<T>::ld(src, i);
         }
     };
-    prefetch(0);
+    for (int st = 0; st < PF; ++st) prefetch(st);
+    cp_async_wait<0>();
+    finish(0);
     int n_cached = 0, n_written = 0;
     __syncthreads();
 
@@ -176,7 +206,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
         const float* wsrc = nullptr;
         if (dc.write) {
             if (dc.is_ev) {
-                wsrc = ebuf[tp & 3];
+                wsrc = ebuf[tp & (NEB - 1)];
             } else if (!CLUSTER || dc.cta == rank) {
                 wsrc = xbuf[tp & 1][dc.ws / kSPW];
             } else {
@@ -192,7 +222,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
             const int tcta = dc.write ? dc.cta : dc.fill % CL;
             const int tls = dc.write ? dc.ws : dc.fill / CL;
             const bool mine = tcta == rank && tls == ls;
-            const float* eb = ebuf[tp & 3];
+            const float* eb = ebuf[tp & (NEB - 1)];
             // ||v||^2 of the evictee with the slot's lane partition (the decode kernel's order)
             float vv = 0.f;
 #pragma unroll
@@ -252,7 +282,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
 
         // ---- score: evictee partial N_e, slot SREs, warp argmin ----
         const bool ev = t >= eta;
-        const float* eb = ebuf[t & 3];
+        const float* eb = ebuf[t & (NEB - 1)];
         if (ev) {
             float pj = 0.f;
 #pragma unroll
@@ -286,7 +316,7 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
 #pragma unroll
             for (int i = 0; i < PV; ++i) xb[D + slot_dim(sub, i)] = sv[i];
         }
-        prefetch(t + 1);
+        prefetch(t + PF);
         __syncthreads();
 
         // ---- decide: evictee SRE, CTA argmin, cluster exchange ----
@@ -330,25 +360,28 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
             }
             if constexpr (CLUSTER) {
                 if (lane < CL) st_cluster(map_rank(smem_addr(&exch[t & 1][rank]), lane), b);
-            } else {
-                if (lane == 0) exch[t & 1][0] = b;
-                __syncwarp();
+            } else if (lane == 0) {
+                exch[t & 1][0] = b;
             }
         }
-        if constexpr (CLUSTER) cluster_barrier();
+        if constexpr (CLUSTER) cluster_barrier(); else __syncwarp();
         if (warp == 0) {
-            Best b = lane < CL ? exch[t & 1][lane] : Best{INFINITY, INT_MAX, -2, 0};
-            int bc = lane;
+            Best b = exch[t & 1][0];
+            int bc = 0;
+            if constexpr (CLUSTER) {
+                b = lane < CL ? exch[t & 1][lane] : Best{INFINITY, INT_MAX, -2, 0};
+                bc = lane;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                Best c;
-                c.sre2 = __shfl_xor_sync(0xffffffffu, b.sre2, o);
-                c.pos = __shfl_xor_sync(0xffffffffu, b.pos, o);
-                c.ws = __shfl_xor_sync(0xffffffffu, b.ws, o);
-                const int cc = __shfl_xor_sync(0xffffffffu, bc, o);
-                if (key_less(c.sre2, c.pos, b.sre2, b.pos) || (c.sre2 == b.sre2 && c.pos == b.pos && cc < bc)) {
-                    b = c;
-                    bc = cc;
+                for (int o = 16; o > 0; o >>= 1) {
+                    Best c;
+                    c.sre2 = __shfl_xor_sync(0xffffffffu, b.sre2, o);
+                    c.pos = __shfl_xor_sync(0xffffffffu, b.pos, o);
+                    c.ws = __shfl_xor_sync(0xffffffffu, b.ws, o);
+                    const int cc = __shfl_xor_sync(0xffffffffu, bc, o);
+                    if (key_less(c.sre2, c.pos, b.sre2, b.pos) || (c.sre2 == b.sre2 && c.pos == b.pos && cc < bc)) {
+                        b = c;
+                        bc = cc;
+                    }
                 }
             }
             if (lane == 0) {
@@ -368,6 +401,8 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
                 }
             }
         }
+        cp_async_wait<PF - 1>();   // this thread's copies for step t + 1 have landed
+        finish(t + 1);
         __syncthreads();
         if (ev && !write) ++n_cached;
         if (write) ++n_written;
@@ -437,9 +472,27 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
         for (int r = n_cached + tid; r < lam; r += kSelThreads) reinterpret_cast<int32_t*>(rec + a.L.c_pos)[r] = -1;
 }
 
+template <int D, int DV>
+constexpr size_t select_dyn_smem() { return sizeof(float) * 2 * kSelWarps * (D + DV); }
+
+template <int D, int DV, typename T>
+cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t st) {
+    auto kern = select_kernel<D, DV, false, T>;
+    const size_t smem = select_dyn_smem<D, DV>();
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<d.BH, kSelThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 template <int D, int DV, typename T>
 cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t st) {
     auto kern = select_kernel<D, DV, true, T>;
+    const size_t smem = select_dyn_smem<D, DV>();
+    {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
     if (a.CL > 8) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
@@ -447,7 +500,7 @@ cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.BH * a.CL);
     cfg.blockDim = dim3(kSelThreads);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -497,16 +550,12 @@ cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void*
     if (a.CL > kMaxCluster) return cudaErrorInvalidValue;
     const bool bf = a.io_bf16;
     if (a.CL == 1) {
-        if (d.D == 128 && d.dv == 128) {
-            if (bf) select_kernel<128, 128, false, __nv_bfloat16><<<d.BH, kSelThreads, 0, st>>>(a);
-            else select_kernel<128, 128, false, float><<<d.BH, kSelThreads, 0, st>>>(a);
-            return cudaGetLastError();
-        }
-        if (d.D == 64 && d.dv == 64) {
-            if (bf) select_kernel<64, 64, false, __nv_bfloat16><<<d.BH, kSelThreads, 0, st>>>(a);
-            else select_kernel<64, 64, false, float><<<d.BH, kSelThreads, 0, st>>>(a);
-            return cudaGetLastError();
-        }
+        if (d.D == 128 && d.dv == 128)
+            return bf ? launch_select_single<128, 128, __nv_bfloat16>(d, a, st)
+                      : launch_select_single<128, 128, float>(d, a, st);
+        if (d.D == 64 && d.dv == 64)
+            return bf ? launch_select_single<64, 64, __nv_bfloat16>(d, a, st)
+                      : launch_select_single<64, 64, float>(d, a, st);
         return cudaErrorInvalidValue;
     }
     if (d.D == 128 && d.dv == 128)
