@@ -93,13 +93,16 @@ typedef struct {
  *   c_phi      float32 [lambda][D]       phi(k) of each cached key
  *   c_N        float32 [lambda][d_v]     H^T phi(k) kept current for each cached key
  *   c_z        float32 [lambda]          s^T phi(k) kept current for each cached key
+ *   ev         float32 [d_v + 4]         the next evictee (token t - eta, eta > 0): its
+ *                                        H^T phi(k) in [0, d_v) and s^T phi(k) at [d_v],
+ *                                        both against the memory after token t - 1
  * The appendix-B element count (eta + lambda)(d_k + d_v) + D d_v + D is the window,
- * cache, H and s above; c_phi, c_N, c_z, positions and the header are the bookkeeping
- * that lets a decode step score the cache without recomputing H^T phi(k). */
+ * cache, H and s above; c_phi, c_N, c_z, ev, positions and the header are the
+ * bookkeeping that lets a decode step score the cache without recomputing H^T phi(k). */
 
 typedef struct {
     int64_t head_bytes;
-    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z;
+    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
 } lola_state_layout;
 
 /* Library version (major * 10000 + minor * 100 + patch). */

@@ -42,7 +42,8 @@ class lola_config(ctypes.Structure):
 
 class lola_state_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
-                ("head_bytes", "H", "s", "win_pos", "win_k", "win_v", "c_pos", "c_k", "c_v", "c_phi", "c_N", "c_z")]
+                ("head_bytes", "H", "s", "win_pos", "win_k", "win_v", "c_pos", "c_k", "c_v", "c_phi", "c_N", "c_z",
+                 "ev")]
 
 
 class LolaError(RuntimeError):
@@ -244,4 +245,5 @@ class Lola:
                     c_v=f(L.c_v, c.lambda_ * c.d_v, io, isz).reshape(BH, c.lambda_, c.d_v),
                     c_phi=f(L.c_phi, c.lambda_ * c.D, np.float32, 4).reshape(BH, c.lambda_, c.D),
                     c_N=f(L.c_N, c.lambda_ * c.d_v, np.float32, 4).reshape(BH, c.lambda_, c.d_v),
-                    c_z=f(L.c_z, c.lambda_, np.float32, 4))
+                    c_z=f(L.c_z, c.lambda_, np.float32, 4),
+                    ev=f(L.ev, c.d_v + 1, np.float32, 4))

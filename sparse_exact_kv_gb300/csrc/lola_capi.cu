@@ -184,6 +184,7 @@ int32_t lola_state_layout_of(const lola_config* cfg, lola_state_layout* out) {
     out->c_phi = L.c_phi;
     out->c_N = L.c_N;
     out->c_z = L.c_z;
+    out->ev = L.ev;
     return LOLA_OK;
 }
 

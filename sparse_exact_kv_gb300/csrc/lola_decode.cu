@@ -8,21 +8,24 @@
 // the per-slot bookkeeping c_phi, c_N = H^T phi(k), c_z = s^T phi(k) that lets the step
 // score the cache without recomputing H^T phi(k) for every slot.
 //
-// One CTA of 512 threads per head.  The arithmetic that decides which candidate is
-// written (phi, the evictee's H^T phi, the slot SREs and their updates) uses the same
-// thread mapping and operation order as the prefill selection kernel, so a decode step
-// continues a prefill bit for bit.
+// One CTA of 512 threads per head, with the layouts and the arithmetic of the prefill
+// chain (lola_chain.cuh): the evictee's N arrives from the state (computed one step
+// ahead, against the memory before the previous write, then corrected by that write),
+// and at the end of the step the next evictee's N is prepared the same way.  A decode
+// step therefore continues a prefill bit for bit whenever eta > 0.  (With eta = 0 the
+// evictee is the token itself, unknown one step ahead; its N is then taken directly
+// against the current memory, equal in exact arithmetic.)
 #include <climits>
 
-#include "lola_internal.cuh"
+#include "lola_chain.cuh"
 
 namespace lola {
 namespace {
 
-constexpr int kDecThreads = 512;
-constexpr int kDecWarps = kDecThreads / kWarp;
-constexpr int kSG = 8;
-constexpr int kSlotsPerPass = kDecThreads / kSG;   // 64
+using namespace chain;
+
+constexpr int kDecWarps = kThreads / kWarp;
+constexpr int kSlotsPerPass = kThreads / kSG;   // 64
 
 struct DecArgs {
     char* state;
@@ -37,31 +40,30 @@ struct DecArgs {
     int32_t* written_pos;
 };
 
-__device__ __forceinline__ int slot_dim(int sub, int i) { return 4 * sub + 32 * (i >> 2) + (i & 3); }
-
 template <int D, int DV, typename T>
-__global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a) {
+__global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
+    using S = Shape<D, DV>;
     constexpr int DK = D;
-    constexpr int PD = D / kSG, PV = DV / kSG;
-    constexpr int NRG = kDecThreads / DV;
-    constexpr int HR = D / NRG;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, CD = S::CD, CV = S::CV;
     extern __shared__ __align__(16) float sm[];
     float* Ws = sm;                              // [D/2][DK+1]
-    float* xq = Ws + (D / 2) * (DK + 1);         // [DK]
+    float* xq = Ws + (D / 2) * (DK + 1);         // [DK]  query
     float* xk = xq + DK;                         // [DK]  new key
     float* xv = xk + DK;                         // [DV]  new value
     float* ek = xv + DV;                         // [DK]  evictee key
     float* evv = ek + DK;                        // [DV]  evictee value
-    float* phq = evv + DV;                       // [D]
-    float* phe = phq + D;                        // [D]
-    float* wphi = phe + D;                       // [D]   written phi
+    float* nk = evv + DV;                        // [DK]  next evictee key
+    float* phq = nk + DK;                        // [D]
+    float* phe = phq + D;                        // [D]   phi of the evictee
+    float* phn = phe + D;                        // [D]   phi of the next evictee
+    float* wphi = phn + D;                       // [D]   written phi
     float* wv = wphi + D;                        // [DV]  written v
-    float* s_sm = wv + DV;                       // [D]
-    float* red = s_sm + D;                       // [NRG][DV]
-    float* Ne = red + NRG * DV;                  // [DV]
-    float* sre = Ne + DV;                        // [lam]   slot SRE^2, then softmax weights
-    float* sc = sre + a.lam;                     // [eta + lam] scores
-    float* misc = sc + a.eta + a.lam;            // ze, vve, ese, ...
+    float* red = wv + DV;                        // [NRG][DV]
+    float* Ne_s = red + NRG * DV;                // [DV]  evictee N (chunk layout, for the slot move)
+    float* lin = Ne_s + DV;                      // [DV]  H^T phi(q)
+    float* sc = lin + DV;                        // [eta + lam] scores, then weights
+    uint2* wkey = reinterpret_cast<uint2*>(sc + a.eta + a.lam + (((a.eta + a.lam) & 1) ? 1 : 0));  // [16+1]
+    float* misc = reinterpret_cast<float*>(wkey + kDecWarps + 2);
     int* imisc = reinterpret_cast<int*>(misc + 8);
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
@@ -82,6 +84,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
     float* cphi = reinterpret_cast<float*>(rec + a.L.c_phi);
     float* cN = reinterpret_cast<float*>(rec + a.L.c_N);
     float* cz = reinterpret_cast<float*>(rec + a.L.c_z);
+    float* evs = reinterpret_cast<float*>(rec + a.L.ev);
     const T* qin = static_cast<const T*>(a.q) + (int64_t)bh * DK;
     const T* kin = static_cast<const T*>(a.k) + (int64_t)bh * DK;
     const T* vin = static_cast<const T*>(a.v) + (int64_t)bh * DV;
@@ -89,14 +92,17 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
     const bool ev = t >= eta;
     const int e = t - eta;
     const int ring = eta > 0 ? t % eta : 0;
+    const bool nxt = eta > 0 && t + 1 - eta >= 0;   // the next step has an evictee known now
+    const int nring = eta > 0 ? (t + 1) % eta : 0;
 
-    // ---- 1. load W, the new token, the evictee, H and s ----
+    // ---- 1. loads: W, tokens, H (H role), s (warp 0 chunk) ----
     const float* Wh = a.W + (int64_t)h * a.w_head_stride;
-    for (int i = tid; i < (D / 2) * DK; i += kDecThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
+    for (int i = tid; i < (D / 2) * DK; i += kThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
     if (tid < DK) {
         xq[tid] = IO<T>::ld(qin, tid);
         xk[tid] = IO<T>::ld(kin, tid);
         if (ev) ek[tid] = eta > 0 ? IO<T>::ld(wk, (int64_t)ring * DK + tid) : IO<T>::ld(kin, tid);
+        if (nxt) nk[tid] = IO<T>::ld(wk, (int64_t)nring * DK + tid);
     }
     if (tid < DV) {
         xv[tid] = IO<T>::ld(vin, tid);
@@ -105,12 +111,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
     const int hj = tid % DV, hrg = tid / DV;
     float hreg[HR];
 #pragma unroll
-    for (int r = 0; r < HR; ++r) hreg[r] = Hg[(hrg + NRG * r) * DV + hj];
-    if (tid < D) s_sm[tid] = sg[tid];
+    for (int r = 0; r < HR; ++r) hreg[r] = Hg[(hrg * HR + r) * DV + hj];
+    float s_reg[CD];
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < CD; ++i) s_reg[i] = sg[lane * CD + i];
+    }
     __syncthreads();
-    if (eta > 0 && ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
+    if (ev && eta > 0 && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
 
-    // ---- 2. phi(q), phi(k_e) ----
+    // ---- 2. phi(q), phi(k_e), phi(k_{e+1}) ----
     if (warp == 0) {
         float ph[D / 32];
         phi_warp<DK, D>(xq, Ws, lane, ph);
@@ -121,164 +131,162 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
         phi_warp<DK, D>(ek, Ws, lane, ph);
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) phe[lane + 32 * m] = ph[m];
+    } else if (warp == 2 && nxt) {
+        float ph[D / 32];
+        phi_warp<DK, D>(nk, Ws, lane, ph);
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) phn[lane + 32 * m] = ph[m];
     }
     __syncthreads();
 
-    // ---- 3. evictee partial H^T phi_e; slot SREs ----
-    if (ev) {
-        float pj = 0.f;
+    // ---- 3. partials against the memory before this step's write: the next evictee's
+    //         (or, with eta = 0, this step's own evictee) H^T phi ----
+    const float* pvec = eta > 0 ? phn : phe;
+    const bool want_partials = eta > 0 ? nxt : ev;
+    if (want_partials) red[hrg * DV + hj] = h_partial<D, DV>(pvec, hreg, hrg);
+    __syncthreads();
+
+    // ---- 4. the evictee's N, z and SRE (warp 0); the next evictee's N', z' ----
+    float Nn[CV], zn = 0.f;
+    if (warp == 0) {
+        uint32_t ehi = kNoKey, elo = kNoKey;
+        if (ev) {
+            float Ne[CV], ze;
+            if (eta > 0) {
 #pragma unroll
-        for (int r = 0; r < HR; ++r) pj = fmaf(phe[hrg + NRG * r], hreg[r], pj);
-        red[hrg * DV + hj] = pj;
+                for (int i = 0; i < CV; ++i) Ne[i] = evs[lane * CV + i];
+                ze = evs[DV];
+            } else {
+                reduce_partials<D, DV>(red, lane, Ne);
+                ze = chunk_dot_reg<D>(s_reg, phe, lane);
+            }
+            float vve;
+            const float es = chunk_sre2<DV>(Ne, ze, evv, lane, &vve);
+#pragma unroll
+            for (int i = 0; i < CV; ++i) Ne_s[lane * CV + i] = Ne[i];
+            if (lane == 0) misc[0] = ze;
+            ehi = key_hi(es);
+            elo = key_lo(e, kEvCode);
+        }
+        if (lane == 0) wkey[kDecWarps] = make_uint2(ehi, elo);
+        if (nxt) {
+            reduce_partials<D, DV>(red, lane, Nn);
+            zn = chunk_dot_reg<D>(s_reg, phn, lane);
+        }
     }
+    // slot SREs, pass by pass; each warp keeps its minimum over all passes
     const int sl = tid / kSG, sub = tid % kSG;
+    uint32_t bhi = kNoKey, blo = kNoKey;
     for (int base = 0; base < nc; base += kSlotsPerPass) {
         const int i = base + sl;
-        float ss = 0.f, vv = 0.f, z = 0.f;
+        float sN[PV], sv[PV], z = 0.f;
+#pragma unroll
+        for (int q = 0; q < PV; ++q) { sN[q] = 0.f; sv[q] = 0.f; }
         if (i < nc) {
             z = cz[i];
 #pragma unroll
             for (int q = 0; q < PV; ++q) {
                 const int dd = slot_dim(sub, q);
-                const float vq = IO<T>::ld(cv, (int64_t)i * DV + dd);
-                const float dlt = fmaf(-z, vq, cN[(int64_t)i * DV + dd]);
-                ss = fmaf(dlt, dlt, ss);
-                vv = fmaf(vq, vq, vv);
+                sv[q] = IO<T>::ld(cv, (int64_t)i * DV + dd);
+                sN[q] = cN[(int64_t)i * DV + dd];
             }
         }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-        vv += __shfl_xor_sync(0xffffffffu, vv, 1);
-        vv += __shfl_xor_sync(0xffffffffu, vv, 2);
-        vv += __shfl_xor_sync(0xffffffffu, vv, 4);
-        if (i < nc && sub == 0) sre[i] = z == 0.f ? vv : ss / (z * z);
+        const float svv = slot_vv<DV>(sv);
+        const float sre = slot_sre2<DV>(sN, z, sv, svv);
+        uint32_t khi = i < nc ? key_hi(sre) : kNoKey;
+        uint32_t klo = i < nc ? key_lo(cpos[i], 0) : kNoKey;
+        warp_min_key(khi, klo);
+        if (khi < bhi || (khi == bhi && klo < blo)) { bhi = khi; blo = klo; }
     }
+    if (lane == 0) wkey[warp] = make_uint2(bhi, blo);
     __syncthreads();
 
-    // ---- 4. decision (warp 0) ----
+    // ---- 5. decision ----
     const bool write = ev && (nc + 1 > lam);
     if (warp == 0) {
-        float es = INFINITY;
-        if (ev) {
-            float Nv[DV / 32], ze = 0.f, sse = 0.f, vve = 0.f;
-#pragma unroll
-            for (int i = 0; i < DV / 32; ++i) {
-                float acc = 0.f;
-#pragma unroll
-                for (int r = 0; r < NRG; ++r) acc += red[r * DV + lane + 32 * i];
-                Nv[i] = acc;
-                Ne[lane + 32 * i] = acc;
-            }
-#pragma unroll
-            for (int i = 0; i < D / 32; ++i) ze = fmaf(s_sm[lane + 32 * i], phe[lane + 32 * i], ze);
-            ze = warp_sum(ze);
-#pragma unroll
-            for (int i = 0; i < DV / 32; ++i) {
-                const float vq = evv[lane + 32 * i];
-                const float dlt = fmaf(-ze, vq, Nv[i]);
-                sse = fmaf(dlt, dlt, sse);
-                vve = fmaf(vq, vq, vve);
-            }
-            sse = warp_sum(sse);
-            vve = warp_sum(vve);
-            es = ze == 0.f ? vve : sse / (ze * ze);
-            if (lane == 0) misc[0] = ze;
-        }
-        float bs = INFINITY;
-        int bp = INT_MAX, bi = -2;
-        for (int i = lane; i < nc; i += kWarp) {
-            const int p = cpos[i];
-            if (key_less(sre[i], p, bs, bp)) { bs = sre[i]; bp = p; bi = i; }
-        }
-        if (ev && lane == 0 && key_less(es, e, bs, bp)) { bs = es; bp = e; bi = -1; }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            const int op = __shfl_xor_sync(0xffffffffu, bp, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            if (key_less(os, op, bs, bp)) { bs = os; bp = op; bi = oi; }
-        }
+        uint2 k = lane <= kDecWarps ? wkey[lane] : make_uint2(kNoKey, kNoKey);
+        warp_min_key(k.x, k.y);
         if (lane == 0) {
-            imisc[0] = write ? bi : -2;     // -1: evictee written; >= 0: slot written
-            imisc[1] = write ? bp : -1;
+            int wsel = -2, wpos = -1;
+            if (write) {
+                wpos = (int)(k.y >> 7);
+                wsel = ((k.y & 127u) == (uint32_t)kEvCode) ? -1 : -3;   // -3: a slot, found below
+            }
+            imisc[0] = wsel;
+            imisc[1] = wpos;
         }
     }
     __syncthreads();
-    const int wsel = imisc[0];
+    int wsel = imisc[0];
     const int wposn = imisc[1];
+    if (wsel == -3) {
+        // the written slot: the one holding position wposn
+        for (int i = tid; i < nc; i += kThreads)
+            if (cpos[i] == wposn) imisc[2] = i;
+        __syncthreads();
+        wsel = imisc[2];
+    }
     const float ze = misc[0];
 
-    // ---- 5. write: phi_w, v_w; H, s, slots ----
+    // ---- 6. write: phi_w, v_w; H, s, slots; the surviving evictee; next evictee ----
     if (write) {
         if (tid < D) wphi[tid] = wsel < 0 ? phe[tid] : cphi[(int64_t)wsel * D + tid];
         if (tid < DV) wv[tid] = wsel < 0 ? evv[tid] : IO<T>::ld(cv, (int64_t)wsel * DV + tid);
         __syncthreads();
-        const float wvj = wv[hj];
+        h_update<D, DV>(hreg, wphi, wv[hj], hrg);
+        if (warp == 0) {
 #pragma unroll
-        for (int r = 0; r < HR; ++r) hreg[r] = fmaf(wphi[hrg + NRG * r], wvj, hreg[r]);
-        if (tid < D) s_sm[tid] += wphi[tid];
-        // every cached slot (and the surviving evictee) absorbs the write
+            for (int i = 0; i < CD; ++i) s_reg[i] += wphi[lane * CD + i];
+        }
         for (int base = 0; base < nc; base += kSlotsPerPass) {
             const int i = base + sl;
-            const bool live = i < nc && i != wsel;
-            float g = 0.f;
-            if (live) {
+            float sphi[PD], sN[PV];
+            const bool live = i < nc;
+            // the written slot takes the evictee, which absorbs the write like the others
+            const bool moved = live && i == wsel;
 #pragma unroll
-                for (int q = 0; q < PD; ++q) {
-                    const int dd = slot_dim(sub, q);
-                    g = fmaf(wphi[dd], cphi[(int64_t)i * D + dd], g);
-                }
+            for (int q = 0; q < PD; ++q) {
+                const int dd = slot_dim(sub, q);
+                sphi[q] = live ? (moved ? phe[dd] : cphi[(int64_t)i * D + dd]) : 0.f;
             }
-            g += __shfl_xor_sync(0xffffffffu, g, 1);
-            g += __shfl_xor_sync(0xffffffffu, g, 2);
-            g += __shfl_xor_sync(0xffffffffu, g, 4);
-            if (live) {
 #pragma unroll
-                for (int q = 0; q < PV; ++q) {
-                    const int dd = slot_dim(sub, q);
-                    float* p = cN + (int64_t)i * DV + dd;
-                    *p = fmaf(g, wv[dd], *p);
-                }
-                if (sub == 0) cz[i] += g;
+            for (int q = 0; q < PV; ++q) {
+                const int dd = slot_dim(sub, q);
+                sN[q] = live ? (moved ? Ne_s[dd] : cN[(int64_t)i * DV + dd]) : 0.f;
+            }
+            const float g = slot_gram<D>(wphi, sphi, sub);
+            if (live) {
+                slot_axpy<DV>(sN, g, wv, sub);
+#pragma unroll
+                for (int q = 0; q < PV; ++q) cN[(int64_t)i * DV + slot_dim(sub, q)] = sN[q];
+                if (sub == 0) cz[i] = (moved ? ze : cz[i]) + g;
             }
         }
-        if (wsel >= 0 && warp == kDecWarps - 1) {
-            // the evictee survives and takes the written slot, after absorbing the write
-            float g = 0.f;
-            if (sub < kSG && lane < kSG) {
-#pragma unroll
-                for (int q = 0; q < PD; ++q) {
-                    const int dd = slot_dim(lane, q);
-                    g = fmaf(wphi[dd], phe[dd], g);
-                }
-            }
-            g += __shfl_xor_sync(0xffffffffu, g, 1);
-            g += __shfl_xor_sync(0xffffffffu, g, 2);
-            g += __shfl_xor_sync(0xffffffffu, g, 4);
-            if (lane < kSG) {
-#pragma unroll
-                for (int q = 0; q < PV; ++q) {
-                    const int dd = slot_dim(lane, q);
-                    cN[(int64_t)wsel * DV + dd] = fmaf(g, wv[dd], Ne[dd]);
-                }
-                if (lane == 0) cz[wsel] = ze + g;
-            }
+        if (warp == 0 && nxt) {
+            const float g = chunk_dot<D>(wphi, phn, lane);
+            chunk_axpy<DV>(Nn, g, wv, lane);
+            zn += g;
         }
     }
     int nc_after = nc;
     int slot_new = -1;
-    if (ev && !write) { slot_new = nc; nc_after = nc + 1; }
+    if (ev && !write) {
+        slot_new = nc;
+        nc_after = nc + 1;
+        if (tid < DV) cN[(int64_t)slot_new * DV + tid] = Ne_s[tid];
+        if (tid == 0) cz[slot_new] = ze;
+    }
     if (write && wsel >= 0) slot_new = wsel;
     if (slot_new >= 0) {
-        if (!write) {
-            if (tid < DV) cN[(int64_t)slot_new * DV + tid] = Ne[tid];
-            if (tid == 0) cz[slot_new] = ze;
-        }
         if (tid < D) cphi[(int64_t)slot_new * D + tid] = phe[tid];
         if (tid < DK) IO<T>::st(ck, (int64_t)slot_new * DK + tid, ek[tid]);
         if (tid < DV) IO<T>::st(cv, (int64_t)slot_new * DV + tid, evv[tid]);
         if (tid == 0) cpos[slot_new] = e;
+    }
+    if (warp == 0 && nxt) {
+#pragma unroll
+        for (int i = 0; i < CV; ++i) evs[lane * CV + i] = Nn[i];
+        if (lane == 0) evs[DV] = zn;
     }
     // the new token enters the window ring (its previous occupant was the evictee)
     if (eta > 0) {
@@ -288,40 +296,27 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
     }
     __syncthreads();
 
-    // ---- 6. output: softmax over window ∪ cache, linear read of (H, s) ----
+    // ---- 7. output: softmax over window ∪ cache, linear read of (H, s) after the write ----
     const float scale = 1.0f / sqrtf((float)DK);
     const int nwin = min(t + 1, eta);
     const int nkeys = nwin + nc_after;
-    // scores: 8 lanes per key
     for (int base = 0; base < nkeys; base += kSlotsPerPass) {
         const int i = base + sl;
         float acc = 0.f;
         if (i < nkeys) {
-            const T* kr;
-            if (i < nwin) {
-                const int p = t - i;                      // window positions t, t-1, ...
-                kr = wk + (int64_t)(p % eta) * DK;
-            } else {
-                kr = ck + (int64_t)(i - nwin) * DK;
-            }
+            const T* kr = i < nwin ? wk + (int64_t)((t - i) % eta) * DK : ck + (int64_t)(i - nwin) * DK;
 #pragma unroll
             for (int q = 0; q < PD; ++q) {
                 const int dd = slot_dim(sub, q);
                 acc = fmaf(xq[dd], IO<T>::ld(kr, dd), acc);
             }
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+        acc += __shfl_xor_sync(kFull, acc, 1);
+        acc += __shfl_xor_sync(kFull, acc, 2);
+        acc += __shfl_xor_sync(kFull, acc, 4);
         if (i < nkeys && sub == 0) sc[i] = acc * scale;
     }
-    // linear read partials
-    {
-        float pj = 0.f;
-#pragma unroll
-        for (int r = 0; r < HR; ++r) pj = fmaf(phq[hrg + NRG * r], hreg[r], pj);
-        red[hrg * DV + hj] = pj;
-    }
+    red[hrg * DV + hj] = h_partial<D, DV>(phq, hreg, hrg);
     __syncthreads();
     if (warp == 0) {
         float m = -INFINITY;
@@ -334,47 +329,49 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
             l += p;
         }
         l = warp_sum(l);
-        float dl = 0.f;
-#pragma unroll
-        for (int i = 0; i < D / 32; ++i) dl = fmaf(phq[lane + 32 * i], s_sm[lane + 32 * i], dl);
-        dl = warp_sum(dl);
+        const float dl = chunk_dot_reg<D>(s_reg, phq, lane);
         if (lane == 0) {
             const bool any = nkeys > 0;
             misc[1] = any ? expf(-m) : 1.f;
             misc[2] = any ? fmaf(misc[1], dl, l) : dl;
         }
+    } else if (warp == 1 && tid - 32 < DV / 4) {
+        // H^T phi(q): sum the row-group partials
+        const int j0 = 4 * (tid - 32);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            float acc = red[j0 + jj];
+#pragma unroll
+            for (int rg = 1; rg < NRG; ++rg) acc += red[rg * DV + j0 + jj];
+            lin[j0 + jj] = acc;
+        }
     }
     __syncthreads();
-    // y_j = (sum_i p_i v_i[j] + e^{-m} (H^T phi_q)_j) / den ; keys split over NRG groups
     {
+        // numerator: keys split over the NRG row groups, then combined
         float acc = 0.f;
         for (int i = hrg; i < nkeys; i += NRG) {
             const T* vr = i < nwin ? wvv + (int64_t)((t - i) % eta) * DV : cv + (int64_t)(i - nwin) * DV;
             acc = fmaf(sc[i], IO<T>::ld(vr, hj), acc);
         }
-        __syncthreads();
-        float lin = 0.f;
-        if (hrg == 0) {
-#pragma unroll
-            for (int r = 0; r < NRG; ++r) lin += red[r * DV + hj];
-        }
-        __syncthreads();
         red[hrg * DV + hj] = acc;
-        if (hrg == 0) Ne[hj] = lin;
         __syncthreads();
         if (tid < DV) {
             float num = 0.f;
 #pragma unroll
             for (int r = 0; r < NRG; ++r) num += red[r * DV + tid];
-            num = fmaf(misc[1], Ne[tid], num);
+            num = fmaf(misc[1], lin[tid], num);
             IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / misc[2]);
         }
     }
 
-    // ---- 7. write back H, s, header ----
+    // ---- 8. write back H, s, header ----
 #pragma unroll
-    for (int r = 0; r < HR; ++r) Hg[(hrg + NRG * r) * DV + hj] = hreg[r];
-    if (tid < D) sg[tid] = s_sm[tid];
+    for (int r = 0; r < HR; ++r) Hg[(hrg * HR + r) * DV + hj] = hreg[r];
+    if (warp == 0) {
+#pragma unroll
+        for (int i = 0; i < CD; ++i) sg[lane * CD + i] = s_reg[i];
+    }
     if (tid == 0) {
         hdr[HDR_T] = t + 1;
         hdr[HDR_NCACHE] = nc_after;
@@ -386,13 +383,14 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_kernel(const DecArgs a)
 template <int D, int DV, typename T>
 cudaError_t launch_decode_t(const Dims& d, const DecArgs& a, cudaStream_t st) {
     constexpr int DK = D;
-    const int NRG = kDecThreads / DV;
-    const size_t smem = sizeof(float) * ((D / 2) * (DK + 1) + 3 * DK + 2 * DV + 3 * D + DV + D + NRG * DV + DV +
-                                         d.lam + d.eta + d.lam + 16);
+    constexpr int NRG = kThreads / DV;
+    const size_t floats = (D / 2) * (DK + 1) + 4 * DK + 2 * DV + 4 * D + DV + NRG * DV + 2 * DV +
+                          (d.eta + d.lam + 1) + 2 * (kDecWarps + 2) + 16;
+    const size_t smem = sizeof(float) * floats + 64;
     auto kern = decode_kernel<D, DV, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<d.BH, kDecThreads, smem, st>>>(a);
+    kern<<<d.BH, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 

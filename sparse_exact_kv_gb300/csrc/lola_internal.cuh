@@ -23,7 +23,7 @@ __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int
 
 struct Layout {
     int64_t head_bytes;
-    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z;
+    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
 };
 
 inline Layout make_layout(const Dims& d) {
@@ -41,6 +41,7 @@ inline Layout make_layout(const Dims& d) {
     L.c_phi = o;    o = align256(o + 4ll * d.lam * d.D);
     L.c_N = o;      o = align256(o + 4ll * d.lam * d.dv);
     L.c_z = o;      o = align256(o + 4ll * d.lam);
+    L.ev = o;       o = align256(o + 4ll * (d.dv + 4));
     L.head_bytes = o;
     return L;
 }

@@ -8,32 +8,36 @@
 // is "write the argmin" (smaller SRE^2, then the older position).
 //
 // The chain is sequential in t, so one CTA -- or a thread-block cluster of CL CTAs when
-// lambda > 64 -- owns one head for the whole sequence:
-//   * cache slots live in registers: 8 lanes per slot, 4 slots per warp, 64 per CTA;
-//     each lane holds D/8 entries of phi(k) and d_v/8 entries of v and N = H^T phi(k);
-//     every slot keeps z = s^T phi(k) current, so a write w only costs each slot
-//     g = phi_w . phi_i, N += g v_w, z += g (exact: H changes by a rank-1 term);
-//   * each CTA holds a replica of H (D x d_v float32) in registers, 32 (or 8) entries
-//     per thread, for the evictee's N_e = H^T phi(k_e) and for the chunk snapshots;
-//   * per step: apply the previous write, score the live slots, warp argmin, then
-//     warp 0 finishes the evictee's SRE and the CTA argmin; with CL > 1 each CTA pushes
-//     its best to every peer's shared memory (st.shared::cluster) and one cluster
-//     barrier orders the exchange; the winner's phi/v are read back through DSMEM.
+// lambda > 64 -- owns one head for the whole sequence (layouts in lola_chain.cuh):
+//   * cache slots live in registers, 8 lanes per slot, 4 slots per warp, 64 per CTA; a
+//     write w costs each slot g = phi_w . phi_i, N += g v_w, z += g (exact: H changes by
+//     a rank-1 term);
+//   * each CTA holds a replica of H in registers (32 or 8 entries per thread) to compute
+//     the next evictee's H^T phi one step ahead and to emit the chunk snapshots; warp 0
+//     holds s and finishes the evictee (correction by the last write, SRE);
+//   * per step: apply the previous write; every warp scores its slots and takes its
+//     packed-key minimum with two redux.sync; warp 0 takes the CTA minimum after one
+//     barrier; with CL > 1 each CTA pushes its best to every peer's shared memory
+//     (st.shared::cluster) and one cluster barrier orders the exchange, and the winner's
+//     phi/v are read back through DSMEM;
+//   * evictee rows (phi(k_e), v_e) arrive by cp.async four steps ahead.
 // At every chunk start it stores H, s and the cache positions, from which the parallel
 // output kernel rebuilds every query's exact set and linear state.
 #include <climits>
 
-#include "lola_internal.cuh"
+#include "lola_chain.cuh"
 
 namespace lola {
 namespace {
 
-constexpr int kSelThreads = 512;
-constexpr int kSelWarps = kSelThreads / kWarp;
-constexpr int kSG = 8;                     // lanes per slot
+using namespace chain;
+
+constexpr int kSelWarps = kThreads / kWarp;
 constexpr int kSPW = kWarp / kSG;          // slots per warp
 constexpr int kSPC = kSelWarps * kSPW;     // slots per CTA
 constexpr int kMaxCluster = 16;
+constexpr int kPF = 4;                     // evictee prefetch distance (steps)
+constexpr int kNEB = 8;                    // evictee ring buffers (indexed by step & 7)
 
 struct SelArgs {
     int n, eta, lam, chunk, nck, CL, io_bf16;
@@ -55,16 +59,9 @@ struct Dec {
     int is_ev;   // ... and it was the evictee
     int pos;     // written position
     int cta;     // owner CTA of the written slot
-    int ws;      // warp * kSPW + slot of the written slot
+    int ws;      // local slot index of the written slot
     int ev;      // an evictee joined the candidates this step
     int fill;    // global slot the evictee fills when nothing was written
-    int pad;
-};
-
-struct __align__(16) Best {
-    float sre2;
-    int pos;
-    int ws;      // warp * kSPW + slot, or -1 for the evictee
     int pad;
 };
 
@@ -84,10 +81,8 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster(uint32_t addr, const Best& b) {
-    asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(__float_as_int(b.sre2)),
-                 "r"(b.pos), "r"(b.ws), "r"(b.pad)
-                 : "memory");
+__device__ __forceinline__ void st_cluster_u2(uint32_t addr, uint32_t x, uint32_t y) {
+    asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
 }
 __device__ __forceinline__ float4 ld_cluster(uint32_t addr) {
     float4 v;
@@ -97,44 +92,32 @@ __device__ __forceinline__ float4 ld_cluster(uint32_t addr) {
                  : "memory");
     return v;
 }
-
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
-
-// entry i (0..PD-1) of lane `sub` of a slot: float4 chunks interleaved across the 8 lanes
-__device__ __forceinline__ int slot_dim(int sub, int i) { return 4 * sub + 32 * (i >> 2) + (i & 3); }
-
-template <typename T>
-__device__ __forceinline__ float ldio(const void* p, int64_t i) {
-    return IO<T>::ld(static_cast<const T*>(p), i);
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 template <int D, int DV, bool CLUSTER, typename T>
-__global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a) {
-    constexpr int PD = D / kSG, PV = DV / kSG;     // per-lane phi / v entries of a slot
-    constexpr int NRG = kSelThreads / DV;          // H row groups
-    constexpr int HR = D / NRG;                    // H rows per thread
-    constexpr int EW = D + DV;                     // phi and v of one candidate
-    static_assert(PD % 4 == 0 && PV % 4 == 0 && kSelThreads % DV == 0 && D % NRG == 0, "shape");
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
+    using S = Shape<D, DV>;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, CD = S::CD, CV = S::CV;
+    constexpr int EW = D + DV;
+    constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
 
     extern __shared__ __align__(16) float dyn_sm[];
     float (*xbuf)[kSelWarps][EW] = reinterpret_cast<float (*)[kSelWarps][EW]>(dyn_sm);  // [2] warp-best phi/v
-    constexpr int PF = 4;                                   // evictee prefetch distance (steps)
-    constexpr int NEB = 8;                                  // ring of evictee buffers, by step & 7
-    constexpr int VCH = DV * (int)sizeof(T) / 16;           // 16-byte chunks of one value row
-    __shared__ __align__(16) float ebuf[NEB][EW];           // evictee phi and v (float32)
-    __shared__ __align__(16) T evraw[NEB][DV];              // value row as stored (cp.async target)
-    __shared__ __align__(16) float wbuf[EW];                // winner phi/v copied from a peer
-    __shared__ __align__(16) float red[NRG][DV];            // N_e partial sums
-    __shared__ __align__(16) float s_sm[D];
-    __shared__ __align__(16) float nbuf[2][DV];             // evictee N_e
-    __shared__ float zbuf[2], vvbuf[2];
-    __shared__ Best wb[kSelWarps];
-    __shared__ Best exch[2][kMaxCluster];
+    __shared__ __align__(16) float ebuf[kNEB][EW];   // evictee phi and v (float32), by step & 7
+    __shared__ __align__(16) T evraw[kNEB][DV];      // value row as stored (cp.async target)
+    __shared__ __align__(16) float wbuf[EW];         // winner phi/v copied from a peer CTA
+    __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
+    __shared__ __align__(16) float nbuf[2][DV];      // the current evictee's N
+    __shared__ float zbuf[2];
+    __shared__ uint2 wkey[kSelWarps + 1];            // per-warp minima; [16] = the evictee
+    __shared__ uint2 exch[2][kMaxCluster];
     __shared__ Dec dec[2];
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
@@ -159,86 +142,85 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
     float h[HR];
 #pragma unroll
     for (int r = 0; r < HR; ++r) h[r] = 0.f;
-    if (tid < D) s_sm[tid] = 0.f;
+    // warp 0: s and the pending evictee's z'
+    float s_reg[CD];
+#pragma unroll
+    for (int i = 0; i < CD; ++i) s_reg[i] = 0.f;
+    float zpend = 0.f;
 
     const float* phiK = a.phiK + (int64_t)bh * n * D;
     const int64_t vrow0 = (int64_t)bh * n;
     int32_t* wpos = a.wpos + (int64_t)bh * n;
     int32_t* wstep = a.wstep + (int64_t)bh * n;
-
     if (rank == 0)
-        for (int i = tid; i < n; i += kSelThreads) wstep[i] = -1;
+        for (int i = tid; i < n; i += kThreads) wstep[i] = -1;
 
-    // Evictee rows arrive by cp.async PF steps ahead: threads [0, D/4) copy phi(k_e),
-    // threads [D/4, D/4 + VCH) copy v_e; each step commits one group (possibly empty).
+    // Evictee rows of step `step` (e = step - eta, for step <= n) arrive by cp.async:
+    // threads [0, D/4) copy phi(k_e), threads [D/4, D/4 + VCH) copy v_e; one group per call.
     auto prefetch = [&](int step) {
         const int e = step - eta;
-        if (step < n && e >= 0) {
-            if (tid < D / 4) cp_async16(&ebuf[step & (NEB - 1)][4 * tid], phiK + (int64_t)e * D + 4 * tid);
-            else if (tid < D / 4 + VCH)
-                cp_async16(reinterpret_cast<char*>(evraw[step & (NEB - 1)]) + 16 * (tid - D / 4),
-                           reinterpret_cast<const char*>(static_cast<const T*>(a.V) + (vrow0 + e) * DV) +
-                               16 * (tid - D / 4));
+        if (step <= n && e >= 0) {
+            if (tid < D / 4) {
+                cp_async16(&ebuf[step & (kNEB - 1)][4 * tid], phiK + (int64_t)e * D + 4 * tid);
+            } else if (tid < D / 4 + VCH) {
+                const char* src = reinterpret_cast<const char*>(static_cast<const T*>(a.V) + (vrow0 + e) * DV);
+                cp_async16(reinterpret_cast<char*>(evraw[step & (kNEB - 1)]) + 16 * (tid - D / 4),
+                           src + 16 * (tid - D / 4));
+            }
         }
         cp_async_commit();
     };
-    // After this thread's copies for `step` have landed: widen its value chunk to float32.
+    // After this thread's own copies for `step` landed: widen its value chunk to float32.
     auto finish = [&](int step) {
-        if (step < n && step - eta >= 0 && tid >= D / 4 && tid < D / 4 + VCH) {
+        if (step <= n && step - eta >= 0 && tid >= D / 4 && tid < D / 4 + VCH) {
             constexpr int PER = 16 / (int)sizeof(T);
             const int c = tid - D / 4;
-            const T* src = &evraw[step & (NEB - 1)][c * PER];
-            float* dst = &ebuf[step & (NEB - 1)][D + c * PER];
+            const T* src = &evraw[step & (kNEB - 1)][c * PER];
+            float* dst = &ebuf[step & (kNEB - 1)][D + c * PER];
 #pragma unroll
             for (int i = 0; i < PER; ++i) dst[i] = IO<T>::ld(src, i);
         }
     };
-    for (int st = 0; st < PF; ++st) prefetch(st);
+    for (int st = 0; st < kPF; ++st) prefetch(st);
     cp_async_wait<0>();
     finish(0);
+    finish(1);
+    // the first evictee's partials are against the empty memory
+    for (int i = tid; i < NRG * DV; i += kThreads) red[0][0][i] = 0.f;
     int n_cached = 0, n_written = 0;
     __syncthreads();
 
-    // Applies the decision taken at step tp: the surviving evictee moves into its slot,
-    // then every live slot, H and s absorb the write.
-    auto apply = [&](int tp) {
-        const Dec dc = dec[tp & 1];
-        const float* wsrc = nullptr;
-        if (dc.write) {
-            if (dc.is_ev) {
-                wsrc = ebuf[tp & (NEB - 1)];
-            } else if (!CLUSTER || dc.cta == rank) {
-                wsrc = xbuf[tp & 1][dc.ws / kSPW];
-            } else {
-                if (tid < EW / 4) {
-                    const uint32_t src = map_rank(smem_addr(&xbuf[tp & 1][dc.ws / kSPW][4 * tid]), dc.cta);
-                    reinterpret_cast<float4*>(wbuf)[tid] = ld_cluster(src);
-                }
-                __syncthreads();
-                wsrc = wbuf;
-            }
+    // The written candidate's phi/v (step tp), possibly copied from a peer CTA.
+    auto winner_src = [&](int tp) -> const float* {
+        const Dec& dc = dec[tp & 1];
+        if (dc.is_ev) return ebuf[tp & (kNEB - 1)];
+        if (!CLUSTER || dc.cta == rank) return xbuf[tp & 1][dc.ws / kSPW];
+        if (tid < EW / 4) {
+            const uint32_t src = map_rank(smem_addr(&xbuf[tp & 1][dc.ws / kSPW][4 * tid]), dc.cta);
+            reinterpret_cast<float4*>(wbuf)[tid] = ld_cluster(src);
         }
+        __syncthreads();
+        return wbuf;
+    };
+
+    // Slots, H and s absorb the decision of step tp; the surviving evictee of step tp
+    // first moves into its slot (it absorbs the write like every other cached key).
+    auto apply = [&](int tp, const float* wsrc) {
+        const Dec dc = dec[tp & 1];
         if (dc.ev && !(dc.write && dc.is_ev)) {
             const int tcta = dc.write ? dc.cta : dc.fill % CL;
             const int tls = dc.write ? dc.ws : dc.fill / CL;
-            const bool mine = tcta == rank && tls == ls;
-            const float* eb = ebuf[tp & (NEB - 1)];
-            // ||v||^2 of the evictee with the slot's lane partition (the decode kernel's order)
-            float vv = 0.f;
+            const float* eb = ebuf[tp & (kNEB - 1)];
+            float tv[PV];
 #pragma unroll
-            for (int i = 0; i < PV; ++i) {
-                const float x = eb[D + slot_dim(sub, i)];
-                vv = fmaf(x, x, vv);
-            }
-            vv += __shfl_xor_sync(0xffffffffu, vv, 1);
-            vv += __shfl_xor_sync(0xffffffffu, vv, 2);
-            vv += __shfl_xor_sync(0xffffffffu, vv, 4);
-            if (mine) {
+            for (int i = 0; i < PV; ++i) tv[i] = eb[D + slot_dim(sub, i)];
+            const float vv = slot_vv<DV>(tv);
+            if (tcta == rank && tls == ls) {
 #pragma unroll
                 for (int i = 0; i < PD; ++i) sphi[i] = eb[slot_dim(sub, i)];
 #pragma unroll
                 for (int i = 0; i < PV; ++i) {
-                    sv[i] = eb[D + slot_dim(sub, i)];
+                    sv[i] = tv[i];
                     sN[i] = nbuf[tp & 1][slot_dim(sub, i)];
                 }
                 sz = zbuf[tp & 1];
@@ -247,26 +229,26 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
             }
         }
         if (dc.write) {
-            float g = 0.f;
-#pragma unroll
-            for (int i = 0; i < PD; ++i) g = fmaf(wsrc[slot_dim(sub, i)], sphi[i], g);
-            g += __shfl_xor_sync(0xffffffffu, g, 1);
-            g += __shfl_xor_sync(0xffffffffu, g, 2);
-            g += __shfl_xor_sync(0xffffffffu, g, 4);
+            const float g = slot_gram<D>(wsrc, sphi, sub);
             if (spos >= 0) {
-#pragma unroll
-                for (int i = 0; i < PV; ++i) sN[i] = fmaf(g, wsrc[D + slot_dim(sub, i)], sN[i]);
+                slot_axpy<DV>(sN, g, wsrc + D, sub);
                 sz += g;
             }
-            const float wvj = wsrc[D + hj];
+            h_update<D, DV>(h, wsrc, wsrc[D + hj], hrg);
+            if (warp == 0) {
 #pragma unroll
-            for (int r = 0; r < HR; ++r) h[r] = fmaf(wsrc[hrg + NRG * r], wvj, h[r]);
-            if (tid < D) s_sm[tid] += wsrc[tid];
+                for (int i = 0; i < CD; ++i) s_reg[i] += wsrc[lane * CD + i];
+            }
         }
     };
 
+    const float* wsrc_prev = nullptr;
     for (int t = 0; t < n; ++t) {
-        if (t > 0) apply(t - 1);
+        const bool prev_write = t > 0 && dec[(t - 1) & 1].write;
+        if (t > 0) {
+            wsrc_prev = prev_write ? winner_src(t - 1) : nullptr;
+            apply(t - 1, wsrc_prev);
+        }
 
         // chunk-start snapshot of the memory before step t
         if (t % a.chunk == 0) {
@@ -274,140 +256,116 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
             if (rank == 0) {
                 float* sh = a.snapH + ((int64_t)bh * a.nck + c) * D * DV;
 #pragma unroll
-                for (int r = 0; r < HR; ++r) sh[(hrg + NRG * r) * DV + hj] = h[r];
-                if (tid < D) a.snapS[((int64_t)bh * a.nck + c) * D + tid] = s_sm[tid];
+                for (int r = 0; r < HR; ++r) sh[(hrg * HR + r) * DV + hj] = h[r];
+                if (warp == 0) {
+#pragma unroll
+                    for (int i = 0; i < CD; ++i) a.snapS[((int64_t)bh * a.nck + c) * D + lane * CD + i] = s_reg[i];
+                }
             }
             if (sub == 0 && gslot < lam) a.snapC[((int64_t)bh * a.nck + c) * lam + gslot] = spos;
         }
 
-        // ---- score: evictee partial N_e, slot SREs, warp argmin ----
+        // ---- warp 0: finish the evictee of step t (N' from step t - 1, corrected) ----
         const bool ev = t >= eta;
-        const float* eb = ebuf[t & (NEB - 1)];
-        if (ev) {
-            float pj = 0.f;
+        if (warp == 0) {
+            uint32_t ehi = kNoKey, elo = kNoKey;
+            if (ev) {
+                const float* eb = ebuf[t & (kNEB - 1)];
+                float Ne[CV];
+                reduce_partials<D, DV>(&red[t & 1][0][0], lane, Ne);
+                float ze = zpend;
+                if (prev_write) {
+                    const float g = chunk_dot<D>(wsrc_prev, eb, lane);
+                    chunk_axpy<DV>(Ne, g, wsrc_prev + D, lane);
+                    ze += g;
+                }
+                float vve;
+                const float es = chunk_sre2<DV>(Ne, ze, eb + D, lane, &vve);
 #pragma unroll
-            for (int r = 0; r < HR; ++r) pj = fmaf(eb[hrg + NRG * r], h[r], pj);
-            red[hrg][hj] = pj;
+                for (int i = 0; i < CV; ++i) nbuf[t & 1][lane * CV + i] = Ne[i];
+                if (lane == 0) zbuf[t & 1] = ze;
+                ehi = key_hi(es);
+                elo = key_lo(t - eta, kEvCode);
+            }
+            // z' of the next evictee against s after the previous write
+            if (t + 1 - eta >= 0) zpend = chunk_dot_reg<D>(s_reg, ebuf[(t + 1) & (kNEB - 1)], lane);
+            if (lane == 0) wkey[kSelWarps] = make_uint2(ehi, elo);
         }
-        float ss = 0.f;
-#pragma unroll
-        for (int i = 0; i < PV; ++i) {
-            const float dlt = fmaf(-sz, sv[i], sN[i]);
-            ss = fmaf(dlt, dlt, ss);
-        }
-        ss += __shfl_xor_sync(0xffffffffu, ss, 1);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 2);
-        ss += __shfl_xor_sync(0xffffffffu, ss, 4);
-        float bs = spos < 0 ? INFINITY : (sz == 0.f ? svv : ss / (sz * sz));
-        int bp = spos < 0 ? INT_MAX : spos;
-        int bsl = sl;
-#pragma unroll
-        for (int o = kSG; o < kWarp; o <<= 1) {
-            const float os = __shfl_xor_sync(0xffffffffu, bs, o);
-            const int op = __shfl_xor_sync(0xffffffffu, bp, o);
-            const int osl = __shfl_xor_sync(0xffffffffu, bsl, o);
-            if (key_less(os, op, bs, bp)) { bs = os; bp = op; bsl = osl; }
-        }
-        if (lane == 0) wb[warp] = Best{bs, bp, warp * kSPW + bsl, 0};
-        if (sl == bsl && bp != INT_MAX) {
+
+        // ---- next evictee's partials; slot SREs; per-warp minimum ----
+        if (t + 1 - eta >= 0) red[(t + 1) & 1][hrg][hj] = h_partial<D, DV>(ebuf[(t + 1) & (kNEB - 1)], h, hrg);
+        const float sre = slot_sre2<DV>(sN, sz, sv, svv);
+        uint32_t khi = spos < 0 ? kNoKey : key_hi(sre);
+        uint32_t klo = spos < 0 ? kNoKey : key_lo(spos, ls);
+        const uint32_t mylo = klo;
+        warp_min_key(khi, klo);
+        if (lane == 0) wkey[warp] = make_uint2(khi, klo);
+        if (mylo == klo && klo != kNoKey) {
             float* xb = xbuf[t & 1][warp];
 #pragma unroll
-            for (int i = 0; i < PD; ++i) xb[slot_dim(sub, i)] = sphi[i];
+            for (int c = 0; c < PD / 4; ++c)
+                *reinterpret_cast<float4*>(xb + 32 * c + 4 * sub) =
+                    make_float4(sphi[4 * c], sphi[4 * c + 1], sphi[4 * c + 2], sphi[4 * c + 3]);
 #pragma unroll
-            for (int i = 0; i < PV; ++i) xb[D + slot_dim(sub, i)] = sv[i];
+            for (int c = 0; c < PV / 4; ++c)
+                *reinterpret_cast<float4*>(xb + D + 32 * c + 4 * sub) =
+                    make_float4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
         }
-        prefetch(t + PF);
+        prefetch(t + kPF);
         __syncthreads();
 
-        // ---- decide: evictee SRE, CTA argmin, cluster exchange ----
+        // ---- decide: CTA minimum, cluster exchange ----
         const bool write = ev && (n_cached + 1 > lam);
         if (warp == 0) {
-            float es = INFINITY;
-            if (ev) {
-                float Ne[DV / 32], ze = 0.f, sse = 0.f, vve = 0.f;
-#pragma unroll
-                for (int i = 0; i < DV / 32; ++i) {
-                    float acc = 0.f;
-#pragma unroll
-                    for (int r = 0; r < NRG; ++r) acc += red[r][lane + 32 * i];
-                    Ne[i] = acc;
-                    nbuf[t & 1][lane + 32 * i] = acc;
-                }
-#pragma unroll
-                for (int i = 0; i < D / 32; ++i) ze = fmaf(s_sm[lane + 32 * i], eb[lane + 32 * i], ze);
-                ze = warp_sum(ze);
-#pragma unroll
-                for (int i = 0; i < DV / 32; ++i) {
-                    const float v = eb[D + lane + 32 * i];
-                    const float dlt = fmaf(-ze, v, Ne[i]);
-                    sse = fmaf(dlt, dlt, sse);
-                    vve = fmaf(v, v, vve);
-                }
-                sse = warp_sum(sse);
-                vve = warp_sum(vve);
-                es = ze == 0.f ? vve : sse / (ze * ze);
-                if (lane == 0) { zbuf[t & 1] = ze; vvbuf[t & 1] = vve; }
-            }
-            Best b = lane < kSelWarps ? wb[lane] : Best{INFINITY, INT_MAX, -2, 0};
-            if (ev && lane == kSelWarps) b = Best{es, t - eta, -1, 0};
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                Best c;
-                c.sre2 = __shfl_xor_sync(0xffffffffu, b.sre2, o);
-                c.pos = __shfl_xor_sync(0xffffffffu, b.pos, o);
-                c.ws = __shfl_xor_sync(0xffffffffu, b.ws, o);
-                if (key_less(c.sre2, c.pos, b.sre2, b.pos)) b = c;
-            }
+            uint2 k = lane <= kSelWarps ? wkey[lane] : make_uint2(kNoKey, kNoKey);
+            warp_min_key(k.x, k.y);
             if constexpr (CLUSTER) {
-                if (lane < CL) st_cluster(map_rank(smem_addr(&exch[t & 1][rank]), lane), b);
+                if (lane < CL) st_cluster_u2(map_rank(smem_addr(&exch[t & 1][rank]), lane), k.x, k.y);
             } else if (lane == 0) {
-                exch[t & 1][0] = b;
+                exch[t & 1][0] = k;
             }
         }
         if constexpr (CLUSTER) cluster_barrier(); else __syncwarp();
         if (warp == 0) {
-            Best b = exch[t & 1][0];
+            uint2 k = exch[t & 1][0];
             int bc = 0;
             if constexpr (CLUSTER) {
-                b = lane < CL ? exch[t & 1][lane] : Best{INFINITY, INT_MAX, -2, 0};
-                bc = lane;
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    Best c;
-                    c.sre2 = __shfl_xor_sync(0xffffffffu, b.sre2, o);
-                    c.pos = __shfl_xor_sync(0xffffffffu, b.pos, o);
-                    c.ws = __shfl_xor_sync(0xffffffffu, b.ws, o);
-                    const int cc = __shfl_xor_sync(0xffffffffu, bc, o);
-                    if (key_less(c.sre2, c.pos, b.sre2, b.pos) || (c.sre2 == b.sre2 && c.pos == b.pos && cc < bc)) {
-                        b = c;
-                        bc = cc;
-                    }
-                }
+                k = lane < CL ? exch[t & 1][lane] : make_uint2(kNoKey, kNoKey);
+                // the owner CTA: lowest rank holding the minimum (the evictee is held by all)
+                uint32_t hi = k.x, lo = k.y;
+                warp_min_key(hi, lo);
+                const unsigned hold = __ballot_sync(kFull, lane < CL && k.x == hi && k.y == lo);
+                bc = __ffs(hold) - 1;
+                k = make_uint2(hi, lo);
             }
             if (lane == 0) {
+                const int code = (int)(k.y & 127u);
+                const int pos = (int)(k.y >> 7);
                 Dec d;
                 d.write = write;
-                d.is_ev = write && b.ws < 0;
-                d.pos = write ? b.pos : -1;
+                d.is_ev = write && code == kEvCode;
+                d.pos = write ? pos : -1;
                 d.cta = bc;
-                d.ws = b.ws;
+                d.ws = code;
                 d.ev = ev;
                 d.fill = n_cached;
                 d.pad = 0;
                 dec[t & 1] = d;
                 if (rank == 0) {
                     wpos[t] = d.pos;
-                    if (write) wstep[b.pos] = t;
+                    if (write) wstep[pos] = t;
                 }
             }
         }
-        cp_async_wait<PF - 1>();   // this thread's copies for step t + 1 have landed
-        finish(t + 1);
+        cp_async_wait<kPF - 2>();   // this thread's copies for step t + 2 have landed
+        finish(t + 2);
         __syncthreads();
         if (ev && !write) ++n_cached;
         if (write) ++n_written;
     }
-    if (n > 0) apply(n - 1);
+    const bool last_write = n > 0 && dec[(n - 1) & 1].write;
+    const float* wlast = last_write ? winner_src(n - 1) : nullptr;
+    apply(n - 1, wlast);
 
     // ---- export the memory after token n-1 into the state record ----
     char* rec = a.state + (int64_t)bh * a.L.head_bytes;
@@ -423,13 +381,33 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
         }
         float* Hs = reinterpret_cast<float*>(rec + a.L.H);
 #pragma unroll
-        for (int r = 0; r < HR; ++r) Hs[(hrg + NRG * r) * DV + hj] = h[r];
-        if (tid < D) reinterpret_cast<float*>(rec + a.L.s)[tid] = s_sm[tid];
+        for (int r = 0; r < HR; ++r) Hs[(hrg * HR + r) * DV + hj] = h[r];
+        if (warp == 0) {
+            float* sg = reinterpret_cast<float*>(rec + a.L.s);
+#pragma unroll
+            for (int i = 0; i < CD; ++i) sg[lane * CD + i] = s_reg[i];
+            // the next evictee (token n - eta): N against the memory after token n - 1
+            if (eta > 0 && n - eta >= 0) {
+                const float* eb = ebuf[n & (kNEB - 1)];
+                float Ne[CV];
+                reduce_partials<D, DV>(&red[n & 1][0][0], lane, Ne);
+                float ze = zpend;
+                if (last_write) {
+                    const float g = chunk_dot<D>(wlast, eb, lane);
+                    chunk_axpy<DV>(Ne, g, wlast + D, lane);
+                    ze += g;
+                }
+                float* evn = reinterpret_cast<float*>(rec + a.L.ev);
+#pragma unroll
+                for (int i = 0; i < CV; ++i) evn[lane * CV + i] = Ne[i];
+                if (lane == 0) evn[DV] = ze;
+            }
+        }
         // window ring: entry e holds the newest position p <= n-1 with p % eta == e
         int32_t* wp = reinterpret_cast<int32_t*>(rec + a.L.win_pos);
         T* wk = reinterpret_cast<T*>(rec + a.L.win_k);
         T* wv = reinterpret_cast<T*>(rec + a.L.win_v);
-        for (int i = tid; i < eta * (1 + D + DV); i += kSelThreads) {
+        for (int i = tid; i < eta * (1 + D + DV); i += kThreads) {
             const int e = i % eta, part = i / eta;
             const int p = (n - 1) - ((((n - 1) - e) % eta) + eta) % eta;
             if (part == 0) wp[e] = p >= 0 ? p : -1;
@@ -448,9 +426,9 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
             const int p = sp[g];
             cnt += (p >= 0 && p < spos) ? 1 : 0;
         }
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, 1);
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, 2);
-    cnt += __shfl_xor_sync(0xffffffffu, cnt, 4);
+    cnt += __shfl_xor_sync(kFull, cnt, 1);
+    cnt += __shfl_xor_sync(kFull, cnt, 2);
+    cnt += __shfl_xor_sync(kFull, cnt, 4);
     if (spos >= 0 && gslot < lam) {
         const int r = cnt;
         float* cphi = reinterpret_cast<float*>(rec + a.L.c_phi) + (int64_t)r * D;
@@ -469,11 +447,13 @@ __global__ void __launch_bounds__(kSelThreads, 1) select_kernel(const SelArgs a)
         }
     }
     if (rank == 0)
-        for (int r = n_cached + tid; r < lam; r += kSelThreads) reinterpret_cast<int32_t*>(rec + a.L.c_pos)[r] = -1;
+        for (int r = n_cached + tid; r < lam; r += kThreads) reinterpret_cast<int32_t*>(rec + a.L.c_pos)[r] = -1;
 }
 
 template <int D, int DV>
-constexpr size_t select_dyn_smem() { return sizeof(float) * 2 * kSelWarps * (D + DV); }
+constexpr size_t select_dyn_smem() {
+    return sizeof(float) * 2 * kSelWarps * (D + DV);
+}
 
 template <int D, int DV, typename T>
 cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t st) {
@@ -481,7 +461,7 @@ cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t s
     const size_t smem = select_dyn_smem<D, DV>();
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<d.BH, kSelThreads, smem, st>>>(a);
+    kern<<<d.BH, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -489,17 +469,15 @@ template <int D, int DV, typename T>
 cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t st) {
     auto kern = select_kernel<D, DV, true, T>;
     const size_t smem = select_dyn_smem<D, DV>();
-    {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     if (a.CL > 8) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(d.BH * a.CL);
-    cfg.blockDim = dim3(kSelThreads);
+    cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -510,7 +488,7 @@ cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t 
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int nclusters = 0;
-    cudaError_t e = cudaOccupancyMaxActiveClusters(&nclusters, (void*)kern, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&nclusters, (void*)kern, &cfg);
     if (e != cudaSuccess) return e;
     if (nclusters < 1) return cudaErrorInvalidConfiguration;
     return cudaLaunchKernelEx(&cfg, kern, a);
@@ -520,7 +498,7 @@ cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t 
 
 // Number of CTAs per head: enough register slots for lambda cache entries (64 per CTA).
 int select_cluster_size(int lam) {
-    int need = (lam + kSPC - 1) / kSPC;
+    const int need = (lam + kSPC - 1) / kSPC;
     int cl = 1;
     while (cl < need) cl <<= 1;
     return cl;
