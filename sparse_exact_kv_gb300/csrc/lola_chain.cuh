@@ -12,8 +12,8 @@
 //   slot role 8 lanes per cached candidate ("slot"); lane `sub` holds entries
 //             slot_dim(sub, i) of phi(k), v and N = H^T phi(k) (float4 chunks interleaved
 //             across the 8 lanes), and every lane holds the slot's z = s^T phi(k).
-//   chunk     warp 0 holds D/32 (or DV/32) consecutive entries per lane of s and of the
-//             evictee's N, for the evictee's SRE.
+//   evictee   8 lanes hold s and the evictee's phi, v and N in the slot layout, so the
+//             evictee is scored by exactly the arithmetic of a cached slot.
 // The evictee's N is computed one step ahead: N' = H^T phi(k_e) against the memory before
 // the previous write, then corrected by that write, N = N' + (phi_w . phi_e) v_w, exactly
 // like every cached slot absorbs a write.
@@ -36,8 +36,6 @@ struct Shape {
     static constexpr int HR = D / NRG;         // H rows per thread
     static constexpr int PD = D / kSG;         // phi entries per slot lane
     static constexpr int PV = DV / kSG;        // v / N entries per slot lane
-    static constexpr int CD = D / 32;          // chunk entries per lane (D vectors)
-    static constexpr int CV = DV / 32;         // chunk entries per lane (DV vectors)
     static_assert(kThreads % DV == 0 && D % NRG == 0 && HR % 4 == 0 && PD % 4 == 0 && PV % 4 == 0, "shape");
 };
 
@@ -58,16 +56,16 @@ template <int D, int DV>
 __device__ __forceinline__ float h_partial(const float* phi, const float* h, int hrg) {
     constexpr int HR = Shape<D, DV>::HR;
     const float4* p4 = reinterpret_cast<const float4*>(phi + hrg * HR);
-    float acc = 0.f;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int c = 0; c < HR / 4; ++c) {
         const float4 f = p4[c];
-        acc = fmaf(f.x, h[4 * c + 0], acc);
-        acc = fmaf(f.y, h[4 * c + 1], acc);
-        acc = fmaf(f.z, h[4 * c + 2], acc);
-        acc = fmaf(f.w, h[4 * c + 3], acc);
+        a0 = fmaf(f.x, h[4 * c + 0], a0);
+        a1 = fmaf(f.y, h[4 * c + 1], a1);
+        a2 = fmaf(f.z, h[4 * c + 2], a2);
+        a3 = fmaf(f.w, h[4 * c + 3], a3);
     }
-    return acc;
+    return (a0 + a1) + (a2 + a3);
 }
 
 template <int D, int DV>
@@ -84,76 +82,20 @@ __device__ __forceinline__ void h_update(float* h, const float* phi_w, float vj,
     }
 }
 
-// N'[j] = sum over row groups (in order) of the partials red[rg][j], j in lane's chunk
-template <int D, int DV>
-__device__ __forceinline__ void reduce_partials(const float* red, int lane, float* out) {
-    constexpr int NRG = Shape<D, DV>::NRG, CV = Shape<D, DV>::CV;
-#pragma unroll
-    for (int i = 0; i < CV; ++i) {
-        const int j = lane * CV + i;
-        float acc = red[j];
-#pragma unroll
-        for (int rg = 1; rg < NRG; ++rg) acc += red[rg * DV + j];
-        out[i] = acc;
-    }
-}
-
-// ---- chunk layout (one warp) ----
-// sum_k a[k] b[k] with a in registers (lane's chunk) and b in shared memory
-template <int N>
-__device__ __forceinline__ float chunk_dot_reg(const float* a_reg, const float* b, int lane) {
-    constexpr int C = N / 32;
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < C; ++i) acc = fmaf(a_reg[i], b[lane * C + i], acc);
-    return warp_sum(acc);
-}
-template <int N>
-__device__ __forceinline__ float chunk_dot(const float* a, const float* b, int lane) {
-    constexpr int C = N / 32;
-    float acc = 0.f;
-#pragma unroll
-    for (int i = 0; i < C; ++i) acc = fmaf(a[lane * C + i], b[lane * C + i], acc);
-    return warp_sum(acc);
-}
-// N += g v over the lane's chunk (v in shared memory)
-template <int DV>
-__device__ __forceinline__ void chunk_axpy(float* N, float g, const float* v, int lane) {
-    constexpr int C = DV / 32;
-#pragma unroll
-    for (int i = 0; i < C; ++i) N[i] = fmaf(g, v[lane * C + i], N[i]);
-}
-// SRE^2 of (N, z, v); *vv receives ||v||^2 (the empty-memory SRE^2)
-template <int DV>
-__device__ __forceinline__ float chunk_sre2(const float* N, float z, const float* v, int lane, float* vv) {
-    constexpr int C = DV / 32;
-    float sse = 0.f, v2 = 0.f;
-#pragma unroll
-    for (int i = 0; i < C; ++i) {
-        const float vi = v[lane * C + i];
-        const float dlt = fmaf(-z, vi, N[i]);
-        sse = fmaf(dlt, dlt, sse);
-        v2 = fmaf(vi, vi, v2);
-    }
-    sse = warp_sum(sse);
-    v2 = warp_sum(v2);
-    *vv = v2;
-    return z == 0.f ? v2 : sse / (z * z);
-}
-
 // ---- slot role (8 lanes per slot) ----
 template <int D>
 __device__ __forceinline__ float slot_gram(const float* wphi, const float* sphi, int sub) {
     constexpr int PD = D / kSG;
-    float g = 0.f;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
     for (int c = 0; c < PD / 4; ++c) {
         const float4 f = *reinterpret_cast<const float4*>(wphi + 32 * c + 4 * sub);
-        g = fmaf(f.x, sphi[4 * c + 0], g);
-        g = fmaf(f.y, sphi[4 * c + 1], g);
-        g = fmaf(f.z, sphi[4 * c + 2], g);
-        g = fmaf(f.w, sphi[4 * c + 3], g);
+        a0 = fmaf(f.x, sphi[4 * c + 0], a0);
+        a1 = fmaf(f.y, sphi[4 * c + 1], a1);
+        a2 = fmaf(f.z, sphi[4 * c + 2], a2);
+        a3 = fmaf(f.w, sphi[4 * c + 3], a3);
     }
+    float g = (a0 + a1) + (a2 + a3);
     g += __shfl_xor_sync(kFull, g, 1);
     g += __shfl_xor_sync(kFull, g, 2);
     g += __shfl_xor_sync(kFull, g, 4);
@@ -174,12 +116,13 @@ __device__ __forceinline__ void slot_axpy(float* sN, float g, const float* wv, i
 template <int DV>
 __device__ __forceinline__ float slot_sre2(const float* sN, float sz, const float* sv, float svv) {
     constexpr int PV = DV / kSG;
-    float ss = 0.f;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < PV; ++i) {
         const float dlt = fmaf(-sz, sv[i], sN[i]);
-        ss = fmaf(dlt, dlt, ss);
+        a[i & 3] = fmaf(dlt, dlt, a[i & 3]);
     }
+    float ss = (a[0] + a[1]) + (a[2] + a[3]);
     ss += __shfl_xor_sync(kFull, ss, 1);
     ss += __shfl_xor_sync(kFull, ss, 2);
     ss += __shfl_xor_sync(kFull, ss, 4);
@@ -188,13 +131,53 @@ __device__ __forceinline__ float slot_sre2(const float* sN, float sz, const floa
 template <int DV>
 __device__ __forceinline__ float slot_vv(const float* sv) {
     constexpr int PV = DV / kSG;
-    float vv = 0.f;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < PV; ++i) vv = fmaf(sv[i], sv[i], vv);
+    for (int i = 0; i < PV; ++i) a[i & 3] = fmaf(sv[i], sv[i], a[i & 3]);
+    float vv = (a[0] + a[1]) + (a[2] + a[3]);
     vv += __shfl_xor_sync(kFull, vv, 1);
     vv += __shfl_xor_sync(kFull, vv, 2);
     vv += __shfl_xor_sync(kFull, vv, 4);
     return vv;
+}
+// N' of the evictee in slot layout: the row-group partials red[rg][j] summed in order
+template <int D, int DV>
+__device__ __forceinline__ void slot_reduce_partials(const float* red, int sub, float* out) {
+    constexpr int NRG = Shape<D, DV>::NRG, PV = DV / kSG;
+#pragma unroll
+    for (int c = 0; c < PV / 4; ++c) {
+        float4 acc = *reinterpret_cast<const float4*>(red + 32 * c + 4 * sub);
+#pragma unroll
+        for (int rg = 1; rg < NRG; ++rg) {
+            const float4 f = *reinterpret_cast<const float4*>(red + rg * DV + 32 * c + 4 * sub);
+            acc.x += f.x;
+            acc.y += f.y;
+            acc.z += f.z;
+            acc.w += f.w;
+        }
+        out[4 * c + 0] = acc.x;
+        out[4 * c + 1] = acc.y;
+        out[4 * c + 2] = acc.z;
+        out[4 * c + 3] = acc.w;
+    }
+}
+// load a slot-layout slice of a shared-memory vector
+template <int N>
+__device__ __forceinline__ void slot_load(const float* v, int sub, float* out) {
+#pragma unroll
+    for (int c = 0; c < N / kSG / 4; ++c) {
+        const float4 f = *reinterpret_cast<const float4*>(v + 32 * c + 4 * sub);
+        out[4 * c + 0] = f.x;
+        out[4 * c + 1] = f.y;
+        out[4 * c + 2] = f.z;
+        out[4 * c + 3] = f.w;
+    }
+}
+template <int N>
+__device__ __forceinline__ void slot_store(float* v, int sub, const float* in) {
+#pragma unroll
+    for (int c = 0; c < N / kSG / 4; ++c)
+        *reinterpret_cast<float4*>(v + 32 * c + 4 * sub) = make_float4(in[4 * c], in[4 * c + 1], in[4 * c + 2], in[4 * c + 3]);
 }
 
 }  // namespace chain

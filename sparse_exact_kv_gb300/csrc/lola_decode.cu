@@ -44,7 +44,8 @@ template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     using S = Shape<D, DV>;
     constexpr int DK = D;
-    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, CD = S::CD, CV = S::CV;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
+    constexpr int kEvWarp = kDecWarps - 1;   // holds s and finishes the evictee (slot layout)
     extern __shared__ __align__(16) float sm[];
     float* Ws = sm;                              // [D/2][DK+1]
     float* xq = Ws + (D / 2) * (DK + 1);         // [DK]  query
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     float* wphi = phn + D;                       // [D]   written phi
     float* wv = wphi + D;                        // [DV]  written v
     float* red = wv + DV;                        // [NRG][DV]
-    float* Ne_s = red + NRG * DV;                // [DV]  evictee N (chunk layout, for the slot move)
+    float* Ne_s = red + NRG * DV;                // [DV]  evictee N (for the move into a slot)
     float* lin = Ne_s + DV;                      // [DV]  H^T phi(q)
     float* sc = lin + DV;                        // [eta + lam] scores, then weights
     uint2* wkey = reinterpret_cast<uint2*>(sc + a.eta + a.lam + (((a.eta + a.lam) & 1) ? 1 : 0));  // [16+1]
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     const bool nxt = eta > 0 && t + 1 - eta >= 0;   // the next step has an evictee known now
     const int nring = eta > 0 ? (t + 1) % eta : 0;
 
-    // ---- 1. loads: W, tokens, H (H role), s (warp 0 chunk) ----
+    // ---- 1. loads: W, tokens, H (H role), s (evictee warp) ----
     const float* Wh = a.W + (int64_t)h * a.w_head_stride;
     for (int i = tid; i < (D / 2) * DK; i += kThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
     if (tid < DK) {
@@ -112,11 +113,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     float hreg[HR];
 #pragma unroll
     for (int r = 0; r < HR; ++r) hreg[r] = Hg[(hrg * HR + r) * DV + hj];
-    float s_reg[CD];
-    if (warp == 0) {
+    const int sl = tid / kSG, sub = tid % kSG;
+    float s_reg[PD];                                      // s, held by the evictee warp
 #pragma unroll
-        for (int i = 0; i < CD; ++i) s_reg[i] = sg[lane * CD + i];
-    }
+    for (int i = 0; i < PD; ++i) s_reg[i] = 0.f;
+    if (warp == kEvWarp) slot_load<D>(sg, sub, s_reg);
     __syncthreads();
     if (ev && eta > 0 && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
 
@@ -146,36 +147,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     if (want_partials) red[hrg * DV + hj] = h_partial<D, DV>(pvec, hreg, hrg);
     __syncthreads();
 
-    // ---- 4. the evictee's N, z and SRE (warp 0); the next evictee's N', z' ----
-    float Nn[CV], zn = 0.f;
-    if (warp == 0) {
+    // ---- 4. the evictee's N, z and SRE; the next evictee's N', z' (evictee warp) ----
+    float Nn[PV], zn = 0.f;
+#pragma unroll
+    for (int i = 0; i < PV; ++i) Nn[i] = 0.f;
+    if (warp == kEvWarp) {
         uint32_t ehi = kNoKey, elo = kNoKey;
         if (ev) {
-            float Ne[CV], ze;
+            float Ne[PV], ve[PV], ze;
             if (eta > 0) {
-#pragma unroll
-                for (int i = 0; i < CV; ++i) Ne[i] = evs[lane * CV + i];
+                slot_load<DV>(evs, sub, Ne);
                 ze = evs[DV];
             } else {
-                reduce_partials<D, DV>(red, lane, Ne);
-                ze = chunk_dot_reg<D>(s_reg, phe, lane);
+                slot_reduce_partials<D, DV>(red, sub, Ne);
+                ze = slot_gram<D>(phe, s_reg, sub);
             }
-            float vve;
-            const float es = chunk_sre2<DV>(Ne, ze, evv, lane, &vve);
-#pragma unroll
-            for (int i = 0; i < CV; ++i) Ne_s[lane * CV + i] = Ne[i];
+            slot_load<DV>(evv, sub, ve);
+            const float es = slot_sre2<DV>(Ne, ze, ve, slot_vv<DV>(ve));
+            if (lane < kSG) slot_store<DV>(Ne_s, sub, Ne);
             if (lane == 0) misc[0] = ze;
             ehi = key_hi(es);
             elo = key_lo(e, kEvCode);
         }
         if (lane == 0) wkey[kDecWarps] = make_uint2(ehi, elo);
         if (nxt) {
-            reduce_partials<D, DV>(red, lane, Nn);
-            zn = chunk_dot_reg<D>(s_reg, phn, lane);
+            slot_reduce_partials<D, DV>(red, sub, Nn);
+            zn = slot_gram<D>(phn, s_reg, sub);
         }
     }
     // slot SREs, pass by pass; each warp keeps its minimum over all passes
-    const int sl = tid / kSG, sub = tid % kSG;
     uint32_t bhi = kNoKey, blo = kNoKey;
     for (int base = 0; base < nc; base += kSlotsPerPass) {
         const int i = base + sl;
@@ -234,9 +234,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         if (tid < DV) wv[tid] = wsel < 0 ? evv[tid] : IO<T>::ld(cv, (int64_t)wsel * DV + tid);
         __syncthreads();
         h_update<D, DV>(hreg, wphi, wv[hj], hrg);
-        if (warp == 0) {
+        if (warp == kEvWarp) {
+            float wp[PD];
+            slot_load<D>(wphi, sub, wp);
 #pragma unroll
-            for (int i = 0; i < CD; ++i) s_reg[i] += wphi[lane * CD + i];
+            for (int i = 0; i < PD; ++i) s_reg[i] += wp[i];
         }
         for (int base = 0; base < nc; base += kSlotsPerPass) {
             const int i = base + sl;
@@ -262,9 +264,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
                 if (sub == 0) cz[i] = (moved ? ze : cz[i]) + g;
             }
         }
-        if (warp == 0 && nxt) {
-            const float g = chunk_dot<D>(wphi, phn, lane);
-            chunk_axpy<DV>(Nn, g, wv, lane);
+        if (warp == kEvWarp && nxt) {
+            float ph[PD];
+            slot_load<D>(phn, sub, ph);
+            const float g = slot_gram<D>(wphi, ph, sub);
+            slot_axpy<DV>(Nn, g, wv, sub);
             zn += g;
         }
     }
@@ -283,9 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         if (tid < DV) IO<T>::st(cv, (int64_t)slot_new * DV + tid, evv[tid]);
         if (tid == 0) cpos[slot_new] = e;
     }
-    if (warp == 0 && nxt) {
-#pragma unroll
-        for (int i = 0; i < CV; ++i) evs[lane * CV + i] = Nn[i];
+    if (warp == kEvWarp && nxt) {
+        if (lane < kSG) slot_store<DV>(evs, sub, Nn);
         if (lane == 0) evs[DV] = zn;
     }
     // the new token enters the window ring (its previous occupant was the evictee)
@@ -329,12 +332,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
             l += p;
         }
         l = warp_sum(l);
-        const float dl = chunk_dot_reg<D>(s_reg, phq, lane);
         if (lane == 0) {
             const bool any = nkeys > 0;
             misc[1] = any ? expf(-m) : 1.f;
-            misc[2] = any ? fmaf(misc[1], dl, l) : dl;
+            misc[3] = l;
         }
+    } else if (warp == kEvWarp) {
+        const float dl = slot_gram<D>(phq, s_reg, sub);
+        if (lane == 0) misc[4] = dl;
     } else if (warp == 1 && tid - 32 < DV / 4) {
         // H^T phi(q): sum the row-group partials
         const int j0 = 4 * (tid - 32);
@@ -361,17 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
 #pragma unroll
             for (int r = 0; r < NRG; ++r) num += red[r * DV + tid];
             num = fmaf(misc[1], lin[tid], num);
-            IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / misc[2]);
+            const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
+            IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
         }
     }
 
     // ---- 8. write back H, s, header ----
 #pragma unroll
     for (int r = 0; r < HR; ++r) Hg[(hrg * HR + r) * DV + hj] = hreg[r];
-    if (warp == 0) {
-#pragma unroll
-        for (int i = 0; i < CD; ++i) sg[lane * CD + i] = s_reg[i];
-    }
+    if (warp == kEvWarp && lane < kSG) slot_store<D>(sg, sub, s_reg);
     if (tid == 0) {
         hdr[HDR_T] = t + 1;
         hdr[HDR_NCACHE] = nc_after;

@@ -13,13 +13,15 @@
 //     write w costs each slot g = phi_w . phi_i, N += g v_w, z += g (exact: H changes by
 //     a rank-1 term);
 //   * each CTA holds a replica of H in registers (32 or 8 entries per thread) to compute
-//     the next evictee's H^T phi one step ahead and to emit the chunk snapshots; warp 0
-//     holds s and finishes the evictee (correction by the last write, SRE);
+//     the next evictee's H^T phi one step ahead and to emit the chunk snapshots; the last
+//     warp holds s and finishes the evictee (correction by the last write, SRE) with the
+//     arithmetic of a slot;
 //   * per step: apply the previous write; every warp scores its slots and takes its
-//     packed-key minimum with two redux.sync; warp 0 takes the CTA minimum after one
-//     barrier; with CL > 1 each CTA pushes its best to every peer's shared memory
-//     (st.shared::cluster) and one cluster barrier orders the exchange, and the winner's
-//     phi/v are read back through DSMEM;
+//     packed-key minimum with two redux.sync; after the step's single barrier every warp
+//     takes the CTA minimum itself and keeps the decision in registers; with CL > 1 warp 0
+//     pushes the CTA's best to every peer's shared memory (st.shared::cluster) and one
+//     cluster barrier orders the exchange, and the winner's phi/v are read back through
+//     DSMEM;
 //   * evictee rows (phi(k_e), v_e) arrive by cp.async four steps ahead.
 // At every chunk start it stores H, s and the cache positions, from which the parallel
 // output kernel rebuilds every query's exact set and linear state.
@@ -52,17 +54,6 @@ struct SelArgs {
     int32_t* slotpos;    // [BH][lam]
     char* state;
     Layout L;
-};
-
-struct Dec {
-    int write;   // a candidate was written this step
-    int is_ev;   // ... and it was the evictee
-    int pos;     // written position
-    int cta;     // owner CTA of the written slot
-    int ws;      // local slot index of the written slot
-    int ev;      // an evictee joined the candidates this step
-    int fill;    // global slot the evictee fills when nothing was written
-    int pad;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -104,9 +95,10 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int D, int DV, bool CLUSTER, typename T>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     using S = Shape<D, DV>;
-    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, CD = S::CD, CV = S::CV;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
     constexpr int EW = D + DV;
     constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
+    constexpr int kEvWarp = kSelWarps - 1;         // finishes the evictee and holds s
 
     extern __shared__ __align__(16) float dyn_sm[];
     float (*xbuf)[kSelWarps][EW] = reinterpret_cast<float (*)[kSelWarps][EW]>(dyn_sm);  // [2] warp-best phi/v
@@ -116,9 +108,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
     __shared__ __align__(16) float nbuf[2][DV];      // the current evictee's N
     __shared__ float zbuf[2];
-    __shared__ uint2 wkey[kSelWarps + 1];            // per-warp minima; [16] = the evictee
+    __shared__ uint2 wkey[2][kSelWarps + 1];         // per-warp minima; [16] = the evictee
     __shared__ uint2 exch[2][kMaxCluster];
-    __shared__ Dec dec[2];
+    __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int rank = CLUSTER ? (int)cluster_rank() : 0;
@@ -142,11 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     float h[HR];
 #pragma unroll
     for (int r = 0; r < HR; ++r) h[r] = 0.f;
-    // warp 0: s and the pending evictee's z'
-    float s_reg[CD];
-#pragma unroll
-    for (int i = 0; i < CD; ++i) s_reg[i] = 0.f;
+    // evictee warp: the pending evictee's z'
     float zpend = 0.f;
+    if (tid < D) s_sm[tid] = 0.f;
 
     const float* phiK = a.phiK + (int64_t)bh * n * D;
     const int64_t vrow0 = (int64_t)bh * n;
@@ -190,13 +180,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     int n_cached = 0, n_written = 0;
     __syncthreads();
 
+    // the decision of the previous step, held by every thread
+    int d_write = 0, d_isev = 0, d_cta = 0, d_ws = 0, d_ev = 0, d_fill = 0;
+
     // The written candidate's phi/v (step tp), possibly copied from a peer CTA.
     auto winner_src = [&](int tp) -> const float* {
-        const Dec& dc = dec[tp & 1];
-        if (dc.is_ev) return ebuf[tp & (kNEB - 1)];
-        if (!CLUSTER || dc.cta == rank) return xbuf[tp & 1][dc.ws / kSPW];
+        if (d_isev) return ebuf[tp & (kNEB - 1)];
+        if (!CLUSTER || d_cta == rank) return xbuf[tp & 1][d_ws / kSPW];
         if (tid < EW / 4) {
-            const uint32_t src = map_rank(smem_addr(&xbuf[tp & 1][dc.ws / kSPW][4 * tid]), dc.cta);
+            const uint32_t src = map_rank(smem_addr(&xbuf[tp & 1][d_ws / kSPW][4 * tid]), d_cta);
             reinterpret_cast<float4*>(wbuf)[tid] = ld_cluster(src);
         }
         __syncthreads();
@@ -206,45 +198,47 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     // Slots, H and s absorb the decision of step tp; the surviving evictee of step tp
     // first moves into its slot (it absorbs the write like every other cached key).
     auto apply = [&](int tp, const float* wsrc) {
-        const Dec dc = dec[tp & 1];
-        if (dc.ev && !(dc.write && dc.is_ev)) {
-            const int tcta = dc.write ? dc.cta : dc.fill % CL;
-            const int tls = dc.write ? dc.ws : dc.fill / CL;
+        if (d_ev && !(d_write && d_isev)) {
+            const int tcta = d_write ? d_cta : d_fill % CL;
+            const int tls = d_write ? d_ws : d_fill / CL;
             const float* eb = ebuf[tp & (kNEB - 1)];
             float tv[PV];
-#pragma unroll
-            for (int i = 0; i < PV; ++i) tv[i] = eb[D + slot_dim(sub, i)];
+            slot_load<DV>(eb + D, sub, tv);
             const float vv = slot_vv<DV>(tv);
             if (tcta == rank && tls == ls) {
+                slot_load<D>(eb, sub, sphi);
+                slot_load<DV>(nbuf[tp & 1], sub, sN);
 #pragma unroll
-                for (int i = 0; i < PD; ++i) sphi[i] = eb[slot_dim(sub, i)];
-#pragma unroll
-                for (int i = 0; i < PV; ++i) {
-                    sv[i] = tv[i];
-                    sN[i] = nbuf[tp & 1][slot_dim(sub, i)];
-                }
+                for (int i = 0; i < PV; ++i) sv[i] = tv[i];
                 sz = zbuf[tp & 1];
                 svv = vv;
                 spos = tp - eta;
             }
         }
-        if (dc.write) {
+        if (d_write) {
             const float g = slot_gram<D>(wsrc, sphi, sub);
             if (spos >= 0) {
                 slot_axpy<DV>(sN, g, wsrc + D, sub);
                 sz += g;
             }
             h_update<D, DV>(h, wsrc, wsrc[D + hj], hrg);
-            if (warp == 0) {
+            if (warp == kEvWarp) {
+                if (lane < kSG) {
+                    float wp[PD], sr[PD];
+                    slot_load<D>(wsrc, sub, wp);
+                    slot_load<D>(s_sm, sub, sr);
 #pragma unroll
-                for (int i = 0; i < CD; ++i) s_reg[i] += wsrc[lane * CD + i];
+                    for (int i = 0; i < PD; ++i) sr[i] += wp[i];
+                    slot_store<D>(s_sm, sub, sr);
+                }
+                __syncwarp();
             }
         }
     };
 
     const float* wsrc_prev = nullptr;
     for (int t = 0; t < n; ++t) {
-        const bool prev_write = t > 0 && dec[(t - 1) & 1].write;
+        const bool prev_write = d_write;
         if (t > 0) {
             wsrc_prev = prev_write ? winner_src(t - 1) : nullptr;
             apply(t - 1, wsrc_prev);
@@ -257,39 +251,45 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
                 float* sh = a.snapH + ((int64_t)bh * a.nck + c) * D * DV;
 #pragma unroll
                 for (int r = 0; r < HR; ++r) sh[(hrg * HR + r) * DV + hj] = h[r];
-                if (warp == 0) {
-#pragma unroll
-                    for (int i = 0; i < CD; ++i) a.snapS[((int64_t)bh * a.nck + c) * D + lane * CD + i] = s_reg[i];
+                if (warp == kEvWarp && lane < kSG) {
+                    float sr[PD];
+                    slot_load<D>(s_sm, sub, sr);
+                    slot_store<D>(a.snapS + ((int64_t)bh * a.nck + c) * D, sub, sr);
                 }
             }
             if (sub == 0 && gslot < lam) a.snapC[((int64_t)bh * a.nck + c) * lam + gslot] = spos;
         }
 
-        // ---- warp 0: finish the evictee of step t (N' from step t - 1, corrected) ----
+        // ---- evictee warp: finish the evictee of step t (N' from step t - 1, corrected
+        //      by the previous write) and prepare the next one's z' ----
         const bool ev = t >= eta;
-        if (warp == 0) {
+        if (warp == kEvWarp) {
             uint32_t ehi = kNoKey, elo = kNoKey;
             if (ev) {
                 const float* eb = ebuf[t & (kNEB - 1)];
-                float Ne[CV];
-                reduce_partials<D, DV>(&red[t & 1][0][0], lane, Ne);
+                float Ne[PV], ve[PV];
+                slot_reduce_partials<D, DV>(&red[t & 1][0][0], sub, Ne);
                 float ze = zpend;
                 if (prev_write) {
-                    const float g = chunk_dot<D>(wsrc_prev, eb, lane);
-                    chunk_axpy<DV>(Ne, g, wsrc_prev + D, lane);
+                    float ph[PD];
+                    slot_load<D>(eb, sub, ph);
+                    const float g = slot_gram<D>(wsrc_prev, ph, sub);
+                    slot_axpy<DV>(Ne, g, wsrc_prev + D, sub);
                     ze += g;
                 }
-                float vve;
-                const float es = chunk_sre2<DV>(Ne, ze, eb + D, lane, &vve);
-#pragma unroll
-                for (int i = 0; i < CV; ++i) nbuf[t & 1][lane * CV + i] = Ne[i];
+                slot_load<DV>(eb + D, sub, ve);
+                const float es = slot_sre2<DV>(Ne, ze, ve, slot_vv<DV>(ve));
+                if (lane < kSG) slot_store<DV>(nbuf[t & 1], sub, Ne);
                 if (lane == 0) zbuf[t & 1] = ze;
                 ehi = key_hi(es);
                 elo = key_lo(t - eta, kEvCode);
             }
-            // z' of the next evictee against s after the previous write
-            if (t + 1 - eta >= 0) zpend = chunk_dot_reg<D>(s_reg, ebuf[(t + 1) & (kNEB - 1)], lane);
-            if (lane == 0) wkey[kSelWarps] = make_uint2(ehi, elo);
+            if (t + 1 - eta >= 0) {
+                float sr[PD];
+                slot_load<D>(s_sm, sub, sr);
+                zpend = slot_gram<D>(ebuf[(t + 1) & (kNEB - 1)], sr, sub);
+            }
+            if (lane == 0) wkey[t & 1][kSelWarps] = make_uint2(ehi, elo);
         }
 
         // ---- next evictee's partials; slot SREs; per-warp minimum ----
@@ -299,71 +299,49 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         uint32_t klo = spos < 0 ? kNoKey : key_lo(spos, ls);
         const uint32_t mylo = klo;
         warp_min_key(khi, klo);
-        if (lane == 0) wkey[warp] = make_uint2(khi, klo);
+        if (lane == 0) wkey[t & 1][warp] = make_uint2(khi, klo);
         if (mylo == klo && klo != kNoKey) {
             float* xb = xbuf[t & 1][warp];
-#pragma unroll
-            for (int c = 0; c < PD / 4; ++c)
-                *reinterpret_cast<float4*>(xb + 32 * c + 4 * sub) =
-                    make_float4(sphi[4 * c], sphi[4 * c + 1], sphi[4 * c + 2], sphi[4 * c + 3]);
-#pragma unroll
-            for (int c = 0; c < PV / 4; ++c)
-                *reinterpret_cast<float4*>(xb + D + 32 * c + 4 * sub) =
-                    make_float4(sv[4 * c], sv[4 * c + 1], sv[4 * c + 2], sv[4 * c + 3]);
+            slot_store<D>(xb, sub, sphi);
+            slot_store<DV>(xb + D, sub, sv);
         }
         prefetch(t + kPF);
-        __syncthreads();
-
-        // ---- decide: CTA minimum, cluster exchange ----
-        const bool write = ev && (n_cached + 1 > lam);
-        if (warp == 0) {
-            uint2 k = lane <= kSelWarps ? wkey[lane] : make_uint2(kNoKey, kNoKey);
-            warp_min_key(k.x, k.y);
-            if constexpr (CLUSTER) {
-                if (lane < CL) st_cluster_u2(map_rank(smem_addr(&exch[t & 1][rank]), lane), k.x, k.y);
-            } else if (lane == 0) {
-                exch[t & 1][0] = k;
-            }
-        }
-        if constexpr (CLUSTER) cluster_barrier(); else __syncwarp();
-        if (warp == 0) {
-            uint2 k = exch[t & 1][0];
-            int bc = 0;
-            if constexpr (CLUSTER) {
-                k = lane < CL ? exch[t & 1][lane] : make_uint2(kNoKey, kNoKey);
-                // the owner CTA: lowest rank holding the minimum (the evictee is held by all)
-                uint32_t hi = k.x, lo = k.y;
-                warp_min_key(hi, lo);
-                const unsigned hold = __ballot_sync(kFull, lane < CL && k.x == hi && k.y == lo);
-                bc = __ffs(hold) - 1;
-                k = make_uint2(hi, lo);
-            }
-            if (lane == 0) {
-                const int code = (int)(k.y & 127u);
-                const int pos = (int)(k.y >> 7);
-                Dec d;
-                d.write = write;
-                d.is_ev = write && code == kEvCode;
-                d.pos = write ? pos : -1;
-                d.cta = bc;
-                d.ws = code;
-                d.ev = ev;
-                d.fill = n_cached;
-                d.pad = 0;
-                dec[t & 1] = d;
-                if (rank == 0) {
-                    wpos[t] = d.pos;
-                    if (write) wstep[pos] = t;
-                }
-            }
-        }
         cp_async_wait<kPF - 2>();   // this thread's copies for step t + 2 have landed
         finish(t + 2);
         __syncthreads();
+
+        // ---- decide (every warp): CTA minimum, then the cluster exchange ----
+        const bool write = ev && (n_cached + 1 > lam);
+        uint2 k = lane <= kSelWarps ? wkey[t & 1][lane] : make_uint2(kNoKey, kNoKey);
+        warp_min_key(k.x, k.y);
+        int bc = 0;
+        if constexpr (CLUSTER) {
+            if (warp == 0 && lane < CL) st_cluster_u2(map_rank(smem_addr(&exch[t & 1][rank]), lane), k.x, k.y);
+            cluster_barrier();
+            uint2 c = lane < CL ? exch[t & 1][lane] : make_uint2(kNoKey, kNoKey);
+            uint32_t hi = c.x, lo = c.y;
+            warp_min_key(hi, lo);
+            // the owner CTA: lowest rank holding the minimum (the evictee is held by all)
+            const unsigned hold = __ballot_sync(kFull, lane < CL && c.x == hi && c.y == lo);
+            bc = __ffs(hold) - 1;
+            k = make_uint2(hi, lo);
+        }
+        const int code = (int)(k.y & 127u);
+        const int pos = (int)(k.y >> 7);
+        d_write = write;
+        d_isev = write && code == kEvCode;
+        d_cta = bc;
+        d_ws = code;
+        d_ev = ev;
+        d_fill = n_cached;
+        if (rank == 0 && tid == 0) {
+            wpos[t] = write ? pos : -1;
+            if (write) wstep[pos] = t;
+        }
         if (ev && !write) ++n_cached;
         if (write) ++n_written;
     }
-    const bool last_write = n > 0 && dec[(n - 1) & 1].write;
+    const bool last_write = d_write;
     const float* wlast = last_write ? winner_src(n - 1) : nullptr;
     apply(n - 1, wlast);
 
@@ -382,24 +360,27 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         float* Hs = reinterpret_cast<float*>(rec + a.L.H);
 #pragma unroll
         for (int r = 0; r < HR; ++r) Hs[(hrg * HR + r) * DV + hj] = h[r];
-        if (warp == 0) {
-            float* sg = reinterpret_cast<float*>(rec + a.L.s);
-#pragma unroll
-            for (int i = 0; i < CD; ++i) sg[lane * CD + i] = s_reg[i];
+        if (warp == kEvWarp) {
+            if (lane < kSG) {
+                float sr[PD];
+                slot_load<D>(s_sm, sub, sr);
+                slot_store<D>(reinterpret_cast<float*>(rec + a.L.s), sub, sr);
+            }
             // the next evictee (token n - eta): N against the memory after token n - 1
             if (eta > 0 && n - eta >= 0) {
                 const float* eb = ebuf[n & (kNEB - 1)];
-                float Ne[CV];
-                reduce_partials<D, DV>(&red[n & 1][0][0], lane, Ne);
+                float Ne[PV];
+                slot_reduce_partials<D, DV>(&red[n & 1][0][0], sub, Ne);
                 float ze = zpend;
                 if (last_write) {
-                    const float g = chunk_dot<D>(wlast, eb, lane);
-                    chunk_axpy<DV>(Ne, g, wlast + D, lane);
+                    float ph[PD];
+                    slot_load<D>(eb, sub, ph);
+                    const float g = slot_gram<D>(wlast, ph, sub);
+                    slot_axpy<DV>(Ne, g, wlast + D, sub);
                     ze += g;
                 }
                 float* evn = reinterpret_cast<float*>(rec + a.L.ev);
-#pragma unroll
-                for (int i = 0; i < CV; ++i) evn[lane * CV + i] = Ne[i];
+                if (lane < kSG) slot_store<DV>(evn, sub, Ne);
                 if (lane == 0) evn[DV] = ze;
             }
         }
