@@ -112,7 +112,8 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
     char* p = static_cast<char*>(base);
     int64_t o = 0;
     const int64_t BH = d.BH;
-    w.nck = (n + d.chunk - 1) / d.chunk;
+    w.snap_interval = d.chunk < 128 ? 128 : d.chunk;
+    w.nck = (n + w.snap_interval - 1) / w.snap_interval;
     auto take = [&](int64_t bytes) {
         char* r = p ? p + o : nullptr;
         o = align256(o + bytes);
@@ -120,6 +121,9 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
     };
     w.phiK = reinterpret_cast<float*>(take(4 * BH * n * d.D));
     w.phiQ = reinterpret_cast<float*>(take(4 * BH * n * d.D));
+    const bool tc = output_tc_supported(d);
+    w.phiKb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * n * d.D) : nullptr);
+    w.phiQb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * n * d.D) : nullptr);
     w.wstep = reinterpret_cast<int32_t*>(take(4 * BH * n));
     w.wpos = reinterpret_cast<int32_t*>(take(4 * BH * n));
     w.snapH = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D * d.dv));
@@ -230,14 +234,20 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = launch_state_init(d, static_cast<char*>(state), L, st);
     if (e != cudaSuccess) return cuda_fail(e, "state init");
-    e = traced(LOLA_KERNEL_PHI, st, [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, st); });
+    e = traced(LOLA_KERNEL_PHI, st,
+               [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, ws.phiKb, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(K)");
-    e = traced(LOLA_KERNEL_PHI, st, [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, st); });
+    e = traced(LOLA_KERNEL_PHI, st,
+               [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
     e = traced(LOLA_KERNEL_SELECT, st,
                [&]() { return launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st); });
     if (e != cudaSuccess) return cuda_fail(e, "selection");
-    e = traced(LOLA_KERNEL_OUTPUT, st, [&]() { return launch_output(d, n, ws, Q, K, V, Y, st); });
+    e = traced(LOLA_KERNEL_OUTPUT, st, [&]() {
+        return output_tc_supported(d)
+                   ? launch_output_tc(d, n, ws, Q, K, V, Y, static_cast<char*>(state), L.head_bytes, st)
+                   : launch_output(d, n, ws, Q, K, V, Y, st);
+    });
     if (e != cudaSuccess) return cuda_fail(e, "output");
     return LOLA_OK;
 }

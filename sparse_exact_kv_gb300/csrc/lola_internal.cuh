@@ -50,7 +50,7 @@ inline Layout make_layout(const Dims& d) {
 enum { HDR_T = 0, HDR_NCACHE = 1, HDR_NWRITTEN = 2, HDR_STATUS = 3, HDR_WORDS = 16 };
 
 // device-side status bits
-enum : int32_t { ST_SLOT_OVERFLOW = 1, ST_BAD_STATE = 2 };
+enum : int32_t { ST_SLOT_OVERFLOW = 1, ST_BAD_STATE = 2, ST_TIMEOUT = 4 };
 
 // ---------------------------------------------------------------------------------
 // Prefill workspace: per-head arrays used between the kernels
@@ -58,12 +58,15 @@ enum : int32_t { ST_SLOT_OVERFLOW = 1, ST_BAD_STATE = 2 };
 struct Workspace {
     float* phiK;       // [BH][n][D]    phi(k_t), float32 (selection precision)
     float* phiQ;       // [BH][n][D]    phi(q_t)
+    __nv_bfloat16* phiKb;  // [BH][n][D] bf16 copies for the tensor-core output kernel (bf16 mode)
+    __nv_bfloat16* phiQb;
     int32_t* wstep;    // [BH][n]       step at which token j was written, -1 never
     int32_t* wpos;     // [BH][n]       position written at step t, -1 none
     float* snapH;      // [BH][nck][D*dv]  H before the first step of each chunk
     float* snapS;      // [BH][nck][D]
     int32_t* snapC;    // [BH][nck][lam]   cache slot positions before each chunk (-1 empty)
     int32_t* slotpos;  // [BH][lam]        final slot positions (export scratch)
+    int snap_interval;  // steps between snapshots: max(C, 128), one tensor-core query tile
     int nck;
     size_t bytes;
 };
@@ -148,11 +151,14 @@ __device__ __forceinline__ void phi_warp(const float* xs, const float* Ws, int l
 // Launchers (each returns the launch's cudaError_t)
 // ---------------------------------------------------------------------------------
 cudaError_t launch_phi(const Dims& d, int n, const void* X, const float* W, int64_t w_head_stride,
-                       float* out, cudaStream_t st);
+                       float* out, __nv_bfloat16* out_bf16, cudaStream_t st);
 cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
                           char* state, const Layout& L, cudaStream_t st);
 cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                           const void* V, void* Y, cudaStream_t st);
+bool output_tc_supported(const Dims& d);
+cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
+                             const void* V, void* Y, char* state, int64_t head_bytes, cudaStream_t st);
 cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W,
                           int64_t w_head_stride, const void* q, const void* k, const void* v, void* y,
                           int32_t* written_pos, cudaStream_t st);

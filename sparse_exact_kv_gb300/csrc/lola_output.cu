@@ -238,7 +238,7 @@ cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void*
     a.n = n;
     a.eta = d.eta;
     a.lam = d.lam;
-    a.chunk = d.chunk;
+    a.chunk = ws.snap_interval;
     a.nck = ws.nck;
     a.Q = Q;
     a.K = K;

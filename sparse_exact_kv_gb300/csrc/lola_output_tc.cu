@@ -1,0 +1,368 @@
+// K3 (bf16, tensor cores): co-normalised LoLA output for every query, in parallel over
+// (head, 128-query tile), with tcgen05 MMAs accumulating in TMEM.
+//
+// LoLA reading notes (arXiv 2505.23666v3), section 2.5, Eq. 14:
+//   y_t = (H_t^T phi(q_t) + sum_{j in G_t ∪ W_t} a_tj v_j) / (phi(q_t)^T s_t + sum a_tj),
+//   a_tj = exp(q_t . k_j / sqrt(d_k)).
+// With w_j the step that wrote key j (none: never), key j is exact for query t iff
+// j <= t < w_j and in the linear memory iff w_j <= t.  From the snapshot taken before
+// the tile's chunk start c0 -- (H_c, s_c) and the cache positions -- the tile's pool is
+// cache(c0) ∪ [c0 - eta, tile end), and for every query t of the tile
+//   O_soft = sum_pool [j <= t < w_j] exp(s_tj - m) v_j,      l_soft = sum of the weights,
+//   O_lin  = phi(q_t)^T H_c + sum_pool [c0 <= w_j <= t] (phi(q_t) . phi(k_j)) v_j,
+//   l_lin  = phi(q_t)^T s_c + sum of those linear weights,
+//   y_t    = (O_soft + e^{-m} O_lin) / (l_soft + e^{-m} l_lin).
+// The tensor cores compute S = Q K^T, L = phi(Q) phi(K)^T (per 64-key pool block),
+// O_soft += P_soft V, O_lin += P_lin V and O_lin = phi(Q) H_c, all bf16 x bf16 -> fp32 in
+// TMEM (M = 128: TMEM lane = query row).  128 threads (one per query row) read S and L
+// from TMEM, apply the masks and an online maximum m that is raised lazily (the
+// accumulator O_soft is rescaled in TMEM only when the block maximum exceeds m by more
+// than 8), and write the bf16 weights back to shared memory for the P V products.
+// Operands are gathered with cp.async into 128-byte-swizzled tiles (pool keys are
+// scattered: the cache positions come from the snapshot).
+#include "lola_internal.cuh"
+#include "lola_tc.cuh"
+
+namespace lola {
+namespace {
+
+using namespace tc;
+
+constexpr int kThreadsTc = 256;
+constexpr int kTM = 128;                 // query rows per tile (MMA M)
+constexpr int kBN = 64;                  // pool keys per block (MMA N of S, L; K of P V)
+constexpr int kD = 128;                  // d_k = d_v = D
+constexpr float kRescale = 8.0f;         // lazy rescale threshold (natural log units)
+constexpr int kWaitLimit = 1 << 24;      // bounded mbarrier polls
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr int SQ = 0;                    // Q tile      K-major, 2 atoms x [128 x 64]
+constexpr int SPQ = 32768;               // phi(Q) tile K-major
+constexpr int SH = 65536;                // H_c         MN-major [K = D x N = d_v]
+constexpr int SK = 98304;                // K block     K-major, 2 atoms x [64 x 64]
+constexpr int SPK = 114688;              // phi(K) block
+constexpr int SV = 131072;               // V block     MN-major [K = 64 x N = d_v]
+constexpr int SPS = 147456;              // soft weights K-major [128 x 64]
+constexpr int SPL = 163840;              // linear weights
+constexpr int SEND = 180224;
+// TMEM columns
+constexpr uint32_t TS = 0, TL = 64, TOS = 128, TOL = 256;
+
+struct TcArgs {
+    int n, eta, lam, chunk, nck;
+    const __nv_bfloat16* Q;
+    const __nv_bfloat16* K;
+    const __nv_bfloat16* V;
+    __nv_bfloat16* Y;
+    const __nv_bfloat16* phiQb;  // [BH][n][D] bf16
+    const __nv_bfloat16* phiKb;
+    const float* phiQ;           // [BH][n][D] float32 (for phi(q)^T s_c)
+    const int32_t* wstep;
+    const float* snapH;
+    const float* snapS;
+    const int32_t* snapC;
+    char* state;                 // per-head status words (timeouts)
+    int64_t head_bytes;
+};
+
+__global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a) {
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    __shared__ uint64_t mbar;
+    __shared__ uint32_t tmem_base;
+    __shared__ int kpos[kBN], kw[kBN];
+
+    const int tid = threadIdx.x, warp = tid / 32;
+    const int bh = blockIdx.y;
+    const int n = a.n;
+    const int t0 = blockIdx.x * kTM, t1 = min(n, t0 + kTM);
+    const int c = t0 / a.chunk, c0 = c * a.chunk;
+    const int wlo = max(0, c0 - a.eta);
+    const int P = a.lam + (t1 - wlo);
+    const int nblk = (P + kBN - 1) / kBN;
+    const int64_t row0 = (int64_t)bh * n;
+    const int32_t* cpos = a.snapC + ((int64_t)bh * a.nck + c) * a.lam;
+    const int32_t* wst = a.wstep + row0;
+    const float scale = 1.0f / sqrtf((float)kD);
+
+    if (tid == 0) mbar_init(smem_u32(&mbar), 1);
+    if (warp == 0) tmem_alloc<512>(smem_u32(&tmem_base));
+
+    // ---- stage Q, phi(Q) (rows t0 .. t0 + 127; beyond n: zero) ----
+    for (int i = tid; i < kTM * 16; i += kThreadsTc) {
+        const int r = i >> 4, c16 = i & 15;
+        const uint32_t off = (c16 >> 3) * 16384 + kmaj_chunk(r, c16 & 7);
+        const int t = t0 + r;
+        if (t < n) {
+            cp_async16(sb + SQ + off, a.Q + (row0 + t) * kD + c16 * 8);
+            cp_async16(sb + SPQ + off, a.phiQb + (row0 + t) * kD + c16 * 8);
+        } else {
+            *reinterpret_cast<uint4*>(sm + SQ + off) = make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(sm + SPQ + off) = make_uint4(0, 0, 0, 0);
+        }
+    }
+    // ---- stage H_c as bf16, MN-major [k = feature][n = value dim] ----
+    {
+        const float* sh = a.snapH + ((int64_t)bh * a.nck + c) * kD * kD;
+        for (int i = tid; i < kD * (kD / 8); i += kThreadsTc) {
+            const int k = i / (kD / 8), n8 = (i % (kD / 8)) * 8;
+            const float4 f0 = *reinterpret_cast<const float4*>(sh + k * kD + n8);
+            const float4 f1 = *reinterpret_cast<const float4*>(sh + k * kD + n8 + 4);
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(f0.x, f0.y), b1 = __floats2bfloat162_rn(f0.z, f0.w);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(f1.x, f1.y), b3 = __floats2bfloat162_rn(f1.z, f1.w);
+            uint4 u;
+            u.x = *reinterpret_cast<uint32_t*>(&b0);
+            u.y = *reinterpret_cast<uint32_t*>(&b1);
+            u.z = *reinterpret_cast<uint32_t*>(&b2);
+            u.w = *reinterpret_cast<uint32_t*>(&b3);
+            *reinterpret_cast<uint4*>(sm + SH + mnmaj_chunk(k, n8, kD)) = u;
+        }
+    }
+    // per-row state (threads 0..127 own query row t0 + tid)
+    const int row = tid;
+    const int t = t0 + row;
+    float m_run = -INFINITY, l_soft = 0.f, l_lin = 0.f;
+    if (tid < kTM && t < n) {
+        const float* pq = a.phiQ + (row0 + t) * kD;
+        const float* ss = a.snapS + ((int64_t)bh * a.nck + c) * kD;
+        float acc = 0.f;
+        for (int k = 0; k < kD; k += 4) {
+            const float4 p = *reinterpret_cast<const float4*>(pq + k);
+            const float4 s = *reinterpret_cast<const float4*>(ss + k);
+            acc = fmaf(p.x, s.x, acc);
+            acc = fmaf(p.y, s.y, acc);
+            acc = fmaf(p.z, s.z, acc);
+            acc = fmaf(p.w, s.w, acc);
+        }
+        l_lin = acc;
+    }
+    cp_async_wait_all();
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tb = tmem_base;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t mb = smem_u32(&mbar);
+    uint32_t phase = 0;
+    bool bad = false;
+
+    // O_lin = phi(Q) H_c
+    if (tid == 0) {
+        constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
+        for (int k = 0; k < kD / 16; ++k) {
+            const uint64_t ad = sdesc(sb + SPQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+            const uint64_t bd = sdesc(sb + SH + k * 2048, 16384, 1024);
+            mma_bf16(tb + TOL, ad, bd, id, k > 0);
+        }
+    }
+
+    for (int b = 0; b < nblk && !bad; ++b) {
+        // ---- gather the block's keys (the previous block's products have completed) ----
+        if (tid < kBN) {
+            const int u = b * kBN + tid;
+            int p = -1;
+            if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
+            kpos[tid] = p;
+            kw[tid] = p >= 0 ? wst[p] : -1;
+        }
+        __syncthreads();
+        for (int i = tid; i < kBN * 16; i += kThreadsTc) {
+            const int r = i >> 4, c16 = i & 15;
+            const int p = kpos[r];
+            const uint32_t off = (c16 >> 3) * 8192 + kmaj_chunk(r, c16 & 7);
+            const uint32_t voff = mnmaj_chunk(r, c16 * 8, kBN);
+            if (p >= 0) {
+                cp_async16(sb + SK + off, a.K + (row0 + p) * kD + c16 * 8);
+                cp_async16(sb + SPK + off, a.phiKb + (row0 + p) * kD + c16 * 8);
+                cp_async16(sb + SV + voff, a.V + (row0 + p) * kD + c16 * 8);
+            } else {
+                *reinterpret_cast<uint4*>(sm + SK + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + SPK + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + SV + voff) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        cp_async_wait_all();
+        fence_async_smem();
+        fence_before();
+        __syncthreads();
+        fence_after();
+        // ---- S = Q K^T, L = phi(Q) phi(K)^T ----
+        if (tid == 0) {
+            constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
+            for (int k = 0; k < kD / 16; ++k) {
+                const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
+                mma_bf16(tb + TS, sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK + bo, 16, 1024), id, k > 0);
+                mma_bf16(tb + TL, sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK + bo, 16, 1024), id, k > 0);
+            }
+            mma_commit(mb);
+        }
+        const bool ok = mbar_wait(mb, phase, kWaitLimit);
+        phase ^= 1;
+        fence_after();
+        // ---- masks, online maximum, weights (one thread per query row) ----
+        if (tid < kTM) {
+            // pass 1: the block's maximum visible score
+            float bm = -INFINITY;
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                float s[32];
+                tmem_ld32(tb + lane_off + TS + 32 * hlf, s);
+                tmem_wait_ld();
+#pragma unroll
+                for (int jj = 0; jj < 32; ++jj) {
+                    const int j = 32 * hlf + jj;
+                    const int p = kpos[j], w = kw[j];
+                    const bool vs = t < n && p >= 0 && p <= t && (w < 0 || w > t);
+                    if (vs) bm = fmaxf(bm, s[jj] * scale);
+                }
+            }
+            if (bm > m_run) {
+                if (m_run == -INFINITY) {
+                    m_run = bm;
+                } else if (bm - m_run > kRescale) {
+                    const float f = expf(m_run - bm);
+                    l_soft *= f;
+                    float o[32];
+#pragma unroll
+                    for (int cc = 0; cc < kD; cc += 32) {
+                        tmem_ld32(tb + lane_off + TOS + cc, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= f;
+                        tmem_st32(tb + lane_off + TOS + cc, o);
+                    }
+                    tmem_wait_st();
+                    m_run = bm;
+                }
+            }
+            // pass 2: bf16 weights into the K-major [128 x 64] tiles (row = query)
+#pragma unroll
+            for (int hlf = 0; hlf < 2; ++hlf) {
+                float s[32], l[32];
+                tmem_ld32(tb + lane_off + TS + 32 * hlf, s);
+                tmem_ld32(tb + lane_off + TL + 32 * hlf, l);
+                tmem_wait_ld();
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                    uint32_t ps[4], pl[4];
+#pragma unroll
+                    for (int hh = 0; hh < 4; ++hh) {
+                        float e[2], g[2];
+#pragma unroll
+                        for (int u = 0; u < 2; ++u) {
+                            const int jj = c4 * 8 + 2 * hh + u, j = 32 * hlf + jj;
+                            const int p = kpos[j], w = kw[j];
+                            const bool vs = t < n && p >= 0 && p <= t && (w < 0 || w > t);
+                            const bool vl = t < n && p >= 0 && w >= c0 && w <= t;
+                            e[u] = vs ? expf(s[jj] * scale - m_run) : 0.f;
+                            g[u] = vl ? l[jj] : 0.f;
+                        }
+                        const __nv_bfloat162 bs = __floats2bfloat162_rn(e[0], e[1]);
+                        const __nv_bfloat162 bl = __floats2bfloat162_rn(g[0], g[1]);
+                        l_soft += __low2float(bs) + __high2float(bs);
+                        l_lin += __low2float(bl) + __high2float(bl);
+                        ps[hh] = *reinterpret_cast<const uint32_t*>(&bs);
+                        pl[hh] = *reinterpret_cast<const uint32_t*>(&bl);
+                    }
+                    const int c16 = 4 * hlf + c4;
+                    *reinterpret_cast<uint4*>(sm + SPS + kmaj_chunk(row, c16)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
+                    *reinterpret_cast<uint4*>(sm + SPL + kmaj_chunk(row, c16)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                }
+            }
+        }
+        fence_async_smem();
+        fence_before();
+        bad = __syncthreads_or(!ok) != 0;
+        fence_after();
+        if (bad) break;
+        // ---- O_soft += P_soft V, O_lin += P_lin V ----
+        if (tid == 0) {
+            constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
+            for (int k = 0; k < kBN / 16; ++k) {
+                const uint64_t vd = sdesc(sb + SV + k * 2048, 8192, 1024);
+                mma_bf16(tb + TOS, sdesc(sb + SPS + k * 32, 16, 1024), vd, id, (b > 0 || k > 0));
+                mma_bf16(tb + TOL, sdesc(sb + SPL + k * 32, 16, 1024), vd, id, 1);
+            }
+            mma_commit(mb);
+        }
+        const bool ok2 = mbar_wait(mb, phase, kWaitLimit);
+        phase ^= 1;
+        fence_after();
+        bad = __syncthreads_or(!ok2) != 0;
+    }
+    if (nblk == 0 && !bad) {
+        // no pool key at all: only the linear base product is pending
+        if (tid == 0) mma_commit(mb);
+        const bool ok = mbar_wait(mb, phase, kWaitLimit);
+        phase ^= 1;
+        fence_after();
+        bad = __syncthreads_or(!ok) != 0;
+    }
+
+    // ---- epilogue: y = (O_soft + e^{-m} O_lin) / (l_soft + e^{-m} l_lin) ----
+    if (!bad && tid < kTM && t < n) {
+        const bool any = m_run != -INFINITY;
+        const float em = any ? expf(-m_run) : 1.f;
+        const float inv = 1.0f / (any ? fmaf(em, l_lin, l_soft) : l_lin);
+        __nv_bfloat16* y = a.Y + (row0 + t) * kD;
+        for (int cc = 0; cc < kD; cc += 32) {
+            float os[32], ol[32];
+            tmem_ld32(tb + lane_off + TOS + cc, os);
+            tmem_ld32(tb + lane_off + TOL + cc, ol);
+            tmem_wait_ld();
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+                const float y0 = (any ? fmaf(em, ol[j], nblk > 0 ? os[j] : 0.f) : ol[j]) * inv;
+                const float y1 = (any ? fmaf(em, ol[j + 1], nblk > 0 ? os[j + 1] : 0.f) : ol[j + 1]) * inv;
+                const __nv_bfloat162 bv = __floats2bfloat162_rn(y0, y1);
+                pk[j / 2] = *reinterpret_cast<const uint32_t*>(&bv);
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+                *reinterpret_cast<uint4*>(y + cc + 8 * q) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+        }
+    }
+    if (bad && tid == 0)
+        atomicOr(reinterpret_cast<int32_t*>(a.state + (int64_t)bh * a.head_bytes) + HDR_STATUS, (int)ST_TIMEOUT);
+    fence_before();
+    __syncthreads();
+    fence_after();
+    if (warp == 0) tmem_dealloc<512>(tb);
+}
+
+}  // namespace
+
+bool output_tc_supported(const Dims& d) { return d.dtype == LOLA_BF16 && d.D == kD && d.dk == kD && d.dv == kD; }
+
+cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K, const void* V,
+                             void* Y, char* state, int64_t head_bytes, cudaStream_t st) {
+    TcArgs a;
+    a.n = n;
+    a.eta = d.eta;
+    a.lam = d.lam;
+    a.chunk = ws.snap_interval;
+    a.nck = ws.nck;
+    a.Q = static_cast<const __nv_bfloat16*>(Q);
+    a.K = static_cast<const __nv_bfloat16*>(K);
+    a.V = static_cast<const __nv_bfloat16*>(V);
+    a.Y = static_cast<__nv_bfloat16*>(Y);
+    a.phiQb = ws.phiQb;
+    a.phiKb = ws.phiKb;
+    a.phiQ = ws.phiQ;
+    a.wstep = ws.wstep;
+    a.snapH = ws.snapH;
+    a.snapS = ws.snapS;
+    a.snapC = ws.snapC;
+    a.state = state;
+    a.head_bytes = head_bytes;
+    const size_t smem = SEND + 1024;
+    cudaError_t e = cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    output_tc_kernel<<<dim3((n + kTM - 1) / kTM, d.BH), kThreadsTc, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace lola

@@ -19,7 +19,8 @@ constexpr int kRowsPerCta = 128;
 template <int DK, int D, typename T>
 __global__ void __launch_bounds__(kPhiThreads) phi_kernel(const T* __restrict__ X, const float* __restrict__ W,
                                                           int64_t w_head_stride, int n, int Hh,
-                                                          float* __restrict__ out) {
+                                                          float* __restrict__ out,
+                                                          __nv_bfloat16* __restrict__ out_bf16) {
     extern __shared__ float sm[];
     float* Ws = sm;                                   // [D/2][DK+1]
     float* xs = sm + (D / 2) * (DK + 1);              // [warps][DK]
@@ -41,33 +42,37 @@ __global__ void __launch_bounds__(kPhiThreads) phi_kernel(const T* __restrict__ 
         phi_warp<DK, D>(xw, Ws, lane, ph);
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) out[row * D + lane + 32 * m] = ph[m];
+        if (out_bf16) {
+#pragma unroll
+            for (int m = 0; m < D / 32; ++m) out_bf16[row * D + lane + 32 * m] = __float2bfloat16_rn(ph[m]);
+        }
         __syncwarp();
     }
 }
 
 template <int DK, int D, typename T>
 cudaError_t launch_phi_t(const Dims& d, int n, const void* X, const float* W, int64_t ws, float* out,
-                         cudaStream_t st) {
+                         __nv_bfloat16* outb, cudaStream_t st) {
     const size_t smem = sizeof(float) * ((D / 2) * (DK + 1) + (kPhiThreads / kWarp) * DK);
     auto kern = phi_kernel<DK, D, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 grid((n + kRowsPerCta - 1) / kRowsPerCta, d.BH);
-    kern<<<grid, kPhiThreads, smem, st>>>(static_cast<const T*>(X), W, ws, n, d.Hh, out);
+    kern<<<grid, kPhiThreads, smem, st>>>(static_cast<const T*>(X), W, ws, n, d.Hh, out, outb);
     return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_phi(const Dims& d, int n, const void* X, const float* W, int64_t ws, float* out,
-                       cudaStream_t st) {
+                       __nv_bfloat16* outb, cudaStream_t st) {
     const bool bf = d.dtype == LOLA_BF16;
     if (d.dk == 128 && d.D == 128)
-        return bf ? launch_phi_t<128, 128, __nv_bfloat16>(d, n, X, W, ws, out, st)
-                  : launch_phi_t<128, 128, float>(d, n, X, W, ws, out, st);
+        return bf ? launch_phi_t<128, 128, __nv_bfloat16>(d, n, X, W, ws, out, outb, st)
+                  : launch_phi_t<128, 128, float>(d, n, X, W, ws, out, outb, st);
     if (d.dk == 64 && d.D == 64)
-        return bf ? launch_phi_t<64, 64, __nv_bfloat16>(d, n, X, W, ws, out, st)
-                  : launch_phi_t<64, 64, float>(d, n, X, W, ws, out, st);
+        return bf ? launch_phi_t<64, 64, __nv_bfloat16>(d, n, X, W, ws, out, outb, st)
+                  : launch_phi_t<64, 64, float>(d, n, X, W, ws, out, outb, st);
     return cudaErrorInvalidValue;
 }
 

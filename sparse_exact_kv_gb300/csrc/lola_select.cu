@@ -491,7 +491,7 @@ cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void*
     a.n = n;
     a.eta = d.eta;
     a.lam = d.lam;
-    a.chunk = d.chunk;
+    a.chunk = ws.snap_interval;
     a.nck = ws.nck;
     a.CL = select_cluster_size(d.lam);
     a.io_bf16 = d.dtype == LOLA_BF16;
