@@ -130,6 +130,7 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
     w.snapS = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D));
     w.snapC = reinterpret_cast<int32_t*>(take(4 * BH * w.nck * (int64_t)(d.lam > 0 ? d.lam : 1)));
     w.slotpos = reinterpret_cast<int32_t*>(take(4 * BH * (int64_t)(d.lam > 0 ? d.lam : 1)));
+    w.abort_flag = reinterpret_cast<int*>(take(4));
     w.bytes = (size_t)o;
     return w;
 }
@@ -234,6 +235,8 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     cudaStream_t st = (cudaStream_t)stream;
     cudaError_t e = launch_state_init(d, static_cast<char*>(state), L, st);
     if (e != cudaSuccess) return cuda_fail(e, "state init");
+    e = cudaMemsetAsync(ws.abort_flag, 0, sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace flag");
     e = traced(LOLA_KERNEL_PHI, st,
                [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, ws.phiKb, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(K)");

@@ -66,6 +66,7 @@ struct Workspace {
     float* snapS;      // [BH][nck][D]
     int32_t* snapC;    // [BH][nck][lam]   cache slot positions before each chunk (-1 empty)
     int32_t* slotpos;  // [BH][lam]        final slot positions (export scratch)
+    int* abort_flag;   // one int, cleared by every lola_prefill call
     int snap_interval;  // steps between snapshots: max(C, 128), one tensor-core query tile
     int nck;
     size_t bytes;

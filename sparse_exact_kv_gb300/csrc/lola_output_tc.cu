@@ -33,7 +33,7 @@ constexpr int kTM = 128;                 // query rows per tile (MMA M)
 constexpr int kBN = 64;                  // pool keys per block (MMA N of S, L; K of P V)
 constexpr int kD = 128;                  // d_k = d_v = D
 constexpr float kRescale = 8.0f;         // lazy rescale threshold (natural log units)
-constexpr int kWaitLimit = 1 << 24;      // bounded mbarrier polls
+constexpr uint64_t kWaitNs = 1000000000ull;  // an MMA group that has not completed in 1 s is an error
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr int SQ = 0;                    // Q tile      K-major, 2 atoms x [128 x 64]
@@ -63,6 +63,7 @@ struct TcArgs {
     const int32_t* snapC;
     char* state;                 // per-head status words (timeouts)
     int64_t head_bytes;
+    int* abort_flag;             // set by any CTA whose wait timed out; later CTAs skip their work
 };
 
 __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a) {
@@ -146,10 +147,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t mb = smem_u32(&mbar);
     uint32_t phase = 0;
-    bool bad = false;
+    bool bad = __syncthreads_or(*reinterpret_cast<volatile int*>(a.abort_flag) != 0) != 0;
 
     // O_lin = phi(Q) H_c
-    if (tid == 0) {
+    if (tid == 0 && !bad) {
         constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
         for (int k = 0; k < kD / 16; ++k) {
             const uint64_t ad = sdesc(sb + SPQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
@@ -198,7 +199,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
             }
             mma_commit(mb);
         }
-        const bool ok = mbar_wait(mb, phase, kWaitLimit);
+        const bool ok = mbar_wait(mb, phase, kWaitNs);
         phase ^= 1;
         fence_after();
         // ---- masks, online maximum, weights (one thread per query row) ----
@@ -218,24 +219,25 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
                     if (vs) bm = fmaxf(bm, s[jj] * scale);
                 }
             }
-            if (bm > m_run) {
-                if (m_run == -INFINITY) {
-                    m_run = bm;
-                } else if (bm - m_run > kRescale) {
-                    const float f = expf(m_run - bm);
-                    l_soft *= f;
-                    float o[32];
+            // lazy rescale of O_soft; TMEM accesses stay warp-uniform (factor 1 for the
+            // rows that keep their maximum)
+            const bool first = bm > m_run && m_run == -INFINITY;
+            const bool need = bm > m_run && m_run != -INFINITY && bm - m_run > kRescale;
+            if (first) m_run = bm;
+            if (__any_sync(0xffffffffu, need)) {
+                const float f = need ? expf(m_run - bm) : 1.f;
+                l_soft *= f;
+                float o[32];
 #pragma unroll
-                    for (int cc = 0; cc < kD; cc += 32) {
-                        tmem_ld32(tb + lane_off + TOS + cc, o);
-                        tmem_wait_ld();
+                for (int cc = 0; cc < kD; cc += 32) {
+                    tmem_ld32(tb + lane_off + TOS + cc, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] *= f;
-                        tmem_st32(tb + lane_off + TOS + cc, o);
-                    }
-                    tmem_wait_st();
-                    m_run = bm;
+                    for (int j = 0; j < 32; ++j) o[j] *= f;
+                    tmem_st32(tb + lane_off + TOS + cc, o);
                 }
+                tmem_wait_st();
+                if (need) m_run = bm;
             }
             // pass 2: bf16 weights into the K-major [128 x 64] tiles (row = query)
 #pragma unroll
@@ -287,26 +289,18 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
             }
             mma_commit(mb);
         }
-        const bool ok2 = mbar_wait(mb, phase, kWaitLimit);
+        const bool ok2 = mbar_wait(mb, phase, kWaitNs);
         phase ^= 1;
         fence_after();
         bad = __syncthreads_or(!ok2) != 0;
     }
-    if (nblk == 0 && !bad) {
-        // no pool key at all: only the linear base product is pending
-        if (tid == 0) mma_commit(mb);
-        const bool ok = mbar_wait(mb, phase, kWaitLimit);
-        phase ^= 1;
-        fence_after();
-        bad = __syncthreads_or(!ok) != 0;
-    }
-
     // ---- epilogue: y = (O_soft + e^{-m} O_lin) / (l_soft + e^{-m} l_lin) ----
-    if (!bad && tid < kTM && t < n) {
+    if (!bad && tid < kTM) {
         const bool any = m_run != -INFINITY;
         const float em = any ? expf(-m_run) : 1.f;
-        const float inv = 1.0f / (any ? fmaf(em, l_lin, l_soft) : l_lin);
-        __nv_bfloat16* y = a.Y + (row0 + t) * kD;
+        const float den = any ? fmaf(em, l_lin, l_soft) : l_lin;
+        const float inv = t < n ? 1.0f / den : 0.f;
+        __nv_bfloat16* y = a.Y + (row0 + (t < n ? t : 0)) * kD;
         for (int cc = 0; cc < kD; cc += 32) {
             float os[32], ol[32];
             tmem_ld32(tb + lane_off + TOS + cc, os);
@@ -315,18 +309,23 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
             uint32_t pk[16];
 #pragma unroll
             for (int j = 0; j < 32; j += 2) {
-                const float y0 = (any ? fmaf(em, ol[j], nblk > 0 ? os[j] : 0.f) : ol[j]) * inv;
-                const float y1 = (any ? fmaf(em, ol[j + 1], nblk > 0 ? os[j + 1] : 0.f) : ol[j + 1]) * inv;
+                const float y0 = (any ? fmaf(em, ol[j], os[j]) : ol[j]) * inv;
+                const float y1 = (any ? fmaf(em, ol[j + 1], os[j + 1]) : ol[j + 1]) * inv;
                 const __nv_bfloat162 bv = __floats2bfloat162_rn(y0, y1);
                 pk[j / 2] = *reinterpret_cast<const uint32_t*>(&bv);
             }
+            if (t < n) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(y + cc + 8 * q) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(y + cc + 8 * q) =
+                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
         }
     }
-    if (bad && tid == 0)
+    if (bad && tid == 0) {
         atomicOr(reinterpret_cast<int32_t*>(a.state + (int64_t)bh * a.head_bytes) + HDR_STATUS, (int)ST_TIMEOUT);
+        atomicExch(a.abort_flag, 1);
+    }
     fence_before();
     __syncthreads();
     fence_after();
@@ -358,6 +357,7 @@ cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const vo
     a.snapC = ws.snapC;
     a.state = state;
     a.head_bytes = head_bytes;
+    a.abort_flag = ws.abort_flag;
     const size_t smem = SEND + 1024;
     cudaError_t e = cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -60,9 +60,15 @@ __device__ __forceinline__ void mbar_init(uint32_t mbar, int count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
-// Bounded wait on an mbarrier phase; returns false after `limit` polls.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int limit) {
-    for (int i = 0; i < limit; ++i) {
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Wait on an mbarrier phase for at most `limit_ns` nanoseconds of wall time; false on timeout.
+__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t start = globaltimer_ns();
+    for (;;) {
         uint32_t ok;
         asm volatile(
             "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -71,8 +77,8 @@ __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity, int li
             : "r"(mbar), "r"(parity)
             : "memory");
         if (ok) return true;
+        if (globaltimer_ns() - start > limit_ns) return false;
     }
-    return false;
 }
 
 template <int NCOLS>
@@ -85,7 +91,9 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t base) {
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(base), "n"(NCOLS));
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32 (w % 4) ..)
+// 32 consecutive fp32 columns of this thread's TMEM lane (warp w reads lanes 32 (w % 4) ..).
+// tcgen05.ld / tcgen05.st / tcgen05.wait are warp-collective: every lane of the warp must
+// execute them, never inside a lane-divergent branch.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
     uint32_t r[32];
     asm volatile(
