@@ -159,6 +159,31 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W,
 int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* host_status,
                          void* stream);
 
+/* ---- prefill without a workspace argument ---------------------------------------------
+ * No counterpart in the LoLA paper: this is an integration convenience of the library.
+ *
+ * For callers that cannot allocate device memory when they call in -- code hosted by a
+ * runtime that owns the device allocator and fixes its budget at start-up, or a
+ * latency-critical path that must not call cudaMalloc/cudaFree, which can synchronise the
+ * whole device.  It computes exactly what lola_prefill computes, but its scratch memory is
+ * a fixed array of LOLA_NOALLOC_SCRATCH_BYTES bytes inside the library's device image:
+ *   - every device that loads the library holds that array until the process exits;
+ *   - the call allocates nothing (no cudaMalloc, cudaFree or allocating library routine);
+ *   - the first call on a device (with that device current) looks up the array's device
+ *     address with cudaGetSymbolAddress and caches it; make that first call before any
+ *     stream capture starts;
+ *   - all calls on a device share the one array and it keeps the last call's contents, so
+ *     calls that overlap on the GPU (different streams, or different host threads, on the
+ *     same device) race with each other: serialise them;
+ *   - returns LOLA_ERR_WORKSPACE, with nothing enqueued, when
+ *     lola_prefill_workspace_bytes(cfg, n) > LOLA_NOALLOC_SCRATCH_BYTES.
+ * Arguments, outputs and errors are otherwise those of lola_prefill. */
+#define LOLA_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+int32_t lola_prefill_noalloc(const lola_config* cfg, int32_t n, const void* Q, const void* K,
+                             const void* V, const float* W, int64_t w_head_stride, void* Y,
+                             void* state, int32_t* write_pos, void* stream);
+
 /* ---- tracing: per-kernel device time of the library's own launches --------------------
  * When enabled, every kernel launch of lola_prefill / lola_decode_step / lola_state_init is
  * bracketed by two CUDA events on the call's stream (a few microseconds of overhead per

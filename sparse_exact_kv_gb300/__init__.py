@@ -30,7 +30,9 @@ LOLA_BF16 = 1
 EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_check_config",
            "lola_state_layout_of", "lola_state_bytes", "lola_prefill_workspace_bytes", "lola_state_init",
            "lola_prefill", "lola_decode_step", "lola_read_status", "lola_kernel_timing", "lola_kernel_time",
-           "lola_kernel_name")
+           "lola_kernel_name", "lola_prefill_noalloc")
+# size of the fixed scratch array behind lola_prefill_noalloc (include/lola.h)
+LOLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNELS = ("state_init", "phi", "select", "output", "decode")
 
 
@@ -79,6 +81,7 @@ def _load():
         "lola_kernel_time": ([ctypes.c_int32, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64)],
                              ctypes.c_int32),
         "lola_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
+        "lola_prefill_noalloc": ([C, ctypes.c_int32, P, P, P, P, ctypes.c_int64, P, P, P, P], ctypes.c_int32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -147,6 +150,15 @@ def lola_prefill(cfg: lola_config, n: int, Q, K, V, W, w_head_stride: int, Y, st
     _check(_lib.lola_prefill(ctypes.byref(cfg), n, _ptr(Q), _ptr(K), _ptr(V), _ptr(W), w_head_stride, _ptr(Y),
                              _ptr(state), _ptr(write_pos), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)), "lola_prefill")
+
+
+def lola_prefill_noalloc(cfg: lola_config, n: int, Q, K, V, W, w_head_stride: int, Y, state, write_pos=None,
+                         stream=None) -> None:
+    """lola_prefill without a workspace: its scratch is the library's fixed device array
+    (LOLA_NOALLOC_SCRATCH_BYTES), for callers that cannot allocate device memory."""
+    _check(_lib.lola_prefill_noalloc(ctypes.byref(cfg), n, _ptr(Q), _ptr(K), _ptr(V), _ptr(W), w_head_stride,
+                                     _ptr(Y), _ptr(state), _ptr(write_pos), _stream(stream)),
+           "lola_prefill_noalloc")
 
 
 def lola_decode_step(cfg: lola_config, state, W, w_head_stride: int, q, k, v, y, written_pos=None,
