@@ -52,33 +52,34 @@ __device__ __forceinline__ void warp_min_key(uint32_t& hi, uint32_t& lo) {
 }
 
 // ---- H role ----
+// Paired FP32 FMAs (__ffma2_rn: two IEEE fmaf in one instruction) with the per-element
+// accumulator assignment and summation order of the scalar form.
 template <int D, int DV>
 __device__ __forceinline__ float h_partial(const float* phi, const float* h, int hrg) {
     constexpr int HR = Shape<D, DV>::HR;
     const float4* p4 = reinterpret_cast<const float4*>(phi + hrg * HR);
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const float2* h2 = reinterpret_cast<const float2*>(h);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < HR / 4; ++c) {
         const float4 f = p4[c];
-        a0 = fmaf(f.x, h[4 * c + 0], a0);
-        a1 = fmaf(f.y, h[4 * c + 1], a1);
-        a2 = fmaf(f.z, h[4 * c + 2], a2);
-        a3 = fmaf(f.w, h[4 * c + 3], a3);
+        a01 = __ffma2_rn(make_float2(f.x, f.y), h2[2 * c], a01);
+        a23 = __ffma2_rn(make_float2(f.z, f.w), h2[2 * c + 1], a23);
     }
-    return (a0 + a1) + (a2 + a3);
+    return (a01.x + a01.y) + (a23.x + a23.y);
 }
 
 template <int D, int DV>
 __device__ __forceinline__ void h_update(float* h, const float* phi_w, float vj, int hrg) {
     constexpr int HR = Shape<D, DV>::HR;
     const float4* p4 = reinterpret_cast<const float4*>(phi_w + hrg * HR);
+    float2* h2 = reinterpret_cast<float2*>(h);
+    const float2 v2 = make_float2(vj, vj);
 #pragma unroll
     for (int c = 0; c < HR / 4; ++c) {
         const float4 f = p4[c];
-        h[4 * c + 0] = fmaf(f.x, vj, h[4 * c + 0]);
-        h[4 * c + 1] = fmaf(f.y, vj, h[4 * c + 1]);
-        h[4 * c + 2] = fmaf(f.z, vj, h[4 * c + 2]);
-        h[4 * c + 3] = fmaf(f.w, vj, h[4 * c + 3]);
+        h2[2 * c] = __ffma2_rn(make_float2(f.x, f.y), v2, h2[2 * c]);
+        h2[2 * c + 1] = __ffma2_rn(make_float2(f.z, f.w), v2, h2[2 * c + 1]);
     }
 }
 
@@ -86,16 +87,15 @@ __device__ __forceinline__ void h_update(float* h, const float* phi_w, float vj,
 template <int D>
 __device__ __forceinline__ float slot_gram(const float* wphi, const float* sphi, int sub) {
     constexpr int PD = D / kSG;
-    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    const float2* s2 = reinterpret_cast<const float2*>(sphi);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
     for (int c = 0; c < PD / 4; ++c) {
         const float4 f = *reinterpret_cast<const float4*>(wphi + 32 * c + 4 * sub);
-        a0 = fmaf(f.x, sphi[4 * c + 0], a0);
-        a1 = fmaf(f.y, sphi[4 * c + 1], a1);
-        a2 = fmaf(f.z, sphi[4 * c + 2], a2);
-        a3 = fmaf(f.w, sphi[4 * c + 3], a3);
+        a01 = __ffma2_rn(make_float2(f.x, f.y), s2[2 * c], a01);
+        a23 = __ffma2_rn(make_float2(f.z, f.w), s2[2 * c + 1], a23);
     }
-    float g = (a0 + a1) + (a2 + a3);
+    float g = (a01.x + a01.y) + (a23.x + a23.y);
     g += __shfl_xor_sync(kFull, g, 1);
     g += __shfl_xor_sync(kFull, g, 2);
     g += __shfl_xor_sync(kFull, g, 4);
@@ -104,25 +104,30 @@ __device__ __forceinline__ float slot_gram(const float* wphi, const float* sphi,
 template <int DV>
 __device__ __forceinline__ void slot_axpy(float* sN, float g, const float* wv, int sub) {
     constexpr int PV = DV / kSG;
+    float2* n2 = reinterpret_cast<float2*>(sN);
+    const float2 g2 = make_float2(g, g);
 #pragma unroll
     for (int c = 0; c < PV / 4; ++c) {
         const float4 f = *reinterpret_cast<const float4*>(wv + 32 * c + 4 * sub);
-        sN[4 * c + 0] = fmaf(g, f.x, sN[4 * c + 0]);
-        sN[4 * c + 1] = fmaf(g, f.y, sN[4 * c + 1]);
-        sN[4 * c + 2] = fmaf(g, f.z, sN[4 * c + 2]);
-        sN[4 * c + 3] = fmaf(g, f.w, sN[4 * c + 3]);
+        n2[2 * c] = __ffma2_rn(g2, make_float2(f.x, f.y), n2[2 * c]);
+        n2[2 * c + 1] = __ffma2_rn(g2, make_float2(f.z, f.w), n2[2 * c + 1]);
     }
 }
 template <int DV>
 __device__ __forceinline__ float slot_sre2(const float* sN, float sz, const float* sv, float svv) {
     constexpr int PV = DV / kSG;
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    const float2* n2 = reinterpret_cast<const float2*>(sN);
+    const float2* v2 = reinterpret_cast<const float2*>(sv);
+    const float2 mz = make_float2(-sz, -sz);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < PV; ++i) {
-        const float dlt = fmaf(-sz, sv[i], sN[i]);
-        a[i & 3] = fmaf(dlt, dlt, a[i & 3]);
+    for (int c = 0; c < PV / 4; ++c) {
+        const float2 d01 = __ffma2_rn(mz, v2[2 * c], n2[2 * c]);
+        const float2 d23 = __ffma2_rn(mz, v2[2 * c + 1], n2[2 * c + 1]);
+        a01 = __ffma2_rn(d01, d01, a01);
+        a23 = __ffma2_rn(d23, d23, a23);
     }
-    float ss = (a[0] + a[1]) + (a[2] + a[3]);
+    float ss = (a01.x + a01.y) + (a23.x + a23.y);
     ss += __shfl_xor_sync(kFull, ss, 1);
     ss += __shfl_xor_sync(kFull, ss, 2);
     ss += __shfl_xor_sync(kFull, ss, 4);
@@ -131,10 +136,14 @@ __device__ __forceinline__ float slot_sre2(const float* sN, float sz, const floa
 template <int DV>
 __device__ __forceinline__ float slot_vv(const float* sv) {
     constexpr int PV = DV / kSG;
-    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    const float2* v2 = reinterpret_cast<const float2*>(sv);
+    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int i = 0; i < PV; ++i) a[i & 3] = fmaf(sv[i], sv[i], a[i & 3]);
-    float vv = (a[0] + a[1]) + (a[2] + a[3]);
+    for (int c = 0; c < PV / 4; ++c) {
+        a01 = __ffma2_rn(v2[2 * c], v2[2 * c], a01);
+        a23 = __ffma2_rn(v2[2 * c + 1], v2[2 * c + 1], a23);
+    }
+    float vv = (a01.x + a01.y) + (a23.x + a23.y);
     vv += __shfl_xor_sync(kFull, vv, 1);
     vv += __shfl_xor_sync(kFull, vv, 2);
     vv += __shfl_xor_sync(kFull, vv, 4);

@@ -107,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ __align__(16) float wbuf[EW];         // winner phi/v copied from a peer CTA
     __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
     __shared__ __align__(16) float nbuf[2][DV];      // the current evictee's N
-    __shared__ float zbuf[2];
+    __shared__ float zbuf[2], vvbuf[2];
     __shared__ uint2 wkey[2][kSelWarps + 1];         // per-warp minima; [16] = the evictee
     __shared__ uint2 exch[2][kMaxCluster];
     __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
@@ -201,17 +201,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         if (d_ev && !(d_write && d_isev)) {
             const int tcta = d_write ? d_cta : d_fill % CL;
             const int tls = d_write ? d_ws : d_fill / CL;
-            const float* eb = ebuf[tp & (kNEB - 1)];
-            float tv[PV];
-            slot_load<DV>(eb + D, sub, tv);
-            const float vv = slot_vv<DV>(tv);
             if (tcta == rank && tls == ls) {
+                const float* eb = ebuf[tp & (kNEB - 1)];
                 slot_load<D>(eb, sub, sphi);
+                slot_load<DV>(eb + D, sub, sv);
                 slot_load<DV>(nbuf[tp & 1], sub, sN);
-#pragma unroll
-                for (int i = 0; i < PV; ++i) sv[i] = tv[i];
                 sz = zbuf[tp & 1];
-                svv = vv;
+                svv = vvbuf[tp & 1];
                 spos = tp - eta;
             }
         }
@@ -278,9 +274,13 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
                     ze += g;
                 }
                 slot_load<DV>(eb + D, sub, ve);
-                const float es = slot_sre2<DV>(Ne, ze, ve, slot_vv<DV>(ve));
+                const float vve = slot_vv<DV>(ve);
+                const float es = slot_sre2<DV>(Ne, ze, ve, vve);
                 if (lane < kSG) slot_store<DV>(nbuf[t & 1], sub, Ne);
-                if (lane == 0) zbuf[t & 1] = ze;
+                if (lane == 0) {
+                    zbuf[t & 1] = ze;
+                    vvbuf[t & 1] = vve;
+                }
                 ehi = key_hi(es);
                 elo = key_lo(t - eta, kEvCode);
             }
