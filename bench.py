@@ -14,6 +14,7 @@ on the data path).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -40,6 +41,8 @@ def parse_args():
     p.add_argument("--no-decode", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--decode-only", action="store_true", help="skip the prefill measurement")
+    p.add_argument("--decode-batch", type=int, default=None, help="batch of the decode workload (profiling)")
     return p.parse_args()
 
 
@@ -296,6 +299,8 @@ def run_decode(L, R, args, pk):
     import torch
     import synth
     w = synth.WORKLOADS[DECODE]
+    if args.decode_batch:
+        w = dataclasses.replace(w, B=args.decode_batch, decode_steps=args.warmup + args.decode_steps)
     x = synth.make_inputs(w)
     dev = torch.device("cuda", R.local)
     steps = min(args.decode_steps, w.decode_steps - args.warmup)
@@ -410,6 +415,12 @@ def main():
     R.init_gpu()
     props = torch.cuda.get_device_properties(R.local)
     pk = peaks(props.multi_processor_count)
+    if args.decode_only:
+        dec = run_decode(L, R, args, pk)
+        if R.rank == 0:
+            print(json.dumps({"metric": "decode tokens/s per layer", **{k: v for k, v in dec.items() if k != "metric"}}))
+        R.close()
+        return 0
     pre = run_prefill(L, R, args, pk)
     w = pre["workload"]
     dec = None if args.no_decode else run_decode(L, R, args, pk)
