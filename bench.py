@@ -308,8 +308,10 @@ def run_decode(L, R, args, pk):
     W = torch.from_numpy(x.W).to(dev)
     P = [dev_tensor(getattr(x, a)[:, :, :w.n], w.dtype, dev) for a in "qkv"]
     lay.prefill(*P, W)
+    torch.cuda.synchronize()
     del P
     lay.workspace = None
+    torch.cuda.empty_cache()
     nt = args.warmup + steps
     dq, dk, dv = (dev_tensor(getattr(x, a)[:, :, w.n:w.n + nt].transpose(2, 0, 1, 3), w.dtype, dev) for a in "qkv")
     y = torch.empty(w.B, w.Hh, w.d, dtype=torch.bfloat16, device=dev)
