@@ -85,6 +85,7 @@ typedef struct {
  *   win_pos    int32   [eta]             window ring: position p sits in entry p % eta
  *   win_k      io      [eta][d_k]
  *   win_v      io      [eta][d_v]
+ *   win_phi    float32 [eta][D]          phi(k) of each window entry
  *   c_pos      int32   [lambda]          cache slots, -1 = empty; after lola_prefill the
  *                                        live slots come first, sorted by position;
  *                                        lola_decode_step reuses slots in place
@@ -97,12 +98,12 @@ typedef struct {
  *                                        H^T phi(k) in [0, d_v) and s^T phi(k) at [d_v],
  *                                        both against the memory after token t - 1
  * The appendix-B element count (eta + lambda)(d_k + d_v) + D d_v + D is the window,
- * cache, H and s above; c_phi, c_N, c_z, ev, positions and the header are the
+ * cache, H and s above; win_phi, c_phi, c_N, c_z, ev, positions and the header are the
  * bookkeeping that lets a decode step score the cache without recomputing H^T phi(k). */
 
 typedef struct {
     int64_t head_bytes;
-    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
+    int64_t H, s, win_pos, win_k, win_v, win_phi, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
 } lola_state_layout;
 
 /* Library version (major * 10000 + minor * 100 + patch). */

@@ -44,8 +44,8 @@ class lola_config(ctypes.Structure):
 
 class lola_state_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
-                ("head_bytes", "H", "s", "win_pos", "win_k", "win_v", "c_pos", "c_k", "c_v", "c_phi", "c_N", "c_z",
-                 "ev")]
+                ("head_bytes", "H", "s", "win_pos", "win_k", "win_v", "win_phi", "c_pos", "c_k", "c_v", "c_phi",
+                 "c_N", "c_z", "ev")]
 
 
 class LolaError(RuntimeError):
@@ -252,6 +252,7 @@ class Lola:
                     win_pos=f(L.win_pos, c.eta, np.int32, 4),
                     win_k=f(L.win_k, c.eta * c.d_k, io, isz).reshape(BH, c.eta, c.d_k),
                     win_v=f(L.win_v, c.eta * c.d_v, io, isz).reshape(BH, c.eta, c.d_v),
+                    win_phi=f(L.win_phi, c.eta * c.D, np.float32, 4).reshape(BH, c.eta, c.D),
                     c_pos=f(L.c_pos, c.lambda_, np.int32, 4),
                     c_k=f(L.c_k, c.lambda_ * c.d_k, io, isz).reshape(BH, c.lambda_, c.d_k),
                     c_v=f(L.c_v, c.lambda_ * c.d_v, io, isz).reshape(BH, c.lambda_, c.d_v),

@@ -183,6 +183,7 @@ int32_t lola_state_layout_of(const lola_config* cfg, lola_state_layout* out) {
     out->win_pos = L.win_pos;
     out->win_k = L.win_k;
     out->win_v = L.win_v;
+    out->win_phi = L.win_phi;
     out->c_pos = L.c_pos;
     out->c_k = L.c_k;
     out->c_v = L.c_v;

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     float* xv = xk + DK;                         // [DV]  new value
     float* ek = xv + DV;                         // [DK]  evictee key
     float* evv = ek + DK;                        // [DV]  evictee value
-    float* nk = evv + DV;                        // [DK]  next evictee key
+    float* nk = evv + DV;                        // [D]   phi(k_t) of the new token
     float* phq = nk + DK;                        // [D]
     float* phe = phq + D;                        // [D]   phi of the evictee
     float* phn = phe + D;                        // [D]   phi of the next evictee
@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     float* cN = reinterpret_cast<float*>(rec + a.L.c_N);
     float* cz = reinterpret_cast<float*>(rec + a.L.c_z);
     float* evs = reinterpret_cast<float*>(rec + a.L.ev);
+    float* wphg = reinterpret_cast<float*>(rec + a.L.win_phi);
     const T* qin = static_cast<const T*>(a.q) + (int64_t)bh * DK;
     const T* kin = static_cast<const T*>(a.k) + (int64_t)bh * DK;
     const T* vin = static_cast<const T*>(a.v) + (int64_t)bh * DV;
@@ -103,7 +104,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         xq[tid] = IO<T>::ld(qin, tid);
         xk[tid] = IO<T>::ld(kin, tid);
         if (ev) ek[tid] = eta > 0 ? IO<T>::ld(wk, (int64_t)ring * DK + tid) : IO<T>::ld(kin, tid);
-        if (nxt) nk[tid] = IO<T>::ld(wk, (int64_t)nring * DK + tid);
+    }
+    if (tid < D && eta > 0) {
+        if (ev) phe[tid] = wphg[(int64_t)ring * D + tid];
+        if (nxt) phn[tid] = wphg[(int64_t)nring * D + tid];
     }
     if (tid < DV) {
         xv[tid] = IO<T>::ld(vin, tid);
@@ -127,16 +131,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         phi_warp<DK, D>(xq, Ws, lane, ph);
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) phq[lane + 32 * m] = ph[m];
-    } else if (warp == 1 && ev) {
+    } else if (warp == 1) {
+        // phi(k_t): stored in the window ring; with eta = 0 it is also the evictee's phi
         float ph[D / 32];
-        phi_warp<DK, D>(ek, Ws, lane, ph);
+        phi_warp<DK, D>(xk, Ws, lane, ph);
 #pragma unroll
-        for (int m = 0; m < D / 32; ++m) phe[lane + 32 * m] = ph[m];
-    } else if (warp == 2 && nxt) {
-        float ph[D / 32];
-        phi_warp<DK, D>(nk, Ws, lane, ph);
-#pragma unroll
-        for (int m = 0; m < D / 32; ++m) phn[lane + 32 * m] = ph[m];
+        for (int m = 0; m < D / 32; ++m) {
+            nk[lane + 32 * m] = ph[m];
+            if (eta == 0) phe[lane + 32 * m] = ph[m];
+        }
     }
     __syncthreads();
 
@@ -295,6 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     if (eta > 0) {
         if (tid < DK) IO<T>::st(wk, (int64_t)ring * DK + tid, xk[tid]);
         if (tid < DV) IO<T>::st(wvv, (int64_t)ring * DV + tid, xv[tid]);
+        if (tid < D) wphg[(int64_t)ring * D + tid] = nk[tid];
         if (tid == 0) winpos[ring] = t;
     }
     __syncthreads();
@@ -383,8 +387,428 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     }
 }
 
+// ---------------------------------------------------------------------------------
+// Fast path (1 <= eta <= kFastEta, lambda <= 64): every byte of a head's step is requested
+// in one burst at the start -- H and the slots' N, z in registers, the slots' phi and the
+// exact KV of cache and window (plus the two evictees' phi) in shared memory by cp.async --
+// because none of it depends on the decision.  The decision, the write and the output then
+// run on chip and everything is written back at the end.  Same chain arithmetic.
+// ---------------------------------------------------------------------------------
+constexpr int kFastLam = 64;
+constexpr int kFastEta = 128;
+
+__device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
+                 "l"(src)
+                 : "memory");
+}
+
+template <int D, int DV, typename T>
+struct FastSmem {
+    static constexpr int DK = D;
+    static constexpr int NRG = kThreads / DV;
+    // byte offsets (16-byte aligned)
+    static constexpr size_t W = 0;                                          // [D/2][DK+1] f32
+    static constexpr size_t CPHI = (W + 4 * (D / 2) * (DK + 1) + 15) / 16 * 16;  // [64][D] f32
+    static constexpr size_t CV = CPHI + 4 * kFastLam * D;                  // [64][DV] T
+    static constexpr size_t CK = CV + sizeof(T) * kFastLam * DV;           // [64][DK] T
+    static constexpr size_t RK = CK + sizeof(T) * kFastLam * DK;           // [kFastEta][DK] T
+    static constexpr size_t RV = RK + sizeof(T) * kFastEta * DK;           // [kFastEta][DV] T
+    static constexpr size_t PHE = RV + sizeof(T) * kFastEta * DV;          // [D] f32 evictee phi
+    static constexpr size_t PHN = PHE + 4 * D;                             // [D] f32 next evictee phi
+    static constexpr size_t EVN = PHN + 4 * D;                             // [DV + 4] f32 evictee N, z
+    static constexpr size_t SS = EVN + 4 * (DV + 4);                       // [D] f32 s
+    static constexpr size_t XQ = SS + 4 * D;                               // [DK] f32
+    static constexpr size_t XK = XQ + 4 * DK;                              // [DK] f32
+    static constexpr size_t XV = XK + 4 * DK;                              // [DV] f32
+    static constexpr size_t PHQ = XV + 4 * DV;                             // [D] f32
+    static constexpr size_t PHK = PHQ + 4 * D;                             // [D] f32
+    static constexpr size_t RED = PHK + 4 * D;                             // [NRG][DV] f32
+    static constexpr size_t RED2 = RED + 4 * NRG * DV;                     // [NRG][DV] f32
+    static constexpr size_t LIN = RED2 + 4 * NRG * DV;                     // [DV] f32
+    static constexpr size_t SC = LIN + 4 * DV;                             // [kFastEta + 64] f32
+    static constexpr size_t WKEY = SC + 4 * (kFastEta + kFastLam);         // [17] uint2
+    static constexpr size_t MISC = WKEY + 8 * 18;                          // [8] f32
+    static constexpr size_t TOTAL = MISC + 4 * 8;
+};
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs a) {
+    using S = Shape<D, DV>;
+    using M = FastSmem<D, DV, T>;
+    constexpr int DK = D;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
+    constexpr int kEvWarp = kDecWarps - 1;
+    extern __shared__ __align__(16) uint8_t smb[];
+    float* Ws = reinterpret_cast<float*>(smb + M::W);
+    float* cphi_s = reinterpret_cast<float*>(smb + M::CPHI);
+    T* cv_s = reinterpret_cast<T*>(smb + M::CV);
+    T* ck_s = reinterpret_cast<T*>(smb + M::CK);
+    T* rk_s = reinterpret_cast<T*>(smb + M::RK);
+    T* rv_s = reinterpret_cast<T*>(smb + M::RV);
+    float* phe = reinterpret_cast<float*>(smb + M::PHE);
+    float* phn = reinterpret_cast<float*>(smb + M::PHN);
+    float* evn = reinterpret_cast<float*>(smb + M::EVN);
+    float* s_sm = reinterpret_cast<float*>(smb + M::SS);
+    float* xq = reinterpret_cast<float*>(smb + M::XQ);
+    float* xk = reinterpret_cast<float*>(smb + M::XK);
+    float* xv = reinterpret_cast<float*>(smb + M::XV);
+    float* phq = reinterpret_cast<float*>(smb + M::PHQ);
+    float* phk = reinterpret_cast<float*>(smb + M::PHK);
+    float* red = reinterpret_cast<float*>(smb + M::RED);
+    float* red2 = reinterpret_cast<float*>(smb + M::RED2);
+    float* lin = reinterpret_cast<float*>(smb + M::LIN);
+    float* sc = reinterpret_cast<float*>(smb + M::SC);
+    uint2* wkey = reinterpret_cast<uint2*>(smb + M::WKEY);
+    float* misc = reinterpret_cast<float*>(smb + M::MISC);
+
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int bh = blockIdx.x, h = bh % a.Hh;
+    const int eta = a.eta, lam = a.lam;
+    char* rec = a.state + (int64_t)bh * a.L.head_bytes;
+    int32_t* hdr = reinterpret_cast<int32_t*>(rec);
+    const int t = hdr[HDR_T];
+    const int nc = hdr[HDR_NCACHE];
+    float* Hg = reinterpret_cast<float*>(rec + a.L.H);
+    float* sg = reinterpret_cast<float*>(rec + a.L.s);
+    int32_t* winpos = reinterpret_cast<int32_t*>(rec + a.L.win_pos);
+    T* wk = reinterpret_cast<T*>(rec + a.L.win_k);
+    T* wvv = reinterpret_cast<T*>(rec + a.L.win_v);
+    float* wphg = reinterpret_cast<float*>(rec + a.L.win_phi);
+    int32_t* cpos = reinterpret_cast<int32_t*>(rec + a.L.c_pos);
+    T* ck = reinterpret_cast<T*>(rec + a.L.c_k);
+    T* cv = reinterpret_cast<T*>(rec + a.L.c_v);
+    float* cphi = reinterpret_cast<float*>(rec + a.L.c_phi);
+    float* cN = reinterpret_cast<float*>(rec + a.L.c_N);
+    float* cz = reinterpret_cast<float*>(rec + a.L.c_z);
+    float* evs = reinterpret_cast<float*>(rec + a.L.ev);
+
+    const bool ev = t >= eta;
+    const int e = t - eta;
+    const int ring = t % eta;
+    const bool nxt = t + 1 - eta >= 0;
+    const int nring = (t + 1) % eta;
+    const int nwin_old = min(t, eta);   // ring entries holding positions t-eta .. t-1 (valid ones)
+
+    // ---- 1. one burst of loads ----
+    {
+        constexpr int PHI_CH = D / 4, V_CH = DV * (int)sizeof(T) / 16, K_CH = DK * (int)sizeof(T) / 16;
+        for (int i = tid; i < nc * PHI_CH; i += kThreads)
+            cp16(cphi_s + (size_t)(i / PHI_CH) * D + 4 * (i % PHI_CH), cphi + (size_t)(i / PHI_CH) * D + 4 * (i % PHI_CH));
+        for (int i = tid; i < nc * V_CH; i += kThreads)
+            cp16(reinterpret_cast<uint8_t*>(cv_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(cv) + 16 * (size_t)i);
+        for (int i = tid; i < nc * K_CH; i += kThreads)
+            cp16(reinterpret_cast<uint8_t*>(ck_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(ck) + 16 * (size_t)i);
+        for (int i = tid; i < eta * K_CH; i += kThreads)
+            cp16(reinterpret_cast<uint8_t*>(rk_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(wk) + 16 * (size_t)i);
+        for (int i = tid; i < eta * V_CH; i += kThreads)
+            cp16(reinterpret_cast<uint8_t*>(rv_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(wvv) + 16 * (size_t)i);
+        if (tid < PHI_CH) {
+            if (ev) cp16(phe + 4 * tid, wphg + (size_t)ring * D + 4 * tid);
+            if (nxt) cp16(phn + 4 * tid, wphg + (size_t)nring * D + 4 * tid);
+            cp16(s_sm + 4 * tid, sg + 4 * tid);
+        }
+        if (tid < (DV + 4) / 4 && ev) cp16(evn + 4 * tid, evs + 4 * tid);
+    }
+    const float* Wh = a.W + (int64_t)h * a.w_head_stride;
+    for (int i = tid; i < (D / 2) * DK; i += kThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
+    if (tid < DK) {
+        xq[tid] = IO<T>::ld(static_cast<const T*>(a.q) + (int64_t)bh * DK, tid);
+        xk[tid] = IO<T>::ld(static_cast<const T*>(a.k) + (int64_t)bh * DK, tid);
+    }
+    if (tid < DV) xv[tid] = IO<T>::ld(static_cast<const T*>(a.v) + (int64_t)bh * DV, tid);
+    const int hj = tid % DV, hrg = tid / DV;
+    float hreg[HR];
+#pragma unroll
+    for (int r = 0; r < HR; ++r) hreg[r] = Hg[(hrg * HR + r) * DV + hj];
+    // slot role (one pass: lambda <= 64)
+    const int sl = tid / kSG, sub = tid % kSG;
+    const bool live = sl < nc;
+    float sN[PV], sz = 0.f;
+    int spos = -1;
+#pragma unroll
+    for (int q = 0; q < PV; ++q) sN[q] = 0.f;
+    if (live) {
+        const float* src = cN + (size_t)sl * DV;
+#pragma unroll
+        for (int c = 0; c < PV / 4; ++c) {
+            const float4 f = *reinterpret_cast<const float4*>(src + 32 * c + 4 * sub);
+            sN[4 * c] = f.x;
+            sN[4 * c + 1] = f.y;
+            sN[4 * c + 2] = f.z;
+            sN[4 * c + 3] = f.w;
+        }
+        sz = cz[sl];
+        spos = cpos[sl];
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
+
+    // ---- 2. phi(q), phi(k_t); next evictee's partials; evictee and slot SREs ----
+    if (warp == 0) {
+        float ph[D / 32];
+        phi_warp<DK, D>(xq, Ws, lane, ph);
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) phq[lane + 32 * m] = ph[m];
+    } else if (warp == 1) {
+        float ph[D / 32];
+        phi_warp<DK, D>(xk, Ws, lane, ph);
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) phk[lane + 32 * m] = ph[m];
+    }
+    if (nxt) red[hrg * DV + hj] = h_partial<D, DV>(phn, hreg, hrg);
+    float ve[PV], zn_prev = 0.f;
+    if (warp == kEvWarp) {
+        uint32_t ehi = kNoKey, elo = kNoKey;
+        if (ev) {
+            float Ne[PV];
+            slot_load<DV>(evn, sub, Ne);
+            const T* vr = rv_s + (size_t)ring * DV;
+#pragma unroll
+            for (int q = 0; q < PV; ++q) ve[q] = IO<T>::ld(vr, slot_dim(sub, q));
+            const float es = slot_sre2<DV>(Ne, evn[DV], ve, slot_vv<DV>(ve));
+            ehi = key_hi(es);
+            elo = key_lo(e, kEvCode);
+        }
+        if (lane == 0) wkey[kDecWarps] = make_uint2(ehi, elo);
+        // z' of the next evictee against s before this step's write
+        if (nxt) {
+            float sr[PD];
+            slot_load<D>(s_sm, sub, sr);
+            zn_prev = slot_gram<D>(phn, sr, sub);
+        }
+    }
+    {
+        float sv[PV];
+        const T* vr = cv_s + (size_t)(live ? sl : 0) * DV;
+#pragma unroll
+        for (int q = 0; q < PV; ++q) sv[q] = live ? IO<T>::ld(vr, slot_dim(sub, q)) : 0.f;
+        const float sre = slot_sre2<DV>(sN, sz, sv, slot_vv<DV>(sv));
+        uint32_t khi = live ? key_hi(sre) : kNoKey;
+        uint32_t klo = live ? key_lo(spos, sl) : kNoKey;
+        warp_min_key(khi, klo);
+        if (lane == 0) wkey[warp] = make_uint2(khi, klo);
+    }
+    __syncthreads();
+
+    // ---- 3. decision (every warp) and write ----
+    const bool write = ev && (nc + 1 > lam);
+    uint2 kk = lane <= kDecWarps ? wkey[lane] : make_uint2(kNoKey, kNoKey);
+    warp_min_key(kk.x, kk.y);
+    const int code = (int)(kk.y & 127u);
+    const int wposn = write ? (int)(kk.y >> 7) : -1;
+    const int wsel = !write ? -2 : (code == kEvCode ? -1 : code);   // -1: the evictee is written
+    const float* wphi = wsel >= 0 ? cphi_s + (size_t)wsel * D : phe;
+    const T* wvT = wsel >= 0 ? cv_s + (size_t)wsel * DV : rv_s + (size_t)ring * DV;
+    float wv4[PV];   // v_w in slot layout (float), for the N updates
+#pragma unroll
+    for (int q = 0; q < PV; ++q) wv4[q] = write ? IO<T>::ld(wvT, slot_dim(sub, q)) : 0.f;
+    // the moved evictee (written slot) and the appended one (no write)
+    const int slot_new = (ev && !write) ? nc : (wsel >= 0 ? wsel : -1);
+    const int nc_after = (ev && !write) ? nc + 1 : nc;
+    if (write) {
+        h_update<D, DV>(hreg, wphi, IO<T>::ld(wvT, hj), hrg);
+        if (warp == kEvWarp && lane < kSG) {
+            float wp[PD], sr[PD];
+            slot_load<D>(wphi, sub, wp);
+            slot_load<D>(s_sm, sub, sr);
+#pragma unroll
+            for (int i = 0; i < PD; ++i) sr[i] += wp[i];
+            slot_store<D>(s_sm, sub, sr);
+        }
+    }
+    // slot update: every live slot absorbs the write; the written slot takes the evictee
+    {
+        const bool moved = live && sl == wsel;
+        float sphi[PD];
+        if (moved) {
+            slot_load<D>(phe, sub, sphi);
+            slot_load<DV>(evn, sub, sN);
+            sz = evn[DV];
+            spos = e;
+        } else {
+            slot_load<D>(cphi_s + (size_t)(live ? sl : 0) * D, sub, sphi);
+        }
+        if (write) {
+            const float g = slot_gram<D>(wphi, sphi, sub);
+            if (live) {
+                float2* n2 = reinterpret_cast<float2*>(sN);
+                const float2 g2 = make_float2(g, g);
+#pragma unroll
+                for (int c = 0; c < PV / 2; ++c) n2[c] = __ffma2_rn(g2, make_float2(wv4[2 * c], wv4[2 * c + 1]), n2[c]);
+                sz += g;
+            }
+        }
+    }
+    // the next evictee: N' corrected by this step's write (evictee warp)
+    float Nn[PV], zn = zn_prev;
+    if (warp == kEvWarp && nxt) {
+        slot_reduce_partials<D, DV>(red, sub, Nn);
+        if (write) {
+            float ph[PD];
+            slot_load<D>(phn, sub, ph);
+            const float g = slot_gram<D>(wphi, ph, sub);
+            float2* n2 = reinterpret_cast<float2*>(Nn);
+            const float2 g2 = make_float2(g, g);
+#pragma unroll
+            for (int c = 0; c < PV / 2; ++c) n2[c] = __ffma2_rn(g2, make_float2(wv4[2 * c], wv4[2 * c + 1]), n2[c]);
+            zn += g;
+        }
+    }
+    __syncwarp();
+
+    // ---- 4. output: scores over window ∪ cache after the write ----
+    const float scale = 1.0f / sqrtf((float)DK);
+    const int nwin = min(t + 1, eta);
+    const int nkeys = nwin + nc_after;
+    for (int base = 0; base < nkeys; base += kThreads / kSG) {
+        const int i = base + sl;
+        float acc = 0.f;
+        if (i < nkeys) {
+            if (i == 0) {                             // the new token
+#pragma unroll
+                for (int q = 0; q < PD; ++q) acc = fmaf(xq[slot_dim(sub, q)], xk[slot_dim(sub, q)], acc);
+            } else {
+                const T* kr;
+                if (i < nwin) {
+                    kr = rk_s + (size_t)((t - i) % eta) * DK;        // positions t-1, t-2, ...
+                } else {
+                    const int j = i - nwin;                          // cache slot
+                    kr = (j == slot_new) ? rk_s + (size_t)ring * DK : ck_s + (size_t)j * DK;
+                }
+#pragma unroll
+                for (int q = 0; q < PD; ++q) acc = fmaf(xq[slot_dim(sub, q)], IO<T>::ld(kr, slot_dim(sub, q)), acc);
+            }
+        }
+        acc += __shfl_xor_sync(kFull, acc, 1);
+        acc += __shfl_xor_sync(kFull, acc, 2);
+        acc += __shfl_xor_sync(kFull, acc, 4);
+        if (i < nkeys && sub == 0) sc[i] = acc * scale;
+    }
+    red2[hrg * DV + hj] = h_partial<D, DV>(phq, hreg, hrg);
+    __syncthreads();
+    if (warp == 0) {
+        float m = -INFINITY;
+        for (int i = lane; i < nkeys; i += kWarp) m = fmaxf(m, sc[i]);
+        m = warp_max(m);
+        float l = 0.f;
+        for (int i = lane; i < nkeys; i += kWarp) {
+            const float p = expf(sc[i] - m);
+            sc[i] = p;
+            l += p;
+        }
+        l = warp_sum(l);
+        if (lane == 0) {
+            misc[1] = nkeys > 0 ? expf(-m) : 1.f;
+            misc[3] = l;
+        }
+    } else if (warp == kEvWarp) {
+        float sr[PD];
+        slot_load<D>(s_sm, sub, sr);
+        const float dl = slot_gram<D>(phq, sr, sub);
+        if (lane == 0) misc[4] = dl;
+    } else if (warp == 1 && lane < DV / 4) {
+        const int j0 = 4 * lane;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            float acc = red2[j0 + jj];
+#pragma unroll
+            for (int rg = 1; rg < NRG; ++rg) acc += red2[rg * DV + j0 + jj];
+            lin[j0 + jj] = acc;
+        }
+    }
+    __syncthreads();
+    {
+        float acc = 0.f;
+        for (int i = hrg; i < nkeys; i += NRG) {
+            float vj;
+            if (i == 0) {
+                vj = xv[hj];
+            } else if (i < nwin) {
+                vj = IO<T>::ld(rv_s + (size_t)((t - i) % eta) * DV, hj);
+            } else {
+                const int j = i - nwin;
+                vj = IO<T>::ld(j == slot_new ? rv_s + (size_t)ring * DV : cv_s + (size_t)j * DV, hj);
+            }
+            acc = fmaf(sc[i], vj, acc);
+        }
+        red[hrg * DV + hj] = acc;
+    }
+    __syncthreads();
+    if (tid < DV) {
+        float num = 0.f;
+#pragma unroll
+        for (int r = 0; r < NRG; ++r) num += red[r * DV + tid];
+        num = fmaf(misc[1], lin[tid], num);
+        const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
+        IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
+    }
+
+    // ---- 5. write back ----
+#pragma unroll
+    for (int r = 0; r < HR; ++r) Hg[(hrg * HR + r) * DV + hj] = hreg[r];
+    if (sl < nc_after) {
+        float* dst = cN + (size_t)sl * DV;
+#pragma unroll
+        for (int c = 0; c < PV / 4; ++c)
+            *reinterpret_cast<float4*>(dst + 32 * c + 4 * sub) =
+                make_float4(sN[4 * c], sN[4 * c + 1], sN[4 * c + 2], sN[4 * c + 3]);
+        if (sub == 0) {
+            cz[sl] = sl == slot_new && !write ? evn[DV] : sz;
+            if (sl == slot_new) cpos[sl] = e;
+        }
+    }
+    if (slot_new >= 0) {
+        if (!write && sl == slot_new) {
+            // appended without a write: N, z are the evictee's own
+            float* dst = cN + (size_t)sl * DV;
+            float Ne[PV];
+            slot_load<DV>(evn, sub, Ne);
+#pragma unroll
+            for (int c = 0; c < PV / 4; ++c)
+                *reinterpret_cast<float4*>(dst + 32 * c + 4 * sub) = make_float4(Ne[4 * c], Ne[4 * c + 1], Ne[4 * c + 2], Ne[4 * c + 3]);
+        }
+        if (tid < D) cphi[(size_t)slot_new * D + tid] = phe[tid];
+        if (tid < DK) ck[(size_t)slot_new * DK + tid] = rk_s[(size_t)ring * DK + tid];
+        if (tid < DV) cv[(size_t)slot_new * DV + tid] = rv_s[(size_t)ring * DV + tid];
+    }
+    if (warp == kEvWarp && lane < kSG) {
+        float sr[PD];
+        slot_load<D>(s_sm, sub, sr);
+        slot_store<D>(sg, sub, sr);
+        if (nxt) slot_store<DV>(evs, sub, Nn);
+        if (lane == 0 && nxt) evs[DV] = zn;
+    }
+    if (tid < DK) IO<T>::st(wk, (int64_t)ring * DK + tid, xk[tid]);
+    if (tid < DV) IO<T>::st(wvv, (int64_t)ring * DV + tid, xv[tid]);
+    if (tid < D) wphg[(int64_t)ring * D + tid] = phk[tid];
+    if (tid == 0) {
+        winpos[ring] = t;
+        hdr[HDR_T] = t + 1;
+        hdr[HDR_NCACHE] = nc_after;
+        if (write) hdr[HDR_NWRITTEN] += 1;
+        if (a.written_pos) a.written_pos[bh] = wposn;
+    }
+    (void)nwin_old;
+}
+
+template <int D, int DV, typename T>
+bool launch_decode_fast(const Dims& d, const DecArgs& a, cudaStream_t st, cudaError_t* err) {
+    if (d.eta < 1 || d.eta > kFastEta || d.lam > kFastLam) return false;
+    const size_t smem = FastSmem<D, DV, T>::TOTAL;
+    auto kern = decode_fast_kernel<D, DV, T>;
+    *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (*err != cudaSuccess) return true;
+    kern<<<d.BH, kThreads, smem, st>>>(a);
+    *err = cudaGetLastError();
+    return true;
+}
+
 template <int D, int DV, typename T>
 cudaError_t launch_decode_t(const Dims& d, const DecArgs& a, cudaStream_t st) {
+    cudaError_t fe = cudaSuccess;
+    if (launch_decode_fast<D, DV, T>(d, a, st, &fe)) return fe;
     constexpr int DK = D;
     constexpr int NRG = kThreads / DV;
     const size_t floats = (D / 2) * (DK + 1) + 4 * DK + 2 * DV + 4 * D + DV + NRG * DV + 2 * DV +

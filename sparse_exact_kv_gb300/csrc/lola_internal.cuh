@@ -23,7 +23,7 @@ __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int
 
 struct Layout {
     int64_t head_bytes;
-    int64_t H, s, win_pos, win_k, win_v, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
+    int64_t H, s, win_pos, win_k, win_v, win_phi, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
 };
 
 inline Layout make_layout(const Dims& d) {
@@ -35,6 +35,7 @@ inline Layout make_layout(const Dims& d) {
     L.win_pos = o;  o = align256(o + 4ll * d.eta);
     L.win_k = o;    o = align256(o + io * d.eta * d.dk);
     L.win_v = o;    o = align256(o + io * d.eta * d.dv);
+    L.win_phi = o;  o = align256(o + 4ll * d.eta * d.D);
     L.c_pos = o;    o = align256(o + 4ll * d.lam);
     L.c_k = o;      o = align256(o + io * d.lam * d.dk);
     L.c_v = o;      o = align256(o + io * d.lam * d.dv);

@@ -388,12 +388,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         int32_t* wp = reinterpret_cast<int32_t*>(rec + a.L.win_pos);
         T* wk = reinterpret_cast<T*>(rec + a.L.win_k);
         T* wv = reinterpret_cast<T*>(rec + a.L.win_v);
-        for (int i = tid; i < eta * (1 + D + DV); i += kThreads) {
+        float* wph = reinterpret_cast<float*>(rec + a.L.win_phi);
+        for (int i = tid; i < eta * (1 + D + DV + D); i += kThreads) {
             const int e = i % eta, part = i / eta;
             const int p = (n - 1) - ((((n - 1) - e) % eta) + eta) % eta;
             if (part == 0) wp[e] = p >= 0 ? p : -1;
-            else if (p >= 0 && part <= D) wk[(int64_t)e * D + (part - 1)] = Kin[(vrow0 + p) * D + (part - 1)];
-            else if (p >= 0) wv[(int64_t)e * DV + (part - 1 - D)] = Vin[(vrow0 + p) * DV + (part - 1 - D)];
+            else if (p < 0) continue;
+            else if (part <= D) wk[(int64_t)e * D + (part - 1)] = Kin[(vrow0 + p) * D + (part - 1)];
+            else if (part <= D + DV) wv[(int64_t)e * DV + (part - 1 - D)] = Vin[(vrow0 + p) * DV + (part - 1 - D)];
+            else wph[(int64_t)e * D + (part - 1 - D - DV)] = phiK[(int64_t)p * D + (part - 1 - D - DV)];
         }
     }
     // cache: live slots first, sorted by position

@@ -76,6 +76,7 @@ def test_state_layout_holds_appendix_b_memory(lib, d, eta, lam, dtype):
     assert L.head_bytes >= min_bytes
     assert lib.lola_state_bytes(cfg) == 15 * L.head_bytes
     regions = [(L.H, 4 * d * d), (L.s, 4 * d), (L.win_pos, 4 * eta), (L.win_k, io * eta * d), (L.win_v, io * eta * d),
+               (L.win_phi, 4 * eta * d),
                (L.c_pos, 4 * lam), (L.c_k, io * lam * d), (L.c_v, io * lam * d), (L.c_phi, 4 * lam * d),
                (L.c_N, 4 * lam * d), (L.c_z, 4 * lam), (L.ev, 4 * (d + 1))]
     end = 64
