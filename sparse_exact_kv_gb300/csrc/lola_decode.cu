@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
 
     // ---- 1. loads: W, tokens, H (H role), s (evictee warp) ----
     const float* Wh = a.W + (int64_t)h * a.w_head_stride;
-    for (int i = tid; i < (D / 2) * DK; i += kThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
+    stage_w<DK, D, kThreads>(Ws, Wh, tid);
     if (tid < DK) {
         xq[tid] = IO<T>::ld(qin, tid);
         xk[tid] = IO<T>::ld(kin, tid);
@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         if (tid < (DV + 4) / 4 && ev) cp16(evn + 4 * tid, evs + 4 * tid);
     }
     const float* Wh = a.W + (int64_t)h * a.w_head_stride;
-    for (int i = tid; i < (D / 2) * DK; i += kThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
+    stage_w<DK, D, kThreads>(Ws, Wh, tid);
     if (tid < DK) {
         xq[tid] = IO<T>::ld(static_cast<const T*>(a.q) + (int64_t)bh * DK, tid);
         xk[tid] = IO<T>::ld(static_cast<const T*>(a.k) + (int64_t)bh * DK, tid);
@@ -720,7 +720,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     __syncthreads();
     {
-        float acc = 0.f;
+        float accs[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = hrg; i < nkeys; i += NRG) {
             float vj;
             if (i == 0) {
@@ -731,9 +731,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
                 const int j = i - nwin;
                 vj = IO<T>::ld(j == slot_new ? rv_s + (size_t)ring * DV : cv_s + (size_t)j * DV, hj);
             }
-            acc = fmaf(sc[i], vj, acc);
+            accs[(i / NRG) & 3] = fmaf(sc[i], vj, accs[(i / NRG) & 3]);
         }
-        red[hrg * DV + hj] = acc;
+        red[hrg * DV + hj] = (accs[0] + accs[1]) + (accs[2] + accs[3]);
     }
     __syncthreads();
     if (tid < DV) {

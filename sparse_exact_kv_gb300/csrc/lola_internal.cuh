@@ -122,10 +122,15 @@ __device__ __forceinline__ void phi_warp(const float* xs, const float* Ws, int l
 #pragma unroll
     for (int m = 0; m < HM; ++m) {
         const float* wr = Ws + (lane + 32 * m) * (DK + 1);
-        float acc = 0.f;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;   // four chains, summed in a fixed order
 #pragma unroll 8
-        for (int c = 0; c < DK; ++c) acc = fmaf(wr[c], xs[c], acc);
-        z[m] = acc;
+        for (int c = 0; c < DK; c += 4) {
+            a0 = fmaf(wr[c + 0], xs[c + 0], a0);
+            a1 = fmaf(wr[c + 1], xs[c + 1], a1);
+            a2 = fmaf(wr[c + 2], xs[c + 2], a2);
+            a3 = fmaf(wr[c + 3], xs[c + 3], a3);
+        }
+        z[m] = (a0 + a1) + (a2 + a3);
     }
     float mx = z[0], mn = z[0];
 #pragma unroll
@@ -146,6 +151,32 @@ __device__ __forceinline__ void phi_warp(const float* xs, const float* Ws, int l
     for (int m = 0; m < HM; ++m) {
         out[m] = ep[m] / sp;
         out[HM + m] = en[m] / sn;
+    }
+}
+
+// Stage W (D/2 x DK, float32, row-major) into shared memory with row stride DK + 1, all
+// loads issued before any store (16-byte loads, fully unrolled over a compile-time count).
+template <int DK, int D, int NT>
+__device__ __forceinline__ void stage_w(float* Ws, const float* W, int tid) {
+    constexpr int N4 = (D / 2) * DK / 4;                 // float4 chunks
+    constexpr int PER = (N4 + NT - 1) / NT;
+    float4 v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int c = tid + i * NT;
+        if (c < N4) v[i] = reinterpret_cast<const float4*>(W)[c];
+    }
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int c = tid + i * NT;
+        if (c < N4) {
+            const int r = (4 * c) / DK, k = (4 * c) % DK;
+            float* dst = Ws + r * (DK + 1) + k;
+            dst[0] = v[i].x;
+            dst[1] = v[i].y;
+            dst[2] = v[i].z;
+            dst[3] = v[i].w;
+        }
     }
 }
 

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(kPhiThreads) phi_kernel(const T* __restrict__ 
     const int bh = blockIdx.y;
     const int h = bh % Hh;
     const float* Wh = W + (int64_t)h * w_head_stride;
-    for (int i = threadIdx.x; i < (D / 2) * DK; i += kPhiThreads) Ws[(i / DK) * (DK + 1) + (i % DK)] = Wh[i];
+    stage_w<DK, D, kPhiThreads>(Ws, Wh, threadIdx.x);
     __syncthreads();
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
     float* xw = xs + warp * DK;
