@@ -48,7 +48,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     constexpr int kEvWarp = kDecWarps - 1;   // holds s and finishes the evictee (slot layout)
     extern __shared__ __align__(16) float sm[];
     float* Ws = sm;                              // [D/2][DK+1]
-    float* xq = Ws + (D / 2) * (DK + 1);         // [DK]  query
+    float* xq = Ws + (D / 2) * w_stride<DK>();   // [DK]  query
     float* xk = xq + DK;                         // [DK]  new key
     float* xv = xk + DK;                         // [DV]  new value
     float* ek = xv + DV;                         // [DK]  evictee key
@@ -409,7 +409,7 @@ struct FastSmem {
     static constexpr int NRG = kThreads / DV;
     // byte offsets (16-byte aligned)
     static constexpr size_t W = 0;                                          // [D/2][DK+1] f32
-    static constexpr size_t CPHI = (W + 4 * (D / 2) * (DK + 1) + 15) / 16 * 16;  // [64][D] f32
+    static constexpr size_t CPHI = (W + 4 * (D / 2) * w_stride<DK>() + 15) / 16 * 16;  // [64][D] f32
     static constexpr size_t CV = CPHI + 4 * kFastLam * D;                  // [64][DV] T
     static constexpr size_t CK = CV + sizeof(T) * kFastLam * DV;           // [64][DK] T
     static constexpr size_t RK = CK + sizeof(T) * kFastLam * DK;           // [kFastEta][DK] T
@@ -811,7 +811,7 @@ cudaError_t launch_decode_t(const Dims& d, const DecArgs& a, cudaStream_t st) {
     if (launch_decode_fast<D, DV, T>(d, a, st, &fe)) return fe;
     constexpr int DK = D;
     constexpr int NRG = kThreads / DV;
-    const size_t floats = (D / 2) * (DK + 1) + 4 * DK + 2 * DV + 4 * D + DV + NRG * DV + 2 * DV +
+    const size_t floats = (D / 2) * w_stride<DK>() + 4 * DK + 2 * DV + 4 * D + DV + NRG * DV + 2 * DV +
                           (d.eta + d.lam + 1) + 2 * (kDecWarps + 2) + 16;
     const size_t smem = sizeof(float) * floats + 64;
     auto kern = decode_kernel<D, DV, T>;

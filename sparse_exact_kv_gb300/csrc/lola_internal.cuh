@@ -109,53 +109,83 @@ __device__ __forceinline__ bool key_less(float a, int pa, float b, int pb) {
 }
 
 // ---------------------------------------------------------------------------------
-// phi(x) = [softmax(W x), softmax(-W x)] for one row, computed by one warp.
-//   xs: the row x (d_k floats) in shared memory;  Ws: W in shared memory with row
-//   stride DK + 1 (conflict-free column reads).  Lane l returns phi[l + 32 m] in
-//   out[m], m < D / 32.  Fixed operation order, shared by every kernel that needs phi,
-//   so prefill and decode produce identical bits.
+// phi(x) = [softmax(W x), softmax(-W x)] for R rows at a time, computed by one warp.
+//   xs: the R rows x (d_k floats each, row stride DK) in shared memory;  Ws: W in shared
+//   memory with row stride DK + 4 (16-byte aligned rows).  Lane l returns phi[l + 32 m]
+//   of row r in out[r][m], m < D / 32.  Each z = W x is summed on four chains (entries
+//   c = 0, 1, 2, 3 mod 4, each in increasing c) added as (c0 + c1) + (c2 + c3); the order
+//   does not depend on R, so every kernel that needs phi produces identical bits.
 // ---------------------------------------------------------------------------------
-template <int DK, int D>
-__device__ __forceinline__ void phi_warp(const float* xs, const float* Ws, int lane, float (&out)[D / 32]) {
-    constexpr int HM = D / 64;  // z values per lane
-    float z[HM];
+template <int DK>
+__host__ __device__ constexpr int w_stride() { return DK + 4; }
+
+template <int DK, int D, int R>
+__device__ __forceinline__ void phi_rows(const float* xs, const float* Ws, int lane, float (&out)[R][D / 32]) {
+    constexpr int HM = D / 64;  // z values per lane and row
+    float acc[R][HM][4];
 #pragma unroll
-    for (int m = 0; m < HM; ++m) {
-        const float* wr = Ws + (lane + 32 * m) * (DK + 1);
-        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;   // four chains, summed in a fixed order
-#pragma unroll 8
-        for (int c = 0; c < DK; c += 4) {
-            a0 = fmaf(wr[c + 0], xs[c + 0], a0);
-            a1 = fmaf(wr[c + 1], xs[c + 1], a1);
-            a2 = fmaf(wr[c + 2], xs[c + 2], a2);
-            a3 = fmaf(wr[c + 3], xs[c + 3], a3);
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int m = 0; m < HM; ++m)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) acc[r][m][j] = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < DK; c += 4) {
+        float4 w[HM];
+#pragma unroll
+        for (int m = 0; m < HM; ++m)
+            w[m] = *reinterpret_cast<const float4*>(Ws + (lane + 32 * m) * w_stride<DK>() + c);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            const float4 x = *reinterpret_cast<const float4*>(xs + r * DK + c);
+#pragma unroll
+            for (int m = 0; m < HM; ++m) {
+                acc[r][m][0] = fmaf(w[m].x, x.x, acc[r][m][0]);
+                acc[r][m][1] = fmaf(w[m].y, x.y, acc[r][m][1]);
+                acc[r][m][2] = fmaf(w[m].z, x.z, acc[r][m][2]);
+                acc[r][m][3] = fmaf(w[m].w, x.w, acc[r][m][3]);
+            }
         }
-        z[m] = (a0 + a1) + (a2 + a3);
     }
-    float mx = z[0], mn = z[0];
 #pragma unroll
-    for (int m = 1; m < HM; ++m) { mx = fmaxf(mx, z[m]); mn = fminf(mn, z[m]); }
-    mx = warp_max(mx);
-    mn = -warp_max(-mn);
-    float ep[HM], en[HM], sp = 0.f, sn = 0.f;
+    for (int r = 0; r < R; ++r) {
+        float z[HM];
 #pragma unroll
-    for (int m = 0; m < HM; ++m) {
-        ep[m] = expf(z[m] - mx);
-        en[m] = expf(mn - z[m]);
-        sp += ep[m];
-        sn += en[m];
-    }
-    sp = warp_sum(sp);
-    sn = warp_sum(sn);
+        for (int m = 0; m < HM; ++m) z[m] = (acc[r][m][0] + acc[r][m][1]) + (acc[r][m][2] + acc[r][m][3]);
+        float mx = z[0], mn = z[0];
 #pragma unroll
-    for (int m = 0; m < HM; ++m) {
-        out[m] = ep[m] / sp;
-        out[HM + m] = en[m] / sn;
+        for (int m = 1; m < HM; ++m) { mx = fmaxf(mx, z[m]); mn = fminf(mn, z[m]); }
+        mx = warp_max(mx);
+        mn = -warp_max(-mn);
+        float ep[HM], en[HM], sp = 0.f, sn = 0.f;
+#pragma unroll
+        for (int m = 0; m < HM; ++m) {
+            ep[m] = expf(z[m] - mx);
+            en[m] = expf(mn - z[m]);
+            sp += ep[m];
+            sn += en[m];
+        }
+        sp = warp_sum(sp);
+        sn = warp_sum(sn);
+#pragma unroll
+        for (int m = 0; m < HM; ++m) {
+            out[r][m] = ep[m] / sp;
+            out[r][HM + m] = en[m] / sn;
+        }
     }
 }
 
-// Stage W (D/2 x DK, float32, row-major) into shared memory with row stride DK + 1, all
-// loads issued before any store (16-byte loads, fully unrolled over a compile-time count).
+// One row: the same arithmetic as phi_rows.
+template <int DK, int D>
+__device__ __forceinline__ void phi_warp(const float* xs, const float* Ws, int lane, float (&out)[D / 32]) {
+    float o[1][D / 32];
+    phi_rows<DK, D, 1>(xs, Ws, lane, o);
+#pragma unroll
+    for (int m = 0; m < D / 32; ++m) out[m] = o[0][m];
+}
+
+// Stage W (D/2 x DK, float32, row-major) into shared memory with row stride DK + 4, all
+// loads issued before any store (16-byte loads and stores, fully unrolled).
 template <int DK, int D, int NT>
 __device__ __forceinline__ void stage_w(float* Ws, const float* W, int tid) {
     constexpr int N4 = (D / 2) * DK / 4;                 // float4 chunks
@@ -171,11 +201,7 @@ __device__ __forceinline__ void stage_w(float* Ws, const float* W, int tid) {
         const int c = tid + i * NT;
         if (c < N4) {
             const int r = (4 * c) / DK, k = (4 * c) % DK;
-            float* dst = Ws + r * (DK + 1) + k;
-            dst[0] = v[i].x;
-            dst[1] = v[i].y;
-            dst[2] = v[i].z;
-            dst[3] = v[i].w;
+            *reinterpret_cast<float4*>(Ws + r * w_stride<DK>() + k) = v[i];
         }
     }
 }

@@ -16,35 +16,44 @@ namespace {
 constexpr int kPhiThreads = 256;
 constexpr int kRowsPerCta = 128;
 
+constexpr int kRowsPerWarp = 8;
+
 template <int DK, int D, typename T>
 __global__ void __launch_bounds__(kPhiThreads) phi_kernel(const T* __restrict__ X, const float* __restrict__ W,
                                                           int64_t w_head_stride, int n, int Hh,
                                                           float* __restrict__ out,
                                                           __nv_bfloat16* __restrict__ out_bf16) {
-    extern __shared__ float sm[];
-    float* Ws = sm;                                   // [D/2][DK+1]
-    float* xs = sm + (D / 2) * (DK + 1);              // [warps][DK]
+    extern __shared__ __align__(16) float sm[];
+    float* Ws = sm;                                           // [D/2][DK+4]
+    float* xs = sm + (D / 2) * w_stride<DK>();                // [warps][kRowsPerWarp][DK]
     const int bh = blockIdx.y;
     const int h = bh % Hh;
-    const float* Wh = W + (int64_t)h * w_head_stride;
-    stage_w<DK, D, kPhiThreads>(Ws, Wh, threadIdx.x);
+    stage_w<DK, D, kPhiThreads>(Ws, W + (int64_t)h * w_head_stride, threadIdx.x);
     __syncthreads();
     const int warp = threadIdx.x / kWarp, lane = threadIdx.x % kWarp;
-    float* xw = xs + warp * DK;
+    float* xw = xs + warp * kRowsPerWarp * DK;
     const int r0 = blockIdx.x * kRowsPerCta;
     const int r1 = min(n, r0 + kRowsPerCta);
-    for (int r = r0 + warp; r < r1; r += kPhiThreads / kWarp) {
-        const int64_t row = (int64_t)bh * n + r;
+    constexpr int kWarps = kPhiThreads / kWarp;
+    for (int rb = r0 + warp * kRowsPerWarp; rb < r1; rb += kWarps * kRowsPerWarp) {
+        const int64_t row = (int64_t)bh * n + rb;
 #pragma unroll
-        for (int c = lane; c < DK; c += kWarp) xw[c] = IO<T>::ld(X, row * DK + c);
+        for (int r = 0; r < kRowsPerWarp; ++r)
+#pragma unroll
+            for (int c = lane; c < DK; c += kWarp)
+                xw[r * DK + c] = rb + r < r1 ? IO<T>::ld(X, (row + r) * DK + c) : 0.f;
         __syncwarp();
-        float ph[D / 32];
-        phi_warp<DK, D>(xw, Ws, lane, ph);
+        float ph[kRowsPerWarp][D / 32];
+        phi_rows<DK, D, kRowsPerWarp>(xw, Ws, lane, ph);
 #pragma unroll
-        for (int m = 0; m < D / 32; ++m) out[row * D + lane + 32 * m] = ph[m];
-        if (out_bf16) {
+        for (int r = 0; r < kRowsPerWarp; ++r) {
+            if (rb + r >= r1) break;
 #pragma unroll
-            for (int m = 0; m < D / 32; ++m) out_bf16[row * D + lane + 32 * m] = __float2bfloat16_rn(ph[m]);
+            for (int m = 0; m < D / 32; ++m) out[(row + r) * D + lane + 32 * m] = ph[r][m];
+            if (out_bf16) {
+#pragma unroll
+                for (int m = 0; m < D / 32; ++m) out_bf16[(row + r) * D + lane + 32 * m] = __float2bfloat16_rn(ph[r][m]);
+            }
         }
         __syncwarp();
     }
@@ -53,7 +62,7 @@ __global__ void __launch_bounds__(kPhiThreads) phi_kernel(const T* __restrict__ 
 template <int DK, int D, typename T>
 cudaError_t launch_phi_t(const Dims& d, int n, const void* X, const float* W, int64_t ws, float* out,
                          __nv_bfloat16* outb, cudaStream_t st) {
-    const size_t smem = sizeof(float) * ((D / 2) * (DK + 1) + (kPhiThreads / kWarp) * DK);
+    const size_t smem = sizeof(float) * ((D / 2) * w_stride<DK>() + (kPhiThreads / kWarp) * kRowsPerWarp * DK);
     auto kern = phi_kernel<DK, D, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
