@@ -131,7 +131,9 @@ __device__ __forceinline__ float slot_sre2(const float* sN, float sz, const floa
     ss += __shfl_xor_sync(kFull, ss, 1);
     ss += __shfl_xor_sync(kFull, ss, 2);
     ss += __shfl_xor_sync(kFull, ss, 4);
-    return sz == 0.f ? svv : ss / (sz * sz);
+    // the fast reciprocal-multiply quotient (about 2 ulp): a decision is a comparison of
+    // these keys, and prefill and decode form them with this same expression
+    return sz == 0.f ? svv : __fdividef(ss, sz * sz);
 }
 template <int DV>
 __device__ __forceinline__ float slot_vv(const float* sv) {

@@ -13,9 +13,11 @@
 //     write w costs each slot g = phi_w . phi_i, N += g v_w, z += g (exact: H changes by
 //     a rank-1 term);
 //   * each CTA holds a replica of H in registers (32 or 8 entries per thread) to compute
-//     the next evictee's H^T phi one step ahead and to emit the chunk snapshots; the last
-//     warp holds s and finishes the evictee (correction by the last write, SRE) with the
-//     arithmetic of a slot;
+//     the next evictee's H^T phi one step ahead and to emit the chunk snapshots;
+//   * the evictee is finished in two parts: right after the previous decision the first
+//     DV/32 warps sum the H^T phi partials and add the last write's correction, one column
+//     per lane, and hand the vector to the last warp through a named barrier; the last
+//     warp holds s and scores the evictee with the arithmetic of a slot;
 //   * per step: apply the previous write; every warp scores its slots and takes its
 //     packed-key minimum with two redux.sync; after the step's single barrier every warp
 //     takes the CTA minimum itself and keeps the decision in registers; with CL > 1 warp 0
@@ -42,7 +44,7 @@ constexpr int kPF = 4;                     // evictee prefetch distance (steps)
 constexpr int kNEB = 8;                    // evictee ring buffers (indexed by step & 7)
 
 struct SelArgs {
-    int n, eta, lam, chunk, nck, CL, io_bf16;
+    int n, eta, lam, chunk, nck, CL, cl_shift, io_bf16;
     const float* phiK;   // [BH][n][D]
     const void* K;       // io [BH][n][D]
     const void* V;       // io [BH][n][DV]
@@ -83,6 +85,13 @@ __device__ __forceinline__ float4 ld_cluster(uint32_t addr) {
                  : "memory");
     return v;
 }
+// named barrier 1: the helper warps arrive, the evictee warp waits
+__device__ __forceinline__ void named_arrive(int nthreads) {
+    asm volatile("bar.arrive 1, %0;" ::"r"(nthreads) : "memory");
+}
+__device__ __forceinline__ void named_sync(int nthreads) {
+    asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory");
+}
 __device__ __forceinline__ void cp_async16(void* dst_smem, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(dst_smem)), "l"(src) : "memory");
 }
@@ -98,7 +107,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
     constexpr int EW = D + DV;
     constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
-    constexpr int kEvWarp = kSelWarps - 1;         // finishes the evictee and holds s
+    constexpr int kEvWarp = kSelWarps - 1;         // scores the evictee and holds s
+    constexpr int kHelp = DV / kWarp;              // warps that build the evictee's N
+    constexpr int kVvWarp = kHelp;                 // computes the next evictee's |v|^2
+    constexpr int kHandoff = (kHelp + 1) * kWarp;  // threads on named barrier 1
+    static_assert(kVvWarp < kEvWarp, "roles");
 
     extern __shared__ __align__(16) float dyn_sm[];
     float (*xbuf)[kSelWarps][EW] = reinterpret_cast<float (*)[kSelWarps][EW]>(dyn_sm);  // [2] warp-best phi/v
@@ -107,7 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ __align__(16) float wbuf[EW];         // winner phi/v copied from a peer CTA
     __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
     __shared__ __align__(16) float nbuf[2][DV];      // the current evictee's N
-    __shared__ float zbuf[2], vvbuf[2];
+    __shared__ float zbuf[2], gbuf[2], vvbuf[4];
     __shared__ uint2 wkey[2][kSelWarps + 1];         // per-warp minima; [16] = the evictee
     __shared__ uint2 exch[2][kMaxCluster];
     __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
@@ -115,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int rank = CLUSTER ? (int)cluster_rank() : 0;
     const int CL = CLUSTER ? a.CL : 1;
-    const int bh = blockIdx.x / CL;
+    const int bh = CLUSTER ? (int)(blockIdx.x >> a.cl_shift) : (int)blockIdx.x;
     const int n = a.n, eta = a.eta, lam = a.lam;
 
     // slot role
@@ -179,6 +192,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     for (int i = tid; i < NRG * DV; i += kThreads) red[0][0][i] = 0.f;
     int n_cached = 0, n_written = 0;
     __syncthreads();
+    // |v_e|^2 of the evictee of step t is computed at step t - 1; step 0's here
+    auto prep_vv = [&](int step) {
+        if (warp == kVvWarp && step <= n && step - eta >= 0) {
+            float ve[PV];
+            slot_load<DV>(ebuf[step & (kNEB - 1)] + D, sub, ve);
+            const float vv = slot_vv<DV>(ve);
+            if (lane == 0) vvbuf[step & 3] = vv;
+        }
+    };
+    prep_vv(0);
+    __syncthreads();
 
     // the decision of the previous step, held by every thread
     int d_write = 0, d_isev = 0, d_cta = 0, d_ws = 0, d_ev = 0, d_fill = 0;
@@ -199,15 +223,15 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     // first moves into its slot (it absorbs the write like every other cached key).
     auto apply = [&](int tp, const float* wsrc) {
         if (d_ev && !(d_write && d_isev)) {
-            const int tcta = d_write ? d_cta : d_fill % CL;
-            const int tls = d_write ? d_ws : d_fill / CL;
+            const int tcta = d_write ? d_cta : (CLUSTER ? d_fill & (CL - 1) : 0);
+            const int tls = d_write ? d_ws : (CLUSTER ? d_fill >> a.cl_shift : d_fill);
             if (tcta == rank && tls == ls) {
                 const float* eb = ebuf[tp & (kNEB - 1)];
                 slot_load<D>(eb, sub, sphi);
                 slot_load<DV>(eb + D, sub, sv);
                 slot_load<DV>(nbuf[tp & 1], sub, sN);
                 sz = zbuf[tp & 1];
-                svv = vvbuf[tp & 1];
+                svv = vvbuf[tp & 3];
                 spos = tp - eta;
             }
         }
@@ -233,16 +257,39 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     };
 
     const float* wsrc_prev = nullptr;
+    int snap_next = 0, snap_c = 0;
     for (int t = 0; t < n; ++t) {
         const bool prev_write = d_write;
-        if (t > 0) {
-            wsrc_prev = prev_write ? winner_src(t - 1) : nullptr;
-            apply(t - 1, wsrc_prev);
+        const bool ev = t >= eta;
+        if (t > 0) wsrc_prev = prev_write ? winner_src(t - 1) : nullptr;
+
+        // ---- helper warps: the evictee's N = (sum of the H^T phi partials against the
+        //      memory before the previous write) + that write's correction, column j per lane
+        //      (the per-element operation order of slot_reduce_partials and slot_axpy) ----
+        if (warp < kHelp && ev) {
+            const int j = warp * kWarp + lane;
+            const float* r = &red[t & 1][0][0];
+            float acc = r[j];
+#pragma unroll
+            for (int rg = 1; rg < NRG; ++rg) acc += r[rg * DV + j];
+            float g = 0.f;
+            if (prev_write) {
+                float ph[PD];
+                slot_load<D>(ebuf[t & (kNEB - 1)], sub, ph);
+                g = slot_gram<D>(wsrc_prev, ph, sub);
+                acc = __fmaf_rn(g, wsrc_prev[D + j], acc);
+            }
+            nbuf[t & 1][j] = acc;
+            if (warp == 0 && lane == 0) gbuf[t & 1] = g;
+            named_arrive(kHandoff);
         }
+        if (t > 0) apply(t - 1, wsrc_prev);
 
         // chunk-start snapshot of the memory before step t
-        if (t % a.chunk == 0) {
-            const int c = t / a.chunk;
+        if (t == snap_next) {
+            const int c = snap_c;
+            snap_next += a.chunk;
+            ++snap_c;
             if (rank == 0) {
                 float* sh = a.snapH + ((int64_t)bh * a.nck + c) * D * DV;
 #pragma unroll
@@ -256,31 +303,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             if (sub == 0 && gslot < lam) a.snapC[((int64_t)bh * a.nck + c) * lam + gslot] = spos;
         }
 
-        // ---- evictee warp: finish the evictee of step t (N' from step t - 1, corrected
-        //      by the previous write) and prepare the next one's z' ----
-        const bool ev = t >= eta;
+        // ---- evictee warp: score the evictee of step t (its N from the helper warps, z'
+        //      from step t - 1 plus the previous write's gram) and prepare the next z' ----
         if (warp == kEvWarp) {
             uint32_t ehi = kNoKey, elo = kNoKey;
             if (ev) {
                 const float* eb = ebuf[t & (kNEB - 1)];
                 float Ne[PV], ve[PV];
-                slot_reduce_partials<D, DV>(&red[t & 1][0][0], sub, Ne);
-                float ze = zpend;
-                if (prev_write) {
-                    float ph[PD];
-                    slot_load<D>(eb, sub, ph);
-                    const float g = slot_gram<D>(wsrc_prev, ph, sub);
-                    slot_axpy<DV>(Ne, g, wsrc_prev + D, sub);
-                    ze += g;
-                }
+                named_sync(kHandoff);
+                slot_load<DV>(nbuf[t & 1], sub, Ne);
+                const float ze = prev_write ? zpend + gbuf[t & 1] : zpend;
                 slot_load<DV>(eb + D, sub, ve);
-                const float vve = slot_vv<DV>(ve);
-                const float es = slot_sre2<DV>(Ne, ze, ve, vve);
-                if (lane < kSG) slot_store<DV>(nbuf[t & 1], sub, Ne);
-                if (lane == 0) {
-                    zbuf[t & 1] = ze;
-                    vvbuf[t & 1] = vve;
-                }
+                const float es = slot_sre2<DV>(Ne, ze, ve, vvbuf[t & 3]);
+                if (lane == 0) zbuf[t & 1] = ze;
                 ehi = key_hi(es);
                 elo = key_lo(t - eta, kEvCode);
             }
@@ -292,8 +327,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             if (lane == 0) wkey[t & 1][kSelWarps] = make_uint2(ehi, elo);
         }
 
-        // ---- next evictee's partials; slot SREs; per-warp minimum ----
+        // ---- next evictee's partials and |v|^2; slot SREs; per-warp minimum ----
         if (t + 1 - eta >= 0) red[(t + 1) & 1][hrg][hj] = h_partial<D, DV>(ebuf[(t + 1) & (kNEB - 1)], h, hrg);
+        prep_vv(t + 1);
         const float sre = slot_sre2<DV>(sN, sz, sv, svv);
         uint32_t khi = spos < 0 ? kNoKey : key_hi(sre);
         uint32_t klo = spos < 0 ? kNoKey : key_lo(spos, ls);
@@ -497,6 +533,8 @@ cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void*
     a.chunk = ws.snap_interval;
     a.nck = ws.nck;
     a.CL = select_cluster_size(d.lam);
+    a.cl_shift = 0;
+    while ((1 << a.cl_shift) < a.CL) ++a.cl_shift;
     a.io_bf16 = d.dtype == LOLA_BF16;
     a.phiK = ws.phiK;
     a.K = K;
