@@ -191,5 +191,79 @@ __device__ __forceinline__ void slot_store(float* v, int sub, const float* in) {
         *reinterpret_cast<float4*>(v + 32 * c + 4 * sub) = make_float4(in[4 * c], in[4 * c + 1], in[4 * c + 2], in[4 * c + 3]);
 }
 
+// ---- value rows kept in the input type (bfloat16 rows are half the shared-memory
+// traffic; widening a bfloat16 to float32 is exact, so the arithmetic is unchanged) ----
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// slot-layout slice of a value row as raw 32-bit words (float: one value per word,
+// bfloat16: two values per word)
+template <int N, typename T>
+struct SlotWords {
+    static constexpr int kWords = (N / kSG) * (int)sizeof(T) / 4;
+};
+template <int N, typename T>
+__device__ __forceinline__ void slot_load_words(const T* v, int sub, uint32_t* w) {
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int c = 0; c < N / kSG / 4; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(v + 32 * c + 4 * sub);
+            w[4 * c + 0] = x.x;
+            w[4 * c + 1] = x.y;
+            w[4 * c + 2] = x.z;
+            w[4 * c + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int c = 0; c < N / kSG / 4; ++c) {
+            const uint2 x = *reinterpret_cast<const uint2*>(v + 32 * c + 4 * sub);
+            w[2 * c + 0] = x.x;
+            w[2 * c + 1] = x.y;
+        }
+    }
+}
+template <int N, typename T>
+__device__ __forceinline__ void slot_store_words(T* v, int sub, const uint32_t* w) {
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int c = 0; c < N / kSG / 4; ++c)
+            *reinterpret_cast<uint4*>(v + 32 * c + 4 * sub) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    } else {
+#pragma unroll
+        for (int c = 0; c < N / kSG / 4; ++c)
+            *reinterpret_cast<uint2*>(v + 32 * c + 4 * sub) = make_uint2(w[2 * c], w[2 * c + 1]);
+    }
+}
+template <int N, typename T>
+__device__ __forceinline__ void slot_widen(const uint32_t* w, float* out) {
+    if constexpr (sizeof(T) == 4) {
+#pragma unroll
+        for (int i = 0; i < N / kSG; ++i) out[i] = __uint_as_float(w[i]);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N / kSG / 2; ++i) {
+            out[2 * i] = bf16_lo(w[i]);
+            out[2 * i + 1] = bf16_hi(w[i]);
+        }
+    }
+}
+template <int N, typename T>
+__device__ __forceinline__ void slot_load_io(const T* v, int sub, float* out) {
+    uint32_t w[SlotWords<N, T>::kWords];
+    slot_load_words<N, T>(v, sub, w);
+    slot_widen<N, T>(w, out);
+}
+// slot_axpy with the written value row in the input type (same per-element FMA)
+template <int DV, typename T>
+__device__ __forceinline__ void slot_axpy_io(float* sN, float g, const T* wv, int sub) {
+    constexpr int PV = DV / kSG;
+    float v[PV];
+    slot_load_io<DV, T>(wv, sub, v);
+    float2* n2 = reinterpret_cast<float2*>(sN);
+    const float2 g2 = make_float2(g, g);
+#pragma unroll
+    for (int c = 0; c < PV / 2; ++c) n2[c] = __ffma2_rn(g2, make_float2(v[2 * c], v[2 * c + 1]), n2[c]);
+}
+
 }  // namespace chain
 }  // namespace lola

@@ -101,23 +101,39 @@ __device__ __forceinline__ void cp_async_wait() {
     asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+template <int D, int DV, typename T>
+struct SelSmem {
+    // dynamic shared memory: the warp-best candidates' phi (float32) and v (input type),
+    // double-buffered by step parity, then (float32 inputs only) the slots' value rows
+    static constexpr size_t kXPhi = sizeof(float) * 2 * kSelWarps * D;
+    static constexpr size_t kXV = sizeof(T) * 2 * kSelWarps * DV;
+    static constexpr size_t kSV = sizeof(T) == 4 ? sizeof(float) * kSPC * DV : 0;
+    static constexpr size_t kBytes = kXPhi + kXV + kSV;
+};
+
 template <int D, int DV, bool CLUSTER, typename T>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     using S = Shape<D, DV>;
+    using M = SelSmem<D, DV, T>;
     constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
-    constexpr int EW = D + DV;
     constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
     constexpr int kEvWarp = kSelWarps - 1;         // scores the evictee and holds s
-    constexpr int kHelp = DV / kWarp;              // warps that build the evictee's N
-    constexpr int kVvWarp = kHelp;                 // computes the next evictee's |v|^2
-    constexpr int kHandoff = (kHelp + 1) * kWarp;  // threads on named barrier 1
-    static_assert(kVvWarp < kEvWarp, "roles");
+    constexpr int kHelpWarp = 0;                   // builds the evictee's N
+    constexpr int kVvWarp = 1;                     // computes the next evictee's |v|^2
+    constexpr int kHandoff = 2 * kWarp;            // threads on named barrier 1
+    constexpr bool kPackV = sizeof(T) == 2;        // bfloat16 slot values stay in registers
+    constexpr int VW = SlotWords<DV, T>::kWords;
 
-    extern __shared__ __align__(16) float dyn_sm[];
-    float (*xbuf)[kSelWarps][EW] = reinterpret_cast<float (*)[kSelWarps][EW]>(dyn_sm);  // [2] warp-best phi/v
-    __shared__ __align__(16) float ebuf[kNEB][EW];   // evictee phi and v (float32), by step & 7
-    __shared__ __align__(16) T evraw[kNEB][DV];      // value row as stored (cp.async target)
-    __shared__ __align__(16) float wbuf[EW];         // winner phi/v copied from a peer CTA
+    extern __shared__ __align__(16) unsigned char dyn_sm[];
+    float (*xphi)[kSelWarps][D] = reinterpret_cast<float (*)[kSelWarps][D]>(dyn_sm);
+    T (*xv)[kSelWarps][DV] = reinterpret_cast<T (*)[kSelWarps][DV]>(dyn_sm + M::kXPhi);
+    float (*sv_sm)[DV] = reinterpret_cast<float (*)[DV]>(dyn_sm + M::kXPhi + M::kXV);
+    __shared__ __align__(16) float ebuf[kNEB][D];    // evictee phi(k), by step & 7
+    __shared__ __align__(16) T evraw[kNEB][DV];      // evictee v as stored, by step & 7
+    __shared__ __align__(16) float wbuf_phi[D];      // winner copied from a peer CTA
+    __shared__ __align__(16) T wbuf_v[DV];
+    __shared__ __align__(16) float zero_phi[D];      // the "nothing written" winner
+    __shared__ __align__(16) T zero_v[DV];
     __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
     __shared__ __align__(16) float nbuf[2][DV];      // the current evictee's N
     __shared__ float zbuf[2], gbuf[2], vvbuf[4];
@@ -131,16 +147,28 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     const int bh = CLUSTER ? (int)(blockIdx.x >> a.cl_shift) : (int)blockIdx.x;
     const int n = a.n, eta = a.eta, lam = a.lam;
 
-    // slot role
+    // slot role: phi and N in registers; v as raw words (bfloat16 pairs in registers,
+    // float32 rows in shared memory)
     const int sl = lane / kSG, sub = lane % kSG;
     const int ls = warp * kSPW + sl;          // local slot
     const int gslot = ls * CL + rank;         // global slot (fill order)
-    float sphi[PD], sv[PV], sN[PV], sz = 0.f, svv = 0.f;
+    float sphi[PD], sN[PV], sz = 0.f, svv = 0.f;
+    uint32_t svw[kPackV ? VW : 1];
     int spos = -1;
 #pragma unroll
     for (int i = 0; i < PD; ++i) sphi[i] = 0.f;
 #pragma unroll
-    for (int i = 0; i < PV; ++i) { sv[i] = 0.f; sN[i] = 0.f; }
+    for (int i = 0; i < PV; ++i) sN[i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < (kPackV ? VW : 1); ++i) svw[i] = 0u;
+    if constexpr (!kPackV) {
+        if (sub == 0)
+            for (int i = 0; i < DV; ++i) sv_sm[ls][i] = 0.f;
+    }
+    auto slot_v = [&](float* out) {
+        if constexpr (kPackV) slot_widen<DV, T>(svw, out);
+        else slot_load<DV>(sv_sm[ls], sub, out);
+    };
 
     // H role
     const int hj = tid % DV, hrg = tid / DV;
@@ -173,30 +201,22 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         }
         cp_async_commit();
     };
-    // After this thread's own copies for `step` landed: widen its value chunk to float32.
-    auto finish = [&](int step) {
-        if (step <= n && step - eta >= 0 && tid >= D / 4 && tid < D / 4 + VCH) {
-            constexpr int PER = 16 / (int)sizeof(T);
-            const int c = tid - D / 4;
-            const T* src = &evraw[step & (kNEB - 1)][c * PER];
-            float* dst = &ebuf[step & (kNEB - 1)][D + c * PER];
-#pragma unroll
-            for (int i = 0; i < PER; ++i) dst[i] = IO<T>::ld(src, i);
-        }
-    };
-    for (int st = 0; st < kPF; ++st) prefetch(st);
-    cp_async_wait<0>();
-    finish(0);
-    finish(1);
+    // phi rows of steps before the first eviction stay zero (their partials are never used)
+    for (int i = tid; i < kNEB * D; i += kThreads) (&ebuf[0][0])[i] = 0.f;
+    for (int i = tid; i < D; i += kThreads) zero_phi[i] = 0.f;
+    for (int i = tid; i < DV; i += kThreads) IO<T>::st(zero_v, i, 0.f);
     // the first evictee's partials are against the empty memory
     for (int i = tid; i < NRG * DV; i += kThreads) red[0][0][i] = 0.f;
+    __syncthreads();
+    for (int st = 0; st < kPF; ++st) prefetch(st);
+    cp_async_wait<0>();
     int n_cached = 0, n_written = 0;
     __syncthreads();
     // |v_e|^2 of the evictee of step t is computed at step t - 1; step 0's here
     auto prep_vv = [&](int step) {
         if (warp == kVvWarp && step <= n && step - eta >= 0) {
             float ve[PV];
-            slot_load<DV>(ebuf[step & (kNEB - 1)] + D, sub, ve);
+            slot_load_io<DV, T>(evraw[step & (kNEB - 1)], sub, ve);
             const float vv = slot_vv<DV>(ve);
             if (lane == 0) vvbuf[step & 3] = vv;
         }
@@ -205,85 +225,127 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __syncthreads();
 
     // the decision of the previous step, held by every thread
-    int d_write = 0, d_isev = 0, d_cta = 0, d_ws = 0, d_ev = 0, d_fill = 0;
+    int d_write = 0, d_isev = 0, d_cta = 0, d_ws = 0;
 
-    // The written candidate's phi/v (step tp), possibly copied from a peer CTA.
-    auto winner_src = [&](int tp) -> const float* {
-        if (d_isev) return ebuf[tp & (kNEB - 1)];
-        if (!CLUSTER || d_cta == rank) return xbuf[tp & 1][d_ws / kSPW];
-        if (tid < EW / 4) {
-            const uint32_t src = map_rank(smem_addr(&xbuf[tp & 1][d_ws / kSPW][4 * tid]), d_cta);
-            reinterpret_cast<float4*>(wbuf)[tid] = ld_cluster(src);
+    // The written candidate of step tp (phi, v), possibly copied from a peer CTA; the
+    // zero row when nothing was written.
+    struct Win {
+        const float* phi;
+        const T* v;
+    };
+    auto winner = [&](bool wrote, int tp) -> Win {
+        if (!wrote) return Win{zero_phi, zero_v};
+        if (d_isev) return Win{ebuf[tp & (kNEB - 1)], evraw[tp & (kNEB - 1)]};
+        const int wb = d_ws / kSPW;
+        if (!CLUSTER || d_cta == rank) return Win{xphi[tp & 1][wb], xv[tp & 1][wb]};
+        if (tid < D / 4) {
+            const float4 x = ld_cluster(map_rank(smem_addr(&xphi[tp & 1][wb][4 * tid]), d_cta));
+            reinterpret_cast<float4*>(wbuf_phi)[tid] = x;
+        } else if (tid < D / 4 + VCH) {
+            const int c = tid - D / 4;
+            const float4 x = ld_cluster(map_rank(smem_addr(reinterpret_cast<const char*>(xv[tp & 1][wb]) + 16 * c), d_cta));
+            reinterpret_cast<float4*>(wbuf_v)[c] = x;
         }
         __syncthreads();
-        return wbuf;
+        return Win{wbuf_phi, wbuf_v};
     };
 
-    // Slots, H and s absorb the decision of step tp; the surviving evictee of step tp
-    // first moves into its slot (it absorbs the write like every other cached key).
-    auto apply = [&](int tp, const float* wsrc) {
-        if (d_ev && !(d_write && d_isev)) {
-            const int tcta = d_write ? d_cta : (CLUSTER ? d_fill & (CL - 1) : 0);
-            const int tls = d_write ? d_ws : (CLUSTER ? d_fill >> a.cl_shift : d_fill);
-            if (tcta == rank && tls == ls) {
-                const float* eb = ebuf[tp & (kNEB - 1)];
-                slot_load<D>(eb, sub, sphi);
-                slot_load<DV>(eb + D, sub, sv);
-                slot_load<DV>(nbuf[tp & 1], sub, sN);
-                sz = zbuf[tp & 1];
-                svv = vvbuf[tp & 3];
-                spos = tp - eta;
-            }
-        }
-        if (d_write) {
-            const float g = slot_gram<D>(wsrc, sphi, sub);
-            if (spos >= 0) {
-                slot_axpy<DV>(sN, g, wsrc + D, sub);
-                sz += g;
-            }
-            h_update<D, DV>(h, wsrc, wsrc[D + hj], hrg);
-            if (warp == kEvWarp) {
-                if (lane < kSG) {
-                    float wp[PD], sr[PD];
-                    slot_load<D>(wsrc, sub, wp);
-                    slot_load<D>(s_sm, sub, sr);
+    // Slots and H absorb the previous step's write (an exact zero update when nothing was
+    // written, so the common path has no branch; an empty slot has phi = 0, hence g = 0).
+    auto absorb = [&](const Win& w) {
+        const float g = slot_gram<D>(w.phi, sphi, sub);
+        slot_axpy_io<DV, T>(sN, g, w.v, sub);
+        sz += g;
+        h_update<D, DV>(h, w.phi, IO<T>::ld(w.v, hj), hrg);
+    };
+    // s absorbs it too (evictee warp, lanes 0-7 hold s in the slot layout)
+    auto absorb_s = [&](const Win& w) {
+        if (lane < kSG) {
+            float wp[PD], sr[PD];
+            slot_load<D>(w.phi, sub, wp);
+            slot_load<D>(s_sm, sub, sr);
 #pragma unroll
-                    for (int i = 0; i < PD; ++i) sr[i] += wp[i];
-                    slot_store<D>(s_sm, sub, sr);
-                }
-                __syncwarp();
-            }
+            for (int i = 0; i < PD; ++i) sr[i] += wp[i];
+            slot_store<D>(s_sm, sub, sr);
         }
+        __syncwarp();
     };
 
-    const float* wsrc_prev = nullptr;
     int snap_next = 0, snap_c = 0;
     for (int t = 0; t < n; ++t) {
         const bool prev_write = d_write;
         const bool ev = t >= eta;
-        if (t > 0) wsrc_prev = prev_write ? winner_src(t - 1) : nullptr;
+        const Win W = winner(prev_write, t - 1);
 
-        // ---- helper warps: the evictee's N = (sum of the H^T phi partials against the
-        //      memory before the previous write) + that write's correction, column j per lane
-        //      (the per-element operation order of slot_reduce_partials and slot_axpy) ----
-        if (warp < kHelp && ev) {
-            const int j = warp * kWarp + lane;
-            const float* r = &red[t & 1][0][0];
-            float acc = r[j];
-#pragma unroll
-            for (int rg = 1; rg < NRG; ++rg) acc += r[rg * DV + j];
+        // ---- helper warp: the evictee's N = (sum of the H^T phi partials against the
+        //      memory before the previous write) + that write's correction, one column per
+        //      lane and pass (the per-element operation order of slot_reduce_partials and
+        //      slot_axpy) ----
+        if (warp == kHelpWarp && ev) {
             float g = 0.f;
             if (prev_write) {
                 float ph[PD];
                 slot_load<D>(ebuf[t & (kNEB - 1)], sub, ph);
-                g = slot_gram<D>(wsrc_prev, ph, sub);
-                acc = __fmaf_rn(g, wsrc_prev[D + j], acc);
+                g = slot_gram<D>(W.phi, ph, sub);
             }
-            nbuf[t & 1][j] = acc;
-            if (warp == 0 && lane == 0) gbuf[t & 1] = g;
+            const float* r = &red[t & 1][0][0];
+#pragma unroll
+            for (int q = 0; q < DV / kWarp; ++q) {
+                const int j = q * kWarp + lane;
+                float acc = r[j];
+#pragma unroll
+                for (int rg = 1; rg < NRG; ++rg) acc += r[rg * DV + j];
+                if (prev_write) acc = __fmaf_rn(g, IO<T>::ld(W.v, j), acc);
+                nbuf[t & 1][j] = acc;
+            }
+            if (lane == 0) gbuf[t & 1] = g;
             named_arrive(kHandoff);
         }
-        if (t > 0) apply(t - 1, wsrc_prev);
+
+        // ---- every warp: absorb the previous write, the next evictee's H^T phi partials
+        //      (against the memory before step t), slot SREs, per-warp minimum ----
+        absorb(W);
+        red[(t + 1) & 1][hrg][hj] = h_partial<D, DV>(ebuf[(t + 1) & (kNEB - 1)], h, hrg);
+        {
+            float vr[PV];
+            slot_v(vr);
+            const float sre = slot_sre2<DV>(sN, sz, vr, svv);
+            uint32_t khi = spos < 0 ? kNoKey : key_hi(sre);
+            uint32_t klo = spos < 0 ? kNoKey : key_lo(spos, ls);
+            const uint32_t mylo = klo;
+            warp_min_key(khi, klo);
+            if (lane == 0) wkey[t & 1][warp] = make_uint2(khi, klo);
+            if (mylo == klo && klo != kNoKey) {
+                slot_store<D>(xphi[t & 1][warp], sub, sphi);
+                if constexpr (kPackV) slot_store_words<DV, T>(xv[t & 1][warp], sub, svw);
+                else slot_store<DV>(reinterpret_cast<float*>(xv[t & 1][warp]), sub, vr);
+            }
+        }
+
+        // ---- evictee warp: s absorbs the write; score the evictee of step t (its N from
+        //      the helper warp, z' from step t - 1 plus the previous write's gram); the
+        //      next evictee's z' against s before step t's write ----
+        if (warp == kEvWarp) {
+            absorb_s(W);
+            uint32_t ehi = kNoKey, elo = kNoKey;
+            if (ev) {
+                float Ne[PV], ve[PV];
+                named_sync(kHandoff);
+                slot_load<DV>(nbuf[t & 1], sub, Ne);
+                const float ze = prev_write ? zpend + gbuf[t & 1] : zpend;
+                slot_load_io<DV, T>(evraw[t & (kNEB - 1)], sub, ve);
+                const float es = slot_sre2<DV>(Ne, ze, ve, vvbuf[t & 3]);
+                if (lane == 0) zbuf[t & 1] = ze;
+                ehi = key_hi(es);
+                elo = key_lo(t - eta, kEvCode);
+            }
+            if (t + 1 - eta >= 0) {
+                float sr[PD];
+                slot_load<D>(s_sm, sub, sr);
+                zpend = slot_gram<D>(ebuf[(t + 1) & (kNEB - 1)], sr, sub);
+            }
+            if (lane == 0) wkey[t & 1][kSelWarps] = make_uint2(ehi, elo);
+        }
 
         // chunk-start snapshot of the memory before step t
         if (t == snap_next) {
@@ -303,47 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             if (sub == 0 && gslot < lam) a.snapC[((int64_t)bh * a.nck + c) * lam + gslot] = spos;
         }
 
-        // ---- evictee warp: score the evictee of step t (its N from the helper warps, z'
-        //      from step t - 1 plus the previous write's gram) and prepare the next z' ----
-        if (warp == kEvWarp) {
-            uint32_t ehi = kNoKey, elo = kNoKey;
-            if (ev) {
-                const float* eb = ebuf[t & (kNEB - 1)];
-                float Ne[PV], ve[PV];
-                named_sync(kHandoff);
-                slot_load<DV>(nbuf[t & 1], sub, Ne);
-                const float ze = prev_write ? zpend + gbuf[t & 1] : zpend;
-                slot_load<DV>(eb + D, sub, ve);
-                const float es = slot_sre2<DV>(Ne, ze, ve, vvbuf[t & 3]);
-                if (lane == 0) zbuf[t & 1] = ze;
-                ehi = key_hi(es);
-                elo = key_lo(t - eta, kEvCode);
-            }
-            if (t + 1 - eta >= 0) {
-                float sr[PD];
-                slot_load<D>(s_sm, sub, sr);
-                zpend = slot_gram<D>(ebuf[(t + 1) & (kNEB - 1)], sr, sub);
-            }
-            if (lane == 0) wkey[t & 1][kSelWarps] = make_uint2(ehi, elo);
-        }
-
-        // ---- next evictee's partials and |v|^2; slot SREs; per-warp minimum ----
-        if (t + 1 - eta >= 0) red[(t + 1) & 1][hrg][hj] = h_partial<D, DV>(ebuf[(t + 1) & (kNEB - 1)], h, hrg);
         prep_vv(t + 1);
-        const float sre = slot_sre2<DV>(sN, sz, sv, svv);
-        uint32_t khi = spos < 0 ? kNoKey : key_hi(sre);
-        uint32_t klo = spos < 0 ? kNoKey : key_lo(spos, ls);
-        const uint32_t mylo = klo;
-        warp_min_key(khi, klo);
-        if (lane == 0) wkey[t & 1][warp] = make_uint2(khi, klo);
-        if (mylo == klo && klo != kNoKey) {
-            float* xb = xbuf[t & 1][warp];
-            slot_store<D>(xb, sub, sphi);
-            slot_store<DV>(xb + D, sub, sv);
-        }
         prefetch(t + kPF);
         cp_async_wait<kPF - 2>();   // this thread's copies for step t + 2 have landed
-        finish(t + 2);
         __syncthreads();
 
         // ---- decide (every warp): CTA minimum, then the cluster exchange ----
@@ -368,18 +392,37 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         d_isev = write && code == kEvCode;
         d_cta = bc;
         d_ws = code;
-        d_ev = ev;
-        d_fill = n_cached;
         if (rank == 0 && tid == 0) {
             wpos[t] = write ? pos : -1;
             if (write) wstep[pos] = t;
+        }
+        // the surviving evictee moves into its slot now; it absorbs this step's write at
+        // the next step like every other cached key
+        if (ev && !d_isev) {
+            const int tcta = write ? bc : (CLUSTER ? n_cached & (CL - 1) : 0);
+            const int tls = write ? code : (CLUSTER ? n_cached >> a.cl_shift : n_cached);
+            if (tcta == rank && tls == ls) {
+                slot_load<D>(ebuf[t & (kNEB - 1)], sub, sphi);
+                if constexpr (kPackV) {
+                    slot_load_words<DV, T>(evraw[t & (kNEB - 1)], sub, svw);
+                } else {
+                    float vr[PV];
+                    slot_load_io<DV, T>(evraw[t & (kNEB - 1)], sub, vr);
+                    slot_store<DV>(sv_sm[ls], sub, vr);
+                }
+                slot_load<DV>(nbuf[t & 1], sub, sN);
+                sz = zbuf[t & 1];
+                svv = vvbuf[t & 3];
+                spos = t - eta;
+            }
         }
         if (ev && !write) ++n_cached;
         if (write) ++n_written;
     }
     const bool last_write = d_write;
-    const float* wlast = last_write ? winner_src(n - 1) : nullptr;
-    apply(n - 1, wlast);
+    const Win WL = winner(last_write, n - 1);
+    absorb(WL);
+    if (warp == kEvWarp) absorb_s(WL);
 
     // ---- export the memory after token n-1 into the state record ----
     char* rec = a.state + (int64_t)bh * a.L.head_bytes;
@@ -411,8 +454,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
                 if (last_write) {
                     float ph[PD];
                     slot_load<D>(eb, sub, ph);
-                    const float g = slot_gram<D>(wlast, ph, sub);
-                    slot_axpy<DV>(Ne, g, wlast + D, sub);
+                    const float g = slot_gram<D>(WL.phi, ph, sub);
+                    slot_axpy_io<DV, T>(Ne, g, WL.v, sub);
                     ze += g;
                 }
                 float* evn = reinterpret_cast<float*>(rec + a.L.ev);
@@ -470,15 +513,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         for (int r = n_cached + tid; r < lam; r += kThreads) reinterpret_cast<int32_t*>(rec + a.L.c_pos)[r] = -1;
 }
 
-template <int D, int DV>
-constexpr size_t select_dyn_smem() {
-    return sizeof(float) * 2 * kSelWarps * (D + DV);
-}
 
 template <int D, int DV, typename T>
 cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t st) {
     auto kern = select_kernel<D, DV, false, T>;
-    const size_t smem = select_dyn_smem<D, DV>();
+    const size_t smem = SelSmem<D, DV, T>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<d.BH, kThreads, smem, st>>>(a);
@@ -488,7 +527,7 @@ cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t s
 template <int D, int DV, typename T>
 cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t st) {
     auto kern = select_kernel<D, DV, true, T>;
-    const size_t smem = select_dyn_smem<D, DV>();
+    const size_t smem = SelSmem<D, DV, T>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (a.CL > 8) {
