@@ -7,8 +7,11 @@
 // 2.2, Eqs. 3-5).
 //
 // Layouts
-//   H role    thread tid holds column hj = tid % DV of H for the HR consecutive rows
-//             hrg*HR .. hrg*HR + HR - 1 (hrg = tid / DV), in registers.
+//   H role    warp w holds the HR = D/16 rows w*HR .. w*HR + HR - 1 of H; lane l holds the
+//             HC = DV/32 columns l*HC .. l*HC + HC - 1 of them, in registers (h[r*HC + c]).
+//             A write then reads HR phi values (one broadcast per warp) and HC values of v;
+//             H^T phi of a key is HR-row partials per warp, summed over the 16 row groups
+//             in order.
 //   slot role 8 lanes per cached candidate ("slot"); lane `sub` holds entries
 //             slot_dim(sub, i) of phi(k), v and N = H^T phi(k) (float4 chunks interleaved
 //             across the 8 lanes), and every lane holds the slot's z = s^T phi(k).
@@ -32,14 +35,20 @@ constexpr int kEvCode = 127;           // owner code of the evictee in a packed 
 
 template <int D, int DV>
 struct Shape {
-    static constexpr int NRG = kThreads / DV;  // H row groups
-    static constexpr int HR = D / NRG;         // H rows per thread
-    static constexpr int PD = D / kSG;         // phi entries per slot lane
-    static constexpr int PV = DV / kSG;        // v / N entries per slot lane
-    static_assert(kThreads % DV == 0 && D % NRG == 0 && HR % 4 == 0 && PD % 4 == 0 && PV % 4 == 0, "shape");
+    static constexpr int NRG = kThreads / kWarp;  // H row groups, one per warp
+    static constexpr int HR = D / NRG;            // H rows per thread
+    static constexpr int HC = DV / kWarp;         // H columns per thread
+    static constexpr int PD = D / kSG;            // phi entries per slot lane
+    static constexpr int PV = DV / kSG;           // v / N entries per slot lane
+    static_assert(D % NRG == 0 && HR % 4 == 0 && (HC == 2 || HC == 4) && PD % 4 == 0 && PV % 4 == 0, "shape");
 };
 
 __device__ __forceinline__ int slot_dim(int sub, int i) { return 4 * sub + 32 * (i >> 2) + (i & 3); }
+
+// bfloat16 halves of a 32-bit word, widened to float32 (exact)
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
 
 // ---- packed keys: smaller SRE^2 first (the bits of a non-negative float order like an
 // unsigned int), then the older position, then the owner code (slot index or kEvCode) ----
@@ -52,35 +61,117 @@ __device__ __forceinline__ void warp_min_key(uint32_t& hi, uint32_t& lo) {
 }
 
 // ---- H role ----
-// Paired FP32 FMAs (__ffma2_rn: two IEEE fmaf in one instruction) with the per-element
-// accumulator assignment and summation order of the scalar form.
-template <int D, int DV>
-__device__ __forceinline__ float h_partial(const float* phi, const float* h, int hrg) {
-    constexpr int HR = Shape<D, DV>::HR;
-    const float4* p4 = reinterpret_cast<const float4*>(phi + hrg * HR);
-    const float2* h2 = reinterpret_cast<const float2*>(h);
-    float2 a01 = make_float2(0.f, 0.f), a23 = make_float2(0.f, 0.f);
-#pragma unroll
-    for (int c = 0; c < HR / 4; ++c) {
-        const float4 f = p4[c];
-        a01 = __ffma2_rn(make_float2(f.x, f.y), h2[2 * c], a01);
-        a23 = __ffma2_rn(make_float2(f.z, f.w), h2[2 * c + 1], a23);
+template <int HC>
+__device__ __forceinline__ void h_vec_load(const float* src, float* out) {
+    if constexpr (HC == 4) {
+        const float4 f = *reinterpret_cast<const float4*>(src);
+        out[0] = f.x; out[1] = f.y; out[2] = f.z; out[3] = f.w;
+    } else {
+        const float2 f = *reinterpret_cast<const float2*>(src);
+        out[0] = f.x; out[1] = f.y;
     }
-    return (a01.x + a01.y) + (a23.x + a23.y);
 }
-
+template <int HC>
+__device__ __forceinline__ void h_vec_store(float* dst, const float* in) {
+    if constexpr (HC == 4) *reinterpret_cast<float4*>(dst) = make_float4(in[0], in[1], in[2], in[3]);
+    else *reinterpret_cast<float2*>(dst) = make_float2(in[0], in[1]);
+}
+// this thread's block of a row-major D x DV matrix (H in the state, a snapshot)
 template <int D, int DV>
-__device__ __forceinline__ void h_update(float* h, const float* phi_w, float vj, int hrg) {
-    constexpr int HR = Shape<D, DV>::HR;
-    const float4* p4 = reinterpret_cast<const float4*>(phi_w + hrg * HR);
-    float2* h2 = reinterpret_cast<float2*>(h);
-    const float2 v2 = make_float2(vj, vj);
+__device__ __forceinline__ void h_load(float* h, const float* Hm, int w, int l) {
+    using S = Shape<D, DV>;
 #pragma unroll
-    for (int c = 0; c < HR / 4; ++c) {
-        const float4 f = p4[c];
-        h2[2 * c] = __ffma2_rn(make_float2(f.x, f.y), v2, h2[2 * c]);
-        h2[2 * c + 1] = __ffma2_rn(make_float2(f.z, f.w), v2, h2[2 * c + 1]);
+    for (int r = 0; r < S::HR; ++r) h_vec_load<S::HC>(Hm + (int64_t)(w * S::HR + r) * DV + l * S::HC, h + r * S::HC);
+}
+template <int D, int DV>
+__device__ __forceinline__ void h_store(float* Hm, const float* h, int w, int l) {
+    using S = Shape<D, DV>;
+#pragma unroll
+    for (int r = 0; r < S::HR; ++r) h_vec_store<S::HC>(Hm + (int64_t)(w * S::HR + r) * DV + l * S::HC, h + r * S::HC);
+}
+// this lane's HC entries of a value row (float32 or bfloat16, widened exactly)
+template <int DV, typename T>
+__device__ __forceinline__ void h_cols(const T* v, int l, float* out) {
+    constexpr int HC = DV / kWarp;
+    if constexpr (sizeof(T) == 4) {
+        h_vec_load<HC>(reinterpret_cast<const float*>(v) + l * HC, out);
+    } else if constexpr (HC == 4) {
+        const uint2 x = *reinterpret_cast<const uint2*>(v + l * HC);
+        out[0] = bf16_lo(x.x); out[1] = bf16_hi(x.x); out[2] = bf16_lo(x.y); out[3] = bf16_hi(x.y);
+    } else {
+        const uint32_t x = *reinterpret_cast<const uint32_t*>(v + l * HC);
+        out[0] = bf16_lo(x); out[1] = bf16_hi(x);
     }
+}
+// H += phi_w v_w^T on this thread's block: per element fma(phi_r, v_c, H[r][c]), paired
+// over columns with __ffma2_rn (two IEEE fmaf in one instruction)
+template <int D, int DV>
+__device__ __forceinline__ void h_update(float* h, const float* phi_w, const float* vw, int w) {
+    using S = Shape<D, DV>;
+    constexpr int HR = S::HR, HC2 = S::HC / 2;
+    const float4* p4 = reinterpret_cast<const float4*>(phi_w + w * HR);
+    float2* h2 = reinterpret_cast<float2*>(h);
+#pragma unroll
+    for (int r4 = 0; r4 < HR / 4; ++r4) {
+        const float4 f = p4[r4];
+        const float ph[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int cp = 0; cp < HC2; ++cp) {
+                float2& x = h2[(4 * r4 + rr) * HC2 + cp];
+                x = __ffma2_rn(make_float2(ph[rr], ph[rr]), make_float2(vw[2 * cp], vw[2 * cp + 1]), x);
+            }
+    }
+}
+// this warp's row-group partial of H^T phi for the lane's HC columns: even and odd rows
+// accumulate separately (in row order), then add
+template <int D, int DV>
+__device__ __forceinline__ void h_partial(const float* phi, const float* h, int w, float* out) {
+    using S = Shape<D, DV>;
+    constexpr int HR = S::HR, HC2 = S::HC / 2;
+    const float4* p4 = reinterpret_cast<const float4*>(phi + w * HR);
+    const float2* h2 = reinterpret_cast<const float2*>(h);
+    float2 a0[HC2], a1[HC2];
+#pragma unroll
+    for (int cp = 0; cp < HC2; ++cp) {
+        a0[cp] = make_float2(0.f, 0.f);
+        a1[cp] = make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int r4 = 0; r4 < HR / 4; ++r4) {
+        const float4 f = p4[r4];
+        const float ph[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr)
+#pragma unroll
+            for (int cp = 0; cp < HC2; ++cp) {
+                float2& acc = (rr & 1) ? a1[cp] : a0[cp];
+                acc = __ffma2_rn(make_float2(ph[rr], ph[rr]), h2[(4 * r4 + rr) * HC2 + cp], acc);
+            }
+    }
+#pragma unroll
+    for (int cp = 0; cp < HC2; ++cp) {
+        out[2 * cp] = a0[cp].x + a1[cp].x;
+        out[2 * cp + 1] = a0[cp].y + a1[cp].y;
+    }
+}
+// the partial stored at red[w][l*HC ..] (red: [NRG][DV])
+template <int D, int DV>
+__device__ __forceinline__ void h_partial_store(float* red, const float* phi, const float* h, int w, int l) {
+    using S = Shape<D, DV>;
+    float out[S::HC];
+    h_partial<D, DV>(phi, h, w, out);
+    h_vec_store<S::HC>(red + w * DV + l * S::HC, out);
+}
+// N' = sum of the row-group partials in row-group order, one column j (any thread)
+template <int D, int DV>
+__device__ __forceinline__ float reduce_partials_col(const float* red, int j) {
+    constexpr int NRG = Shape<D, DV>::NRG;
+    float acc = red[j];
+#pragma unroll
+    for (int rg = 1; rg < NRG; ++rg) acc += red[rg * DV + j];
+    return acc;
 }
 
 // ---- slot role (8 lanes per slot) ----
@@ -193,8 +284,6 @@ __device__ __forceinline__ void slot_store(float* v, int sub, const float* in) {
 
 // ---- value rows kept in the input type (bfloat16 rows are half the shared-memory
 // traffic; widening a bfloat16 to float32 is exact, so the arithmetic is unchanged) ----
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 // slot-layout slice of a value row as raw 32-bit words (float: one value per word,
 // bfloat16: two values per word)

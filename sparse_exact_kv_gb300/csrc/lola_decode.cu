@@ -44,7 +44,8 @@ template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     using S = Shape<D, DV>;
     constexpr int DK = D;
-    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, HC = S::HC;
+    constexpr int KS = kThreads / DV;        // key splits of the output numerator
     constexpr int kEvWarp = kDecWarps - 1;   // holds s and finishes the evictee (slot layout)
     extern __shared__ __align__(16) float sm[];
     float* Ws = sm;                              // [D/2][DK+1]
@@ -113,10 +114,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         xv[tid] = IO<T>::ld(vin, tid);
         if (ev) evv[tid] = eta > 0 ? IO<T>::ld(wvv, (int64_t)ring * DV + tid) : IO<T>::ld(vin, tid);
     }
-    const int hj = tid % DV, hrg = tid / DV;
-    float hreg[HR];
-#pragma unroll
-    for (int r = 0; r < HR; ++r) hreg[r] = Hg[(hrg * HR + r) * DV + hj];
+    float hreg[HR * HC];
+    h_load<D, DV>(hreg, Hg, warp, lane);
     const int sl = tid / kSG, sub = tid % kSG;
     float s_reg[PD];                                      // s, held by the evictee warp
 #pragma unroll
@@ -147,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     //         (or, with eta = 0, this step's own evictee) H^T phi ----
     const float* pvec = eta > 0 ? phn : phe;
     const bool want_partials = eta > 0 ? nxt : ev;
-    if (want_partials) red[hrg * DV + hj] = h_partial<D, DV>(pvec, hreg, hrg);
+    if (want_partials) h_partial_store<D, DV>(red, pvec, hreg, warp, lane);
     __syncthreads();
 
     // ---- 4. the evictee's N, z and SRE; the next evictee's N', z' (evictee warp) ----
@@ -236,7 +235,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         if (tid < D) wphi[tid] = wsel < 0 ? phe[tid] : cphi[(int64_t)wsel * D + tid];
         if (tid < DV) wv[tid] = wsel < 0 ? evv[tid] : IO<T>::ld(cv, (int64_t)wsel * DV + tid);
         __syncthreads();
-        h_update<D, DV>(hreg, wphi, wv[hj], hrg);
+        float vh[HC];
+        h_vec_load<HC>(wv + lane * HC, vh);
+        h_update<D, DV>(hreg, wphi, vh, warp);
         if (warp == kEvWarp) {
             float wp[PD];
             slot_load<D>(wphi, sub, wp);
@@ -323,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         acc += __shfl_xor_sync(kFull, acc, 4);
         if (i < nkeys && sub == 0) sc[i] = acc * scale;
     }
-    red[hrg * DV + hj] = h_partial<D, DV>(phq, hreg, hrg);
+    h_partial_store<D, DV>(red, phq, hreg, warp, lane);
     __syncthreads();
     if (warp == 0) {
         float m = -INFINITY;
@@ -357,18 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     }
     __syncthreads();
     {
-        // numerator: keys split over the NRG row groups, then combined
+        // numerator: keys split KS ways (thread: split ks, column kj), then combined
+        const int ks = tid / DV, kj = tid % DV;
         float acc = 0.f;
-        for (int i = hrg; i < nkeys; i += NRG) {
+        for (int i = ks; i < nkeys; i += KS) {
             const T* vr = i < nwin ? wvv + (int64_t)((t - i) % eta) * DV : cv + (int64_t)(i - nwin) * DV;
-            acc = fmaf(sc[i], IO<T>::ld(vr, hj), acc);
+            acc = fmaf(sc[i], IO<T>::ld(vr, kj), acc);
         }
-        red[hrg * DV + hj] = acc;
+        red[ks * DV + kj] = acc;
         __syncthreads();
         if (tid < DV) {
             float num = 0.f;
 #pragma unroll
-            for (int r = 0; r < NRG; ++r) num += red[r * DV + tid];
+            for (int r = 0; r < KS; ++r) num += red[r * DV + tid];
             num = fmaf(misc[1], lin[tid], num);
             const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
             IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
@@ -376,8 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     }
 
     // ---- 8. write back H, s, header ----
-#pragma unroll
-    for (int r = 0; r < HR; ++r) Hg[(hrg * HR + r) * DV + hj] = hreg[r];
+    h_store<D, DV>(Hg, hreg, warp, lane);
     if (warp == kEvWarp && lane < kSG) slot_store<D>(sg, sub, s_reg);
     if (tid == 0) {
         hdr[HDR_T] = t + 1;
@@ -406,7 +407,7 @@ __device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
 template <int D, int DV, typename T>
 struct FastSmem {
     static constexpr int DK = D;
-    static constexpr int NRG = kThreads / DV;
+    static constexpr int NRG = Shape<D, DV>::NRG;   // H row groups (partials)
     // byte offsets (16-byte aligned)
     static constexpr size_t W = 0;                                          // [D/2][DK+1] f32
     static constexpr size_t CPHI = (W + 4 * (D / 2) * w_stride<DK>() + 15) / 16 * 16;  // [64][D] f32
@@ -437,7 +438,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     using S = Shape<D, DV>;
     using M = FastSmem<D, DV, T>;
     constexpr int DK = D;
-    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, HC = S::HC;
+    constexpr int KS = kThreads / DV;        // key splits of the output numerator
     constexpr int kEvWarp = kDecWarps - 1;
     extern __shared__ __align__(16) uint8_t smb[];
     float* Ws = reinterpret_cast<float*>(smb + M::W);
@@ -517,10 +519,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         xk[tid] = IO<T>::ld(static_cast<const T*>(a.k) + (int64_t)bh * DK, tid);
     }
     if (tid < DV) xv[tid] = IO<T>::ld(static_cast<const T*>(a.v) + (int64_t)bh * DV, tid);
-    const int hj = tid % DV, hrg = tid / DV;
-    float hreg[HR];
-#pragma unroll
-    for (int r = 0; r < HR; ++r) hreg[r] = Hg[(hrg * HR + r) * DV + hj];
+    float hreg[HR * HC];
+    h_load<D, DV>(hreg, Hg, warp, lane);
     // slot role (one pass: lambda <= 64)
     const int sl = tid / kSG, sub = tid % kSG;
     const bool live = sl < nc;
@@ -557,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) phk[lane + 32 * m] = ph[m];
     }
-    if (nxt) red[hrg * DV + hj] = h_partial<D, DV>(phn, hreg, hrg);
+    if (nxt) h_partial_store<D, DV>(red, phn, hreg, warp, lane);
     float ve[PV], zn_prev = 0.f;
     if (warp == kEvWarp) {
         uint32_t ehi = kNoKey, elo = kNoKey;
@@ -608,7 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const int slot_new = (ev && !write) ? nc : (wsel >= 0 ? wsel : -1);
     const int nc_after = (ev && !write) ? nc + 1 : nc;
     if (write) {
-        h_update<D, DV>(hreg, wphi, IO<T>::ld(wvT, hj), hrg);
+        float vh[HC];
+        h_cols<DV, T>(wvT, lane, vh);
+        h_update<D, DV>(hreg, wphi, vh, warp);
         if (warp == kEvWarp && lane < kSG) {
             float wp[PD], sr[PD];
             slot_load<D>(wphi, sub, wp);
@@ -686,7 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         acc += __shfl_xor_sync(kFull, acc, 4);
         if (i < nkeys && sub == 0) sc[i] = acc * scale;
     }
-    red2[hrg * DV + hj] = h_partial<D, DV>(phq, hreg, hrg);
+    h_partial_store<D, DV>(red2, phq, hreg, warp, lane);
     __syncthreads();
     if (warp == 0) {
         float m = -INFINITY;
@@ -720,34 +722,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     __syncthreads();
     {
+        // numerator: keys split KS ways (thread: split ks, column kj), then combined
+        const int ks = tid / DV, kj = tid % DV;
         float accs[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = hrg; i < nkeys; i += NRG) {
+        for (int i = ks; i < nkeys; i += KS) {
             float vj;
             if (i == 0) {
-                vj = xv[hj];
+                vj = xv[kj];
             } else if (i < nwin) {
-                vj = IO<T>::ld(rv_s + (size_t)((t - i) % eta) * DV, hj);
+                vj = IO<T>::ld(rv_s + (size_t)((t - i) % eta) * DV, kj);
             } else {
                 const int j = i - nwin;
-                vj = IO<T>::ld(j == slot_new ? rv_s + (size_t)ring * DV : cv_s + (size_t)j * DV, hj);
+                vj = IO<T>::ld(j == slot_new ? rv_s + (size_t)ring * DV : cv_s + (size_t)j * DV, kj);
             }
-            accs[(i / NRG) & 3] = fmaf(sc[i], vj, accs[(i / NRG) & 3]);
+            accs[(i / KS) & 3] = fmaf(sc[i], vj, accs[(i / KS) & 3]);
         }
-        red[hrg * DV + hj] = (accs[0] + accs[1]) + (accs[2] + accs[3]);
+        red[ks * DV + kj] = (accs[0] + accs[1]) + (accs[2] + accs[3]);
     }
     __syncthreads();
     if (tid < DV) {
         float num = 0.f;
 #pragma unroll
-        for (int r = 0; r < NRG; ++r) num += red[r * DV + tid];
+        for (int r = 0; r < KS; ++r) num += red[r * DV + tid];
         num = fmaf(misc[1], lin[tid], num);
         const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
         IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
     }
 
     // ---- 5. write back ----
-#pragma unroll
-    for (int r = 0; r < HR; ++r) Hg[(hrg * HR + r) * DV + hj] = hreg[r];
+    h_store<D, DV>(Hg, hreg, warp, lane);
     if (sl < nc_after) {
         float* dst = cN + (size_t)sl * DV;
 #pragma unroll
@@ -810,7 +813,7 @@ cudaError_t launch_decode_t(const Dims& d, const DecArgs& a, cudaStream_t st) {
     cudaError_t fe = cudaSuccess;
     if (launch_decode_fast<D, DV, T>(d, a, st, &fe)) return fe;
     constexpr int DK = D;
-    constexpr int NRG = kThreads / DV;
+    constexpr int NRG = Shape<D, DV>::NRG;
     const size_t floats = (D / 2) * w_stride<DK>() + 4 * DK + 2 * DV + 4 * D + DV + NRG * DV + 2 * DV +
                           (d.eta + d.lam + 1) + 2 * (kDecWarps + 2) + 16;
     const size_t smem = sizeof(float) * floats + 64;

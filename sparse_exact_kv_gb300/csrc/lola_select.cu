@@ -12,7 +12,7 @@
 //   * cache slots live in registers, 8 lanes per slot, 4 slots per warp, 64 per CTA; a
 //     write w costs each slot g = phi_w . phi_i, N += g v_w, z += g (exact: H changes by
 //     a rank-1 term);
-//   * each CTA holds a replica of H in registers (32 or 8 entries per thread) to compute
+//   * each CTA holds a replica of H in registers (8 rows x 4 columns, or 4 x 2, per thread) to compute
 //     the next evictee's H^T phi one step ahead and to emit the chunk snapshots;
 //   * the evictee is finished in two parts: right after the previous decision the first
 //     DV/32 warps sum the H^T phi partials and add the last write's correction, one column
@@ -115,12 +115,19 @@ template <int D, int DV, bool CLUSTER, typename T>
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     using S = Shape<D, DV>;
     using M = SelSmem<D, DV, T>;
-    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR;
+    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, HC = S::HC;
     constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
-    constexpr int kEvWarp = kSelWarps - 1;         // scores the evictee and holds s
-    constexpr int kHelpWarp = 0;                   // builds the evictee's N
-    constexpr int kVvWarp = 1;                     // computes the next evictee's |v|^2
-    constexpr int kHandoff = 2 * kWarp;            // threads on named barrier 1
+    // Evictee roles: warps 0 .. kHelp-1 sum the H^T phi partials (one column per lane) and
+    // warp 0 also forms the previous write's gram with the evictee; warp kSWarp holds s
+    // and forms the next evictee's z'; warp kVvWarp its |v|^2; the last warp corrects N
+    // and z by the write and scores the evictee.  Named barrier 1 hands the partial sums
+    // and the gram to the last warp.
+    constexpr int kEvWarp = kSelWarps - 1;
+    constexpr int kHelp = DV / kWarp;
+    constexpr int kSWarp = kSelWarps - 2;
+    constexpr int kVvWarp = kSelWarps - 3;
+    constexpr int kHandoff = (kHelp + 1) * kWarp;  // threads on named barrier 1
+    static_assert(kHelp < kVvWarp, "roles");
     constexpr bool kPackV = sizeof(T) == 2;        // bfloat16 slot values stay in registers
     constexpr int VW = SlotWords<DV, T>::kWords;
 
@@ -135,8 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ __align__(16) float zero_phi[D];      // the "nothing written" winner
     __shared__ __align__(16) T zero_v[DV];
     __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
-    __shared__ __align__(16) float nbuf[2][DV];      // the current evictee's N
-    __shared__ float zbuf[2], gbuf[2], vvbuf[4];
+    __shared__ __align__(16) float npart[2][DV];     // the evictee's summed partials
+    __shared__ __align__(16) float nbuf[2][DV];      // the evictee's N (for its move into a slot)
+    __shared__ float zbuf[2], gbuf[2], zpbuf[2], vvbuf[4];
     __shared__ uint2 wkey[2][kSelWarps + 1];         // per-warp minima; [16] = the evictee
     __shared__ uint2 exch[2][kMaxCluster];
     __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
@@ -171,13 +179,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     };
 
     // H role
-    const int hj = tid % DV, hrg = tid / DV;
-    float h[HR];
+    float h[HR * HC];
 #pragma unroll
-    for (int r = 0; r < HR; ++r) h[r] = 0.f;
-    // evictee warp: the pending evictee's z'
-    float zpend = 0.f;
+    for (int r = 0; r < HR * HC; ++r) h[r] = 0.f;
     if (tid < D) s_sm[tid] = 0.f;
+    if (tid < 2) zpbuf[tid] = 0.f;    // z' against the empty memory
 
     const float* phiK = a.phiK + (int64_t)bh * n * D;
     const int64_t vrow0 = (int64_t)bh * n;
@@ -250,15 +256,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         return Win{wbuf_phi, wbuf_v};
     };
 
-    // Slots and H absorb the previous step's write (an exact zero update when nothing was
-    // written, so the common path has no branch; an empty slot has phi = 0, hence g = 0).
-    auto absorb = [&](const Win& w) {
+    // Slots, then H, absorb the previous step's write (an exact zero update when nothing
+    // was written, so the common path has no branch; an empty slot has phi = 0, g = 0).
+    auto absorb_slot = [&](const Win& w) {
         const float g = slot_gram<D>(w.phi, sphi, sub);
         slot_axpy_io<DV, T>(sN, g, w.v, sub);
         sz += g;
-        h_update<D, DV>(h, w.phi, IO<T>::ld(w.v, hj), hrg);
     };
-    // s absorbs it too (evictee warp, lanes 0-7 hold s in the slot layout)
+    auto absorb_h = [&](const Win& w) {
+        float vh[HC];
+        h_cols<DV, T>(w.v, lane, vh);
+        h_update<D, DV>(h, w.phi, vh, warp);
+    };
+    // s absorbs it too (warp kSWarp, lanes 0-7 hold s in the slot layout)
     auto absorb_s = [&](const Win& w) {
         if (lane < kSG) {
             float wp[PD], sr[PD];
@@ -277,35 +287,26 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         const bool ev = t >= eta;
         const Win W = winner(prev_write, t - 1);
 
-        // ---- helper warp: the evictee's N = (sum of the H^T phi partials against the
-        //      memory before the previous write) + that write's correction, one column per
-        //      lane and pass (the per-element operation order of slot_reduce_partials and
-        //      slot_axpy) ----
-        if (warp == kHelpWarp && ev) {
-            float g = 0.f;
-            if (prev_write) {
-                float ph[PD];
-                slot_load<D>(ebuf[t & (kNEB - 1)], sub, ph);
-                g = slot_gram<D>(W.phi, ph, sub);
+        // ---- helper warps: the evictee's partials summed in row-group order (column j per
+        //      lane; the per-element order of slot_reduce_partials); warp 0: the gram of the
+        //      previous write with the evictee ----
+        if (warp < kHelp && ev) {
+            if (warp == 0) {
+                float g = 0.f;
+                if (prev_write) {
+                    float ph[PD];
+                    slot_load<D>(ebuf[t & (kNEB - 1)], sub, ph);
+                    g = slot_gram<D>(W.phi, ph, sub);
+                }
+                if (lane == 0) gbuf[t & 1] = g;
             }
-            const float* r = &red[t & 1][0][0];
-#pragma unroll
-            for (int q = 0; q < DV / kWarp; ++q) {
-                const int j = q * kWarp + lane;
-                float acc = r[j];
-#pragma unroll
-                for (int rg = 1; rg < NRG; ++rg) acc += r[rg * DV + j];
-                if (prev_write) acc = __fmaf_rn(g, IO<T>::ld(W.v, j), acc);
-                nbuf[t & 1][j] = acc;
-            }
-            if (lane == 0) gbuf[t & 1] = g;
+            const int j = warp * kWarp + lane;
+            npart[t & 1][j] = reduce_partials_col<D, DV>(&red[t & 1][0][0], j);
             named_arrive(kHandoff);
         }
 
-        // ---- every warp: absorb the previous write, the next evictee's H^T phi partials
-        //      (against the memory before step t), slot SREs, per-warp minimum ----
-        absorb(W);
-        red[(t + 1) & 1][hrg][hj] = h_partial<D, DV>(ebuf[(t + 1) & (kNEB - 1)], h, hrg);
+        // ---- every warp: slots absorb the previous write; slot SREs; per-warp minimum ----
+        absorb_slot(W);
         {
             float vr[PV];
             slot_v(vr);
@@ -322,30 +323,45 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             }
         }
 
-        // ---- evictee warp: s absorbs the write; score the evictee of step t (its N from
-        //      the helper warp, z' from step t - 1 plus the previous write's gram); the
-        //      next evictee's z' against s before step t's write ----
+        // ---- last warp: the evictee of step t.  N = partials + g v_w (slot_axpy's order),
+        //      z = z' + g, then its SRE with the arithmetic of a slot ----
         if (warp == kEvWarp) {
-            absorb_s(W);
             uint32_t ehi = kNoKey, elo = kNoKey;
             if (ev) {
                 float Ne[PV], ve[PV];
                 named_sync(kHandoff);
-                slot_load<DV>(nbuf[t & 1], sub, Ne);
-                const float ze = prev_write ? zpend + gbuf[t & 1] : zpend;
+                slot_load<DV>(npart[t & 1], sub, Ne);
+                float ze = zpbuf[t & 1];
+                if (prev_write) {
+                    const float g = gbuf[t & 1];
+                    slot_axpy_io<DV, T>(Ne, g, W.v, sub);
+                    ze += g;
+                }
                 slot_load_io<DV, T>(evraw[t & (kNEB - 1)], sub, ve);
                 const float es = slot_sre2<DV>(Ne, ze, ve, vvbuf[t & 3]);
+                if (lane < kSG) slot_store<DV>(nbuf[t & 1], sub, Ne);
                 if (lane == 0) zbuf[t & 1] = ze;
                 ehi = key_hi(es);
                 elo = key_lo(t - eta, kEvCode);
             }
+            if (lane == 0) wkey[t & 1][kSelWarps] = make_uint2(ehi, elo);
+        }
+        // ---- warp kSWarp: s absorbs the write; the next evictee's z' against s before
+        //      step t's write ----
+        if (warp == kSWarp) {
+            absorb_s(W);
             if (t + 1 - eta >= 0) {
                 float sr[PD];
                 slot_load<D>(s_sm, sub, sr);
-                zpend = slot_gram<D>(ebuf[(t + 1) & (kNEB - 1)], sr, sub);
+                const float zp = slot_gram<D>(ebuf[(t + 1) & (kNEB - 1)], sr, sub);
+                if (lane == 0) zpbuf[(t + 1) & 1] = zp;
             }
-            if (lane == 0) wkey[t & 1][kSelWarps] = make_uint2(ehi, elo);
         }
+
+        // ---- every warp: H absorbs the write; the next evictee's H^T phi partials against
+        //      the memory before step t's write ----
+        absorb_h(W);
+        h_partial_store<D, DV>(&red[(t + 1) & 1][0][0], ebuf[(t + 1) & (kNEB - 1)], h, warp, lane);
 
         // chunk-start snapshot of the memory before step t
         if (t == snap_next) {
@@ -353,10 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             snap_next += a.chunk;
             ++snap_c;
             if (rank == 0) {
-                float* sh = a.snapH + ((int64_t)bh * a.nck + c) * D * DV;
-#pragma unroll
-                for (int r = 0; r < HR; ++r) sh[(hrg * HR + r) * DV + hj] = h[r];
-                if (warp == kEvWarp && lane < kSG) {
+                h_store<D, DV>(a.snapH + ((int64_t)bh * a.nck + c) * D * DV, h, warp, lane);
+                if (warp == kSWarp && lane < kSG) {
                     float sr[PD];
                     slot_load<D>(s_sm, sub, sr);
                     slot_store<D>(a.snapS + ((int64_t)bh * a.nck + c) * D, sub, sr);
@@ -421,8 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     }
     const bool last_write = d_write;
     const Win WL = winner(last_write, n - 1);
-    absorb(WL);
-    if (warp == kEvWarp) absorb_s(WL);
+    absorb_slot(WL);
+    absorb_h(WL);
+    if (warp == kSWarp) absorb_s(WL);
 
     // ---- export the memory after token n-1 into the state record ----
     char* rec = a.state + (int64_t)bh * a.L.head_bytes;
@@ -436,21 +451,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             hdr[HDR_NWRITTEN] = n_written;
             hdr[HDR_STATUS] = 0;
         }
-        float* Hs = reinterpret_cast<float*>(rec + a.L.H);
-#pragma unroll
-        for (int r = 0; r < HR; ++r) Hs[(hrg * HR + r) * DV + hj] = h[r];
+        h_store<D, DV>(reinterpret_cast<float*>(rec + a.L.H), h, warp, lane);
+        if (warp == kSWarp && lane < kSG) {
+            float sr[PD];
+            slot_load<D>(s_sm, sub, sr);
+            slot_store<D>(reinterpret_cast<float*>(rec + a.L.s), sub, sr);
+        }
         if (warp == kEvWarp) {
-            if (lane < kSG) {
-                float sr[PD];
-                slot_load<D>(s_sm, sub, sr);
-                slot_store<D>(reinterpret_cast<float*>(rec + a.L.s), sub, sr);
-            }
             // the next evictee (token n - eta): N against the memory after token n - 1
             if (eta > 0 && n - eta >= 0) {
                 const float* eb = ebuf[n & (kNEB - 1)];
                 float Ne[PV];
                 slot_reduce_partials<D, DV>(&red[n & 1][0][0], sub, Ne);
-                float ze = zpend;
+                float ze = zpbuf[n & 1];
                 if (last_write) {
                     float ph[PD];
                     slot_load<D>(eb, sub, ph);
