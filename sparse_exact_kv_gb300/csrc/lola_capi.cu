@@ -119,14 +119,17 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
         o = align256(o + bytes);
         return r;
     };
-    w.phiK = reinterpret_cast<float*>(take(4 * BH * n * d.D));
-    w.phiQ = reinterpret_cast<float*>(take(4 * BH * n * d.D));
+    // The tensor-core output path reads phi(Q), phi(K) and the H snapshots in bf16 only;
+    // the float32 path reads float32 copies.  phi(K) in float32 is always kept (selection).
     const bool tc = output_tc_supported(d);
+    w.phiK = reinterpret_cast<float*>(take(4 * BH * n * d.D));
+    w.phiQ = reinterpret_cast<float*>(tc ? nullptr : take(4 * BH * n * d.D));
     w.phiKb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * n * d.D) : nullptr);
     w.phiQb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * n * d.D) : nullptr);
     w.wstep = reinterpret_cast<int32_t*>(take(4 * BH * n));
     w.wpos = reinterpret_cast<int32_t*>(take(4 * BH * n));
-    w.snapH = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D * d.dv));
+    w.snapH = reinterpret_cast<float*>(tc ? nullptr : take(4 * BH * w.nck * d.D * d.dv));
+    w.snapHb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * w.nck * d.D * d.dv) : nullptr);
     w.snapS = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D));
     w.snapC = reinterpret_cast<int32_t*>(take(4 * BH * w.nck * (int64_t)(d.lam > 0 ? d.lam : 1)));
     w.slotpos = reinterpret_cast<int32_t*>(take(4 * BH * (int64_t)(d.lam > 0 ? d.lam : 1)));

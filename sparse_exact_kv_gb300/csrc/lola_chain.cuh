@@ -89,6 +89,24 @@ __device__ __forceinline__ void h_store(float* Hm, const float* h, int w, int l)
 #pragma unroll
     for (int r = 0; r < S::HR; ++r) h_vec_store<S::HC>(Hm + (int64_t)(w * S::HR + r) * DV + l * S::HC, h + r * S::HC);
 }
+// the same block rounded to bf16 (round to nearest even)
+template <int D, int DV>
+__device__ __forceinline__ void h_store_bf16(__nv_bfloat16* Hm, const float* h, int w, int l) {
+    using S = Shape<D, DV>;
+#pragma unroll
+    for (int r = 0; r < S::HR; ++r) {
+        __nv_bfloat16* dst = Hm + (int64_t)(w * S::HR + r) * DV + l * S::HC;
+        const float* x = h + r * S::HC;
+        const __nv_bfloat162 b0 = __floats2bfloat162_rn(x[0], x[1]);
+        if constexpr (S::HC == 4) {
+            const __nv_bfloat162 b1 = __floats2bfloat162_rn(x[2], x[3]);
+            *reinterpret_cast<uint2*>(dst) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&b0), *reinterpret_cast<const uint32_t*>(&b1));
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = *reinterpret_cast<const uint32_t*>(&b0);
+        }
+    }
+}
 // this lane's HC entries of a value row (float32 or bfloat16, widened exactly)
 template <int DV, typename T>
 __device__ __forceinline__ void h_cols(const T* v, int l, float* out) {

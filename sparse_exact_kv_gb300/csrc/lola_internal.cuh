@@ -58,12 +58,13 @@ enum : int32_t { ST_SLOT_OVERFLOW = 1, ST_BAD_STATE = 2, ST_TIMEOUT = 4 };
 // ---------------------------------------------------------------------------------
 struct Workspace {
     float* phiK;       // [BH][n][D]    phi(k_t), float32 (selection precision)
-    float* phiQ;       // [BH][n][D]    phi(q_t)
+    float* phiQ;       // [BH][n][D]    phi(q_t) (float32 output path only)
     __nv_bfloat16* phiKb;  // [BH][n][D] bf16 copies for the tensor-core output kernel (bf16 mode)
     __nv_bfloat16* phiQb;
     int32_t* wstep;    // [BH][n]       step at which token j was written, -1 never
     int32_t* wpos;     // [BH][n]       position written at step t, -1 none
-    float* snapH;      // [BH][nck][D*dv]  H before the first step of each chunk
+    float* snapH;      // [BH][nck][D*dv]  H before the first step of each chunk (float32 path)
+    __nv_bfloat16* snapHb;  // the same in bf16 (tensor-core path: its MMA operand)
     float* snapS;      // [BH][nck][D]
     int32_t* snapC;    // [BH][nck][lam]   cache slot positions before each chunk (-1 empty)
     int32_t* slotpos;  // [BH][lam]        final slot positions (export scratch)

@@ -8,18 +8,21 @@
 // j <= t < w_j and in the linear memory iff w_j <= t.  From the snapshot taken before
 // the tile's chunk start c0 -- (H_c, s_c) and the cache positions -- the tile's pool is
 // cache(c0) ∪ [c0 - eta, tile end), and for every query t of the tile
-//   O_soft = sum_pool [j <= t < w_j] exp(s_tj - m) v_j,      l_soft = sum of the weights,
+//   O_soft = sum_pool [j <= t < w_j] 2^(s_tj - m) v_j,      l_soft = sum of the weights,
 //   O_lin  = phi(q_t)^T H_c + sum_pool [c0 <= w_j <= t] (phi(q_t) . phi(k_j)) v_j,
 //   l_lin  = phi(q_t)^T s_c + sum of those linear weights,
-//   y_t    = (O_soft + e^{-m} O_lin) / (l_soft + e^{-m} l_lin).
+//   y_t    = (O_soft + 2^{-m} O_lin) / (l_soft + 2^{-m} l_lin),
+// with scores s_tj = q_t . k_j log2(e) / sqrt(d_k) in log2 units.
 // The tensor cores compute S = Q K^T, L = phi(Q) phi(K)^T (per 64-key pool block),
 // O_soft += P_soft V, O_lin += P_lin V and O_lin = phi(Q) H_c, all bf16 x bf16 -> fp32 in
-// TMEM (M = 128: TMEM lane = query row).  128 threads (one per query row) read S and L
-// from TMEM, apply the masks and an online maximum m that is raised lazily (the
-// accumulator O_soft is rescaled in TMEM only when the block maximum exceeds m by more
-// than 8), and write the bf16 weights back to shared memory for the P V products.
-// Operands are gathered with cp.async into 128-byte-swizzled tiles (pool keys are
-// scattered: the cache positions come from the snapshot).
+// TMEM (M = 128: TMEM lane = query row).  Warps 0-3 (one thread per query row) read S and
+// L from TMEM, apply the masks (each key's visible rows are precomputed once per block as
+// three row bounds) and an online maximum m that is raised lazily (O_soft is rescaled in
+// TMEM only when the block maximum exceeds m by more than 2^12), and write the bf16 weights
+// to shared memory for the P V products.  Meanwhile warps 4-7 gather the next block's
+// keys with cp.async into the other half of a two-stage buffer (the pool keys are
+// scattered: the cache positions come from the snapshot).  One commit per block covers
+// that block's P V products and the next block's S, L.
 #include "lola_internal.cuh"
 #include "lola_tc.cuh"
 
@@ -28,23 +31,27 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreadsTc = 256;
+constexpr int kThreadsTc = 256;          // warps 0-3: one query row per thread; warps 4-7: gathers
 constexpr int kTM = 128;                 // query rows per tile (MMA M)
 constexpr int kBN = 64;                  // pool keys per block (MMA N of S, L; K of P V)
 constexpr int kD = 128;                  // d_k = d_v = D
-constexpr float kRescale = 8.0f;         // lazy rescale threshold (natural log units)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kRescale2 = 12.0f;       // lazy rescale threshold (log2 units)
 constexpr uint64_t kWaitNs = 1000000000ull;  // an MMA group that has not completed in 1 s is an error
 
-// shared-memory map (bytes from a 1024-aligned base)
+// shared-memory map (bytes from a 1024-aligned base).  Key blocks are double-buffered;
+// stage 1's K and phi(K) tiles reuse the H_c tile once phi(Q) H_c has been issued (the
+// first wait covers it).
 constexpr int SQ = 0;                    // Q tile      K-major, 2 atoms x [128 x 64]
 constexpr int SPQ = 32768;               // phi(Q) tile K-major
-constexpr int SH = 65536;                // H_c         MN-major [K = D x N = d_v]
-constexpr int SK = 98304;                // K block     K-major, 2 atoms x [64 x 64]
-constexpr int SPK = 114688;              // phi(K) block
-constexpr int SV = 131072;               // V block     MN-major [K = 64 x N = d_v]
-constexpr int SPS = 147456;              // soft weights K-major [128 x 64]
-constexpr int SPL = 163840;              // linear weights
-constexpr int SEND = 180224;
+constexpr int SH = 98304;                // H_c         MN-major [K = D x N = d_v]
+// stage st: K block K-major, 2 atoms x [64 x 64]; phi(K) block; V block MN-major [64 x d_v]
+__device__ __forceinline__ uint32_t SK(int st) { return st ? 98304u : 65536u; }
+__device__ __forceinline__ uint32_t SPK(int st) { return st ? 114688u : 81920u; }
+__device__ __forceinline__ uint32_t SV(int st) { return st ? 147456u : 131072u; }
+constexpr int SPS = 163840;              // soft weights K-major [128 x 64]
+constexpr int SPL = 180224;              // linear weights
+constexpr int SEND = 196608;
 // TMEM columns
 constexpr uint32_t TS = 0, TL = 64, TOS = 128, TOL = 256;
 
@@ -56,9 +63,8 @@ struct TcArgs {
     __nv_bfloat16* Y;
     const __nv_bfloat16* phiQb;  // [BH][n][D] bf16
     const __nv_bfloat16* phiKb;
-    const float* phiQ;           // [BH][n][D] float32 (for phi(q)^T s_c)
     const int32_t* wstep;
-    const float* snapH;
+    const __nv_bfloat16* snapHb; // [BH][nck][D][DV] bf16
     const float* snapS;
     const int32_t* snapC;
     char* state;                 // per-head status words (timeouts)
@@ -66,13 +72,22 @@ struct TcArgs {
     int* abort_flag;             // set by any CTA whose wait timed out; later CTAs skip their work
 };
 
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void producers_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
     __shared__ uint64_t mbar;
     __shared__ uint32_t tmem_base;
-    __shared__ int kpos[kBN], kw[kBN];
+    __shared__ int kpos[2][kBN];
+    __shared__ uint32_t kinfo[2][kBN];   // per key: soft rows [lo, hi), linear rows >= llo (bytes 0-2)
+    __shared__ float sS[kD];
 
     const int tid = threadIdx.x, warp = tid / 32;
     const int bh = blockIdx.y;
@@ -85,12 +100,46 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
     const int64_t row0 = (int64_t)bh * n;
     const int32_t* cpos = a.snapC + ((int64_t)bh * a.nck + c) * a.lam;
     const int32_t* wst = a.wstep + row0;
-    const float scale = 1.0f / sqrtf((float)kD);
 
     if (tid == 0) mbar_init(smem_u32(&mbar), 1);
     if (warp == 0) tmem_alloc<512>(smem_u32(&tmem_base));
 
-    // ---- stage Q, phi(Q) (rows t0 .. t0 + 127; beyond n: zero) ----
+    // ---- producers (warps 4-7): the keys of block bb and their rows into stage st ----
+    const int ptid = tid - 128;
+    auto gather = [&](int bb, int st) {
+        if (ptid < kBN) {
+            const int u = bb * kBN + ptid;
+            int p = -1;
+            if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
+            const int w = p >= 0 ? wst[p] : -1;
+            // row r = t - t0 sees key p exactly iff lo <= r < hi, linearly iff r >= llo
+            const int lo = p < 0 ? 255 : min(max(p - t0, 0), 255);
+            const int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
+            const int llo = (p < 0 || w < c0) ? 255 : min(max(w - t0, 0), 255);
+            kpos[st][ptid] = p;
+            kinfo[st][ptid] = (uint32_t)lo | ((uint32_t)hi << 8) | ((uint32_t)llo << 16);
+        }
+        producers_sync();
+        for (int i = ptid; i < kBN * 16; i += 128) {
+            const int r = i >> 4, c16 = i & 15;
+            const int p = kpos[st][r];
+            const uint32_t off = (c16 >> 3) * 8192 + kmaj_chunk(r, c16 & 7);
+            const uint32_t voff = mnmaj_chunk(r, c16 * 8, kBN);
+            if (p >= 0) {
+                cp_async16(sb + SK(st) + off, a.K + (row0 + p) * kD + c16 * 8);
+                cp_async16(sb + SPK(st) + off, a.phiKb + (row0 + p) * kD + c16 * 8);
+                cp_async16(sb + SV(st) + voff, a.V + (row0 + p) * kD + c16 * 8);
+            } else {
+                *reinterpret_cast<uint4*>(sm + SK(st) + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + SPK(st) + off) = make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(sm + SV(st) + voff) = make_uint4(0, 0, 0, 0);
+            }
+        }
+        cp_async_wait_all();
+        fence_async_smem();
+    };
+
+    // ---- stage Q, phi(Q) (rows t0 .. t0 + 127; beyond n: zero), H_c, s_c; block 0 ----
     for (int i = tid; i < kTM * 16; i += kThreadsTc) {
         const int r = i >> 4, c16 = i & 15;
         const uint32_t off = (c16 >> 3) * 16384 + kmaj_chunk(r, c16 & 7);
@@ -103,53 +152,56 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
             *reinterpret_cast<uint4*>(sm + SPQ + off) = make_uint4(0, 0, 0, 0);
         }
     }
-    // ---- stage H_c as bf16, MN-major [k = feature][n = value dim] ----
     {
-        const float* sh = a.snapH + ((int64_t)bh * a.nck + c) * kD * kD;
+        const __nv_bfloat16* sh = a.snapHb + ((int64_t)bh * a.nck + c) * kD * kD;
         for (int i = tid; i < kD * (kD / 8); i += kThreadsTc) {
             const int k = i / (kD / 8), n8 = (i % (kD / 8)) * 8;
-            const float4 f0 = *reinterpret_cast<const float4*>(sh + k * kD + n8);
-            const float4 f1 = *reinterpret_cast<const float4*>(sh + k * kD + n8 + 4);
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(f0.x, f0.y), b1 = __floats2bfloat162_rn(f0.z, f0.w);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(f1.x, f1.y), b3 = __floats2bfloat162_rn(f1.z, f1.w);
-            uint4 u;
-            u.x = *reinterpret_cast<uint32_t*>(&b0);
-            u.y = *reinterpret_cast<uint32_t*>(&b1);
-            u.z = *reinterpret_cast<uint32_t*>(&b2);
-            u.w = *reinterpret_cast<uint32_t*>(&b3);
-            *reinterpret_cast<uint4*>(sm + SH + mnmaj_chunk(k, n8, kD)) = u;
+            cp_async16(sb + SH + mnmaj_chunk(k, n8, kD), sh + k * kD + n8);
         }
     }
-    // per-row state (threads 0..127 own query row t0 + tid)
-    const int row = tid;
-    const int t = t0 + row;
-    float m_run = -INFINITY, l_soft = 0.f, l_lin = 0.f;
-    if (tid < kTM && t < n) {
-        const float* pq = a.phiQ + (row0 + t) * kD;
-        const float* ss = a.snapS + ((int64_t)bh * a.nck + c) * kD;
-        float acc = 0.f;
-        for (int k = 0; k < kD; k += 4) {
-            const float4 p = *reinterpret_cast<const float4*>(pq + k);
-            const float4 s = *reinterpret_cast<const float4*>(ss + k);
-            acc = fmaf(p.x, s.x, acc);
-            acc = fmaf(p.y, s.y, acc);
-            acc = fmaf(p.z, s.z, acc);
-            acc = fmaf(p.w, s.w, acc);
-        }
-        l_lin = acc;
-    }
+    if (tid < kD) sS[tid] = a.snapS[((int64_t)bh * a.nck + c) * kD + tid];
+    if (warp >= 4) gather(0, 0);
     cp_async_wait_all();
     fence_async_smem();
     fence_before();
     __syncthreads();
     fence_after();
+
+    // per-row state (threads 0..127 own query row t0 + tid); scores in log2 units
+    const int row = tid;
+    const int t = t0 + row;
+    const float c2 = kLog2e / sqrtf((float)kD);
+    float m_run = -INFINITY, l_soft = 0.f, l_lin = 0.f;
+    if (tid < kTM) {
+        // phi(q_t)^T s_c from the bf16 phi(Q) tile, in feature order
+        float acc = 0.f;
+#pragma unroll
+        for (int c16 = 0; c16 < 16; ++c16) {
+            const uint4 x = *reinterpret_cast<const uint4*>(sm + SPQ + (c16 >> 3) * 16384 + kmaj_chunk(row, c16 & 7));
+            const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc = fmaf(__uint_as_float(wds[q] << 16), sS[c16 * 8 + 2 * q], acc);
+                acc = fmaf(__uint_as_float(wds[q] & 0xffff0000u), sS[c16 * 8 + 2 * q + 1], acc);
+            }
+        }
+        l_lin = acc;
+    }
     const uint32_t tb = tmem_base;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t mb = smem_u32(&mbar);
     uint32_t phase = 0;
     bool bad = __syncthreads_or(*reinterpret_cast<volatile int*>(a.abort_flag) != 0) != 0;
 
-    // O_lin = phi(Q) H_c
+    // O_lin = phi(Q) H_c, then S, L of block 0
+    auto issue_sl = [&](int st) {
+        constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
+        for (int k = 0; k < kD / 16; ++k) {
+            const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
+            mma_bf16(tb + TS, sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK(st) + bo, 16, 1024), id, k > 0);
+            mma_bf16(tb + TL, sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(st) + bo, 16, 1024), id, k > 0);
+        }
+    };
     if (tid == 0 && !bad) {
         constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
         for (int k = 0; k < kD / 16; ++k) {
@@ -157,75 +209,45 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
             const uint64_t bd = sdesc(sb + SH + k * 2048, 16384, 1024);
             mma_bf16(tb + TOL, ad, bd, id, k > 0);
         }
+        issue_sl(0);
+        mma_commit(mb);
     }
 
     for (int b = 0; b < nblk && !bad; ++b) {
-        // ---- gather the block's keys (the previous block's products have completed) ----
-        if (tid < kBN) {
-            const int u = b * kBN + tid;
-            int p = -1;
-            if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
-            kpos[tid] = p;
-            kw[tid] = p >= 0 ? wst[p] : -1;
-        }
-        __syncthreads();
-        for (int i = tid; i < kBN * 16; i += kThreadsTc) {
-            const int r = i >> 4, c16 = i & 15;
-            const int p = kpos[r];
-            const uint32_t off = (c16 >> 3) * 8192 + kmaj_chunk(r, c16 & 7);
-            const uint32_t voff = mnmaj_chunk(r, c16 * 8, kBN);
-            if (p >= 0) {
-                cp_async16(sb + SK + off, a.K + (row0 + p) * kD + c16 * 8);
-                cp_async16(sb + SPK + off, a.phiKb + (row0 + p) * kD + c16 * 8);
-                cp_async16(sb + SV + voff, a.V + (row0 + p) * kD + c16 * 8);
-            } else {
-                *reinterpret_cast<uint4*>(sm + SK + off) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + SPK + off) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + SV + voff) = make_uint4(0, 0, 0, 0);
-            }
-        }
-        cp_async_wait_all();
-        fence_async_smem();
-        fence_before();
-        __syncthreads();
-        fence_after();
-        // ---- S = Q K^T, L = phi(Q) phi(K)^T ----
-        if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
-            for (int k = 0; k < kD / 16; ++k) {
-                const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
-                mma_bf16(tb + TS, sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK + bo, 16, 1024), id, k > 0);
-                mma_bf16(tb + TL, sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK + bo, 16, 1024), id, k > 0);
-            }
-            mma_commit(mb);
-        }
+        const int st = b & 1;
+        // S, L of block b (and the previous P V, and phi(Q) H_c) have completed
         const bool ok = mbar_wait(mb, phase, kWaitNs);
         phase ^= 1;
         fence_after();
-        // ---- masks, online maximum, weights (one thread per query row) ----
-        if (tid < kTM) {
-            // pass 1: the block's maximum visible score
+        if (warp >= 4) {
+            if (b + 1 < nblk) gather(b + 1, st ^ 1);
+        } else {
+            // ---- masks, online maximum (log2 units), weights: one thread per query row ----
+            const uint32_t* ki = kinfo[st];
+            float sv[64];
+            uint32_t vis_s[2] = {0u, 0u};
             float bm = -INFINITY;
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
-                float s[32];
-                tmem_ld32(tb + lane_off + TS + 32 * hlf, s);
+                tmem_ld32(tb + lane_off + TS + 32 * hlf, sv + 32 * hlf);
                 tmem_wait_ld();
 #pragma unroll
                 for (int jj = 0; jj < 32; ++jj) {
-                    const int j = 32 * hlf + jj;
-                    const int p = kpos[j], w = kw[j];
-                    const bool vs = t < n && p >= 0 && p <= t && (w < 0 || w > t);
-                    if (vs) bm = fmaxf(bm, s[jj] * scale);
+                    const uint32_t info = ki[32 * hlf + jj];
+                    const bool vs = row >= (int)(info & 255u) && row < (int)((info >> 8) & 255u);
+                    const float x = sv[32 * hlf + jj] * c2;
+                    sv[32 * hlf + jj] = x;
+                    vis_s[hlf] |= (uint32_t)vs << jj;
+                    bm = vs ? fmaxf(bm, x) : bm;
                 }
             }
             // lazy rescale of O_soft; TMEM accesses stay warp-uniform (factor 1 for the
             // rows that keep their maximum)
             const bool first = bm > m_run && m_run == -INFINITY;
-            const bool need = bm > m_run && m_run != -INFINITY && bm - m_run > kRescale;
+            const bool need = bm > m_run && m_run != -INFINITY && bm - m_run > kRescale2;
             if (first) m_run = bm;
             if (__any_sync(0xffffffffu, need)) {
-                const float f = need ? expf(m_run - bm) : 1.f;
+                const float f = need ? ex2(m_run - bm) : 1.f;
                 l_soft *= f;
                 float o[32];
 #pragma unroll
@@ -239,12 +261,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
                 tmem_wait_st();
                 if (need) m_run = bm;
             }
-            // pass 2: bf16 weights into the K-major [128 x 64] tiles (row = query)
+            const float mr = m_run;
 #pragma unroll
             for (int hlf = 0; hlf < 2; ++hlf) {
-                float s[32], l[32];
-                tmem_ld32(tb + lane_off + TS + 32 * hlf, s);
-                tmem_ld32(tb + lane_off + TL + 32 * hlf, l);
+                float lv[32];
+                tmem_ld32(tb + lane_off + TL + 32 * hlf, lv);
                 tmem_wait_ld();
 #pragma unroll
                 for (int c4 = 0; c4 < 4; ++c4) {
@@ -254,12 +275,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
                         float e[2], g[2];
 #pragma unroll
                         for (int u = 0; u < 2; ++u) {
-                            const int jj = c4 * 8 + 2 * hh + u, j = 32 * hlf + jj;
-                            const int p = kpos[j], w = kw[j];
-                            const bool vs = t < n && p >= 0 && p <= t && (w < 0 || w > t);
-                            const bool vl = t < n && p >= 0 && w >= c0 && w <= t;
-                            e[u] = vs ? expf(s[jj] * scale - m_run) : 0.f;
-                            g[u] = vl ? l[jj] : 0.f;
+                            const int jj = c4 * 8 + 2 * hh + u;
+                            const uint32_t info = ki[32 * hlf + jj];
+                            const bool vs = (vis_s[hlf] >> jj) & 1u;
+                            const bool vl = row >= (int)((info >> 16) & 255u);
+                            e[u] = vs ? ex2(sv[32 * hlf + jj] - mr) : 0.f;
+                            g[u] = vl ? lv[jj] : 0.f;
                         }
                         const __nv_bfloat162 bs = __floats2bfloat162_rn(e[0], e[1]);
                         const __nv_bfloat162 bl = __floats2bfloat162_rn(g[0], g[1]);
@@ -273,31 +294,33 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
                     *reinterpret_cast<uint4*>(sm + SPL + kmaj_chunk(row, c16)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
                 }
             }
+            fence_async_smem();
         }
-        fence_async_smem();
         fence_before();
         bad = __syncthreads_or(!ok) != 0;
         fence_after();
         if (bad) break;
-        // ---- O_soft += P_soft V, O_lin += P_lin V ----
+        // ---- O_soft += P_soft V, O_lin += P_lin V; then S, L of the next block ----
         if (tid == 0) {
             constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
             for (int k = 0; k < kBN / 16; ++k) {
-                const uint64_t vd = sdesc(sb + SV + k * 2048, 8192, 1024);
+                const uint64_t vd = sdesc(sb + SV(st) + k * 2048, 8192, 1024);
                 mma_bf16(tb + TOS, sdesc(sb + SPS + k * 32, 16, 1024), vd, id, (b > 0 || k > 0));
                 mma_bf16(tb + TOL, sdesc(sb + SPL + k * 32, 16, 1024), vd, id, 1);
             }
+            if (b + 1 < nblk) issue_sl(st ^ 1);
             mma_commit(mb);
         }
-        const bool ok2 = mbar_wait(mb, phase, kWaitNs);
-        phase ^= 1;
-        fence_after();
-        bad = __syncthreads_or(!ok2) != 0;
     }
-    // ---- epilogue: y = (O_soft + e^{-m} O_lin) / (l_soft + e^{-m} l_lin) ----
+    if (!bad) {
+        const bool ok = mbar_wait(mb, phase, kWaitNs);
+        fence_after();
+        bad = __syncthreads_or(!ok) != 0;
+    }
+    // ---- epilogue: y = (O_soft + 2^{-m} O_lin) / (l_soft + 2^{-m} l_lin) ----
     if (!bad && tid < kTM) {
         const bool any = m_run != -INFINITY;
-        const float em = any ? expf(-m_run) : 1.f;
+        const float em = any ? ex2(-m_run) : 1.f;
         const float den = any ? fmaf(em, l_lin, l_soft) : l_lin;
         const float inv = t < n ? 1.0f / den : 0.f;
         __nv_bfloat16* y = a.Y + (row0 + (t < n ? t : 0)) * kD;
@@ -350,9 +373,8 @@ cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const vo
     a.Y = static_cast<__nv_bfloat16*>(Y);
     a.phiQb = ws.phiQb;
     a.phiKb = ws.phiKb;
-    a.phiQ = ws.phiQ;
     a.wstep = ws.wstep;
-    a.snapH = ws.snapH;
+    a.snapHb = ws.snapHb;
     a.snapS = ws.snapS;
     a.snapC = ws.snapC;
     a.state = state;

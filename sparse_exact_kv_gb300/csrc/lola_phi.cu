@@ -48,8 +48,10 @@ __global__ void __launch_bounds__(kPhiThreads) phi_kernel(const T* __restrict__ 
 #pragma unroll
         for (int r = 0; r < kRowsPerWarp; ++r) {
             if (rb + r >= r1) break;
+            if (out) {
 #pragma unroll
-            for (int m = 0; m < D / 32; ++m) out[(row + r) * D + lane + 32 * m] = ph[r][m];
+                for (int m = 0; m < D / 32; ++m) out[(row + r) * D + lane + 32 * m] = ph[r][m];
+            }
             if (out_bf16) {
 #pragma unroll
                 for (int m = 0; m < D / 32; ++m) out_bf16[(row + r) * D + lane + 32 * m] = __float2bfloat16_rn(ph[r][m]);

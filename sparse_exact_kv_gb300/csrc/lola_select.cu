@@ -50,7 +50,8 @@ struct SelArgs {
     const void* V;       // io [BH][n][DV]
     int32_t* wpos;       // [BH][n]
     int32_t* wstep;      // [BH][n]
-    float* snapH;        // [BH][nck][D*DV]
+    float* snapH;        // [BH][nck][D*DV] float32, or
+    __nv_bfloat16* snapHb;  // the same in bf16 (exactly one of the two is set)
     float* snapS;        // [BH][nck][D]
     int32_t* snapC;      // [BH][nck][lam]
     int32_t* slotpos;    // [BH][lam]
@@ -369,7 +370,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             snap_next += a.chunk;
             ++snap_c;
             if (rank == 0) {
-                h_store<D, DV>(a.snapH + ((int64_t)bh * a.nck + c) * D * DV, h, warp, lane);
+                if (a.snapHb) h_store_bf16<D, DV>(a.snapHb + ((int64_t)bh * a.nck + c) * D * DV, h, warp, lane);
+                else h_store<D, DV>(a.snapH + ((int64_t)bh * a.nck + c) * D * DV, h, warp, lane);
                 if (warp == kSWarp && lane < kSG) {
                     float sr[PD];
                     slot_load<D>(s_sm, sub, sr);
@@ -594,6 +596,7 @@ cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void*
     a.wpos = ws.wpos;
     a.wstep = ws.wstep;
     a.snapH = ws.snapH;
+    a.snapHb = ws.snapHb;
     a.snapS = ws.snapS;
     a.snapC = ws.snapC;
     a.slotpos = ws.slotpos;

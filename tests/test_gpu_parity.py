@@ -81,18 +81,31 @@ def test_zero_budget_prefill_is_linear_attention(L):
     check_outputs(Y[0, 0], want, "f32")
 
 
+def _bf16_bits_to_f64(t):
+    return (t.view(torch.int16).to(torch.int32) << 16).view(torch.float32).cpu().numpy().astype(np.float64)
+
+
 def test_phi_kernel_matches_oracle_phi(L):
-    """K1 output (left in the prefill workspace) against the float64 feature map."""
+    """K1 output (left in the prefill workspace) against the float64 feature map.  The bf16
+    tensor-core path keeps phi(K) in float32 (selection) and bf16 copies of phi(K), phi(Q)
+    (output MMAs): float32 to 2e-6, each bf16 copy equal to its float32 value rounded to
+    nearest even, phi(Q) in bf16 within half a bf16 ulp of the float64 feature map."""
     x = synth.gauss_inputs(2, 3, 77, 128, 128, "bf16", seed=7)
     _, _, lay = run_prefill(L, x, 8, 8, 16)
     BH, n, D = 6, 77, 128
     ws = lay.workspace
-    nb = 4 * BH * n * D
-    phiK = ws[:nb].view(torch.float32).cpu().numpy().reshape(2, 3, n, D)
-    off = (nb + 255) // 256 * 256
-    phiQ = ws[off:off + nb].view(torch.float32).cpu().numpy().reshape(2, 3, n, D)
+    align = lambda v: (v + 255) // 256 * 256  # noqa: E731
+    nb, nh = 4 * BH * n * D, 2 * BH * n * D
+    phiK_t = ws[:nb].view(torch.float32)
+    phiK = phiK_t.cpu().numpy().reshape(2, 3, n, D)
+    okb = align(nb)
+    phiKb = ws[okb:okb + nh].view(torch.bfloat16)
+    oqb = align(okb + nh)
+    phiQb = _bf16_bits_to_f64(ws[oqb:oqb + nh].view(torch.bfloat16)).reshape(2, 3, n, D)
     np.testing.assert_allclose(phiK, R.phi(x.widened("k"), x.W), rtol=2e-6, atol=1e-8)
-    np.testing.assert_allclose(phiQ, R.phi(x.widened("q"), x.W), rtol=2e-6, atol=1e-8)
+    assert torch.equal(phiKb.cpu(), phiK_t.cpu().to(torch.bfloat16))
+    ref_q = R.phi(x.widened("q"), x.W)
+    np.testing.assert_allclose(phiQb, ref_q, rtol=2.0 ** -8 + 2e-6, atol=1e-8)
 
 
 @pytest.mark.parametrize("eta,lam,chunk,n", [(16, 16, 16, 400), (64, 64, 64, 1000), (8, 200, 32, 600)])
