@@ -15,12 +15,13 @@
 // with scores s_tj = q_t . k_j log2(e) / sqrt(d_k) in log2 units.
 // The tensor cores compute S = Q K^T, L = phi(Q) phi(K)^T (per 64-key pool block),
 // O_soft += P_soft V, O_lin += P_lin V and O_lin = phi(Q) H_c, all bf16 x bf16 -> fp32 in
-// TMEM (M = 128: TMEM lane = query row).  Warps 0-3 (one thread per query row) read S and
-// L from TMEM, apply the masks (each key's visible rows are precomputed once per block as
-// three row bounds) and an online maximum m that is raised lazily (O_soft is rescaled in
-// TMEM only when the block maximum exceeds m by more than 2^12), and write the bf16 weights
-// to shared memory for the P V products.  Meanwhile warps 4-7 gather the next block's
-// keys with cp.async into the other half of a two-stage buffer (the pool keys are
+// TMEM (M = 128: TMEM lane = query row).  Two threads per query row (warps w and w + 4
+// share TMEM lanes) each take half of a block's keys: they read S and L from TMEM, apply
+// the masks (each key's visible rows are precomputed once per block as three row bounds)
+// and an online maximum m that is raised lazily (O_soft is rescaled in TMEM only when the
+// block maximum exceeds m by more than 2^12), and write the bf16 weights to shared memory
+// for the P V products.  Before their half, warps 4-7 start the cp.async gathers of the
+// next block's keys into the other half of a two-stage buffer (the pool keys are
 // scattered: the cache positions come from the snapshot).  One commit per block covers
 // that block's P V products and the next block's S, L.
 #include "lola_internal.cuh"
@@ -31,7 +32,7 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreadsTc = 256;          // warps 0-3: one query row per thread; warps 4-7: gathers
+constexpr int kThreadsTc = 256;          // two threads per query row (warps w and w + 4)
 constexpr int kTM = 128;                 // query rows per tile (MMA M)
 constexpr int kBN = 64;                  // pool keys per block (MMA N of S, L; K of P V)
 constexpr int kD = 128;                  // d_k = d_v = D
@@ -86,8 +87,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
     __shared__ uint64_t mbar;
     __shared__ uint32_t tmem_base;
     __shared__ int kpos[2][kBN];
-    __shared__ uint32_t kinfo[2][kBN];   // per key: soft rows [lo, hi), linear rows >= llo (bytes 0-2)
+    __shared__ __align__(16) uint32_t kinfo[2][kBN];   // per key: soft rows [lo, hi), linear rows >= llo
     __shared__ float sS[kD];
+    __shared__ float bmx[2][kTM];        // the two half-block maxima of each row
+    __shared__ float lsum[2][2][kTM];    // [soft, linear][half][row] partial denominators
 
     const int tid = threadIdx.x, warp = tid / 32;
     const int bh = blockIdx.y;
@@ -135,8 +138,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
                 *reinterpret_cast<uint4*>(sm + SV(st) + voff) = make_uint4(0, 0, 0, 0);
             }
         }
-        cp_async_wait_all();
-        fence_async_smem();
     };
 
     // ---- stage Q, phi(Q) (rows t0 .. t0 + 127; beyond n: zero), H_c, s_c; block 0 ----
@@ -167,12 +168,14 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
     __syncthreads();
     fence_after();
 
-    // per-row state (threads 0..127 own query row t0 + tid); scores in log2 units
-    const int row = tid;
+    // per-row state: thread tid owns query row t0 + (tid & 127) and key half hf = tid >> 7
+    // (pool keys 32 hf .. 32 hf + 31 of every block, output columns 64 hf .. 64 hf + 63);
+    // scores in log2 units
+    const int row = tid & (kTM - 1), hf = tid >> 7;
     const int t = t0 + row;
     const float c2 = kLog2e / sqrtf((float)kD);
     float m_run = -INFINITY, l_soft = 0.f, l_lin = 0.f;
-    if (tid < kTM) {
+    if (hf == 0) {
         // phi(q_t)^T s_c from the bf16 phi(Q) tile, in feature order
         float acc = 0.f;
 #pragma unroll
@@ -219,30 +222,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
         const bool ok = mbar_wait(mb, phase, kWaitNs);
         phase ^= 1;
         fence_after();
-        if (warp >= 4) {
-            if (b + 1 < nblk) gather(b + 1, st ^ 1);
-        } else {
-            // ---- masks, online maximum (log2 units), weights: one thread per query row ----
-            const uint32_t* ki = kinfo[st];
-            float sv[64];
-            uint32_t vis_s[2] = {0u, 0u};
+        const bool prod = warp >= 4 && b + 1 < nblk;
+        if (prod) gather(b + 1, st ^ 1);   // copies land while this block is weighted
+        {
+            // ---- masks, block maximum, weights for keys 32 hf .. 32 hf + 31 ----
+            const uint32_t* ki = kinfo[st] + 32 * hf;
+            float sv[32];
+            uint32_t vis = 0u;
             float bm = -INFINITY;
+            tmem_ld32(tb + lane_off + TS + 32 * hf, sv);
+            tmem_wait_ld();
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                tmem_ld32(tb + lane_off + TS + 32 * hlf, sv + 32 * hlf);
-                tmem_wait_ld();
-#pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const uint32_t info = ki[32 * hlf + jj];
-                    const bool vs = row >= (int)(info & 255u) && row < (int)((info >> 8) & 255u);
-                    const float x = sv[32 * hlf + jj] * c2;
-                    sv[32 * hlf + jj] = x;
-                    vis_s[hlf] |= (uint32_t)vs << jj;
-                    bm = vs ? fmaxf(bm, x) : bm;
-                }
+            for (int jj = 0; jj < 32; ++jj) {
+                const uint32_t info = ki[jj];
+                const bool vs = row >= (int)(info & 255u) && row < (int)((info >> 8) & 255u);
+                vis |= (uint32_t)vs << jj;
+                bm = vs ? fmaxf(bm, sv[jj]) : bm;
             }
-            // lazy rescale of O_soft; TMEM accesses stay warp-uniform (factor 1 for the
-            // rows that keep their maximum)
+            bmx[hf][row] = bm;
+            __syncthreads();
+            bm = fmaxf(bmx[0][row], bmx[1][row]) * c2;
+            // lazy rescale of O_soft (columns 64 hf ..); both threads of a row take the same
+            // decision; TMEM accesses stay warp-uniform (factor 1 for the rows that keep m)
             const bool first = bm > m_run && m_run == -INFINITY;
             const bool need = bm > m_run && m_run != -INFINITY && bm - m_run > kRescale2;
             if (first) m_run = bm;
@@ -251,49 +252,50 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
                 l_soft *= f;
                 float o[32];
 #pragma unroll
-                for (int cc = 0; cc < kD; cc += 32) {
-                    tmem_ld32(tb + lane_off + TOS + cc, o);
+                for (int cc = 0; cc < kD / 2; cc += 32) {
+                    tmem_ld32(tb + lane_off + TOS + 64 * hf + cc, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[j] *= f;
-                    tmem_st32(tb + lane_off + TOS + cc, o);
+                    tmem_st32(tb + lane_off + TOS + 64 * hf + cc, o);
                 }
                 tmem_wait_st();
                 if (need) m_run = bm;
             }
             const float mr = m_run;
+            float lv[32];
+            tmem_ld32(tb + lane_off + TL + 32 * hf, lv);
+            tmem_wait_ld();
 #pragma unroll
-            for (int hlf = 0; hlf < 2; ++hlf) {
-                float lv[32];
-                tmem_ld32(tb + lane_off + TL + 32 * hlf, lv);
-                tmem_wait_ld();
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t ps[4], pl[4];
 #pragma unroll
-                for (int c4 = 0; c4 < 4; ++c4) {
-                    uint32_t ps[4], pl[4];
+                for (int hh = 0; hh < 4; ++hh) {
+                    float e[2], g[2];
 #pragma unroll
-                    for (int hh = 0; hh < 4; ++hh) {
-                        float e[2], g[2];
-#pragma unroll
-                        for (int u = 0; u < 2; ++u) {
-                            const int jj = c4 * 8 + 2 * hh + u;
-                            const uint32_t info = ki[32 * hlf + jj];
-                            const bool vs = (vis_s[hlf] >> jj) & 1u;
-                            const bool vl = row >= (int)((info >> 16) & 255u);
-                            e[u] = vs ? ex2(sv[32 * hlf + jj] - mr) : 0.f;
-                            g[u] = vl ? lv[jj] : 0.f;
-                        }
-                        const __nv_bfloat162 bs = __floats2bfloat162_rn(e[0], e[1]);
-                        const __nv_bfloat162 bl = __floats2bfloat162_rn(g[0], g[1]);
-                        l_soft += __low2float(bs) + __high2float(bs);
-                        l_lin += __low2float(bl) + __high2float(bl);
-                        ps[hh] = *reinterpret_cast<const uint32_t*>(&bs);
-                        pl[hh] = *reinterpret_cast<const uint32_t*>(&bl);
+                    for (int u = 0; u < 2; ++u) {
+                        const int jj = c4 * 8 + 2 * hh + u;
+                        const bool vs = (vis >> jj) & 1u;
+                        const bool vl = row >= (int)((ki[jj] >> 16) & 255u);
+                        e[u] = vs ? ex2(fmaf(sv[jj], c2, -mr)) : 0.f;
+                        g[u] = vl ? lv[jj] : 0.f;
                     }
-                    const int c16 = 4 * hlf + c4;
-                    *reinterpret_cast<uint4*>(sm + SPS + kmaj_chunk(row, c16)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
-                    *reinterpret_cast<uint4*>(sm + SPL + kmaj_chunk(row, c16)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                    const __nv_bfloat162 bs = __floats2bfloat162_rn(e[0], e[1]);
+                    const __nv_bfloat162 bl = __floats2bfloat162_rn(g[0], g[1]);
+                    const float2 fs = __bfloat1622float2(bs), fl = __bfloat1622float2(bl);
+                    l_soft += fs.x + fs.y;
+                    l_lin += fl.x + fl.y;
+                    ps[hh] = *reinterpret_cast<const uint32_t*>(&bs);
+                    pl[hh] = *reinterpret_cast<const uint32_t*>(&bl);
                 }
+                const int c16 = 4 * hf + c4;
+                *reinterpret_cast<uint4*>(sm + SPS + kmaj_chunk(row, c16)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
+                *reinterpret_cast<uint4*>(sm + SPL + kmaj_chunk(row, c16)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
             }
+            fence_async_smem();
+        }
+        if (prod) {
+            cp_async_wait_all();
             fence_async_smem();
         }
         fence_before();
@@ -317,17 +319,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
         fence_after();
         bad = __syncthreads_or(!ok) != 0;
     }
-    // ---- epilogue: y = (O_soft + 2^{-m} O_lin) / (l_soft + 2^{-m} l_lin) ----
-    if (!bad && tid < kTM) {
+    // ---- epilogue: y = (O_soft + 2^{-m} O_lin) / (l_soft + 2^{-m} l_lin); thread (row, hf)
+    //      writes output columns 64 hf .. 64 hf + 63 ----
+    lsum[0][hf][row] = l_soft;
+    lsum[1][hf][row] = l_lin;
+    __syncthreads();
+    if (!bad) {
+        const float ls = lsum[0][0][row] + lsum[0][1][row], ll = lsum[1][0][row] + lsum[1][1][row];
         const bool any = m_run != -INFINITY;
         const float em = any ? ex2(-m_run) : 1.f;
-        const float den = any ? fmaf(em, l_lin, l_soft) : l_lin;
+        const float den = any ? fmaf(em, ll, ls) : ll;
         const float inv = t < n ? 1.0f / den : 0.f;
-        __nv_bfloat16* y = a.Y + (row0 + (t < n ? t : 0)) * kD;
-        for (int cc = 0; cc < kD; cc += 32) {
+        __nv_bfloat16* y = a.Y + (row0 + (t < n ? t : 0)) * kD + 64 * hf;
+        for (int cc = 0; cc < kD / 2; cc += 32) {
             float os[32], ol[32];
-            tmem_ld32(tb + lane_off + TOS + cc, os);
-            tmem_ld32(tb + lane_off + TOL + cc, ol);
+            tmem_ld32(tb + lane_off + TOS + 64 * hf + cc, os);
+            tmem_ld32(tb + lane_off + TOL + 64 * hf + cc, ol);
             tmem_wait_ld();
             uint32_t pk[16];
 #pragma unroll
