@@ -408,14 +408,16 @@ template <int D, int DV, typename T>
 struct FastSmem {
     static constexpr int DK = D;
     static constexpr int NRG = Shape<D, DV>::NRG;   // H row groups (partials)
+    static constexpr size_t a16(size_t x) { return (x + 15) / 16 * 16; }
     // byte offsets (16-byte aligned)
-    static constexpr size_t W = 0;                                          // [D/2][DK+1] f32
-    static constexpr size_t CPHI = (W + 4 * (D / 2) * w_stride<DK>() + 15) / 16 * 16;  // [64][D] f32
+    static constexpr size_t W = 0;                                          // [D/2][DK+4] f32
+    static constexpr size_t CPHI = a16(W + 4 * (D / 2) * w_stride<DK>());   // [64][D] f32
     static constexpr size_t CV = CPHI + 4 * kFastLam * D;                  // [64][DV] T
     static constexpr size_t CK = CV + sizeof(T) * kFastLam * DV;           // [64][DK] T
     static constexpr size_t RK = CK + sizeof(T) * kFastLam * DK;           // [kFastEta][DK] T
     static constexpr size_t RV = RK + sizeof(T) * kFastEta * DK;           // [kFastEta][DV] T
-    static constexpr size_t PHE = RV + sizeof(T) * kFastEta * DV;          // [D] f32 evictee phi
+    static constexpr size_t NV = RV + sizeof(T) * kFastEta * DV;           // [DV] T the new token's v
+    static constexpr size_t PHE = a16(NV + sizeof(T) * DV);                // [D] f32 evictee phi
     static constexpr size_t PHN = PHE + 4 * D;                             // [D] f32 next evictee phi
     static constexpr size_t EVN = PHN + 4 * D;                             // [DV + 4] f32 evictee N, z
     static constexpr size_t SS = EVN + 4 * (DV + 4);                       // [D] f32 s
@@ -426,9 +428,11 @@ struct FastSmem {
     static constexpr size_t PHK = PHQ + 4 * D;                             // [D] f32
     static constexpr size_t RED = PHK + 4 * D;                             // [NRG][DV] f32
     static constexpr size_t RED2 = RED + 4 * NRG * DV;                     // [NRG][DV] f32
-    static constexpr size_t LIN = RED2 + 4 * NRG * DV;                     // [DV] f32
+    static constexpr size_t NPART = RED2 + 4 * NRG * DV;                   // [DV] f32 next evictee's summed partials
+    static constexpr size_t LIN = NPART + 4 * DV;                          // [DV] f32
     static constexpr size_t SC = LIN + 4 * DV;                             // [kFastEta + 64] f32
-    static constexpr size_t WKEY = SC + 4 * (kFastEta + kFastLam);         // [17] uint2
+    static constexpr size_t VOFF = SC + 4 * (kFastEta + kFastLam);         // [kFastEta + 64] i32 value-row offsets
+    static constexpr size_t WKEY = VOFF + 4 * (kFastEta + kFastLam);       // [17] uint2
     static constexpr size_t MISC = WKEY + 8 * 18;                          // [8] f32
     static constexpr size_t TOTAL = MISC + 4 * 8;
 };
@@ -438,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     using S = Shape<D, DV>;
     using M = FastSmem<D, DV, T>;
     constexpr int DK = D;
-    constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, HC = S::HC;
+    constexpr int PD = S::PD, PV = S::PV, HR = S::HR, HC = S::HC;
     constexpr int KS = kThreads / DV;        // key splits of the output numerator
     constexpr int kEvWarp = kDecWarps - 1;
     extern __shared__ __align__(16) uint8_t smb[];
@@ -448,6 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     T* ck_s = reinterpret_cast<T*>(smb + M::CK);
     T* rk_s = reinterpret_cast<T*>(smb + M::RK);
     T* rv_s = reinterpret_cast<T*>(smb + M::RV);
+    T* nv_s = reinterpret_cast<T*>(smb + M::NV);
     float* phe = reinterpret_cast<float*>(smb + M::PHE);
     float* phn = reinterpret_cast<float*>(smb + M::PHN);
     float* evn = reinterpret_cast<float*>(smb + M::EVN);
@@ -459,8 +464,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     float* phk = reinterpret_cast<float*>(smb + M::PHK);
     float* red = reinterpret_cast<float*>(smb + M::RED);
     float* red2 = reinterpret_cast<float*>(smb + M::RED2);
+    float* npart = reinterpret_cast<float*>(smb + M::NPART);
     float* lin = reinterpret_cast<float*>(smb + M::LIN);
     float* sc = reinterpret_cast<float*>(smb + M::SC);
+    int* voff = reinterpret_cast<int*>(smb + M::VOFF);
     uint2* wkey = reinterpret_cast<uint2*>(smb + M::WKEY);
     float* misc = reinterpret_cast<float*>(smb + M::MISC);
 
@@ -490,9 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const int ring = t % eta;
     const bool nxt = t + 1 - eta >= 0;
     const int nring = (t + 1) % eta;
-    const int nwin_old = min(t, eta);   // ring entries holding positions t-eta .. t-1 (valid ones)
 
-    // ---- 1. one burst of loads ----
+    // ---- 1. one burst of loads: the exact KV of cache and window, the slots' phi, the two
+    //         evictees' phi, s and the evictee's N, z by cp.async; W, the new token, H and
+    //         the slots' N, z, positions by plain loads ----
     {
         constexpr int PHI_CH = D / 4, V_CH = DV * (int)sizeof(T) / 16, K_CH = DK * (int)sizeof(T) / 16;
         for (int i = tid; i < nc * PHI_CH; i += kThreads)
@@ -518,7 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         xq[tid] = IO<T>::ld(static_cast<const T*>(a.q) + (int64_t)bh * DK, tid);
         xk[tid] = IO<T>::ld(static_cast<const T*>(a.k) + (int64_t)bh * DK, tid);
     }
-    if (tid < DV) xv[tid] = IO<T>::ld(static_cast<const T*>(a.v) + (int64_t)bh * DV, tid);
+    if (tid < DV) {
+        const T* vin = static_cast<const T*>(a.v) + (int64_t)bh * DV;
+        xv[tid] = IO<T>::ld(vin, tid);
+        nv_s[tid] = vin[tid];
+    }
     float hreg[HR * HC];
     h_load<D, DV>(hreg, Hg, warp, lane);
     // slot role (one pass: lambda <= 64)
@@ -529,23 +541,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
 #pragma unroll
     for (int q = 0; q < PV; ++q) sN[q] = 0.f;
     if (live) {
-        const float* src = cN + (size_t)sl * DV;
-#pragma unroll
-        for (int c = 0; c < PV / 4; ++c) {
-            const float4 f = *reinterpret_cast<const float4*>(src + 32 * c + 4 * sub);
-            sN[4 * c] = f.x;
-            sN[4 * c + 1] = f.y;
-            sN[4 * c + 2] = f.z;
-            sN[4 * c + 3] = f.w;
-        }
+        slot_load<DV>(cN + (size_t)sl * DV, sub, sN);
         sz = cz[sl];
         spos = cpos[sl];
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    __syncthreads();
-    if (ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
+    __syncthreads();   // W and the new token staged; the burst may still be in flight
 
-    // ---- 2. phi(q), phi(k_t); next evictee's partials; evictee and slot SREs ----
+    // ---- 2a. phi(q), phi(k_t) while the burst lands ----
     if (warp == 0) {
         float ph[D / 32];
         phi_warp<DK, D>(xq, Ws, lane, ph);
@@ -557,16 +559,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
 #pragma unroll
         for (int m = 0; m < D / 32; ++m) phk[lane + 32 * m] = ph[m];
     }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();
+    if (ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
+
+    // ---- 2b. next evictee's partials; evictee and slot SREs ----
     if (nxt) h_partial_store<D, DV>(red, phn, hreg, warp, lane);
-    float ve[PV], zn_prev = 0.f;
+    float zn_prev = 0.f;
     if (warp == kEvWarp) {
         uint32_t ehi = kNoKey, elo = kNoKey;
         if (ev) {
-            float Ne[PV];
+            float Ne[PV], ve[PV];
             slot_load<DV>(evn, sub, Ne);
-            const T* vr = rv_s + (size_t)ring * DV;
-#pragma unroll
-            for (int q = 0; q < PV; ++q) ve[q] = IO<T>::ld(vr, slot_dim(sub, q));
+            slot_load_io<DV, T>(rv_s + (size_t)ring * DV, sub, ve);
             const float es = slot_sre2<DV>(Ne, evn[DV], ve, slot_vv<DV>(ve));
             ehi = key_hi(es);
             elo = key_lo(e, kEvCode);
@@ -581,9 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     {
         float sv[PV];
-        const T* vr = cv_s + (size_t)(live ? sl : 0) * DV;
-#pragma unroll
-        for (int q = 0; q < PV; ++q) sv[q] = live ? IO<T>::ld(vr, slot_dim(sub, q)) : 0.f;
+        slot_load_io<DV, T>(cv_s + (size_t)(live ? sl : 0) * DV, sub, sv);
         const float sre = slot_sre2<DV>(sN, sz, sv, slot_vv<DV>(sv));
         uint32_t khi = live ? key_hi(sre) : kNoKey;
         uint32_t klo = live ? key_lo(spos, sl) : kNoKey;
@@ -601,9 +604,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const int wsel = !write ? -2 : (code == kEvCode ? -1 : code);   // -1: the evictee is written
     const float* wphi = wsel >= 0 ? cphi_s + (size_t)wsel * D : phe;
     const T* wvT = wsel >= 0 ? cv_s + (size_t)wsel * DV : rv_s + (size_t)ring * DV;
-    float wv4[PV];   // v_w in slot layout (float), for the N updates
-#pragma unroll
-    for (int q = 0; q < PV; ++q) wv4[q] = write ? IO<T>::ld(wvT, slot_dim(sub, q)) : 0.f;
     // the moved evictee (written slot) and the appended one (no write)
     const int slot_new = (ev && !write) ? nc : (wsel >= 0 ? wsel : -1);
     const int nc_after = (ev && !write) ? nc + 1 : nc;
@@ -635,32 +635,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         if (write) {
             const float g = slot_gram<D>(wphi, sphi, sub);
             if (live) {
-                float2* n2 = reinterpret_cast<float2*>(sN);
-                const float2 g2 = make_float2(g, g);
-#pragma unroll
-                for (int c = 0; c < PV / 2; ++c) n2[c] = __ffma2_rn(g2, make_float2(wv4[2 * c], wv4[2 * c + 1]), n2[c]);
+                slot_axpy_io<DV, T>(sN, g, wvT, sub);
                 sz += g;
             }
         }
     }
-    // the next evictee: N' corrected by this step's write (evictee warp)
-    float Nn[PV], zn = zn_prev;
-    if (warp == kEvWarp && nxt) {
-        slot_reduce_partials<D, DV>(red, sub, Nn);
-        if (write) {
-            float ph[PD];
-            slot_load<D>(phn, sub, ph);
-            const float g = slot_gram<D>(wphi, ph, sub);
-            float2* n2 = reinterpret_cast<float2*>(Nn);
-            const float2 g2 = make_float2(g, g);
-#pragma unroll
-            for (int c = 0; c < PV / 2; ++c) n2[c] = __ffma2_rn(g2, make_float2(wv4[2 * c], wv4[2 * c + 1]), n2[c]);
-            zn += g;
-        }
+    // the next evictee: its partials summed in row-group order (column form); the gram of
+    // this step's write with it (evictee warp; the correction is applied at the write-back)
+    if (nxt && tid < DV) npart[tid] = reduce_partials_col<D, DV>(red, tid);
+    float gn = 0.f, zn = zn_prev;
+    if (warp == kEvWarp && nxt && write) {
+        float ph[PD];
+        slot_load<D>(phn, sub, ph);
+        gn = slot_gram<D>(wphi, ph, sub);
+        zn += gn;
     }
     __syncwarp();
 
-    // ---- 4. output: scores over window ∪ cache after the write ----
+    // ---- 4. output: scores over window ∪ cache after the write; each key's value row ----
     const float scale = 1.0f / sqrtf((float)DK);
     const int nwin = min(t + 1, eta);
     const int nkeys = nwin + nc_after;
@@ -668,20 +660,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         const int i = base + sl;
         float acc = 0.f;
         if (i < nkeys) {
+            int vo;
             if (i == 0) {                             // the new token
 #pragma unroll
                 for (int q = 0; q < PD; ++q) acc = fmaf(xq[slot_dim(sub, q)], xk[slot_dim(sub, q)], acc);
+                vo = (int)M::NV;
             } else {
                 const T* kr;
                 if (i < nwin) {
-                    kr = rk_s + (size_t)((t - i) % eta) * DK;        // positions t-1, t-2, ...
+                    const int r = (t - i) % eta;                   // positions t-1, t-2, ...
+                    kr = rk_s + (size_t)r * DK;
+                    vo = (int)(M::RV + sizeof(T) * (size_t)r * DV);
                 } else {
                     const int j = i - nwin;                          // cache slot
                     kr = (j == slot_new) ? rk_s + (size_t)ring * DK : ck_s + (size_t)j * DK;
+                    vo = (j == slot_new) ? (int)(M::RV + sizeof(T) * (size_t)ring * DV)
+                                         : (int)(M::CV + sizeof(T) * (size_t)j * DV);
                 }
 #pragma unroll
                 for (int q = 0; q < PD; ++q) acc = fmaf(xq[slot_dim(sub, q)], IO<T>::ld(kr, slot_dim(sub, q)), acc);
             }
+            if (sub == 0) voff[i] = vo;
         }
         acc += __shfl_xor_sync(kFull, acc, 1);
         acc += __shfl_xor_sync(kFull, acc, 2);
@@ -710,15 +709,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         slot_load<D>(s_sm, sub, sr);
         const float dl = slot_gram<D>(phq, sr, sub);
         if (lane == 0) misc[4] = dl;
-    } else if (warp == 1 && lane < DV / 4) {
-        const int j0 = 4 * lane;
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-            float acc = red2[j0 + jj];
-#pragma unroll
-            for (int rg = 1; rg < NRG; ++rg) acc += red2[rg * DV + j0 + jj];
-            lin[j0 + jj] = acc;
-        }
+    } else if (warp >= 1 && warp <= DV / kWarp) {
+        // H^T phi(q): the row-group partials summed (column per thread)
+        const int j = tid - kWarp;
+        lin[j] = reduce_partials_col<D, DV>(red2, j);
     }
     __syncthreads();
     {
@@ -726,16 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         const int ks = tid / DV, kj = tid % DV;
         float accs[4] = {0.f, 0.f, 0.f, 0.f};
         for (int i = ks; i < nkeys; i += KS) {
-            float vj;
-            if (i == 0) {
-                vj = xv[kj];
-            } else if (i < nwin) {
-                vj = IO<T>::ld(rv_s + (size_t)((t - i) % eta) * DV, kj);
-            } else {
-                const int j = i - nwin;
-                vj = IO<T>::ld(j == slot_new ? rv_s + (size_t)ring * DV : cv_s + (size_t)j * DV, kj);
-            }
-            accs[(i / KS) & 3] = fmaf(sc[i], vj, accs[(i / KS) & 3]);
+            const T* vr = reinterpret_cast<const T*>(smb + voff[i]);
+            accs[(i / KS) & 3] = fmaf(sc[i], IO<T>::ld(vr, kj), accs[(i / KS) & 3]);
         }
         red[ks * DV + kj] = (accs[0] + accs[1]) + (accs[2] + accs[3]);
     }
@@ -780,11 +766,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         float sr[PD];
         slot_load<D>(s_sm, sub, sr);
         slot_store<D>(sg, sub, sr);
-        if (nxt) slot_store<DV>(evs, sub, Nn);
-        if (lane == 0 && nxt) evs[DV] = zn;
+        if (nxt) {
+            // N of the next evictee: summed partials + this step's write (slot_axpy's order)
+            float Nn[PV];
+            slot_load<DV>(npart, sub, Nn);
+            if (write) slot_axpy_io<DV, T>(Nn, gn, wvT, sub);
+            slot_store<DV>(evs, sub, Nn);
+            if (lane == 0) evs[DV] = zn;
+        }
     }
     if (tid < DK) IO<T>::st(wk, (int64_t)ring * DK + tid, xk[tid]);
-    if (tid < DV) IO<T>::st(wvv, (int64_t)ring * DV + tid, xv[tid]);
+    if (tid < DV) wvv[(int64_t)ring * DV + tid] = nv_s[tid];
     if (tid < D) wphg[(int64_t)ring * D + tid] = phk[tid];
     if (tid == 0) {
         winpos[ring] = t;
@@ -793,7 +785,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         if (write) hdr[HDR_NWRITTEN] += 1;
         if (a.written_pos) a.written_pos[bh] = wposn;
     }
-    (void)nwin_old;
 }
 
 template <int D, int DV, typename T>
