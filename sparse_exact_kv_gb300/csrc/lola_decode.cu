@@ -404,6 +404,20 @@ __device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
                  : "memory");
 }
 
+// values 2 kc and 2 kc + 1 of a value row (float32 or bfloat16, widened exactly)
+template <typename T>
+__device__ __forceinline__ void h_cols2(const T* v, int kc, float* out) {
+    if constexpr (sizeof(T) == 4) {
+        const float2 f = reinterpret_cast<const float2*>(v)[kc];
+        out[0] = f.x;
+        out[1] = f.y;
+    } else {
+        const uint32_t x = reinterpret_cast<const uint32_t*>(v)[kc];
+        out[0] = bf16_lo(x);
+        out[1] = bf16_hi(x);
+    }
+}
+
 template <int D, int DV, typename T>
 struct FastSmem {
     static constexpr int DK = D;
@@ -656,36 +670,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const float scale = 1.0f / sqrtf((float)DK);
     const int nwin = min(t + 1, eta);
     const int nkeys = nwin + nc_after;
-    for (int base = 0; base < nkeys; base += kThreads / kSG) {
-        const int i = base + sl;
-        float acc = 0.f;
-        if (i < nkeys) {
-            int vo;
-            if (i == 0) {                             // the new token
-#pragma unroll
-                for (int q = 0; q < PD; ++q) acc = fmaf(xq[slot_dim(sub, q)], xk[slot_dim(sub, q)], acc);
-                vo = (int)M::NV;
-            } else {
-                const T* kr;
-                if (i < nwin) {
-                    const int r = (t - i) % eta;                   // positions t-1, t-2, ...
-                    kr = rk_s + (size_t)r * DK;
-                    vo = (int)(M::RV + sizeof(T) * (size_t)r * DV);
+    {
+        float qs[PD];
+        slot_load<DK>(xq, sub, qs);
+        for (int base = 0; base < nkeys; base += kThreads / kSG) {
+            const int i = base + sl;
+            float acc = 0.f;
+            if (i < nkeys) {
+                int vo;
+                float kv[PD];
+                if (i == 0) {                             // the new token
+                    slot_load<DK>(xk, sub, kv);
+                    vo = (int)M::NV;
                 } else {
-                    const int j = i - nwin;                          // cache slot
-                    kr = (j == slot_new) ? rk_s + (size_t)ring * DK : ck_s + (size_t)j * DK;
-                    vo = (j == slot_new) ? (int)(M::RV + sizeof(T) * (size_t)ring * DV)
-                                         : (int)(M::CV + sizeof(T) * (size_t)j * DV);
+                    const T* kr;
+                    if (i < nwin) {
+                        int r = ring - i;                               // positions t-1, t-2, ...
+                        r += r < 0 ? eta : 0;
+                        kr = rk_s + (size_t)r * DK;
+                        vo = (int)(M::RV + sizeof(T) * (size_t)r * DV);
+                    } else {
+                        const int j = i - nwin;                          // cache slot
+                        kr = (j == slot_new) ? rk_s + (size_t)ring * DK : ck_s + (size_t)j * DK;
+                        vo = (j == slot_new) ? (int)(M::RV + sizeof(T) * (size_t)ring * DV)
+                                             : (int)(M::CV + sizeof(T) * (size_t)j * DV);
+                    }
+                    slot_load_io<DK, T>(kr, sub, kv);
                 }
 #pragma unroll
-                for (int q = 0; q < PD; ++q) acc = fmaf(xq[slot_dim(sub, q)], IO<T>::ld(kr, slot_dim(sub, q)), acc);
+                for (int q = 0; q < PD; ++q) acc = fmaf(qs[q], kv[q], acc);
+                if (sub == 0) voff[i] = vo;
             }
-            if (sub == 0) voff[i] = vo;
+            acc += __shfl_xor_sync(kFull, acc, 1);
+            acc += __shfl_xor_sync(kFull, acc, 2);
+            acc += __shfl_xor_sync(kFull, acc, 4);
+            if (i < nkeys && sub == 0) sc[i] = acc * scale;
         }
-        acc += __shfl_xor_sync(kFull, acc, 1);
-        acc += __shfl_xor_sync(kFull, acc, 2);
-        acc += __shfl_xor_sync(kFull, acc, 4);
-        if (i < nkeys && sub == 0) sc[i] = acc * scale;
     }
     h_partial_store<D, DV>(red2, phq, hreg, warp, lane);
     __syncthreads();
@@ -716,20 +736,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     __syncthreads();
     {
-        // numerator: keys split KS ways (thread: split ks, column kj), then combined
-        const int ks = tid / DV, kj = tid % DV;
-        float accs[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int i = ks; i < nkeys; i += KS) {
-            const T* vr = reinterpret_cast<const T*>(smb + voff[i]);
-            accs[(i / KS) & 3] = fmaf(sc[i], IO<T>::ld(vr, kj), accs[(i / KS) & 3]);
+        // numerator: thread (split ks, column pair 2 kc, 2 kc + 1) over keys ks, ks + NS, ...;
+        // the NS splits are then summed in order
+        constexpr int NS = kThreads / (DV / 2);
+        const int ks = tid / (DV / 2), kc = tid % (DV / 2);
+        float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+        int i = ks;
+        for (; i + NS < nkeys; i += 2 * NS) {
+            float v0[2], v1[2];
+            h_cols2<T>(reinterpret_cast<const T*>(smb + voff[i]), kc, v0);
+            h_cols2<T>(reinterpret_cast<const T*>(smb + voff[i + NS]), kc, v1);
+            const float p0 = sc[i], p1 = sc[i + NS];
+            a0 = __ffma2_rn(make_float2(p0, p0), make_float2(v0[0], v0[1]), a0);
+            a1 = __ffma2_rn(make_float2(p1, p1), make_float2(v1[0], v1[1]), a1);
         }
-        red[ks * DV + kj] = (accs[0] + accs[1]) + (accs[2] + accs[3]);
+        if (i < nkeys) {
+            float v0[2];
+            h_cols2<T>(reinterpret_cast<const T*>(smb + voff[i]), kc, v0);
+            const float p0 = sc[i];
+            a0 = __ffma2_rn(make_float2(p0, p0), make_float2(v0[0], v0[1]), a0);
+        }
+        *reinterpret_cast<float2*>(red + ks * DV + 2 * kc) = make_float2(a0.x + a1.x, a0.y + a1.y);
     }
     __syncthreads();
     if (tid < DV) {
+        constexpr int NS = kThreads / (DV / 2);
         float num = 0.f;
 #pragma unroll
-        for (int r = 0; r < KS; ++r) num += red[r * DV + tid];
+        for (int r = 0; r < NS; ++r) num += red[r * DV + tid];
         num = fmaf(misc[1], lin[tid], num);
         const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
         IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
