@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import dataclasses
+import hashlib
 import json
 import os
 import statistics
@@ -150,6 +151,36 @@ class Clocks:
                 "samples": len(rows)}
 
 
+# DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
+# the kernel on the workload named beside it, valid only for the kernel sources it was taken
+# on: the digest of those files must match, otherwise the traffic is reported as null.
+CSRC = os.path.join(ROOT, "sparse_exact_kv_gb300", "csrc")
+NCU_TRAFFIC = {
+    # w2 prefill (4 x 32 heads, n = 4096): one select launch
+    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "8a4e40c300f5ff74",
+               "bytes_per_launch": 409095936 + 131939840},
+    # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
+    # (every byte is per head)
+    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "f27b37c23056869b",
+               "bytes_per_launch": 2 * (205230592 + 55027917)},
+}
+
+
+def sources_digest(files) -> str:
+    h = hashlib.sha1()
+    for f in files:
+        with open(os.path.join(CSRC, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic(kernel: str):
+    e = NCU_TRAFFIC.get(kernel)
+    if not e or sources_digest(e["sources"]) != e["digest"]:
+        return None
+    return e["bytes_per_launch"]
+
+
 def peaks(sm_count: int):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -260,7 +291,7 @@ def run_prefill(L, R, args, pk):
         fl = heads * w.n * select_flops_per_step(w.D, w.d, w.lam)
         ach = fl / (sel["avg_ms"] / 1e3) / 1e12
         res["roofline"] = {"kernel": "select", "bound": "alu", "achieved": ach, "peak": pk["fp32_tflops"],
-                           "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"], "traffic": None,
+                           "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"], "traffic": traffic("select"),
                            "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
     out = kt.get("output")
     if out:
@@ -345,7 +376,7 @@ def run_decode(L, R, args, pk):
         byts = heads * decode_bytes_per_head(w.d, w.D, w.eta, w.lam)
         ach = byts / (dk_["avg_ms"] / 1e3) / 1e9
         res["roofline"] = {"kernel": "decode", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                           "frac": ach / pk["hbm_gbs"], "traffic": None,
+                           "frac": ach / pk["hbm_gbs"], "traffic": traffic("decode"),
                            "algorithmic_bytes_per_launch": byts}
     return res
 
@@ -371,10 +402,11 @@ def oracle_sample(x, w, heads: int):
 
 
 def cpu_baseline(x, w):
-    heads = min(w.B * w.Hh, 2 * (os.cpu_count() or 1))
+    """The oracle over every head of the prefill workload (about 35 core-seconds)."""
+    heads = w.B * w.Hh
     dt, tokens, threads = oracle_sample(x, w, heads)
     return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"first {heads} of {w.B * w.Hh} heads of {w.name}, full n={w.n} "
+            "sample": f"all {heads} heads of {w.name}, full n={w.n} "
                       f"({tokens:g} token-equivalents in {dt:.2f} s)"}
 
 
