@@ -182,6 +182,37 @@ __device__ __forceinline__ void h_partial_store(float* red, const float* phi, co
     h_partial<D, DV>(phi, h, w, out);
     h_vec_store<S::HC>(red + w * DV + l * S::HC, out);
 }
+// ---- warp role (32 lanes, N/32 consecutive entries per lane): the evictee's gram with the
+// written key, its z' = s^T phi and its SRE.  Fixed operation order: per lane in entry order,
+// then a butterfly over xor 16, 8, 4, 2, 1; every lane gets the result. ----
+template <int N>
+__device__ __forceinline__ float warp_dot(const float* a, const float* b, int lane) {
+    constexpr int E = N / kWarp;
+    float x[E], y[E];
+    h_vec_load<E>(a + lane * E, x);
+    h_vec_load<E>(b + lane * E, y);
+    float p = x[0] * y[0];
+#pragma unroll
+    for (int e = 1; e < E; ++e) p = __fmaf_rn(x[e], y[e], p);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) p += __shfl_xor_sync(kFull, p, o);
+    return p;
+}
+// SRE^2 from this lane's entries of N and v (the fallback vv when z = 0, as slot_sre2)
+template <int DV>
+__device__ __forceinline__ float warp_sre2(const float* Nl, float z, const float* vl, float vv) {
+    constexpr int E = DV / kWarp;
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+        const float d = __fmaf_rn(-z, vl[e], Nl[e]);
+        ss = __fmaf_rn(d, d, ss);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(kFull, ss, o);
+    return z == 0.f ? vv : __fdividef(ss, z * z);
+}
+
 // N' = sum of the row-group partials in row-group order, one column j (any thread)
 template <int D, int DV>
 __device__ __forceinline__ float reduce_partials_col(const float* red, int j) {

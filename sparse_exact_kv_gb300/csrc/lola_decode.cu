@@ -156,17 +156,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     if (warp == kEvWarp) {
         uint32_t ehi = kNoKey, elo = kNoKey;
         if (ev) {
-            float Ne[PV], ve[PV], ze;
+            // the evictee's SRE in the warp layout (DV/32 consecutive entries per lane), the
+            // arithmetic of the prefill chain's evictee warp
+            constexpr int EV = DV / kWarp;
+            float ze;
             if (eta > 0) {
-                slot_load<DV>(evs, sub, Ne);
+                if (tid - kEvWarp * kWarp < DV / 4)
+                    reinterpret_cast<float4*>(Ne_s)[tid - kEvWarp * kWarp] = reinterpret_cast<const float4*>(evs)[tid - kEvWarp * kWarp];
                 ze = evs[DV];
             } else {
+                float Ne[PV];
                 slot_reduce_partials<D, DV>(red, sub, Ne);
+                if (lane < kSG) slot_store<DV>(Ne_s, sub, Ne);
                 ze = slot_gram<D>(phe, s_reg, sub);
             }
+            __syncwarp();
+            float ve[PV], Nw[EV], vw[EV];
             slot_load<DV>(evv, sub, ve);
-            const float es = slot_sre2<DV>(Ne, ze, ve, slot_vv<DV>(ve));
-            if (lane < kSG) slot_store<DV>(Ne_s, sub, Ne);
+            h_vec_load<EV>(Ne_s + lane * EV, Nw);
+            h_vec_load<EV>(evv + lane * EV, vw);
+            const float es = warp_sre2<DV>(Nw, ze, vw, slot_vv<DV>(ve));
             if (lane == 0) misc[0] = ze;
             ehi = key_hi(es);
             elo = key_lo(e, kEvCode);
@@ -174,7 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
         if (lane == 0) wkey[kDecWarps] = make_uint2(ehi, elo);
         if (nxt) {
             slot_reduce_partials<D, DV>(red, sub, Nn);
-            zn = slot_gram<D>(phn, s_reg, sub);
+            zn = warp_dot<D>(phn, sg, lane);   // s before this step's write
         }
     }
     // slot SREs, pass by pass; each warp keeps its minimum over all passes
@@ -269,9 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
             }
         }
         if (warp == kEvWarp && nxt) {
-            float ph[PD];
-            slot_load<D>(phn, sub, ph);
-            const float g = slot_gram<D>(wphi, ph, sub);
+            const float g = warp_dot<D>(wphi, phn, lane);
             slot_axpy<DV>(Nn, g, wv, sub);
             zn += g;
         }
@@ -583,20 +590,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     if (warp == kEvWarp) {
         uint32_t ehi = kNoKey, elo = kNoKey;
         if (ev) {
-            float Ne[PV], ve[PV];
-            slot_load<DV>(evn, sub, Ne);
+            // the evictee's SRE in the warp layout (DV/32 consecutive entries per lane), the
+            // arithmetic of the prefill chain's evictee warp
+            constexpr int EV = DV / kWarp;
+            float ve[PV], Nw[EV], vw[EV];
             slot_load_io<DV, T>(rv_s + (size_t)ring * DV, sub, ve);
-            const float es = slot_sre2<DV>(Ne, evn[DV], ve, slot_vv<DV>(ve));
+            h_vec_load<EV>(evn + lane * EV, Nw);
+            h_cols<DV, T>(rv_s + (size_t)ring * DV, lane, vw);
+            const float es = warp_sre2<DV>(Nw, evn[DV], vw, slot_vv<DV>(ve));
             ehi = key_hi(es);
             elo = key_lo(e, kEvCode);
         }
         if (lane == 0) wkey[kDecWarps] = make_uint2(ehi, elo);
         // z' of the next evictee against s before this step's write
-        if (nxt) {
-            float sr[PD];
-            slot_load<D>(s_sm, sub, sr);
-            zn_prev = slot_gram<D>(phn, sr, sub);
-        }
+        if (nxt) zn_prev = warp_dot<D>(phn, s_sm, lane);
     }
     {
         float sv[PV];
@@ -659,9 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     if (nxt && tid < DV) npart[tid] = reduce_partials_col<D, DV>(red, tid);
     float gn = 0.f, zn = zn_prev;
     if (warp == kEvWarp && nxt && write) {
-        float ph[PD];
-        slot_load<D>(phn, sub, ph);
-        gn = slot_gram<D>(wphi, ph, sub);
+        gn = warp_dot<D>(wphi, phn, lane);
         zn += gn;
     }
     __syncwarp();

@@ -269,17 +269,21 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         h_cols<DV, T>(w.v, lane, vh);
         h_update<D, DV>(h, w.phi, vh, warp);
     };
-    // s absorbs it too (warp kSWarp, lanes 0-7 hold s in the slot layout)
+    // s absorbs it too (warp kSWarp, D/32 consecutive entries per lane)
+    constexpr int ES = D / kWarp, EV = DV / kWarp;
     auto absorb_s = [&](const Win& w) {
-        if (lane < kSG) {
-            float wp[PD], sr[PD];
-            slot_load<D>(w.phi, sub, wp);
-            slot_load<D>(s_sm, sub, sr);
+        float wp[ES], sr[ES];
+        h_vec_load<ES>(w.phi + lane * ES, wp);
+        h_vec_load<ES>(s_sm + lane * ES, sr);
 #pragma unroll
-            for (int i = 0; i < PD; ++i) sr[i] += wp[i];
-            slot_store<D>(s_sm, sub, sr);
-        }
+        for (int i = 0; i < ES; ++i) sr[i] += wp[i];
+        h_vec_store<ES>(s_sm + lane * ES, sr);
         __syncwarp();
+    };
+    auto store_s = [&](float* dst) {
+        float sr[ES];
+        h_vec_load<ES>(s_sm + lane * ES, sr);
+        h_vec_store<ES>(dst + lane * ES, sr);
     };
 
     int snap_next = 0, snap_c = 0;
@@ -293,12 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         //      previous write with the evictee ----
         if (warp < kHelp && ev) {
             if (warp == 0) {
-                float g = 0.f;
-                if (prev_write) {
-                    float ph[PD];
-                    slot_load<D>(ebuf[t & (kNEB - 1)], sub, ph);
-                    g = slot_gram<D>(W.phi, ph, sub);
-                }
+                const float g = prev_write ? warp_dot<D>(W.phi, ebuf[t & (kNEB - 1)], lane) : 0.f;
                 if (lane == 0) gbuf[t & 1] = g;
             }
             const int j = warp * kWarp + lane;
@@ -324,23 +323,26 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             }
         }
 
-        // ---- last warp: the evictee of step t.  N = partials + g v_w (slot_axpy's order),
-        //      z = z' + g, then its SRE with the arithmetic of a slot ----
+        // ---- last warp: the evictee of step t, DV/32 consecutive entries per lane.
+        //      N = partials + g v_w (one fma per entry), z = z' + g, then warp_sre2 ----
         if (warp == kEvWarp) {
             uint32_t ehi = kNoKey, elo = kNoKey;
             if (ev) {
-                float Ne[PV], ve[PV];
+                float Ne[EV], ve[EV];
                 named_sync(kHandoff);
-                slot_load<DV>(npart[t & 1], sub, Ne);
+                h_vec_load<EV>(&npart[t & 1][lane * EV], Ne);
                 float ze = zpbuf[t & 1];
                 if (prev_write) {
                     const float g = gbuf[t & 1];
-                    slot_axpy_io<DV, T>(Ne, g, W.v, sub);
+                    float vw[EV];
+                    h_cols<DV, T>(W.v, lane, vw);
+#pragma unroll
+                    for (int i = 0; i < EV; ++i) Ne[i] = __fmaf_rn(g, vw[i], Ne[i]);
                     ze += g;
                 }
-                slot_load_io<DV, T>(evraw[t & (kNEB - 1)], sub, ve);
-                const float es = slot_sre2<DV>(Ne, ze, ve, vvbuf[t & 3]);
-                if (lane < kSG) slot_store<DV>(nbuf[t & 1], sub, Ne);
+                h_cols<DV, T>(evraw[t & (kNEB - 1)], lane, ve);
+                const float es = warp_sre2<DV>(Ne, ze, ve, vvbuf[t & 3]);
+                h_vec_store<EV>(&nbuf[t & 1][lane * EV], Ne);
                 if (lane == 0) zbuf[t & 1] = ze;
                 ehi = key_hi(es);
                 elo = key_lo(t - eta, kEvCode);
@@ -352,9 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         if (warp == kSWarp) {
             absorb_s(W);
             if (t + 1 - eta >= 0) {
-                float sr[PD];
-                slot_load<D>(s_sm, sub, sr);
-                const float zp = slot_gram<D>(ebuf[(t + 1) & (kNEB - 1)], sr, sub);
+                const float zp = warp_dot<D>(ebuf[(t + 1) & (kNEB - 1)], s_sm, lane);
                 if (lane == 0) zpbuf[(t + 1) & 1] = zp;
             }
         }
@@ -372,11 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             if (rank == 0) {
                 if (a.snapHb) h_store_bf16<D, DV>(a.snapHb + ((int64_t)bh * a.nck + c) * D * DV, h, warp, lane);
                 else h_store<D, DV>(a.snapH + ((int64_t)bh * a.nck + c) * D * DV, h, warp, lane);
-                if (warp == kSWarp && lane < kSG) {
-                    float sr[PD];
-                    slot_load<D>(s_sm, sub, sr);
-                    slot_store<D>(a.snapS + ((int64_t)bh * a.nck + c) * D, sub, sr);
-                }
+                if (warp == kSWarp) store_s(a.snapS + ((int64_t)bh * a.nck + c) * D);
             }
             if (sub == 0 && gslot < lam) a.snapC[((int64_t)bh * a.nck + c) * lam + gslot] = spos;
         }
@@ -454,11 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             hdr[HDR_STATUS] = 0;
         }
         h_store<D, DV>(reinterpret_cast<float*>(rec + a.L.H), h, warp, lane);
-        if (warp == kSWarp && lane < kSG) {
-            float sr[PD];
-            slot_load<D>(s_sm, sub, sr);
-            slot_store<D>(reinterpret_cast<float*>(rec + a.L.s), sub, sr);
-        }
+        if (warp == kSWarp) store_s(reinterpret_cast<float*>(rec + a.L.s));
         if (warp == kEvWarp) {
             // the next evictee (token n - eta): N against the memory after token n - 1
             if (eta > 0 && n - eta >= 0) {
@@ -467,9 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
                 slot_reduce_partials<D, DV>(&red[n & 1][0][0], sub, Ne);
                 float ze = zpbuf[n & 1];
                 if (last_write) {
-                    float ph[PD];
-                    slot_load<D>(eb, sub, ph);
-                    const float g = slot_gram<D>(WL.phi, ph, sub);
+                    const float g = warp_dot<D>(WL.phi, eb, lane);
                     slot_axpy_io<DV, T>(Ne, g, WL.v, sub);
                     ze += g;
                 }
