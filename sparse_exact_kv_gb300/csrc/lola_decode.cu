@@ -38,7 +38,17 @@ struct DecArgs {
     const void* v;
     void* y;
     int32_t* written_pos;
+    int BH;
+    int prefetch_ahead;   // heads ahead of this one whose state is prefetched into L2 (0: none)
 };
+
+// Ask L2 to fetch [p, p + bytes) (one prefetch per 128-byte line, spread over the CTA's
+// threads) and to keep it: the CTA that processes that head about one wave later then
+// finds its state in L2 instead of waiting on DRAM.
+__device__ __forceinline__ void prefetch_l2(const char* p, int64_t bytes, int tid, int nthreads) {
+    for (int64_t o = (int64_t)tid * 128; o < bytes; o += (int64_t)nthreads * 128)
+        asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p + o));
+}
 
 template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
@@ -583,6 +593,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
     if (ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
+    // the state of the head one wave ahead, into L2 (all heads step together, so its window
+    // ring rows for this step are ring and nring as here); the window phi ring is skipped
+    // but for those two rows
+    if (a.prefetch_ahead > 0 && bh + a.prefetch_ahead < a.BH) {
+        const char* nr = a.state + (int64_t)(bh + a.prefetch_ahead) * a.L.head_bytes;
+        prefetch_l2(nr, a.L.win_phi, tid, kThreads);
+        prefetch_l2(nr + a.L.win_phi + (int64_t)ring * D * 4, D * 4, tid, kThreads);
+        prefetch_l2(nr + a.L.win_phi + (int64_t)nring * D * 4, D * 4, tid, kThreads);
+        prefetch_l2(nr + a.L.c_pos, a.L.head_bytes - a.L.c_pos, tid, kThreads);
+    }
 
     // ---- 2b. next evictee's partials; evictee and slot SREs ----
     if (nxt) h_partial_store<D, DV>(red, phn, hreg, warp, lane);
@@ -872,6 +892,14 @@ cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const flo
     a.v = v;
     a.y = y;
     a.written_pos = written_pos;
+    a.BH = d.BH;
+    a.prefetch_ahead = 0;
+    {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess &&
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+            a.prefetch_ahead = sms;   // one resident CTA per SM
+    }
     const bool bf = d.dtype == LOLA_BF16;
     if (d.D == 128 && d.dv == 128)
         return bf ? launch_decode_t<128, 128, __nv_bfloat16>(d, a, st) : launch_decode_t<128, 128, float>(d, a, st);
