@@ -681,6 +681,40 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
             }
         }
     }
+    // ---- write back what is final now (the stores drain during the read): H, s and every
+    //      slot's N, z change only with a write; an append stores the evictee's own N, z;
+    //      the new cache row; the new token into the window ring ----
+    if (write) {
+        h_store<D, DV>(Hg, hreg, warp, lane);
+        if (warp == kEvWarp && lane < kSG) {
+            float sr[PD];
+            slot_load<D>(s_sm, sub, sr);
+            slot_store<D>(sg, sub, sr);
+        }
+        if (live) {
+            slot_store<DV>(cN + (size_t)sl * DV, sub, sN);
+            if (sub == 0) {
+                cz[sl] = sz;
+                if (sl == wsel) cpos[sl] = e;
+            }
+        }
+    } else if (ev && sl == nc) {
+        float Ne[PV];
+        slot_load<DV>(evn, sub, Ne);
+        slot_store<DV>(cN + (size_t)sl * DV, sub, Ne);
+        if (sub == 0) {
+            cz[sl] = evn[DV];
+            cpos[sl] = e;
+        }
+    }
+    if (slot_new >= 0) {
+        if (tid < D) cphi[(size_t)slot_new * D + tid] = phe[tid];
+        if (tid < DK) ck[(size_t)slot_new * DK + tid] = rk_s[(size_t)ring * DK + tid];
+        if (tid < DV) cv[(size_t)slot_new * DV + tid] = rv_s[(size_t)ring * DV + tid];
+    }
+    if (tid < DK) IO<T>::st(wk, (int64_t)ring * DK + tid, xk[tid]);
+    if (tid < DV) wvv[(int64_t)ring * DV + tid] = nv_s[tid];
+    if (tid < D) wphg[(int64_t)ring * D + tid] = phk[tid];
     // the next evictee: its partials summed in row-group order (column form); the gram of
     // this step's write with it (evictee warp; the correction is applied at the write-back)
     if (nxt && tid < DV) npart[tid] = reduce_partials_col<D, DV>(red, tid);
@@ -794,37 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
     }
 
-    // ---- 5. write back ----
-    h_store<D, DV>(Hg, hreg, warp, lane);
-    if (sl < nc_after) {
-        float* dst = cN + (size_t)sl * DV;
-#pragma unroll
-        for (int c = 0; c < PV / 4; ++c)
-            *reinterpret_cast<float4*>(dst + 32 * c + 4 * sub) =
-                make_float4(sN[4 * c], sN[4 * c + 1], sN[4 * c + 2], sN[4 * c + 3]);
-        if (sub == 0) {
-            cz[sl] = sl == slot_new && !write ? evn[DV] : sz;
-            if (sl == slot_new) cpos[sl] = e;
-        }
-    }
-    if (slot_new >= 0) {
-        if (!write && sl == slot_new) {
-            // appended without a write: N, z are the evictee's own
-            float* dst = cN + (size_t)sl * DV;
-            float Ne[PV];
-            slot_load<DV>(evn, sub, Ne);
-#pragma unroll
-            for (int c = 0; c < PV / 4; ++c)
-                *reinterpret_cast<float4*>(dst + 32 * c + 4 * sub) = make_float4(Ne[4 * c], Ne[4 * c + 1], Ne[4 * c + 2], Ne[4 * c + 3]);
-        }
-        if (tid < D) cphi[(size_t)slot_new * D + tid] = phe[tid];
-        if (tid < DK) ck[(size_t)slot_new * DK + tid] = rk_s[(size_t)ring * DK + tid];
-        if (tid < DV) cv[(size_t)slot_new * DV + tid] = rv_s[(size_t)ring * DV + tid];
-    }
+    // ---- 5. the next evictee's N, z; the header ----
     if (warp == kEvWarp && lane < kSG) {
-        float sr[PD];
-        slot_load<D>(s_sm, sub, sr);
-        slot_store<D>(sg, sub, sr);
         if (nxt) {
             // N of the next evictee: summed partials + this step's write (slot_axpy's order)
             float Nn[PV];
@@ -834,9 +839,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
             if (lane == 0) evs[DV] = zn;
         }
     }
-    if (tid < DK) IO<T>::st(wk, (int64_t)ring * DK + tid, xk[tid]);
-    if (tid < DV) wvv[(int64_t)ring * DV + tid] = nv_s[tid];
-    if (tid < D) wphg[(int64_t)ring * D + tid] = phk[tid];
     if (tid == 0) {
         winpos[ring] = t;
         hdr[HDR_T] = t + 1;
