@@ -42,12 +42,14 @@ struct DecArgs {
     int prefetch_ahead;   // heads ahead of this one whose state is prefetched into L2 (0: none)
 };
 
-// Ask L2 to fetch [p, p + bytes) with bulk prefetches of at most 16 KB each, one per thread
-// (p 16-byte aligned, bytes a multiple of 16): the CTA that processes that head about one wave
-// later then finds its state in L2 instead of waiting on DRAM.
+// Ask L2 to fetch [p, p + bytes) with bulk prefetches of at most 16 KB each, issued by
+// lane 0 of successive warps (p 16-byte aligned, bytes a multiple of 16): the CTA that
+// processes that head about one wave later then finds its state in L2 instead of DRAM.
 constexpr int kPrefetchChunk = 16384;
 __device__ __forceinline__ void prefetch_l2(const char* p, int64_t bytes, int tid, int nthreads) {
-    for (int64_t o = (int64_t)tid * kPrefetchChunk; o < bytes; o += (int64_t)nthreads * kPrefetchChunk) {
+    if (tid % kWarp != 0) return;
+    for (int64_t o = (int64_t)(tid / kWarp) * kPrefetchChunk; o < bytes;
+         o += (int64_t)(nthreads / kWarp) * kPrefetchChunk) {
         const int64_t left = bytes - o;
         const uint32_t n = (uint32_t)(left < kPrefetchChunk ? left : kPrefetchChunk);
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"(n) : "memory");
