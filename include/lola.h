@@ -142,7 +142,12 @@ int32_t lola_state_init(const lola_config* cfg, void* state, void* stream);
  *   write_pos  nullable device int32 [B, Hh, n]: the position written into (H, s) at each
  *         step, or -1 when the step wrote nothing (the decision log)
  *   workspace  device, >= lola_prefill_workspace_bytes(cfg, n), 256-byte aligned
- * n >= 1.  Every device pointer must be 16-byte aligned. */
+ * n >= 1.  Every device pointer must be 16-byte aligned.
+ * Stream-ordered on `stream`: the call forks the feature map of the queries onto the
+ * library's lower-priority side stream (it runs beside the selection chain) and joins it
+ * back before the output pass, so all of the call's work precedes later work on `stream`.
+ * The first call on a device (with that device current) creates that side stream and two
+ * events, held until the process exits; make it before any stream capture starts. */
 int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const void* K,
                      const void* V, const float* W, int64_t w_head_stride, void* Y, void* state,
                      int32_t* write_pos, void* workspace, size_t workspace_bytes, void* stream);
@@ -171,8 +176,9 @@ int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* hos
  *   - every device that loads the library holds that array until the process exits;
  *   - the call allocates nothing (no cudaMalloc, cudaFree or allocating library routine);
  *   - the first call on a device (with that device current) looks up the array's device
- *     address with cudaGetSymbolAddress and caches it; make that first call before any
- *     stream capture starts;
+ *     address with cudaGetSymbolAddress and caches it, and (as lola_prefill's first call)
+ *     creates the side stream and its two events; make that first call before any stream
+ *     capture starts;
  *   - all calls on a device share the one array and it keeps the last call's contents, so
  *     calls that overlap on the GPU (different streams, or different host threads, on the
  *     same device) race with each other: serialise them;
@@ -187,8 +193,9 @@ int32_t lola_prefill_noalloc(const lola_config* cfg, int32_t n, const void* Q, c
 
 /* ---- tracing: per-kernel device time of the library's own launches --------------------
  * When enabled, every kernel launch of lola_prefill / lola_decode_step / lola_state_init is
- * bracketed by two CUDA events on the call's stream (a few microseconds of overhead per
- * launch, no device memory).  Kernel ids: */
+ * bracketed by two CUDA events on the stream it runs on (the call's stream; the side stream
+ * for the queries' feature map, whose time then includes sharing the GPU with the selection
+ * chain); a few microseconds of overhead per launch, no device memory.  Kernel ids: */
 typedef enum {
     LOLA_KERNEL_STATE_INIT = 0,  /* state reset */
     LOLA_KERNEL_PHI = 1,         /* feature map of Q and K */

@@ -87,6 +87,35 @@ cudaError_t traced(int id, cudaStream_t st, F&& launch) {
     return cudaSuccess;
 }
 
+// ---- a lower-priority side stream per device: the feature map of the queries runs on it
+// while the selection chain (one CTA per head: 128 of the 152 SMs at 4 x 32 heads) runs on
+// the caller's stream, then the caller's stream waits for it before the output pass ----
+struct SideStream {
+    cudaStream_t st = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+std::mutex g_side_mu;   // held from the fork to the join of one call (host side only)
+SideStream g_side[kMaxDevices];
+
+cudaError_t side_stream_locked(SideStream** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    SideStream& s = g_side[dev];
+    if (!s.st) {
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s.st, cudaStreamNonBlocking, least);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.fork, cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s.join, cudaEventDisableTiming);
+        if (e != cudaSuccess) return e;
+    }
+    *out = &s;
+    return cudaSuccess;
+}
+
 void drain_pending(int id) {
     std::vector<TimedLaunch> keep;
     for (auto& r : g_pending) {
@@ -244,12 +273,28 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     e = traced(LOLA_KERNEL_PHI, st,
                [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, ws.phiKb, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(K)");
-    e = traced(LOLA_KERNEL_PHI, st,
-               [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
-    e = traced(LOLA_KERNEL_SELECT, st,
-               [&]() { return launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st); });
-    if (e != cudaSuccess) return cuda_fail(e, "selection");
+    {
+        // the selection on the caller's stream, phi(Q) beside it on the side stream (launched
+        // second, at lower priority, so the chain's CTAs are placed first)
+        std::lock_guard<std::mutex> g(g_side_mu);
+        SideStream* side = nullptr;
+        e = side_stream_locked(&side);
+        if (e != cudaSuccess) return cuda_fail(e, "side stream");
+        e = cudaEventRecord(side->fork, st);
+        if (e != cudaSuccess) return cuda_fail(e, "fork");
+        e = traced(LOLA_KERNEL_SELECT, st,
+                   [&]() { return launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "selection");
+        e = cudaStreamWaitEvent(side->st, side->fork, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "fork wait");
+        e = traced(LOLA_KERNEL_PHI, side->st,
+                   [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, side->st); });
+        if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
+        e = cudaEventRecord(side->join, side->st);
+        if (e != cudaSuccess) return cuda_fail(e, "join");
+        e = cudaStreamWaitEvent(st, side->join, 0);
+        if (e != cudaSuccess) return cuda_fail(e, "join wait");
+    }
     e = traced(LOLA_KERNEL_OUTPUT, st, [&]() {
         return output_tc_supported(d)
                    ? launch_output_tc(d, n, ws, Q, K, V, Y, static_cast<char*>(state), L.head_bytes, st)
