@@ -303,25 +303,61 @@ def run_prefill(L, R, args, pk):
     if phi:
         byts = heads * w.n * (w.d * 2 + w.D * 4)
         phi["achieved_gbs"] = byts / (phi["avg_ms"] / 1e3) / 1e9
-    # end to end: pinned host inputs in, Y back to pinned host memory, every step
+    # end to end through the C ABI: every step's Q, K, V copied in from pinned host memory and
+    # its Y copied back to pinned host memory.  The copies run on a copy stream into a second
+    # set of device buffers, so step i + 1's inputs travel while step i computes (double
+    # buffering); the timed region spans from before the first copy to after the last read-back.
     if not args.no_e2e:
         hq, hk, hv = (t.cpu().pin_memory() for t in (Q, K, V))
         hy = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+        bufs = [(Q, K, V, Y), tuple(torch.empty_like(t) for t in (Q, K, V, Y))]
+        cs = torch.cuda.Stream(device=dev)
+        copied = [torch.cuda.Event(), torch.cuda.Event()]
+        done = [torch.cuda.Event(), torch.cuda.Event()]
 
-        def e2e_step():
-            Q.copy_(hq, non_blocking=True)
-            K.copy_(hk, non_blocking=True)
-            V.copy_(hv, non_blocking=True)
-            step()
-            hy.copy_(Y, non_blocking=True)
+        def h2d(b):
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b])          # the compute that last read buffer b
+                for dst, src in zip(bufs[b][:3], (hq, hk, hv)):
+                    dst.copy_(src, non_blocking=True)
+                copied[b].record(cs)
 
-        e2e_step()
-        torch.cuda.synchronize()
+        def compute(b):
+            stream.wait_event(copied[b])
+            q_, k_, v_, y_ = bufs[b]
+            L.lola_prefill(lay.cfg, w.n, q_, k_, v_, W, 0, y_, lay.state, wpos, ws, stream)
+            done[b].record(stream)
+
+        def d2h(b):
+            with torch.cuda.stream(cs):
+                cs.wait_event(done[b])
+                hy.copy_(bufs[b][3], non_blocking=True)
+
+        def pipeline(nsteps):
+            start = torch.cuda.Event(enable_timing=True)
+            end = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            start.record(stream)
+            cs.wait_event(start)
+            h2d(0)
+            for i in range(nsteps):
+                b = i % 2
+                if i + 1 < nsteps:
+                    h2d(1 - b)
+                compute(b)
+                d2h(b)
+            stream.wait_stream(cs)
+            end.record(stream)
+            torch.cuda.synchronize()
+            return start.elapsed_time(end)
+
+        pipeline(2)
         R.barrier()
-        ems = R.max(time_loop(e2e_step, args.steps, stream)) / args.steps
+        ems = R.max(pipeline(args.steps)) / args.steps
         res["e2e"] = {"value": R.world * tokens / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
                       "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(),
-                      "d2h_bytes_per_step": Y.numel() * Y.element_size()}
+                      "d2h_bytes_per_step": Y.numel() * Y.element_size(),
+                      "overlap": "step i+1's inputs are copied while step i computes (two device buffers)"}
     res["x"] = x
     return res
 
