@@ -157,12 +157,12 @@ class Clocks:
 CSRC = os.path.join(ROOT, "sparse_exact_kv_gb300", "csrc")
 NCU_TRAFFIC = {
     # w2 prefill (4 x 32 heads, n = 4096): one select launch
-    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "8a4e40c300f5ff74",
-               "bytes_per_launch": 409095936 + 131939840},
+    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "c1bc18db426f8ac7",
+               "bytes_per_launch": 409313536 + 131975680},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
-    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "f27b37c23056869b",
-               "bytes_per_launch": 2 * (205230592 + 55027917)},
+    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "c4728e6b425b3f04",
+               "bytes_per_launch": 2 * (205599999 + 56527360)},
 }
 
 
