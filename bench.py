@@ -399,7 +399,7 @@ def run_decode(L, R, args, pk):
         ms = time_loop(step, steps, stream)
         R.barrier()
         L.lola_kernel_timing(False)
-        kt = kernel_times(L, ["decode"])
+        kt = kernel_times(L, ["phi", "decode"])
     ms = R.max(ms) / steps
     heads = w.B * w.Hh
     res = {"metric": "decode tokens/s per layer", "value": R.world * w.B / (ms / 1e3), "unit": "tokens/s",

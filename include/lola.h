@@ -97,13 +97,15 @@ typedef struct {
  *   ev         float32 [d_v + 4]         the next evictee (token t - eta, eta > 0): its
  *                                        H^T phi(k) in [0, d_v) and s^T phi(k) at [d_v],
  *                                        both against the memory after token t - 1
+ *   tok_phi    float32 [2][D]            scratch of lola_decode_step: phi(q), phi(k) of the
+ *                                        token being decoded (no meaning between calls)
  * The appendix-B element count (eta + lambda)(d_k + d_v) + D d_v + D is the window,
  * cache, H and s above; win_phi, c_phi, c_N, c_z, ev, positions and the header are the
  * bookkeeping that lets a decode step score the cache without recomputing H^T phi(k). */
 
 typedef struct {
     int64_t head_bytes;
-    int64_t H, s, win_pos, win_k, win_v, win_phi, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
+    int64_t H, s, win_pos, win_k, win_v, win_phi, c_pos, c_k, c_v, c_phi, c_N, c_z, ev, tok_phi;
 } lola_state_layout;
 
 /* Library version (major * 10000 + minor * 100 + patch). */
@@ -135,7 +137,8 @@ int32_t lola_state_init(const lola_config* cfg, void* state, void* stream);
  * (section 2.4, Eqs. 11-13; output section 2.5, Eq. 14).
  *   Q, K  device io [B, Hh, n, d_k];  V device io [B, Hh, n, d_v]
  *   W     device float32 [D/2, d_k] shared by all heads when w_head_stride == 0, else head
- *         h uses W + h * w_head_stride (elements)
+ *         h uses W + h * w_head_stride (elements; a multiple of 4, so that every head's W
+ *         starts on a 16-byte boundary, else LOLA_ERR_INVALID_ARG)
  *   Y     device io [B, Hh, n, d_v]: the outputs y_0 .. y_{n-1}
  *   state device, lola_state_bytes(cfg): overwritten with the memory after token n-1,
  *         ready for lola_decode_step
@@ -198,7 +201,7 @@ int32_t lola_prefill_noalloc(const lola_config* cfg, int32_t n, const void* Q, c
  * chain); a few microseconds of overhead per launch, no device memory.  Kernel ids: */
 typedef enum {
     LOLA_KERNEL_STATE_INIT = 0,  /* state reset */
-    LOLA_KERNEL_PHI = 1,         /* feature map of Q and K */
+    LOLA_KERNEL_PHI = 1,         /* feature map of Q and K (in a decode step: of the token's q, k) */
     LOLA_KERNEL_SELECT = 2,      /* allocation chain: SRE scoring, argmin, (H, s) write */
     LOLA_KERNEL_OUTPUT = 3,      /* co-normalised output of every query */
     LOLA_KERNEL_DECODE = 4,      /* one decode step */

@@ -45,7 +45,7 @@ class lola_config(ctypes.Structure):
 class lola_state_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int64) for n in
                 ("head_bytes", "H", "s", "win_pos", "win_k", "win_v", "win_phi", "c_pos", "c_k", "c_v", "c_phi",
-                 "c_N", "c_z", "ev")]
+                 "c_N", "c_z", "ev", "tok_phi")]
 
 
 class LolaError(RuntimeError):

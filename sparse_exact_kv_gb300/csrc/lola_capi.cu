@@ -223,6 +223,7 @@ int32_t lola_state_layout_of(const lola_config* cfg, lola_state_layout* out) {
     out->c_N = L.c_N;
     out->c_z = L.c_z;
     out->ev = L.ev;
+    out->tok_phi = L.tok_phi;
     return LOLA_OK;
 }
 
@@ -256,7 +257,7 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     if (n < 1) return LOLA_ERR_INVALID_ARG;
     if ((int64_t)n * d.BH * d.D > ((int64_t)1 << 40)) return LOLA_ERR_UNSUPPORTED;
     if (!Q || !K || !V || !W || !Y || !state || !workspace) return LOLA_ERR_INVALID_ARG;
-    if (w_head_stride < 0) return LOLA_ERR_INVALID_ARG;
+    if (w_head_stride < 0 || w_head_stride % 4 != 0) return LOLA_ERR_INVALID_ARG;
     const void* ptrs[] = {Q, K, V, W, Y, state, workspace};
     for (const void* p : ptrs)
         if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;
@@ -309,15 +310,22 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W, in
     Dims d;
     int32_t s = to_dims(cfg, &d);
     if (s != LOLA_OK) return s;
-    if (!state || !W || !q || !k || !v || !y || w_head_stride < 0) return LOLA_ERR_INVALID_ARG;
+    if (!state || !W || !q || !k || !v || !y || w_head_stride < 0 || w_head_stride % 4 != 0)
+        return LOLA_ERR_INVALID_ARG;
     const void* ptrs[] = {state, W, q, k, v, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;
     if (written_pos && (reinterpret_cast<uintptr_t>(written_pos) & 3)) return LOLA_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
+    const Layout L = make_layout(d);
+    if (decode_uses_tok_phi(d)) {
+        const cudaError_t e = traced(LOLA_KERNEL_PHI, st, [&]() {
+            return launch_tok_phi(d, static_cast<char*>(state), L, W, w_head_stride, q, k, st);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "decode step feature map");
+    }
     cudaError_t e = traced(LOLA_KERNEL_DECODE, st, [&]() {
-        return launch_decode(d, static_cast<char*>(state), make_layout(d), W, w_head_stride, q, k, v, y, written_pos,
-                             st);
+        return launch_decode(d, static_cast<char*>(state), L, W, w_head_stride, q, k, v, y, written_pos, st);
     });
     return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "decode step");
 }

@@ -18,11 +18,14 @@
 #include <climits>
 
 #include "lola_chain.cuh"
+#include "lola_tc.cuh"
 
 namespace lola {
 namespace {
 
 using namespace chain;
+using tc::mbar_init;
+using tc::mbar_wait;
 
 constexpr int kDecWarps = kThreads / kWarp;
 constexpr int kSlotsPerPass = kThreads / kSG;   // 64
@@ -43,13 +46,15 @@ struct DecArgs {
 };
 
 // Ask L2 to fetch [p, p + bytes) with bulk prefetches of at most 16 KB each, issued by
-// lane 0 of successive warps (p 16-byte aligned, bytes a multiple of 16): the CTA that
-// processes that head about one wave later then finds its state in L2 instead of DRAM.
+// lane 0 of successive warps from warp first_warp on (p 16-byte aligned, bytes a multiple of
+// 16): the CTA that processes that head about one wave later then finds its state in L2
+// instead of DRAM.
 constexpr int kPrefetchChunk = 16384;
-__device__ __forceinline__ void prefetch_l2(const char* p, int64_t bytes, int tid, int nthreads) {
+__device__ __forceinline__ void prefetch_l2(const char* p, int64_t bytes, int tid, int nthreads, int first_warp = 0) {
     if (tid % kWarp != 0) return;
-    for (int64_t o = (int64_t)(tid / kWarp) * kPrefetchChunk; o < bytes;
-         o += (int64_t)(nthreads / kWarp) * kPrefetchChunk) {
+    const int nw = nthreads / kWarp;
+    const int rank = (tid / kWarp - first_warp + nw) % nw;
+    for (int64_t o = (int64_t)rank * kPrefetchChunk; o < bytes; o += (int64_t)nw * kPrefetchChunk) {
         const int64_t left = bytes - o;
         const uint32_t n = (uint32_t)(left < kPrefetchChunk ? left : kPrefetchChunk);
         asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p + o), "r"(n) : "memory");
@@ -420,12 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
 // ---------------------------------------------------------------------------------
 constexpr int kFastLam = 64;
 constexpr int kFastEta = 128;
-
-__device__ __forceinline__ void cp16(void* dst_smem, const void* src) {
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst_smem)),
-                 "l"(src)
-                 : "memory");
-}
+constexpr size_t kMaxSmemPerCta = 227 * 1024;   // opt-in dynamic shared memory of one sm_103 CTA
 
 // values 2 kc and 2 kc + 1 of a value row (float32 or bfloat16, widened exactly)
 template <typename T>
@@ -447,8 +447,8 @@ struct FastSmem {
     static constexpr int NRG = Shape<D, DV>::NRG;   // H row groups (partials)
     static constexpr size_t a16(size_t x) { return (x + 15) / 16 * 16; }
     // byte offsets (16-byte aligned)
-    static constexpr size_t W = 0;                                          // [D/2][DK+4] f32
-    static constexpr size_t CPHI = a16(W + 4 * (D / 2) * w_stride<DK>());   // [64][D] f32
+    static constexpr size_t HST = 0;                                        // [D][DV] f32 H, for its bulk store
+    static constexpr size_t CPHI = HST + 4 * D * DV;                       // [64][D] f32; then the N rows' bulk store
     static constexpr size_t CV = CPHI + 4 * kFastLam * D;                  // [64][DV] T
     static constexpr size_t CK = CV + sizeof(T) * kFastLam * DV;           // [64][DK] T
     static constexpr size_t RK = CK + sizeof(T) * kFastLam * DK;           // [kFastEta][DK] T
@@ -460,19 +460,46 @@ struct FastSmem {
     static constexpr size_t SS = EVN + 4 * (DV + 4);                       // [D] f32 s
     static constexpr size_t XQ = SS + 4 * D;                               // [DK] f32
     static constexpr size_t XK = XQ + 4 * DK;                              // [DK] f32
-    static constexpr size_t XV = XK + 4 * DK;                              // [DV] f32
-    static constexpr size_t PHQ = XV + 4 * DV;                             // [D] f32
+    static constexpr size_t PHQ = XK + 4 * DK;                             // [D] f32
     static constexpr size_t PHK = PHQ + 4 * D;                             // [D] f32
     static constexpr size_t RED = PHK + 4 * D;                             // [NRG][DV] f32
     static constexpr size_t RED2 = RED + 4 * NRG * DV;                     // [NRG][DV] f32
     static constexpr size_t NPART = RED2 + 4 * NRG * DV;                   // [DV] f32 next evictee's summed partials
     static constexpr size_t LIN = NPART + 4 * DV;                          // [DV] f32
     static constexpr size_t SC = LIN + 4 * DV;                             // [kFastEta + 64] f32
-    static constexpr size_t VOFF = SC + 4 * (kFastEta + kFastLam);         // [kFastEta + 64] i32 value-row offsets
+    static constexpr size_t PB = SC + 4 * (kFastEta + kFastLam);           // [kFastEta + 64] f32 weights
+    static constexpr size_t LPART = PB + 4 * (kFastEta + kFastLam);        // [16] f32 per-warp weight sums
+    static constexpr size_t VOFF = LPART + 4 * kDecWarps;                  // [kFastEta + 64] i32 value-row offsets
     static constexpr size_t WKEY = VOFF + 4 * (kFastEta + kFastLam);       // [17] uint2
     static constexpr size_t MISC = WKEY + 8 * 18;                          // [8] f32
-    static constexpr size_t TOTAL = MISC + 4 * 8;
+    static_assert(DV <= D, "the N rows are staged in the slot phi rows");
+    static constexpr size_t MBAR = a16(MISC + 4 * 8);                      // u64 burst barrier
+    static constexpr size_t TOTAL = MBAR + 8;
 };
+
+// bulk copies (TMA engine) of the burst, completing on an mbarrier
+constexpr uint64_t kBurstWaitNs = 1000000000ull;   // a burst that has not landed in 1 s is an error
+__device__ __forceinline__ void mbar_expect(uint32_t mbar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+}
+// [src, src + bytes) -> shared dst; both 16-byte aligned, bytes a nonzero multiple of 16
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint32_t mbar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src), "r"(bytes), "r"(mbar)
+                 : "memory");
+}
+// shared [src, src + bytes) -> global dst (same rules), in this thread's current bulk group
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"((uint32_t)__cvta_generic_to_shared(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// the shared-memory sources of this thread's bulk stores have been read
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// this thread's shared-memory writes become visible to the bulk copies (async proxy)
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs a) {
@@ -480,10 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     using M = FastSmem<D, DV, T>;
     constexpr int DK = D;
     constexpr int PD = S::PD, PV = S::PV, HR = S::HR, HC = S::HC;
-    constexpr int KS = kThreads / DV;        // key splits of the output numerator
     constexpr int kEvWarp = kDecWarps - 1;
     extern __shared__ __align__(16) uint8_t smb[];
-    float* Ws = reinterpret_cast<float*>(smb + M::W);
+    float* hst = reinterpret_cast<float*>(smb + M::HST);
     float* cphi_s = reinterpret_cast<float*>(smb + M::CPHI);
     T* cv_s = reinterpret_cast<T*>(smb + M::CV);
     T* ck_s = reinterpret_cast<T*>(smb + M::CK);
@@ -496,7 +522,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     float* s_sm = reinterpret_cast<float*>(smb + M::SS);
     float* xq = reinterpret_cast<float*>(smb + M::XQ);
     float* xk = reinterpret_cast<float*>(smb + M::XK);
-    float* xv = reinterpret_cast<float*>(smb + M::XV);
     float* phq = reinterpret_cast<float*>(smb + M::PHQ);
     float* phk = reinterpret_cast<float*>(smb + M::PHK);
     float* red = reinterpret_cast<float*>(smb + M::RED);
@@ -504,12 +529,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     float* npart = reinterpret_cast<float*>(smb + M::NPART);
     float* lin = reinterpret_cast<float*>(smb + M::LIN);
     float* sc = reinterpret_cast<float*>(smb + M::SC);
+    float* pb = reinterpret_cast<float*>(smb + M::PB);
+    float* lpart = reinterpret_cast<float*>(smb + M::LPART);
     int* voff = reinterpret_cast<int*>(smb + M::VOFF);
     uint2* wkey = reinterpret_cast<uint2*>(smb + M::WKEY);
     float* misc = reinterpret_cast<float*>(smb + M::MISC);
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int bh = blockIdx.x, h = bh % a.Hh;
+    const int bh = blockIdx.x;
     const int eta = a.eta, lam = a.lam;
     char* rec = a.state + (int64_t)bh * a.L.head_bytes;
     int32_t* hdr = reinterpret_cast<int32_t*>(rec);
@@ -535,39 +562,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const bool nxt = t + 1 - eta >= 0;
     const int nring = (t + 1) % eta;
 
-    // ---- 1. one burst of loads: the exact KV of cache and window, the slots' phi, the two
-    //         evictees' phi, s and the evictee's N, z by cp.async; W, the new token, H and
-    //         the slots' N, z, positions by plain loads ----
-    {
-        constexpr int PHI_CH = D / 4, V_CH = DV * (int)sizeof(T) / 16, K_CH = DK * (int)sizeof(T) / 16;
-        for (int i = tid; i < nc * PHI_CH; i += kThreads)
-            cp16(cphi_s + (size_t)(i / PHI_CH) * D + 4 * (i % PHI_CH), cphi + (size_t)(i / PHI_CH) * D + 4 * (i % PHI_CH));
-        for (int i = tid; i < nc * V_CH; i += kThreads)
-            cp16(reinterpret_cast<uint8_t*>(cv_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(cv) + 16 * (size_t)i);
-        for (int i = tid; i < nc * K_CH; i += kThreads)
-            cp16(reinterpret_cast<uint8_t*>(ck_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(ck) + 16 * (size_t)i);
-        for (int i = tid; i < eta * K_CH; i += kThreads)
-            cp16(reinterpret_cast<uint8_t*>(rk_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(wk) + 16 * (size_t)i);
-        for (int i = tid; i < eta * V_CH; i += kThreads)
-            cp16(reinterpret_cast<uint8_t*>(rv_s) + 16 * (size_t)i, reinterpret_cast<const uint8_t*>(wvv) + 16 * (size_t)i);
-        if (tid < PHI_CH) {
-            if (ev) cp16(phe + 4 * tid, wphg + (size_t)ring * D + 4 * tid);
-            if (nxt) cp16(phn + 4 * tid, wphg + (size_t)nring * D + 4 * tid);
-            cp16(s_sm + 4 * tid, sg + 4 * tid);
+    // ---- 1. one burst of bulk copies issued by lanes of warp 0 (the TMA engine moves them
+    //         while the threads load): the exact KV of cache and window, the slots' phi, the
+    //         two evictees' phi, s, the evictee's N, z and phi(q), phi(k) of the token (from
+    //         the tok_phi scratch, filled by tok_phi_kernel just before).  The new token, H
+    //         and the slots' N, z, positions come by plain loads meanwhile ----
+    const uint32_t bar = (uint32_t)__cvta_generic_to_shared(smb + M::MBAR);
+    int* fail = reinterpret_cast<int*>(misc + 7);
+    if (warp == 0) {
+        constexpr uint32_t kPhiB = 4 * D, kKB = sizeof(T) * DK, kVB = sizeof(T) * DV;
+        const uint32_t bytes = (uint32_t)nc * (kPhiB + kVB + kKB) + (uint32_t)eta * (kKB + kVB) +
+                               (ev ? kPhiB + 4 * (DV + 4) : 0) + (nxt ? kPhiB : 0) + 3 * kPhiB;
+        if (lane == 0) {
+            *fail = 0;
+            mbar_init(bar, 1);
+            mbar_expect(bar, bytes);
         }
-        if (tid < (DV + 4) / 4 && ev) cp16(evn + 4 * tid, evs + 4 * tid);
+        __syncwarp();
+        switch (lane) {
+            case 0: if (nc > 0) bulk_g2s(cphi_s, cphi, nc * kPhiB, bar); break;
+            case 1: bulk_g2s(rk_s, wk, eta * kKB, bar); break;
+            case 2: if (nc > 0) bulk_g2s(cv_s, cv, nc * kVB, bar); break;
+            case 3: bulk_g2s(rv_s, wvv, eta * kVB, bar); break;
+            case 4: if (nc > 0) bulk_g2s(ck_s, ck, nc * kKB, bar); break;
+            case 5: if (ev) bulk_g2s(phe, wphg + (size_t)ring * D, kPhiB, bar); break;
+            case 6: if (nxt) bulk_g2s(phn, wphg + (size_t)nring * D, kPhiB, bar); break;
+            case 7: bulk_g2s(s_sm, sg, kPhiB, bar); break;
+            case 8: if (ev) bulk_g2s(evn, evs, 4 * (DV + 4), bar); break;
+            case 9: bulk_g2s(phq, rec + a.L.tok_phi, 2 * kPhiB, bar); break;   // phq, phk
+            default: break;
+        }
     }
-    const float* Wh = a.W + (int64_t)h * a.w_head_stride;
-    stage_w<DK, D, kThreads>(Ws, Wh, tid);
     if (tid < DK) {
         xq[tid] = IO<T>::ld(static_cast<const T*>(a.q) + (int64_t)bh * DK, tid);
         xk[tid] = IO<T>::ld(static_cast<const T*>(a.k) + (int64_t)bh * DK, tid);
     }
-    if (tid < DV) {
-        const T* vin = static_cast<const T*>(a.v) + (int64_t)bh * DV;
-        xv[tid] = IO<T>::ld(vin, tid);
-        nv_s[tid] = vin[tid];
-    }
+    if (tid < DV) nv_s[tid] = static_cast<const T*>(a.v)[(int64_t)bh * DV + tid];
     float hreg[HR * HC];
     h_load<D, DV>(hreg, Hg, warp, lane);
     // slot role (one pass: lambda <= 64)
@@ -582,32 +612,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         sz = cz[sl];
         spos = cpos[sl];
     }
-    __syncthreads();   // W and the new token staged; the burst may still be in flight
-
-    // ---- 2a. phi(q), phi(k_t) while the burst lands ----
-    if (warp == 0) {
-        float ph[D / 32];
-        phi_warp<DK, D>(xq, Ws, lane, ph);
-#pragma unroll
-        for (int m = 0; m < D / 32; ++m) phq[lane + 32 * m] = ph[m];
-    } else if (warp == 1) {
-        float ph[D / 32];
-        phi_warp<DK, D>(xk, Ws, lane, ph);
-#pragma unroll
-        for (int m = 0; m < D / 32; ++m) phk[lane + 32 * m] = ph[m];
-    }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncthreads();   // the new token staged, the barrier initialised; the burst may still be in flight
+    if (!mbar_wait(bar, 0, kBurstWaitNs)) *fail = 1;
     __syncthreads();
+    if (*fail) {
+        // the burst did not land in time: flag the head and leave once its copies are done
+        if (tid == 0) {
+            atomicOr(&hdr[HDR_STATUS], (int)ST_TIMEOUT);
+            mbar_wait(bar, 0, kBurstWaitNs);
+        }
+        return;
+    }
     if (ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
     // the state of the head one wave ahead, into L2 (all heads step together, so its window
     // ring rows for this step are ring and nring as here); the window phi ring is skipped
     // but for those two rows
     if (a.prefetch_ahead > 0 && bh + a.prefetch_ahead < a.BH) {
         const char* nr = a.state + (int64_t)(bh + a.prefetch_ahead) * a.L.head_bytes;
-        prefetch_l2(nr, a.L.win_phi, tid, kThreads);
-        prefetch_l2(nr + a.L.win_phi + (int64_t)ring * D * 4, D * 4, tid, kThreads);
-        prefetch_l2(nr + a.L.win_phi + (int64_t)nring * D * 4, D * 4, tid, kThreads);
-        prefetch_l2(nr + a.L.c_pos, a.L.head_bytes - a.L.c_pos, tid, kThreads);
+        // (spread over warps 1 .. 14: warp 0 has just issued the burst, warp 15 scores the
+        // evictee next)
+        prefetch_l2(nr, a.L.win_phi, tid, kThreads, 1);
+        prefetch_l2(nr + a.L.win_phi + (int64_t)ring * D * 4, D * 4, tid, kThreads, 2);
+        prefetch_l2(nr + a.L.win_phi + (int64_t)nring * D * 4, D * 4, tid, kThreads, 3);
+        prefetch_l2(nr + a.L.c_pos, a.L.head_bytes - a.L.c_pos, tid, kThreads, 8);
     }
 
     // ---- 2b. next evictee's partials; evictee and slot SREs ----
@@ -658,6 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         float vh[HC];
         h_cols<DV, T>(wvT, lane, vh);
         h_update<D, DV>(hreg, wphi, vh, warp);
+        h_store<D, DV>(hst, hreg, warp, lane);   // staged for one bulk store (issued after the scores)
         if (warp == kEvWarp && lane < kSG) {
             float wp[PD], sr[PD];
             slot_load<D>(wphi, sub, wp);
@@ -687,23 +715,26 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
             }
         }
     }
-    // ---- write back what is final now (the stores drain during the read): H, s and every
-    //      slot's N, z change only with a write; an append stores the evictee's own N, z;
-    //      the new cache row; the new token into the window ring ----
+    // ---- write back what is final now: H, s and every slot's N, z change only with a
+    //      write (H and the N rows go out as bulk stores from shared memory once the scores
+    //      are done; the moved slot's N row, whose phi row others still read, by plain
+    //      stores); an append stores the evictee's own N, z; the new cache row; the new
+    //      token into the window ring ----
     if (write) {
-        h_store<D, DV>(Hg, hreg, warp, lane);
         if (warp == kEvWarp && lane < kSG) {
             float sr[PD];
             slot_load<D>(s_sm, sub, sr);
             slot_store<D>(sg, sub, sr);
         }
         if (live) {
-            slot_store<DV>(cN + (size_t)sl * DV, sub, sN);
+            if (sl == wsel) slot_store<DV>(cN + (size_t)sl * DV, sub, sN);
+            else slot_store<DV>(cphi_s + (size_t)sl * DV, sub, sN);
             if (sub == 0) {
                 cz[sl] = sz;
                 if (sl == wsel) cpos[sl] = e;
             }
         }
+        fence_proxy_async();
     } else if (ev && sl == nc) {
         float Ne[PV];
         slot_load<DV>(evn, sub, Ne);
@@ -774,22 +805,27 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     h_partial_store<D, DV>(red2, phq, hreg, warp, lane);
     __syncthreads();
-    if (warp == 0) {
-        float m = -INFINITY;
-        for (int i = lane; i < nkeys; i += kWarp) m = fmaxf(m, sc[i]);
-        m = warp_max(m);
-        float l = 0.f;
-        for (int i = lane; i < nkeys; i += kWarp) {
-            const float p = expf(sc[i] - m);
-            sc[i] = p;
-            l += p;
-        }
-        l = warp_sum(l);
-        if (lane == 0) {
-            misc[1] = nkeys > 0 ? expf(-m) : 1.f;
-            misc[3] = l;
-        }
-    } else if (warp == kEvWarp) {
+    if (write && tid == 0) {
+        // H, then the N rows but the moved slot's: they drain while the output is formed
+        bulk_s2g(Hg, hst, 4 * D * DV);
+        if (wsel > 0) bulk_s2g(cN, cphi_s, 4 * DV * wsel);
+        const int r0 = wsel + 1;   // wsel = -1 (the evictee was written): every row
+        if (r0 < nc) bulk_s2g(cN + (size_t)r0 * DV, cphi_s + (size_t)r0 * DV, 4 * DV * (nc - r0));
+        bulk_commit();
+    }
+    // weights: every warp takes the maximum m over all scores (the order does not matter);
+    // thread i < nkeys forms p_i = exp(score_i - m); the per-warp sums of p are added in warp
+    // order at the end
+    float mx = -INFINITY;
+    for (int i = lane; i < nkeys; i += kWarp) mx = fmaxf(mx, sc[i]);
+    mx = warp_max(mx);
+    {
+        const float p = tid < nkeys ? expf(sc[tid] - mx) : 0.f;
+        if (tid < nkeys) pb[tid] = p;
+        const float lw = warp_sum(p);
+        if (lane == 0) lpart[warp] = lw;
+    }
+    if (warp == kEvWarp) {
         float sr[PD];
         slot_load<D>(s_sm, sub, sr);
         const float dl = slot_gram<D>(phq, sr, sub);
@@ -811,14 +847,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
             float v0[2], v1[2];
             h_cols2<T>(reinterpret_cast<const T*>(smb + voff[i]), kc, v0);
             h_cols2<T>(reinterpret_cast<const T*>(smb + voff[i + NS]), kc, v1);
-            const float p0 = sc[i], p1 = sc[i + NS];
+            const float p0 = pb[i], p1 = pb[i + NS];
             a0 = __ffma2_rn(make_float2(p0, p0), make_float2(v0[0], v0[1]), a0);
             a1 = __ffma2_rn(make_float2(p1, p1), make_float2(v1[0], v1[1]), a1);
         }
         if (i < nkeys) {
             float v0[2];
             h_cols2<T>(reinterpret_cast<const T*>(smb + voff[i]), kc, v0);
-            const float p0 = sc[i];
+            const float p0 = pb[i];
             a0 = __ffma2_rn(make_float2(p0, p0), make_float2(v0[0], v0[1]), a0);
         }
         *reinterpret_cast<float2*>(red + ks * DV + 2 * kc) = make_float2(a0.x + a1.x, a0.y + a1.y);
@@ -829,8 +865,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         float num = 0.f;
 #pragma unroll
         for (int r = 0; r < NS; ++r) num += red[r * DV + tid];
-        num = fmaf(misc[1], lin[tid], num);
-        const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
+        const float emx = expf(-mx);   // nkeys >= 1: the new token is always a key
+        num = fmaf(emx, lin[tid], num);
+        float l = 0.f;
+#pragma unroll
+        for (int w = 0; w < kDecWarps; ++w) l += lpart[w];
+        const float den = fmaf(emx, misc[4], l);
         IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
     }
 
@@ -851,12 +891,97 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         hdr[HDR_NCACHE] = nc_after;
         if (write) hdr[HDR_NWRITTEN] += 1;
         if (a.written_pos) a.written_pos[bh] = wposn;
+        bulk_wait_read();   // the bulk stores' shared-memory sources are read before the CTA ends
     }
+}
+
+// phi(q) and phi(k) of the token of every head into its tok_phi scratch, for
+// decode_fast_kernel.  Head h has 2B rows to map (q then k of every batch row); CTA (h, g)
+// stages W_h once and its kTokPhiWarps warps take kTokPhiRows consecutive rows each from
+// row kTokPhiRowsPerCta * g on, with the arithmetic of the prefill's feature map (phi_rows:
+// each row's result does not depend on how many rows a warp maps together).
+constexpr int kTokPhiWarps = 4;
+constexpr int kTokPhiRows = 8;
+constexpr int kTokPhiRowsPerCta = kTokPhiWarps * kTokPhiRows;
+template <int D, typename T>
+__global__ void __launch_bounds__(kTokPhiWarps * kWarp) tok_phi_kernel(const DecArgs a, int B) {
+    constexpr int DK = D;
+    constexpr int NT = kTokPhiWarps * kWarp;
+    extern __shared__ __align__(16) float smf[];
+    float* Ws = smf;                                    // [D/2][DK+4]
+    float* xs = smf + (D / 2) * w_stride<DK>();         // [kTokPhiWarps][kTokPhiRows][DK]
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int h = blockIdx.x;
+    const int j0 = blockIdx.y * kTokPhiRowsPerCta + warp * kTokPhiRows;   // this warp's first row
+    const int t = reinterpret_cast<const int32_t*>(a.state)[HDR_T];   // all heads are at step t
+    float* xw = xs + warp * kTokPhiRows * DK;
+    // the rows first (their loads overlap W's), then W
+    float xv[kTokPhiRows][DK / kWarp];
+#pragma unroll
+    for (int r = 0; r < kTokPhiRows; ++r) {
+        const int j = j0 + r;
+        const int b = j < B ? j : j - B;
+        const T* src = static_cast<const T*>(j < B ? a.q : a.k) + ((int64_t)b * a.Hh + h) * DK;
+#pragma unroll
+        for (int c = 0; c < DK / kWarp; ++c) xv[r][c] = j < 2 * B ? IO<T>::ld(src, lane + kWarp * c) : 0.f;
+    }
+    stage_w<DK, D, NT>(Ws, a.W + (int64_t)h * a.w_head_stride, tid);
+#pragma unroll
+    for (int r = 0; r < kTokPhiRows; ++r)
+#pragma unroll
+        for (int c = 0; c < DK / kWarp; ++c) xw[r * DK + lane + kWarp * c] = xv[r][c];
+    __syncthreads();
+    // with this CTA's own loads in: the state of decode_fast_kernel's first wave (heads
+    // 0 .. prefetch_ahead - 1) into L2, shared among this grid's CTAs (each later wave is
+    // prefetched by the wave before it); of the window phi ring only the two rows the step
+    // reads (the evictee's and the next one's)
+    {
+        const int ncta = gridDim.x * gridDim.y, cta = blockIdx.y * gridDim.x + blockIdx.x;
+        const int wave = a.prefetch_ahead < a.BH ? a.prefetch_ahead : a.BH;
+        const int64_t r0 = (int64_t)(t % a.eta) * 4 * D, r1 = (int64_t)((t + 1) % a.eta) * 4 * D;
+        for (int hb = cta; hb < wave; hb += ncta) {
+            const char* nr = a.state + (int64_t)hb * a.L.head_bytes;
+            prefetch_l2(nr, a.L.win_phi, tid, NT);
+            prefetch_l2(nr + a.L.c_pos, a.L.head_bytes - a.L.c_pos, tid, NT, 1);
+            prefetch_l2(nr + a.L.win_phi + r0, 4 * D, tid, NT, 2);
+            prefetch_l2(nr + a.L.win_phi + r1, 4 * D, tid, NT, 3);
+        }
+    }
+    float ph[kTokPhiRows][D / 32];
+    phi_rows<DK, D, kTokPhiRows>(xw, Ws, lane, ph);
+#pragma unroll
+    for (int r = 0; r < kTokPhiRows; ++r) {
+        const int j = j0 + r;
+        if (j >= 2 * B) break;
+        const int b = j < B ? j : j - B;
+        float* out = reinterpret_cast<float*>(a.state + ((int64_t)b * a.Hh + h) * a.L.head_bytes + a.L.tok_phi) +
+                     (j < B ? 0 : D);
+#pragma unroll
+        for (int m = 0; m < D / 32; ++m) out[lane + 32 * m] = ph[r][m];
+    }
+}
+
+// the fast path's limits (float32 KV at D = 128 does not fit one CTA's shared memory: the
+// general kernel runs it)
+template <int D, int DV, typename T>
+bool fast_fits(const Dims& d) {
+    return d.eta >= 1 && d.eta <= kFastEta && d.lam <= kFastLam && FastSmem<D, DV, T>::TOTAL <= kMaxSmemPerCta;
+}
+
+template <int D, typename T>
+cudaError_t launch_tok_phi_t(const Dims& d, const DecArgs& a, cudaStream_t st) {
+    const size_t smem = sizeof(float) * ((D / 2) * w_stride<D>() + kTokPhiRowsPerCta * D);
+    auto kern = tok_phi_kernel<D, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int B = d.BH / d.Hh;
+    kern<<<dim3(d.Hh, (2 * B + kTokPhiRowsPerCta - 1) / kTokPhiRowsPerCta), kTokPhiWarps * kWarp, smem, st>>>(a, B);
+    return cudaGetLastError();
 }
 
 template <int D, int DV, typename T>
 bool launch_decode_fast(const Dims& d, const DecArgs& a, cudaStream_t st, cudaError_t* err) {
-    if (d.eta < 1 || d.eta > kFastEta || d.lam > kFastLam) return false;
+    if (!fast_fits<D, DV, T>(d)) return false;
     const size_t smem = FastSmem<D, DV, T>::TOTAL;
     auto kern = decode_fast_kernel<D, DV, T>;
     *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -884,9 +1009,9 @@ cudaError_t launch_decode_t(const Dims& d, const DecArgs& a, cudaStream_t st) {
 
 }  // namespace
 
-cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
-                          const void* q, const void* k, const void* v, void* y, int32_t* written_pos,
-                          cudaStream_t st) {
+namespace {
+DecArgs make_args(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
+                  const void* q, const void* k, const void* v, void* y, int32_t* written_pos) {
     DecArgs a;
     a.state = state;
     a.L = L;
@@ -908,6 +1033,32 @@ cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const flo
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
             a.prefetch_ahead = sms;   // one resident CTA per SM
     }
+    return a;
+}
+}  // namespace
+
+bool decode_uses_tok_phi(const Dims& d) {
+    const bool bf = d.dtype == LOLA_BF16;
+    if (d.D == 128 && d.dv == 128) return bf ? fast_fits<128, 128, __nv_bfloat16>(d) : fast_fits<128, 128, float>(d);
+    if (d.D == 64 && d.dv == 64) return bf ? fast_fits<64, 64, __nv_bfloat16>(d) : fast_fits<64, 64, float>(d);
+    return false;
+}
+
+cudaError_t launch_tok_phi(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
+                           const void* q, const void* k, cudaStream_t st) {
+    const DecArgs a = make_args(d, state, L, W, w_head_stride, q, k, nullptr, nullptr, nullptr);
+    const bool bf = d.dtype == LOLA_BF16;
+    if (d.D == 128 && d.dk == 128)
+        return bf ? launch_tok_phi_t<128, __nv_bfloat16>(d, a, st) : launch_tok_phi_t<128, float>(d, a, st);
+    if (d.D == 64 && d.dk == 64)
+        return bf ? launch_tok_phi_t<64, __nv_bfloat16>(d, a, st) : launch_tok_phi_t<64, float>(d, a, st);
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
+                          const void* q, const void* k, const void* v, void* y, int32_t* written_pos,
+                          cudaStream_t st) {
+    const DecArgs a = make_args(d, state, L, W, w_head_stride, q, k, v, y, written_pos);
     const bool bf = d.dtype == LOLA_BF16;
     if (d.D == 128 && d.dv == 128)
         return bf ? launch_decode_t<128, 128, __nv_bfloat16>(d, a, st) : launch_decode_t<128, 128, float>(d, a, st);

@@ -23,7 +23,7 @@ __host__ __device__ inline int64_t align256(int64_t x) { return (x + 255) & ~int
 
 struct Layout {
     int64_t head_bytes;
-    int64_t H, s, win_pos, win_k, win_v, win_phi, c_pos, c_k, c_v, c_phi, c_N, c_z, ev;
+    int64_t H, s, win_pos, win_k, win_v, win_phi, c_pos, c_k, c_v, c_phi, c_N, c_z, ev, tok_phi;
 };
 
 inline Layout make_layout(const Dims& d) {
@@ -43,6 +43,7 @@ inline Layout make_layout(const Dims& d) {
     L.c_N = o;      o = align256(o + 4ll * d.lam * d.dv);
     L.c_z = o;      o = align256(o + 4ll * d.lam);
     L.ev = o;       o = align256(o + 4ll * (d.dv + 4));
+    L.tok_phi = o;  o = align256(o + 4ll * 2 * d.D);
     L.head_bytes = o;
     return L;
 }
@@ -219,6 +220,11 @@ cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void*
 bool output_tc_supported(const Dims& d);
 cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                              const void* V, void* Y, char* state, int64_t head_bytes, cudaStream_t st);
+// The fast decode kernel reads phi(q), phi(k) of the token from the state's tok_phi scratch:
+// when decode_uses_tok_phi(d), launch_tok_phi must run on the stream first.
+bool decode_uses_tok_phi(const Dims& d);
+cudaError_t launch_tok_phi(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
+                           const void* q, const void* k, cudaStream_t st);
 cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W,
                           int64_t w_head_stride, const void* q, const void* k, const void* v, void* y,
                           int32_t* written_pos, cudaStream_t st);

@@ -78,7 +78,7 @@ def test_state_layout_holds_appendix_b_memory(lib, d, eta, lam, dtype):
     regions = [(L.H, 4 * d * d), (L.s, 4 * d), (L.win_pos, 4 * eta), (L.win_k, io * eta * d), (L.win_v, io * eta * d),
                (L.win_phi, 4 * eta * d),
                (L.c_pos, 4 * lam), (L.c_k, io * lam * d), (L.c_v, io * lam * d), (L.c_phi, 4 * lam * d),
-               (L.c_N, 4 * lam * d), (L.c_z, 4 * lam), (L.ev, 4 * (d + 1))]
+               (L.c_N, 4 * lam * d), (L.c_z, 4 * lam), (L.ev, 4 * (d + 1)), (L.tok_phi, 4 * 2 * d)]
     end = 64
     for off, size in regions:
         assert off % 256 == 0 and off >= end
@@ -114,4 +114,10 @@ def test_null_and_misaligned_pointers_rejected_before_any_launch(lib):
     st = so.lola_decode_step(ctypes.byref(cfg), None, P(256), 0, P(256), P(256), P(256), P(256), None, None)
     assert st == lib.LOLA_ERR_INVALID_ARG
     st = so.lola_decode_step(ctypes.byref(cfg), P(256), P(256), -1, P(256), P(256), P(256), P(256), None, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG
+    # a per-head W must start on a 16-byte boundary: the stride is a multiple of 4 floats
+    st = so.lola_decode_step(ctypes.byref(cfg), P(256), P(256), 6, P(256), P(256), P(256), P(256), None, None)
+    assert st == lib.LOLA_ERR_INVALID_ARG
+    st = so.lola_prefill(ctypes.byref(cfg), 16, P(256), P(256), P(256), P(256), 6, P(256), P(256), None, P(256),
+                         1 << 30, None)
     assert st == lib.LOLA_ERR_INVALID_ARG

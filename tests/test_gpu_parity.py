@@ -142,7 +142,7 @@ def test_chunk_length_has_no_effect(L, dtype):
 
 
 @pytest.mark.parametrize("dtype,d,eta,lam", [("f32", 64, 16, 24), ("bf16", 128, 32, 64), ("bf16", 128, 8, 130),
-                                             ("f32", 64, 0, 5), ("f32", 64, 6, 0)])
+                                             ("f32", 128, 32, 64), ("f32", 64, 0, 5), ("f32", 64, 6, 0)])
 def test_prefill_then_decode_equals_longer_prefill(L, dtype, d, eta, lam):
     """prefill(x[:n]) followed by m decode steps reproduces prefill(x[:n+m]): the same
     decisions, outputs and final memory (the per-token rule is causal)."""
