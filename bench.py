@@ -254,6 +254,18 @@ def kernel_times(L, names):
     return out
 
 
+def traced_kernel_times(L, R, step, steps, stream, names):
+    """Per-kernel device times over `steps` more steps with the library's launch tracing on
+    (an event pair around every launch).  The timed loop runs without it, so the events do
+    not sit between its launches; its launch count per step is the same."""
+    L.lola_kernel_timing(True)
+    R.barrier()
+    time_loop(step, steps, stream)
+    R.barrier()
+    L.lola_kernel_timing(False)
+    return kernel_times(L, names)
+
+
 def run_prefill(L, R, args, pk):
     import torch
     import synth
@@ -275,12 +287,10 @@ def run_prefill(L, R, args, pk):
         step()
     torch.cuda.synchronize()
     with Clocks(R.local) as clk:
-        L.lola_kernel_timing(True)
         R.barrier()
         ms = time_loop(step, args.steps, stream)
         R.barrier()
-        L.lola_kernel_timing(False)
-        kt = kernel_times(L, ["state_init", "phi", "select", "output"])
+    kt = traced_kernel_times(L, R, step, args.steps, stream, ["state_init", "phi", "select", "output"])
     ms = R.max(ms) / args.steps
     tokens = w.B * w.n
     res = {"workload": w, "ms": ms, "value": R.world * tokens / (ms / 1e3), "kernels": kt, "clocks": clk.summary(),
@@ -370,7 +380,8 @@ def run_decode(L, R, args, pk):
         w = dataclasses.replace(w, B=args.decode_batch, decode_steps=args.warmup + args.decode_steps)
     x = synth.make_inputs(w)
     dev = torch.device("cuda", R.local)
-    steps = min(args.decode_steps, w.decode_steps - args.warmup)
+    # the timed steps, then as many again with per-kernel tracing (each step advances the state)
+    steps = min(args.decode_steps, (w.decode_steps - args.warmup) // 2)
     lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev)
     W = torch.from_numpy(x.W).to(dev)
     P = [dev_tensor(getattr(x, a)[:, :, :w.n], w.dtype, dev) for a in "qkv"]
@@ -379,7 +390,7 @@ def run_decode(L, R, args, pk):
     del P
     lay.workspace = None
     torch.cuda.empty_cache()
-    nt = args.warmup + steps
+    nt = args.warmup + 2 * steps
     dq, dk, dv = (dev_tensor(getattr(x, a)[:, :, w.n:w.n + nt].transpose(2, 0, 1, 3), w.dtype, dev) for a in "qkv")
     y = torch.empty(w.B, w.Hh, w.d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
@@ -394,12 +405,10 @@ def run_decode(L, R, args, pk):
         step()
     torch.cuda.synchronize()
     with Clocks(R.local) as clk:
-        L.lola_kernel_timing(True)
         R.barrier()
         ms = time_loop(step, steps, stream)
         R.barrier()
-        L.lola_kernel_timing(False)
-        kt = kernel_times(L, ["phi", "decode"])
+    kt = traced_kernel_times(L, R, step, steps, stream, ["phi", "decode"])
     ms = R.max(ms) / steps
     heads = w.B * w.Hh
     res = {"metric": "decode tokens/s per layer", "value": R.world * w.B / (ms / 1e3), "unit": "tokens/s",

@@ -461,8 +461,7 @@ struct FastSmem {
     static constexpr size_t XQ = SS + 4 * D;                               // [DK] f32
     static constexpr size_t XK = XQ + 4 * DK;                              // [DK] f32
     static constexpr size_t PHQ = XK + 4 * DK;                             // [D] f32
-    static constexpr size_t PHK = PHQ + 4 * D;                             // [D] f32
-    static constexpr size_t RED = PHK + 4 * D;                             // [NRG][DV] f32
+    static constexpr size_t RED = PHQ + 4 * D;                             // [NRG][DV] f32
     static constexpr size_t RED2 = RED + 4 * NRG * DV;                     // [NRG][DV] f32
     static constexpr size_t NPART = RED2 + 4 * NRG * DV;                   // [DV] f32 next evictee's summed partials
     static constexpr size_t LIN = NPART + 4 * DV;                          // [DV] f32
@@ -495,6 +494,10 @@ __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t by
                  "r"((uint32_t)__cvta_generic_to_shared(src)), "r"(bytes)
                  : "memory");
 }
+// programmatic dependent launch: wait for the preceding grid (a no-op without it) / let the
+// next grid start launching
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // the shared-memory sources of this thread's bulk stores have been read
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
@@ -523,7 +526,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     float* xq = reinterpret_cast<float*>(smb + M::XQ);
     float* xk = reinterpret_cast<float*>(smb + M::XK);
     float* phq = reinterpret_cast<float*>(smb + M::PHQ);
-    float* phk = reinterpret_cast<float*>(smb + M::PHK);
     float* red = reinterpret_cast<float*>(smb + M::RED);
     float* red2 = reinterpret_cast<float*>(smb + M::RED2);
     float* npart = reinterpret_cast<float*>(smb + M::NPART);
@@ -564,15 +566,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
 
     // ---- 1. one burst of bulk copies issued by lanes of warp 0 (the TMA engine moves them
     //         while the threads load): the exact KV of cache and window, the slots' phi, the
-    //         two evictees' phi, s, the evictee's N, z and phi(q), phi(k) of the token (from
-    //         the tok_phi scratch, filled by tok_phi_kernel just before).  The new token, H
-    //         and the slots' N, z, positions come by plain loads meanwhile ----
+    //         two evictees' phi, s and the evictee's N, z.  The new token, H and the slots'
+    //         N, z, positions come by plain loads meanwhile ----
     const uint32_t bar = (uint32_t)__cvta_generic_to_shared(smb + M::MBAR);
     int* fail = reinterpret_cast<int*>(misc + 7);
     if (warp == 0) {
         constexpr uint32_t kPhiB = 4 * D, kKB = sizeof(T) * DK, kVB = sizeof(T) * DV;
         const uint32_t bytes = (uint32_t)nc * (kPhiB + kVB + kKB) + (uint32_t)eta * (kKB + kVB) +
-                               (ev ? kPhiB + 4 * (DV + 4) : 0) + (nxt ? kPhiB : 0) + 3 * kPhiB;
+                               (ev ? kPhiB + 4 * (DV + 4) : 0) + (nxt ? kPhiB : 0) + kPhiB;
         if (lane == 0) {
             *fail = 0;
             mbar_init(bar, 1);
@@ -589,7 +590,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
             case 6: if (nxt) bulk_g2s(phn, wphg + (size_t)nring * D, kPhiB, bar); break;
             case 7: bulk_g2s(s_sm, sg, kPhiB, bar); break;
             case 8: if (ev) bulk_g2s(evn, evs, 4 * (DV + 4), bar); break;
-            case 9: bulk_g2s(phq, rec + a.L.tok_phi, 2 * kPhiB, bar); break;   // phq, phk
             default: break;
         }
     }
@@ -670,6 +670,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     __syncthreads();
 
     // ---- 3. decision (every warp) and write ----
+    // phi(q), phi(k) of the token come from tok_phi_kernel, which may still be running when
+    // this grid starts (programmatic dependent launch): wait for it, then fetch them into
+    // registers (used at the write-back: each warp the phi(q) entries of its own H rows, the
+    // first D threads the phi(k) row)
+    grid_dep_wait();
+    const float* tphi = reinterpret_cast<const float*>(rec + a.L.tok_phi);
+    const float pq = lane < HR ? tphi[warp * HR + lane] : 0.f;
+    const float pk = tid < D ? tphi[D + tid] : 0.f;
     const bool write = ev && (nc + 1 > lam);
     uint2 kk = lane <= kDecWarps ? wkey[lane] : make_uint2(kNoKey, kNoKey);
     warp_min_key(kk.x, kk.y);
@@ -751,7 +759,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     if (tid < DK) IO<T>::st(wk, (int64_t)ring * DK + tid, xk[tid]);
     if (tid < DV) wvv[(int64_t)ring * DV + tid] = nv_s[tid];
-    if (tid < D) wphg[(int64_t)ring * D + tid] = phk[tid];
+    if (tid < D) wphg[(int64_t)ring * D + tid] = pk;
+    if (lane < HR) phq[warp * HR + lane] = pq;   // this warp's rows (all of phq after the next barrier)
     // the next evictee: its partials summed in row-group order (column form); the gram of
     // this step's write with it (evictee warp; the correction is applied at the write-back)
     if (nxt && tid < DV) npart[tid] = reduce_partials_col<D, DV>(red, tid);
@@ -910,6 +919,8 @@ __global__ void __launch_bounds__(kTokPhiWarps * kWarp) tok_phi_kernel(const Dec
     extern __shared__ __align__(16) float smf[];
     float* Ws = smf;                                    // [D/2][DK+4]
     float* xs = smf + (D / 2) * w_stride<DK>();         // [kTokPhiWarps][kTokPhiRows][DK]
+    grid_dep_launch();   // decode_fast_kernel may start its burst now; it waits for this grid
+                         // before it reads tok_phi
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int h = blockIdx.x;
     const int j0 = blockIdx.y * kTokPhiRowsPerCta + warp * kTokPhiRows;   // this warp's first row
@@ -986,8 +997,18 @@ bool launch_decode_fast(const Dims& d, const DecArgs& a, cudaStream_t st, cudaEr
     auto kern = decode_fast_kernel<D, DV, T>;
     *err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (*err != cudaSuccess) return true;
-    kern<<<d.BH, kThreads, smem, st>>>(a);
-    *err = cudaGetLastError();
+    // launched as a programmatic dependent of tok_phi_kernel (the launch before it on `st`)
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(d.BH);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    *err = cudaLaunchKernelEx(&cfg, kern, a);
     return true;
 }
 
