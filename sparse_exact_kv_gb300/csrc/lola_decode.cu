@@ -667,6 +667,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         warp_min_key(khi, klo);
         if (lane == 0) wkey[warp] = make_uint2(khi, klo);
     }
+    // ---- the scores q.k / sqrt(d) of every key the output may read, ahead of the decision:
+    //      key 0 the new token, keys 1 .. nwin-1 the window (positions t-1, t-2, ...), key
+    //      nwin + j cache slot j; the evictee's (its window row before the write) is kept
+    //      aside (sc_e) and put in place once the decision says where it goes ----
+    const float scale = 1.0f / sqrtf((float)DK);
+    const int nwin = min(t + 1, eta);
+    {
+        float qs[PD];
+        slot_load<DK>(xq, sub, qs);
+        const int nk0 = nwin + nc;
+        for (int base = 0; base < nk0; base += kThreads / kSG) {
+            const int i = base + sl;
+            float acc = 0.f;
+            if (i < nk0) {
+                int vo;
+                float kv[PD];
+                if (i == 0) {
+                    slot_load<DK>(xk, sub, kv);
+                    vo = (int)M::NV;
+                } else {
+                    const T* kr;
+                    if (i < nwin) {
+                        int r = ring - i;
+                        r += r < 0 ? eta : 0;
+                        kr = rk_s + (size_t)r * DK;
+                        vo = (int)(M::RV + sizeof(T) * (size_t)r * DV);
+                    } else {
+                        const int j = i - nwin;
+                        kr = ck_s + (size_t)j * DK;
+                        vo = (int)(M::CV + sizeof(T) * (size_t)j * DV);
+                    }
+                    slot_load_io<DK, T>(kr, sub, kv);
+                }
+#pragma unroll
+                for (int q = 0; q < PD; ++q) acc = fmaf(qs[q], kv[q], acc);
+                if (sub == 0) voff[i] = vo;
+            }
+            acc += __shfl_xor_sync(kFull, acc, 1);
+            acc += __shfl_xor_sync(kFull, acc, 2);
+            acc += __shfl_xor_sync(kFull, acc, 4);
+            if (i < nk0 && sub == 0) sc[i] = acc * scale;
+        }
+    }
+    float sc_e = 0.f;   // the evictee's score (evictee warp)
+    if (warp == kEvWarp && ev) {
+        float qv[DK / kWarp], kv[DK / kWarp];
+        h_vec_load<DK / kWarp>(xq + lane * (DK / kWarp), qv);
+        h_cols<DK, T>(rk_s + (size_t)ring * DK, lane, kv);
+        float acc = 0.f;
+#pragma unroll
+        for (int q = 0; q < DK / kWarp; ++q) acc = fmaf(qv[q], kv[q], acc);
+        sc_e = warp_sum(acc) * scale;
+    }
     __syncthreads();
 
     // ---- 3. decision (every warp) and write ----
@@ -771,46 +824,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     __syncwarp();
 
-    // ---- 4. output: scores over window ∪ cache after the write; each key's value row ----
-    const float scale = 1.0f / sqrtf((float)DK);
-    const int nwin = min(t + 1, eta);
+    // ---- 4. output over window ∪ cache after the write: the evictee's score and value row
+    //      where the decision put it (the slot it replaced, or appended as slot nc) ----
     const int nkeys = nwin + nc_after;
-    {
-        float qs[PD];
-        slot_load<DK>(xq, sub, qs);
-        for (int base = 0; base < nkeys; base += kThreads / kSG) {
-            const int i = base + sl;
-            float acc = 0.f;
-            if (i < nkeys) {
-                int vo;
-                float kv[PD];
-                if (i == 0) {                             // the new token
-                    slot_load<DK>(xk, sub, kv);
-                    vo = (int)M::NV;
-                } else {
-                    const T* kr;
-                    if (i < nwin) {
-                        int r = ring - i;                               // positions t-1, t-2, ...
-                        r += r < 0 ? eta : 0;
-                        kr = rk_s + (size_t)r * DK;
-                        vo = (int)(M::RV + sizeof(T) * (size_t)r * DV);
-                    } else {
-                        const int j = i - nwin;                          // cache slot
-                        kr = (j == slot_new) ? rk_s + (size_t)ring * DK : ck_s + (size_t)j * DK;
-                        vo = (j == slot_new) ? (int)(M::RV + sizeof(T) * (size_t)ring * DV)
-                                             : (int)(M::CV + sizeof(T) * (size_t)j * DV);
-                    }
-                    slot_load_io<DK, T>(kr, sub, kv);
-                }
-#pragma unroll
-                for (int q = 0; q < PD; ++q) acc = fmaf(qs[q], kv[q], acc);
-                if (sub == 0) voff[i] = vo;
-            }
-            acc += __shfl_xor_sync(kFull, acc, 1);
-            acc += __shfl_xor_sync(kFull, acc, 2);
-            acc += __shfl_xor_sync(kFull, acc, 4);
-            if (i < nkeys && sub == 0) sc[i] = acc * scale;
-        }
+    if (warp == kEvWarp && lane == 0 && slot_new >= 0) {
+        sc[nwin + slot_new] = sc_e;
+        voff[nwin + slot_new] = (int)(M::RV + sizeof(T) * (size_t)ring * DV);
     }
     h_partial_store<D, DV>(red2, phq, hreg, warp, lane);
     __syncthreads();
