@@ -156,13 +156,13 @@ class Clocks:
 # on: the digest of those files must match, otherwise the traffic is reported as null.
 CSRC = os.path.join(ROOT, "sparse_exact_kv_gb300", "csrc")
 NCU_TRAFFIC = {
-    # w2 prefill (4 x 32 heads, n = 4096): one select launch
-    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "c1bc18db426f8ac7",
-               "bytes_per_launch": 409313536 + 131975680},
+    # w2 prefill (4 x 32 heads, n = 4096): mean of 3 select launches
+    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "0472a8cba8bf4a00",
+               "bytes_per_launch": 410079403 + 132202923},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
-    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "c4728e6b425b3f04",
-               "bytes_per_launch": 2 * (205599999 + 56527360)},
+    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "f549833f12b9d616",
+               "bytes_per_launch": 2 * (206886963 + 56314061)},
 }
 
 

@@ -158,7 +158,10 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
 /* One decode step for every head: token t = state.t with q, k, v (device io [B, Hh, d])
  * goes through the same rule as one prefill step; y (device io [B, Hh, d_v]) receives
  * its output; written_pos (nullable device int32 [B, Hh]) receives the position written
- * this step or -1.  W as in lola_prefill.  The state advances by one token. */
+ * this step or -1.  W as in lola_prefill.  The state advances by one token.
+ * For 1 <= eta <= 128, lambda <= 64 (and not float32 I/O at D = 128) the step is two kernels
+ * on `stream`: the token's feature map (into the state's tok_phi scratch; traced as
+ * LOLA_KERNEL_PHI), then the step itself as its programmatic dependent launch. */
 int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W,
                          int64_t w_head_stride, const void* q, const void* k, const void* v,
                          void* y, int32_t* written_pos, void* stream);
