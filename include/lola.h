@@ -222,6 +222,17 @@ int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches);
 /* Static name of a kernel id ("" if out of range). */
 const char* lola_kernel_name(int32_t id);
 
+/* ---- self-test of the bounded waits -----------------------------------------------------
+ * No counterpart in the LoLA paper.  Every wait of the library's kernels on an mbarrier (the
+ * decode step's burst, the output pass's MMA groups) gives up after a time limit, records a
+ * status bit and returns, so that the CUDA context stays usable.  This call runs that same
+ * wait on an mbarrier that nothing completes: one thread waits limit_ns nanoseconds
+ * (1 .. 10^9) and *host_elapsed_ns (host, nullable) receives how long it waited.  Synchronises
+ * `stream`; not for concurrent use.  Returns LOLA_ERR_DEVICE when the wait gave up as designed,
+ * LOLA_OK if it returned without giving up (a defect), LOLA_ERR_INVALID_ARG for a limit outside
+ * the range (before anything is enqueued), LOLA_ERR_CUDA on a CUDA failure. */
+int32_t lola_selftest_bounded_wait(int64_t limit_ns, int64_t* host_elapsed_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

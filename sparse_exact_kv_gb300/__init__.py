@@ -30,7 +30,7 @@ LOLA_BF16 = 1
 EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_check_config",
            "lola_state_layout_of", "lola_state_bytes", "lola_prefill_workspace_bytes", "lola_state_init",
            "lola_prefill", "lola_decode_step", "lola_read_status", "lola_kernel_timing", "lola_kernel_time",
-           "lola_kernel_name", "lola_prefill_noalloc")
+           "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait")
 # size of the fixed scratch array behind lola_prefill_noalloc (include/lola.h)
 LOLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNELS = ("state_init", "phi", "select", "output", "decode")
@@ -82,6 +82,7 @@ def _load():
                              ctypes.c_int32),
         "lola_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
         "lola_prefill_noalloc": ([C, ctypes.c_int32, P, P, P, P, ctypes.c_int64, P, P, P, P], ctypes.c_int32),
+        "lola_selftest_bounded_wait": ([ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), P], ctypes.c_int32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -104,6 +105,8 @@ def _ptr(t):
 
 
 def _stream(stream):
+    if isinstance(stream, int):          # a raw cudaStream_t (0: the legacy default stream)
+        return ctypes.c_void_p(stream)
     if stream is None:
         stream = torch.cuda.current_stream()
     return ctypes.c_void_p(stream.cuda_stream)
@@ -189,6 +192,14 @@ def lola_kernel_time(kernel) -> tuple[float, int]:
 
 def lola_kernel_name(kid: int) -> str:
     return _lib.lola_kernel_name(kid).decode()
+
+
+def lola_selftest_bounded_wait(limit_ns: int, stream=None):
+    """Runs the kernels' bounded mbarrier wait on a barrier nothing completes; returns
+    (status, nanoseconds waited): LOLA_ERR_DEVICE when the wait gave up as designed."""
+    ns = ctypes.c_int64(0)
+    st = _lib.lola_selftest_bounded_wait(int(limit_ns), ctypes.byref(ns), _stream(stream))
+    return st, ns.value
 
 
 # ---------------------------------------------------------------------------------------

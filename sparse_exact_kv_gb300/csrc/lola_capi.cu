@@ -6,6 +6,7 @@
 #include <vector>
 
 #include "lola_internal.cuh"
+#include "lola_tc.cuh"
 
 namespace lola {
 
@@ -132,6 +133,21 @@ void drain_pending(int id) {
         cudaEventDestroy(r.stop);
     }
     g_pending.swap(keep);
+}
+
+// lola_selftest_bounded_wait: one thread waits on an mbarrier that nothing completes, with
+// the wait the kernels use (tc::mbar_wait: bounded by %globaltimer); [0] = 1 if it returned
+// without giving up, [1] = the nanoseconds it waited
+__device__ int64_t g_selftest[2];
+__global__ void bounded_wait_kernel(int64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    const uint32_t b = (uint32_t)__cvta_generic_to_shared(&bar);
+    tc::mbar_init(b, 1);
+    const uint64_t t0 = tc::globaltimer_ns();
+    const bool done = tc::mbar_wait(b, 0, (uint64_t)limit_ns);
+    g_selftest[0] = done ? 1 : 0;
+    g_selftest[1] = (int64_t)(tc::globaltimer_ns() - t0);
 }
 
 }  // namespace
@@ -376,6 +392,19 @@ int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches) {
 const char* lola_kernel_name(int32_t id) {
     static const char* names[LOLA_KERNEL_COUNT] = {"state_init", "phi", "select", "output", "decode"};
     return (id >= 0 && id < LOLA_KERNEL_COUNT) ? names[id] : "";
+}
+
+int32_t lola_selftest_bounded_wait(int64_t limit_ns, int64_t* host_elapsed_ns, void* stream) {
+    if (limit_ns < 1 || limit_ns > 1000000000ll) return LOLA_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    bounded_wait_kernel<<<1, 32, 0, st>>>(limit_ns);
+    cudaError_t e = cudaGetLastError();
+    int64_t out[2] = {0, 0};
+    if (e == cudaSuccess) e = cudaMemcpyFromSymbolAsync(out, g_selftest, sizeof(out), 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e, "lola_selftest_bounded_wait");
+    if (host_elapsed_ns) *host_elapsed_ns = out[1];
+    return out[0] ? LOLA_OK : LOLA_ERR_DEVICE;
 }
 
 }  // extern "C"

@@ -121,3 +121,10 @@ def test_null_and_misaligned_pointers_rejected_before_any_launch(lib):
     st = so.lola_prefill(ctypes.byref(cfg), 16, P(256), P(256), P(256), P(256), 6, P(256), P(256), None, P(256),
                          1 << 30, None)
     assert st == lib.LOLA_ERR_INVALID_ARG
+
+
+def test_bounded_wait_selftest_rejects_bad_limits(lib):
+    """The limit is checked before anything is enqueued (safe without a GPU)."""
+    for bad in (0, -5, 10 ** 9 + 1):
+        st, _ = lib.lola_selftest_bounded_wait(bad, stream=0)
+        assert st == lib.LOLA_ERR_INVALID_ARG

@@ -197,6 +197,16 @@ def test_decode_from_empty_matches_oracle(L, dtype):
     assert st == 0, words
 
 
+def test_bounded_wait_gives_up_and_reports(L):
+    """The kernels' mbarrier wait, run on a barrier that nothing completes, gives up after its
+    limit and reports it; the context stays usable (a prefill runs right after)."""
+    st, ns = L.lola_selftest_bounded_wait(2_000_000)
+    assert st == L.LOLA_ERR_DEVICE
+    assert 2_000_000 <= ns < 1_000_000_000
+    x = synth.gauss_inputs(1, 2, 64, 64, 64, "f32", seed=23)
+    run_prefill(L, x, 8, 8, 16)
+
+
 def test_status_words_clear_after_prefill(L):
     x = synth.gauss_inputs(1, 4, 200, 128, 128, "bf16", seed=19)
     _, _, lay = run_prefill(L, x, 16, 16, 64)
