@@ -118,17 +118,18 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     using M = SelSmem<D, DV, T>;
     constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, HC = S::HC;
     constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
-    // Evictee roles: warps 0 .. kHelp-1 sum the H^T phi partials (one column per lane) and
-    // warp 0 also forms the previous write's gram with the evictee; warp kSWarp holds s
-    // and forms the next evictee's z'; warp kVvWarp its |v|^2; the last warp corrects N
-    // and z by the write and scores the evictee.  Named barrier 1 hands the partial sums
-    // and the gram to the last warp.
+    // Evictee roles: kHelp helper warps (warps 0, 1, 2, 6; helper i sums columns 32 i ..
+    // 32 i + 31 of the H^T phi partials) and warp 0 also forms the previous write's gram with
+    // the evictee; warp kSWarp holds s and forms the next evictee's z'; warp kVvWarp its
+    // |v|^2; the last warp corrects N and z by the write and scores the evictee.  Named
+    // barrier 1 hands the partial sums and the gram to the last warp.  Warp w issues from
+    // scheduler w % 4: the roles leave the last warp's scheduler to it alone.
     constexpr int kEvWarp = kSelWarps - 1;
     constexpr int kHelp = DV / kWarp;
-    constexpr int kSWarp = kSelWarps - 2;
-    constexpr int kVvWarp = kSelWarps - 3;
+    constexpr int kSWarp = 5;
+    constexpr int kVvWarp = 4;
     constexpr int kHandoff = (kHelp + 1) * kWarp;  // threads on named barrier 1
-    static_assert(kHelp < kVvWarp, "roles");
+    static_assert(kHelp <= 4 && kSelWarps == 16, "roles");
     constexpr bool kPackV = sizeof(T) == 2;        // bfloat16 slot values stay in registers
     constexpr int VW = SlotWords<DV, T>::kWords;
 
@@ -151,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int hidx = warp < 3 ? warp : (warp == 6 ? 3 : kHelp);   // helper index (kHelp: none)
     const int rank = CLUSTER ? (int)cluster_rank() : 0;
     const int CL = CLUSTER ? a.CL : 1;
     const int bh = CLUSTER ? (int)(blockIdx.x >> a.cl_shift) : (int)blockIdx.x;
@@ -295,12 +297,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         // ---- helper warps: the evictee's partials summed in row-group order (column j per
         //      lane; the per-element order of slot_reduce_partials); warp 0: the gram of the
         //      previous write with the evictee ----
-        if (warp < kHelp && ev) {
+        if (hidx < kHelp && ev) {
             if (warp == 0) {
                 const float g = prev_write ? warp_dot<D>(W.phi, ebuf[t & (kNEB - 1)], lane) : 0.f;
                 if (lane == 0) gbuf[t & 1] = g;
             }
-            const int j = warp * kWarp + lane;
+            const int j = hidx * kWarp + lane;
             npart[t & 1][j] = reduce_partials_col<D, DV>(&red[t & 1][0][0], j);
             named_arrive(kHandoff);
         }
