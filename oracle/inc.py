@@ -29,7 +29,7 @@ def _lib():
     if _LIB is None:
         lib = ctypes.CDLL(build())
         p = ctypes.c_void_p
-        lib.lola_oracle_run.argtypes = [ctypes.c_int] * 8 + [p] * 12 + [ctypes.c_int]
+        lib.lola_oracle_run.argtypes = [ctypes.c_int] * 8 + [p] * 12 + [ctypes.c_int, ctypes.c_int]
         lib.lola_oracle_run.restype = ctypes.c_int
         _LIB = lib
     return _LIB
@@ -39,8 +39,12 @@ def _ptr(a):
     return None if a is None else a.ctypes.data
 
 
-def run(q, k, v, W, eta: int, lam: int, dtype: str, replay=None, nthreads: int | None = None):
+def run(q, k, v, W, eta: int, lam: int, dtype: str, replay=None, nthreads: int | None = None,
+        read_mask: int = 0):
     """Run the incremental oracle over every head.
+
+    ``read_mask``: bit 0 hides the state, bit 1 the cache from every query's read (the
+    decisions and the memory are unchanged); nonzero needs eta >= 1.
 
     ``q, k, v``: (..., n, d) arrays in storage type (float32, or uint16 bf16 words when
     ``dtype == "bf16"``); the leading axes are flattened into independent heads.
@@ -77,7 +81,7 @@ def run(q, k, v, W, eta: int, lam: int, dtype: str, replay=None, nthreads: int |
     nth = nthreads or os.cpu_count() or 1
     rc = _lib().lola_oracle_run(BH, n, dk, dv, D, eta, lam, 1 if dtype == "bf16" else 0,
                                 _ptr(q), _ptr(k), _ptr(v), _ptr(W), _ptr(rep), _ptr(Y), _ptr(wpos),
-                                _ptr(wstep), _ptr(H), _ptr(s), _ptr(cache), _ptr(stats), nth)
+                                _ptr(wstep), _ptr(H), _ptr(s), _ptr(cache), _ptr(stats), nth, int(read_mask))
     if rc != 0:
         raise ValueError("oracle rejected the sizes")
     shp = lead

@@ -11,6 +11,10 @@
  *      SRE is taken against (H, s) before this step's write, the smallest (ties: the
  *      older position) is written H += phi(k)v^T, s += phi(k), and the rest stay;
  *   3. y_t is the co-normalised read over window, cache and (H, s) after the write.
+ *      The read mask (the notes' appendix I ablation, Table 12: the cache and the state
+ *      are updated as always, only what the query reads is restricted) drops the state's
+ *      terms (bit 0) and/or the cache's keys (bit 1) from the read; the window is always
+ *      read.
  *
  * Incremental form: instead of recomputing H^T phi(k_c) for every candidate c at every
  * step, each cached candidate keeps N_c = H^T phi(k_c) and z_c = s^T phi(k_c), set when
@@ -48,6 +52,7 @@ typedef struct {
     int32_t* cache_out;          /* nullable [BH, lam] sorted, -1 padded */
     double* stats;               /* [BH, 4]: min_gap, max_gap, mismatches, status */
     int next;                    /* work counter */
+    int read_mask;               /* bit 0: the state is not read; bit 1: the cache is not read */
 } job_t;
 
 static double widen(const void* base, int dtype, size_t idx) {
@@ -207,14 +212,16 @@ static void run_chain(job_t* J, int bh) {
             status = 2.0;    /* replay writes when no write is due */
             break;
         }
-        /* 3. co-normalised output over window ∪ cache ∪ (H, s) */
+        /* 3. co-normalised output over window ∪ cache ∪ (H, s), less what the read mask hides */
+        const int ncache_read = (J->read_mask & 2) ? 0 : count;
+        const int read_state = !(J->read_mask & 1);
         for (int c = 0; c < dk; ++c) x[c] = widen(J->Q, J->in_dtype, base_k + (size_t)t * dk + c);
         feature(x, W, dk, D, phiq, z);
         int w0 = t - eta + 1 < 0 ? 0 : t - eta + 1;
         int nex = 0;
         double m = -INFINITY;
         for (int pass = 0; pass < 2; ++pass) {
-            int cnt = pass == 0 ? (t - w0 + 1) : count;
+            int cnt = pass == 0 ? (t - w0 + 1) : ncache_read;
             for (int i = 0; i < cnt; ++i) {
                 int p = pass == 0 ? w0 + i : cpos[i];
                 double a = 0.0;
@@ -231,11 +238,11 @@ static void run_chain(job_t* J, int bh) {
             for (int j = 0; j < dv; ++j) hq[j] += phiq[r] * Hr[j];
             dl += phiq[r] * s[r];
         }
-        double em = nex > 0 ? exp(-m) : 1.0, den = em * dl;
-        for (int j = 0; j < dv; ++j) num[j] = em * hq[j];
+        double em = nex > 0 ? exp(-m) : 1.0, den = read_state ? em * dl : 0.0;
+        for (int j = 0; j < dv; ++j) num[j] = read_state ? em * hq[j] : 0.0;
         nex = 0;
         for (int pass = 0; pass < 2; ++pass) {
-            int cnt = pass == 0 ? (t - w0 + 1) : count;
+            int cnt = pass == 0 ? (t - w0 + 1) : ncache_read;
             for (int i = 0; i < cnt; ++i) {
                 int p = pass == 0 ? w0 + i : cpos[i];
                 double wgt = exp(ascore[nex++] - m);
@@ -271,14 +278,18 @@ static void* worker(void* arg) {
     return 0;
 }
 
-/* Runs BH independent heads.  Returns 0, or -1 on invalid sizes. */
+/* Runs BH independent heads.  Returns 0, or -1 on invalid sizes or a read mask that
+ * leaves nothing to read (any nonzero mask needs eta >= 1: the window then always holds
+ * the current token). */
 int lola_oracle_run(int BH, int n, int dk, int dv, int D, int eta, int lam, int in_dtype,
                     const void* Q, const void* K, const void* V, const float* W,
                     const int32_t* replay, double* Y, int32_t* write_pos, int32_t* write_step,
-                    double* H_out, double* s_out, int32_t* cache_out, double* stats, int nthreads) {
+                    double* H_out, double* s_out, int32_t* cache_out, double* stats, int nthreads,
+                    int read_mask) {
     if (BH < 0 || n < 0 || dk <= 0 || dv <= 0 || D <= 0 || (D & 1) || eta < 0 || lam < 0) return -1;
+    if (read_mask < 0 || read_mask > 3 || (read_mask != 0 && eta < 1)) return -1;
     job_t J = {BH, n, dk, dv, D, eta, lam, in_dtype, Q, K, V, W, replay, Y, write_pos, write_step,
-               H_out, s_out, cache_out, stats, 0};
+               H_out, s_out, cache_out, stats, 0, read_mask};
     if (nthreads < 1) nthreads = 1;
     if (nthreads > 256) nthreads = 256;
     if (nthreads > BH) nthreads = BH > 0 ? BH : 1;

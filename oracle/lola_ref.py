@@ -33,7 +33,11 @@ Readings taken where the notes are silent (each is listed in the design notes):
 * the output is read after this step's write, with H_t, G_t and W_t (so every token
   <= t is in exactly one of window, cache, state);
 * only the softmax branch carries the 1/sqrt(d_k) temperature; the linear branch is the
-  plain ``phi(q)^T phi(k)``.  The max-subtraction in the output is for range only.
+  plain ``phi(q)^T phi(k)``.  The max-subtraction in the output is for range only;
+* read mask (appendix I, Table 12: a read-time ablation; the cache and the state are
+  updated exactly as without it): bit 0 leaves the state's terms ``H^T phi(q)`` and
+  ``phi(q)^T s`` out of the read, bit 1 the cache's keys; the window is always read, and
+  a nonzero mask needs eta >= 1 (then the window holds the current token).
 
 Three formulations live here and in ``lola_inc.c``: ``lola_run`` (running H, s; all
 SREs recomputed from H each step), ``lola_set`` (no running state: H is re-summed from
@@ -69,6 +73,11 @@ def sre_sq(H: np.ndarray, s: np.ndarray, phik: np.ndarray, v: np.ndarray) -> flo
     return float(r @ r)
 
 
+def _check_mask(eta: int, read_mask: int) -> None:
+    if read_mask not in (0, 1, 2, 3) or (read_mask and eta < 1):
+        raise ValueError(f"read mask {read_mask} with eta = {eta}: nothing would be left to read")
+
+
 def _output(qt, phiq, exact, K, V, H_num, den_lin, scale):
     """Co-normalised read (section 2.5, Eq. 14).  ``H_num = H^T phi(q)``, ``den_lin = phi(q)^T s``."""
     if len(exact):
@@ -84,19 +93,20 @@ def _output(qt, phiq, exact, K, V, H_num, den_lin, scale):
     return num / den
 
 
-def lola_run(q, k, v, W, eta: int, lam: int, replay=None):
+def lola_run(q, k, v, W, eta: int, lam: int, replay=None, read_mask: int = 0):
     """Per-token LoLA on one head with a running (H, s); float64.
 
     ``q, k``: (n, d_k); ``v``: (n, d_v); ``W``: (D/2, d_k).  ``replay``: optional (n,)
     int array of the position written at each step (-1: none); when given, the oracle
     follows those decisions instead of its own and reports how far each was from its
-    own best (relative SRE gap).
+    own best (relative SRE gap).  ``read_mask``: see the module notes (read time only).
 
     Returns a dict with Y (n, d_v), write_pos (n,), write_step (n,), H, s, cache
     (sorted positions), window (positions), min_gap (smallest relative SRE gap between
     the best and the second-best candidate over all decisions of a free run), max_gap
     and mismatches (replay only).
     """
+    _check_mask(eta, read_mask)
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -145,21 +155,25 @@ def lola_run(q, k, v, W, eta: int, lam: int, replay=None):
             write_pos[t] = w
             write_step[w] = t
             cache = [j for j in E if j != w]
-        exact = list(window) + cache
-        Y[t] = _output(q[t], PQ[t], exact, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
+        exact = list(window) + ([] if read_mask & 2 else cache)
+        if read_mask & 1:
+            Y[t] = _output(q[t], PQ[t], exact, k, v, np.zeros(dv), 0.0, scale)
+        else:
+            Y[t] = _output(q[t], PQ[t], exact, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
     return dict(Y=Y, write_pos=write_pos, write_step=write_step, H=H, s=s,
                 cache=np.array(sorted(cache), np.int64), window=np.array(list(window), np.int64),
                 min_gap=min_gap, max_gap=max_gap, mismatches=mismatches)
 
 
-def lola_set(q, k, v, W, eta: int, lam: int):
+def lola_set(q, k, v, W, eta: int, lam: int, read_mask: int = 0):
     """Brute-force LoLA with no running state (small n only).
 
     Every quantity is summed from explicit sets each step: the memory read-out for a
     key c is ``sum_{j in S} (phi_c . phi_j) v_j / sum_{j in S} phi_c . phi_j`` over the
     written set S, and the output's linear terms are ``sum_{j in S} (phi_q . phi_j) v_j``
     and ``sum_{j in S} phi_q . phi_j``.  Same decisions and outputs as ``lola_run`` in
-    exact arithmetic."""
+    exact arithmetic (with the same read mask)."""
+    _check_mask(eta, read_mask)
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -191,9 +205,10 @@ def lola_set(q, k, v, W, eta: int, lam: int):
             write_pos[t] = w
             write_step[w] = t
             cache = [j for j in E if j != w]
-        gl = np.array([PQ[t] @ PK[j] for j in written]) if written else np.zeros(0)
-        num_lin = gl @ v[written] if written else np.zeros(v.shape[1])
-        Y[t] = _output(q[t], PQ[t], win + cache, k, v, num_lin, float(gl.sum()), scale)
+        read = [] if read_mask & 1 else written
+        gl = np.array([PQ[t] @ PK[j] for j in read]) if read else np.zeros(0)
+        num_lin = gl @ v[read] if read else np.zeros(v.shape[1])
+        Y[t] = _output(q[t], PQ[t], win + ([] if read_mask & 2 else cache), k, v, num_lin, float(gl.sum()), scale)
     return dict(Y=Y, write_pos=write_pos, write_step=write_step,
                 cache=np.array(sorted(cache), np.int64), written=np.array(written, np.int64))
 
@@ -210,6 +225,21 @@ def causal_softmax_attention(q, k, v):
     n = q.shape[0]
     a = (q @ k.T) / math.sqrt(q.shape[1])
     a = np.where(np.tril(np.ones((n, n), bool)), a, -np.inf)
+    p = np.exp(a - a.max(axis=1, keepdims=True))
+    return (p / p.sum(axis=1, keepdims=True)) @ v
+
+
+def sliding_window_attention(q, k, v, eta: int):
+    """Causal softmax attention restricted to the last eta tokens (inclusive):
+    ``softmax(q k^T / sqrt(d_k))`` over t - eta < j <= t."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n = q.shape[0]
+    t = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    a = (q @ k.T) / math.sqrt(q.shape[1])
+    a = np.where((j <= t) & (j > t - eta), a, -np.inf)
     p = np.exp(a - a.max(axis=1, keepdims=True))
     return (p / p.sum(axis=1, keepdims=True)) @ v
 

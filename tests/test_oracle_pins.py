@@ -24,12 +24,13 @@ def _load(name):
             for k, v in g.items()}
 
 
-def _all_forms(q, k, v, W, eta, lam):
+def _all_forms(q, k, v, W, eta, lam, read_mask=0):
     """The three oracle formulations on one head (float32 inputs for the C form)."""
-    a = R.lola_run(q, k, v, W, eta, lam)
-    b = R.lola_set(q, k, v, W, eta, lam)
+    a = R.lola_run(q, k, v, W, eta, lam, read_mask=read_mask)
+    b = R.lola_set(q, k, v, W, eta, lam, read_mask=read_mask)
     c = inc.run(np.asarray(q, np.float32)[None], np.asarray(k, np.float32)[None],
-                np.asarray(v, np.float32)[None], np.asarray(W, np.float32), eta, lam, "f32")
+                np.asarray(v, np.float32)[None], np.asarray(W, np.float32), eta, lam, "f32",
+                read_mask=read_mask)
     c1 = {key: (val[0] if isinstance(val, np.ndarray) and val.ndim >= 1 else val) for key, val in c.items()}
     return a, b, c1
 
@@ -277,3 +278,85 @@ def test_state_element_formula():
     """Appendix B: min{t(d_k+d_v), (eta+lambda)(d_k+d_v) + D d_v + D}."""
     assert R.state_elements(10, 64, 64, 64, 64, 64) == 10 * 128
     assert R.state_elements(4096, 128, 128, 128, 64, 64) == 128 * 256 + 128 * 128 + 128
+
+
+# ---------------------------------------------------------------------------
+# read mask (appendix I, Table 12: what a query reads is restricted; the cache and the
+# state are updated as always)
+# ---------------------------------------------------------------------------
+
+HIDE_STATE, HIDE_CACHE = 1, 2
+
+
+@pytest.mark.parametrize("eta,lam", [(1, 3), (4, 4), (9, 2), (6, 40)])
+def test_window_only_read_is_sliding_window_attention(eta, lam):
+    """Both memories hidden: y_t is softmax attention over the last eta tokens, whatever the
+    cache and the state hold (Table 12's window-only row)."""
+    x = synth.gauss_inputs(1, 1, 48, 8, 8, "f32", seed=40 + eta, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    ref = R.sliding_window_attention(q, k, v, eta)
+    a, b, c = _all_forms(q, k, v, x.W, eta, lam, read_mask=HIDE_STATE | HIDE_CACHE)
+    for o in (a, b, c):
+        np.testing.assert_allclose(o["Y"], ref, rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask", [HIDE_STATE, HIDE_CACHE, HIDE_STATE | HIDE_CACHE])
+def test_read_mask_keeps_decisions_and_memory(mask):
+    """The mask changes the read only: the decision log, H, s and the cache are those of
+    the unmasked run, and at least one output row differs."""
+    x = synth.gauss_inputs(1, 1, 60, 8, 8, "f32", seed=44, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    base = R.lola_run(q, k, v, x.W, 5, 4)
+    o = R.lola_run(q, k, v, x.W, 5, 4, read_mask=mask)
+    assert np.array_equal(o["write_pos"], base["write_pos"])
+    assert np.array_equal(o["cache"], base["cache"])
+    np.testing.assert_array_equal(o["H"], base["H"])
+    np.testing.assert_array_equal(o["s"], base["s"])
+    assert np.abs(o["Y"] - base["Y"]).max() > 1e-6
+
+
+def test_hide_state_with_empty_cache_is_sliding_window():
+    """lambda = 0: the cache is empty, so hiding the state leaves the window alone."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=46, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 7, 0, read_mask=HIDE_STATE)
+    np.testing.assert_allclose(o["Y"], R.sliding_window_attention(q, k, v, 7), rtol=1e-11, atol=1e-12)
+
+
+def test_hide_cache_with_empty_cache_changes_nothing():
+    """lambda = 0: there is no cache to hide; the read is the window plus the state."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=47, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 5, 0, read_mask=HIDE_CACHE)
+    np.testing.assert_allclose(o["Y"], R.window_plus_linear(q, k, v, x.W, 5), rtol=1e-11, atol=1e-12)
+
+
+def test_hide_cache_without_writes_is_sliding_window():
+    """eta + lambda >= n: nothing is ever written, so hiding the cache leaves the window."""
+    x = synth.gauss_inputs(1, 1, 30, 8, 8, "f32", seed=48, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 6, 30, read_mask=HIDE_CACHE)
+    assert (o["write_pos"] == -1).all()
+    np.testing.assert_allclose(o["Y"], R.sliding_window_attention(q, k, v, 6), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("mask", [HIDE_STATE, HIDE_CACHE])
+@pytest.mark.parametrize("eta,lam", [(1, 5), (3, 2), (4, 4)])
+def test_three_forms_agree_with_read_mask(mask, eta, lam):
+    x = synth.gauss_inputs(1, 1, 32, 8, 8, "f32", seed=49 + lam, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    a, b, c = _all_forms(q, k, v, x.W, eta, lam, read_mask=mask)
+    assert np.array_equal(a["write_pos"], b["write_pos"]) and np.array_equal(a["write_pos"], c["write_pos"])
+    np.testing.assert_allclose(b["Y"], a["Y"], rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(c["Y"], a["Y"], rtol=1e-11, atol=1e-12)
+
+
+def test_read_mask_that_leaves_nothing_is_rejected():
+    """With eta = 0 the window is empty: a nonzero mask could leave no term to read."""
+    x = synth.gauss_inputs(1, 1, 8, 8, 8, "f32", seed=50, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    with pytest.raises(ValueError):
+        R.lola_run(q, k, v, x.W, 0, 3, read_mask=HIDE_CACHE)
+    with pytest.raises(ValueError):
+        inc.run(np.asarray(q, np.float32)[None], np.asarray(k, np.float32)[None], np.asarray(v, np.float32)[None],
+                x.W, 0, 3, "f32", read_mask=HIDE_STATE)
