@@ -69,7 +69,14 @@ typedef struct {
     int32_t lambda;     /* sparse-cache capacity (>= 0) */
     int32_t chunk;      /* prefill schedule granularity C; no effect on results */
     int32_t dtype;      /* lola_dtype */
+    int32_t read_mask;  /* 0, or lola_read_flags: memories left out of every query's read */
 } lola_config;
+
+/* Read mask (appendix I, Table 12: a read-time ablation).  The cache and the state are
+ * updated exactly as with read_mask = 0 (same decisions, same memory); only the output
+ * leaves out H^T phi(q), phi(q)^T s (HIDE_STATE) and/or the cached keys (HIDE_CACHE).  The
+ * window is always read; a nonzero mask needs eta >= 1 (LOLA_ERR_INVALID_ARG otherwise). */
+typedef enum { LOLA_READ_HIDE_STATE = 1, LOLA_READ_HIDE_CACHE = 2 } lola_read_flags;
 
 /* Supported by this build: d_k = d_v = D in {64, 128}; lambda <= 1024; eta <= 8192;
  * chunk a power of two in [16, 256]; B * Hh >= 1. */

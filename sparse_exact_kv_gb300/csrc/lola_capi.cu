@@ -28,6 +28,7 @@ int32_t to_dims(const lola_config* c, Dims* d) {
     if (c->B < 1 || c->Hh < 1 || c->d_k < 1 || c->d_v < 1 || c->D < 2 || (c->D & 1) || c->eta < 0 ||
         c->lambda < 0 || c->chunk < 1 || (c->dtype != LOLA_F32 && c->dtype != LOLA_BF16))
         return LOLA_ERR_INVALID_ARG;
+    if (c->read_mask < 0 || c->read_mask > 3 || (c->read_mask != 0 && c->eta < 1)) return LOLA_ERR_INVALID_ARG;
     if ((int64_t)c->B * c->Hh > (1 << 24)) return LOLA_ERR_UNSUPPORTED;
     const bool dims_ok = (c->d_k == 128 && c->d_v == 128 && c->D == 128) || (c->d_k == 64 && c->d_v == 64 && c->D == 64);
     if (!dims_ok) return LOLA_ERR_UNSUPPORTED;
@@ -43,6 +44,7 @@ int32_t to_dims(const lola_config* c, Dims* d) {
     d->lam = c->lambda;
     d->chunk = c->chunk;
     d->dtype = c->dtype;
+    d->read_mask = c->read_mask;
     return LOLA_OK;
 }
 

@@ -43,6 +43,7 @@ struct DecArgs {
     int32_t* written_pos;
     int BH;
     int prefetch_ahead;   // heads ahead of this one whose state is prefetched into L2 (0: none)
+    int read_mask;        // lola_read_flags: memories left out of the read (the update is unchanged)
 };
 
 // Ask L2 to fetch [p, p + bytes) with bulk prefetches of at most 16 KB each, issued by
@@ -335,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     // ---- 7. output: softmax over window ∪ cache, linear read of (H, s) after the write ----
     const float scale = 1.0f / sqrtf((float)DK);
     const int nwin = min(t + 1, eta);
-    const int nkeys = nwin + nc_after;
+    const int nkeys = (a.read_mask & LOLA_READ_HIDE_CACHE) ? nwin : nwin + nc_after;   // window first
     for (int base = 0; base < nkeys; base += kSlotsPerPass) {
         const int i = base + sl;
         float acc = 0.f;
@@ -399,8 +400,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
             float num = 0.f;
 #pragma unroll
             for (int r = 0; r < KS; ++r) num += red[r * DV + tid];
-            num = fmaf(misc[1], lin[tid], num);
-            const float den = nkeys > 0 ? fmaf(misc[1], misc[4], misc[3]) : misc[4];
+            const float el = (a.read_mask & LOLA_READ_HIDE_STATE) ? 0.f : misc[1];   // the state's weight
+            num = fmaf(el, lin[tid], num);
+            const float den = nkeys > 0 ? fmaf(el, misc[4], misc[3]) : misc[4];
             IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
         }
     }
@@ -826,7 +828,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
 
     // ---- 4. output over window ∪ cache after the write: the evictee's score and value row
     //      where the decision put it (the slot it replaced, or appended as slot nc) ----
-    const int nkeys = nwin + nc_after;
+    // (the read mask's HIDE_CACHE reads the window keys only: they come first)
+    const int nkeys = (a.read_mask & LOLA_READ_HIDE_CACHE) ? nwin : nwin + nc_after;
     if (warp == kEvWarp && lane == 0 && slot_new >= 0) {
         sc[nwin + slot_new] = sc_e;
         voff[nwin + slot_new] = (int)(M::RV + sizeof(T) * (size_t)ring * DV);
@@ -894,11 +897,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
 #pragma unroll
         for (int r = 0; r < NS; ++r) num += red[r * DV + tid];
         const float emx = expf(-mx);   // nkeys >= 1: the new token is always a key
-        num = fmaf(emx, lin[tid], num);
+        const float el = (a.read_mask & LOLA_READ_HIDE_STATE) ? 0.f : emx;   // the state's weight
+        num = fmaf(el, lin[tid], num);
         float l = 0.f;
 #pragma unroll
         for (int w = 0; w < kDecWarps; ++w) l += lpart[w];
-        const float den = fmaf(emx, misc[4], l);
+        const float den = fmaf(el, misc[4], l);
         IO<T>::st(static_cast<T*>(a.y), (int64_t)bh * DV + tid, num / den);
     }
 
@@ -1066,6 +1070,7 @@ DecArgs make_args(const Dims& d, char* state, const Layout& L, const float* W, i
     a.y = y;
     a.written_pos = written_pos;
     a.BH = d.BH;
+    a.read_mask = d.read_mask;
     a.prefetch_ahead = 0;
     {
         int dev = 0, sms = 0;

@@ -15,7 +15,7 @@ constexpr int kWarp = 32;
 // Sizes and the public per-head state layout (see lola.h)
 // ---------------------------------------------------------------------------------
 struct Dims {
-    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype;
+    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype, read_mask;
     int io_bytes() const { return dtype == LOLA_BF16 ? 2 : 4; }
 };
 

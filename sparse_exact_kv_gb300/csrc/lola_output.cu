@@ -28,7 +28,7 @@ constexpr int kSubRows = kOutWarps * kRowsPerWarp;   // 64 query rows per pass
 constexpr int kKeyTile = 32;
 
 struct OutArgs {
-    int n, eta, lam, chunk, nck;
+    int n, eta, lam, chunk, nck, read_mask;
     const void* Q;
     const void* K;
     const void* V;
@@ -146,7 +146,9 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const OutArgs a)
                 const int r = warp * kRowsPerWarp + i;
                 const int t = t0 + r;
                 const bool row_ok = t < c1;
-                const bool vs = row_ok && p >= 0 && p <= t && (w < 0 || w > t);
+                // (the read mask's HIDE_CACHE keeps only the window: t - eta < p)
+                const bool vs = row_ok && p >= 0 && p <= t && (w < 0 || w > t) &&
+                                (!(a.read_mask & LOLA_READ_HIDE_CACHE) || p > t - a.eta);
                 const bool vl = row_ok && p >= 0 && w >= c0 && w <= t;
                 float sc = -INFINITY;
                 if (vs) {
@@ -205,11 +207,14 @@ __global__ void __launch_bounds__(kOutThreads, 1) output_kernel(const OutArgs a)
             if (t >= c1) continue;
             const bool any = mrow[i] != -INFINITY;
             const float em = any ? expf(-mrow[i]) : 1.f;
-            const float den = any ? fmaf(em, llr[i], lsr[i]) : llr[i];
+            // HIDE_STATE: the linear terms stay out of the read (then the window's current
+            // token makes any true)
+            const float el = (a.read_mask & LOLA_READ_HIDE_STATE) ? 0.f : em;
+            const float den = any ? fmaf(el, llr[i], lsr[i]) : llr[i];
             const float inv = 1.0f / den;
 #pragma unroll
             for (int q = 0; q < NI; ++q) {
-                const float num = any ? fmaf(em, accl[i][q], accs[i][q]) : accl[i][q];
+                const float num = any ? fmaf(el, accl[i][q], accs[i][q]) : accl[i][q];
                 IO<T>::st(Y, (row0 + t) * DV + lane + 32 * q, num * inv);
             }
         }
@@ -240,6 +245,7 @@ cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void*
     a.lam = d.lam;
     a.chunk = ws.snap_interval;
     a.nck = ws.nck;
+    a.read_mask = d.read_mask;
     a.Q = Q;
     a.K = K;
     a.V = V;

@@ -57,7 +57,7 @@ constexpr int SEND = 196608;
 constexpr uint32_t TS = 0, TL = 64, TOS = 128, TOL = 256;
 
 struct TcArgs {
-    int n, eta, lam, chunk, nck;
+    int n, eta, lam, chunk, nck, read_mask;
     const __nv_bfloat16* Q;
     const __nv_bfloat16* K;
     const __nv_bfloat16* V;
@@ -117,7 +117,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
             const int w = p >= 0 ? wst[p] : -1;
             // row r = t - t0 sees key p exactly iff lo <= r < hi, linearly iff r >= llo
             const int lo = p < 0 ? 255 : min(max(p - t0, 0), 255);
-            const int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
+            int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
+            // the read mask's HIDE_CACHE: only while the key is in the window (t < p + eta)
+            if (p >= 0 && (a.read_mask & LOLA_READ_HIDE_CACHE)) hi = min(hi, min(max(p + a.eta - t0, 0), 255));
             const int llo = (p < 0 || w < c0) ? 255 : min(max(w - t0, 0), 255);
             kpos[st][ptid] = p;
             kinfo[st][ptid] = (uint32_t)lo | ((uint32_t)hi << 8) | ((uint32_t)llo << 16);
@@ -327,7 +329,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
     if (!bad) {
         const float ls = lsum[0][0][row] + lsum[0][1][row], ll = lsum[1][0][row] + lsum[1][1][row];
         const bool any = m_run != -INFINITY;
-        const float em = any ? ex2(-m_run) : 1.f;
+        // HIDE_STATE: the linear terms stay out of the read (then the window's current token
+        // makes any true)
+        const float em = any ? ((a.read_mask & LOLA_READ_HIDE_STATE) ? 0.f : ex2(-m_run)) : 1.f;
         const float den = any ? fmaf(em, ll, ls) : ll;
         const float inv = t < n ? 1.0f / den : 0.f;
         __nv_bfloat16* y = a.Y + (row0 + (t < n ? t : 0)) * kD + 64 * hf;
@@ -374,6 +378,7 @@ cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const vo
     a.lam = d.lam;
     a.chunk = ws.snap_interval;
     a.nck = ws.nck;
+    a.read_mask = d.read_mask;
     a.Q = static_cast<const __nv_bfloat16*>(Q);
     a.K = static_cast<const __nv_bfloat16*>(K);
     a.V = static_cast<const __nv_bfloat16*>(V);

@@ -28,13 +28,13 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_prefill(L, x, eta, lam, chunk, n=None, dev="cuda"):
+def run_prefill(L, x, eta, lam, chunk, n=None, dev="cuda", read_mask=0):
     """Prefill through the C ABI; returns (Y float64, write_pos, layer)."""
     w = x.w
     dt = w.dtype
     n = n or x.q.shape[2]
     lay = L.Lola(w.B, w.Hh, w.d, w.D, eta, lam, chunk=chunk,
-                 dtype=torch.bfloat16 if dt == "bf16" else torch.float32, device=dev)
+                 dtype=torch.bfloat16 if dt == "bf16" else torch.float32, device=dev, read_mask=read_mask)
     Q, K, V = (to_dev(getattr(x, a)[:, :, :n], dev, dt) for a in "qkv")
     W = torch.from_numpy(x.W).to(dev)
     wpos = torch.full((w.B, w.Hh, n), -7, dtype=torch.int32, device=dev)
@@ -55,18 +55,18 @@ def check_outputs(got, ref, dtype, what="Y"):
     return ma, rl
 
 
-def check_decisions(x, wpos, eta, lam, n=None, nthreads=None):
+def check_decisions(x, wpos, eta, lam, n=None, nthreads=None, read_mask=0):
     """Validates the GPU decision log against the oracle; returns the oracle run along the
-    GPU's trajectory (replay) and the free-running oracle."""
+    GPU's trajectory (replay) and the free-running oracle (outputs read with read_mask)."""
     dt = x.w.dtype
     n = n or wpos.shape[-1]
     q, k, v = (getattr(x, a)[..., :n, :] for a in "qkv")
-    free = inc.run(q, k, v, x.W, eta, lam, dt, nthreads=nthreads)
+    free = inc.run(q, k, v, x.W, eta, lam, dt, nthreads=nthreads, read_mask=read_mask)
     if dt == "f32":
         diff = np.argwhere(free["write_pos"] != wpos)
         assert diff.size == 0, f"float32 decision log differs at (head..., step) {diff[:5].tolist()}"
         return free, free
-    rep = inc.run(q, k, v, x.W, eta, lam, dt, replay=wpos, nthreads=nthreads)
+    rep = inc.run(q, k, v, x.W, eta, lam, dt, replay=wpos, nthreads=nthreads, read_mask=read_mask)
     assert (rep["status"] == 0).all(), f"replay rejected the GPU log: status {np.unique(rep['status'])}"
     worst = float(np.max(rep["max_gap"]))
     assert worst < GAP, f"a GPU decision is {worst:.3e} (relative SRE) away from the best candidate"

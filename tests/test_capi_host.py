@@ -128,3 +128,19 @@ def test_bounded_wait_selftest_rejects_bad_limits(lib):
     for bad in (0, -5, 10 ** 9 + 1):
         st, _ = lib.lola_selftest_bounded_wait(bad, stream=0)
         assert st == lib.LOLA_ERR_INVALID_ARG
+
+
+def test_read_mask_validation(lib):
+    """The read mask is 0..3 and, when nonzero, needs a window (eta >= 1)."""
+    ok = lib.make_config(2, 4, 128, 128, 128, 64, 64, 64, "bf16", read_mask=lib.LOLA_READ_HIDE_STATE)
+    assert lib.lola_check_config(ok) == 0
+    both = lib.make_config(2, 4, 128, 128, 128, 1, 0, 64, "f32", read_mask=3)
+    assert lib.lola_check_config(both) == 0
+    assert lib.lola_check_config(lib.make_config(2, 4, 128, 128, 128, 64, 64, 64, "bf16", read_mask=4)) == \
+        lib.LOLA_ERR_INVALID_ARG
+    assert lib.lola_check_config(lib.make_config(2, 4, 128, 128, 128, 0, 64, 64, "bf16", read_mask=2)) == \
+        lib.LOLA_ERR_INVALID_ARG
+    # the mask changes neither the state layout nor the workspace
+    base = lib.make_config(2, 4, 128, 128, 128, 64, 64, 64, "bf16")
+    assert lib.lola_state_bytes(ok) == lib.lola_state_bytes(base)
+    assert lib.lola_prefill_workspace_bytes(ok, 512) == lib.lola_prefill_workspace_bytes(base, 512)

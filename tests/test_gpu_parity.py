@@ -197,6 +197,34 @@ def test_decode_from_empty_matches_oracle(L, dtype):
     assert st == 0, words
 
 
+@pytest.mark.parametrize("dtype,d", [("f32", 64), ("bf16", 128), ("f32", 128)])
+@pytest.mark.parametrize("mask", [1, 2, 3])
+def test_read_mask_prefill_and_decode_match_oracle(L, dtype, d, mask):
+    """The read mask (appendix I, Table 12) changes what queries read, never the memory:
+    decisions equal the unmasked run's; outputs of the prefill and of the decode steps
+    after it follow the oracle read with the same mask."""
+    B, Hh, n, m, eta, lam = 1, 3, 150, 30, 12, 20
+    x = synth.gauss_inputs(B, Hh, n + m, d, d, dtype, seed=60 + mask)
+    Y0, w0, _ = run_prefill(L, x, eta, lam, 32, n=n)
+    Y, wpos, lay = run_prefill(L, x, eta, lam, 32, n=n, read_mask=mask)
+    assert np.array_equal(wpos, w0), "the read mask changed a decision"
+    assert np.abs(Y - Y0).max() > 1e-4, "the read mask changed nothing"
+    dev = "cuda"
+    Q, K, V = (to_dev(getattr(x, a), dev, dtype) for a in "qkv")
+    W = torch.from_numpy(x.W).to(dev)
+    ys, ws = [], []
+    for t in range(n, n + m):
+        wpt = torch.empty(B, Hh, dtype=torch.int32, device=dev)
+        ys.append(lay.decode_step(Q[:, :, t].contiguous(), K[:, :, t].contiguous(), V[:, :, t].contiguous(), W,
+                                  written_pos=wpt))
+        ws.append(wpt)
+    torch.cuda.synchronize()
+    wall = np.concatenate([wpos, torch.stack(ws, -1).cpu().numpy()], axis=-1)
+    yall = np.concatenate([Y, to_f64(torch.stack(ys, 2))], axis=2)
+    ref, _ = check_decisions(x, wall, eta, lam, read_mask=mask)
+    check_outputs(yall, ref["Y"], dtype)
+
+
 def test_bounded_wait_gives_up_and_reports(L):
     """The kernels' mbarrier wait, run on a barrier that nothing completes, gives up after its
     limit and reports it; the context stays usable (a prefill runs right after)."""
