@@ -44,6 +44,8 @@ def parse_args():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--decode-only", action="store_true", help="skip the prefill measurement")
     p.add_argument("--decode-batch", type=int, default=None, help="batch of the decode workload (profiling)")
+    p.add_argument("--read-mask", type=int, default=0, choices=[0, 1, 2, 3],
+                   help="read mask of the layer (1: state hidden, 2: cache hidden, 3: both)")
     return p.parse_args()
 
 
@@ -274,7 +276,8 @@ def run_prefill(L, R, args, pk):
     dev = torch.device("cuda", R.local)
     Q, K, V = (dev_tensor(getattr(x, a), w.dtype, dev) for a in "qkv")
     W = torch.from_numpy(x.W).to(dev)
-    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev)
+    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev,
+                 read_mask=args.read_mask)
     ws = lay.workspace_for(w.n)
     Y = torch.empty_like(V)
     wpos = torch.empty(w.B, w.Hh, w.n, dtype=torch.int32, device=dev)
@@ -382,7 +385,8 @@ def run_decode(L, R, args, pk):
     dev = torch.device("cuda", R.local)
     # the timed steps, then as many again with per-kernel tracing (each step advances the state)
     steps = min(args.decode_steps, (w.decode_steps - args.warmup) // 2)
-    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev)
+    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev,
+                 read_mask=args.read_mask)
     W = torch.from_numpy(x.W).to(dev)
     P = [dev_tensor(getattr(x, a)[:, :, :w.n], w.dtype, dev) for a in "qkv"]
     lay.prefill(*P, W)
@@ -414,7 +418,7 @@ def run_decode(L, R, args, pk):
     res = {"metric": "decode tokens/s per layer", "value": R.world * w.B / (ms / 1e3), "unit": "tokens/s",
            "ms_per_step": ms, "steps": steps,
            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "d": w.d, "D": w.D, "eta": w.eta, "lambda": w.lam,
-                      "prefix": w.n, "state_bytes": lola_state_bytes(L, lay)},
+                      "prefix": w.n, "state_bytes": lola_state_bytes(L, lay), "read_mask": args.read_mask},
            "kernels": kt, "clocks": clk.summary(), "gpu_launches": sum(v["launches"] for v in kt.values())}
     dk_ = kt.get("decode")
     if dk_:
@@ -434,22 +438,22 @@ def lola_state_bytes(L, lay):
 # the CPU oracle
 # ---------------------------------------------------------------------------------------
 
-def oracle_sample(x, w, heads: int):
+def oracle_sample(x, w, heads: int, read_mask: int = 0):
     """Runs the oracle on the first `heads` heads of the workload; returns (seconds, tokens, threads)."""
     from oracle import inc
     BH = w.B * w.Hh
     heads = min(heads, BH)
     sl = lambda a: a.reshape(BH, *a.shape[2:])[:heads]  # noqa: E731
     t0 = time.perf_counter()
-    out = inc.run(sl(x.q), sl(x.k), sl(x.v), x.W, w.eta, w.lam, w.dtype)
+    out = inc.run(sl(x.q), sl(x.k), sl(x.v), x.W, w.eta, w.lam, w.dtype, read_mask=read_mask)
     dt = time.perf_counter() - t0
     return dt, heads * w.n / w.Hh, out["threads"]
 
 
-def cpu_baseline(x, w):
+def cpu_baseline(x, w, read_mask: int = 0):
     """The oracle over every head of the prefill workload (about 35 core-seconds)."""
     heads = w.B * w.Hh
-    dt, tokens, threads = oracle_sample(x, w, heads)
+    dt, tokens, threads = oracle_sample(x, w, heads, read_mask)
     return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"all {heads} heads of {w.name}, full n={w.n} "
                       f"({tokens:g} token-equivalents in {dt:.2f} s)"}
@@ -464,11 +468,11 @@ def run_reference(args):
     x = synth.make_inputs(w, B=1)         # one sequence's 32 heads: the sample is drawn from them
     heads = min(w.Hh, max(1, os.cpu_count() or 1))
     for _ in range(args.warmup):
-        oracle_sample(x, x.w, heads)
+        oracle_sample(x, x.w, heads, args.read_mask)
     times = []
     tokens = threads = 0
     for _ in range(args.steps):
-        dt, tokens, threads = oracle_sample(x, x.w, heads)
+        dt, tokens, threads = oracle_sample(x, x.w, heads, args.read_mask)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = tokens / (ms / 1e3)
@@ -505,7 +509,7 @@ def main():
     dec = None if args.no_decode else run_decode(L, R, args, pk)
     cpu = None
     if R.rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(pre["x"], w)
+        cpu = cpu_baseline(pre["x"], w, args.read_mask)
     if R.rank == 0:
         launches = pre["launches"] * 1
         line = {
@@ -514,7 +518,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta,
                        "lambda": w.lam, "chunk": w.chunk, "l2": "inputs 402 MB > 129 MB L2, no flush",
-                       "parallelism": f"replicas x{R.world}"},
+                       "parallelism": f"replicas x{R.world}", "read_mask": args.read_mask},
             "roofline": pre.get("roofline"), "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
             "clocks": pre["clocks"], "kernels": pre["kernels"], "peaks": {k: pk[k] for k in
                                                                         ("hbm_gbs", "bf16_tflops", "fp32_tflops",
