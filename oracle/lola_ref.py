@@ -213,6 +213,90 @@ def lola_set(q, k, v, W, eta: int, lam: int, read_mask: int = 0):
                 cache=np.array(sorted(cache), np.int64), written=np.array(written, np.int64))
 
 
+def lola_chunk_run(q, k, v, W, eta: int, lam: int, C: int, trace=None):
+    """Chunk-granular LoLA (section 2.6, Eq. 15, the notes' own prefill) on one head; float64.
+
+    Readings (the notes call the mapping between eta, the window and the chunk length
+    ambiguous; these are the ones taken): the sequence is cut into chunks of C tokens; the
+    window holds the last eta / C chunks, the current one included (eta a positive
+    multiple of C), so a query of chunk c reads its own chunk up to itself and the eta/C - 1
+    chunks before it; every query of a chunk reads the state (H, s) and the cache as they
+    stood when the chunk began; when a chunk begins (after the first eta/C), the oldest
+    chunk of the previous window leaves it and joins the cache as candidates, each scored
+    (SRE, Eq. 10, the empty-memory rule R3) against the current (H, s); if there are more
+    than lambda, the lambda highest stay and the rest are written into (H, s) at once, the
+    lowest SRE first and the older position first among equal ones.  With C = 1 this is the
+    per-token rule (``lola_run``), final state included.
+
+    Returns Y (n, d_v), write_step (n,): for every written key the start of the chunk
+    before which it was written (the first query that reads it through the state), else
+    -1; H, s and the final cache and window positions.  ``trace``: an optional list that
+    receives (chunk start, {candidate: SRE^2}, written, kept) for every scored decision."""
+    if C < 1 or eta < C or eta % C:
+        raise ValueError(f"chunk mode needs eta a positive multiple of C (eta = {eta}, C = {C})")
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n, dk = k.shape
+    dv = v.shape[1]
+    PQ, PK = phi(q, W), phi(k, W)
+    D = PK.shape[1]
+    scale = 1.0 / math.sqrt(dk)
+    nwc = eta // C
+    H = np.zeros((D, dv))
+    s = np.zeros(D)
+    cache: list[int] = []
+    write_step = np.full(n, -1, np.int64)
+    Y = np.zeros((n, dv))
+    nch = (n + C - 1) // C
+    for c in range(nch):
+        c0, c1 = c * C, min(n, (c + 1) * C)
+        e = c - nwc          # the chunk that leaves the window as chunk c begins
+        if e >= 0:
+            E = list(cache) + list(range(e * C, (e + 1) * C))
+            if len(E) <= lam:
+                cache = E
+            else:
+                sq = {j: sre_sq(H, s, PK[j], v[j]) for j in E}
+                order = sorted(E, key=lambda j: (sq[j], j))
+                if trace is not None:
+                    trace.append((c0, sq, order[:len(E) - lam], order[len(E) - lam:]))
+                for j in order[:len(E) - lam]:
+                    H += np.outer(PK[j], v[j])
+                    s += PK[j]
+                    write_step[j] = c0
+                cache = sorted(order[len(E) - lam:])
+        w0 = max(0, (c - nwc + 1) * C)
+        for t in range(c0, c1):
+            exact = list(range(w0, t + 1)) + cache
+            Y[t] = _output(q[t], PQ[t], exact, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
+    win = list(range(max(0, (nch - nwc) * C), n)) if nch else []
+    return dict(Y=Y, write_step=write_step, H=H, s=s, cache=np.array(sorted(cache), np.int64),
+                window=np.array(win, np.int64))
+
+
+def window_chunks_plus_linear(q, k, v, W, eta: int, C: int):
+    """lambda = 0 in chunk mode: a query of chunk c reads softmax over its window chunks
+    (chunks c - eta/C + 1 .. c, up to itself) and the linear state over every token
+    before them, one shared denominator."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n = q.shape[0]
+    PQ, PK = phi(q, W), phi(k, W)
+    t = np.arange(n)[:, None]
+    j = np.arange(n)[None, :]
+    wstart = np.maximum(0, (t // C - eta // C + 1) * C)
+    in_win = (j <= t) & (j >= wstart)
+    in_state = j < wstart
+    a = (q @ k.T) / math.sqrt(q.shape[1])
+    m = np.where(in_win, a, -np.inf).max(axis=1, keepdims=True)
+    ws = np.where(in_win, np.exp(np.where(in_win, a, 0.0) - m), 0.0)
+    wl = np.where(in_state, PQ @ PK.T, 0.0) * np.exp(-m)
+    wt = ws + wl
+    return (wt @ v) / wt.sum(axis=1, keepdims=True)
+
+
 # ---------------------------------------------------------------------------
 # Closed forms the method reduces to (used as pins)
 # ---------------------------------------------------------------------------

@@ -360,3 +360,73 @@ def test_read_mask_that_leaves_nothing_is_rejected():
     with pytest.raises(ValueError):
         inc.run(np.asarray(q, np.float32)[None], np.asarray(k, np.float32)[None], np.asarray(v, np.float32)[None],
                 x.W, 0, 3, "f32", read_mask=HIDE_STATE)
+
+
+# ---------------------------------------------------------------------------
+# chunk-granular allocation (section 2.6, Eq. 15; readings in lola_chunk_run)
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("eta,lam", [(1, 0), (1, 6), (3, 2), (5, 4), (6, 60)])
+def test_chunk_mode_with_unit_chunks_is_the_per_token_rule(eta, lam):
+    """C = 1: every step evicts one token before its read, as the per-token rule does."""
+    x = synth.gauss_inputs(1, 1, 48, 8, 8, "f32", seed=70 + eta, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    a = R.lola_run(q, k, v, x.W, eta, lam)
+    b = R.lola_chunk_run(q, k, v, x.W, eta, lam, 1)
+    assert np.array_equal(a["write_step"], b["write_step"])
+    np.testing.assert_array_equal(b["Y"], a["Y"])
+    np.testing.assert_array_equal(b["H"], a["H"])
+    assert np.array_equal(a["cache"], b["cache"]) and np.array_equal(np.sort(a["window"]), b["window"])
+
+
+@pytest.mark.parametrize("C,mult", [(4, 1), (4, 2), (8, 1), (8, 3)])
+def test_chunk_mode_zero_cache_is_window_chunks_plus_linear(C, mult):
+    """lambda = 0: every token leaving the window chunks is written; the read is the window
+    chunks plus the linear state over everything before them."""
+    x = synth.gauss_inputs(1, 1, 50, 8, 8, "f32", seed=75 + C, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_chunk_run(q, k, v, x.W, mult * C, 0, C)
+    np.testing.assert_allclose(o["Y"], R.window_chunks_plus_linear(q, k, v, x.W, mult * C, C), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("C,eta", [(4, 8), (8, 8), (16, 32)])
+def test_chunk_mode_without_writes_is_causal_softmax(C, eta):
+    """lambda >= n: nothing is written, the cache keeps every evicted key, so the read is
+    causal softmax attention."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=80 + C, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_chunk_run(q, k, v, x.W, eta, 40, C)
+    assert (o["write_step"] == -1).all()
+    np.testing.assert_allclose(o["Y"], R.causal_softmax_attention(q, k, v), rtol=1e-11, atol=1e-12)
+
+
+@pytest.mark.parametrize("C,eta,lam", [(4, 8, 6), (8, 8, 5), (8, 16, 12)])
+def test_chunk_mode_keeps_the_highest_sre_and_writes_each_key_once(C, eta, lam):
+    """Every scored decision keeps exactly lambda candidates, all with larger (SRE, position)
+    than every written one; at the end window, cache and written set partition the tokens
+    and (H, s) are the sums over the written set."""
+    x = synth.gauss_inputs(1, 1, 64, 8, 8, "f32", seed=85 + C, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    tr = []
+    o = R.lola_chunk_run(q, k, v, x.W, eta, lam, C, trace=tr)
+    assert tr, "no decision was scored"
+    for c0, sq, written, kept in tr:
+        assert c0 % C == 0 and len(kept) == lam and written
+        assert max((sq[j], j) for j in written) < min((sq[j], j) for j in kept)
+        assert all(o["write_step"][j] == c0 for j in written)
+    written = set(np.flatnonzero(o["write_step"] >= 0).tolist())
+    win, cache = set(o["window"].tolist()), set(o["cache"].tolist())
+    assert not (win & cache) and not (win & written) and not (cache & written)
+    assert win | cache | written == set(range(64))
+    PK = R.phi(k, x.W)
+    wl = sorted(written)
+    np.testing.assert_allclose(o["H"], PK[wl].T @ v[wl], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o["s"], PK[wl].sum(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_chunk_mode_needs_whole_window_chunks():
+    x = synth.gauss_inputs(1, 1, 16, 8, 8, "f32", seed=90, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    for eta, C in ((6, 4), (2, 4), (0, 1)):
+        with pytest.raises(ValueError):
+            R.lola_chunk_run(q, k, v, x.W, eta, 4, C)
