@@ -70,7 +70,20 @@ typedef struct {
     int32_t chunk;      /* prefill schedule granularity C; no effect on results */
     int32_t dtype;      /* lola_dtype */
     int32_t read_mask;  /* 0, or lola_read_flags: memories left out of every query's read */
+    int32_t alloc;      /* lola_alloc: LOLA_ALLOC_TOKEN (0, the default) or LOLA_ALLOC_CHUNK */
 } lola_config;
+
+/* Allocation granularity.  LOLA_ALLOC_TOKEN: the per-token rule (sections 2.3-2.4); the
+ * chunk length only schedules the work.  LOLA_ALLOC_CHUNK (section 2.6, Eq. 15, the notes'
+ * own prefill): the window is the last eta / chunk chunks, the current one included; each
+ * chunk's queries read the state and cache it began with; as a chunk begins, the oldest
+ * chunk of the previous window joins the cache, every candidate is scored against the
+ * current state, the lambda highest-SRE stay and the rest are written at once.  Needs eta
+ * a positive multiple of chunk and read_mask = 0; lola_prefill only (lola_decode_step
+ * returns LOLA_ERR_UNSUPPORTED), and its write_pos log is per key: the chunk start at which
+ * key j was written, -1 if never.  The exported state holds H, s, the cache positions and
+ * rows and the window ring; the per-slot N, z and the next evictee's record stay zero. */
+typedef enum { LOLA_ALLOC_TOKEN = 0, LOLA_ALLOC_CHUNK = 1 } lola_alloc;
 
 /* Read mask (appendix I, Table 12: a read-time ablation).  The cache and the state are
  * updated exactly as with read_mask = 0 (same decisions, same memory); only the output

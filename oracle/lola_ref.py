@@ -213,7 +213,7 @@ def lola_set(q, k, v, W, eta: int, lam: int, read_mask: int = 0):
                 cache=np.array(sorted(cache), np.int64), written=np.array(written, np.int64))
 
 
-def lola_chunk_run(q, k, v, W, eta: int, lam: int, C: int, trace=None):
+def lola_chunk_run(q, k, v, W, eta: int, lam: int, C: int, trace=None, replay=None):
     """Chunk-granular LoLA (section 2.6, Eq. 15, the notes' own prefill) on one head; float64.
 
     Readings (the notes call the mapping between eta, the window and the chunk length
@@ -231,7 +231,12 @@ def lola_chunk_run(q, k, v, W, eta: int, lam: int, C: int, trace=None):
     Returns Y (n, d_v), write_step (n,): for every written key the start of the chunk
     before which it was written (the first query that reads it through the state), else
     -1; H, s and the final cache and window positions.  ``trace``: an optional list that
-    receives (chunk start, {candidate: SRE^2}, written, kept) for every scored decision."""
+    receives (chunk start, {candidate: SRE^2}, written, kept) for every scored decision.
+    ``replay``: another implementation's write_step; the oracle then writes, at every
+    chunk start, the candidates that log says, checks that their count is the one due, and
+    reports as max_gap the largest relative SRE excess of a written candidate over a kept
+    one (0 when the log follows the oracle's own order; ValueError if it is not a valid
+    decision)."""
     if C < 1 or eta < C or eta % C:
         raise ValueError(f"chunk mode needs eta a positive multiple of C (eta = {eta}, C = {C})")
     q = np.asarray(q, np.float64)
@@ -249,6 +254,7 @@ def lola_chunk_run(q, k, v, W, eta: int, lam: int, C: int, trace=None):
     write_step = np.full(n, -1, np.int64)
     Y = np.zeros((n, dv))
     nch = (n + C - 1) // C
+    max_gap = 0.0
     for c in range(nch):
         c0, c1 = c * C, min(n, (c + 1) * C)
         e = c - nwc          # the chunk that leaves the window as chunk c begins
@@ -259,20 +265,33 @@ def lola_chunk_run(q, k, v, W, eta: int, lam: int, C: int, trace=None):
             else:
                 sq = {j: sre_sq(H, s, PK[j], v[j]) for j in E}
                 order = sorted(E, key=lambda j: (sq[j], j))
+                written, kept = order[:len(E) - lam], order[len(E) - lam:]
+                if replay is not None:
+                    written = [j for j in order if replay[j] == c0]   # added in (SRE, position) order
+                    kept = [j for j in order if replay[j] != c0]
+                    if len(written) != len(E) - lam:
+                        raise ValueError(f"replay writes {len(written)} keys at {c0}, {len(E) - lam} are due")
+                    for w in written:
+                        for kp in kept:
+                            if (sq[w], w) > (sq[kp], kp):
+                                sw, sk = math.sqrt(sq[w]), math.sqrt(sq[kp])
+                                max_gap = max(max_gap, (sw - sk) / sk if sk > 0 else math.inf)
                 if trace is not None:
-                    trace.append((c0, sq, order[:len(E) - lam], order[len(E) - lam:]))
-                for j in order[:len(E) - lam]:
+                    trace.append((c0, sq, written, kept))
+                for j in written:
                     H += np.outer(PK[j], v[j])
                     s += PK[j]
                     write_step[j] = c0
-                cache = sorted(order[len(E) - lam:])
+                cache = sorted(kept)
         w0 = max(0, (c - nwc + 1) * C)
         for t in range(c0, c1):
             exact = list(range(w0, t + 1)) + cache
             Y[t] = _output(q[t], PQ[t], exact, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
     win = list(range(max(0, (nch - nwc) * C), n)) if nch else []
+    if replay is not None and not np.array_equal(np.asarray(replay), write_step):
+        raise ValueError("replay writes a key that is not a candidate when it says")
     return dict(Y=Y, write_step=write_step, H=H, s=s, cache=np.array(sorted(cache), np.int64),
-                window=np.array(win, np.int64))
+                window=np.array(win, np.int64), max_gap=max_gap)
 
 
 def window_chunks_plus_linear(q, k, v, W, eta: int, C: int):

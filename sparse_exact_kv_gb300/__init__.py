@@ -27,6 +27,8 @@ LOLA_F32 = 0
 LOLA_BF16 = 1
 LOLA_READ_HIDE_STATE = 1
 LOLA_READ_HIDE_CACHE = 2
+LOLA_ALLOC_TOKEN = 0
+LOLA_ALLOC_CHUNK = 1
 
 # every symbol include/lola.h declares
 EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_check_config",
@@ -42,7 +44,7 @@ class lola_config(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hh", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("D", ctypes.c_int32), ("eta", ctypes.c_int32),
                 ("lambda_", ctypes.c_int32), ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("read_mask", ctypes.c_int32)]
+                ("read_mask", ctypes.c_int32), ("alloc", ctypes.c_int32)]
 
 
 class lola_state_layout(ctypes.Structure):
@@ -97,12 +99,13 @@ def _load():
 _lib = _load()
 
 
-def make_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dtype, read_mask=0) -> lola_config:
+def make_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dtype, read_mask=0, alloc=LOLA_ALLOC_TOKEN) -> lola_config:
     """``read_mask``: LOLA_READ_HIDE_STATE | LOLA_READ_HIDE_CACHE, memories left out of every
-    query's read (the memory and the decisions are unchanged)."""
+    query's read (the memory and the decisions are unchanged).  ``alloc``: LOLA_ALLOC_TOKEN
+    (the per-token rule) or LOLA_ALLOC_CHUNK (chunk-granular allocation)."""
     dt = dtype if isinstance(dtype, int) else {"f32": LOLA_F32, "bf16": LOLA_BF16,
                                                torch.float32: LOLA_F32, torch.bfloat16: LOLA_BF16}[dtype]
-    return lola_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dt, read_mask)
+    return lola_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dt, read_mask, alloc)
 
 
 def _ptr(t):
@@ -214,8 +217,9 @@ def lola_selftest_bounded_wait(limit_ns: int, stream=None):
 class Lola:
     """One layer's LoLA memory for B x Hh heads: owns the state and the prefill workspace."""
 
-    def __init__(self, B, Hh, d, D, eta, lam, chunk=64, dtype=torch.bfloat16, device="cuda", read_mask=0):
-        self.cfg = make_config(B, Hh, d, d, D, eta, lam, chunk, dtype, read_mask)
+    def __init__(self, B, Hh, d, D, eta, lam, chunk=64, dtype=torch.bfloat16, device="cuda", read_mask=0,
+                 alloc=LOLA_ALLOC_TOKEN):
+        self.cfg = make_config(B, Hh, d, d, D, eta, lam, chunk, dtype, read_mask, alloc)
         _check(lola_check_config(self.cfg), "config")
         self.dtype = dtype
         self.device = torch.device(device)

@@ -29,6 +29,10 @@ int32_t to_dims(const lola_config* c, Dims* d) {
         c->lambda < 0 || c->chunk < 1 || (c->dtype != LOLA_F32 && c->dtype != LOLA_BF16))
         return LOLA_ERR_INVALID_ARG;
     if (c->read_mask < 0 || c->read_mask > 3 || (c->read_mask != 0 && c->eta < 1)) return LOLA_ERR_INVALID_ARG;
+    if (c->alloc != LOLA_ALLOC_TOKEN && c->alloc != LOLA_ALLOC_CHUNK) return LOLA_ERR_INVALID_ARG;
+    if (c->alloc == LOLA_ALLOC_CHUNK &&
+        (c->chunk < 1 || c->eta < c->chunk || c->eta % c->chunk != 0 || c->read_mask != 0))
+        return LOLA_ERR_INVALID_ARG;
     if ((int64_t)c->B * c->Hh > (1 << 24)) return LOLA_ERR_UNSUPPORTED;
     const bool dims_ok = (c->d_k == 128 && c->d_v == 128 && c->D == 128) || (c->d_k == 64 && c->d_v == 64 && c->D == 64);
     if (!dims_ok) return LOLA_ERR_UNSUPPORTED;
@@ -45,6 +49,8 @@ int32_t to_dims(const lola_config* c, Dims* d) {
     d->chunk = c->chunk;
     d->dtype = c->dtype;
     d->read_mask = c->read_mask;
+    d->alloc = c->alloc;
+    if (d->alloc == LOLA_ALLOC_CHUNK && !chunk_mode_fits(*d)) return LOLA_ERR_UNSUPPORTED;
     return LOLA_OK;
 }
 
@@ -301,8 +307,10 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
         if (e != cudaSuccess) return cuda_fail(e, "side stream");
         e = cudaEventRecord(side->fork, st);
         if (e != cudaSuccess) return cuda_fail(e, "fork");
-        e = traced(LOLA_KERNEL_SELECT, st,
-                   [&]() { return launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st); });
+        e = traced(LOLA_KERNEL_SELECT, st, [&]() {
+            return d.alloc == LOLA_ALLOC_CHUNK ? launch_chunk_select(d, n, ws, K, V, static_cast<char*>(state), L, st)
+                                               : launch_select(d, n, ws, K, V, static_cast<char*>(state), L, st);
+        });
         if (e != cudaSuccess) return cuda_fail(e, "selection");
         e = cudaStreamWaitEvent(side->st, side->fork, 0);
         if (e != cudaSuccess) return cuda_fail(e, "fork wait");
@@ -330,6 +338,7 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W, in
     if (s != LOLA_OK) return s;
     if (!state || !W || !q || !k || !v || !y || w_head_stride < 0 || w_head_stride % 4 != 0)
         return LOLA_ERR_INVALID_ARG;
+    if (d.alloc == LOLA_ALLOC_CHUNK) return LOLA_ERR_UNSUPPORTED;   // the decode step is per token
     const void* ptrs[] = {state, W, q, k, v, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;

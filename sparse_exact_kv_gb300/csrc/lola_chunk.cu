@@ -1,0 +1,336 @@
+// K2c: chunk-granular allocation of LoLA prefill -- the notes' own prefill schedule.
+//
+// LoLA reading notes (arXiv 2505.23666v3), section 2.6, Eq. 15: the sequence is cut into
+// chunks of C tokens that share the memory they begin with; once a chunk is done, the
+// oldest window chunk is scored together with the sparse cache (about C + lambda
+// candidates, SRE of section 2.3, Eq. 10, against the current state), the lambda highest
+// stay exact and the rest are written into (H, s) at once.  Readings taken (the notes
+// call the window / chunk mapping ambiguous): the window is the last eta / C chunks, the
+// current one included; the scoring happens as the next chunk begins (so the memory after
+// the last token is not evicted from); the lowest SRE is written first and the older
+// position first among equal ones; the empty memory predicts 0 (SRE = ||v||).  With C = 1
+// this is the per-token rule.
+//
+// One CTA of 512 threads per head walks its chunks; H (float32) lives in shared memory.
+// At every chunk start c0: the snapshot for the output pass when c0 is a multiple of its
+// interval (the memory before this start's writes, as in the per-token chain); then the
+// candidates -- the cache, then the chunk leaving the window -- are scored 64 at a time
+// (warp w takes four candidates, lane l the value columns l*HC.., H rows read from shared
+// memory against the candidates' phi staged transposed), ranked by (SRE^2, position), and
+// the lowest P - lambda are added to H and s in rank order.  Every written key's step is
+// recorded as c0 (the first query that reads it through the state), which is the rule the
+// output kernels apply: key j is exact for query t iff j <= t < w_j, linear iff w_j <= t.
+#include "lola_chain.cuh"
+
+namespace lola {
+namespace {
+
+using chain::Shape;
+
+constexpr int kCkThreads = 512;
+constexpr int kCkWarps = kCkThreads / kWarp;
+constexpr int kG = 64;                 // candidates per scoring group, 4 per warp
+static_assert(kG == 4 * kCkWarps, "four candidates per warp");
+constexpr int kTS = kG + 4;            // row stride of the transposed phi tile (floats)
+
+struct ChunkArgs {
+    int n, eta, lam, C, nwc, snap, nck;
+    const float* phiK;         // [BH][n][D] float32
+    const void* K;             // io [BH][n][D]
+    const void* V;             // io [BH][n][DV]
+    int32_t* wstep;            // [BH][n]: chunk start at which key j was written, -1 never
+    int32_t* wpos;             // [BH][n] (the caller's log, nullable): the same per key
+    float* snapH;              // [BH][nck][D*DV] float32, or
+    __nv_bfloat16* snapHb;     // the same in bf16
+    float* snapS;              // [BH][nck][D]
+    int32_t* snapC;            // [BH][nck][lam]
+    char* state;
+    Layout L;
+};
+
+__host__ __device__ constexpr size_t a16c(size_t x) { return (x + 15) / 16 * 16; }
+
+// shared-memory plan (bytes), from the runtime lambda and C
+template <int D, int DV>
+struct CkPlan {
+    size_t H, tile, s, cpos, cand, keys, wlist, klist, total;
+    __host__ __device__ CkPlan(int lam, int C) {
+        const size_t P = (size_t)lam + C;
+        H = 0;
+        tile = H + 4ull * D * DV;
+        const size_t tile_b = 4ull * (D * kTS > kG * (D + DV) ? D * kTS : kG * (D + DV));
+        s = a16c(tile + tile_b);
+        cpos = a16c(s + 4ull * D);
+        cand = a16c(cpos + 4ull * (lam > 0 ? lam : 1));
+        keys = a16c(cand + 4 * P);
+        wlist = a16c(keys + 8 * P);
+        klist = a16c(wlist + 4 * P);
+        total = a16c(klist + 4ull * (lam > 0 ? lam : 1));
+    }
+};
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const ChunkArgs a) {
+    using S = Shape<D, DV>;
+    constexpr int HR = S::HR, HC = S::HC;
+    static_assert(kCkThreads == chain::kThreads, "H blocks of the chain layout");
+    extern __shared__ __align__(16) unsigned char sm[];
+    const CkPlan<D, DV> pl(a.lam, a.C);
+    float* Hs = reinterpret_cast<float*>(sm + pl.H);
+    float* tile = reinterpret_cast<float*>(sm + pl.tile);
+    float* ss = reinterpret_cast<float*>(sm + pl.s);
+    int* cpos = reinterpret_cast<int*>(sm + pl.cpos);
+    int* cand = reinterpret_cast<int*>(sm + pl.cand);
+    unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm + pl.keys);
+    int* wlist = reinterpret_cast<int*>(sm + pl.wlist);
+    int* klist = reinterpret_cast<int*>(sm + pl.klist);
+
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int bh = blockIdx.x;
+    const int n = a.n, lam = a.lam, C = a.C;
+    const int64_t row0 = (int64_t)bh * n;
+    const float* phiK = a.phiK + row0 * D;
+    const T* Vin = static_cast<const T*>(a.V) + row0 * DV;
+    int32_t* wst = a.wstep + row0;
+    int32_t* wps = a.wpos ? a.wpos + row0 : nullptr;
+
+    for (int i = tid; i < D * DV; i += kCkThreads) Hs[i] = 0.f;
+    for (int i = tid; i < D; i += kCkThreads) ss[i] = 0.f;
+    for (int i = tid; i < n; i += kCkThreads) {
+        wst[i] = -1;
+        if (wps) wps[i] = -1;
+    }
+    int nc = 0, nwritten = 0;   // (uniform)
+    __syncthreads();
+
+    const int nch = (n + C - 1) / C;
+    for (int c = 0; c < nch; ++c) {
+        const int c0 = c * C;
+        // ---- the output pass's snapshot: the memory the chunk begins with, before this
+        //      start's writes ----
+        if (c0 % a.snap == 0) {
+            const int64_t sc = (int64_t)bh * a.nck + c0 / a.snap;
+            if (a.snapHb) {
+                for (int i = tid; i < D * DV; i += kCkThreads) a.snapHb[sc * D * DV + i] = __float2bfloat16_rn(Hs[i]);
+            } else {
+                for (int i = tid; i < D * DV; i += kCkThreads) a.snapH[sc * D * DV + i] = Hs[i];
+            }
+            for (int i = tid; i < D; i += kCkThreads) a.snapS[sc * D + i] = ss[i];
+            for (int i = tid; i < lam; i += kCkThreads) a.snapC[sc * lam + i] = i < nc ? cpos[i] : -1;
+        }
+        const int e = c - a.nwc;   // the chunk that leaves the window now
+        if (e < 0) continue;
+        const int P = nc + C;
+        for (int i = tid; i < P; i += kCkThreads) cand[i] = i < nc ? cpos[i] : e * C + (i - nc);
+        __syncthreads();
+        if (P <= lam) {             // room for every candidate
+            for (int i = tid; i < C; i += kCkThreads) cpos[nc + i] = e * C + i;
+            nc = P;
+            __syncthreads();
+            continue;
+        }
+
+        // ---- SRE^2 of every candidate against the current (H, s), kG at a time ----
+        for (int g0 = 0; g0 < P; g0 += kG) {
+            for (int i = tid; i < kG * D; i += kCkThreads) {
+                const int j = i / D, r = i % D;
+                const int p = g0 + j < P ? cand[g0 + j] : -1;
+                tile[r * kTS + j] = p >= 0 ? phiK[(int64_t)p * D + r] : 0.f;
+            }
+            __syncthreads();
+            float acc[4][HC];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int q = 0; q < HC; ++q) acc[i][q] = 0.f;
+#pragma unroll 4
+            for (int r = 0; r < D; ++r) {
+                float h[HC];
+                chain::h_vec_load<HC>(Hs + r * DV + lane * HC, h);
+                const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
+                const float fi[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+#pragma unroll
+                    for (int q = 0; q < HC; ++q) acc[i][q] = fmaf(fi[i], h[q], acc[i][q]);
+            }
+            // z = s^T phi(k): lane l takes rows l, l + 32, ...
+            float z4[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int r = lane; r < D; r += kWarp) {
+                const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
+                const float sr = ss[r];
+                z4[0] = fmaf(f.x, sr, z4[0]);
+                z4[1] = fmaf(f.y, sr, z4[1]);
+                z4[2] = fmaf(f.z, sr, z4[2]);
+                z4[3] = fmaf(f.w, sr, z4[3]);
+            }
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int j = g0 + 4 * warp + i;
+                const int p = j < P ? cand[j] : -1;
+                const float z = warp_sum(z4[i]);
+                float dd = 0.f, vv = 0.f;
+                if (p >= 0) {
+#pragma unroll
+                    for (int q = 0; q < HC; ++q) {
+                        const float vq = IO<T>::ld(Vin, (int64_t)p * DV + lane * HC + q);
+                        const float d = fmaf(-z, vq, acc[i][q]);   // (N - z v), SRE^2 = |.|^2 / z^2
+                        dd = fmaf(d, d, dd);
+                        vv = fmaf(vq, vq, vv);
+                    }
+                }
+                dd = warp_sum(dd);
+                vv = warp_sum(vv);
+                if (lane == 0 && p >= 0) {
+                    const float sre2 = z == 0.f ? vv : dd / (z * z);   // empty memory: ||v||^2
+                    keys[j] = ((unsigned long long)__float_as_uint(sre2) << 32) | (unsigned)p;
+                }
+            }
+            __syncthreads();   // the tile is restaged
+        }
+
+        // ---- rank by (SRE^2, position): the lowest P - lambda are written ----
+        const int nwr = P - lam;
+        for (int i = tid; i < P; i += kCkThreads) {
+            const unsigned long long k = keys[i];
+            int r = 0;
+            for (int j = 0; j < P; ++j) r += keys[j] < k ? 1 : 0;
+            const int p = (int)(k & 0xffffffffu);
+            if (r < nwr) wlist[r] = p;
+            else klist[r - nwr] = p;
+        }
+        __syncthreads();
+
+        // ---- H += sum phi(k) v^T and s += sum phi(k) over the written keys, in rank order;
+        //      thread (warp w, lane l) owns rows w*HR .. and columns l*HC .. of H ----
+        float hreg[HR * HC];
+        chain::h_load<D, DV>(hreg, Hs, warp, lane);
+        float sreg = tid < D ? ss[tid] : 0.f;
+        float* tphi = tile;              // [kG][D]
+        float* tv = tile + kG * D;       // [kG][DV]
+        for (int w0 = 0; w0 < nwr; w0 += kG) {
+            const int cnt = min(kG, nwr - w0);
+            for (int i = tid; i < cnt * D; i += kCkThreads) {
+                const int j = i / D, r = i % D;
+                tphi[j * D + r] = phiK[(int64_t)wlist[w0 + j] * D + r];
+            }
+            for (int i = tid; i < cnt * DV; i += kCkThreads) {
+                const int j = i / DV, q = i % DV;
+                tv[j * DV + q] = IO<T>::ld(Vin, (int64_t)wlist[w0 + j] * DV + q);
+            }
+            __syncthreads();
+            for (int j = 0; j < cnt; ++j) {
+                float vh[HC];
+                chain::h_vec_load<HC>(tv + j * DV + lane * HC, vh);
+                chain::h_update<D, DV>(hreg, tphi + j * D, vh, warp);
+                if (tid < D) sreg += tphi[j * D + tid];
+            }
+            __syncthreads();
+        }
+        chain::h_store<D, DV>(Hs, hreg, warp, lane);
+        if (tid < D) ss[tid] = sreg;
+        for (int i = tid; i < nwr; i += kCkThreads) {
+            wst[wlist[i]] = c0;
+            if (wps) wps[wlist[i]] = c0;
+        }
+        for (int i = tid; i < lam; i += kCkThreads) cpos[i] = klist[i];
+        nc = lam;
+        nwritten += nwr;
+        __syncthreads();
+    }
+
+    // ---- export: header, H, s, the cache (positions and rows) and the window ring ----
+    char* rec = a.state + (int64_t)bh * a.L.head_bytes;
+    if (tid == 0) {
+        int32_t* hdr = reinterpret_cast<int32_t*>(rec);
+        hdr[HDR_T] = n;
+        hdr[HDR_NCACHE] = nc;
+        hdr[HDR_NWRITTEN] = nwritten;
+        hdr[HDR_STATUS] = 0;
+    }
+    float* Hg = reinterpret_cast<float*>(rec + a.L.H);
+    for (int i = tid; i < D * DV; i += kCkThreads) Hg[i] = Hs[i];
+    float* sg = reinterpret_cast<float*>(rec + a.L.s);
+    for (int i = tid; i < D; i += kCkThreads) sg[i] = ss[i];
+    const T* Kin = static_cast<const T*>(a.K) + row0 * D;
+    int32_t* cp = reinterpret_cast<int32_t*>(rec + a.L.c_pos);
+    T* ck = reinterpret_cast<T*>(rec + a.L.c_k);
+    T* cv = reinterpret_cast<T*>(rec + a.L.c_v);
+    float* cph = reinterpret_cast<float*>(rec + a.L.c_phi);
+    for (int i = tid; i < nc; i += kCkThreads) cp[i] = cpos[i];
+    for (int i = tid; i < nc * D; i += kCkThreads) {
+        const int sl = i / D, r = i % D;
+        ck[(int64_t)sl * D + r] = Kin[(int64_t)cpos[sl] * D + r];
+        cph[(int64_t)sl * D + r] = phiK[(int64_t)cpos[sl] * D + r];
+    }
+    for (int i = tid; i < nc * DV; i += kCkThreads) {
+        const int sl = i / DV, q = i % DV;
+        cv[(int64_t)sl * DV + q] = Vin[(int64_t)cpos[sl] * DV + q];
+    }
+    // the window after the last token: positions [(nch - nwc) C, n), entry p % eta
+    const int wlo = max(0, (nch - a.nwc) * C);
+    int32_t* wp = reinterpret_cast<int32_t*>(rec + a.L.win_pos);
+    T* wk = reinterpret_cast<T*>(rec + a.L.win_k);
+    T* wv = reinterpret_cast<T*>(rec + a.L.win_v);
+    float* wph = reinterpret_cast<float*>(rec + a.L.win_phi);
+    for (int p = wlo + tid; p < n; p += kCkThreads) {
+        const int e = p % a.eta;
+        wp[e] = p;
+        for (int r = 0; r < D; ++r) {
+            wk[(int64_t)e * D + r] = Kin[(int64_t)p * D + r];
+            wph[(int64_t)e * D + r] = phiK[(int64_t)p * D + r];
+        }
+        for (int q = 0; q < DV; ++q) wv[(int64_t)e * DV + q] = Vin[(int64_t)p * DV + q];
+    }
+}
+
+template <int D, int DV, typename T>
+cudaError_t launch_chunk_t(const Dims& d, int n, const Workspace& ws, const void* K, const void* V, char* state,
+                           const Layout& L, cudaStream_t st) {
+    ChunkArgs a;
+    a.n = n;
+    a.eta = d.eta;
+    a.lam = d.lam;
+    a.C = d.chunk;
+    a.nwc = d.eta / d.chunk;
+    a.snap = ws.snap_interval;
+    a.nck = ws.nck;
+    a.phiK = ws.phiK;
+    a.K = K;
+    a.V = V;
+    a.wstep = ws.wstep;
+    a.wpos = ws.wpos;
+    a.snapH = ws.snapH;
+    a.snapHb = ws.snapHb;
+    a.snapS = ws.snapS;
+    a.snapC = ws.snapC;
+    a.state = state;
+    a.L = L;
+    const size_t smem = CkPlan<D, DV>(d.lam, d.chunk).total;
+    auto kern = chunk_select_kernel<D, DV, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<d.BH, kCkThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool chunk_mode_fits(const Dims& d) {
+    const size_t smem = d.D == 128 ? CkPlan<128, 128>(d.lam, d.chunk).total : CkPlan<64, 64>(d.lam, d.chunk).total;
+    return smem <= 227 * 1024;
+}
+
+cudaError_t launch_chunk_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
+                                char* state, const Layout& L, cudaStream_t st) {
+    const bool bf = d.dtype == LOLA_BF16;
+    if (d.D == 128 && d.dv == 128)
+        return bf ? launch_chunk_t<128, 128, __nv_bfloat16>(d, n, ws, K, V, state, L, st)
+                  : launch_chunk_t<128, 128, float>(d, n, ws, K, V, state, L, st);
+    if (d.D == 64 && d.dv == 64)
+        return bf ? launch_chunk_t<64, 64, __nv_bfloat16>(d, n, ws, K, V, state, L, st)
+                  : launch_chunk_t<64, 64, float>(d, n, ws, K, V, state, L, st);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace lola

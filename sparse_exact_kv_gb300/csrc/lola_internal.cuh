@@ -15,7 +15,7 @@ constexpr int kWarp = 32;
 // Sizes and the public per-head state layout (see lola.h)
 // ---------------------------------------------------------------------------------
 struct Dims {
-    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype, read_mask;
+    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype, read_mask, alloc;
     int io_bytes() const { return dtype == LOLA_BF16 ? 2 : 4; }
 };
 
@@ -215,6 +215,11 @@ cudaError_t launch_phi(const Dims& d, int n, const void* X, const float* W, int6
                        float* out, __nv_bfloat16* out_bf16, cudaStream_t st);
 cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
                           char* state, const Layout& L, cudaStream_t st);
+// the chunk-granular allocation (alloc = LOLA_ALLOC_CHUNK); chunk_mode_fits: its shared
+// memory plan fits one CTA
+bool chunk_mode_fits(const Dims& d);
+cudaError_t launch_chunk_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
+                                char* state, const Layout& L, cudaStream_t st);
 cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                           const void* V, void* Y, cudaStream_t st);
 bool output_tc_supported(const Dims& d);

@@ -144,3 +144,19 @@ def test_read_mask_validation(lib):
     base = lib.make_config(2, 4, 128, 128, 128, 64, 64, 64, "bf16")
     assert lib.lola_state_bytes(ok) == lib.lola_state_bytes(base)
     assert lib.lola_prefill_workspace_bytes(ok, 512) == lib.lola_prefill_workspace_bytes(base, 512)
+
+
+def test_chunk_alloc_validation(lib):
+    """Chunk-granular allocation needs whole window chunks and no read mask."""
+    C = lib.LOLA_ALLOC_CHUNK
+    ok = lib.make_config(2, 4, 128, 128, 128, 128, 64, 64, "bf16", alloc=C)
+    assert lib.lola_check_config(ok) == 0
+    for eta, chunk, mask in ((96, 64, 0), (32, 64, 0), (128, 64, 1)):
+        cfg = lib.make_config(2, 4, 128, 128, 128, eta, 64, chunk, "bf16", read_mask=mask, alloc=C)
+        assert lib.lola_check_config(cfg) == lib.LOLA_ERR_INVALID_ARG, (eta, chunk, mask)
+    assert lib.lola_check_config(lib.make_config(2, 4, 128, 128, 128, 64, 64, 64, "bf16", alloc=2)) == \
+        lib.LOLA_ERR_INVALID_ARG
+    # the decode step is per token: refused for a chunk-mode layer before anything runs
+    P = ctypes.c_void_p
+    st = lib._lib.lola_decode_step(ctypes.byref(ok), P(256), P(256), 0, P(256), P(256), P(256), P(256), None, None)
+    assert st == lib.LOLA_ERR_UNSUPPORTED

@@ -11,7 +11,7 @@ import synth
 from oracle import inc
 from oracle import lola_ref as R
 
-from lola_parity import check_decisions, check_outputs, run_prefill, to_dev, to_f64
+from lola_parity import GAP, check_decisions, check_outputs, run_prefill, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -223,6 +223,38 @@ def test_read_mask_prefill_and_decode_match_oracle(L, dtype, d, mask):
     yall = np.concatenate([Y, to_f64(torch.stack(ys, 2))], axis=2)
     ref, _ = check_decisions(x, wall, eta, lam, read_mask=mask)
     check_outputs(yall, ref["Y"], dtype)
+
+
+@pytest.mark.parametrize("dtype,d,eta,lam,chunk", [("f32", 64, 32, 24, 16), ("f32", 128, 32, 40, 16),
+                                                   ("bf16", 128, 64, 64, 64), ("bf16", 128, 128, 32, 64),
+                                                   ("bf16", 64, 16, 100, 16)])
+def test_chunk_alloc_prefill_matches_oracle(L, dtype, d, eta, lam, chunk):
+    """Chunk-granular allocation (section 2.6, Eq. 15): the per-key write log equals the
+    oracle's in float32 (bf16: may differ only where the SRE gap is below 1e-3, checked by
+    replaying it); outputs along that log, the final memory and cache follow the oracle."""
+    from oracle import lola_ref as R
+    B, Hh, n = 1, 2, 300
+    x = synth.gauss_inputs(B, Hh, n, d, d, dtype, seed=100 + lam)
+    Y, wlog, lay = run_prefill(L, x, eta, lam, chunk, alloc=L.LOLA_ALLOC_CHUNK)
+    st = lay.read_state()
+    q, k, v = (x.widened(a) for a in "qkv")
+    for h in range(Hh):
+        if dtype == "f32":
+            ref = R.lola_chunk_run(q[0, h], k[0, h], v[0, h], x.W, eta, lam, chunk)
+            assert np.array_equal(wlog[0, h], ref["write_step"]), "float32 chunk decisions differ"
+        else:
+            ref = R.lola_chunk_run(q[0, h], k[0, h], v[0, h], x.W, eta, lam, chunk, replay=wlog[0, h])
+            assert ref["max_gap"] < GAP, f"a chunk decision is {ref['max_gap']:.3e} away from the best"
+        check_outputs(Y[0, h], ref["Y"], dtype)
+        np.testing.assert_allclose(st["H"][h], ref["H"], rtol=2e-4, atol=2e-4)
+        np.testing.assert_allclose(st["s"][h], ref["s"], rtol=2e-5, atol=2e-5)
+        assert sorted(p for p in st["c_pos"][h] if p >= 0) == ref["cache"].tolist()
+        assert st["t"][h] == n and st["n_cache"][h] == len(ref["cache"])
+    with pytest.raises(L.LolaError):
+        dev = "cuda"
+        Q, K, V = (to_dev(getattr(x, a), dev, dtype) for a in "qkv")
+        lay.decode_step(Q[:, :, 0].contiguous(), K[:, :, 0].contiguous(), V[:, :, 0].contiguous(),
+                        torch.from_numpy(x.W).to(dev))
 
 
 def test_bounded_wait_gives_up_and_reports(L):

@@ -430,3 +430,27 @@ def test_chunk_mode_needs_whole_window_chunks():
     for eta, C in ((6, 4), (2, 4), (0, 1)):
         with pytest.raises(ValueError):
             R.lola_chunk_run(q, k, v, x.W, eta, 4, C)
+
+
+def test_chunk_mode_replay_of_own_and_of_a_swapped_log():
+    """Replaying the oracle's own log reproduces it with no gap; swapping one written and one
+    kept candidate of a decision is followed and reported as that pair's SRE excess."""
+    x = synth.gauss_inputs(1, 1, 64, 8, 8, "f32", seed=91, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    tr = []
+    own = R.lola_chunk_run(q, k, v, x.W, 8, 6, 8, trace=tr)
+    rep = R.lola_chunk_run(q, k, v, x.W, 8, 6, 8, replay=own["write_step"])
+    assert rep["max_gap"] == 0.0
+    np.testing.assert_array_equal(rep["Y"], own["Y"])
+    c0, sq, written, kept = tr[-1]
+    w, kp = max(written, key=lambda j: (sq[j], j)), min(kept, key=lambda j: (sq[j], j))
+    log = own["write_step"].copy()
+    log[w], log[kp] = -1, c0
+    tr2 = []
+    swapped = R.lola_chunk_run(q, k, v, x.W, 8, 6, 8, replay=log, trace=tr2)
+    expect = (math.sqrt(sq[kp]) - math.sqrt(sq[w])) / math.sqrt(sq[w])
+    assert swapped["max_gap"] == pytest.approx(expect, rel=1e-12)
+    bad = own["write_step"].copy()
+    bad[w] = -1
+    with pytest.raises(ValueError):
+        R.lola_chunk_run(q, k, v, x.W, 8, 6, 8, replay=bad)
