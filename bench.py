@@ -46,6 +46,9 @@ def parse_args():
     p.add_argument("--decode-batch", type=int, default=None, help="batch of the decode workload (profiling)")
     p.add_argument("--read-mask", type=int, default=0, choices=[0, 1, 2, 3],
                    help="read mask of the layer (1: state hidden, 2: cache hidden, 3: both)")
+    p.add_argument("--alloc", default="token", choices=["token", "chunk"],
+                   help="allocation granularity of the prefill (chunk: the chunk-granular variant; "
+                        "no decode line, the decode step is per token)")
     return p.parse_args()
 
 
@@ -209,6 +212,14 @@ def select_flops_per_step(D, dv, lam):
     return 2 * D * dv + 2 * D * dv + 2 * lam * D + 2 * lam * dv + 4 * (lam + 1) * dv
 
 
+def chunk_select_flops_per_chunk(D, dv, lam, C):
+    """Chunk-granular allocation per chunk (steady state, lambda + C candidates, C written):
+    every candidate's H^T phi (2 D dv) and s^T phi (2 D) and its SRE (4 dv), then the
+    written keys' rank-1 terms (2 D dv + D each)."""
+    P = lam + C
+    return 2 * P * D * dv + 2 * P * D + 4 * P * dv + C * (2 * D * dv + D)
+
+
 def output_flops_per_token(dk, dv, D, eta, lam):
     """Co-normalised read per query: softmax branch over eta + lambda exact keys
     (2 (eta + lambda)(dk + dv)) and the linear read H^T phi(q), phi(q)^T s (2 D dv + 2 D)."""
@@ -277,7 +288,7 @@ def run_prefill(L, R, args, pk):
     Q, K, V = (dev_tensor(getattr(x, a), w.dtype, dev) for a in "qkv")
     W = torch.from_numpy(x.W).to(dev)
     lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev,
-                 read_mask=args.read_mask)
+                 read_mask=args.read_mask, alloc=L.LOLA_ALLOC_CHUNK if args.alloc == "chunk" else L.LOLA_ALLOC_TOKEN)
     ws = lay.workspace_for(w.n)
     Y = torch.empty_like(V)
     wpos = torch.empty(w.B, w.Hh, w.n, dtype=torch.int32, device=dev)
@@ -301,10 +312,15 @@ def run_prefill(L, R, args, pk):
     heads = w.B * w.Hh
     sel = kt.get("select")
     if sel:
-        fl = heads * w.n * select_flops_per_step(w.D, w.d, w.lam)
+        if args.alloc == "chunk":   # chunk starts that score (the first eta / C only fill the window)
+            fl = heads * max(0, w.n // w.chunk - w.eta // w.chunk) * chunk_select_flops_per_chunk(w.D, w.d, w.lam,
+                                                                                                  w.chunk)
+        else:
+            fl = heads * w.n * select_flops_per_step(w.D, w.d, w.lam)
         ach = fl / (sel["avg_ms"] / 1e3) / 1e12
         res["roofline"] = {"kernel": "select", "bound": "alu", "achieved": ach, "peak": pk["fp32_tflops"],
-                           "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"], "traffic": traffic("select"),
+                           "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"],
+                           "traffic": traffic("select") if args.alloc == "token" else None,
                            "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
     out = kt.get("output")
     if out:
@@ -506,9 +522,9 @@ def main():
         return 0
     pre = run_prefill(L, R, args, pk)
     w = pre["workload"]
-    dec = None if args.no_decode else run_decode(L, R, args, pk)
+    dec = None if args.no_decode or args.alloc == "chunk" else run_decode(L, R, args, pk)
     cpu = None
-    if R.rank == 0 and not args.no_cpu:
+    if R.rank == 0 and not args.no_cpu and args.alloc == "token":   # (the C oracle is per token)
         cpu = cpu_baseline(pre["x"], w, args.read_mask)
     if R.rank == 0:
         launches = pre["launches"] * 1
@@ -518,7 +534,7 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta,
                        "lambda": w.lam, "chunk": w.chunk, "l2": "inputs 402 MB > 129 MB L2, no flush",
-                       "parallelism": f"replicas x{R.world}", "read_mask": args.read_mask},
+                       "parallelism": f"replicas x{R.world}", "read_mask": args.read_mask, "alloc": args.alloc},
             "roofline": pre.get("roofline"), "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
             "clocks": pre["clocks"], "kernels": pre["kernels"], "peaks": {k: pk[k] for k in
                                                                         ("hbm_gbs", "bf16_tflops", "fp32_tflops",

@@ -58,7 +58,8 @@ struct CkPlan {
         const size_t P = (size_t)lam + C;
         H = 0;
         tile = H + 4ull * D * DV;
-        const size_t tile_b = 4ull * (D * kTS > kG * (D + DV) ? D * kTS : kG * (D + DV));
+        // scoring: phi transposed [D][kTS] + v [kG][DV]; writing: phi [kG][D] + v [kG][DV]
+        const size_t tile_b = 4ull * (D * kTS > kG * D ? D * kTS : kG * D) + 4ull * kG * DV;
         s = a16c(tile + tile_b);
         cpos = a16c(s + 4ull * D);
         cand = a16c(cpos + 4ull * (lam > 0 ? lam : 1));
@@ -68,6 +69,58 @@ struct CkPlan {
         total = a16c(klist + 4ull * (lam > 0 ? lam : 1));
     }
 };
+
+// kG rows of phi (float32, D wide) and of v (input type, DV wide, widened exactly) for the
+// keys at positions pos(j), j < cnt (zero rows beyond), all loads issued before any store.
+// phi moves as float4 into phi_at(j, r) (four consecutive r); with JM the 32 lanes of a
+// warp take 32 consecutive keys (conflict-free stores into a transposed tile), else 32
+// consecutive float4 of one row.  v moves 16 bytes at a time into vt[j * DV + q].
+template <int D, int DV, typename T, bool JM, typename Pos, typename PhiAt>
+__device__ __forceinline__ void stage_rows(const float* phiK, const T* Vin, int cnt, Pos pos, PhiAt phi_at, float* vt,
+                                           int tid) {
+    constexpr int F4 = kG * D / 4 / kCkThreads;           // float4 of phi per thread
+    constexpr int VE = 16 / (int)sizeof(T);               // values per 16-byte chunk of v
+    constexpr int V4 = kG * DV / VE / kCkThreads;         // chunks of v per thread
+    static_assert(F4 * 4 * kCkThreads == kG * D && V4 * VE * kCkThreads == kG * DV, "staging split");
+    float4 f[F4];
+    uint4 vr[V4];
+#pragma unroll
+    for (int u = 0; u < F4; ++u) {
+        const int i = tid + u * kCkThreads;
+        const int j = JM ? i % kG : i / (D / 4), r4 = JM ? i / kG : i % (D / 4);
+        f[u] = j < cnt ? *reinterpret_cast<const float4*>(phiK + (int64_t)pos(j) * D + 4 * r4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < V4; ++u) {
+        const int i = tid + u * kCkThreads, j = i / (DV / VE), c = i % (DV / VE);
+        vr[u] = j < cnt ? *reinterpret_cast<const uint4*>(Vin + (int64_t)pos(j) * DV + VE * c) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < F4; ++u) {
+        const int i = tid + u * kCkThreads;
+        const int j = JM ? i % kG : i / (D / 4), r4 = JM ? i / kG : i % (D / 4);
+        phi_at(j, 4 * r4 + 0) = f[u].x;
+        phi_at(j, 4 * r4 + 1) = f[u].y;
+        phi_at(j, 4 * r4 + 2) = f[u].z;
+        phi_at(j, 4 * r4 + 3) = f[u].w;
+    }
+#pragma unroll
+    for (int u = 0; u < V4; ++u) {
+        const int i = tid + u * kCkThreads, j = i / (DV / VE), c = i % (DV / VE);
+        float* dst = vt + j * DV + VE * c;
+        if constexpr (sizeof(T) == 4) {
+            *reinterpret_cast<float4*>(dst) = make_float4(__uint_as_float(vr[u].x), __uint_as_float(vr[u].y),
+                                                          __uint_as_float(vr[u].z), __uint_as_float(vr[u].w));
+        } else {
+            const uint32_t w4[4] = {vr[u].x, vr[u].y, vr[u].z, vr[u].w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                dst[2 * k] = chain::bf16_lo(w4[k]);
+                dst[2 * k + 1] = chain::bf16_hi(w4[k]);
+            }
+        }
+    }
+}
 
 template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const ChunkArgs a) {
@@ -131,12 +184,10 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         }
 
         // ---- SRE^2 of every candidate against the current (H, s), kG at a time ----
+        float* vts = tile + D * kTS;   // [kG][DV] the group's values (float32)
         for (int g0 = 0; g0 < P; g0 += kG) {
-            for (int i = tid; i < kG * D; i += kCkThreads) {
-                const int j = i / D, r = i % D;
-                const int p = g0 + j < P ? cand[g0 + j] : -1;
-                tile[r * kTS + j] = p >= 0 ? phiK[(int64_t)p * D + r] : 0.f;
-            }
+            stage_rows<D, DV, T, true>(phiK, Vin, min(kG, P - g0), [&](int j) { return cand[g0 + j]; },
+                                 [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
             __syncthreads();
             float acc[4][HC];
 #pragma unroll
@@ -173,7 +224,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
                 if (p >= 0) {
 #pragma unroll
                     for (int q = 0; q < HC; ++q) {
-                        const float vq = IO<T>::ld(Vin, (int64_t)p * DV + lane * HC + q);
+                        const float vq = vts[(4 * warp + i) * DV + lane * HC + q];
                         const float d = fmaf(-z, vq, acc[i][q]);   // (N - z v), SRE^2 = |.|^2 / z^2
                         dd = fmaf(d, d, dd);
                         vv = fmaf(vq, vq, vv);
@@ -207,17 +258,11 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         chain::h_load<D, DV>(hreg, Hs, warp, lane);
         float sreg = tid < D ? ss[tid] : 0.f;
         float* tphi = tile;              // [kG][D]
-        float* tv = tile + kG * D;       // [kG][DV]
+        float* tv = tile + D * kTS;      // [kG][DV]
         for (int w0 = 0; w0 < nwr; w0 += kG) {
             const int cnt = min(kG, nwr - w0);
-            for (int i = tid; i < cnt * D; i += kCkThreads) {
-                const int j = i / D, r = i % D;
-                tphi[j * D + r] = phiK[(int64_t)wlist[w0 + j] * D + r];
-            }
-            for (int i = tid; i < cnt * DV; i += kCkThreads) {
-                const int j = i / DV, q = i % DV;
-                tv[j * DV + q] = IO<T>::ld(Vin, (int64_t)wlist[w0 + j] * DV + q);
-            }
+            stage_rows<D, DV, T, false>(phiK, Vin, cnt, [&](int j) { return wlist[w0 + j]; },
+                                 [&](int j, int r) -> float& { return tphi[j * D + r]; }, tv, tid);
             __syncthreads();
             for (int j = 0; j < cnt; ++j) {
                 float vh[HC];
