@@ -316,6 +316,28 @@ def window_chunks_plus_linear(q, k, v, W, eta: int, C: int):
     return (wt @ v) / wt.sum(axis=1, keepdims=True)
 
 
+def sre_map(k, v, W, write_step, times):
+    """Self-recall error of every key held by the linear memory at each state time (the
+    notes' Fig. 3 diagnostic, section 4.4): out[c, j] = SRE(k_j, v_j | H_t, s_t) for
+    t = times[c], where (H_t, s_t) is the memory before step t -- the sums of phi(k) v^T and
+    phi(k) over the keys written before t (write_step[j] < t) -- and 0 for keys it does not
+    hold (still exact in the window or cache, or not yet seen)."""
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    PK = phi(k, W)
+    ws = np.asarray(write_step)
+    out = np.zeros((len(times), k.shape[0]))
+    for c, t in enumerate(times):
+        held = np.flatnonzero((ws >= 0) & (ws < t))
+        if held.size == 0:
+            continue
+        H = PK[held].T @ v[held]
+        s = PK[held].sum(axis=0)
+        for j in held:
+            out[c, j] = math.sqrt(sre_sq(H, s, PK[j], v[j]))
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Closed forms the method reduces to (used as pins)
 # ---------------------------------------------------------------------------

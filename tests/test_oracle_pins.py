@@ -454,3 +454,35 @@ def test_chunk_mode_replay_of_own_and_of_a_swapped_log():
     bad[w] = -1
     with pytest.raises(ValueError):
         R.lola_chunk_run(q, k, v, x.W, 8, 6, 8, replay=bad)
+
+
+# ---------------------------------------------------------------------------
+# SRE diagnostics (Fig. 3)
+# ---------------------------------------------------------------------------
+
+def test_sre_map_against_the_running_memory():
+    """At every chunk start the map's memory is the run's (H, s) before that step: the
+    per-token run replayed up to t gives the same SREs; zero columns for keys not held."""
+    x = synth.gauss_inputs(1, 1, 48, 8, 8, "f32", seed=95, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 4, 3)
+    times = [0, 8, 16, 24, 32, 40, 48]
+    m = R.sre_map(k, v, x.W, o["write_step"], times)
+    assert (m[0] == 0).all()
+    PK = R.phi(k, x.W)
+    for c, t in enumerate(times):
+        held = (o["write_step"] >= 0) & (o["write_step"] < t)
+        assert (m[c][~held] == 0).all()
+        if t == 0:
+            continue
+        pre = R.lola_run(q[:t], k[:t], v[:t], x.W, 4, 3)   # the memory after step t - 1
+        for j in np.flatnonzero(held):
+            assert m[c, j] == pytest.approx(math.sqrt(R.sre_sq(pre["H"], pre["s"], PK[j], v[j])), rel=1e-12)
+
+
+def test_sre_map_single_written_key_is_zero():
+    """A memory holding one key recalls it exactly (section 2.3): SRE 0 at the next time."""
+    x = synth.gauss_inputs(1, 1, 4, 8, 8, "f32", seed=96, dv=6)
+    k, v = x.widened("k")[0, 0], x.widened("v")[0, 0]
+    m = R.sre_map(k, v, x.W, np.array([2, -1, -1, -1]), [2, 3])
+    assert m[0, 0] == 0.0 and m[1, 0] == pytest.approx(0.0, abs=1e-12) and (m[:, 1:] == 0).all()
