@@ -242,6 +242,20 @@ int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches);
 /* Static name of a kernel id ("" if out of range). */
 const char* lola_kernel_name(int32_t id);
 
+/* ---- SRE diagnostics ---------------------------------------------------------------------
+ * Section 4.4 (the notes' Fig. 3): the self-recall error of every key the linear memory
+ * holds, over state time.  Reads the snapshots that the last lola_prefill(cfg, n, ...) left
+ * in `workspace` (same cfg and n, nothing written to it since): snapshot c is the memory
+ * (H, s) before step c * P, P = max(chunk, 128), c < nck = ceil(n / P).
+ *   V    device io [B, Hh, n, d_v]: the values given to that prefill
+ *   out  device float32 [B, Hh, nck, n]: out[b, h, c, j] = SRE(k_j, v_j | H, s of snapshot
+ *        c) = || H^T phi(k_j) / phi(k_j)^T s - v_j || if key j was written before step c * P,
+ *        else 0 (the key is still exact, or not seen yet).  On the bf16 tensor-core path the
+ *        snapshots of H are bf16 (rounded to nearest even), so the map carries that rounding.
+ * Stream-ordered; validation errors return before anything is enqueued. */
+int32_t lola_sre_map(const lola_config* cfg, int32_t n, const void* V, const void* workspace,
+                     size_t workspace_bytes, float* out, void* stream);
+
 /* ---- self-test of the bounded waits -----------------------------------------------------
  * No counterpart in the LoLA paper.  Every wait of the library's kernels on an mbarrier (the
  * decode step's burst, the output pass's MMA groups) gives up after a time limit, records a

@@ -34,7 +34,7 @@ LOLA_ALLOC_CHUNK = 1
 EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_check_config",
            "lola_state_layout_of", "lola_state_bytes", "lola_prefill_workspace_bytes", "lola_state_init",
            "lola_prefill", "lola_decode_step", "lola_read_status", "lola_kernel_timing", "lola_kernel_time",
-           "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait")
+           "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait", "lola_sre_map")
 # size of the fixed scratch array behind lola_prefill_noalloc (include/lola.h)
 LOLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNELS = ("state_init", "phi", "select", "output", "decode")
@@ -88,6 +88,7 @@ def _load():
         "lola_kernel_name": ([ctypes.c_int32], ctypes.c_char_p),
         "lola_prefill_noalloc": ([C, ctypes.c_int32, P, P, P, P, ctypes.c_int64, P, P, P, P], ctypes.c_int32),
         "lola_selftest_bounded_wait": ([ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), P], ctypes.c_int32),
+        "lola_sre_map": ([C, ctypes.c_int32, P, P, ctypes.c_size_t, P, P], ctypes.c_int32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -200,6 +201,13 @@ def lola_kernel_time(kernel) -> tuple[float, int]:
 
 def lola_kernel_name(kid: int) -> str:
     return _lib.lola_kernel_name(kid).decode()
+
+
+def lola_sre_map(cfg: lola_config, n: int, V, workspace, out, stream=None) -> None:
+    """SRE of every key held by each snapshot of the last prefill in ``workspace`` (section
+    4.4): ``out`` float32 [B, Hh, nck, n]."""
+    _check(_lib.lola_sre_map(ctypes.byref(cfg), n, _ptr(V), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                             _ptr(out), _stream(stream)), "lola_sre_map")
 
 
 def lola_selftest_bounded_wait(limit_ns: int, stream=None):

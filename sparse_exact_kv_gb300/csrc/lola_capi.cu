@@ -405,6 +405,21 @@ const char* lola_kernel_name(int32_t id) {
     return (id >= 0 && id < LOLA_KERNEL_COUNT) ? names[id] : "";
 }
 
+int32_t lola_sre_map(const lola_config* cfg, int32_t n, const void* V, const void* workspace, size_t workspace_bytes,
+                     float* out, void* stream) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (n < 1 || !V || !workspace || !out) return LOLA_ERR_INVALID_ARG;
+    if (!aligned16(V) || !aligned16(workspace) || !aligned16(out)) return LOLA_ERR_INVALID_ARG;
+    if ((int64_t)n * d.BH * d.D > ((int64_t)1 << 40)) return LOLA_ERR_UNSUPPORTED;
+    const Workspace ws = carve_workspace(d, n, const_cast<void*>(workspace));
+    if (workspace_bytes < ws.bytes) return LOLA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = launch_sre_map(d, n, ws, V, out, st);
+    return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "sre map");
+}
+
 int32_t lola_selftest_bounded_wait(int64_t limit_ns, int64_t* host_elapsed_ns, void* stream) {
     if (limit_ns < 1 || limit_ns > 1000000000ll) return LOLA_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;

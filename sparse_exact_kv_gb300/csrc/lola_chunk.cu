@@ -122,6 +122,59 @@ __device__ __forceinline__ void stage_rows(const float* phiK, const T* Vin, int 
     }
 }
 
+// SRE^2 of the kG keys staged in the tile (phi transposed [D][kTS], values [kG][DV]) against
+// (H, s) in shared memory, for keys j < nvalid: warp w takes keys 4w .. 4w + 3, lane l the
+// value columns l*HC ..; N = H^T phi accumulated over the D rows, z = s^T phi, then
+// SRE^2 = |N - z v|^2 / z^2, or |v|^2 when z = 0 (the empty memory predicts 0).  Lane 0 of
+// each warp hands (j, SRE^2) to emit.
+template <int D, int DV, typename Emit>
+__device__ __forceinline__ void tile_sre2(const float* Hs, const float* ss, const float* tile, const float* vts,
+                                          int nvalid, int warp, int lane, Emit emit) {
+    constexpr int HC = DV / kWarp;
+    float acc[4][HC];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int q = 0; q < HC; ++q) acc[i][q] = 0.f;
+#pragma unroll 4
+    for (int r = 0; r < D; ++r) {
+        float h[HC];
+        chain::h_vec_load<HC>(Hs + r * DV + lane * HC, h);
+        const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
+        const float fi[4] = {f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int q = 0; q < HC; ++q) acc[i][q] = fmaf(fi[i], h[q], acc[i][q]);
+    }
+    // z = s^T phi(k): lane l takes rows l, l + 32, ...
+    float z4[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int r = lane; r < D; r += kWarp) {
+        const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
+        const float sr = ss[r];
+        z4[0] = fmaf(f.x, sr, z4[0]);
+        z4[1] = fmaf(f.y, sr, z4[1]);
+        z4[2] = fmaf(f.z, sr, z4[2]);
+        z4[3] = fmaf(f.w, sr, z4[3]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = 4 * warp + i;
+        const float z = warp_sum(z4[i]);
+        float dd = 0.f, vv = 0.f;
+#pragma unroll
+        for (int q = 0; q < HC; ++q) {
+            const float vq = vts[j * DV + lane * HC + q];
+            const float d = fmaf(-z, vq, acc[i][q]);
+            dd = fmaf(d, d, dd);
+            vv = fmaf(vq, vq, vv);
+        }
+        dd = warp_sum(dd);
+        vv = warp_sum(vv);
+        if (lane == 0 && j < nvalid) emit(j, z == 0.f ? vv : dd / (z * z));
+    }
+}
+
 template <int D, int DV, typename T>
 __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const ChunkArgs a) {
     using S = Shape<D, DV>;
@@ -186,57 +239,13 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         // ---- SRE^2 of every candidate against the current (H, s), kG at a time ----
         float* vts = tile + D * kTS;   // [kG][DV] the group's values (float32)
         for (int g0 = 0; g0 < P; g0 += kG) {
-            stage_rows<D, DV, T, true>(phiK, Vin, min(kG, P - g0), [&](int j) { return cand[g0 + j]; },
-                                 [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
+            const int cnt = min(kG, P - g0);
+            stage_rows<D, DV, T, true>(phiK, Vin, cnt, [&](int j) { return cand[g0 + j]; },
+                                       [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
             __syncthreads();
-            float acc[4][HC];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int q = 0; q < HC; ++q) acc[i][q] = 0.f;
-#pragma unroll 4
-            for (int r = 0; r < D; ++r) {
-                float h[HC];
-                chain::h_vec_load<HC>(Hs + r * DV + lane * HC, h);
-                const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
-                const float fi[4] = {f.x, f.y, f.z, f.w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-#pragma unroll
-                    for (int q = 0; q < HC; ++q) acc[i][q] = fmaf(fi[i], h[q], acc[i][q]);
-            }
-            // z = s^T phi(k): lane l takes rows l, l + 32, ...
-            float z4[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int r = lane; r < D; r += kWarp) {
-                const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
-                const float sr = ss[r];
-                z4[0] = fmaf(f.x, sr, z4[0]);
-                z4[1] = fmaf(f.y, sr, z4[1]);
-                z4[2] = fmaf(f.z, sr, z4[2]);
-                z4[3] = fmaf(f.w, sr, z4[3]);
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int j = g0 + 4 * warp + i;
-                const int p = j < P ? cand[j] : -1;
-                const float z = warp_sum(z4[i]);
-                float dd = 0.f, vv = 0.f;
-                if (p >= 0) {
-#pragma unroll
-                    for (int q = 0; q < HC; ++q) {
-                        const float vq = vts[(4 * warp + i) * DV + lane * HC + q];
-                        const float d = fmaf(-z, vq, acc[i][q]);   // (N - z v), SRE^2 = |.|^2 / z^2
-                        dd = fmaf(d, d, dd);
-                        vv = fmaf(vq, vq, vv);
-                    }
-                }
-                dd = warp_sum(dd);
-                vv = warp_sum(vv);
-                if (lane == 0 && p >= 0) {
-                    const float sre2 = z == 0.f ? vv : dd / (z * z);   // empty memory: ||v||^2
-                    keys[j] = ((unsigned long long)__float_as_uint(sre2) << 32) | (unsigned)p;
-                }
-            }
+            tile_sre2<D, DV>(Hs, ss, tile, vts, cnt, warp, lane, [&](int j, float sre2) {
+                keys[g0 + j] = ((unsigned long long)__float_as_uint(sre2) << 32) | (unsigned)cand[g0 + j];
+            });
             __syncthreads();   // the tile is restaged
         }
 
@@ -359,7 +368,87 @@ cudaError_t launch_chunk_t(const Dims& d, int n, const Workspace& ws, const void
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------------
+// SRE map (the notes' Fig. 3 diagnostic, section 4.4): CTA (c, bh) takes the memory the
+// prefill snapshotted before step c * snap and the SRE of every key it holds (written
+// before that step); the keys it does not hold read 0.  Same scoring routine as above.
+// ---------------------------------------------------------------------------------
+struct SreArgs {
+    int n, snap, nck;
+    const float* phiK;          // [BH][n][D]
+    const void* V;              // io [BH][n][DV]
+    const int32_t* wstep;       // [BH][n]
+    const float* snapH;         // [BH][nck][D*DV] float32, or
+    const __nv_bfloat16* snapHb;
+    const float* snapS;         // [BH][nck][D]
+    float* out;                 // [BH][nck][n]
+};
+
+template <int D, int DV, typename T>
+__global__ void __launch_bounds__(kCkThreads, 1) sre_map_kernel(const SreArgs a) {
+    extern __shared__ __align__(16) unsigned char sm[];
+    float* Hs = reinterpret_cast<float*>(sm);                           // [D][DV]
+    float* tile = Hs + D * DV;                                           // [D][kTS]
+    float* vts = tile + D * kTS;                                         // [kG][DV]
+    float* ss = vts + kG * DV;                                           // [D]
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int c = blockIdx.x, bh = blockIdx.y;
+    const int n = a.n, tc = c * a.snap;
+    const int64_t row0 = (int64_t)bh * n, sc = (int64_t)bh * a.nck + c;
+    const float* phiK = a.phiK + row0 * D;
+    const T* Vin = static_cast<const T*>(a.V) + row0 * DV;
+    const int32_t* wst = a.wstep + row0;
+    float* out = a.out + sc * n;
+    for (int i = tid; i < D * DV; i += kCkThreads)
+        Hs[i] = a.snapHb ? __bfloat162float(a.snapHb[sc * D * DV + i]) : a.snapH[sc * D * DV + i];
+    for (int i = tid; i < D; i += kCkThreads) ss[i] = a.snapS[sc * D + i];
+    for (int j = tc + tid; j < n; j += kCkThreads) out[j] = 0.f;   // not seen before step tc
+    for (int j0 = 0; j0 < tc; j0 += kG) {
+        const int cnt = min(kG, tc - j0);
+        __syncthreads();   // H and s staged; the previous tile is consumed
+        stage_rows<D, DV, T, true>(phiK, Vin, cnt, [&](int j) { return j0 + j; },
+                                   [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
+        __syncthreads();
+        tile_sre2<D, DV>(Hs, ss, tile, vts, cnt, warp, lane, [&](int j, float sre2) {
+            const int w = wst[j0 + j];
+            out[j0 + j] = (w >= 0 && w < tc) ? sqrtf(sre2) : 0.f;   // held by the memory, else 0
+        });
+    }
+}
+
+template <int D, int DV, typename T>
+cudaError_t launch_sre_map_t(const Dims& d, int n, const Workspace& ws, const void* V, float* out, cudaStream_t st) {
+    SreArgs a;
+    a.n = n;
+    a.snap = ws.snap_interval;
+    a.nck = ws.nck;
+    a.phiK = ws.phiK;
+    a.V = V;
+    a.wstep = ws.wstep;
+    a.snapH = ws.snapH;
+    a.snapHb = ws.snapHb;
+    a.snapS = ws.snapS;
+    a.out = out;
+    const size_t smem = sizeof(float) * ((size_t)D * DV + D * kTS + kG * DV + D);
+    auto kern = sre_map_kernel<D, DV, T>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(ws.nck, d.BH), kCkThreads, smem, st>>>(a);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t launch_sre_map(const Dims& d, int n, const Workspace& ws, const void* V, float* out, cudaStream_t st) {
+    const bool bf = d.dtype == LOLA_BF16;
+    if (d.D == 128 && d.dv == 128)
+        return bf ? launch_sre_map_t<128, 128, __nv_bfloat16>(d, n, ws, V, out, st)
+                  : launch_sre_map_t<128, 128, float>(d, n, ws, V, out, st);
+    if (d.D == 64 && d.dv == 64)
+        return bf ? launch_sre_map_t<64, 64, __nv_bfloat16>(d, n, ws, V, out, st)
+                  : launch_sre_map_t<64, 64, float>(d, n, ws, V, out, st);
+    return cudaErrorInvalidValue;
+}
 
 bool chunk_mode_fits(const Dims& d) {
     const size_t smem = d.D == 128 ? CkPlan<128, 128>(d.lam, d.chunk).total : CkPlan<64, 64>(d.lam, d.chunk).total;

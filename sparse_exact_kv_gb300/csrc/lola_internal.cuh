@@ -220,6 +220,8 @@ cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void*
 bool chunk_mode_fits(const Dims& d);
 cudaError_t launch_chunk_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
                                 char* state, const Layout& L, cudaStream_t st);
+// the SRE map of the keys held by each snapshot of a prefill's workspace
+cudaError_t launch_sre_map(const Dims& d, int n, const Workspace& ws, const void* V, float* out, cudaStream_t st);
 cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                           const void* V, void* Y, cudaStream_t st);
 bool output_tc_supported(const Dims& d);

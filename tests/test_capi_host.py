@@ -160,3 +160,13 @@ def test_chunk_alloc_validation(lib):
     P = ctypes.c_void_p
     st = lib._lib.lola_decode_step(ctypes.byref(ok), P(256), P(256), 0, P(256), P(256), P(256), P(256), None, None)
     assert st == lib.LOLA_ERR_UNSUPPORTED
+
+
+def test_sre_map_validation(lib):
+    """Null pointers and a workspace smaller than the prefill's are refused before any launch."""
+    cfg = lib.make_config(1, 1, 64, 64, 64, 4, 4, 16, "f32")
+    so = lib._lib
+    P = ctypes.c_void_p
+    assert so.lola_sre_map(ctypes.byref(cfg), 16, None, P(256), 1 << 30, P(256), None) == lib.LOLA_ERR_INVALID_ARG
+    assert so.lola_sre_map(ctypes.byref(cfg), 0, P(256), P(256), 1 << 30, P(256), None) == lib.LOLA_ERR_INVALID_ARG
+    assert so.lola_sre_map(ctypes.byref(cfg), 16, P(256), P(256), 16, P(256), None) == lib.LOLA_ERR_WORKSPACE

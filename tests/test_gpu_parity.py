@@ -257,6 +257,38 @@ def test_chunk_alloc_prefill_matches_oracle(L, dtype, d, eta, lam, chunk):
                         torch.from_numpy(x.W).to(dev))
 
 
+@pytest.mark.parametrize("dtype,d,alloc", [("f32", 64, 0), ("bf16", 128, 0), ("f32", 64, 1)])
+def test_sre_map_matches_oracle(L, dtype, d, alloc):
+    """The SRE map (section 4.4, Fig. 3) from a prefill's snapshots equals the oracle's map
+    of the same write log: SRE of the keys each snapshot's memory holds, 0 elsewhere."""
+    from oracle import lola_ref as R
+    B, Hh, n, eta, lam, chunk = 1, 2, 400, 16, 20, 16
+    x = synth.gauss_inputs(B, Hh, n, d, d, dtype, seed=120 + d)
+    Y, wlog, lay = run_prefill(L, x, eta, lam, chunk, alloc=alloc)
+    snap = max(chunk, 128)
+    nck = (n + snap - 1) // snap
+    V = to_dev(x.v, "cuda", dtype)
+    out = torch.full((B, Hh, nck, n), float("nan"), dtype=torch.float32, device="cuda")
+    L.lola_sre_map(lay.cfg, n, V, lay.workspace, out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy().astype(np.float64)
+    k, v = x.widened("k"), x.widened("v")
+    for h in range(Hh):
+        if alloc:
+            ws = wlog[0, h]                                   # per key already
+        else:
+            ws = np.full(n, -1, np.int64)                     # per step -> per key
+            for t, p in enumerate(wlog[0, h]):
+                if p >= 0:
+                    ws[p] = t
+        times = [c * snap for c in range(nck)]
+        ref = R.sre_map(k[0, h], v[0, h], x.W, ws, times)
+        held = (ws[None, :] >= 0) & (ws[None, :] < np.array(times)[:, None])
+        assert held.any() and (got[0, h][~held] == 0).all(), "a key the memory does not hold has a nonzero SRE"
+        tol = dict(rtol=2e-4, atol=2e-4) if dtype == "f32" else dict(rtol=3e-2, atol=3e-2)
+        np.testing.assert_allclose(got[0, h], ref, **tol)
+
+
 def test_bounded_wait_gives_up_and_reports(L):
     """The kernels' mbarrier wait, run on a barrier that nothing completes, gives up after its
     limit and reports it; the context stays usable (a prefill runs right after)."""
