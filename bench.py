@@ -46,6 +46,8 @@ def parse_args():
     p.add_argument("--decode-batch", type=int, default=None, help="batch of the decode workload (profiling)")
     p.add_argument("--read-mask", type=int, default=0, choices=[0, 1, 2, 3],
                    help="read mask of the layer (1: state hidden, 2: cache hidden, 3: both)")
+    p.add_argument("--sre-map", action="store_true",
+                   help="also time lola_sre_map over the prefill's snapshots (reported under sre_map)")
     p.add_argument("--alloc", default="token", choices=["token", "chunk"],
                    help="allocation granularity of the prefill (chunk: the chunk-granular variant; "
                         "no decode line, the decode step is per token)")
@@ -267,6 +269,22 @@ def kernel_times(L, names):
     return out
 
 
+def sre_map_timing(L, lay, w, V, ws, stream, pk, reps=5):
+    """lola_sre_map over the snapshots of the last prefill in ws (a diagnostic, section 4.4):
+    device time per call and its FP32 rate on the algorithmic flops (every snapshot c scores
+    the c * P keys before it: 2 D d_v + 2 D + 4 d_v each)."""
+    import torch
+    P = max(w.chunk, 128)
+    nck = (w.n + P - 1) // P
+    out = torch.empty(w.B, w.Hh, nck, w.n, dtype=torch.float32, device=V.device)
+    L.lola_sre_map(lay.cfg, w.n, V, ws, out, stream)
+    ms = time_loop(lambda: L.lola_sre_map(lay.cfg, w.n, V, ws, out, stream), reps, stream) / reps
+    keys = sum(c * P for c in range(nck))
+    fl = w.B * w.Hh * keys * (2 * w.D * w.d + 2 * w.D + 4 * w.d)
+    tf = fl / (ms / 1e3) / 1e12
+    return {"ms": ms, "achieved_tflops": tf, "frac_of_fp32_peak": tf / pk["fp32_tflops"], "snapshots": nck}
+
+
 def traced_kernel_times(L, R, step, steps, stream, names):
     """Per-kernel device times over `steps` more steps with the library's launch tracing on
     (an event pair around every launch).  The timed loop runs without it, so the events do
@@ -305,10 +323,11 @@ def run_prefill(L, R, args, pk):
         ms = time_loop(step, args.steps, stream)
         R.barrier()
     kt = traced_kernel_times(L, R, step, args.steps, stream, ["state_init", "phi", "select", "output"])
+    sre = sre_map_timing(L, lay, w, V, ws, stream, pk) if args.sre_map else None
     ms = R.max(ms) / args.steps
     tokens = w.B * w.n
     res = {"workload": w, "ms": ms, "value": R.world * tokens / (ms / 1e3), "kernels": kt, "clocks": clk.summary(),
-           "launches": sum(v["launches"] for v in kt.values())}
+           "launches": sum(v["launches"] for v in kt.values()), "sre_map": sre}
     heads = w.B * w.Hh
     sel = kt.get("select")
     if sel:
@@ -536,7 +555,9 @@ def main():
                        "lambda": w.lam, "chunk": w.chunk, "l2": "inputs 402 MB > 129 MB L2, no flush",
                        "parallelism": f"replicas x{R.world}", "read_mask": args.read_mask, "alloc": args.alloc},
             "roofline": pre.get("roofline"), "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
-            "clocks": pre["clocks"], "kernels": pre["kernels"], "peaks": {k: pk[k] for k in
+            "clocks": pre["clocks"], "kernels": pre["kernels"],
+            **({"sre_map": pre["sre_map"]} if pre.get("sre_map") else {}),
+            "peaks": {k: pk[k] for k in
                                                                         ("hbm_gbs", "bf16_tflops", "fp32_tflops",
                                                                          "source")},
             "decode": dec,
