@@ -164,12 +164,12 @@ class Clocks:
 CSRC = os.path.join(ROOT, "sparse_exact_kv_gb300", "csrc")
 NCU_TRAFFIC = {
     # w2 prefill (4 x 32 heads, n = 4096): mean of 3 select launches
-    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "0472a8cba8bf4a00",
-               "bytes_per_launch": 410079403 + 132202923},
+    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "8ef752573e82a0a9",
+               "bytes_per_launch": 409638656 + 132049067},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
-    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "f549833f12b9d616",
-               "bytes_per_launch": 2 * (206886963 + 56314061)},
+    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "850fe64c2562ac87",
+               "bytes_per_launch": 2 * (206851584 + 56466483)},
 }
 
 
