@@ -112,3 +112,33 @@ def test_w4_decode_full_sampled_heads(L):
                            to_f64(ys).reshape(steps, BH, w.d).transpose(1, 0, 2)], axis=1)
     check_outputs(Yall[heads][:, w.n:], rep["Y"][:, w.n:], "bf16", what="decode outputs")
     check_outputs(Yall[heads][:, :w.n], rep["Y"][:, :w.n], "bf16", what="prefix outputs")
+
+
+def _chunk_parity(L, name, heads):
+    """Chunk-granular allocation at a workload's full size: the GPU runs every head; the float64
+    chunk oracle replays the GPU's per-key log on the sampled heads."""
+    from oracle import lola_ref as R
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w)
+    Y, wlog, lay = run_prefill(L, x, w.eta, w.lam, w.chunk, alloc=L.LOLA_ALLOC_CHUNK)
+    BH = w.B * w.Hh
+    q, k, v = (x.widened(a).reshape(BH, w.n, -1) for a in "qkv")
+    wl = wlog.reshape(BH, w.n)
+    for h in heads:
+        ref = R.lola_chunk_run(q[h], k[h], v[h], x.W, w.eta, w.lam, w.chunk, replay=wl[h])
+        assert ref["max_gap"] < GAP, f"head {h}: a chunk decision {ref['max_gap']:.3e} away from the best"
+        check_outputs(Y.reshape(BH, w.n, w.d)[h], ref["Y"], "bf16", what=f"{name} head {h}")
+    st, words = L.lola_read_status(lay.cfg, lay.state)
+    assert st == 0, words
+
+
+def test_w2_chunk_allocation_sampled_heads(L):
+    """w2 (4 x 32 heads, n = 4096, eta = lambda = C = 64) with chunk-granular allocation: the
+    GPU runs all 128 heads; the chunk oracle replays heads 0, 77 and 127."""
+    _chunk_parity(L, "w2_bf16_b4h32_n4096", heads=[0, 77, 127])
+
+
+def test_w3_chunk_allocation_sampled_heads(L):
+    """w3 (32 heads, n = 16384, eta = lambda = 256, C = 128: window = two chunks) with
+    chunk-granular allocation and the planted needles: heads 3 and 30 replayed."""
+    _chunk_parity(L, "w3_bf16_h32_n16384_needle", heads=[3, 30])
