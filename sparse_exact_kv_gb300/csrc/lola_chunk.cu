@@ -136,7 +136,7 @@ __device__ __forceinline__ void tile_sre2(const float* Hs, const float* ss, cons
     for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int q = 0; q < HC; ++q) acc[i][q] = 0.f;
-#pragma unroll 4
+#pragma unroll 8
     for (int r = 0; r < D; ++r) {
         float h[HC];
         chain::h_vec_load<HC>(Hs + r * DV + lane * HC, h);
@@ -250,14 +250,21 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         }
 
         // ---- rank by (SRE^2, position): the lowest P - lambda are written ----
+        // (four consecutive lanes per candidate, each counting a quarter of the keys)
         const int nwr = P - lam;
-        for (int i = tid; i < P; i += kCkThreads) {
-            const unsigned long long k = keys[i];
+        for (int base = 0; base < P; base += kCkThreads / 4) {
+            const int i = base + tid / 4, part = tid % 4;
+            const unsigned long long k = i < P ? keys[i] : 0ull;
             int r = 0;
-            for (int j = 0; j < P; ++j) r += keys[j] < k ? 1 : 0;
-            const int p = (int)(k & 0xffffffffu);
-            if (r < nwr) wlist[r] = p;
-            else klist[r - nwr] = p;
+            if (i < P)
+                for (int j = part; j < P; j += 4) r += keys[j] < k ? 1 : 0;
+            r += __shfl_xor_sync(0xffffffffu, r, 1);
+            r += __shfl_xor_sync(0xffffffffu, r, 2);
+            if (i < P && part == 0) {
+                const int p = (int)(k & 0xffffffffu);
+                if (r < nwr) wlist[r] = p;
+                else klist[r - nwr] = p;
+            }
         }
         __syncthreads();
 
