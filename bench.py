@@ -59,11 +59,16 @@ def parse_args():
 # ---------------------------------------------------------------------------------------
 
 class Ranks:
+    """One process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE).  The path shards by
+    (batch, head) with no data-path exchange, so N > 1 runs N replicas: a barrier brackets the
+    timed region and the time is the maximum over ranks."""
+
     def __init__(self):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
         self.rank = int(os.environ.get("RANK", "0"))
         self.local = int(os.environ.get("LOCAL_RANK", "0"))
         self.pg = False
+        self.cpu = False
 
     def init_gpu(self):
         import torch
@@ -72,6 +77,14 @@ class Ranks:
             import torch.distributed as dist
             dist.init_process_group("nccl", device_id=torch.device("cuda", self.local))
             self.pg = True
+
+    def init_cpu(self):
+        """The same rank logic over gloo (multi-process tests without a GPU)."""
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.pg = True
+            self.cpu = True
 
     def barrier(self):
         if self.pg:
@@ -83,7 +96,7 @@ class Ranks:
             return x
         import torch
         import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device="cuda")
+        t = torch.tensor([x], dtype=torch.float64, device="cpu" if self.cpu else "cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
@@ -91,6 +104,11 @@ class Ranks:
         if self.pg:
             import torch.distributed as dist
             dist.destroy_process_group()
+
+
+def whole_job_value(world: int, units_per_rank: float, ms_max: float) -> float:
+    """Units per second over all ranks: every rank processed units_per_rank in at most ms_max."""
+    return world * units_per_rank / (ms_max / 1e3)
 
 
 # ---------------------------------------------------------------------------------------
@@ -326,7 +344,7 @@ def run_prefill(L, R, args, pk):
     sre = sre_map_timing(L, lay, w, V, ws, stream, pk) if args.sre_map else None
     ms = R.max(ms) / args.steps
     tokens = w.B * w.n
-    res = {"workload": w, "ms": ms, "value": R.world * tokens / (ms / 1e3), "kernels": kt, "clocks": clk.summary(),
+    res = {"workload": w, "ms": ms, "value": whole_job_value(R.world, tokens, ms), "kernels": kt, "clocks": clk.summary(),
            "launches": sum(v["launches"] for v in kt.values()), "sre_map": sre}
     heads = w.B * w.Hh
     sel = kt.get("select")
@@ -402,7 +420,7 @@ def run_prefill(L, R, args, pk):
         pipeline(2)
         R.barrier()
         ems = R.max(pipeline(args.steps)) / args.steps
-        res["e2e"] = {"value": R.world * tokens / (ems / 1e3), "unit": "tokens/s", "ms_per_step": ems,
+        res["e2e"] = {"value": whole_job_value(R.world, tokens, ems), "unit": "tokens/s", "ms_per_step": ems,
                       "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(),
                       "d2h_bytes_per_step": Y.numel() * Y.element_size(),
                       "overlap": "step i+1's inputs are copied while step i computes (two device buffers)"}
@@ -450,7 +468,7 @@ def run_decode(L, R, args, pk):
     kt = traced_kernel_times(L, R, step, steps, stream, ["phi", "decode"])
     ms = R.max(ms) / steps
     heads = w.B * w.Hh
-    res = {"metric": "decode tokens/s per layer", "value": R.world * w.B / (ms / 1e3), "unit": "tokens/s",
+    res = {"metric": "decode tokens/s per layer", "value": whole_job_value(R.world, w.B, ms), "unit": "tokens/s",
            "ms_per_step": ms, "steps": steps,
            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "d": w.d, "D": w.D, "eta": w.eta, "lambda": w.lam,
                       "prefix": w.n, "state_bytes": lola_state_bytes(L, lay), "read_mask": args.read_mask},

@@ -1,0 +1,66 @@
+"""Multi-process logic of the benchmark on CPU (gloo, world size 2): the path shards by
+(batch, head) with no data-path exchange, so N processes run N replicas; the timed region is
+bracketed by barriers, the time is the maximum over ranks and the value counts every rank's
+units.  The reference arm runs on rank 0 only."""
+import os
+import socket
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    R = bench.Ranks()
+    R.init_cpu()
+    R.barrier()
+    ms = R.max(10.0 + 5.0 * rank)           # rank 1 is the slower replica
+    value = bench.whole_job_value(R.world, 1000, ms)
+    R.barrier()
+    R.close()
+    q.put((rank, ms, value))
+
+
+def test_two_ranks_take_the_slowest_time_and_count_every_rank():
+    world, port = 2, _free_port()
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    procs = [ctx.Process(target=_worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(world))
+    for rank, ms, value in got:
+        assert ms == 15.0, "every rank sees the slowest rank's time"
+        assert value == pytest.approx(2 * 1000 / 0.015), "the value counts the units of both replicas"
+
+
+def test_single_process_is_its_own_world(monkeypatch):
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    R = bench.Ranks()
+    R.init_cpu()
+    assert R.world == 1 and R.rank == 0 and R.max(3.0) == 3.0
+
+
+def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
+    """Under torchrun the other ranks exit 0 at once, without work and without output."""
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1"])
+    assert bench.run_reference(bench.parse_args()) == 0
+    assert capsys.readouterr().out == ""
