@@ -15,12 +15,13 @@
 // At every chunk start c0: the snapshot for the output pass when c0 is a multiple of its
 // interval (the memory before this start's writes, as in the per-token chain); then the
 // candidates -- the cache, then the chunk leaving the window -- are scored 64 at a time
-// (warp w takes four candidates, lane l the value columns l*HC.., H rows read from shared
-// memory against the candidates' phi staged transposed), ranked by (SRE^2, position), and
+// (a 64 x d_v product of their phi, staged transposed, with H read from shared memory; each
+// warp a 16-key x d_v/4-column tile of it), ranked by (SRE^2, position), and
 // the lowest P - lambda are added to H and s in rank order.  Every written key's step is
 // recorded as c0 (the first query that reads it through the state), which is the rule the
 // output kernels apply: key j is exact for query t iff j <= t < w_j, linear iff w_j <= t.
 #include "lola_chain.cuh"
+#include "lola_tc.cuh"
 
 namespace lola {
 namespace {
@@ -32,6 +33,12 @@ constexpr int kCkWarps = kCkThreads / kWarp;
 constexpr int kG = 64;                 // candidates per scoring group, 4 per warp
 static_assert(kG == 4 * kCkWarps, "four candidates per warp");
 constexpr int kTS = kG + 4;            // row stride of the transposed phi tile (floats)
+// tensor-core scoring (bfloat16 io, D = d_v = 128): candidates per MMA group (M), TMEM
+// columns (the fp32 N tile), the halves of the split operands, the completion wait limit
+constexpr int kGT = 128;
+constexpr int kTmemCols = 128;
+constexpr uint32_t kAhalf = 2u * kGT * 128, kBhalf = 2u * 128 * 128;
+constexpr uint64_t kCkWaitNs = 1000000000ull;
 
 struct ChunkArgs {
     int n, eta, lam, C, nwc, snap, nck;
@@ -50,25 +57,56 @@ struct ChunkArgs {
 
 __host__ __device__ constexpr size_t a16c(size_t x) { return (x + 15) / 16 * 16; }
 
-// shared-memory plan (bytes), from the runtime lambda and C
-template <int D, int DV>
+// shared-memory plan (bytes), from the runtime lambda and C; with TC the offsets are from a
+// 1024-byte aligned base (the swizzled operand tiles) and `total` includes the slack
+template <int D, int DV, bool TC>
 struct CkPlan {
-    size_t H, tile, s, cpos, cand, keys, wlist, klist, total;
+    size_t A, B, H, tile, red, s, cpos, cand, keys, wlist, klist, total;
     __host__ __device__ CkPlan(int lam, int C) {
         const size_t P = (size_t)lam + C;
-        H = 0;
-        tile = H + 4ull * D * DV;
-        // scoring: phi transposed [D][kTS] + v [kG][DV]; writing: phi [kG][D] + v [kG][DV]
+        // scoring on CUDA cores: phi transposed [D][kTS] + v [kG][DV]; writing: phi [kG][D] +
+        // v [kG][DV] (float32)
         const size_t tile_b = 4ull * (D * kTS > kG * D ? D * kTS : kG * D) + 4ull * kG * DV;
-        s = a16c(tile + tile_b);
+        if (TC) {
+            // A: the candidates' phi as bf16 hi and lo parts (K-major [kGT][D] each), B: H
+            // likewise (MN-major [D][DV] each); the write phase's staging reuses A and B
+            A = 0;
+            B = A + 2ull * kAhalf;
+            H = B + 2ull * kBhalf;
+            tile = 0;
+            red = H + 4ull * D * DV;             // z and the column blocks' partials
+            s = a16c(red + 4ull * 9 * kGT);
+        } else {
+            A = B = 0;
+            H = 0;
+            tile = H + 4ull * D * DV;
+            red = a16c(tile + tile_b);           // tile_sre2's z and column-block partials
+            s = a16c(red + 4ull * 9 * kG);
+        }
         cpos = a16c(s + 4ull * D);
         cand = a16c(cpos + 4ull * (lam > 0 ? lam : 1));
         keys = a16c(cand + 4 * P);
         wlist = a16c(keys + 8 * P);
         klist = a16c(wlist + 4 * P);
-        total = a16c(klist + 4ull * (lam > 0 ? lam : 1));
+        total = a16c(klist + 4ull * (lam > 0 ? lam : 1)) + (TC ? 1024 : 0);
     }
 };
+
+// eight float32 as bfloat16 hi parts and the bfloat16 of the remainders (x - hi is exact)
+__device__ __forceinline__ void split8(const float4& a, const float4& b, uint4& hi, uint4& lo) {
+    const float x[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hh);
+        const __nv_bfloat162 ll = __floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y);
+        h[e] = *reinterpret_cast<const uint32_t*>(&hh);
+        l[e] = *reinterpret_cast<const uint32_t*>(&ll);
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
 
 // kG rows of phi (float32, D wide) and of v (input type, DV wide, widened exactly) for the
 // keys at positions pos(j), j < cnt (zero rows beyond), all loads issued before any store.
@@ -123,67 +161,123 @@ __device__ __forceinline__ void stage_rows(const float* phiK, const T* Vin, int 
 }
 
 // SRE^2 of the kG keys staged in the tile (phi transposed [D][kTS], values [kG][DV]) against
-// (H, s) in shared memory, for keys j < nvalid: warp w takes keys 4w .. 4w + 3, lane l the
-// value columns l*HC ..; N = H^T phi accumulated over the D rows, z = s^T phi, then
-// SRE^2 = |N - z v|^2 / z^2, or |v|^2 when z = 0 (the empty memory predicts 0).  Lane 0 of
-// each warp hands (j, SRE^2) to emit.
+// (H, s) in shared memory, for keys j < nvalid.  N = H^T phi is a [kG x DV] product over the D
+// rows: warp w takes keys 16 (w % 4) .. + 15 and value columns (w / 4) * 8 LC .. (LC = DV / 32),
+// lane l four of those keys (4 (l / 8) ..) and LC columns ((l % 8) LC ..), so that a row costs
+// the warp one shared-memory wavefront of phi and one of H.  z = s^T phi is formed first (warp w
+// for keys 4w .. 4w + 3, lane-strided rows, then a warp sum) and shared through red[0 .. kG);
+// each warp's |N - z v|^2 and |v|^2 over its columns go to red[kG ..], and thread j < kG adds the
+// four column blocks in order: SRE^2 = |N - z v|^2 / z^2, or |v|^2 when z = 0 (the empty memory
+// predicts 0).  Thread j hands (j, SRE^2) to emit.  red holds kG + 2 * 4 * kG floats; contains
+// two block-wide barriers, so every thread of the CTA calls it.
 template <int D, int DV, typename Emit>
 __device__ __forceinline__ void tile_sre2(const float* Hs, const float* ss, const float* tile, const float* vts,
-                                          int nvalid, int warp, int lane, Emit emit) {
-    constexpr int HC = DV / kWarp;
-    float acc[4][HC];
+                                          float* red, int nvalid, int warp, int lane, Emit emit) {
+    constexpr int LC = DV / kWarp, LC2 = LC / 2, NCB = 4;   // columns per lane, column blocks
+    static_assert(LC % 2 == 0 && kG == 16 * 4 && kCkWarps == 4 * NCB && DV == NCB * 8 * LC, "warp tiling");
+    float* zs = red;
+    float* part = red + kG;   // [NCB][kG][2]
+    // z = s^T phi(k) for keys 4w .. 4w + 3: lane l takes rows l, l + 32, ...
+    {
+        float z4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int r = lane; r < D; r += kWarp) {
+            const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
+            const float sr = ss[r];
+            z4[0] = fmaf(f.x, sr, z4[0]);
+            z4[1] = fmaf(f.y, sr, z4[1]);
+            z4[2] = fmaf(f.z, sr, z4[2]);
+            z4[3] = fmaf(f.w, sr, z4[3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float z = warp_sum(z4[i]);
+            if (lane == 0) zs[4 * warp + i] = z;
+        }
+    }
+    const int cb = warp % 4, colb = warp / 4;
+    const int j0 = 16 * cb + 4 * (lane / 8);                 // this lane's four keys
+    const int c0 = colb * 8 * LC + (lane % 8) * LC;          // and LC columns
+    // column pairs in float2: one paired FMA per two products, each rounded as a single fmaf;
+    // every element takes the rows in order
+    float2 acc2[4][LC2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int q = 0; q < HC; ++q) acc[i][q] = 0.f;
+        for (int q = 0; q < LC2; ++q) acc2[i][q] = make_float2(0.f, 0.f);
 #pragma unroll 8
     for (int r = 0; r < D; ++r) {
-        float h[HC];
-        chain::h_vec_load<HC>(Hs + r * DV + lane * HC, h);
-        const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
+        float h[LC];
+        chain::h_vec_load<LC>(Hs + r * DV + c0, h);
+        const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + j0);
         const float fi[4] = {f.x, f.y, f.z, f.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
-            for (int q = 0; q < HC; ++q) acc[i][q] = fmaf(fi[i], h[q], acc[i][q]);
+            for (int q = 0; q < LC2; ++q)
+                acc2[i][q] = __ffma2_rn(make_float2(fi[i], fi[i]), make_float2(h[2 * q], h[2 * q + 1]), acc2[i][q]);
     }
-    // z = s^T phi(k): lane l takes rows l, l + 32, ...
-    float z4[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int r = lane; r < D; r += kWarp) {
-        const float4 f = *reinterpret_cast<const float4*>(tile + r * kTS + 4 * warp);
-        const float sr = ss[r];
-        z4[0] = fmaf(f.x, sr, z4[0]);
-        z4[1] = fmaf(f.y, sr, z4[1]);
-        z4[2] = fmaf(f.z, sr, z4[2]);
-        z4[3] = fmaf(f.w, sr, z4[3]);
-    }
+    __syncthreads();   // zs complete
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const int j = 4 * warp + i;
-        const float z = warp_sum(z4[i]);
+        const int j = j0 + i;
+        const float z = zs[j];
+        float v[LC];
+        chain::h_vec_load<LC>(vts + j * DV + c0, v);
         float dd = 0.f, vv = 0.f;
 #pragma unroll
-        for (int q = 0; q < HC; ++q) {
-            const float vq = vts[j * DV + lane * HC + q];
-            const float d = fmaf(-z, vq, acc[i][q]);
-            dd = fmaf(d, d, dd);
-            vv = fmaf(vq, vq, vv);
+        for (int q = 0; q < LC2; ++q) {
+            const float d0 = fmaf(-z, v[2 * q], acc2[i][q].x), d1 = fmaf(-z, v[2 * q + 1], acc2[i][q].y);
+            dd = fmaf(d0, d0, dd);
+            dd = fmaf(d1, d1, dd);
+            vv = fmaf(v[2 * q], v[2 * q], vv);
+            vv = fmaf(v[2 * q + 1], v[2 * q + 1], vv);
         }
-        dd = warp_sum(dd);
-        vv = warp_sum(vv);
-        if (lane == 0 && j < nvalid) emit(j, z == 0.f ? vv : dd / (z * z));
+        // the eight lanes of this key group hold the warp's column block
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            dd += __shfl_xor_sync(0xffffffffu, dd, o);
+            vv += __shfl_xor_sync(0xffffffffu, vv, o);
+        }
+        if (lane % 8 == 0) {
+            part[(colb * kG + j) * 2] = dd;
+            part[(colb * kG + j) * 2 + 1] = vv;
+        }
+    }
+    __syncthreads();   // the column blocks' partials
+    const int j = warp * kWarp + lane;
+    if (j < kG && j < nvalid) {
+        float dd = 0.f, vv = 0.f;
+#pragma unroll
+        for (int b = 0; b < NCB; ++b) {
+            dd += part[(b * kG + j) * 2];
+            vv += part[(b * kG + j) * 2 + 1];
+        }
+        const float z = zs[j];
+        emit(j, z == 0.f ? vv : dd / (z * z));
     }
 }
 
-template <int D, int DV, typename T>
+// TC: the scoring runs on the tensor cores (bfloat16 io, D = d_v = 128 only).  N = Phi H is
+// formed from bfloat16 hi/lo splits of both operands, Phi_hi H_hi + Phi_hi H_lo + Phi_lo H_hi,
+// accumulated in float32 in TMEM (relative error about 2^-16; the lo x lo term is dropped),
+// kGT candidates per group (M = kGT, N = d_v, K = D; A K-major, B MN-major, 128-byte
+// swizzle).  z = s^T phi stays float32 on the CUDA cores, formed while A is staged; the
+// epilogue reads N from TMEM (warp w: TMEM lanes 32 (w % 4) .., columns 32 (w / 4) ..).
+template <int D, int DV, typename T, bool TC>
 __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const ChunkArgs a) {
     using S = Shape<D, DV>;
     constexpr int HR = S::HR, HC = S::HC;
     static_assert(kCkThreads == chain::kThreads, "H blocks of the chain layout");
-    extern __shared__ __align__(16) unsigned char sm[];
-    const CkPlan<D, DV> pl(a.lam, a.C);
+    static_assert(!TC || (D == 128 && DV == 128 && sizeof(T) == 2), "tensor-core scoring: bf16, D = d_v = 128");
+    extern __shared__ __align__(16) unsigned char smraw[];
+    unsigned char* sm = TC ? reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023))
+                           : smraw;
+    __shared__ uint64_t mbar;
+    __shared__ uint32_t tmem_base;
+    const CkPlan<D, DV, TC> pl(a.lam, a.C);
     float* Hs = reinterpret_cast<float*>(sm + pl.H);
     float* tile = reinterpret_cast<float*>(sm + pl.tile);
+    float* red = reinterpret_cast<float*>(sm + pl.red);
     float* ss = reinterpret_cast<float*>(sm + pl.s);
     int* cpos = reinterpret_cast<int*>(sm + pl.cpos);
     int* cand = reinterpret_cast<int*>(sm + pl.cand);
@@ -207,7 +301,18 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         if (wps) wps[i] = -1;
     }
     int nc = 0, nwritten = 0;   // (uniform)
+    uint32_t tb = 0, phase = 0;
+    bool timed_out = false;     // (uniform)
+    if constexpr (TC) {
+        if (tid == 0) tc::mbar_init(tc::smem_u32(&mbar), 1);
+        if (warp == 0) tc::tmem_alloc<kTmemCols>(tc::smem_u32(&tmem_base));
+        tc::fence_before();
+    }
     __syncthreads();
+    if constexpr (TC) {
+        tc::fence_after();
+        tb = tmem_base;
+    }
 
     const int nch = (n + C - 1) / C;
     for (int c = 0; c < nch; ++c) {
@@ -236,17 +341,152 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
             continue;
         }
 
-        // ---- SRE^2 of every candidate against the current (H, s), kG at a time ----
-        float* vts = tile + D * kTS;   // [kG][DV] the group's values (float32)
-        for (int g0 = 0; g0 < P; g0 += kG) {
-            const int cnt = min(kG, P - g0);
-            stage_rows<D, DV, T, true>(phiK, Vin, cnt, [&](int j) { return cand[g0 + j]; },
-                                       [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
-            __syncthreads();
-            tile_sre2<D, DV>(Hs, ss, tile, vts, cnt, warp, lane, [&](int j, float sre2) {
-                keys[g0 + j] = ((unsigned long long)__float_as_uint(sre2) << 32) | (unsigned)cand[g0 + j];
-            });
-            __syncthreads();   // the tile is restaged
+        // ---- SRE^2 of every candidate against the current (H, s) ----
+        if constexpr (TC) {
+            unsigned char* Ab = sm + pl.A;
+            unsigned char* Bb = sm + pl.B;
+            float* zs = red;              // [kGT]
+            float* part = red + kGT;      // [4][kGT][2]
+            // B = H as bf16 hi and lo (MN-major), once per scoring chunk start
+            for (int i = tid; i < D * (DV / 8); i += kCkThreads) {
+                const int k = i / (DV / 8), n8 = (i % (DV / 8)) * 8;
+                uint4 hi, lo;
+                split8(*reinterpret_cast<const float4*>(Hs + k * DV + n8),
+                       *reinterpret_cast<const float4*>(Hs + k * DV + n8 + 4), hi, lo);
+                const uint32_t off = tc::mnmaj_chunk(k, n8, D);
+                *reinterpret_cast<uint4*>(Bb + off) = hi;
+                *reinterpret_cast<uint4*>(Bb + kBhalf + off) = lo;
+            }
+            for (int g0 = 0; g0 < P; g0 += kGT) {
+                const int cnt = min(kGT, P - g0);
+                // A = the group's phi rows split (K-major; rows >= cnt zero); thread tid takes
+                // the 16-byte chunk c16 = tid % 16 of rows tid / 16 + 32 u, u < 4, and z of
+                // those rows is summed over the 16 lanes that hold a row
+                {
+                    constexpr int U = kGT * (D / 8) / kCkThreads;
+                    static_assert(U * kCkThreads == kGT * (D / 8) && D / 8 == 16, "A staging split");
+                    const int c16 = tid & 15;
+                    float4 f[U][2];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int r = (tid >> 4) + 32 * u;
+                        if (r < cnt) {
+                            const float* src = phiK + (int64_t)cand[g0 + r] * D + c16 * 8;
+                            f[u][0] = *reinterpret_cast<const float4*>(src);
+                            f[u][1] = *reinterpret_cast<const float4*>(src + 4);
+                        } else {
+                            f[u][0] = f[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        }
+                    }
+                    const float4 s0 = *reinterpret_cast<const float4*>(ss + c16 * 8);
+                    const float4 s1 = *reinterpret_cast<const float4*>(ss + c16 * 8 + 4);
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int r = (tid >> 4) + 32 * u;
+                        uint4 hi, lo;
+                        split8(f[u][0], f[u][1], hi, lo);
+                        const uint32_t off = (c16 >> 3) * 16384 + tc::kmaj_chunk(r, c16 & 7);
+                        *reinterpret_cast<uint4*>(Ab + off) = hi;
+                        *reinterpret_cast<uint4*>(Ab + kAhalf + off) = lo;
+                        float z = 0.f;
+                        z = fmaf(f[u][0].x, s0.x, z);
+                        z = fmaf(f[u][0].y, s0.y, z);
+                        z = fmaf(f[u][0].z, s0.z, z);
+                        z = fmaf(f[u][0].w, s0.w, z);
+                        z = fmaf(f[u][1].x, s1.x, z);
+                        z = fmaf(f[u][1].y, s1.y, z);
+                        z = fmaf(f[u][1].z, s1.z, z);
+                        z = fmaf(f[u][1].w, s1.w, z);
+#pragma unroll
+                        for (int o = 1; o < 16; o <<= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                        if (c16 == 0) zs[r] = z;
+                    }
+                }
+                tc::fence_async_smem();
+                tc::fence_before();
+                __syncthreads();
+                tc::fence_after();
+                if (tid == 0) {
+                    constexpr uint32_t id = tc::idesc_bf16(kGT, DV, 1);
+                    const uint32_t sa = tc::smem_u32(Ab), sb = tc::smem_u32(Bb);
+#pragma unroll 1
+                    for (int pass = 0; pass < 3; ++pass) {   // hi x hi, hi x lo, lo x hi
+                        const uint32_t ao = pass == 2 ? kAhalf : 0u, bo = pass == 1 ? kBhalf : 0u;
+#pragma unroll
+                        for (int k = 0; k < D / 16; ++k) {
+                            const uint64_t ad = tc::sdesc(sa + ao + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+                            const uint64_t bd = tc::sdesc(sb + bo + k * 2048, 16384, 1024);
+                            tc::mma_bf16(tb, ad, bd, id, (pass | k) != 0);
+                        }
+                    }
+                    tc::mma_commit(tc::smem_u32(&mbar));
+                }
+                // the epilogue's values, loaded while the products run
+                const int ql = warp & 3, colb = warp >> 2, j = 32 * ql + lane;
+                uint4 vr[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) vr[q] = make_uint4(0, 0, 0, 0);
+                if (j < cnt) {
+                    const uint4* src = reinterpret_cast<const uint4*>(Vin + (int64_t)cand[g0 + j] * DV + 32 * colb);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) vr[q] = src[q];
+                }
+                const bool ok = tc::mbar_wait(tc::smem_u32(&mbar), phase, kCkWaitNs);
+                phase ^= 1u;
+                tc::fence_after();
+                if (__syncthreads_or(!ok)) {
+                    timed_out = true;
+                    break;
+                }
+                float nv[32];
+                tc::tmem_ld32(tb + ((uint32_t)(32 * ql) << 16) + 32 * colb, nv);
+                tc::tmem_wait_ld();
+                const float z = zs[j];
+                float dd = 0.f, vv = 0.f;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t w4[4] = {vr[q].x, vr[q].y, vr[q].z, vr[q].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float v0 = chain::bf16_lo(w4[e]), v1 = chain::bf16_hi(w4[e]);
+                        const float d0 = fmaf(-z, v0, nv[8 * q + 2 * e]), d1 = fmaf(-z, v1, nv[8 * q + 2 * e + 1]);
+                        dd = fmaf(d0, d0, dd);
+                        dd = fmaf(d1, d1, dd);
+                        vv = fmaf(v0, v0, vv);
+                        vv = fmaf(v1, v1, vv);
+                    }
+                }
+                part[(colb * kGT + j) * 2] = dd;
+                part[(colb * kGT + j) * 2 + 1] = vv;
+                tc::fence_before();
+                __syncthreads();
+                if (tid < cnt) {
+                    float d2 = 0.f, v2 = 0.f;
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) {
+                        d2 += part[(b * kGT + tid) * 2];
+                        v2 += part[(b * kGT + tid) * 2 + 1];
+                    }
+                    const float zt = zs[tid];
+                    const float sre2 = zt == 0.f ? v2 : d2 / (zt * zt);
+                    keys[g0 + tid] = ((unsigned long long)__float_as_uint(sre2) << 32) | (unsigned)cand[g0 + tid];
+                }
+                __syncthreads();   // A, z and the partials are restaged; TMEM is read
+            }
+            if (timed_out) break;
+        } else {
+            // on the CUDA cores, kG candidates at a time
+            float* vts = tile + D * kTS;   // [kG][DV] the group's values (float32)
+            for (int g0 = 0; g0 < P; g0 += kG) {
+                const int cnt = min(kG, P - g0);
+                stage_rows<D, DV, T, true>(phiK, Vin, cnt, [&](int j) { return cand[g0 + j]; },
+                                           [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
+                __syncthreads();
+                tile_sre2<D, DV>(Hs, ss, tile, vts, red, cnt, warp, lane, [&](int j, float sre2) {
+                    keys[g0 + j] = ((unsigned long long)__float_as_uint(sre2) << 32) | (unsigned)cand[g0 + j];
+                });
+                __syncthreads();   // the tile is restaged
+            }
         }
 
         // ---- rank by (SRE^2, position): the lowest P - lambda are written ----
@@ -280,12 +520,16 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
             stage_rows<D, DV, T, false>(phiK, Vin, cnt, [&](int j) { return wlist[w0 + j]; },
                                  [&](int j, int r) -> float& { return tphi[j * D + r]; }, tv, tid);
             __syncthreads();
+            // (unrolled so that the next keys' loads overlap this key's products; every
+            //  element still takes the keys one after another, in rank order)
+#pragma unroll 4
             for (int j = 0; j < cnt; ++j) {
                 float vh[HC];
                 chain::h_vec_load<HC>(tv + j * DV + lane * HC, vh);
                 chain::h_update<D, DV>(hreg, tphi + j * D, vh, warp);
-                if (tid < D) sreg += tphi[j * D + tid];
             }
+            if (tid < D)
+                for (int j = 0; j < cnt; ++j) sreg += tphi[j * D + tid];
             __syncthreads();
         }
         chain::h_store<D, DV>(Hs, hreg, warp, lane);
@@ -300,8 +544,19 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         __syncthreads();
     }
 
-    // ---- export: header, H, s, the cache (positions and rows) and the window ring ----
     char* rec = a.state + (int64_t)bh * a.L.head_bytes;
+    if constexpr (TC) {
+        tc::fence_before();
+        __syncthreads();
+        tc::fence_after();
+        if (warp == 0) tc::tmem_dealloc<kTmemCols>(tb);
+        if (timed_out) {   // a product group did not complete: report it, export nothing
+            if (tid == 0) reinterpret_cast<int32_t*>(rec)[HDR_STATUS] = ST_TIMEOUT;
+            return;
+        }
+    }
+
+    // ---- export: header, H, s, the cache (positions and rows) and the window ring ----
     if (tid == 0) {
         int32_t* hdr = reinterpret_cast<int32_t*>(rec);
         hdr[HDR_T] = n;
@@ -367,8 +622,9 @@ cudaError_t launch_chunk_t(const Dims& d, int n, const Workspace& ws, const void
     a.snapC = ws.snapC;
     a.state = state;
     a.L = L;
-    const size_t smem = CkPlan<D, DV>(d.lam, d.chunk).total;
-    auto kern = chunk_select_kernel<D, DV, T>;
+    constexpr bool TC = sizeof(T) == 2 && D == 128 && DV == 128;
+    const size_t smem = CkPlan<D, DV, TC>(d.lam, d.chunk).total;
+    auto kern = chunk_select_kernel<D, DV, T, TC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<d.BH, kCkThreads, smem, st>>>(a);
@@ -398,6 +654,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) sre_map_kernel(const SreArgs a)
     float* tile = Hs + D * DV;                                           // [D][kTS]
     float* vts = tile + D * kTS;                                         // [kG][DV]
     float* ss = vts + kG * DV;                                           // [D]
+    float* red = ss + D;                                                 // [9 kG]
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int c = blockIdx.x, bh = blockIdx.y;
     const int n = a.n, tc = c * a.snap;
@@ -416,7 +673,7 @@ __global__ void __launch_bounds__(kCkThreads, 1) sre_map_kernel(const SreArgs a)
         stage_rows<D, DV, T, true>(phiK, Vin, cnt, [&](int j) { return j0 + j; },
                                    [&](int j, int r) -> float& { return tile[r * kTS + j]; }, vts, tid);
         __syncthreads();
-        tile_sre2<D, DV>(Hs, ss, tile, vts, cnt, warp, lane, [&](int j, float sre2) {
+        tile_sre2<D, DV>(Hs, ss, tile, vts, red, cnt, warp, lane, [&](int j, float sre2) {
             const int w = wst[j0 + j];
             out[j0 + j] = (w >= 0 && w < tc) ? sqrtf(sre2) : 0.f;   // held by the memory, else 0
         });
@@ -436,7 +693,7 @@ cudaError_t launch_sre_map_t(const Dims& d, int n, const Workspace& ws, const vo
     a.snapHb = ws.snapHb;
     a.snapS = ws.snapS;
     a.out = out;
-    const size_t smem = sizeof(float) * ((size_t)D * DV + D * kTS + kG * DV + D);
+    const size_t smem = sizeof(float) * ((size_t)D * DV + D * kTS + kG * DV + D + 9 * kG);
     auto kern = sre_map_kernel<D, DV, T>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -458,7 +715,10 @@ cudaError_t launch_sre_map(const Dims& d, int n, const Workspace& ws, const void
 }
 
 bool chunk_mode_fits(const Dims& d) {
-    const size_t smem = d.D == 128 ? CkPlan<128, 128>(d.lam, d.chunk).total : CkPlan<64, 64>(d.lam, d.chunk).total;
+    const bool bf = d.dtype == LOLA_BF16;
+    const size_t smem = d.D == 128 ? (bf ? CkPlan<128, 128, true>(d.lam, d.chunk).total
+                                         : CkPlan<128, 128, false>(d.lam, d.chunk).total)
+                                   : CkPlan<64, 64, false>(d.lam, d.chunk).total;
     return smem <= 227 * 1024;
 }
 
