@@ -355,10 +355,21 @@ def run_prefill(L, R, args, pk):
         else:
             fl = heads * w.n * select_flops_per_step(w.D, w.d, w.lam)
         ach = fl / (sel["avg_ms"] / 1e3) / 1e12
-        res["roofline"] = {"kernel": "select", "bound": "alu", "achieved": ach, "peak": pk["fp32_tflops"],
-                           "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"],
-                           "traffic": traffic("select") if args.alloc == "token" else None,
-                           "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+        if args.alloc == "chunk" and w.dtype == "bf16" and w.D == 128 and w.d == 128:
+            # the candidates' products and the H update run on the tensor cores as split-bf16
+            # passes (3 for the scoring, 2 for the write); the bound is the bf16 tensor peak
+            nch = heads * max(0, w.n // w.chunk - w.eta // w.chunk)
+            P = w.lam + w.chunk
+            executed = nch * 2 * (3 * P * w.D * w.d + 2 * w.chunk * w.D * w.d)
+            res["roofline"] = {"kernel": "select", "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+                               "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None,
+                               "peak_source": "measured cuBLAS bf16 (burst)",
+                               "executed_tensor_tflops": executed / (sel["avg_ms"] / 1e3) / 1e12}
+        else:
+            res["roofline"] = {"kernel": "select", "bound": "alu", "achieved": ach, "peak": pk["fp32_tflops"],
+                               "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"],
+                               "traffic": traffic("select") if args.alloc == "token" else None,
+                               "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
     out = kt.get("output")
     if out:
         fl = heads * w.n * output_flops_per_token(w.d, w.d, w.D, w.eta, w.lam)

@@ -36,8 +36,10 @@ constexpr int kTS = kG + 4;            // row stride of the transposed phi tile 
 // tensor-core scoring (bfloat16 io, D = d_v = 128): candidates per MMA group (M), TMEM
 // columns (the fp32 N tile), the halves of the split operands, the completion wait limit
 constexpr int kGT = 128;
-constexpr int kTmemCols = 128;
-constexpr uint32_t kAhalf = 2u * kGT * 128, kBhalf = 2u * 128 * 128;
+constexpr int kGW = 64;                // written keys per H-update product group (K)
+constexpr int kTmemCols = 256;         // [0, 128): the scoring tile N; [128, 256): H (float32)
+constexpr uint32_t kTH = 128;
+constexpr uint32_t kAhalf = 2u * kGT * 128, kBhalf = 2u * 128 * 128, kAWhalf = 2u * kGW * 128;
 constexpr uint64_t kCkWaitNs = 1000000000ull;
 
 struct ChunkArgs {
@@ -69,12 +71,13 @@ struct CkPlan {
         const size_t tile_b = 4ull * (D * kTS > kG * D ? D * kTS : kG * D) + 4ull * kG * DV;
         if (TC) {
             // A: the candidates' phi as bf16 hi and lo parts (K-major [kGT][D] each), B: H
-            // likewise (MN-major [D][DV] each); the write phase's staging reuses A and B
+            // likewise (MN-major [D][DV] each); the write phase's operands reuse A; H itself
+            // lives in TMEM
             A = 0;
             B = A + 2ull * kAhalf;
-            H = B + 2ull * kBhalf;
+            H = 0;
             tile = 0;
-            red = H + 4ull * D * DV;             // z and the column blocks' partials
+            red = B + 2ull * kBhalf;             // z and the column blocks' partials
             s = a16c(red + 4ull * 9 * kGT);
         } else {
             A = B = 0;
@@ -294,7 +297,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
     int32_t* wst = a.wstep + row0;
     int32_t* wps = a.wpos ? a.wpos + row0 : nullptr;
 
-    for (int i = tid; i < D * DV; i += kCkThreads) Hs[i] = 0.f;
+    if constexpr (!TC)
+        for (int i = tid; i < D * DV; i += kCkThreads) Hs[i] = 0.f;
     for (int i = tid; i < D; i += kCkThreads) ss[i] = 0.f;
     for (int i = tid; i < n; i += kCkThreads) {
         wst[i] = -1;
@@ -309,9 +313,18 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         tc::fence_before();
     }
     __syncthreads();
+    // TC: thread (warp w, lane l) reads and writes H row 32 (w % 4) + l, columns 32 (w / 4) ..
+    // (its TMEM lane quarter and column block)
+    const uint32_t lane_q = (uint32_t)(32 * (warp & 3)) << 16;
+    const int hrow = 32 * (warp & 3) + lane, hcol = 32 * (warp >> 2);
     if constexpr (TC) {
         tc::fence_after();
         tb = tmem_base;
+        float zero[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) zero[i] = 0.f;
+        tc::tmem_st32(tb + lane_q + kTH + hcol, zero);   // H = 0
+        tc::tmem_wait_st();
     }
 
     const int nch = (n + C - 1) / C;
@@ -321,7 +334,29 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         //      start's writes ----
         if (c0 % a.snap == 0) {
             const int64_t sc = (int64_t)bh * a.nck + c0 / a.snap;
-            if (a.snapHb) {
+            if constexpr (TC) {
+                float hv[32];
+                tc::tmem_ld32(tb + lane_q + kTH + hcol, hv);
+                tc::tmem_wait_ld();
+                const int64_t o = sc * D * DV + (int64_t)hrow * DV + hcol;
+                if (a.snapHb) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 b = __floats2bfloat162_rn(hv[8 * q + 2 * e], hv[8 * q + 2 * e + 1]);
+                            w[e] = *reinterpret_cast<const uint32_t*>(&b);
+                        }
+                        *reinterpret_cast<uint4*>(a.snapHb + o + 8 * q) = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4*>(a.snapH + o + 4 * q) =
+                            make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                }
+            } else if (a.snapHb) {
                 for (int i = tid; i < D * DV; i += kCkThreads) a.snapHb[sc * D * DV + i] = __float2bfloat16_rn(Hs[i]);
             } else {
                 for (int i = tid; i < D * DV; i += kCkThreads) a.snapH[sc * D * DV + i] = Hs[i];
@@ -347,15 +382,20 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
             unsigned char* Bb = sm + pl.B;
             float* zs = red;              // [kGT]
             float* part = red + kGT;      // [4][kGT][2]
-            // B = H as bf16 hi and lo (MN-major), once per scoring chunk start
-            for (int i = tid; i < D * (DV / 8); i += kCkThreads) {
-                const int k = i / (DV / 8), n8 = (i % (DV / 8)) * 8;
-                uint4 hi, lo;
-                split8(*reinterpret_cast<const float4*>(Hs + k * DV + n8),
-                       *reinterpret_cast<const float4*>(Hs + k * DV + n8 + 4), hi, lo);
-                const uint32_t off = tc::mnmaj_chunk(k, n8, D);
-                *reinterpret_cast<uint4*>(Bb + off) = hi;
-                *reinterpret_cast<uint4*>(Bb + kBhalf + off) = lo;
+            // B = H as bf16 hi and lo (MN-major), once per scoring chunk start, from TMEM
+            {
+                float hv[32];
+                tc::tmem_ld32(tb + lane_q + kTH + hcol, hv);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 hi, lo;
+                    split8(make_float4(hv[8 * q], hv[8 * q + 1], hv[8 * q + 2], hv[8 * q + 3]),
+                           make_float4(hv[8 * q + 4], hv[8 * q + 5], hv[8 * q + 6], hv[8 * q + 7]), hi, lo);
+                    const uint32_t off = tc::mnmaj_chunk(hrow, hcol + 8 * q, D);
+                    *reinterpret_cast<uint4*>(Bb + off) = hi;
+                    *reinterpret_cast<uint4*>(Bb + kBhalf + off) = lo;
+                }
             }
             for (int g0 = 0; g0 < P; g0 += kGT) {
                 const int cnt = min(kGT, P - g0);
@@ -508,32 +548,102 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         }
         __syncthreads();
 
-        // ---- H += sum phi(k) v^T and s += sum phi(k) over the written keys, in rank order;
-        //      thread (warp w, lane l) owns rows w*HR .. and columns l*HC .. of H ----
-        float hreg[HR * HC];
-        chain::h_load<D, DV>(hreg, Hs, warp, lane);
-        float sreg = tid < D ? ss[tid] : 0.f;
-        float* tphi = tile;              // [kG][D]
-        float* tv = tile + D * kTS;      // [kG][DV]
-        for (int w0 = 0; w0 < nwr; w0 += kG) {
-            const int cnt = min(kG, nwr - w0);
-            stage_rows<D, DV, T, false>(phiK, Vin, cnt, [&](int j) { return wlist[w0 + j]; },
-                                 [&](int j, int r) -> float& { return tphi[j * D + r]; }, tv, tid);
-            __syncthreads();
-            // (unrolled so that the next keys' loads overlap this key's products; every
-            //  element still takes the keys one after another, in rank order)
-#pragma unroll 4
-            for (int j = 0; j < cnt; ++j) {
-                float vh[HC];
-                chain::h_vec_load<HC>(tv + j * DV + lane * HC, vh);
-                chain::h_update<D, DV>(hreg, tphi + j * D, vh, warp);
+        // ---- H += sum phi(k) v^T and s += sum phi(k) over the written keys ----
+        if constexpr (TC) {
+            // on the tensor cores, into H in TMEM: kGW keys per group, A = their phi split
+            // into bf16 hi and lo, B = their values (both MN-major [keys][D]); two passes,
+            // Phi_hi^T V + Phi_lo^T V; s in float32 on the CUDA cores, in rank order
+            unsigned char* AW = sm + pl.A;
+            unsigned char* VW = sm + pl.A + 2 * kAWhalf;
+            float sreg = tid < D ? ss[tid] : 0.f;
+            for (int w0 = 0; w0 < nwr; w0 += kGW) {
+                const int cnt = min(kGW, nwr - w0);
+                constexpr int U = kGW * (D / 8) / kCkThreads;
+                static_assert(U * kCkThreads == kGW * (D / 8) && D == DV, "write staging split");
+                const int c16 = tid & 15;
+                float4 f[U][2];
+                uint4 vr[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = (tid >> 4) + 32 * u;
+                    if (k < cnt) {
+                        const int p = wlist[w0 + k];
+                        const float* src = phiK + (int64_t)p * D + c16 * 8;
+                        f[u][0] = *reinterpret_cast<const float4*>(src);
+                        f[u][1] = *reinterpret_cast<const float4*>(src + 4);
+                        vr[u] = *reinterpret_cast<const uint4*>(Vin + (int64_t)p * DV + c16 * 8);
+                    } else {
+                        f[u][0] = f[u][1] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        vr[u] = make_uint4(0, 0, 0, 0);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int k = (tid >> 4) + 32 * u;
+                    uint4 hi, lo;
+                    split8(f[u][0], f[u][1], hi, lo);
+                    const uint32_t off = tc::mnmaj_chunk(k, c16 * 8, kGW);
+                    *reinterpret_cast<uint4*>(AW + off) = hi;
+                    *reinterpret_cast<uint4*>(AW + kAWhalf + off) = lo;
+                    *reinterpret_cast<uint4*>(VW + off) = vr[u];
+                }
+                if (tid < D)
+                    for (int j = 0; j < cnt; ++j) sreg += phiK[(int64_t)wlist[w0 + j] * D + tid];
+                tc::fence_async_smem();
+                tc::fence_before();
+                __syncthreads();
+                tc::fence_after();
+                if (tid == 0) {
+                    constexpr uint32_t id = tc::idesc_bf16(D, DV, 1) | (1u << 15);   // A MN-major too
+                    const uint32_t sa = tc::smem_u32(AW), sv = tc::smem_u32(VW);
+#pragma unroll
+                    for (int pass = 0; pass < 2; ++pass)
+#pragma unroll
+                        for (int k = 0; k < kGW / 16; ++k) {
+                            const uint64_t ad = tc::sdesc(sa + pass * kAWhalf + k * 2048, (kGW / 8) * 1024, 1024);
+                            const uint64_t bd = tc::sdesc(sv + k * 2048, (kGW / 8) * 1024, 1024);
+                            tc::mma_bf16(tb + kTH, ad, bd, id, 1);
+                        }
+                    tc::mma_commit(tc::smem_u32(&mbar));
+                }
+                const bool ok = tc::mbar_wait(tc::smem_u32(&mbar), phase, kCkWaitNs);
+                phase ^= 1u;
+                tc::fence_after();
+                if (__syncthreads_or(!ok)) {   // (also: this group's operands are consumed)
+                    timed_out = true;
+                    break;
+                }
             }
-            if (tid < D)
-                for (int j = 0; j < cnt; ++j) sreg += tphi[j * D + tid];
-            __syncthreads();
+            if (timed_out) break;
+            if (tid < D) ss[tid] = sreg;
+        } else {
+            // on the CUDA cores, in rank order: thread (warp w, lane l) owns rows w*HR .. and
+            // columns l*HC .. of H
+            float hreg[HR * HC];
+            chain::h_load<D, DV>(hreg, Hs, warp, lane);
+            float sreg = tid < D ? ss[tid] : 0.f;
+            float* tphi = tile;              // [kG][D]
+            float* tv = tile + D * kTS;      // [kG][DV]
+            for (int w0 = 0; w0 < nwr; w0 += kG) {
+                const int cnt = min(kG, nwr - w0);
+                stage_rows<D, DV, T, false>(phiK, Vin, cnt, [&](int j) { return wlist[w0 + j]; },
+                                     [&](int j, int r) -> float& { return tphi[j * D + r]; }, tv, tid);
+                __syncthreads();
+                // (unrolled so that the next keys' loads overlap this key's products; every
+                //  element still takes the keys one after another, in rank order)
+#pragma unroll 4
+                for (int j = 0; j < cnt; ++j) {
+                    float vh[HC];
+                    chain::h_vec_load<HC>(tv + j * DV + lane * HC, vh);
+                    chain::h_update<D, DV>(hreg, tphi + j * D, vh, warp);
+                }
+                if (tid < D)
+                    for (int j = 0; j < cnt; ++j) sreg += tphi[j * D + tid];
+                __syncthreads();
+            }
+            chain::h_store<D, DV>(Hs, hreg, warp, lane);
+            if (tid < D) ss[tid] = sreg;
         }
-        chain::h_store<D, DV>(Hs, hreg, warp, lane);
-        if (tid < D) ss[tid] = sreg;
         for (int i = tid; i < nwr; i += kCkThreads) {
             wst[wlist[i]] = c0;
             if (wps) wps[wlist[i]] = c0;
@@ -545,7 +655,17 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
     }
 
     char* rec = a.state + (int64_t)bh * a.L.head_bytes;
+    float* Hg = reinterpret_cast<float*>(rec + a.L.H);
     if constexpr (TC) {
+        if (!timed_out) {
+            float hv[32];
+            tc::tmem_ld32(tb + lane_q + kTH + hcol, hv);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                *reinterpret_cast<float4*>(Hg + (int64_t)hrow * DV + hcol + 4 * q) =
+                    make_float4(hv[4 * q], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+        }
         tc::fence_before();
         __syncthreads();
         tc::fence_after();
@@ -564,8 +684,8 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         hdr[HDR_NWRITTEN] = nwritten;
         hdr[HDR_STATUS] = 0;
     }
-    float* Hg = reinterpret_cast<float*>(rec + a.L.H);
-    for (int i = tid; i < D * DV; i += kCkThreads) Hg[i] = Hs[i];
+    if constexpr (!TC)
+        for (int i = tid; i < D * DV; i += kCkThreads) Hg[i] = Hs[i];
     float* sg = reinterpret_cast<float*>(rec + a.L.s);
     for (int i = tid; i < D; i += kCkThreads) sg[i] = ss[i];
     const T* Kin = static_cast<const T*>(a.K) + row0 * D;
