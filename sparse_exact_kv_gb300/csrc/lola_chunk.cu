@@ -552,9 +552,13 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
         if constexpr (TC) {
             // on the tensor cores, into H in TMEM: kGW keys per group, A = their phi split
             // into bf16 hi and lo, B = their values (both MN-major [keys][D]); two passes,
-            // Phi_hi^T V + Phi_lo^T V; s in float32 on the CUDA cores, in rank order
+            // Phi_hi^T V + Phi_lo^T V.  s in float32 on the CUDA cores from the staged rows:
+            // each thread adds its two keys, the two lanes holding one column block add, the
+            // 16 warps' partials go to spart (the scoring B tile, idle here) and thread r < D
+            // adds them in warp order while the products run
             unsigned char* AW = sm + pl.A;
             unsigned char* VW = sm + pl.A + 2 * kAWhalf;
+            float* spart = reinterpret_cast<float*>(sm + pl.B);   // [kCkWarps][D]
             float sreg = tid < D ? ss[tid] : 0.f;
             for (int w0 = 0; w0 < nwr; w0 += kGW) {
                 const int cnt = min(kGW, nwr - w0);
@@ -587,8 +591,19 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
                     *reinterpret_cast<uint4*>(AW + kAWhalf + off) = lo;
                     *reinterpret_cast<uint4*>(VW + off) = vr[u];
                 }
-                if (tid < D)
-                    for (int j = 0; j < cnt; ++j) sreg += phiK[(int64_t)wlist[w0 + j] * D + tid];
+                {
+                    static_assert(U == 2, "two keys per thread");
+                    float sp[8] = {f[0][0].x + f[1][0].x, f[0][0].y + f[1][0].y, f[0][0].z + f[1][0].z,
+                                   f[0][0].w + f[1][0].w, f[0][1].x + f[1][1].x, f[0][1].y + f[1][1].y,
+                                   f[0][1].z + f[1][1].z, f[0][1].w + f[1][1].w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sp[e] += __shfl_xor_sync(0xffffffffu, sp[e], 16);
+                    if (lane < 16) {
+                        float* dst = spart + warp * D + c16 * 8;
+                        *reinterpret_cast<float4*>(dst) = make_float4(sp[0], sp[1], sp[2], sp[3]);
+                        *reinterpret_cast<float4*>(dst + 4) = make_float4(sp[4], sp[5], sp[6], sp[7]);
+                    }
+                }
                 tc::fence_async_smem();
                 tc::fence_before();
                 __syncthreads();
@@ -606,10 +621,16 @@ __global__ void __launch_bounds__(kCkThreads, 1) chunk_select_kernel(const Chunk
                         }
                     tc::mma_commit(tc::smem_u32(&mbar));
                 }
+                if (tid < D) {
+                    float inc = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kCkWarps; ++w) inc += spart[w * D + tid];
+                    sreg += inc;
+                }
                 const bool ok = tc::mbar_wait(tc::smem_u32(&mbar), phase, kCkWaitNs);
                 phase ^= 1u;
                 tc::fence_after();
-                if (__syncthreads_or(!ok)) {   // (also: this group's operands are consumed)
+                if (__syncthreads_or(!ok)) {   // (also: this group's operands and spart are consumed)
                     timed_out = true;
                     break;
                 }
