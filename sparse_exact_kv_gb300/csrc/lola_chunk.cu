@@ -11,15 +11,22 @@
 // position first among equal ones; the empty memory predicts 0 (SRE = ||v||).  With C = 1
 // this is the per-token rule.
 //
-// One CTA of 512 threads per head walks its chunks; H (float32) lives in shared memory.
-// At every chunk start c0: the snapshot for the output pass when c0 is a multiple of its
-// interval (the memory before this start's writes, as in the per-token chain); then the
-// candidates -- the cache, then the chunk leaving the window -- are scored 64 at a time
-// (a 64 x d_v product of their phi, staged transposed, with H read from shared memory; each
-// warp a 16-key x d_v/4-column tile of it), ranked by (SRE^2, position), and
-// the lowest P - lambda are added to H and s in rank order.  Every written key's step is
-// recorded as c0 (the first query that reads it through the state), which is the rule the
-// output kernels apply: key j is exact for query t iff j <= t < w_j, linear iff w_j <= t.
+// One CTA of 512 threads per head walks its chunks.  At every chunk start c0: the snapshot for
+// the output pass when c0 is a multiple of its interval (the memory before this start's writes,
+// as in the per-token chain); then the candidates -- the cache, then the chunk leaving the
+// window -- are scored, ranked by (SRE^2, position), and the lowest P - lambda are added to H
+// and s.  Every written key's step is recorded as c0 (the first query that reads it through
+// the state), which is the rule the output kernels apply: key j is exact for query t iff
+// j <= t < w_j, linear iff w_j <= t.
+//
+// Two builds.  bfloat16 io with D = d_v = 128: both contractions on the tensor cores
+// (tcgen05), H in TMEM (float32) for the whole launch -- the candidates' N = Phi H from
+// bfloat16 hi/lo splits of both operands, the written keys' H += Phi^T V from the split Phi
+// and the (exact) bfloat16 values.  Otherwise (float32 io, or D = 64): CUDA cores, H in shared
+// memory, the candidates scored 64 at a time (a 64 x d_v product of their phi, staged
+// transposed, with H; each warp a 16-key x d_v/4-column tile of it) and the written keys
+// added in rank order by rank-1 FMAs, so that the float32 decisions match an exact-arithmetic
+// reference wherever their SREs differ at float32 resolution.
 #include "lola_chain.cuh"
 #include "lola_tc.cuh"
 

@@ -1,7 +1,7 @@
-// Blackwell (sm_100 family) tensor-core primitives used by the output kernel: TMEM
-// allocation, tcgen05.mma with shared-memory descriptors, commit to an mbarrier,
-// TMEM loads/stores, and the 128-byte-swizzled shared-memory layouts the descriptors
-// describe.  All written as inline PTX.
+// Blackwell (sm_100 family) tensor-core primitives used by the output and chunk-allocation
+// kernels: TMEM allocation, tcgen05.mma with shared-memory descriptors, commit to an
+// mbarrier, TMEM loads/stores, and the 128-byte-swizzled shared-memory layouts the
+// descriptors describe.  All written as inline PTX.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -35,7 +35,8 @@ __device__ __forceinline__ uint64_t sdesc(uint32_t addr, uint32_t lbo, uint32_t 
     d |= (uint64_t)2 << 61;
     return d;
 }
-// instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, A K-major
+// instruction descriptor, kind::f16: bf16 A and B, fp32 accumulator, A K-major (OR in
+// 1 << 15 for an MN-major A)
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn_major) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)b_mn_major << 16) | ((uint32_t)(N >> 3) << 17) |
            ((uint32_t)(M >> 4) << 24);
