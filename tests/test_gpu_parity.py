@@ -227,6 +227,7 @@ def test_read_mask_prefill_and_decode_match_oracle(L, dtype, d, mask):
 
 @pytest.mark.parametrize("dtype,d,eta,lam,chunk", [("f32", 64, 32, 24, 16), ("f32", 128, 32, 40, 16),
                                                    ("bf16", 128, 64, 64, 64), ("bf16", 128, 128, 32, 64),
+                                                   ("bf16", 128, 32, 40, 16), ("bf16", 128, 64, 200, 32),
                                                    ("bf16", 64, 16, 100, 16)])
 def test_chunk_alloc_prefill_matches_oracle(L, dtype, d, eta, lam, chunk):
     """Chunk-granular allocation (section 2.6, Eq. 15): the per-key write log equals the
