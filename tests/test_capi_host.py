@@ -156,6 +156,12 @@ def test_chunk_alloc_validation(lib):
         assert lib.lola_check_config(cfg) == lib.LOLA_ERR_INVALID_ARG, (eta, chunk, mask)
     assert lib.lola_check_config(lib.make_config(2, 4, 128, 128, 128, 64, 64, 64, "bf16", alloc=2)) == \
         lib.LOLA_ERR_INVALID_ARG
+    # the selection kernel's shared-memory plan fits the largest cache and chunk accepted, in both
+    # builds (tensor-core bf16 at D = 128, CUDA-core float32)
+    for dt in ("bf16", "f32"):
+        for D in (64, 128):
+            big = lib.make_config(1, 1, D, D, D, 256, 1024, 256, dt, alloc=C)
+            assert lib.lola_check_config(big) == 0, (dt, D)
     # the decode step is per token: refused for a chunk-mode layer before anything runs
     P = ctypes.c_void_p
     st = lib._lib.lola_decode_step(ctypes.byref(ok), P(256), P(256), 0, P(256), P(256), P(256), P(256), None, None)
