@@ -424,6 +424,23 @@ def test_chunk_mode_keeps_the_highest_sre_and_writes_each_key_once(C, eta, lam):
     np.testing.assert_allclose(o["s"], PK[wl].sum(axis=0), rtol=1e-12, atol=1e-12)
 
 
+def test_chunk_mode_value_scaling_and_shift():
+    """Chunk mode: V -> cV scales Y by c and keeps every decision; V -> V + b shifts Y by b and
+    keeps the decisions taken against a non-empty memory (the memory's read-out and every
+    co-normalised read are weighted averages of values).  b is small so that the one
+    empty-memory decision keeps its order."""
+    x = synth.gauss_inputs(1, 1, 96, 8, 8, "f32", seed=93, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    base = R.lola_chunk_run(q, k, v, x.W, 8, 6, 4)
+    sc = R.lola_chunk_run(q, k, 3.0 * v, x.W, 8, 6, 4)
+    assert np.array_equal(base["write_step"], sc["write_step"])
+    np.testing.assert_allclose(sc["Y"], 3.0 * base["Y"], rtol=1e-12, atol=1e-12)
+    b = 1e-3 * np.arange(1, 7)
+    sh = R.lola_chunk_run(q, k, v + b, x.W, 8, 6, 4)
+    assert np.array_equal(base["write_step"], sh["write_step"])
+    np.testing.assert_allclose(sh["Y"], base["Y"] + b, rtol=1e-11, atol=1e-11)
+
+
 def test_chunk_mode_needs_whole_window_chunks():
     x = synth.gauss_inputs(1, 1, 16, 8, 8, "f32", seed=90, dv=6)
     q, k, v = (x.widened(n)[0, 0] for n in "qkv")
