@@ -82,7 +82,12 @@ typedef struct {
  * a positive multiple of chunk and read_mask = 0; lola_prefill only (lola_decode_step
  * returns LOLA_ERR_UNSUPPORTED), and its write_pos log is per key: the chunk start at which
  * key j was written, -1 if never.  The exported state holds H, s, the cache positions and
- * rows and the window ring; the per-slot N, z and the next evictee's record stay zero. */
+ * rows and the window ring; the per-slot N, z and the next evictee's record stay zero.
+ * Precision: with bfloat16 io at D = d_v = 128 the candidates' H^T phi and the written keys'
+ * phi v^T are tensor-core products of bfloat16 hi + lo splits of the float32 operands (about
+ * 2^-16 relative; H, s and z = s^T phi accumulate in float32), so a decision can differ from
+ * an exact-arithmetic one only between candidates whose SREs agree to about that; float32 io
+ * and D = 64 score and write in float32 on the CUDA cores. */
 typedef enum { LOLA_ALLOC_TOKEN = 0, LOLA_ALLOC_CHUNK = 1 } lola_alloc;
 
 /* Read mask (appendix I, Table 12: a read-time ablation).  The cache and the state are
