@@ -39,6 +39,12 @@ Readings taken where the notes are silent (each is listed in the design notes):
   ``phi(q)^T s`` out of the read, bit 1 the cache's keys; the window is always read, and
   a nonzero mask needs eta >= 1 (then the window holds the current token).
 
+Diagnostics (not on the path): the SRE map (section 4.4, Fig. 3) -- every key's SRE against
+the memory at chosen state times, 0 for keys it does not hold -- and the relative map
+(appendix G, Fig. 10, Eq. 26): the SRE now minus the SRE at first write.  Reading taken for
+the latter's baseline: the SRE against the first memory that holds the key, i.e. the
+memory right after its write step (not the score it had just before the write).
+
 Three formulations live here and in ``lola_inc.c``: ``lola_run`` (running H, s; all
 SREs recomputed from H each step), ``lola_set`` (no running state: H is re-summed from
 the written set every step) and the C incremental form.  Tests check that they agree,
@@ -335,6 +341,39 @@ def sre_map(k, v, W, write_step, times):
         s = PK[held].sum(axis=0)
         for j in held:
             out[c, j] = math.sqrt(sre_sq(H, s, PK[j], v[j]))
+    return out
+
+
+def sre_at_first_write(k, v, W, write_step):
+    """SRE of every written key against the first memory that holds it (the notes' appendix
+    G, Eq. 26 baseline): the sums over the keys written at or before its own write step
+    (write_step[i] <= write_step[j]; with chunk-granular allocation that includes the keys
+    written at the same chunk start).  0 for keys never written."""
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    PK = phi(k, W)
+    ws = np.asarray(write_step)
+    out = np.zeros(k.shape[0])
+    for w in np.unique(ws[ws >= 0]):
+        held = np.flatnonzero((ws >= 0) & (ws <= w))
+        H = PK[held].T @ v[held]
+        s = PK[held].sum(axis=0)
+        for j in np.flatnonzero(ws == w):
+            out[j] = math.sqrt(sre_sq(H, s, PK[j], v[j]))
+    return out
+
+
+def sre_map_relative(k, v, W, write_step, times):
+    """The relative SRE map (the notes' appendix G, Fig. 10, Eq. 26): for every key held by
+    the memory at state time t = times[c], its SRE now minus its SRE at first write (a
+    difference, not a ratio); 0 for keys the memory does not hold."""
+    m = sre_map(k, v, W, write_step, times)
+    base = sre_at_first_write(k, v, W, write_step)
+    ws = np.asarray(write_step)
+    out = np.zeros_like(m)
+    for c, t in enumerate(times):
+        held = (ws >= 0) & (ws < t)
+        out[c, held] = m[c, held] - base[held]
     return out
 
 

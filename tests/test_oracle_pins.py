@@ -503,3 +503,61 @@ def test_sre_map_single_written_key_is_zero():
     k, v = x.widened("k")[0, 0], x.widened("v")[0, 0]
     m = R.sre_map(k, v, x.W, np.array([2, -1, -1, -1]), [2, 3])
     assert m[0, 0] == 0.0 and m[1, 0] == pytest.approx(0.0, abs=1e-12) and (m[:, 1:] == 0).all()
+
+
+def test_sre_at_first_write_is_the_rank_one_shrink_of_the_score():
+    """Writing (k, v) into (H, s) adds g v to H^T phi(k) and g to phi(k)^T s (g = |phi(k)|^2),
+    so its SRE right after the write is its score just before times z / (z + g) (0 into an
+    empty memory).  The baseline of the relative map (appendix G, Eq. 26) is checked against
+    that closed form, with the pre-write memory taken from the running oracle."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=97, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 4, 3)
+    base = R.sre_at_first_write(k, v, x.W, o["write_step"])
+    PK = R.phi(k, x.W)
+    written = np.flatnonzero(o["write_step"] >= 0)
+    assert written.size >= 10
+    for j in written:
+        w = int(o["write_step"][j])
+        pre = R.lola_run(q[:w], k[:w], v[:w], x.W, 4, 3)   # the memory before step w's write
+        z = float(PK[j] @ pre["s"])
+        g = float(PK[j] @ PK[j])
+        score = math.sqrt(R.sre_sq(pre["H"], pre["s"], PK[j], v[j]))
+        assert base[j] == pytest.approx(score * z / (z + g), rel=1e-10, abs=1e-13)
+    assert (base[o["write_step"] < 0] == 0).all()
+
+
+def test_sre_map_relative_is_zero_right_after_the_write_and_tracks_later_writes():
+    """Per token: at the time right after its write the relative SRE of a key is 0; later it
+    is the map's SRE minus that baseline.  Chunk mode: the keys written at one chunk start
+    share their first memory, so each one's baseline includes the others."""
+    x = synth.gauss_inputs(1, 1, 48, 8, 8, "f32", seed=98, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run(q, k, v, x.W, 4, 3)
+    ws = o["write_step"]
+    times = list(range(0, 49, 4))
+    rel = R.sre_map_relative(k, v, x.W, ws, times)
+    m = R.sre_map(k, v, x.W, ws, times)
+    base = R.sre_at_first_write(k, v, x.W, ws)
+    for j in np.flatnonzero(ws >= 0):
+        right_after = R.sre_map_relative(k, v, x.W, ws, [int(ws[j]) + 1])
+        assert right_after[0, j] == pytest.approx(0.0, abs=1e-12)
+        for c, t in enumerate(times):
+            expect = m[c, j] - base[j] if ws[j] < t else 0.0
+            assert rel[c, j] == pytest.approx(expect, abs=1e-12)
+    co = R.lola_chunk_run(q, k, v, x.W, 8, 6, 4)
+    cws = co["write_step"]
+    starts = np.unique(cws[cws >= 0])
+    multi = [c0 for c0 in starts if (cws == c0).sum() > 1]
+    assert multi, "no chunk start wrote more than one key"
+    PK = R.phi(k, x.W)
+    cbase = R.sre_at_first_write(k, v, x.W, cws)
+    for c0 in multi:
+        held = np.flatnonzero((cws >= 0) & (cws <= c0))
+        H, s = PK[held].T @ v[held], PK[held].sum(axis=0)
+        for j in np.flatnonzero(cws == c0):
+            assert cbase[j] == pytest.approx(math.sqrt(R.sre_sq(H, s, PK[j], v[j])), rel=1e-12)
+            alone = np.array([i for i in held if cws[i] < c0] + [j])
+            Ha, sa = PK[alone].T @ v[alone], PK[alone].sum(axis=0)
+            assert abs(cbase[j] - math.sqrt(R.sre_sq(Ha, sa, PK[j], v[j]))) > 1e-9
+
