@@ -39,6 +39,13 @@ Readings taken where the notes are silent (each is listed in the design notes):
   ``phi(q)^T s`` out of the read, bit 1 the cache's keys; the window is always read, and
   a nonzero mask needs eta >= 1 (then the window holds the current token).
 
+Scoring ablation (section 4.4, Table 4; appendix F, whose formulas the notes do not
+reproduce): ``lola_run_fixed_score`` runs the per-token rule with one of four
+query-dependent scores in place of the SRE, each accumulated while the key is in the window
+and frozen from its eviction on.  Readings taken: e = exp(q . k / sqrt(d_k)) and
+l = phi(q) . phi(k) are the two branches' unnormalised weights; the scores are sum (e - l)^2,
+sum |e - l|, sum l / e and sum e over the key's window queries; a larger score keeps the key.
+
 Diagnostics (not on the path): the SRE map (section 4.4, Fig. 3) -- every key's SRE against
 the memory at chosen state times, 0 for keys it does not hold -- and the relative map
 (appendix G, Fig. 10, Eq. 26): the SRE now minus the SRE at first write.  Reading taken for
@@ -169,6 +176,83 @@ def lola_run(q, k, v, W, eta: int, lam: int, replay=None, read_mask: int = 0):
     return dict(Y=Y, write_pos=write_pos, write_step=write_step, H=H, s=s,
                 cache=np.array(sorted(cache), np.int64), window=np.array(list(window), np.int64),
                 min_gap=min_gap, max_gap=max_gap, mismatches=mismatches)
+
+
+SCORE_KINDS = ("kernel_sq", "kernel_abs", "kernel_ratio", "attention")
+
+
+def window_scores(q, k, W, eta: int, kind: str):
+    """Query-dependent cache scores of the notes' scoring ablation (section 4.4, Table 4;
+    appendix F), accumulated while key j is in the window, i.e. over the queries of steps
+    t = j .. min(n, j + eta) - 1.  With e = exp(q_t . k_j / sqrt(d_k)) (the softmax branch's
+    weight) and l = phi(q_t) . phi(k_j) (the linear branch's weight):
+    kernel_sq = sum (e - l)^2, kernel_abs = sum |e - l|, kernel_ratio = sum l / e (large
+    when the linear kernel over-weights the key), attention = sum e.  A larger score keeps
+    the key exact."""
+    if kind not in SCORE_KINDS:
+        raise ValueError(f"unknown score {kind!r}")
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    n, dk = k.shape
+    PQ, PK = phi(q, W), phi(k, W)
+    scale = 1.0 / math.sqrt(dk)
+    out = np.zeros(n)
+    for j in range(n):
+        for t in range(j, min(n, j + eta)):
+            e = math.exp(float(q[t] @ k[j]) * scale)
+            lin = float(PQ[t] @ PK[j])
+            if kind == "kernel_sq":
+                out[j] += (e - lin) ** 2
+            elif kind == "kernel_abs":
+                out[j] += abs(e - lin)
+            elif kind == "kernel_ratio":
+                out[j] += lin / e
+            else:
+                out[j] += e
+    return out
+
+
+def lola_run_fixed_score(q, k, v, W, eta: int, lam: int, kind: str):
+    """The per-token rule with a query-dependent score in place of the SRE (the notes'
+    scoring ablation, section 4.4, Table 4).  Every key's score is complete when it leaves
+    the window (``window_scores``) and never changes after, so no rescoring happens: at each
+    eviction the candidates are the cache and the evictee, and when they exceed lambda the
+    one with the lowest (score, position) is written (the older among equal scores).  The
+    memory and the co-normalised read are those of ``lola_run``.  Returns the same keys
+    as ``lola_run`` (without the gap fields) plus ``score``."""
+    q = np.asarray(q, np.float64)
+    k = np.asarray(k, np.float64)
+    v = np.asarray(v, np.float64)
+    n, dk = k.shape
+    dv = v.shape[1]
+    if eta < 1:
+        raise ValueError("a query-dependent score needs eta >= 1 (the key's queries are read in the window)")
+    score = window_scores(q, k, W, eta, kind)
+    PQ, PK = phi(q, W), phi(k, W)
+    scale = 1.0 / math.sqrt(dk)
+    H = np.zeros((PK.shape[1], dv))
+    s = np.zeros(PK.shape[1])
+    window: deque[int] = deque()
+    cache: list[int] = []
+    write_pos = np.full(n, -1, np.int64)
+    write_step = np.full(n, -1, np.int64)
+    Y = np.zeros((n, dv))
+    for t in range(n):
+        window.append(t)
+        E = list(cache)
+        if len(window) > eta:
+            E.append(window.popleft())
+        if len(E) > lam:
+            w = min(E, key=lambda j: (score[j], j))
+            H += np.outer(PK[w], v[w])
+            s += PK[w]
+            write_pos[t] = w
+            write_step[w] = t
+            E = [j for j in E if j != w]
+        cache = E
+        Y[t] = _output(q[t], PQ[t], list(window) + cache, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
+    return dict(Y=Y, write_pos=write_pos, write_step=write_step, H=H, s=s, score=score,
+                cache=np.array(sorted(cache), np.int64), window=np.array(list(window), np.int64))
 
 
 def lola_set(q, k, v, W, eta: int, lam: int, read_mask: int = 0):

@@ -561,3 +561,80 @@ def test_sre_map_relative_is_zero_right_after_the_write_and_tracks_later_writes(
             Ha, sa = PK[alone].T @ v[alone], PK[alone].sum(axis=0)
             assert abs(cbase[j] - math.sqrt(R.sre_sq(Ha, sa, PK[j], v[j]))) > 1e-9
 
+
+
+# ---------------------------------------------------------------------------
+# Scoring ablation (section 4.4, Table 4): query-dependent scores in place of the SRE
+# ---------------------------------------------------------------------------
+
+def _top_lambda_write_steps(score, n, eta, lam):
+    """Set definition with a score that never changes: at step t the evicted keys are
+    {i : i + eta <= t}; the cache is the lam of them with the largest (score, position); a
+    key is written at the first step at which it is evicted but not among those."""
+    ws = np.full(n, -1, np.int64)
+    for t in range(n):
+        ev = [i for i in range(n) if i + eta <= t]
+        keep = set(sorted(ev, key=lambda i: (score[i], i))[max(0, len(ev) - lam):])
+        for i in ev:
+            if i not in keep and ws[i] < 0:
+                ws[i] = t
+    return ws
+
+
+@pytest.mark.parametrize("kind", ["kernel_sq", "kernel_abs", "kernel_ratio", "attention"])
+@pytest.mark.parametrize("eta,lam", [(4, 3), (1, 5), (6, 1)])
+def test_fixed_score_rule_keeps_the_top_lambda_of_the_evicted(kind, eta, lam):
+    """A frozen score makes the cache the lam highest-scored evicted keys at every step (the
+    incremental write-the-minimum rule equals the set definition), and (H, s) are the sums
+    over the written keys."""
+    x = synth.gauss_inputs(1, 1, 36, 8, 8, "f32", seed=101, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    o = R.lola_run_fixed_score(q, k, v, x.W, eta, lam, kind)
+    assert np.array_equal(o["write_step"], _top_lambda_write_steps(o["score"], 36, eta, lam))
+    wl = np.flatnonzero(o["write_step"] >= 0)
+    PK = R.phi(k, x.W)
+    np.testing.assert_allclose(o["H"], PK[wl].T @ v[wl], rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(o["s"], PK[wl].sum(axis=0), rtol=1e-12, atol=1e-12)
+
+
+def test_fixed_score_decisions_do_not_depend_on_values():
+    """The query-dependent scores read q and k only, so any other V gives the same write log
+    (unlike the SRE, which is a value reconstruction error)."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=102, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    other = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=103, dv=6).widened("v")[0, 0]
+    for kind in R.SCORE_KINDS:
+        a = R.lola_run_fixed_score(q, k, v, x.W, 4, 3, kind)
+        b = R.lola_run_fixed_score(q, k, other, x.W, 4, 3, kind)
+        assert np.array_equal(a["write_step"], b["write_step"]), kind
+
+
+def test_fixed_score_reductions():
+    """lambda = 0 writes every evictee at once, whatever the score: the SRE run's window +
+    linear result.  lambda >= n (nothing written): causal softmax attention."""
+    x = synth.gauss_inputs(1, 1, 30, 8, 8, "f32", seed=104, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    ref0 = R.lola_run(q, k, v, x.W, 5, 0)
+    full = R.causal_softmax_attention(q, k, v)
+    for kind in R.SCORE_KINDS:
+        o = R.lola_run_fixed_score(q, k, v, x.W, 5, 0, kind)
+        assert np.array_equal(o["write_step"], ref0["write_step"])
+        np.testing.assert_allclose(o["Y"], ref0["Y"], rtol=1e-12, atol=1e-12)
+        o = R.lola_run_fixed_score(q, k, v, x.W, 3, 30, kind)
+        assert (o["write_step"] < 0).all()
+        np.testing.assert_allclose(o["Y"], full, rtol=1e-11, atol=1e-12)
+
+
+def test_window_scores_of_a_key_seen_by_one_query():
+    """eta = 1: each key is read only by its own step's query, so its scores are those of
+    one (e, l) pair: e = exp(q_j . k_j / sqrt(d_k)), l = phi(q_j) . phi(k_j)."""
+    q = np.array([[1.0, 0.0], [0.5, -0.5]])
+    k = np.array([[2.0, 1.0], [0.0, 1.0]])
+    W = np.array([[1.0, 0.0]])
+    e = np.exp(np.array([2.0, -0.5]) / math.sqrt(2.0))
+    # phi(x) = [softmax(W x), softmax(-W x)] with one row: both halves are 1, so l = 2
+    assert np.allclose(R.phi(q, W), 1.0)
+    np.testing.assert_allclose(R.window_scores(q, k, W, 1, "attention"), e, rtol=1e-15)
+    np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_sq"), (e - 2.0) ** 2, rtol=1e-14)
+    np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_abs"), np.abs(e - 2.0), rtol=1e-14)
+    np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_ratio"), 2.0 / e, rtol=1e-15)
