@@ -581,16 +581,34 @@ def _top_lambda_write_steps(score, n, eta, lam):
     return ws
 
 
+def _closed_form_write_steps(score, n, eta, lam):
+    """Per key, with no steps simulated: j is written once it has been evicted and lam keys of
+    higher (score, position) have been evicted too, i.e. at step max(j, p) + eta with p the
+    lam-th smallest position among the higher keys (at j + eta when lam = 0); never if that
+    step is past the end or there are fewer than lam higher keys."""
+    ws = np.full(n, -1, np.int64)
+    for j in range(n):
+        higher = sorted(i for i in range(n) if (score[i], i) > (score[j], j))
+        if len(higher) < lam:
+            continue
+        p = higher[lam - 1] if lam > 0 else j
+        t = max(j, p) + eta
+        if t <= n - 1:
+            ws[j] = t
+    return ws
+
+
 @pytest.mark.parametrize("kind", ["kernel_sq", "kernel_abs", "kernel_ratio", "attention"])
 @pytest.mark.parametrize("eta,lam", [(4, 3), (1, 5), (6, 1)])
 def test_fixed_score_rule_keeps_the_top_lambda_of_the_evicted(kind, eta, lam):
     """A frozen score makes the cache the lam highest-scored evicted keys at every step (the
-    incremental write-the-minimum rule equals the set definition), and (H, s) are the sums
-    over the written keys."""
+    incremental write-the-minimum rule equals the set definition and the per-key closed
+    form), and (H, s) are the sums over the written keys."""
     x = synth.gauss_inputs(1, 1, 36, 8, 8, "f32", seed=101, dv=6)
     q, k, v = (x.widened(n)[0, 0] for n in "qkv")
     o = R.lola_run_fixed_score(q, k, v, x.W, eta, lam, kind)
     assert np.array_equal(o["write_step"], _top_lambda_write_steps(o["score"], 36, eta, lam))
+    assert np.array_equal(o["write_step"], _closed_form_write_steps(o["score"], 36, eta, lam))
     wl = np.flatnonzero(o["write_step"] >= 0)
     PK = R.phi(k, x.W)
     np.testing.assert_allclose(o["H"], PK[wl].T @ v[wl], rtol=1e-12, atol=1e-12)
