@@ -212,14 +212,17 @@ def window_scores(q, k, W, eta: int, kind: str):
     return out
 
 
-def lola_run_fixed_score(q, k, v, W, eta: int, lam: int, kind: str):
+def lola_run_fixed_score(q, k, v, W, eta: int, lam: int, kind: str, replay=None):
     """The per-token rule with a query-dependent score in place of the SRE (the notes'
     scoring ablation, section 4.4, Table 4).  Every key's score is complete when it leaves
     the window (``window_scores``) and never changes after, so no rescoring happens: at each
     eviction the candidates are the cache and the evictee, and when they exceed lambda the
     one with the lowest (score, position) is written (the older among equal scores).  The
-    memory and the co-normalised read are those of ``lola_run``.  Returns the same keys
-    as ``lola_run`` (without the gap fields) plus ``score``."""
+    memory and the co-normalised read are those of ``lola_run``.  ``replay``: an optional
+    (n,) per-key write step (-1: never) to follow instead of the own choice; a step whose
+    replayed write is not one of its candidates, or a write due with none replayed, raises.
+    Returns the same keys as ``lola_run`` plus ``score``; ``max_gap`` is the largest
+    (score_written - score_lowest) / |score_lowest| over the replayed decisions."""
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -237,13 +240,32 @@ def lola_run_fixed_score(q, k, v, W, eta: int, lam: int, kind: str):
     write_pos = np.full(n, -1, np.int64)
     write_step = np.full(n, -1, np.int64)
     Y = np.zeros((n, dv))
+    due = {}
+    if replay is not None:
+        for j, st in enumerate(np.asarray(replay)):
+            if st >= 0:
+                if int(st) in due:
+                    raise ValueError(f"replay writes two keys at step {int(st)}")
+                due[int(st)] = j
+    max_gap, mismatches = 0.0, 0
     for t in range(n):
         window.append(t)
         E = list(cache)
         if len(window) > eta:
             E.append(window.popleft())
+        if replay is not None and (t in due) != (len(E) > lam):
+            raise ValueError(f"replay and the capacity disagree on a write at step {t}")
         if len(E) > lam:
             w = min(E, key=lambda j: (score[j], j))
+            if replay is not None:
+                best, w = w, due[t]
+                if w not in E:
+                    raise ValueError(f"replay writes position {w} at step {t}, not a candidate")
+                if w != best:
+                    mismatches += 1
+                    sb = score[best]
+                    gap = (score[w] - sb) / abs(sb) if sb != 0 else (math.inf if score[w] != sb else 0.0)
+                    max_gap = max(max_gap, gap)
             H += np.outer(PK[w], v[w])
             s += PK[w]
             write_pos[t] = w
@@ -252,7 +274,8 @@ def lola_run_fixed_score(q, k, v, W, eta: int, lam: int, kind: str):
         cache = E
         Y[t] = _output(q[t], PQ[t], list(window) + cache, k, v, H.T @ PQ[t], float(PQ[t] @ s), scale)
     return dict(Y=Y, write_pos=write_pos, write_step=write_step, H=H, s=s, score=score,
-                cache=np.array(sorted(cache), np.int64), window=np.array(list(window), np.int64))
+                cache=np.array(sorted(cache), np.int64), window=np.array(list(window), np.int64),
+                max_gap=max_gap, mismatches=mismatches)
 
 
 def lola_set(q, k, v, W, eta: int, lam: int, read_mask: int = 0):

@@ -656,3 +656,31 @@ def test_window_scores_of_a_key_seen_by_one_query():
     np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_sq"), (e - 2.0) ** 2, rtol=1e-14)
     np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_abs"), np.abs(e - 2.0), rtol=1e-14)
     np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_ratio"), 2.0 / e, rtol=1e-15)
+
+
+def test_fixed_score_replay_of_own_and_of_a_swapped_log():
+    """Replaying the own log reproduces it with no gap; writing, at one decision, the lowest
+    kept key instead of the written one is followed and reported as their relative score
+    difference; a log that writes a non-candidate is refused."""
+    x = synth.gauss_inputs(1, 1, 40, 8, 8, "f32", seed=105, dv=6)
+    q, k, v = (x.widened(n)[0, 0] for n in "qkv")
+    own = R.lola_run_fixed_score(q, k, v, x.W, 4, 3, "attention")
+    rep = R.lola_run_fixed_score(q, k, v, x.W, 4, 3, "attention", replay=own["write_step"])
+    assert rep["max_gap"] == 0.0 and rep["mismatches"] == 0
+    np.testing.assert_array_equal(rep["Y"], own["Y"])
+    sc, ws = own["score"], own["write_step"]
+    # the last decision: its written key and the lowest key kept at that step
+    t = int(ws.max())
+    w = int(np.flatnonzero(ws == t)[0])
+    kept = [i for i in range(40) if i + 4 <= t and (ws[i] < 0 or ws[i] > t) and i != w]
+    kp = min(kept, key=lambda i: (sc[i], i))
+    log = ws.copy()
+    log[w], log[kp] = -1, t
+    sw = R.lola_run_fixed_score(q, k, v, x.W, 4, 3, "attention", replay=log)
+    assert sw["mismatches"] == 1
+    assert sw["max_gap"] == pytest.approx((sc[kp] - sc[w]) / abs(sc[w]), rel=1e-12)
+    bad = ws.copy()
+    bad[w], bad[int(np.flatnonzero(ws < 0)[-1])] = -1, t   # a key still in the window
+    with pytest.raises(ValueError):
+        R.lola_run_fixed_score(q, k, v, x.W, 4, 3, "attention", replay=bad)
+
