@@ -534,6 +534,26 @@ def cpu_baseline(x, w, read_mask: int = 0):
                       f"({tokens:g} token-equivalents in {dt:.2f} s)"}
 
 
+def cpu_baseline_chunk(x, w, heads: int = 16):
+    """The oracle's chunk-granular rule (one thread, float64) on the first `heads` heads of the
+    prefill workload (about 0.4-0.6 s per head)."""
+    import numpy as np
+    import synth
+    from oracle import lola_ref as Rf
+    heads = min(heads, w.B * w.Hh)
+    wide = (lambda a: synth.bf16_bits_to_f32(a).astype(np.float64)) if w.dtype == "bf16" else \
+        (lambda a: a.astype(np.float64))
+    t0 = time.perf_counter()
+    for i in range(heads):
+        b, h = divmod(i, w.Hh)
+        Rf.lola_chunk_run(wide(x.q[b, h]), wide(x.k[b, h]), wide(x.v[b, h]), x.W, w.eta, w.lam, w.chunk)
+    dt = time.perf_counter() - t0
+    tokens = heads * w.n / w.Hh
+    return {"value": tokens / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"chunk-granular rule on {heads} of {w.B * w.Hh} heads of {w.name}, full n={w.n} "
+                      f"({tokens:g} token-equivalents in {dt:.2f} s)"}
+
+
 def run_reference(args):
     R = Ranks()
     if R.rank != 0:
@@ -583,8 +603,8 @@ def main():
     w = pre["workload"]
     dec = None if args.no_decode or args.alloc == "chunk" else run_decode(L, R, args, pk)
     cpu = None
-    if R.rank == 0 and not args.no_cpu and args.alloc == "token":   # (the C oracle is per token)
-        cpu = cpu_baseline(pre["x"], w, args.read_mask)
+    if R.rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(pre["x"], w, args.read_mask) if args.alloc == "token" else cpu_baseline_chunk(pre["x"], w)
     if R.rank == 0:
         launches = pre["launches"] * 1
         line = {

@@ -64,3 +64,15 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     monkeypatch.setattr(sys, "argv", ["bench.py", "--impl", "reference", "--gpus", "2", "--steps", "1"])
     assert bench.run_reference(bench.parse_args()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_chunk_mode_cpu_baseline_times_the_oracle_rule():
+    """The chunk-mode line's CPU baseline runs the oracle's chunk-granular rule on a bounded
+    sample of heads and reports token-equivalents per second on one thread."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import synth
+    w = synth.Workload("tiny_chunk", 1, 2, 96, 8, 8, 16, 8, 16, "bf16", "gauss")
+    x = synth.make_inputs(w)
+    cpu = bench.cpu_baseline_chunk(x, w, heads=3)
+    assert cpu["kind"] == "oracle" and cpu["cores"] == 1 and cpu["unit"] == "tokens/s"
+    assert cpu["value"] > 0 and "2 of 2 heads" in cpu["sample"]
