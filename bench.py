@@ -1,13 +1,27 @@
 #!/usr/bin/env python
 """Benchmark of the LoLA hybrid-attention hot path on one GB300 (or N, one process each).
 
-One step = one lola_prefill over the workload the metric is quoted on: 4 sequences x 32
-heads, n = 4096, d = D = 128, eta = lambda = 64, C = 64, bf16 inputs (K rows normalised to
-norm sqrt(128)); inputs (402 MB) exceed the 129 MB L2.  `value` is prefill tokens/s per
-layer (B * n / step time, summed over ranks).  The decode workload (64 x 32 heads, state
-prefilled from a 4096-token prefix, then single-token steps) is timed in the same run and
-reported under "decode".  Each rank runs its own replica (weak scaling, no collective
-on the data path).
+One step = one lola_prefill over the long-prefill workload: 1 sequence x 8 heads, n = 131072,
+d = D = 128, eta = lambda = 512, C = 256, bf16 inputs drawn from a per-channel AR(1) process
+(rho = 0.9); the inputs (805 MB) exceed the 129 MB L2, so no flush is needed between steps.
+`value` is prefill tokens/s per layer (B * n / step time, summed over ranks).
+
+Beside it, in the same line:
+  * `roofline`: the prefill's contraction flops (per head-token: phi of q and k, the softmax
+    branch over eta + lambda keys, the linear read, the write, the evictee's SRE and one Gram
+    row) over the whole step time, against the measured bf16 tensor-core peak; `kernels`
+    carries each kernel's own roofline (the chain against the FP32 CUDA-core peak derived
+    from unit counts and clock, the output pass against the bf16 peak, phi(K) against HBM);
+  * `prefill_more`: the same measurement on the other prefill workloads (4 x 32 heads at
+    n = 4096; 32 heads at n = 16384 with planted needle keys; the float32 head at n = 1024);
+  * `decode`: 64 x 32 heads whose state was prefilled from a 4096-token prefix, then all
+    1024 single-token steps, timed as whole passes from the restored post-prefix state;
+  * `e2e`: the same prefill through the C ABI from pinned host buffers, copies included;
+  * `cpu_baseline`: the float64 C oracle on a stated sample of the workload.
+
+With N processes (torchrun) the global batch is N blocks of B sequences, block r drawn with
+seed + r; rank r takes the contiguous slice of heads [r B Hh, (r + 1) B Hh) -- its block -- so
+per-GPU work is fixed as N grows (weak scaling) and no data crosses GPUs.
 
 --impl reference times the CPU float64 oracle on a bounded sample of the same workload.
 """
@@ -28,22 +42,31 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "prefill & decode tokens/s per layer on 1 GB300; % of tensor/HBM roofline"
-PREFILL = "w2_bf16_b4h32_n4096"
+PREFILL = "w5_bf16_h8_n131072_ar1"
+MORE_PREFILL = ("w2_bf16_b4h32_n4096", "w3_bf16_h32_n16384_needle", "w1_f32_n1024")
 DECODE = "w4_bf16_decode_b64h32"
+# timed steps of the other prefill workloads (a fraction of a second each)
+MORE_STEPS = {"w2_bf16_b4h32_n4096": 20, "w3_bf16_h32_n16384_needle": 10, "w1_f32_n1024": 20}
+# tokens of each head the CPU oracle baseline runs (the sample), per prefill workload
+CPU_SAMPLE_TOKENS = 16384
 
 
-def parse_args():
+def parse_args(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--steps", type=int, default=5)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="lola", choices=["lola", "reference"])
-    p.add_argument("--decode-steps", type=int, default=64, help="timed decode steps")
+    p.add_argument("--workload", default=PREFILL, help="prefill workload of the headline value")
+    p.add_argument("--decode-passes", type=int, default=2,
+                   help="timed decode passes (each: every decode step of the workload from the post-prefix state)")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-more", action="store_true", help="skip the other prefill workloads")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--decode-only", action="store_true", help="skip the prefill measurement")
     p.add_argument("--decode-batch", type=int, default=None, help="batch of the decode workload (profiling)")
+    p.add_argument("--decode-steps", type=int, default=None, help="decode steps per pass (profiling)")
     p.add_argument("--read-mask", type=int, default=0, choices=[0, 1, 2, 3],
                    help="read mask of the layer (1: state hidden, 2: cache hidden, 3: both)")
     p.add_argument("--sre-map", action="store_true",
@@ -51,7 +74,7 @@ def parse_args():
     p.add_argument("--alloc", default="token", choices=["token", "chunk"],
                    help="allocation granularity of the prefill (chunk: the chunk-granular variant; "
                         "no decode line, the decode step is per token)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 # ---------------------------------------------------------------------------------------
@@ -60,8 +83,8 @@ def parse_args():
 
 class Ranks:
     """One process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE).  The path shards by
-    (batch, head) with no data-path exchange, so N > 1 runs N replicas: a barrier brackets the
-    timed region and the time is the maximum over ranks."""
+    (batch, head) with no data-path exchange: rank r runs its own block of sequences (see
+    head_slice); a barrier brackets the timed region and the time is the maximum over ranks."""
 
     def __init__(self):
         self.world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -100,10 +123,48 @@ class Ranks:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         return float(t.item())
 
+    def gather_heads(self, local, total_heads: int):
+        """Reassembles per-rank head slices (numpy arrays whose first axis is this rank's
+        heads, head_slice order) into the whole [total_heads, ...] array on every rank.
+        Used off the timed path (checks), never between kernels."""
+        import numpy as np
+        if not self.pg:
+            return local
+        import torch
+        import torch.distributed as dist
+        lo, hi = head_slice(total_heads, self.world, self.rank)
+        assert local.shape[0] == hi - lo
+        per = -(-total_heads // self.world)
+        dev = "cpu" if self.cpu else "cuda"
+        buf = torch.zeros((per,) + local.shape[1:], dtype=torch.from_numpy(local[:0]).dtype, device=dev)
+        buf[: hi - lo] = torch.from_numpy(np.ascontiguousarray(local)).to(dev)
+        parts = [torch.empty_like(buf) for _ in range(self.world)]
+        dist.all_gather(parts, buf)
+        out = []
+        for r, t in enumerate(parts):
+            a, b = head_slice(total_heads, self.world, r)
+            out.append(t[: b - a].cpu().numpy())
+        return np.concatenate(out, axis=0)
+
     def close(self):
         if self.pg:
             import torch.distributed as dist
             dist.destroy_process_group()
+
+
+def head_slice(total_heads: int, world: int, rank: int) -> tuple[int, int]:
+    """Contiguous slice [lo, hi) of the global heads owned by `rank`: the first
+    total_heads % world ranks take one head more; every head is owned exactly once."""
+    base, extra = divmod(total_heads, world)
+    lo = rank * base + min(rank, extra)
+    return lo, lo + base + (1 if rank < extra else 0)
+
+
+def rank_inputs(w, rank: int):
+    """This rank's block of the global batch: B sequences drawn with seed w.seed + rank
+    (global heads [rank B Hh, (rank + 1) B Hh), the head_slice of rank over world B Hh heads)."""
+    import synth
+    return synth.make_inputs(w, seed=w.seed + rank)
 
 
 def whole_job_value(world: int, units_per_rank: float, ms_max: float) -> float:
@@ -177,17 +238,15 @@ class Clocks:
 
 
 # DRAM traffic per launch (dram__bytes_read.sum + dram__bytes_write.sum) from one ncu capture of
-# the kernel on the workload named beside it, valid only for the kernel sources it was taken
-# on: the digest of those files must match, otherwise the traffic is reported as null.
+# a kernel on the workload named in the key, valid only for the kernel sources it was taken on:
+# the digest of those files must match, otherwise the traffic is reported as null.
 CSRC = os.path.join(ROOT, "sparse_exact_kv_gb300", "csrc")
 NCU_TRAFFIC = {
-    # w2 prefill (4 x 32 heads, n = 4096): mean of 3 select launches
-    "select": {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "8ef752573e82a0a9",
-               "bytes_per_launch": 409638656 + 132049067},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
-    "decode": {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"], "digest": "850fe64c2562ac87",
-               "bytes_per_launch": 2 * (206851584 + 56466483)},
+    ("decode", "w4_bf16_decode_b64h32"): {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"],
+                                          "digest": "850fe64c2562ac87",
+                                          "bytes_per_launch": 2 * (206851584 + 56466483)},
 }
 
 
@@ -199,8 +258,8 @@ def sources_digest(files) -> str:
     return h.hexdigest()[:16]
 
 
-def traffic(kernel: str):
-    e = NCU_TRAFFIC.get(kernel)
+def traffic(kernel: str, workload: str):
+    e = NCU_TRAFFIC.get((kernel, workload))
     if not e or sources_digest(e["sources"]) != e["digest"]:
         return None
     return e["bytes_per_launch"]
@@ -222,14 +281,19 @@ def peaks(sm_count: int):
 
 
 # ---------------------------------------------------------------------------------------
-# algorithmic work (per head-token), stated in the design notes
+# algorithmic work per head-token (steady state: every query sees eta + lambda exact keys and
+# every step writes one key), as the design notes state it
 # ---------------------------------------------------------------------------------------
 
-def select_flops_per_step(D, dv, lam):
-    """Allocation chain per step (steady state): the evictee's H^T phi (2 D dv), the rank-1
-    write of H (2 D dv), one Gram row phi_w . phi_i (2 lambda D), the N update of every
-    candidate (2 lambda dv) and the SRE of the lambda + 1 candidates (4 (lambda + 1) dv)."""
-    return 2 * D * dv + 2 * D * dv + 2 * lam * D + 2 * lam * dv + 4 * (lam + 1) * dv
+def contraction_flops(d, D, eta, lam):
+    """The prefill's contraction flops per head-token, by term: the feature map of q and k
+    (2 D d: W has D/2 rows), the softmax branch over eta + lambda keys (2 (eta + lambda)
+    (d_k + d_v)), the linear read H^T phi(q), phi(q)^T s (2 D d_v + 2 D), the write
+    phi v^T, phi (2 D d_v + D), the evictee's H^T phi and s^T phi (2 D d_v + 2 D) and one
+    Gram row phi_w . phi_i over the cache (2 lambda D).  The lambda N / z refreshes and SREs
+    (about 3 lambda d_v FMAs per step) are CUDA-core work, not counted."""
+    return {"phi": 2 * D * d, "soft": 2 * (eta + lam) * (d + d), "read": 2 * D * d + 2 * D,
+            "write": 2 * D * d + D, "sre_new": 2 * D * d + 2 * D, "gram": 2 * lam * D}
 
 
 def chunk_select_flops_per_chunk(D, dv, lam, C):
@@ -240,16 +304,16 @@ def chunk_select_flops_per_chunk(D, dv, lam, C):
     return 2 * P * D * dv + 2 * P * D + 4 * P * dv + C * (2 * D * dv + D)
 
 
-def output_flops_per_token(dk, dv, D, eta, lam):
-    """Co-normalised read per query: softmax branch over eta + lambda exact keys
-    (2 (eta + lambda)(dk + dv)) and the linear read H^T phi(q), phi(q)^T s (2 D dv + 2 D)."""
-    return 2 * (eta + lam) * (dk + dv) + 2 * D * dv + 2 * D
-
-
 def decode_bytes_per_head(d, D, eta, lam, io=2):
     """Algorithmic HBM bytes of one decode step of one head: H read + write, s read + write,
     the eta + lambda exact KV read, q, k, v in and y out, and the new KV written."""
     return 2 * 4 * D * d + 2 * 4 * D + (eta + lam) * 2 * d * io + 4 * d * io + 2 * d * io
+
+
+def phi_k_bytes_per_row(d, D, io):
+    """Algorithmic HBM bytes of phi(K) per key row: the row read, phi(k) written once in
+    float32 (the selection's precision)."""
+    return d * io + 4 * D
 
 
 # ---------------------------------------------------------------------------------------
@@ -315,15 +379,144 @@ def traced_kernel_times(L, R, step, steps, stream, names):
     return kernel_times(L, names)
 
 
-def run_prefill(L, R, args, pk):
+def prefill_rooflines(w, kt, ms, pk, alloc="token"):
+    """The step's roofline (contraction flops over the whole step time against the measured
+    bf16 peak) and each kernel's own."""
+    heads = w.B * w.Hh
+    ht = heads * w.n
+    io = 2 if w.dtype == "bf16" else 4
+    cf = contraction_flops(w.d, w.D, w.eta, w.lam)
+    per_ht = sum(cf.values())
+    ach = ht * per_ht / (ms / 1e3) / 1e12
+    step = {"kernel": "prefill step (all kernels)", "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
+            "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None,
+            "flop_per_head_token": per_ht, "flop_terms": cf, "head_tokens": ht, "ms": ms,
+            "peak_source": f"{pk['source']} cuBLAS bf16 (burst)"}
+    tr = [traffic(k, w.name) for k in ("phi", "phi_q", "select", "output")]
+    if all(t is not None for t in tr):
+        step["traffic"] = sum(tr)
+    per = {}
+    sel = kt.get("select")
+    if sel and alloc == "token":
+        f = cf["sre_new"] + cf["write"] + cf["gram"]
+        a_ = ht * f / (sel["avg_ms"] / 1e3) / 1e12
+        per["select"] = {"bound": "alu", "achieved": a_, "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
+                         "frac": a_ / pk["fp32_tflops"], "flop_per_head_token": f, "avg_ms": sel["avg_ms"],
+                         "traffic": traffic("select", w.name),
+                         "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+    elif sel:
+        nch = heads * max(0, w.n // w.chunk - w.eta // w.chunk)
+        fl = nch * chunk_select_flops_per_chunk(w.D, w.d, w.lam, w.chunk)
+        a_ = fl / (sel["avg_ms"] / 1e3) / 1e12
+        P = w.lam + w.chunk
+        executed = nch * 2 * (3 * P * w.D * w.d + 2 * w.chunk * w.D * w.d)
+        per["select"] = {"bound": "tensor", "achieved": a_, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac": a_ / pk["bf16_tflops"], "avg_ms": sel["avg_ms"], "traffic": None,
+                         "executed_tensor_tflops": executed / (sel["avg_ms"] / 1e3) / 1e12,
+                         "peak_source": f"{pk['source']} cuBLAS bf16 (burst)"}
+    out = kt.get("output")
+    if out:
+        f = cf["soft"] + cf["read"]
+        a_ = ht * f / (out["avg_ms"] / 1e3) / 1e12
+        tc = w.dtype == "bf16"
+        pkv = pk["bf16_tflops"] if tc else pk["fp32_tflops"]
+        per["output"] = {"bound": "tensor" if tc else "alu", "achieved": a_, "peak": pkv, "unit": "TFLOP/s",
+                         "frac": a_ / pkv, "flop_per_head_token": f, "avg_ms": out["avg_ms"],
+                         "traffic": traffic("output", w.name)}
+    phi = kt.get("phi")
+    if phi:
+        byts = ht * phi_k_bytes_per_row(w.d, w.D, io)
+        a_ = byts / (phi["avg_ms"] / 1e3) / 1e9
+        per["phi_k"] = {"bound": "hbm", "achieved": a_, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": a_ / pk["hbm_gbs"], "bytes_per_launch": byts, "avg_ms": phi["avg_ms"],
+                        "traffic": traffic("phi", w.name)}
+    return step, per
+
+
+def e2e_prefill(L, R, lay, w, Q, K, V, Y, W, wpos, ws, stream, steps):
+    """End to end through the C ABI: every step's Q, K, V copied in from pinned host memory
+    and its Y copied back to pinned host memory.  The copies run on one copy stream per
+    direction into a second set of device buffers, so step i + 1's inputs travel while step i
+    computes (double buffering); the timed region spans from before the first copy to after
+    the last read-back."""
+    import torch
+    dev = Q.device
+    hq, hk, hv = (t.cpu().pin_memory() for t in (Q, K, V))
+    hy = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+    bufs = [(Q, K, V, Y), tuple(torch.empty_like(t) for t in (Q, K, V, Y))]
+    cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    copied = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    read = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def h2d(b):
+        with torch.cuda.stream(cin):
+            cin.wait_event(done[b])         # the compute that last read buffer b
+            for dst, src in zip(bufs[b][:3], (hq, hk, hv)):
+                dst.copy_(src, non_blocking=True)
+            copied[b].record(cin)
+
+    def compute(b):
+        stream.wait_event(copied[b])
+        stream.wait_event(read[b])          # the copy-out of buffer b's previous output
+        q_, k_, v_, y_ = bufs[b]
+        L.lola_prefill(lay.cfg, w.n, q_, k_, v_, W, 0, y_, lay.state, wpos, ws, stream)
+        done[b].record(stream)
+
+    def d2h(b):
+        with torch.cuda.stream(cout):
+            cout.wait_event(done[b])
+            hy.copy_(bufs[b][3], non_blocking=True)
+            read[b].record(cout)
+
+    def pipeline(nsteps):
+        start = torch.cuda.Event(enable_timing=True)
+        end = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        start.record(stream)
+        cin.wait_event(start)
+        cout.wait_event(start)
+        for b in (0, 1):
+            read[b].record(cout)
+            done[b].record(stream)
+        h2d(0)
+        for i in range(nsteps):
+            b = i % 2
+            if i + 1 < nsteps:
+                h2d(1 - b)
+            compute(b)
+            d2h(b)
+        stream.wait_stream(cin)
+        stream.wait_stream(cout)
+        end.record(stream)
+        torch.cuda.synchronize()
+        return start.elapsed_time(end)
+
+    pipeline(2)
+    R.barrier()
+    ems = R.max(pipeline(steps)) / steps
+    tokens = w.B * w.n
+    out = {"value": whole_job_value(R.world, tokens, ems), "unit": "tokens/s", "ms_per_step": ems,
+           "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(), "d2h_bytes_per_step": Y.numel() * Y.element_size(),
+           "overlap": "step i+1's inputs are copied in while step i computes and step i-1's output "
+                      "is copied out (two device buffers, one copy stream per direction)"}
+    del bufs
+    return out
+
+
+PREFILL_KERNELS = ["state_init", "phi", "phi_q", "select", "output"]
+
+
+def run_prefill(L, R, args, pk, name, steps, warmup, e2e=True, sre_map=False):
     import torch
     import synth
-    w = synth.WORKLOADS[PREFILL]
-    x = synth.make_inputs(w)
+    w = synth.WORKLOADS[name]
+    x = rank_inputs(w, R.rank)
     dev = torch.device("cuda", R.local)
     Q, K, V = (dev_tensor(getattr(x, a), w.dtype, dev) for a in "qkv")
     W = torch.from_numpy(x.W).to(dev)
-    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev,
+    lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk,
+                 dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float32, device=dev,
                  read_mask=args.read_mask, alloc=L.LOLA_ALLOC_CHUNK if args.alloc == "chunk" else L.LOLA_ALLOC_TOKEN)
     ws = lay.workspace_for(w.n)
     Y = torch.empty_like(V)
@@ -333,133 +526,57 @@ def run_prefill(L, R, args, pk):
     def step():
         L.lola_prefill(lay.cfg, w.n, Q, K, V, W, 0, Y, lay.state, wpos, ws, stream)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     with Clocks(R.local) as clk:
         R.barrier()
-        ms = time_loop(step, args.steps, stream)
+        ms = time_loop(step, steps, stream)
         R.barrier()
-    kt = traced_kernel_times(L, R, step, args.steps, stream, ["state_init", "phi", "select", "output"])
-    sre = sre_map_timing(L, lay, w, V, ws, stream, pk) if args.sre_map else None
-    ms = R.max(ms) / args.steps
+    kt = traced_kernel_times(L, R, step, steps, stream, PREFILL_KERNELS)
+    ms = R.max(ms) / steps
     tokens = w.B * w.n
-    res = {"workload": w, "ms": ms, "value": whole_job_value(R.world, tokens, ms), "kernels": kt, "clocks": clk.summary(),
-           "launches": sum(v["launches"] for v in kt.values()), "sre_map": sre}
-    heads = w.B * w.Hh
-    sel = kt.get("select")
-    if sel:
-        if args.alloc == "chunk":   # chunk starts that score (the first eta / C only fill the window)
-            fl = heads * max(0, w.n // w.chunk - w.eta // w.chunk) * chunk_select_flops_per_chunk(w.D, w.d, w.lam,
-                                                                                                  w.chunk)
-        else:
-            fl = heads * w.n * select_flops_per_step(w.D, w.d, w.lam)
-        ach = fl / (sel["avg_ms"] / 1e3) / 1e12
-        if args.alloc == "chunk" and w.dtype == "bf16" and w.D == 128 and w.d == 128:
-            # the candidates' products and the H update run on the tensor cores as split-bf16
-            # passes (3 for the scoring, 2 for the write); the bound is the bf16 tensor peak
-            nch = heads * max(0, w.n // w.chunk - w.eta // w.chunk)
-            P = w.lam + w.chunk
-            executed = nch * 2 * (3 * P * w.D * w.d + 2 * w.chunk * w.D * w.d)
-            res["roofline"] = {"kernel": "select", "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops"],
-                               "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops"], "traffic": None,
-                               "peak_source": "measured cuBLAS bf16 (burst)",
-                               "executed_tensor_tflops": executed / (sel["avg_ms"] / 1e3) / 1e12}
-        else:
-            res["roofline"] = {"kernel": "select", "bound": "alu", "achieved": ach, "peak": pk["fp32_tflops"],
-                               "unit": "TFLOP/s", "frac": ach / pk["fp32_tflops"],
-                               "traffic": traffic("select") if args.alloc == "token" else None,
-                               "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
-    out = kt.get("output")
-    if out:
-        fl = heads * w.n * output_flops_per_token(w.d, w.d, w.D, w.eta, w.lam)
-        ach = fl / (out["avg_ms"] / 1e3) / 1e12
-        out["achieved_tflops"] = ach
-        out["frac_of_bf16_peak"] = ach / pk["bf16_tflops"]
-    phi = kt.get("phi")
-    if phi:
-        byts = heads * w.n * (w.d * 2 + w.D * 4)
-        phi["achieved_gbs"] = byts / (phi["avg_ms"] / 1e3) / 1e9
-    # end to end through the C ABI: every step's Q, K, V copied in from pinned host memory and
-    # its Y copied back to pinned host memory.  The copies run on a copy stream into a second
-    # set of device buffers, so step i + 1's inputs travel while step i computes (double
-    # buffering); the timed region spans from before the first copy to after the last read-back.
-    if not args.no_e2e:
-        hq, hk, hv = (t.cpu().pin_memory() for t in (Q, K, V))
-        hy = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
-        bufs = [(Q, K, V, Y), tuple(torch.empty_like(t) for t in (Q, K, V, Y))]
-        # inputs in and outputs out on two copy streams, so the two directions of the link
-        # run at once
-        cin, cout = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        copied = [torch.cuda.Event(), torch.cuda.Event()]
-        done = [torch.cuda.Event(), torch.cuda.Event()]
-        read = [torch.cuda.Event(), torch.cuda.Event()]
-
-        def h2d(b):
-            with torch.cuda.stream(cin):
-                cin.wait_event(done[b])         # the compute that last read buffer b
-                for dst, src in zip(bufs[b][:3], (hq, hk, hv)):
-                    dst.copy_(src, non_blocking=True)
-                copied[b].record(cin)
-
-        def compute(b):
-            stream.wait_event(copied[b])
-            stream.wait_event(read[b])          # the copy-out of buffer b's previous output
-            q_, k_, v_, y_ = bufs[b]
-            L.lola_prefill(lay.cfg, w.n, q_, k_, v_, W, 0, y_, lay.state, wpos, ws, stream)
-            done[b].record(stream)
-
-        def d2h(b):
-            with torch.cuda.stream(cout):
-                cout.wait_event(done[b])
-                hy.copy_(bufs[b][3], non_blocking=True)
-                read[b].record(cout)
-
-        def pipeline(nsteps):
-            start = torch.cuda.Event(enable_timing=True)
-            end = torch.cuda.Event(enable_timing=True)
-            torch.cuda.synchronize()
-            start.record(stream)
-            cin.wait_event(start)
-            cout.wait_event(start)
-            for b in (0, 1):
-                read[b].record(cout)
-                done[b].record(stream)
-            h2d(0)
-            for i in range(nsteps):
-                b = i % 2
-                if i + 1 < nsteps:
-                    h2d(1 - b)
-                compute(b)
-                d2h(b)
-            stream.wait_stream(cin)
-            stream.wait_stream(cout)
-            end.record(stream)
-            torch.cuda.synchronize()
-            return start.elapsed_time(end)
-
-        pipeline(2)
-        R.barrier()
-        ems = R.max(pipeline(args.steps)) / args.steps
-        res["e2e"] = {"value": whole_job_value(R.world, tokens, ems), "unit": "tokens/s", "ms_per_step": ems,
-                      "h2d_bytes_per_step": 3 * Q.numel() * Q.element_size(),
-                      "d2h_bytes_per_step": Y.numel() * Y.element_size(),
-                      "overlap": "step i+1's inputs are copied in while step i computes and step i-1's output "
-                                 "is copied out (two device buffers, one copy stream per direction)"}
+    in_bytes = 3 * Q.numel() * Q.element_size()
+    roof, per = prefill_rooflines(w, kt, ms, pk, args.alloc)
+    res = {"workload": w, "ms": ms, "value": whole_job_value(R.world, tokens, ms), "kernels": kt,
+           "clocks": clk.summary(), "launches_per_step": sum(v["launches"] for v in kt.values()) / steps,
+           "roofline": roof, "kernel_rooflines": per,
+           "l2": (f"inputs {in_bytes / 1e6:.0f} MB > 129 MB L2, no flush" if in_bytes > 129e6 else
+                  f"inputs {in_bytes / 1e6:.1f} MB fit in L2 and are not flushed (small case)")}
+    if sre_map:
+        res["sre_map"] = sre_map_timing(L, lay, w, V, ws, stream, pk)
+    if e2e:
+        res["e2e"] = e2e_prefill(L, R, lay, w, Q, K, V, Y, W, wpos, ws, stream, steps)
     res["x"] = x
     return res
 
 
+def summarize_prefill(p):
+    w = p["workload"]
+    return {"workload": w.name, "value": p["value"], "unit": "tokens/s", "ms_per_step": p["ms"],
+            "dtype": w.dtype, "config": workload_config(w), "roofline": p["roofline"],
+            "kernels": {k: {**v, **p["kernel_rooflines"].get(k if k != "phi" else "phi_k", {})}
+                        for k, v in p["kernels"].items()},
+            "clocks": p["clocks"], **({"e2e": p["e2e"]} if p.get("e2e") else {})}
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta, "lambda": w.lam,
+            "chunk": w.chunk, "inputs": w.kind}
+
+
 def run_decode(L, R, args, pk):
+    """The decode workload: the state is prefilled from the prefix, saved, and every timed pass
+    restores it and runs all decode steps of the workload (one lola_decode_step per token)."""
     import torch
     import synth
     w = synth.WORKLOADS[DECODE]
     if args.decode_batch:
-        w = dataclasses.replace(w, B=args.decode_batch, decode_steps=args.warmup + args.decode_steps)
-    x = synth.make_inputs(w)
+        w = dataclasses.replace(w, B=args.decode_batch)
+    if args.decode_steps:
+        w = dataclasses.replace(w, decode_steps=args.decode_steps)
+    x = rank_inputs(w, R.rank)
     dev = torch.device("cuda", R.local)
-    # the timed steps, then as many again with per-kernel tracing (each step advances the state)
-    steps = min(args.decode_steps, (w.decode_steps - args.warmup) // 2)
     lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk, dtype=torch.bfloat16, device=dev,
                  read_mask=args.read_mask)
     W = torch.from_numpy(x.W).to(dev)
@@ -469,68 +586,81 @@ def run_decode(L, R, args, pk):
     del P
     lay.workspace = None
     torch.cuda.empty_cache()
-    nt = args.warmup + 2 * steps
-    dq, dk, dv = (dev_tensor(getattr(x, a)[:, :, w.n:w.n + nt].transpose(2, 0, 1, 3), w.dtype, dev) for a in "qkv")
+    saved = lay.state.clone()
+    m = w.decode_steps
+    dq, dk, dv = (dev_tensor(getattr(x, a)[:, :, w.n:w.n + m].transpose(2, 0, 1, 3), w.dtype, dev) for a in "qkv")
     y = torch.empty(w.B, w.Hh, w.d, dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
-    it = [0]
 
-    def step():
-        i = it[0]
-        L.lola_decode_step(lay.cfg, lay.state, W, 0, dq[i], dk[i], dv[i], y, None, stream)
-        it[0] += 1
+    def one_pass():
+        for i in range(m):
+            L.lola_decode_step(lay.cfg, lay.state, W, 0, dq[i], dk[i], dv[i], y, None, stream)
 
-    for _ in range(args.warmup):
-        step()
+    def restore():
+        lay.state.copy_(saved)
+
+    for _ in range(max(1, args.warmup // 2)):
+        restore()
+        one_pass()
     torch.cuda.synchronize()
+    total = 0.0
     with Clocks(R.local) as clk:
         R.barrier()
-        ms = time_loop(step, steps, stream)
+        for _ in range(args.decode_passes):
+            restore()
+            total += time_loop(one_pass, 1, stream)
         R.barrier()
-    kt = traced_kernel_times(L, R, step, steps, stream, ["phi", "decode"])
-    ms = R.max(ms) / steps
+    restore()
+    kt = traced_kernel_times(L, R, one_pass, 1, stream, ["phi", "decode"])
+    ms = R.max(total / args.decode_passes) / m          # per decode step
     heads = w.B * w.Hh
     res = {"metric": "decode tokens/s per layer", "value": whole_job_value(R.world, w.B, ms), "unit": "tokens/s",
-           "ms_per_step": ms, "steps": steps,
+           "ms_per_step": ms, "steps_per_pass": m, "passes": args.decode_passes,
            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "d": w.d, "D": w.D, "eta": w.eta, "lambda": w.lam,
-                      "prefix": w.n, "state_bytes": lola_state_bytes(L, lay), "read_mask": args.read_mask},
+                      "prefix": w.n, "state_bytes": L.lola_state_bytes(lay.cfg), "read_mask": args.read_mask,
+                      "l2": f"state {L.lola_state_bytes(lay.cfg) / 1e6:.0f} MB > 129 MB L2, no flush"},
            "kernels": kt, "clocks": clk.summary(), "gpu_launches": sum(v["launches"] for v in kt.values())}
     dk_ = kt.get("decode")
     if dk_:
         byts = heads * decode_bytes_per_head(w.d, w.D, w.eta, w.lam)
         ach = byts / (dk_["avg_ms"] / 1e3) / 1e9
         res["roofline"] = {"kernel": "decode", "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                           "frac": ach / pk["hbm_gbs"], "traffic": traffic("decode"),
-                           "algorithmic_bytes_per_launch": byts}
+                           "frac": ach / pk["hbm_gbs"], "traffic": traffic("decode", w.name),
+                           "algorithmic_bytes_per_launch": byts, "avg_ms": dk_["avg_ms"],
+                           "peak_source": f"{pk['source']} copy bandwidth"}
+        step_ms = ms
+        res["roofline_step"] = {"achieved": byts / (step_ms / 1e3) / 1e9, "unit": "GB/s",
+                                "frac": byts / (step_ms / 1e3) / 1e9 / pk["hbm_gbs"],
+                                "note": "algorithmic bytes over the whole step (token feature map + decode kernel)"}
     return res
-
-
-def lola_state_bytes(L, lay):
-    return L.lola_state_bytes(lay.cfg)
 
 
 # ---------------------------------------------------------------------------------------
 # the CPU oracle
 # ---------------------------------------------------------------------------------------
 
-def oracle_sample(x, w, heads: int, read_mask: int = 0):
-    """Runs the oracle on the first `heads` heads of the workload; returns (seconds, tokens, threads)."""
+def oracle_sample(x, w, heads: int, tokens: int, read_mask: int = 0):
+    """Runs the oracle on the first `tokens` tokens of the first `heads` heads of the
+    workload; returns (seconds, token-equivalents, threads): a token-equivalent is one token
+    of all Hh heads."""
     from oracle import inc
     BH = w.B * w.Hh
     heads = min(heads, BH)
-    sl = lambda a: a.reshape(BH, *a.shape[2:])[:heads]  # noqa: E731
+    tokens = min(tokens, w.n)
+    sl = lambda a: a.reshape(BH, *a.shape[2:])[:heads, :tokens]  # noqa: E731
     t0 = time.perf_counter()
     out = inc.run(sl(x.q), sl(x.k), sl(x.v), x.W, w.eta, w.lam, w.dtype, read_mask=read_mask)
     dt = time.perf_counter() - t0
-    return dt, heads * w.n / w.Hh, out["threads"]
+    return dt, heads * tokens / w.Hh, out["threads"]
 
 
 def cpu_baseline(x, w, read_mask: int = 0):
-    """The oracle over every head of the prefill workload (about 35 core-seconds)."""
-    heads = w.B * w.Hh
-    dt, tokens, threads = oracle_sample(x, w, heads, read_mask)
+    """The float64 oracle on the first CPU_SAMPLE_TOKENS tokens of every head of one sequence
+    (threads over heads, one per host core at most)."""
+    heads = min(w.B * w.Hh, w.Hh)
+    dt, tokens, threads = oracle_sample(x, w, heads, CPU_SAMPLE_TOKENS, read_mask)
     return {"value": tokens / dt, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"all {heads} heads of {w.name}, full n={w.n} "
+            "sample": f"{heads} heads of {w.name} (one sequence), first {min(CPU_SAMPLE_TOKENS, w.n)} tokens "
                       f"({tokens:g} token-equivalents in {dt:.2f} s)"}
 
 
@@ -554,37 +684,41 @@ def cpu_baseline_chunk(x, w, heads: int = 16):
                       f"({tokens:g} token-equivalents in {dt:.2f} s)"}
 
 
+# tokens per head of each reference-arm step (a bounded sample of the workload)
+REFERENCE_SAMPLE_TOKENS = 4096
+
+
 def run_reference(args):
     R = Ranks()
     if R.rank != 0:
         return 0
     import synth
-    w = synth.WORKLOADS[PREFILL]
-    x = synth.make_inputs(w, B=1)         # one sequence's 32 heads: the sample is drawn from them
-    heads = min(w.Hh, max(1, os.cpu_count() or 1))
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w, n=min(w.n, REFERENCE_SAMPLE_TOKENS), B=1)   # the sample: one sequence's heads
+    heads = w.Hh
     for _ in range(args.warmup):
-        oracle_sample(x, x.w, heads, args.read_mask)
+        oracle_sample(x, x.w, heads, REFERENCE_SAMPLE_TOKENS, args.read_mask)
     times = []
     tokens = threads = 0
     for _ in range(args.steps):
-        dt, tokens, threads = oracle_sample(x, x.w, heads, args.read_mask)
+        dt, tokens, threads = oracle_sample(x, x.w, heads, REFERENCE_SAMPLE_TOKENS, args.read_mask)
         times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = tokens / (ms / 1e3)
-    sample = f"each step: {heads} of {w.B * w.Hh} heads of {w.name}, full n={w.n}"
+    sample = (f"each step: all {heads} heads of one sequence of {w.name}, first {x.w.n} of n={w.n} tokens "
+              f"(token-equivalents per second)")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta,
-                       "lambda": w.lam, "chunk": w.chunk},
+            "config": workload_config(w),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle", "sample": sample},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
 
 
-def main():
-    args = parse_args()
+def main(argv=None):
+    args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
     import torch
@@ -599,27 +733,44 @@ def main():
             print(json.dumps({"metric": "decode tokens/s per layer", **{k: v for k, v in dec.items() if k != "metric"}}))
         R.close()
         return 0
-    pre = run_prefill(L, R, args, pk)
+    pre = run_prefill(L, R, args, pk, args.workload, args.steps, args.warmup, e2e=not args.no_e2e,
+                      sre_map=args.sre_map)
     w = pre["workload"]
-    dec = None if args.no_decode or args.alloc == "chunk" else run_decode(L, R, args, pk)
+    x = pre.pop("x")
     cpu = None
     if R.rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(pre["x"], w, args.read_mask) if args.alloc == "token" else cpu_baseline_chunk(pre["x"], w)
+        cpu = cpu_baseline(x, w, args.read_mask) if args.alloc == "token" else cpu_baseline_chunk(x, w)
+    del x
+    more = []
+    if not args.no_more and args.alloc == "token":
+        for name in MORE_PREFILL:
+            if name == args.workload:
+                continue
+            import synth
+            mw = synth.WORKLOADS[name]
+            k = MORE_STEPS.get(name, 5)
+            p = run_prefill(L, R, args, pk, name, k, max(3, args.warmup), e2e=False)
+            p.pop("x")
+            more.append({**summarize_prefill(p), "steps": k})
+            torch.cuda.empty_cache()
+    dec = None if args.no_decode or args.alloc == "chunk" else run_decode(L, R, args, pk)
     if R.rank == 0:
-        launches = pre["launches"] * 1
+        kt = pre["kernels"]
+        launches = int(round(pre["launches_per_step"] * args.steps))
         line = {
             "metric": METRIC, "value": pre["value"], "unit": "tokens/s", "n_gpus": R.world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": pre["ms"], "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta,
-                       "lambda": w.lam, "chunk": w.chunk, "l2": "inputs 402 MB > 129 MB L2, no flush",
-                       "parallelism": f"replicas x{R.world}", "read_mask": args.read_mask, "alloc": args.alloc},
-            "roofline": pre.get("roofline"), "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
-            "clocks": pre["clocks"], "kernels": pre["kernels"],
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {**workload_config(w), "l2": pre["l2"],
+                       "parallelism": f"heads sharded: rank r runs batch block r (seed + r), {R.world} rank(s)",
+                       "read_mask": args.read_mask, "alloc": args.alloc},
+            "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
+            "clocks": pre["clocks"],
+            "kernels": {k: {**v, **pre["kernel_rooflines"].get(k if k != "phi" else "phi_k", {})}
+                        for k, v in kt.items()},
             **({"sre_map": pre["sre_map"]} if pre.get("sre_map") else {}),
-            "peaks": {k: pk[k] for k in
-                                                                        ("hbm_gbs", "bf16_tflops", "fp32_tflops",
-                                                                         "source")},
+            "peaks": {k: pk[k] for k in ("hbm_gbs", "bf16_tflops", "fp32_tflops", "source")},
+            "prefill_more": more,
             "decode": dec,
         }
         print(json.dumps(line))

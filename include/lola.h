@@ -209,7 +209,8 @@ int32_t lola_read_status(const lola_config* cfg, const void* state, int32_t* hos
  *   - the first call on a device (with that device current) looks up the array's device
  *     address with cudaGetSymbolAddress and caches it, and (as lola_prefill's first call)
  *     creates the side stream and its two events; make that first call before any stream
- *     capture starts;
+ *     capture starts.  Both stay cached until the process exits, so cudaDeviceReset on that
+ *     device after the first call is not supported;
  *   - all calls on a device share the one array and it keeps the last call's contents, so
  *     calls that overlap on the GPU (different streams, or different host threads, on the
  *     same device) race with each other: serialise them;
@@ -225,15 +226,16 @@ int32_t lola_prefill_noalloc(const lola_config* cfg, int32_t n, const void* Q, c
 /* ---- tracing: per-kernel device time of the library's own launches --------------------
  * When enabled, every kernel launch of lola_prefill / lola_decode_step / lola_state_init is
  * bracketed by two CUDA events on the stream it runs on (the call's stream; the side stream
- * for the queries' feature map, whose time then includes sharing the GPU with the selection
- * chain); a few microseconds of overhead per launch, no device memory.  Kernel ids: */
+ * for the queries' feature map, LOLA_KERNEL_PHI_Q, whose time then includes sharing the GPU
+ * with the selection chain); a few microseconds of overhead per launch, no device memory.  Kernel ids: */
 typedef enum {
     LOLA_KERNEL_STATE_INIT = 0,  /* state reset */
-    LOLA_KERNEL_PHI = 1,         /* feature map of Q and K (in a decode step: of the token's q, k) */
+    LOLA_KERNEL_PHI = 1,         /* prefill: feature map of K; decode step: of the token's q, k */
     LOLA_KERNEL_SELECT = 2,      /* allocation chain: SRE scoring, argmin, (H, s) write */
     LOLA_KERNEL_OUTPUT = 3,      /* co-normalised output of every query */
     LOLA_KERNEL_DECODE = 4,      /* one decode step */
-    LOLA_KERNEL_COUNT = 5
+    LOLA_KERNEL_PHI_Q = 5,       /* prefill: feature map of Q (on the side stream) */
+    LOLA_KERNEL_COUNT = 6
 } lola_kernel_id;
 
 /* enable != 0: clear the totals and start recording (process-wide); 0: stop recording. */

@@ -37,7 +37,7 @@ EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_c
            "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait", "lola_sre_map")
 # size of the fixed scratch array behind lola_prefill_noalloc (include/lola.h)
 LOLA_NOALLOC_SCRATCH_BYTES = 32 << 20
-KERNELS = ("state_init", "phi", "select", "output", "decode")
+KERNELS = ("state_init", "phi", "select", "output", "decode", "phi_q")
 
 
 class lola_config(ctypes.Structure):

@@ -13,13 +13,15 @@ namespace lola {
 int select_cluster_size(int lam);
 
 namespace {
-
 thread_local char g_cuda_error[256] = "";
+}  // namespace
 
 int32_t cuda_fail(cudaError_t e, const char* where) {
     snprintf(g_cuda_error, sizeof(g_cuda_error), "%s: %s", where, cudaGetErrorString(e));
     return LOLA_ERR_CUDA;
 }
+
+namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
@@ -314,7 +316,7 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
         if (e != cudaSuccess) return cuda_fail(e, "selection");
         e = cudaStreamWaitEvent(side->st, side->fork, 0);
         if (e != cudaSuccess) return cuda_fail(e, "fork wait");
-        e = traced(LOLA_KERNEL_PHI, side->st,
+        e = traced(LOLA_KERNEL_PHI_Q, side->st,
                    [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, side->st); });
         if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
         e = cudaEventRecord(side->join, side->st);
@@ -401,7 +403,8 @@ int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches) {
 }
 
 const char* lola_kernel_name(int32_t id) {
-    static const char* names[LOLA_KERNEL_COUNT] = {"state_init", "phi", "select", "output", "decode"};
+    static const char* names[LOLA_KERNEL_COUNT] = {"state_init", "phi", "select", "output", "decode",
+                                                        "phi_q"};
     return (id >= 0 && id < LOLA_KERNEL_COUNT) ? names[id] : "";
 }
 

@@ -618,10 +618,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     if (!mbar_wait(bar, 0, kBurstWaitNs)) *fail = 1;
     __syncthreads();
     if (*fail) {
-        // the burst did not land in time: flag the head and leave once its copies are done
+        // the burst did not land in time: flag the head and leave once its copies are done.
+        // The second wait is long but finite (20 s): copies still in flight after it would
+        // land in shared memory the CTA no longer owns, so the head's status word keeps
+        // ST_TIMEOUT and nothing read after a timed-out step is trusted.
         if (tid == 0) {
             atomicOr(&hdr[HDR_STATUS], (int)ST_TIMEOUT);
-            mbar_wait(bar, 0, kBurstWaitNs);
+            mbar_wait(bar, 0, 20ull * kBurstWaitNs);
         }
         return;
     }

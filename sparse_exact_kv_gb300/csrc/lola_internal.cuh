@@ -208,6 +208,10 @@ __device__ __forceinline__ void stage_w(float* Ws, const float* W, int tid) {
     }
 }
 
+// Records the CUDA error text for lola_last_cuda_error() (the calling thread's) and
+// returns LOLA_ERR_CUDA.
+int32_t cuda_fail(cudaError_t e, const char* where);
+
 // ---------------------------------------------------------------------------------
 // Launchers (each returns the launch's cudaError_t)
 // ---------------------------------------------------------------------------------

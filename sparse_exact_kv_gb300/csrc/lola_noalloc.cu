@@ -10,7 +10,9 @@
 //
 // Host code cannot use the array's name as a device address (in host code it names a
 // host-side stand-in), so the address is looked up with cudaGetSymbolAddress, once per
-// device, by the first call made on that device (with that device current), and cached.
+// device, by the first call made on that device (with that device current), and cached for
+// the life of the process: a cudaDeviceReset after that first call is not supported (the
+// cached address would name memory of the destroyed context).
 #include <mutex>
 
 #include "lola_internal.cuh"
@@ -38,14 +40,16 @@ int32_t lola_prefill_noalloc(const lola_config* cfg, int32_t n, const void* Q, c
     if (need > (size_t)LOLA_NOALLOC_SCRATCH_BYTES) return LOLA_ERR_WORKSPACE;  // beyond the fixed array
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) return LOLA_ERR_CUDA;
+    if (e != cudaSuccess) return lola::cuda_fail(e, "noalloc: current device");
+    if (dev < 0 || dev >= kMaxDevices) return lola::cuda_fail(cudaErrorInvalidDevice, "noalloc: device ordinal");
     void* scratch = nullptr;
     {
         std::lock_guard<std::mutex> g(g_mu);
         if (!g_scratch_ptr[dev]) {
             void* p = nullptr;
             e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-            if (e != cudaSuccess || !p) return LOLA_ERR_CUDA;
+            if (e != cudaSuccess) return lola::cuda_fail(e, "noalloc: scratch symbol address");
+            if (!p) return lola::cuda_fail(cudaErrorInvalidSymbol, "noalloc: scratch symbol address");
             g_scratch_ptr[dev] = p;
         }
         scratch = g_scratch_ptr[dev];

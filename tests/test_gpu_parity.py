@@ -11,7 +11,7 @@ import synth
 from oracle import inc
 from oracle import lola_ref as R
 
-from lola_parity import GAP, check_decisions, check_outputs, run_prefill, to_dev, to_f64
+from lola_parity import GAP, check_decisions, check_final_state, check_outputs, run_prefill, to_dev, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -25,24 +25,7 @@ def L():
 
 
 def _final_state_matches(lay, ref, eta, n, dtype):
-    st = lay.read_state()
-    BH = lay.cfg.B * lay.cfg.Hh
-    H_ref = ref["H"].reshape(BH, *ref["H"].shape[-2:])
-    s_ref = ref["s"].reshape(BH, -1)
-    tol = 1e-4 if dtype == "f32" else 2e-3
-    scale = max(1.0, float(np.abs(H_ref).max()))
-    assert np.abs(st["H"] - H_ref).max() <= tol * scale
-    assert np.abs(st["s"] - s_ref).max() <= tol * max(1.0, float(np.abs(s_ref).max()))
-    cache_ref = ref["cache"].reshape(BH, -1)
-    for i in range(BH):
-        live = st["c_pos"][i][st["c_pos"][i] >= 0]
-        assert list(live) == sorted(live), "cache not exported sorted by position"
-        assert list(live) == [p for p in cache_ref[i] if p >= 0]
-        assert st["n_cache"][i] == len(live)
-        want_win = sorted(range(max(0, n - eta), n))
-        got_win = sorted(p for p in st["win_pos"][i] if p >= 0)
-        assert got_win == want_win
-    assert (st["t"] == n).all() and (st["status"] == 0).all()
+    check_final_state(lay.read_state(), ref, dtype, eta, n)
 
 
 @pytest.mark.parametrize("d,eta,lam,chunk,n", [
@@ -114,6 +97,7 @@ def test_prefill_bf16_within_gap_and_tolerance(L, eta, lam, chunk, n):
     Y, wpos, lay = run_prefill(L, x, eta, lam, chunk)
     rep, free = check_decisions(x, wpos, eta, lam)
     check_outputs(Y, rep["Y"], "bf16")
+    _final_state_matches(lay, rep, eta, n, "bf16")
 
 
 def test_workload1_f32_full(L):

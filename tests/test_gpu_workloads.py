@@ -15,7 +15,7 @@ import torch
 import synth
 from oracle import inc
 
-from lola_parity import GAP, check_outputs, run_prefill, to_dev, to_f64
+from lola_parity import GAP, check_final_state, check_outputs, run_prefill, to_dev, to_f64
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -28,36 +28,48 @@ def L():
     return lib
 
 
-def _replay(x, wpos, eta, lam, heads):
+def _replay(x, wpos, eta, lam, heads, read_mask=0):
     """Oracle replay over a subset of heads (flattened indices)."""
     BH = x.w.B * x.w.Hh
     n = wpos.shape[-1]
     pick = lambda a: a.reshape(BH, *a.shape[2:])[heads]  # noqa: E731
     rep = inc.run(pick(x.q)[:, :n], pick(x.k)[:, :n], pick(x.v)[:, :n], x.W, eta, lam, x.w.dtype,
-                  replay=wpos.reshape(BH, -1)[heads])
+                  replay=wpos.reshape(BH, -1)[heads], read_mask=read_mask)
     assert (rep["status"] == 0).all(), np.unique(rep["status"])
     worst = float(np.max(rep["max_gap"]))
     assert worst < GAP, f"decision {worst:.3e} relative SRE away from the best"
     return rep
 
 
-def _prefill_parity(L, name, heads=None):
+def _prefill_parity(L, name, heads=None, read_mask=0):
     w = synth.WORKLOADS[name]
     x = synth.make_inputs(w)
-    Y, wpos, lay = run_prefill(L, x, w.eta, w.lam, w.chunk)
+    Y, wpos, lay = run_prefill(L, x, w.eta, w.lam, w.chunk, read_mask=read_mask)
     BH = w.B * w.Hh
     heads = np.arange(BH) if heads is None else np.asarray(heads)
-    rep = _replay(x, wpos, w.eta, w.lam, heads)
+    rep = _replay(x, wpos, w.eta, w.lam, heads, read_mask=read_mask)
     check_outputs(Y.reshape(BH, w.n, w.d)[heads], rep["Y"], "bf16", what=name)
     st, words = L.lola_read_status(lay.cfg, lay.state)
     assert st == 0, words
-    return rep
+    check_final_state(lay.read_state(), rep, "bf16", w.eta, w.n, heads=heads)
+    return rep, wpos
 
 
 def test_w2_full_every_head(L):
     """4 x 32 heads, n = 4096, eta = lambda = 64 (the benchmark's prefill): all 128 heads."""
-    rep = _prefill_parity(L, "w2_bf16_b4h32_n4096")
+    rep, _ = _prefill_parity(L, "w2_bf16_b4h32_n4096")
     assert rep["Y"].shape == (128, 4096, 128)
+
+
+def test_w2_read_mask_full_every_head(L):
+    """w2 with both the state and the cache hidden from every read (appendix I, Table 12's
+    window-only row): the decisions equal the unmasked run's (the mask never changes the
+    memory) and every head's outputs follow the oracle read with the same mask."""
+    _, w_masked = _prefill_parity(L, "w2_bf16_b4h32_n4096", read_mask=3)
+    w = synth.WORKLOADS["w2_bf16_b4h32_n4096"]
+    x = synth.make_inputs(w)
+    _, w_plain, _ = run_prefill(L, x, w.eta, w.lam, w.chunk)
+    assert np.array_equal(w_masked, w_plain)
 
 
 def test_w3_needles_full_every_head(L):
@@ -75,10 +87,11 @@ def test_w1_f32_full_free_running(L):
     """The float32 workload: the decision log equals the free-running oracle's."""
     w = synth.WORKLOADS["w1_f32_n1024"]
     x = synth.make_inputs(w)
-    Y, wpos, _ = run_prefill(L, x, w.eta, w.lam, w.chunk)
+    Y, wpos, lay = run_prefill(L, x, w.eta, w.lam, w.chunk)
     ref = inc.run(x.q, x.k, x.v, x.W, w.eta, w.lam, "f32")
     assert np.array_equal(wpos, ref["write_pos"])
     check_outputs(Y, ref["Y"], "f32")
+    check_final_state(lay.read_state(), ref, "f32", w.eta, w.n)
 
 
 def test_w4_decode_full_sampled_heads(L):
@@ -136,6 +149,13 @@ def test_w2_chunk_allocation_sampled_heads(L):
     """w2 (4 x 32 heads, n = 4096, eta = lambda = C = 64) with chunk-granular allocation: the
     GPU runs all 128 heads; the chunk oracle replays heads 0, 77 and 127."""
     _chunk_parity(L, "w2_bf16_b4h32_n4096", heads=[0, 77, 127])
+
+
+def test_w5_chunk_allocation_sampled_head(L):
+    """w5 (8 heads, n = 131072, eta = lambda = 512, C = 256: window = two chunks, AR(1)
+    inputs) with chunk-granular allocation: the GPU runs all 8 heads; the chunk oracle
+    replays head 6 over all 512 chunk starts."""
+    _chunk_parity(L, "w5_bf16_h8_n131072_ar1", heads=[6])
 
 
 def test_w3_chunk_allocation_sampled_heads(L):

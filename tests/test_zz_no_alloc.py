@@ -49,12 +49,23 @@ def test_noalloc_prefill_matches_workspace_prefill_on_consecutive_calls():
         (synth.gauss_inputs(1, 3, 700, 128, 128, "bf16", seed=41), 32, 48, 64),
         (synth.gauss_inputs(2, 2, 500, 64, 64, "f32", seed=42), 16, 24, 32),
     ]
+    first = None
     for x, eta, lam, chunk in cases:       # two noalloc calls in a row, different shapes
         Yr, wr, sr = _run(L, x, eta, lam, chunk, noalloc=False)
         Yn, wn, sn = _run(L, x, eta, lam, chunk, noalloc=True)
         assert np.array_equal(wn, wr)
         check_outputs(Yn, Yr, x.w.dtype, what="noalloc Y")
         np.testing.assert_array_equal(sn, sr)
+        if first is None:
+            first = (Yn, wn, sn)
+    # the first case again, straight after the second: whatever the array still holds from
+    # the earlier calls must not change a bit of the result
+    x, eta, lam, chunk = cases[0]
+    Y3, w3, s3 = _run(L, x, eta, lam, chunk, noalloc=True)
+    Y4, w4, s4 = _run(L, x, eta, lam, chunk, noalloc=True)
+    for got in ((Y3, w3, s3), (Y4, w4, s4)):
+        for a, b in zip(got, first):
+            np.testing.assert_array_equal(a, b)
 
 
 def test_noalloc_rejects_problems_beyond_its_array():
