@@ -20,16 +20,18 @@
 //     warp holds s and scores the evictee with the arithmetic of a slot;
 //   * per step: apply the previous write; every warp scores its slots and takes its
 //     packed-key minimum with two redux.sync; after the step's single barrier every warp
-//     takes the CTA minimum itself and keeps the decision in registers; with CL > 1 warp 0
-//     pushes the CTA's best to every peer's shared memory (st.shared::cluster) and one
-//     cluster barrier orders the exchange, and the winner's phi/v are read back through
-//     DSMEM;
+//     takes the CTA minimum itself and keeps the decision in registers; with CL > 1 each
+//     CTA pushes its best key and that candidate's phi / v row into every peer's shared
+//     memory with st.async, completing on the peer's exchange mbarrier, so the winner's
+//     row is local whatever CTA owns it (one thread waits on the mbarrier, bounded by 1 s,
+//     and a CTA barrier hands the result to the others);
 //   * evictee rows (phi(k_e), v_e) arrive by cp.async four steps ahead.
 // At every chunk start it stores H, s and the cache positions, from which the parallel
 // output kernel rebuilds every query's exact set and linear state.
 #include <climits>
 
 #include "lola_chain.cuh"
+#include "lola_tc.cuh"
 
 namespace lola {
 namespace {
@@ -42,6 +44,7 @@ constexpr int kSPC = kSelWarps * kSPW;     // slots per CTA
 constexpr int kMaxCluster = 16;
 constexpr int kPF = 4;                     // evictee prefetch distance (steps)
 constexpr int kNEB = 8;                    // evictee ring buffers (indexed by step & 7)
+constexpr uint64_t kXWaitNs = 1000000000ull;  // a cluster exchange not complete within 1 s is an error
 
 struct SelArgs {
     int n, eta, lam, chunk, nck, CL, cl_shift, io_bf16;
@@ -75,16 +78,36 @@ __device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_u2(uint32_t addr, uint32_t x, uint32_t y) {
-    asm volatile("st.shared::cluster.v2.b32 [%0], {%1, %2};" ::"r"(addr), "r"(x), "r"(y) : "memory");
-}
-__device__ __forceinline__ float4 ld_cluster(uint32_t addr) {
-    float4 v;
-    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                 : "r"(addr)
+// ---- the cluster exchange: DSMEM pushes completing on the receiver's mbarrier ----
+__device__ __forceinline__ void st_async_v2(uint32_t raddr, uint32_t x, uint32_t y, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(raddr),
+                 "r"(x), "r"(y), "r"(rbar)
                  : "memory");
-    return v;
+}
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     raddr),
+                 "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// Waits (acquire, cluster scope) for the phase of `parity` to complete, for at most
+// kXWaitNs of wall time; false when it gave up.
+__device__ __forceinline__ bool xbar_wait(uint32_t bar, uint32_t parity) {
+    const uint64_t t0 = tc::globaltimer_ns();
+    for (;;) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}\n"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (tc::globaltimer_ns() - t0 > kXWaitNs) return false;
+    }
 }
 // named barrier 1: the helper warps arrive, the evictee warp waits
 __device__ __forceinline__ void named_arrive(int nthreads) {
@@ -105,11 +128,14 @@ __device__ __forceinline__ void cp_async_wait() {
 template <int D, int DV, typename T>
 struct SelSmem {
     // dynamic shared memory: the warp-best candidates' phi (float32) and v (input type),
-    // double-buffered by step parity, then (float32 inputs only) the slots' value rows
+    // double-buffered by step parity; (float32 inputs only) the slots' value rows; then
+    // (clusters only) the rows the peer CTAs push, [2][CL] records of phi then v
+    static constexpr size_t kRowBytes = sizeof(float) * D + sizeof(T) * DV;
     static constexpr size_t kXPhi = sizeof(float) * 2 * kSelWarps * D;
     static constexpr size_t kXV = sizeof(T) * 2 * kSelWarps * DV;
     static constexpr size_t kSV = sizeof(T) == 4 ? sizeof(float) * kSPC * DV : 0;
-    static constexpr size_t kBytes = kXPhi + kXV + kSV;
+    static size_t bytes(int CL) { return kXPhi + kXV + kSV + (CL > 1 ? 2 * (size_t)CL * kRowBytes : 0); }
+    static_assert(kRowBytes % 16 == 0, "pushed rows move in 16-byte pieces");
 };
 
 template <int D, int DV, bool CLUSTER, typename T>
@@ -118,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     using M = SelSmem<D, DV, T>;
     constexpr int PD = S::PD, PV = S::PV, NRG = S::NRG, HR = S::HR, HC = S::HC;
     constexpr int VCH = DV * (int)sizeof(T) / 16;  // 16-byte chunks of one value row
+    constexpr int RCH = (int)(M::kRowBytes / 16);  // 16-byte chunks of one pushed row
     // Evictee roles: kHelp helper warps (warps 0, 1, 2, 6; helper i sums columns 32 i ..
     // 32 i + 31 of the H^T phi partials) and warp 0 also forms the previous write's gram with
     // the evictee; warp kSWarp holds s and forms the next evictee's z'; warp kVvWarp its
@@ -137,10 +164,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     float (*xphi)[kSelWarps][D] = reinterpret_cast<float (*)[kSelWarps][D]>(dyn_sm);
     T (*xv)[kSelWarps][DV] = reinterpret_cast<T (*)[kSelWarps][DV]>(dyn_sm + M::kXPhi);
     float (*sv_sm)[DV] = reinterpret_cast<float (*)[DV]>(dyn_sm + M::kXPhi + M::kXV);
+    unsigned char* rows = dyn_sm + M::kXPhi + M::kXV + M::kSV;   // pushed rows [2][CL]
     __shared__ __align__(16) float ebuf[kNEB][D];    // evictee phi(k), by step & 7
     __shared__ __align__(16) T evraw[kNEB][DV];      // evictee v as stored, by step & 7
-    __shared__ __align__(16) float wbuf_phi[D];      // winner copied from a peer CTA
-    __shared__ __align__(16) T wbuf_v[DV];
     __shared__ __align__(16) float zero_phi[D];      // the "nothing written" winner
     __shared__ __align__(16) T zero_v[DV];
     __shared__ __align__(16) float red[2][NRG][DV];  // partials of the next evictee's H^T phi
@@ -149,6 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ float zbuf[2], gbuf[2], zpbuf[2], vvbuf[4];
     __shared__ uint2 wkey[2][kSelWarps + 1];         // per-warp minima; [16] = the evictee
     __shared__ uint2 exch[2][kMaxCluster];
+    __shared__ __align__(8) uint64_t xbar[2];        // exchange mbarriers (clusters)
+    __shared__ int x_abort;
     __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
 
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
@@ -187,6 +215,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     for (int r = 0; r < HR * HC; ++r) h[r] = 0.f;
     if (tid < D) s_sm[tid] = 0.f;
     if (tid < 2) zpbuf[tid] = 0.f;    // z' against the empty memory
+    const uint32_t xbar0 = smem_addr(&xbar[0]);
+    if (tid == 0) {
+        x_abort = 0;
+        if (CLUSTER) {
+            tc::mbar_init(xbar0, 1);
+            tc::mbar_init(xbar0 + 8, 1);
+        }
+    }
 
     const float* phiK = a.phiK + (int64_t)bh * n * D;
     const int64_t vrow0 = (int64_t)bh * n;
@@ -220,7 +256,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     for (int st = 0; st < kPF; ++st) prefetch(st);
     cp_async_wait<0>();
     int n_cached = 0, n_written = 0;
-    __syncthreads();
+    // (clusters: every peer's exchange mbarriers are initialised before anything is pushed)
+    if constexpr (CLUSTER) cluster_barrier(); else __syncthreads();
     // |v_e|^2 of the evictee of step t is computed at step t - 1; step 0's here
     auto prep_vv = [&](int step) {
         if (warp == kVvWarp && step <= n && step - eta >= 0) {
@@ -236,8 +273,9 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     // the decision of the previous step, held by every thread
     int d_write = 0, d_isev = 0, d_cta = 0, d_ws = 0;
 
-    // The written candidate of step tp (phi, v), possibly copied from a peer CTA; the
-    // zero row when nothing was written.
+    // The written candidate of step tp (phi, v) in this CTA's shared memory: the evictee
+    // ring, this CTA's warp-best rows, or the row the owner CTA pushed; the zero row when
+    // nothing was written.
     struct Win {
         const float* phi;
         const T* v;
@@ -247,16 +285,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         if (d_isev) return Win{ebuf[tp & (kNEB - 1)], evraw[tp & (kNEB - 1)]};
         const int wb = d_ws / kSPW;
         if (!CLUSTER || d_cta == rank) return Win{xphi[tp & 1][wb], xv[tp & 1][wb]};
-        if (tid < D / 4) {
-            const float4 x = ld_cluster(map_rank(smem_addr(&xphi[tp & 1][wb][4 * tid]), d_cta));
-            reinterpret_cast<float4*>(wbuf_phi)[tid] = x;
-        } else if (tid < D / 4 + VCH) {
-            const int c = tid - D / 4;
-            const float4 x = ld_cluster(map_rank(smem_addr(reinterpret_cast<const char*>(xv[tp & 1][wb]) + 16 * c), d_cta));
-            reinterpret_cast<float4*>(wbuf_v)[c] = x;
-        }
-        __syncthreads();
-        return Win{wbuf_phi, wbuf_v};
+        const unsigned char* r = rows + ((size_t)(tp & 1) * CL + d_cta) * M::kRowBytes;
+        return Win{reinterpret_cast<const float*>(r), reinterpret_cast<const T*>(r + sizeof(float) * D)};
     };
 
     // Slots, then H, absorb the previous step's write (an exact zero update when nothing
@@ -289,6 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     };
 
     int snap_next = 0, snap_c = 0;
+    bool aborted = false;
     for (int t = 0; t < n; ++t) {
         const bool prev_write = d_write;
         const bool ev = t >= eta;
@@ -390,9 +421,46 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         warp_min_key(k.x, k.y);
         int bc = 0;
         if constexpr (CLUSTER) {
-            if (warp == 0 && lane < CL) st_cluster_u2(map_rank(smem_addr(&exch[t & 1][rank]), lane), k.x, k.y);
-            cluster_barrier();
-            uint2 c = lane < CL ? exch[t & 1][lane] : make_uint2(kNoKey, kNoKey);
+            // push this CTA's best key (warp 0) and its candidate's row (warps 1..4) to every
+            // peer; the exchange mbarrier of step parity b completes once all CL - 1 peers'
+            // keys and rows have landed here
+            const int b = t & 1;
+            const uint32_t xb = xbar0 + 8 * b;
+            if (warp == 0 && lane < CL && lane != rank) {
+                st_async_v2(map_rank(smem_addr(&exch[b][rank]), lane), k.x, k.y, map_rank(xb, lane));
+            } else if (warp >= 1 && warp <= 4) {
+                const int code = (int)(k.y & 127u);
+                const unsigned char* sphi_;
+                const unsigned char* sv_;
+                if (k.y == kNoKey) {
+                    sphi_ = reinterpret_cast<const unsigned char*>(zero_phi);
+                    sv_ = reinterpret_cast<const unsigned char*>(zero_v);
+                } else if (code == kEvCode) {
+                    sphi_ = reinterpret_cast<const unsigned char*>(ebuf[t & (kNEB - 1)]);
+                    sv_ = reinterpret_cast<const unsigned char*>(evraw[t & (kNEB - 1)]);
+                } else {
+                    sphi_ = reinterpret_cast<const unsigned char*>(xphi[b][code / kSPW]);
+                    sv_ = reinterpret_cast<const unsigned char*>(xv[b][code / kSPW]);
+                }
+                const uint32_t dst0 = smem_addr(rows + ((size_t)b * CL + rank) * M::kRowBytes);
+                for (int i = tid - kWarp; i < (CL - 1) * RCH; i += 4 * kWarp) {
+                    const int pr = i / RCH, ch = i % RCH;
+                    const int peer = pr < rank ? pr : pr + 1;
+                    const uint4 v = ch < D / 4 ? reinterpret_cast<const uint4*>(sphi_)[ch]
+                                               : reinterpret_cast<const uint4*>(sv_)[ch - D / 4];
+                    st_async_v4(map_rank(dst0 + 16 * ch, peer), v, map_rank(xb, peer));
+                }
+            }
+            if (tid == kThreads - 1) {
+                mbar_arrive_expect_tx(xb, (uint32_t)((CL - 1) * (8 + M::kRowBytes)));
+                if (!xbar_wait(xb, (uint32_t)(t >> 1) & 1u)) x_abort = 1;
+            }
+            __syncthreads();
+            if (x_abort) {
+                aborted = true;
+                break;
+            }
+            uint2 c = lane < CL ? (lane == rank ? k : exch[b][lane]) : make_uint2(kNoKey, kNoKey);
             uint32_t hi = c.x, lo = c.y;
             warp_min_key(hi, lo);
             // the owner CTA: lowest rank holding the minimum (the evictee is held by all)
@@ -433,6 +501,20 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         if (ev && !write) ++n_cached;
         if (write) ++n_written;
     }
+    if (aborted) {
+        // an exchange did not complete in time: flag the head, leave its state as it is, and
+        // give pushes still in flight time to land before the cluster's CTAs exit
+        cp_async_wait<0>();
+        if (tid == 0) atomicOr(reinterpret_cast<int32_t*>(a.state + (int64_t)bh * a.L.head_bytes) + HDR_STATUS,
+                               (int)ST_TIMEOUT);
+        if constexpr (CLUSTER) {
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (tc::globaltimer_ns() - t0 < 20000ull) {
+            }
+            cluster_barrier();
+        }
+        return;
+    }
     const bool last_write = d_write;
     const Win WL = winner(last_write, n - 1);
     absorb_slot(WL);
@@ -445,11 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     const T* Vin = static_cast<const T*>(a.V);
     if (rank == 0) {
         int32_t* hdr = reinterpret_cast<int32_t*>(rec);
-        if (tid == 0) {
+        if (tid == 0) {   // (the status word was cleared with the state before this launch)
             hdr[HDR_T] = n;
             hdr[HDR_NCACHE] = n_cached;
             hdr[HDR_NWRITTEN] = n_written;
-            hdr[HDR_STATUS] = 0;
         }
         h_store<D, DV>(reinterpret_cast<float*>(rec + a.L.H), h, warp, lane);
         if (warp == kSWarp) store_s(reinterpret_cast<float*>(rec + a.L.s));
@@ -524,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
 template <int D, int DV, typename T>
 cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t st) {
     auto kern = select_kernel<D, DV, false, T>;
-    const size_t smem = SelSmem<D, DV, T>::kBytes;
+    const size_t smem = SelSmem<D, DV, T>::bytes(1);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     kern<<<d.BH, kThreads, smem, st>>>(a);
@@ -534,7 +615,7 @@ cudaError_t launch_select_single(const Dims& d, const SelArgs& a, cudaStream_t s
 template <int D, int DV, typename T>
 cudaError_t launch_select_cluster(const Dims& d, const SelArgs& a, cudaStream_t st) {
     auto kern = select_kernel<D, DV, true, T>;
-    const size_t smem = SelSmem<D, DV, T>::kBytes;
+    const size_t smem = SelSmem<D, DV, T>::bytes(a.CL);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     if (a.CL > 8) {
