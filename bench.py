@@ -354,17 +354,22 @@ def kernel_times(L, names):
 def sre_map_timing(L, lay, w, V, ws, stream, pk, reps=5):
     """lola_sre_map over the snapshots of the last prefill in ws (a diagnostic, section 4.4):
     device time per call and its FP32 rate on the algorithmic flops (every snapshot c scores
-    the c * P keys before it: 2 D d_v + 2 D + 4 d_v each)."""
+    the c * P keys before it: 2 D d_v + 2 D + 4 d_v each); and lola_sre_map_relative (the
+    same map minus each key's SRE at first write, appendix G)."""
     import torch
     P = max(w.chunk, 128)
     nck = (w.n + P - 1) // P
     out = torch.empty(w.B, w.Hh, nck, w.n, dtype=torch.float32, device=V.device)
+    base = torch.empty(w.B, w.Hh, w.n, dtype=torch.float32, device=V.device)
     L.lola_sre_map(lay.cfg, w.n, V, ws, out, stream)
     ms = time_loop(lambda: L.lola_sre_map(lay.cfg, w.n, V, ws, out, stream), reps, stream) / reps
+    L.lola_sre_map_relative(lay.cfg, w.n, V, ws, out, base, stream)
+    ms_rel = time_loop(lambda: L.lola_sre_map_relative(lay.cfg, w.n, V, ws, out, base, stream), reps, stream) / reps
     keys = sum(c * P for c in range(nck))
     fl = w.B * w.Hh * keys * (2 * w.D * w.d + 2 * w.D + 4 * w.d)
     tf = fl / (ms / 1e3) / 1e12
-    return {"ms": ms, "achieved_tflops": tf, "frac_of_fp32_peak": tf / pk["fp32_tflops"], "snapshots": nck}
+    return {"ms": ms, "achieved_tflops": tf, "frac_of_fp32_peak": tf / pk["fp32_tflops"], "snapshots": nck,
+            "relative_ms": ms_rel}
 
 
 def traced_kernel_times(L, R, step, steps, stream, names):

@@ -71,6 +71,7 @@ typedef struct {
     int32_t dtype;      /* lola_dtype */
     int32_t read_mask;  /* 0, or lola_read_flags: memories left out of every query's read */
     int32_t alloc;      /* lola_alloc: LOLA_ALLOC_TOKEN (0, the default) or LOLA_ALLOC_CHUNK */
+    int32_t score;      /* lola_score: LOLA_SCORE_SRE (0, the default) or a query-dependent score */
 } lola_config;
 
 /* Allocation granularity.  LOLA_ALLOC_TOKEN: the per-token rule (sections 2.3-2.4); the
@@ -95,6 +96,26 @@ typedef enum { LOLA_ALLOC_TOKEN = 0, LOLA_ALLOC_CHUNK = 1 } lola_alloc;
  * leaves out H^T phi(q), phi(q)^T s (HIDE_STATE) and/or the cached keys (HIDE_CACHE).  The
  * window is always read; a nonzero mask needs eta >= 1 (LOLA_ERR_INVALID_ARG otherwise). */
 typedef enum { LOLA_READ_HIDE_STATE = 1, LOLA_READ_HIDE_CACHE = 2 } lola_read_flags;
+
+/* Cache score (section 4.4, Table 4: the scoring ablation).  LOLA_SCORE_SRE: the self-recall
+ * error, scored against the current memory at every eviction (sections 2.3-2.4).  The others
+ * are query-dependent scores that a key collects while it is in the window: with
+ * e = exp(q_t . k_j / sqrt(d_k)) and l = phi(q_t) . phi(k_j), summed over the eta queries of the
+ * steps t = j .. j + eta - 1 -- (e - l)^2 (KERNEL_SQ), |e - l| (KERNEL_ABS), l / e
+ * (KERNEL_RATIO), e (ATTENTION).  The score is complete when the key leaves the window and is
+ * never updated: when the candidates exceed lambda the lowest (score, position) is written
+ * (the older among equal scores), so the cache is the lambda highest-scored evicted keys.
+ * Needs eta >= 1 and alloc = LOLA_ALLOC_TOKEN (else LOLA_ERR_INVALID_ARG); lola_prefill only
+ * (lola_decode_step returns LOLA_ERR_UNSUPPORTED: the state keeps no window scores).  Scores
+ * are summed in float32.  The exported state holds H, s, the cache positions and rows and the
+ * window ring; the per-slot N, z and the next evictee's record stay zero. */
+typedef enum {
+    LOLA_SCORE_SRE = 0,
+    LOLA_SCORE_KERNEL_SQ = 1,
+    LOLA_SCORE_KERNEL_ABS = 2,
+    LOLA_SCORE_KERNEL_RATIO = 3,
+    LOLA_SCORE_ATTENTION = 4
+} lola_score;
 
 /* Supported by this build: d_k = d_v = D in {64, 128}; lambda <= 1024; eta <= 8192;
  * chunk a power of two in [16, 256]; B * Hh >= 1. */
@@ -262,6 +283,21 @@ const char* lola_kernel_name(int32_t id);
  * Stream-ordered; validation errors return before anything is enqueued. */
 int32_t lola_sre_map(const lola_config* cfg, int32_t n, const void* V, const void* workspace,
                      size_t workspace_bytes, float* out, void* stream);
+
+/* The relative SRE map (appendix G, Fig. 10, Eq. 26): for each key a snapshot's memory holds,
+ * its SRE against that memory minus its SRE against the first memory that held it.  Reads
+ * the same workspace, cfg and n as lola_sre_map.
+ *   out   device float32 [B, Hh, nck, n]: out[b, h, c, j] = SRE_c(j) - base[b, h, j] if key j
+ *         was written before step c * P, else 0
+ *   base  device float32 [B, Hh, n]: base[b, h, j] = SRE of key j against the memory right
+ *         after its write step w_j (the sums over the keys written at or before w_j; in
+ *         chunk-granular allocation every key written at that chunk start is included); 0 for
+ *         keys never written.  Formed from the snapshot before j's interval plus the
+ *         interval's writes up to w_j, so on the bf16 tensor-core path it carries the bf16
+ *         rounding of that snapshot, like the map.
+ * Stream-ordered; validation errors return before anything is enqueued. */
+int32_t lola_sre_map_relative(const lola_config* cfg, int32_t n, const void* V, const void* workspace,
+                              size_t workspace_bytes, float* out, float* base, void* stream);
 
 /* ---- self-test of the bounded waits -----------------------------------------------------
  * No counterpart in the LoLA paper.  Every wait of the library's kernels on an mbarrier (the

@@ -29,12 +29,19 @@ LOLA_READ_HIDE_STATE = 1
 LOLA_READ_HIDE_CACHE = 2
 LOLA_ALLOC_TOKEN = 0
 LOLA_ALLOC_CHUNK = 1
+LOLA_SCORE_SRE = 0
+LOLA_SCORE_KERNEL_SQ = 1
+LOLA_SCORE_KERNEL_ABS = 2
+LOLA_SCORE_KERNEL_RATIO = 3
+LOLA_SCORE_ATTENTION = 4
+SCORES = {"sre": 0, "kernel_sq": 1, "kernel_abs": 2, "kernel_ratio": 3, "attention": 4}
 
 # every symbol include/lola.h declares
 EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_check_config",
            "lola_state_layout_of", "lola_state_bytes", "lola_prefill_workspace_bytes", "lola_state_init",
            "lola_prefill", "lola_decode_step", "lola_read_status", "lola_kernel_timing", "lola_kernel_time",
-           "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait", "lola_sre_map")
+           "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait", "lola_sre_map",
+           "lola_sre_map_relative")
 # size of the fixed scratch array behind lola_prefill_noalloc (include/lola.h)
 LOLA_NOALLOC_SCRATCH_BYTES = 32 << 20
 KERNELS = ("state_init", "phi", "select", "output", "decode", "phi_q")
@@ -44,7 +51,7 @@ class lola_config(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int32), ("Hh", ctypes.c_int32), ("d_k", ctypes.c_int32),
                 ("d_v", ctypes.c_int32), ("D", ctypes.c_int32), ("eta", ctypes.c_int32),
                 ("lambda_", ctypes.c_int32), ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("read_mask", ctypes.c_int32), ("alloc", ctypes.c_int32)]
+                ("read_mask", ctypes.c_int32), ("alloc", ctypes.c_int32), ("score", ctypes.c_int32)]
 
 
 class lola_state_layout(ctypes.Structure):
@@ -89,6 +96,7 @@ def _load():
         "lola_prefill_noalloc": ([C, ctypes.c_int32, P, P, P, P, ctypes.c_int64, P, P, P, P], ctypes.c_int32),
         "lola_selftest_bounded_wait": ([ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), P], ctypes.c_int32),
         "lola_sre_map": ([C, ctypes.c_int32, P, P, ctypes.c_size_t, P, P], ctypes.c_int32),
+        "lola_sre_map_relative": ([C, ctypes.c_int32, P, P, ctypes.c_size_t, P, P, P], ctypes.c_int32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -100,13 +108,17 @@ def _load():
 _lib = _load()
 
 
-def make_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dtype, read_mask=0, alloc=LOLA_ALLOC_TOKEN) -> lola_config:
+def make_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dtype, read_mask=0, alloc=LOLA_ALLOC_TOKEN,
+                score=LOLA_SCORE_SRE) -> lola_config:
     """``read_mask``: LOLA_READ_HIDE_STATE | LOLA_READ_HIDE_CACHE, memories left out of every
     query's read (the memory and the decisions are unchanged).  ``alloc``: LOLA_ALLOC_TOKEN
-    (the per-token rule) or LOLA_ALLOC_CHUNK (chunk-granular allocation)."""
+    (the per-token rule) or LOLA_ALLOC_CHUNK (chunk-granular allocation).  ``score``:
+    LOLA_SCORE_SRE (the self-recall error) or one of the query-dependent scores of the scoring
+    ablation (a LOLA_SCORE_* value or its name in SCORES)."""
     dt = dtype if isinstance(dtype, int) else {"f32": LOLA_F32, "bf16": LOLA_BF16,
                                                torch.float32: LOLA_F32, torch.bfloat16: LOLA_BF16}[dtype]
-    return lola_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dt, read_mask, alloc)
+    sc = SCORES[score] if isinstance(score, str) else int(score)
+    return lola_config(B, Hh, d_k, d_v, D, eta, lam, chunk, dt, read_mask, alloc, sc)
 
 
 def _ptr(t):
@@ -210,6 +222,14 @@ def lola_sre_map(cfg: lola_config, n: int, V, workspace, out, stream=None) -> No
                              _ptr(out), _stream(stream)), "lola_sre_map")
 
 
+def lola_sre_map_relative(cfg: lola_config, n: int, V, workspace, out, base, stream=None) -> None:
+    """The relative SRE map (appendix G, Eq. 26): ``out`` float32 [B, Hh, nck, n] = the map
+    minus each held key's SRE at first write, ``base`` float32 [B, Hh, n] = that SRE."""
+    _check(_lib.lola_sre_map_relative(ctypes.byref(cfg), n, _ptr(V), _ptr(workspace),
+                                      workspace.numel() * workspace.element_size(), _ptr(out), _ptr(base),
+                                      _stream(stream)), "lola_sre_map_relative")
+
+
 def lola_selftest_bounded_wait(limit_ns: int, stream=None):
     """Runs the kernels' bounded mbarrier wait on a barrier nothing completes; returns
     (status, nanoseconds waited): LOLA_ERR_DEVICE when the wait gave up as designed."""
@@ -226,8 +246,8 @@ class Lola:
     """One layer's LoLA memory for B x Hh heads: owns the state and the prefill workspace."""
 
     def __init__(self, B, Hh, d, D, eta, lam, chunk=64, dtype=torch.bfloat16, device="cuda", read_mask=0,
-                 alloc=LOLA_ALLOC_TOKEN):
-        self.cfg = make_config(B, Hh, d, d, D, eta, lam, chunk, dtype, read_mask, alloc)
+                 alloc=LOLA_ALLOC_TOKEN, score=LOLA_SCORE_SRE):
+        self.cfg = make_config(B, Hh, d, d, D, eta, lam, chunk, dtype, read_mask, alloc, score)
         _check(lola_check_config(self.cfg), "config")
         self.dtype = dtype
         self.device = torch.device(device)

@@ -32,6 +32,8 @@ int32_t to_dims(const lola_config* c, Dims* d) {
         return LOLA_ERR_INVALID_ARG;
     if (c->read_mask < 0 || c->read_mask > 3 || (c->read_mask != 0 && c->eta < 1)) return LOLA_ERR_INVALID_ARG;
     if (c->alloc != LOLA_ALLOC_TOKEN && c->alloc != LOLA_ALLOC_CHUNK) return LOLA_ERR_INVALID_ARG;
+    if (c->score < LOLA_SCORE_SRE || c->score > LOLA_SCORE_ATTENTION) return LOLA_ERR_INVALID_ARG;
+    if (c->score != LOLA_SCORE_SRE && (c->eta < 1 || c->alloc != LOLA_ALLOC_TOKEN)) return LOLA_ERR_INVALID_ARG;
     if (c->alloc == LOLA_ALLOC_CHUNK &&
         (c->chunk < 1 || c->eta < c->chunk || c->eta % c->chunk != 0 || c->read_mask != 0))
         return LOLA_ERR_INVALID_ARG;
@@ -52,6 +54,7 @@ int32_t to_dims(const lola_config* c, Dims* d) {
     d->dtype = c->dtype;
     d->read_mask = c->read_mask;
     d->alloc = c->alloc;
+    d->score = c->score;
     if (d->alloc == LOLA_ALLOC_CHUNK && !chunk_mode_fits(*d)) return LOLA_ERR_UNSUPPORTED;
     return LOLA_OK;
 }
@@ -177,8 +180,9 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
     // The tensor-core output path reads phi(Q), phi(K) and the H snapshots in bf16 only;
     // the float32 path reads float32 copies.  phi(K) in float32 is always kept (selection).
     const bool tc = output_tc_supported(d);
+    const bool fixed = d.score != LOLA_SCORE_SRE;   // the query-dependent scores read phi(Q) in float32
     w.phiK = reinterpret_cast<float*>(take(4 * BH * n * d.D));
-    w.phiQ = reinterpret_cast<float*>(tc ? nullptr : take(4 * BH * n * d.D));
+    w.phiQ = reinterpret_cast<float*>(tc && !fixed ? nullptr : take(4 * BH * n * d.D));
     w.phiKb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * n * d.D) : nullptr);
     w.phiQb = reinterpret_cast<__nv_bfloat16*>(tc ? take(2 * BH * n * d.D) : nullptr);
     w.wstep = reinterpret_cast<int32_t*>(take(4 * BH * n));
@@ -188,6 +192,9 @@ Workspace carve_workspace(const Dims& d, int n, void* base) {
     w.snapS = reinterpret_cast<float*>(take(4 * BH * w.nck * d.D));
     w.snapC = reinterpret_cast<int32_t*>(take(4 * BH * w.nck * (int64_t)(d.lam > 0 ? d.lam : 1)));
     w.slotpos = reinterpret_cast<int32_t*>(take(4 * BH * (int64_t)(d.lam > 0 ? d.lam : 1)));
+    w.score = reinterpret_cast<float*>(fixed ? take(4 * BH * n) : nullptr);
+    w.dH = reinterpret_cast<float*>(fixed ? take(4 * BH * w.nck * d.D * d.dv) : nullptr);
+    w.dS = reinterpret_cast<float*>(fixed ? take(4 * BH * w.nck * d.D) : nullptr);
     w.abort_flag = reinterpret_cast<int*>(take(4));
     w.bytes = (size_t)o;
     return w;
@@ -300,7 +307,17 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     e = traced(LOLA_KERNEL_PHI, st,
                [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, ws.phiKb, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(K)");
-    {
+    if (d.score != LOLA_SCORE_SRE) {
+        // query-dependent scores: phi(Q) first (the scores read it in float32), then the
+        // chain-free allocation
+        e = traced(LOLA_KERNEL_PHI_Q, st,
+                   [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, st); });
+        if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
+        e = traced(LOLA_KERNEL_SELECT, st, [&]() {
+            return launch_fixed_select(d, n, ws, Q, K, V, static_cast<char*>(state), L, st);
+        });
+        if (e != cudaSuccess) return cuda_fail(e, "selection (query-dependent score)");
+    } else {
         // the selection on the caller's stream, phi(Q) beside it on the side stream (launched
         // second, at lower priority, so the chain's CTAs are placed first)
         std::lock_guard<std::mutex> g(g_side_mu);
@@ -341,6 +358,7 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W, in
     if (!state || !W || !q || !k || !v || !y || w_head_stride < 0 || w_head_stride % 4 != 0)
         return LOLA_ERR_INVALID_ARG;
     if (d.alloc == LOLA_ALLOC_CHUNK) return LOLA_ERR_UNSUPPORTED;   // the decode step is per token
+    if (d.score != LOLA_SCORE_SRE) return LOLA_ERR_UNSUPPORTED;     // the state keeps no window scores
     const void* ptrs[] = {state, W, q, k, v, y};
     for (const void* p : ptrs)
         if (!aligned16(p)) return LOLA_ERR_INVALID_ARG;
@@ -421,6 +439,21 @@ int32_t lola_sre_map(const lola_config* cfg, int32_t n, const void* V, const voi
     cudaStream_t st = (cudaStream_t)stream;
     const cudaError_t e = launch_sre_map(d, n, ws, V, out, st);
     return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "sre map");
+}
+
+int32_t lola_sre_map_relative(const lola_config* cfg, int32_t n, const void* V, const void* workspace,
+                              size_t workspace_bytes, float* out, float* base, void* stream) {
+    Dims d;
+    int32_t s = to_dims(cfg, &d);
+    if (s != LOLA_OK) return s;
+    if (n < 1 || !V || !workspace || !out || !base) return LOLA_ERR_INVALID_ARG;
+    if (!aligned16(V) || !aligned16(workspace) || !aligned16(out) || !aligned16(base)) return LOLA_ERR_INVALID_ARG;
+    if ((int64_t)n * d.BH * d.D > ((int64_t)1 << 40)) return LOLA_ERR_UNSUPPORTED;
+    const Workspace ws = carve_workspace(d, n, const_cast<void*>(workspace));
+    if (workspace_bytes < ws.bytes) return LOLA_ERR_WORKSPACE;
+    cudaStream_t st = (cudaStream_t)stream;
+    const cudaError_t e = launch_sre_map_relative(d, n, ws, V, out, base, st);
+    return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "relative sre map");
 }
 
 int32_t lola_selftest_bounded_wait(int64_t limit_ns, int64_t* host_elapsed_ns, void* stream) {

@@ -15,7 +15,7 @@ constexpr int kWarp = 32;
 // Sizes and the public per-head state layout (see lola.h)
 // ---------------------------------------------------------------------------------
 struct Dims {
-    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype, read_mask, alloc;
+    int B, Hh, BH, dk, dv, D, eta, lam, chunk, dtype, read_mask, alloc, score;
     int io_bytes() const { return dtype == LOLA_BF16 ? 2 : 4; }
 };
 
@@ -69,6 +69,9 @@ struct Workspace {
     float* snapS;      // [BH][nck][D]
     int32_t* snapC;    // [BH][nck][lam]   cache slot positions before each chunk (-1 empty)
     int32_t* slotpos;  // [BH][lam]        final slot positions (export scratch)
+    float* score;      // [BH][n]       query-dependent cache scores (score != LOLA_SCORE_SRE only)
+    float* dH;         // [BH][nck][D*dv]  per-interval write sums (score != LOLA_SCORE_SRE only)
+    float* dS;         // [BH][nck][D]
     int* abort_flag;   // one int, cleared by every lola_prefill call
     int snap_interval;  // steps between snapshots: max(C, 128), one tensor-core query tile
     int nck;
@@ -226,6 +229,12 @@ cudaError_t launch_chunk_select(const Dims& d, int n, const Workspace& ws, const
                                 char* state, const Layout& L, cudaStream_t st);
 // the SRE map of the keys held by each snapshot of a prefill's workspace
 cudaError_t launch_sre_map(const Dims& d, int n, const Workspace& ws, const void* V, float* out, cudaStream_t st);
+// the relative SRE map: the map above, minus each key's SRE at its first write (kept in base)
+cudaError_t launch_sre_map_relative(const Dims& d, int n, const Workspace& ws, const void* V, float* out,
+                                    float* base, cudaStream_t st);
+// the allocation with a query-dependent score (d.score != LOLA_SCORE_SRE): chain-free
+cudaError_t launch_fixed_select(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
+                                const void* V, char* state, const Layout& L, cudaStream_t st);
 cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                           const void* V, void* Y, cudaStream_t st);
 bool output_tc_supported(const Dims& d);

@@ -28,14 +28,14 @@ def to_f64(t: torch.Tensor) -> np.ndarray:
     return t.float().cpu().numpy().astype(np.float64)
 
 
-def run_prefill(L, x, eta, lam, chunk, n=None, dev="cuda", read_mask=0, alloc=0):
+def run_prefill(L, x, eta, lam, chunk, n=None, dev="cuda", read_mask=0, alloc=0, score=0):
     """Prefill through the C ABI; returns (Y float64, write_pos, layer)."""
     w = x.w
     dt = w.dtype
     n = n or x.q.shape[2]
     lay = L.Lola(w.B, w.Hh, w.d, w.D, eta, lam, chunk=chunk,
                  dtype=torch.bfloat16 if dt == "bf16" else torch.float32, device=dev, read_mask=read_mask,
-                 alloc=alloc)
+                 alloc=alloc, score=score)
     Q, K, V = (to_dev(getattr(x, a)[:, :, :n], dev, dt) for a in "qkv")
     W = torch.from_numpy(x.W).to(dev)
     wpos = torch.full((w.B, w.Hh, n), -7, dtype=torch.int32, device=dev)

@@ -176,3 +176,30 @@ def test_sre_map_validation(lib):
     assert so.lola_sre_map(ctypes.byref(cfg), 16, None, P(256), 1 << 30, P(256), None) == lib.LOLA_ERR_INVALID_ARG
     assert so.lola_sre_map(ctypes.byref(cfg), 0, P(256), P(256), 1 << 30, P(256), None) == lib.LOLA_ERR_INVALID_ARG
     assert so.lola_sre_map(ctypes.byref(cfg), 16, P(256), P(256), 16, P(256), None) == lib.LOLA_ERR_WORKSPACE
+    rel = so.lola_sre_map_relative
+    assert rel(ctypes.byref(cfg), 16, P(256), P(256), 1 << 30, P(256), None, None) == lib.LOLA_ERR_INVALID_ARG
+    assert rel(ctypes.byref(cfg), 16, None, P(256), 1 << 30, P(256), P(256), None) == lib.LOLA_ERR_INVALID_ARG
+    assert rel(ctypes.byref(cfg), 16, P(256), P(256), 16, P(256), P(256), None) == lib.LOLA_ERR_WORKSPACE
+    assert rel(ctypes.byref(cfg), 16, P(256), P(256), 1 << 30, P(256), P(264), None) == lib.LOLA_ERR_INVALID_ARG
+
+
+def test_query_dependent_score_validation(lib):
+    """The scoring ablation's configs: a known score, a window (eta >= 1) and per-token
+    allocation; the decode step is refused for such a layer before anything runs."""
+    mk = lambda **kw: lib.make_config(1, 1, 64, 64, 64, kw.get("eta", 8), 8, 16, "f32",  # noqa: E731
+                                      alloc=kw.get("alloc", 0), score=kw.get("score", 0))
+    for sc in range(5):
+        assert lib.lola_check_config(mk(score=sc)) == 0
+    for name, val in lib.SCORES.items():
+        assert lib.make_config(1, 1, 64, 64, 64, 8, 8, 16, "f32", score=name).score == val
+    assert lib.lola_check_config(mk(score=5)) == lib.LOLA_ERR_INVALID_ARG
+    assert lib.lola_check_config(mk(score=-1)) == lib.LOLA_ERR_INVALID_ARG
+    assert lib.lola_check_config(mk(score=2, eta=0)) == lib.LOLA_ERR_INVALID_ARG
+    assert lib.lola_check_config(mk(score=2, alloc=lib.LOLA_ALLOC_CHUNK)) == lib.LOLA_ERR_INVALID_ARG
+    assert lib.lola_check_config(mk(score=0, eta=0)) == 0
+    cfg = mk(score=4)
+    P = ctypes.c_void_p
+    st = lib._lib.lola_decode_step(ctypes.byref(cfg), P(256), P(256), 0, P(256), P(256), P(256), P(256), None, None)
+    assert st == lib.LOLA_ERR_UNSUPPORTED
+    # the float32 phi(Q) the scores read, the scores and the interval sums make the workspace larger
+    assert lib.lola_prefill_workspace_bytes(cfg, 100) > lib.lola_prefill_workspace_bytes(mk(score=0), 100)

@@ -274,6 +274,46 @@ def test_sre_map_matches_oracle(L, dtype, d, alloc):
         np.testing.assert_allclose(got[0, h], ref, **tol)
 
 
+@pytest.mark.parametrize("dtype,d,alloc", [("f32", 64, 0), ("bf16", 128, 0), ("f32", 64, 1), ("f32", 128, 0),
+                                           ("bf16", 128, 1)])
+def test_relative_sre_map_matches_oracle(L, dtype, d, alloc):
+    """The relative SRE map (appendix G, Fig. 10, Eq. 26) and its baseline, the SRE of each
+    written key against the first memory that holds it, equal the oracle's along the GPU's
+    write log (per token and chunk-granular; with chunk allocation every key written at one
+    chunk start shares its first memory).  The bf16 path's snapshots of H are bf16, so its
+    bar is the map's."""
+    from oracle import lola_ref as R
+    B, Hh, n, eta, lam, chunk = 1, 2, 420, 16, 20, 16
+    x = synth.gauss_inputs(B, Hh, n, d, d, dtype, seed=140 + d + alloc)
+    Y, wlog, lay = run_prefill(L, x, eta, lam, chunk, alloc=alloc)
+    snap = max(chunk, 128)
+    nck = (n + snap - 1) // snap
+    V = to_dev(x.v, "cuda", dtype)
+    out = torch.full((B, Hh, nck, n), float("nan"), dtype=torch.float32, device="cuda")
+    base = torch.full((B, Hh, n), float("nan"), dtype=torch.float32, device="cuda")
+    L.lola_sre_map_relative(lay.cfg, n, V, lay.workspace, out, base)
+    torch.cuda.synchronize()
+    got, gbase = out.cpu().numpy().astype(np.float64), base.cpu().numpy().astype(np.float64)
+    k, v = x.widened("k"), x.widened("v")
+    tol = dict(rtol=2e-4, atol=2e-4) if dtype == "f32" else dict(rtol=3e-2, atol=3e-2)
+    for h in range(Hh):
+        if alloc:
+            ws = wlog[0, h]
+        else:
+            ws = np.full(n, -1, np.int64)
+            for t, p in enumerate(wlog[0, h]):
+                if p >= 0:
+                    ws[p] = t
+        times = [c * snap for c in range(nck)]
+        want_base = R.sre_at_first_write(k[0, h], v[0, h], x.W, ws)
+        want = R.sre_map_relative(k[0, h], v[0, h], x.W, ws, times)
+        assert (ws >= 0).sum() > 50 and (gbase[0, h][ws < 0] == 0).all()
+        np.testing.assert_allclose(gbase[0, h], want_base, **tol)
+        held = (ws[None, :] >= 0) & (ws[None, :] < np.array(times)[:, None])
+        assert (got[0, h][~held] == 0).all(), "a key the memory does not hold has a nonzero entry"
+        np.testing.assert_allclose(got[0, h], want, **tol)
+
+
 def test_bounded_wait_gives_up_and_reports(L):
     """The kernels' mbarrier wait, run on a barrier that nothing completes, gives up after its
     limit and reports it; the context stays usable (a prefill runs right after)."""
@@ -289,3 +329,42 @@ def test_status_words_clear_after_prefill(L):
     _, _, lay = run_prefill(L, x, 16, 16, 64)
     st, words = L.lola_read_status(lay.cfg, lay.state)
     assert st == 0 and words == [0, 0, 0, 0]
+
+
+@pytest.mark.parametrize("kind", ["kernel_sq", "kernel_abs", "kernel_ratio", "attention"])
+@pytest.mark.parametrize("dtype,d,eta,lam", [("f32", 64, 16, 20), ("bf16", 128, 24, 40), ("f32", 128, 8, 0),
+                                             ("bf16", 64, 32, 100)])
+def test_query_dependent_score_prefill_matches_oracle(L, kind, dtype, d, eta, lam):
+    """The scoring ablation (section 4.4, Table 4): query-dependent scores collected over each
+    key's window queries, frozen at eviction.  float32: the write log equals the oracle's;
+    bf16: every decision is within 1e-3 relative score of the oracle's lowest candidate
+    (replayed).  Outputs along the log, the final H, s and cache follow the oracle."""
+    from oracle import lola_ref as R
+    B, Hh, n, chunk = 1, 2, 330, 16
+    x = synth.gauss_inputs(B, Hh, n, d, d, dtype, seed=170 + d + lam)
+    Y, wpos, lay = run_prefill(L, x, eta, lam, chunk, score=kind)
+    st = lay.read_state()
+    q, k, v = (x.widened(a) for a in "qkv")
+    for h in range(Hh):
+        ws = np.full(n, -1, np.int64)
+        for t, p in enumerate(wpos[0, h]):
+            if p >= 0:
+                ws[p] = t
+        if dtype == "f32":
+            ref = R.lola_run_fixed_score(q[0, h], k[0, h], v[0, h], x.W, eta, lam, kind)
+            assert np.array_equal(wpos[0, h], ref["write_pos"]), "float32 write log differs"
+        else:
+            ref = R.lola_run_fixed_score(q[0, h], k[0, h], v[0, h], x.W, eta, lam, kind, replay=ws)
+            assert ref["max_gap"] < GAP, f"a decision is {ref['max_gap']:.3e} (relative score) from the lowest"
+        check_outputs(Y[0, h], ref["Y"], dtype)
+        np.testing.assert_allclose(st["H"][h], ref["H"], rtol=2e-4, atol=2e-4)
+        np.testing.assert_allclose(st["s"][h], ref["s"], rtol=2e-5, atol=2e-5)
+        assert [p for p in st["c_pos"][h] if p >= 0] == ref["cache"].tolist()
+        assert st["t"][h] == n and st["n_cache"][h] == len(ref["cache"]) and st["status"][h] == 0
+    if lam == 0:
+        assert (wpos[0, :, eta:] >= 0).all(), "with no cache every evicted key is written at once"
+    with pytest.raises(L.LolaError):
+        dev = "cuda"
+        Q, K, V = (to_dev(getattr(x, a), dev, dtype) for a in "qkv")
+        lay.decode_step(Q[:, :, 0].contiguous(), K[:, :, 0].contiguous(), V[:, :, 0].contiguous(),
+                        torch.from_numpy(x.W).to(dev))
