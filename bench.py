@@ -71,6 +71,9 @@ def parse_args(argv=None):
                    help="read mask of the layer (1: state hidden, 2: cache hidden, 3: both)")
     p.add_argument("--sre-map", action="store_true",
                    help="also time lola_sre_map over the prefill's snapshots (reported under sre_map)")
+    p.add_argument("--score", default="sre", choices=["sre", "kernel_sq", "kernel_abs", "kernel_ratio", "attention"],
+                   help="cache score (sre: the self-recall error; others: the scoring ablation's query-dependent "
+                        "scores, frozen at eviction; no decode line)")
     p.add_argument("--alloc", default="token", choices=["token", "chunk"],
                    help="allocation granularity of the prefill (chunk: the chunk-granular variant; "
                         "no decode line, the decode step is per token)")
@@ -384,7 +387,13 @@ def traced_kernel_times(L, R, step, steps, stream, names):
     return kernel_times(L, names)
 
 
-def prefill_rooflines(w, kt, ms, pk, alloc="token"):
+def fixed_score_flops_per_key(d, D, eta):
+    """The scoring ablation's score pass per key: over its eta window queries, q . k (2 d) and
+    phi(q) . phi(k) (2 D)."""
+    return eta * (2 * d + 2 * D)
+
+
+def prefill_rooflines(w, kt, ms, pk, alloc="token", score="sre"):
     """The step's roofline (contraction flops over the whole step time against the measured
     bf16 peak) and each kernel's own."""
     heads = w.B * w.Hh
@@ -402,7 +411,14 @@ def prefill_rooflines(w, kt, ms, pk, alloc="token"):
         step["traffic"] = sum(tr)
     per = {}
     sel = kt.get("select")
-    if sel and alloc == "token":
+    if sel and score != "sre":
+        f = fixed_score_flops_per_key(w.d, w.D, w.eta)
+        a_ = ht * f / (sel["avg_ms"] / 1e3) / 1e12
+        per["select"] = {"bound": "alu", "achieved": a_, "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
+                         "frac": a_ / pk["fp32_tflops"], "flop_per_head_token": f, "avg_ms": sel["avg_ms"],
+                         "traffic": None, "what": "score pass + closed-form write steps + interval sums",
+                         "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+    elif sel and alloc == "token":
         f = cf["sre_new"] + cf["write"] + cf["gram"]
         a_ = ht * f / (sel["avg_ms"] / 1e3) / 1e12
         per["select"] = {"bound": "alu", "achieved": a_, "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
@@ -522,7 +538,8 @@ def run_prefill(L, R, args, pk, name, steps, warmup, e2e=True, sre_map=False):
     W = torch.from_numpy(x.W).to(dev)
     lay = L.Lola(w.B, w.Hh, w.d, w.D, w.eta, w.lam, chunk=w.chunk,
                  dtype=torch.bfloat16 if w.dtype == "bf16" else torch.float32, device=dev,
-                 read_mask=args.read_mask, alloc=L.LOLA_ALLOC_CHUNK if args.alloc == "chunk" else L.LOLA_ALLOC_TOKEN)
+                 read_mask=args.read_mask, alloc=L.LOLA_ALLOC_CHUNK if args.alloc == "chunk" else L.LOLA_ALLOC_TOKEN,
+                 score=args.score)
     ws = lay.workspace_for(w.n)
     Y = torch.empty_like(V)
     wpos = torch.empty(w.B, w.Hh, w.n, dtype=torch.int32, device=dev)
@@ -542,7 +559,7 @@ def run_prefill(L, R, args, pk, name, steps, warmup, e2e=True, sre_map=False):
     ms = R.max(ms) / steps
     tokens = w.B * w.n
     in_bytes = 3 * Q.numel() * Q.element_size()
-    roof, per = prefill_rooflines(w, kt, ms, pk, args.alloc)
+    roof, per = prefill_rooflines(w, kt, ms, pk, args.alloc, args.score)
     res = {"workload": w, "ms": ms, "value": whole_job_value(R.world, tokens, ms), "kernels": kt,
            "clocks": clk.summary(), "launches_per_step": sum(v["launches"] for v in kt.values()) / steps,
            "roofline": roof, "kernel_rooflines": per,
@@ -689,6 +706,28 @@ def cpu_baseline_chunk(x, w, heads: int = 16):
                       f"({tokens:g} token-equivalents in {dt:.2f} s)"}
 
 
+def cpu_baseline_fixed(x, w, kind: str, heads: int = 2, tokens: int = 2048):
+    """The oracle's query-dependent-score rule (one thread, float64) on the first `tokens`
+    tokens of the first `heads` heads."""
+    import numpy as np
+    import synth
+    from oracle import lola_ref as Rf
+    heads = min(heads, w.B * w.Hh)
+    tokens = min(tokens, w.n)
+    wide = (lambda a: synth.bf16_bits_to_f32(a).astype(np.float64)) if w.dtype == "bf16" else \
+        (lambda a: a.astype(np.float64))
+    t0 = time.perf_counter()
+    for i in range(heads):
+        b, h = divmod(i, w.Hh)
+        Rf.lola_run_fixed_score(wide(x.q[b, h, :tokens]), wide(x.k[b, h, :tokens]), wide(x.v[b, h, :tokens]), x.W,
+                                w.eta, w.lam, kind)
+    dt = time.perf_counter() - t0
+    te = heads * tokens / w.Hh
+    return {"value": te / dt, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{kind} rule on {heads} of {w.B * w.Hh} heads of {w.name}, first {tokens} tokens "
+                      f"({te:g} token-equivalents in {dt:.2f} s)"}
+
+
 # tokens per head of each reference-arm step (a bounded sample of the workload)
 REFERENCE_SAMPLE_TOKENS = 4096
 
@@ -744,10 +783,15 @@ def main(argv=None):
     x = pre.pop("x")
     cpu = None
     if R.rank == 0 and not args.no_cpu:
-        cpu = cpu_baseline(x, w, args.read_mask) if args.alloc == "token" else cpu_baseline_chunk(x, w)
+        if args.score != "sre":
+            cpu = cpu_baseline_fixed(x, w, args.score)
+        elif args.alloc == "token":
+            cpu = cpu_baseline(x, w, args.read_mask)
+        else:
+            cpu = cpu_baseline_chunk(x, w)
     del x
     more = []
-    if not args.no_more and args.alloc == "token":
+    if not args.no_more and args.alloc == "token" and args.score == "sre":
         for name in MORE_PREFILL:
             if name == args.workload:
                 continue
@@ -758,7 +802,7 @@ def main(argv=None):
             p.pop("x")
             more.append({**summarize_prefill(p), "steps": k})
             torch.cuda.empty_cache()
-    dec = None if args.no_decode or args.alloc == "chunk" else run_decode(L, R, args, pk)
+    dec = None if args.no_decode or args.alloc == "chunk" or args.score != "sre" else run_decode(L, R, args, pk)
     if R.rank == 0:
         kt = pre["kernels"]
         launches = int(round(pre["launches_per_step"] * args.steps))
@@ -768,7 +812,7 @@ def main(argv=None):
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {**workload_config(w), "l2": pre["l2"],
                        "parallelism": f"heads sharded: rank r runs batch block r (seed + r), {R.world} rank(s)",
-                       "read_mask": args.read_mask, "alloc": args.alloc},
+                       "read_mask": args.read_mask, "alloc": args.alloc, "score": args.score},
             "roofline": pre["roofline"], "cpu_baseline": cpu, "e2e": pre.get("e2e"), "gpu_launches": launches,
             "clocks": pre["clocks"],
             "kernels": {k: {**v, **pre["kernel_rooflines"].get(k if k != "phi" else "phi_k", {})}

@@ -1,29 +1,44 @@
 // K3 (bf16, tensor cores): co-normalised LoLA output for every query, in parallel over
-// (head, 128-query tile), with tcgen05 MMAs accumulating in TMEM.
+// (head, 128-query tile), as a warp-specialised tcgen05 pipeline.
 //
 // LoLA reading notes (arXiv 2505.23666v3), section 2.5, Eq. 14:
 //   y_t = (H_t^T phi(q_t) + sum_{j in G_t ∪ W_t} a_tj v_j) / (phi(q_t)^T s_t + sum a_tj),
 //   a_tj = exp(q_t . k_j / sqrt(d_k)).
 // With w_j the step that wrote key j (none: never), key j is exact for query t iff
-// j <= t < w_j and in the linear memory iff w_j <= t.  From the snapshot taken before
-// the tile's chunk start c0 -- (H_c, s_c) and the cache positions -- the tile's pool is
+// j <= t < w_j and in the linear memory iff w_j <= t.  From the snapshot taken before the
+// tile's chunk start c0 -- (H_c, s_c) and the cache positions -- the tile's pool is
 // cache(c0) ∪ [c0 - eta, tile end), and for every query t of the tile
-//   O_soft = sum_pool [j <= t < w_j] 2^(s_tj - m) v_j,      l_soft = sum of the weights,
-//   O_lin  = phi(q_t)^T H_c + sum_pool [c0 <= w_j <= t] (phi(q_t) . phi(k_j)) v_j,
-//   l_lin  = phi(q_t)^T s_c + sum of those linear weights,
-//   y_t    = (O_soft + 2^{-m} O_lin) / (l_soft + 2^{-m} l_lin),
-// with scores s_tj = q_t . k_j log2(e) / sqrt(d_k) in log2 units.
-// The tensor cores compute S = Q K^T, L = phi(Q) phi(K)^T (per 64-key pool block),
-// O_soft += P_soft V, O_lin += P_lin V and O_lin = phi(Q) H_c, all bf16 x bf16 -> fp32 in
-// TMEM (M = 128: TMEM lane = query row).  Two threads per query row (warps w and w + 4
-// share TMEM lanes) each take half of a block's keys: they read S and L from TMEM, apply
-// the masks (each key's visible rows are precomputed once per block as three row bounds)
-// and an online maximum m that is raised lazily (O_soft is rescaled in TMEM only when the
-// block maximum exceeds m by more than 2^12), and write the bf16 weights to shared memory
-// for the P V products.  Before their half, warps 4-7 start the cp.async gathers of the
-// next block's keys into the other half of a two-stage buffer (the pool keys are
-// scattered: the cache positions come from the snapshot).  One commit per block covers
-// that block's P V products and the next block's S, L.
+//   y_t = O_t / l_t,  O_t = 2^{-m} (phi(q_t)^T H_c + sum_pool p_tj v_j),
+//                     l_t = 2^{-m} (phi(q_t)^T s_c + sum_pool p_tj),
+//   p_tj = 2^{s_tj}             if j <= t < w_j   (s_tj = q_t . k_j log2(e) / sqrt(d_k)),
+//        = phi(q_t) . phi(k_j)   if c0 <= w_j <= t  (written inside the chunk, before t),
+//        = 0                     otherwise.
+// The two cases exclude each other, so one weight matrix P carries both branches and one
+// product P V accumulates the numerator.  m is a running maximum raised lazily: O is
+// rescaled in TMEM only when a block's maximum exceeds m by more than 2^12 (m starts at 0,
+// the scale of the snapshot term).
+//
+// Roles (416 threads):
+//   * warps 9-12 (loaders): Q, phi(Q) and H_c tiles by TMA (cp.async.bulk.tensor, 128-byte
+//     swizzle, rows past n zero-filled); per 64-key pool block the keys' positions and row
+//     bounds (four blocks ahead, into a ring), then its K, phi(K), V rows into one of two
+//     stages -- a window block (consecutive positions) as TMA tiles, a cache block
+//     (scattered positions) as 16-byte cp.async gathers from all 128 loader threads (many
+//     requests in flight);
+//   * warp 8 (MMA, one thread): O = phi(Q) H_c, then per block S = Q K^T and
+//     L = phi(Q) phi(K)^T into one of two TMEM buffers, and O += P V of the block before,
+//     each group committed to an mbarrier;
+//   * warps 0-7 (weighting): two threads per query row (TMEM lane = row; warp w takes keys
+//     32 (w / 4) .. + 31 of every block) read S and L, apply the masks, agree on the row
+//     maximum, write bf16 P to shared memory and keep the row's partial normaliser.
+// Double buffers let block b + 1's S, L products and block b - 1's P V product run while
+// block b is weighted.  Every wait is bounded by %globaltimer (1 s, then a status bit in
+// the head's state and a per-launch abort flag).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "lola_internal.cuh"
 #include "lola_tc.cuh"
 
@@ -32,40 +47,48 @@ namespace {
 
 using namespace tc;
 
-constexpr int kThreadsTc = 256;          // two threads per query row (warps w and w + 4)
+constexpr int kWeightWarps = 8;
+constexpr int kMmaWarp = 8, kLoadWarp0 = 9, kLoadWarps = 4;
+constexpr int kLoadThreads = kLoadWarps * kWarp;
+constexpr int kThreadsTc = 13 * kWarp;   // 416
 constexpr int kTM = 128;                 // query rows per tile (MMA M)
 constexpr int kBN = 64;                  // pool keys per block (MMA N of S, L; K of P V)
 constexpr int kD = 128;                  // d_k = d_v = D
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kRescale2 = 12.0f;       // lazy rescale threshold (log2 units)
-constexpr uint64_t kWaitNs = 1000000000ull;  // an MMA group that has not completed in 1 s is an error
+constexpr int kRing = 8;                 // blocks of key positions / row bounds kept
+constexpr int kAhead = 4;                // blocks of row bounds computed ahead of the loads
+constexpr uint64_t kWaitNs = 1000000000ull;  // a stage not reached within 1 s is an error
 
-// shared-memory map (bytes from a 1024-aligned base).  Key blocks are double-buffered;
-// stage 1's K and phi(K) tiles reuse the H_c tile once phi(Q) H_c has been issued (the
-// first wait covers it).
-constexpr int SQ = 0;                    // Q tile      K-major, 2 atoms x [128 x 64]
-constexpr int SPQ = 32768;               // phi(Q) tile K-major
-constexpr int SH = 98304;                // H_c         MN-major [K = D x N = d_v]
-// stage st: K block K-major, 2 atoms x [64 x 64]; phi(K) block; V block MN-major [64 x d_v]
-__device__ __forceinline__ uint32_t SK(int st) { return st ? 98304u : 65536u; }
-__device__ __forceinline__ uint32_t SPK(int st) { return st ? 114688u : 81920u; }
-__device__ __forceinline__ uint32_t SV(int st) { return st ? 147456u : 131072u; }
-constexpr int SPS = 163840;              // soft weights K-major [128 x 64]
-constexpr int SPL = 180224;              // linear weights
-constexpr int SEND = 196608;
-// TMEM columns
-constexpr uint32_t TS = 0, TL = 64, TOS = 128, TOL = 256;
+// shared-memory map (bytes from a 1024-aligned base).  Stage 1's K and phi(K) tiles reuse
+// the H_c tile once phi(Q) H_c has completed.
+constexpr uint32_t SQ = 0;               // Q tile      K-major, 2 atoms x [128 x 64]
+constexpr uint32_t SPQ = 32768;          // phi(Q) tile K-major
+constexpr uint32_t SH = 98304;           // H_c         MN-major [K = D x N = d_v], 2 atoms
+__device__ __forceinline__ uint32_t SK(int st) { return st ? 98304u : 65536u; }    // K block, 2 atoms x [64 x 64]
+__device__ __forceinline__ uint32_t SPK(int st) { return st ? 114688u : 81920u; }  // phi(K) block
+__device__ __forceinline__ uint32_t SV(int st) { return st ? 147456u : 131072u; }  // V block MN-major [64 x d_v]
+__device__ __forceinline__ uint32_t SP(int st) { return st ? 180224u : 163840u; }  // P K-major [128 x 64]
+constexpr uint32_t SEND = 196608;
+// TMEM columns: S and L double-buffered, then O
+__device__ __forceinline__ uint32_t TS(int st) { return st ? 64u : 0u; }
+__device__ __forceinline__ uint32_t TL(int st) { return st ? 192u : 128u; }
+constexpr uint32_t TO = 256;
+
+// barrier slots
+enum { B_Q = 0, B_H = 1, B_O = 2, B_KVFULL = 3, B_KVEMPTY = 5, B_SFULL = 7, B_SFREE = 9, B_PFULL = 11, B_NBARS = 13 };
+
+struct TcMaps {
+    CUtensorMap q, pq, k, pk, v, h;      // 3-D bf16 maps, 64-column boxes, 128-byte swizzle
+};
 
 struct TcArgs {
     int n, eta, lam, chunk, nck, read_mask;
-    const __nv_bfloat16* Q;
     const __nv_bfloat16* K;
     const __nv_bfloat16* V;
     __nv_bfloat16* Y;
-    const __nv_bfloat16* phiQb;  // [BH][n][D] bf16
-    const __nv_bfloat16* phiKb;
+    const __nv_bfloat16* phiKb;  // [BH][n][D] bf16
     const int32_t* wstep;
-    const __nv_bfloat16* snapHb; // [BH][nck][D][DV] bf16
     const float* snapS;
     const int32_t* snapC;
     char* state;                 // per-head status words (timeouts)
@@ -78,21 +101,59 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-__device__ __forceinline__ void producers_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+__device__ __forceinline__ void weight_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+// barrier over the four loader warps that also ORs a predicate across them (every loader
+// thread takes the same branch afterwards)
+__device__ __forceinline__ bool loaders_or(bool x) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbarrier.red.or.pred q, 2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"((uint32_t)x)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive1(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+// TMA: box (x, y, z) of a 3-D tensor map into shared memory, completing on `bar`
+__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+            dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective)
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 
-__global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a) {
+__global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_constant__ TcMaps maps, const TcArgs a) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    __shared__ uint64_t mbar;
+    __shared__ __align__(8) uint64_t bars[B_NBARS];
     __shared__ uint32_t tmem_base;
-    __shared__ int kpos[2][kBN];
-    __shared__ __align__(16) uint32_t kinfo[2][kBN];   // per key: soft rows [lo, hi), linear rows >= llo
+    __shared__ int abort_sm;
+    __shared__ int kpos[kRing][kBN];
+    __shared__ __align__(16) uint32_t kinfo[kRing][kBN];   // per key: soft rows [lo, hi), linear rows >= llo
     __shared__ float sS[kD];
-    __shared__ float bmx[2][kTM];        // the two half-block maxima of each row
-    __shared__ float lsum[2][2][kTM];    // [soft, linear][half][row] partial denominators
+    __shared__ float bmx[2][2][kTM];     // per block parity, the two half-block maxima of each row
+    __shared__ float lpart[2][kTM];      // the two partial normalisers of each row
 
-    const int tid = threadIdx.x, warp = tid / 32;
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int bh = blockIdx.y;
     const int n = a.n;
     const int t0 = blockIdx.x * kTM, t1 = min(n, t0 + kTM);
@@ -101,269 +162,377 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const TcArgs a
     const int P = a.lam + (t1 - wlo);
     const int nblk = (P + kBN - 1) / kBN;
     const int64_t row0 = (int64_t)bh * n;
-    const int32_t* cpos = a.snapC + ((int64_t)bh * a.nck + c) * a.lam;
-    const int32_t* wst = a.wstep + row0;
+    const bool hide_state = (a.read_mask & LOLA_READ_HIDE_STATE) != 0;
+    auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
-    if (tid == 0) mbar_init(smem_u32(&mbar), 1);
-    if (warp == 0) tmem_alloc<512>(smem_u32(&tmem_base));
-
-    // ---- producers (warps 4-7): the keys of block bb and their rows into stage st ----
-    const int ptid = tid - 128;
-    auto gather = [&](int bb, int st) {
-        if (ptid < kBN) {
-            const int u = bb * kBN + ptid;
-            int p = -1;
-            if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
-            const int w = p >= 0 ? wst[p] : -1;
-            // row r = t - t0 sees key p exactly iff lo <= r < hi, linearly iff r >= llo
-            const int lo = p < 0 ? 255 : min(max(p - t0, 0), 255);
-            int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
-            // the read mask's HIDE_CACHE: only while the key is in the window (t < p + eta)
-            if (p >= 0 && (a.read_mask & LOLA_READ_HIDE_CACHE)) hi = min(hi, min(max(p + a.eta - t0, 0), 255));
-            const int llo = (p < 0 || w < c0) ? 255 : min(max(w - t0, 0), 255);
-            kpos[st][ptid] = p;
-            kinfo[st][ptid] = (uint32_t)lo | ((uint32_t)hi << 8) | ((uint32_t)llo << 16);
+    if (tid == 0) {
+        mbar_init(bar(B_Q), 1);
+        mbar_init(bar(B_H), 1);
+        mbar_init(bar(B_O), 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(bar(B_KVFULL + s), 1);
+            mbar_init(bar(B_KVEMPTY + s), 1);
+            mbar_init(bar(B_SFULL + s), 1);
+            mbar_init(bar(B_SFREE + s), kWeightWarps);
+            mbar_init(bar(B_PFULL + s), kWeightWarps);
         }
-        producers_sync();
-        for (int i = ptid; i < kBN * 16; i += 128) {
-            const int r = i >> 4, c16 = i & 15;
-            const int p = kpos[st][r];
-            const uint32_t off = (c16 >> 3) * 8192 + kmaj_chunk(r, c16 & 7);
-            const uint32_t voff = mnmaj_chunk(r, c16 * 8, kBN);
-            if (p >= 0) {
-                cp_async16(sb + SK(st) + off, a.K + (row0 + p) * kD + c16 * 8);
-                cp_async16(sb + SPK(st) + off, a.phiKb + (row0 + p) * kD + c16 * 8);
-                cp_async16(sb + SV(st) + voff, a.V + (row0 + p) * kD + c16 * 8);
-            } else {
-                *reinterpret_cast<uint4*>(sm + SK(st) + off) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + SPK(st) + off) = make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(sm + SV(st) + voff) = make_uint4(0, 0, 0, 0);
-            }
-        }
-    };
-
-    // ---- stage Q, phi(Q) (rows t0 .. t0 + 127; beyond n: zero), H_c, s_c; block 0 ----
-    for (int i = tid; i < kTM * 16; i += kThreadsTc) {
-        const int r = i >> 4, c16 = i & 15;
-        const uint32_t off = (c16 >> 3) * 16384 + kmaj_chunk(r, c16 & 7);
-        const int t = t0 + r;
-        if (t < n) {
-            cp_async16(sb + SQ + off, a.Q + (row0 + t) * kD + c16 * 8);
-            cp_async16(sb + SPQ + off, a.phiQb + (row0 + t) * kD + c16 * 8);
-        } else {
-            *reinterpret_cast<uint4*>(sm + SQ + off) = make_uint4(0, 0, 0, 0);
-            *reinterpret_cast<uint4*>(sm + SPQ + off) = make_uint4(0, 0, 0, 0);
-        }
-    }
-    {
-        const __nv_bfloat16* sh = a.snapHb + ((int64_t)bh * a.nck + c) * kD * kD;
-        for (int i = tid; i < kD * (kD / 8); i += kThreadsTc) {
-            const int k = i / (kD / 8), n8 = (i % (kD / 8)) * 8;
-            cp_async16(sb + SH + mnmaj_chunk(k, n8, kD), sh + k * kD + n8);
-        }
+        abort_sm = *reinterpret_cast<volatile int*>(a.abort_flag) != 0;
     }
     if (tid < kD) sS[tid] = a.snapS[((int64_t)bh * a.nck + c) * kD + tid];
-    if (warp >= 4) gather(0, 0);
-    cp_async_wait_all();
-    fence_async_smem();
+    if (warp == kMmaWarp) tmem_alloc<512>(smem_u32(&tmem_base));
     fence_before();
     __syncthreads();
     fence_after();
+    const uint32_t tb = tmem_base;
 
-    // per-row state: thread tid owns query row t0 + (tid & 127) and key half hf = tid >> 7
-    // (pool keys 32 hf .. 32 hf + 31 of every block, output columns 64 hf .. 64 hf + 63);
-    // scores in log2 units
-    const int row = tid & (kTM - 1), hf = tid >> 7;
-    const int t = t0 + row;
-    const float c2 = kLog2e / sqrtf((float)kD);
-    float m_run = -INFINITY, l_soft = 0.f, l_lin = 0.f;
-    if (hf == 0) {
-        // phi(q_t)^T s_c from the bf16 phi(Q) tile, in feature order
-        float acc = 0.f;
-#pragma unroll
-        for (int c16 = 0; c16 < 16; ++c16) {
-            const uint4 x = *reinterpret_cast<const uint4*>(sm + SPQ + (c16 >> 3) * 16384 + kmaj_chunk(row, c16 & 7));
-            const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc = fmaf(__uint_as_float(wds[q] << 16), sS[c16 * 8 + 2 * q], acc);
-                acc = fmaf(__uint_as_float(wds[q] & 0xffff0000u), sS[c16 * 8 + 2 * q + 1], acc);
+    // bounded wait on a barrier phase; gives up at once when another role has given up
+    auto wait = [&](int i, uint32_t parity) -> bool {
+        const uint32_t b = bar(i);
+        uint64_t start = 0;
+        for (int it = 0;; ++it) {
+            uint32_t ok;
+            asm volatile(
+                "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}\n"
+                : "=r"(ok)
+                : "r"(b), "r"(parity)
+                : "memory");
+            if (ok) return true;
+            if (*reinterpret_cast<volatile int*>(&abort_sm)) return false;
+            const uint64_t now = globaltimer_ns();
+            if (it == 0) start = now;
+            else if (now - start > kWaitNs) {
+                abort_sm = 1;
+                return false;
             }
         }
-        l_lin = acc;
-    }
-    const uint32_t tb = tmem_base;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t mb = smem_u32(&mbar);
-    uint32_t phase = 0;
-    bool bad = __syncthreads_or(*reinterpret_cast<volatile int*>(a.abort_flag) != 0) != 0;
-
-    // O_lin = phi(Q) H_c, then S, L of block 0
-    auto issue_sl = [&](int st) {
-        constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
-        for (int k = 0; k < kD / 16; ++k) {
-            const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
-            mma_bf16(tb + TS, sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK(st) + bo, 16, 1024), id, k > 0);
-            mma_bf16(tb + TL, sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(st) + bo, 16, 1024), id, k > 0);
-        }
     };
-    if (tid == 0 && !bad) {
-        constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
-        for (int k = 0; k < kD / 16; ++k) {
-            const uint64_t ad = sdesc(sb + SPQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
-            const uint64_t bd = sdesc(sb + SH + k * 2048, 16384, 1024);
-            mma_bf16(tb + TOL, ad, bd, id, k > 0);
-        }
-        issue_sl(0);
-        mma_commit(mb);
-    }
 
-    for (int b = 0; b < nblk && !bad; ++b) {
-        const int st = b & 1;
-        // S, L of block b (and the previous P V, and phi(Q) H_c) have completed
-        const bool ok = mbar_wait(mb, phase, kWaitNs);
-        phase ^= 1;
+    if (warp >= kLoadWarp0) {
+        // ================================ loaders ================================
+        const int ltid = tid - kLoadWarp0 * kWarp;
+        const int32_t* cpos = a.snapC + ((int64_t)bh * a.nck + c) * a.lam;
+        const int32_t* wst = a.wstep + row0;
+        bool ok = !abort_sm;
+        if (ok && ltid == 0) {
+            mbar_expect(bar(B_Q), 3 * 32768);
+            for (int x = 0; x < 2; ++x) {
+                tma_load3(sb + SQ + 16384 * x, &maps.q, 64 * x, t0, bh, bar(B_Q));
+                tma_load3(sb + SPQ + 16384 * x, &maps.pq, 64 * x, t0, bh, bar(B_Q));
+                tma_load3(sb + SH + 16384 * x, &maps.h, 64 * x, 0, bh * a.nck + c, bar(B_Q));
+            }
+        }
+        // positions and row bounds of block bb into ring slot bb % kRing (threads 0..63)
+        auto bounds = [&](int bb) {
+            const int sl = bb & (kRing - 1);
+            if (ltid < kBN) {
+                const int u = bb * kBN + ltid;
+                int p = -1;
+                if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
+                const int w = p >= 0 ? wst[p] : -1;
+                // row r = t - t0 sees key p exactly iff lo <= r < hi, linearly iff r >= llo
+                const int lo = p < 0 ? 255 : min(max(p - t0, 0), 255);
+                int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
+                // the read mask's HIDE_CACHE: only while the key is in the window (t < p + eta)
+                if (p >= 0 && (a.read_mask & LOLA_READ_HIDE_CACHE)) hi = min(hi, min(max(p + a.eta - t0, 0), 255));
+                const int llo = (p < 0 || w < c0 || hide_state) ? 255 : min(max(w - t0, 0), 255);
+                kpos[sl][ltid] = p;
+                kinfo[sl][ltid] = (uint32_t)lo | ((uint32_t)hi << 8) | ((uint32_t)llo << 16);
+            }
+        };
+        for (int bb = 0; bb < min(nblk, kAhead); ++bb) bounds(bb);
+        ok = !loaders_or(!ok);
+        int issued = 0;
+        for (int b = 0; b < nblk && ok; ++b) {
+            const int st = b & 1, u0 = b * kBN, sl = b & (kRing - 1);
+            bool fail = false;
+            if (ltid == 0) {
+                if (b == 1) fail = !wait(B_H, 0);                      // stage 1 overlaps H_c
+                if (!fail && b >= 2) fail = !wait(B_KVEMPTY + st, ((b - 2) >> 1) & 1);
+            }
+            if (loaders_or(fail)) {
+                ok = false;
+                break;
+            }
+            if (u0 >= a.lam) {
+                // window block: consecutive positions wlo + u - lam (rows past the pool are masked)
+                if (ltid == 0) {
+                    const int r0 = wlo + (u0 - a.lam);
+                    mbar_expect(bar(B_KVFULL + st), 3 * 16384);
+                    for (int x = 0; x < 2; ++x) {
+                        tma_load3(sb + SK(st) + 8192 * x, &maps.k, 64 * x, r0, bh, bar(B_KVFULL + st));
+                        tma_load3(sb + SPK(st) + 8192 * x, &maps.pk, 64 * x, r0, bh, bar(B_KVFULL + st));
+                        tma_load3(sb + SV(st) + 8192 * x, &maps.v, 64 * x, r0, bh, bar(B_KVFULL + st));
+                    }
+                }
+            } else {
+                // cache (or mixed) block: gathered rows, zero rows for empty slots
+                for (int i = ltid; i < kBN * 16; i += kLoadThreads) {
+                    const int r = i >> 4, c16 = i & 15;
+                    const int p = kpos[sl][r];
+                    const uint32_t off = (c16 >> 3) * 8192 + kmaj_chunk(r, c16 & 7);
+                    const uint32_t voff = mnmaj_chunk(r, c16 * 8, kBN);
+                    if (p >= 0) {
+                        cp_async16(sb + SK(st) + off, a.K + (row0 + p) * kD + c16 * 8);
+                        cp_async16(sb + SPK(st) + off, a.phiKb + (row0 + p) * kD + c16 * 8);
+                        cp_async16(sb + SV(st) + voff, a.V + (row0 + p) * kD + c16 * 8);
+                    } else {
+                        *reinterpret_cast<uint4*>(sm + SK(st) + off) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(sm + SPK(st) + off) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(sm + SV(st) + voff) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                cp_async_wait_all();
+                fence_async_smem();
+                loaders_or(false);                               // every loader's rows have landed
+                if (ltid == 0) mbar_arrive1(bar(B_KVFULL + st));
+            }
+            if (b + kAhead < nblk) bounds(b + kAhead);   // its slot's block (b - 4) is long weighted
+            loaders_or(false);                           // the ring slot is written before it is read
+            issued = b + 1;
+        }
+        // leave no copy in flight: wait for the stages the loaders filled (bounded)
+        if (ltid == 0 && issued > 0) {
+            const uint64_t t_start = globaltimer_ns();
+            for (int b = max(0, issued - 2); b < issued; ++b)
+                while (!mbar_wait(bar(B_KVFULL + (b & 1)), (b >> 1) & 1, 1000000ull))
+                    if (globaltimer_ns() - t_start > kWaitNs) break;
+        }
+    } else if (warp == kMmaWarp) {
+        // ================================ MMA issue ================================
+        bool ok = !abort_sm && wait(B_Q, 0);
         fence_after();
-        const bool prod = warp >= 4 && b + 1 < nblk;
-        if (prod) gather(b + 1, st ^ 1);   // copies land while this block is weighted
-        {
-            // ---- masks, block maximum, weights for keys 32 hf .. 32 hf + 31 ----
-            const uint32_t* ki = kinfo[st] + 32 * hf;
+        if (lane == 0) {
+            if (ok && !hide_state) {
+                constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint64_t ad = sdesc(sb + SPQ + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024);
+                    const uint64_t bd = sdesc(sb + SH + k * 2048, 16384, 1024);
+                    mma_bf16(tb + TO, ad, bd, id, k > 0);
+                }
+            }
+            mma_commit(bar(B_H));
+            auto pv = [&](int j) -> bool {
+                const int sj = j & 1;
+                if (!wait(B_PFULL + sj, (j >> 1) & 1)) return false;
+                fence_after();
+                constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
+                for (int k = 0; k < kBN / 16; ++k) {
+                    const uint64_t vd = sdesc(sb + SV(sj) + k * 2048, 8192, 1024);
+                    mma_bf16(tb + TO, sdesc(sb + SP(sj) + k * 32, 16, 1024), vd, id, !(hide_state && j == 0 && k == 0));
+                }
+                mma_commit(bar(B_KVEMPTY + sj));
+                return true;
+            };
+            for (int b = 0; b < nblk && ok; ++b) {
+                const int st = b & 1;
+                ok = wait(B_KVFULL + st, (b >> 1) & 1);
+                if (ok && b >= 2) ok = wait(B_SFREE + st, ((b - 2) >> 1) & 1);
+                if (!ok) break;
+                fence_after();
+                constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
+                for (int k = 0; k < kD / 16; ++k) {
+                    const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
+                    mma_bf16(tb + TS(st), sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK(st) + bo, 16, 1024), id, k > 0);
+                    mma_bf16(tb + TL(st), sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(st) + bo, 16, 1024), id, k > 0);
+                }
+                mma_commit(bar(B_SFULL + st));
+                if (b >= 1) ok = pv(b - 1);
+            }
+            if (ok) ok = pv(nblk - 1);
+            mma_commit(bar(B_O));
+            // leave no MMA in flight
+            if (!mbar_wait(bar(B_O), 0, kWaitNs)) abort_sm = 1;
+        }
+        __syncwarp();
+    } else {
+        // ================================ weighting ================================
+        // Every weighting warp runs all nblk iterations and both named-barrier syncs of each,
+        // whatever happens, so the barrier counts always match; after a failed wait (warp-
+        // uniform through __all_sync) an iteration only keeps the counts.
+        const int hf = warp >> 2, row = ((warp & 3) << 5) + lane, t = t0 + row;
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const float c2 = kLog2e / sqrtf((float)kD);
+        auto wwait = [&](int i, uint32_t parity) -> bool { return __all_sync(0xffffffffu, wait(i, parity)); };
+        float m_run = 0.f, lp = 0.f;
+        bool ok = __all_sync(0xffffffffu, !abort_sm) && wwait(B_Q, 0);
+        if (ok && !hide_state) {
+            // phi(q_t)^T s_c over features 64 hf .. 64 hf + 63, from the bf16 phi(Q) tile
+#pragma unroll
+            for (int c8 = 0; c8 < 8; ++c8) {
+                const int c16 = 8 * hf + c8;
+                const uint4 x = *reinterpret_cast<const uint4*>(sm + SPQ + (c16 >> 3) * 16384 + kmaj_chunk(row, c16 & 7));
+                const uint32_t wds[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    lp = fmaf(__uint_as_float(wds[q] << 16), sS[c16 * 8 + 2 * q], lp);
+                    lp = fmaf(__uint_as_float(wds[q] & 0xffff0000u), sS[c16 * 8 + 2 * q + 1], lp);
+                }
+            }
+        }
+        for (int b = 0; b < nblk; ++b) {
+            const int st = b & 1;
+            if (ok) ok = wwait(B_SFULL + st, (b >> 1) & 1) && wwait(B_KVFULL + st, (b >> 1) & 1);
             float sv[32];
             uint32_t vis = 0u;
             float bm = -INFINITY;
-            tmem_ld32(tb + lane_off + TS + 32 * hf, sv);
-            tmem_wait_ld();
+            const uint32_t* ki = kinfo[b & (kRing - 1)] + 32 * hf;
+            if (ok) {
+                fence_after();
+                tmem_ld32(tb + lane_off + TS(st) + 32 * hf, sv);
+                tmem_wait_ld();
+                // ---- masks and this half's maximum ----
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-                const uint32_t info = ki[jj];
-                const bool vs = row >= (int)(info & 255u) && row < (int)((info >> 8) & 255u);
-                vis |= (uint32_t)vs << jj;
-                bm = vs ? fmaxf(bm, sv[jj]) : bm;
-            }
-            bmx[hf][row] = bm;
-            __syncthreads();
-            bm = fmaxf(bmx[0][row], bmx[1][row]) * c2;
-            // lazy rescale of O_soft (columns 64 hf ..); both threads of a row take the same
-            // decision; TMEM accesses stay warp-uniform (factor 1 for the rows that keep m)
-            const bool first = bm > m_run && m_run == -INFINITY;
-            const bool need = bm > m_run && m_run != -INFINITY && bm - m_run > kRescale2;
-            if (first) m_run = bm;
-            if (__any_sync(0xffffffffu, need)) {
-                const float f = need ? ex2(m_run - bm) : 1.f;
-                l_soft *= f;
-                float o[32];
-#pragma unroll
-                for (int cc = 0; cc < kD / 2; cc += 32) {
-                    tmem_ld32(tb + lane_off + TOS + 64 * hf + cc, o);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) o[j] *= f;
-                    tmem_st32(tb + lane_off + TOS + 64 * hf + cc, o);
+                for (int jj = 0; jj < 32; ++jj) {
+                    const uint32_t info = ki[jj];
+                    const bool vs = row >= (int)(info & 255u) && row < (int)((info >> 8) & 255u);
+                    vis |= (uint32_t)vs << jj;
+                    bm = vs ? fmaxf(bm, sv[jj]) : bm;
                 }
-                tmem_wait_st();
-                if (need) m_run = bm;
             }
-            const float mr = m_run;
-            float lv[32];
-            tmem_ld32(tb + lane_off + TL + 32 * hf, lv);
-            tmem_wait_ld();
+            bmx[st][hf][row] = bm;
+            weight_sync();
+            if (!ok) continue;
+            bm = fmaxf(bmx[st][0][row], bmx[st][1][row]) * c2;
+            // lazy rescale: both threads of a row take the same decision; TMEM accesses stay
+            // warp-uniform (factor 1 for the rows that keep m)
+            const bool need = bm > m_run + kRescale2;
+            if (__any_sync(0xffffffffu, need)) {
+                if (b == 0 && hide_state) {
+                    if (need) m_run = bm;                  // O holds nothing yet
+                } else {
+                    // O is quiescent once the product before this block has completed
+                    ok = b >= 1 ? wwait(B_KVEMPTY + ((b - 1) & 1), ((b - 1) >> 1) & 1) : wwait(B_H, 0);
+                    if (!ok) continue;
+                    fence_after();
+                    const float f = need ? ex2(m_run - bm) : 1.f;
+                    lp *= f;
+#pragma unroll
+                    for (int cc = 0; cc < kD / 2; cc += 32) {
+                        float o[32];
+                        tmem_ld32(tb + lane_off + TO + 64 * hf + cc, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) o[j] *= f;
+                        tmem_st32(tb + lane_off + TO + 64 * hf + cc, o);
+                    }
+                    tmem_wait_st();
+                    fence_before();
+                    if (need) m_run = bm;
+                }
+            }
+            const float mr = m_run, em = ex2(-m_run);
+            float lnext[8];
+            // P[st] is free once the product of block b - 2 has completed
+            if (b >= 2) {
+                ok = wwait(B_KVEMPTY + st, ((b - 2) >> 1) & 1);
+                if (!ok) continue;
+            }
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
-                uint32_t ps[4], pl[4];
+                float lv[8];
+                if ((c4 & 1) == 0) {
+                    float l16[16];
+                    tmem_ld16(tb + lane_off + TL(st) + 32 * hf + 8 * c4, l16);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) lv[j] = l16[j];
+                    lnext[0] = l16[8]; lnext[1] = l16[9]; lnext[2] = l16[10]; lnext[3] = l16[11];
+                    lnext[4] = l16[12]; lnext[5] = l16[13]; lnext[6] = l16[14]; lnext[7] = l16[15];
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) lv[j] = lnext[j];
+                }
+                uint32_t pk[4];
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
-                    float e[2], g[2];
+                    float e[2];
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int jj = c4 * 8 + 2 * hh + u;
                         const bool vs = (vis >> jj) & 1u;
                         const bool vl = row >= (int)((ki[jj] >> 16) & 255u);
-                        e[u] = vs ? ex2(fmaf(sv[jj], c2, -mr)) : 0.f;
-                        g[u] = vl ? lv[jj] : 0.f;
+                        e[u] = vs ? ex2(fmaf(sv[jj], c2, -mr)) : (vl ? lv[jj - 8 * c4] * em : 0.f);
                     }
-                    const __nv_bfloat162 bs = __floats2bfloat162_rn(e[0], e[1]);
-                    const __nv_bfloat162 bl = __floats2bfloat162_rn(g[0], g[1]);
-                    const float2 fs = __bfloat1622float2(bs), fl = __bfloat1622float2(bl);
-                    l_soft += fs.x + fs.y;
-                    l_lin += fl.x + fl.y;
-                    ps[hh] = *reinterpret_cast<const uint32_t*>(&bs);
-                    pl[hh] = *reinterpret_cast<const uint32_t*>(&bl);
+                    const __nv_bfloat162 bp = __floats2bfloat162_rn(e[0], e[1]);
+                    const float2 fp = __bfloat1622float2(bp);
+                    lp += fp.x + fp.y;
+                    pk[hh] = *reinterpret_cast<const uint32_t*>(&bp);
                 }
-                const int c16 = 4 * hf + c4;
-                *reinterpret_cast<uint4*>(sm + SPS + kmaj_chunk(row, c16)) = make_uint4(ps[0], ps[1], ps[2], ps[3]);
-                *reinterpret_cast<uint4*>(sm + SPL + kmaj_chunk(row, c16)) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+                *reinterpret_cast<uint4*>(sm + SP(st) + kmaj_chunk(row, 4 * hf + c4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
+            // S[st], L[st] are read: the MMA may overwrite them with block b + 2's products
+            fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(bar(B_SFREE + st));
             fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive1(bar(B_PFULL + st));
         }
-        if (prod) {
-            cp_async_wait_all();
-            fence_async_smem();
-        }
-        fence_before();
-        bad = __syncthreads_or(!ok) != 0;
+        // ---- epilogue: y = O / l; thread (row, hf) writes output columns 64 hf .. 64 hf + 63 ----
+        if (ok) ok = wwait(B_O, 0);
         fence_after();
-        if (bad) break;
-        // ---- O_soft += P_soft V, O_lin += P_lin V; then S, L of the next block ----
-        if (tid == 0) {
-            constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
-            for (int k = 0; k < kBN / 16; ++k) {
-                const uint64_t vd = sdesc(sb + SV(st) + k * 2048, 8192, 1024);
-                mma_bf16(tb + TOS, sdesc(sb + SPS + k * 32, 16, 1024), vd, id, (b > 0 || k > 0));
-                mma_bf16(tb + TOL, sdesc(sb + SPL + k * 32, 16, 1024), vd, id, 1);
-            }
-            if (b + 1 < nblk) issue_sl(st ^ 1);
-            mma_commit(mb);
-        }
-    }
-    if (!bad) {
-        const bool ok = mbar_wait(mb, phase, kWaitNs);
-        fence_after();
-        bad = __syncthreads_or(!ok) != 0;
-    }
-    // ---- epilogue: y = (O_soft + 2^{-m} O_lin) / (l_soft + 2^{-m} l_lin); thread (row, hf)
-    //      writes output columns 64 hf .. 64 hf + 63 ----
-    lsum[0][hf][row] = l_soft;
-    lsum[1][hf][row] = l_lin;
-    __syncthreads();
-    if (!bad) {
-        const float ls = lsum[0][0][row] + lsum[0][1][row], ll = lsum[1][0][row] + lsum[1][1][row];
-        const bool any = m_run != -INFINITY;
-        // HIDE_STATE: the linear terms stay out of the read (then the window's current token
-        // makes any true)
-        const float em = any ? ((a.read_mask & LOLA_READ_HIDE_STATE) ? 0.f : ex2(-m_run)) : 1.f;
-        const float den = any ? fmaf(em, ll, ls) : ll;
-        const float inv = t < n ? 1.0f / den : 0.f;
-        __nv_bfloat16* y = a.Y + (row0 + (t < n ? t : 0)) * kD + 64 * hf;
-        for (int cc = 0; cc < kD / 2; cc += 32) {
-            float os[32], ol[32];
-            tmem_ld32(tb + lane_off + TOS + 64 * hf + cc, os);
-            tmem_ld32(tb + lane_off + TOL + 64 * hf + cc, ol);
-            tmem_wait_ld();
-            uint32_t pk[16];
+        lpart[hf][row] = lp;
+        weight_sync();
+        if (ok) {
+            const float l = lpart[0][row] + lpart[1][row];
+            const float inv = t < n ? 1.0f / l : 0.f;
 #pragma unroll
-            for (int j = 0; j < 32; j += 2) {
-                const float y0 = (any ? fmaf(em, ol[j], os[j]) : ol[j]) * inv;
-                const float y1 = (any ? fmaf(em, ol[j + 1], os[j + 1]) : ol[j + 1]) * inv;
-                const __nv_bfloat162 bv = __floats2bfloat162_rn(y0, y1);
-                pk[j / 2] = *reinterpret_cast<const uint32_t*>(&bv);
-            }
-            if (t < n) {
+            for (int cc = 0; cc < kD / 2; cc += 32) {
+                float o[32];
+                tmem_ld32(tb + lane_off + TO + 64 * hf + cc, o);
+                tmem_wait_ld();
+                uint32_t pk[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(y + cc + 8 * q) =
-                        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int j = 0; j < 32; j += 2) {
+                    const __nv_bfloat162 bv = __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
+                    pk[j / 2] = *reinterpret_cast<const uint32_t*>(&bv);
+                }
+                if (t < n) {
+                    __nv_bfloat16* y = a.Y + (row0 + t) * kD + 64 * hf + cc;
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        *reinterpret_cast<uint4*>(y + 8 * q) =
+                            make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                }
             }
         }
-    }
-    if (bad && tid == 0) {
-        atomicOr(reinterpret_cast<int32_t*>(a.state + (int64_t)bh * a.head_bytes) + HDR_STATUS, (int)ST_TIMEOUT);
-        atomicExch(a.abort_flag, 1);
     }
     fence_before();
     __syncthreads();
     fence_after();
-    if (warp == 0) tmem_dealloc<512>(tb);
+    if (abort_sm && tid == 0) {
+        atomicOr(reinterpret_cast<int32_t*>(a.state + (int64_t)bh * a.head_bytes) + HDR_STATUS, (int)ST_TIMEOUT);
+        atomicExch(a.abort_flag, 1);
+    }
+    if (warp == kMmaWarp) tmem_dealloc<512>(tb);
+}
+
+// ---- tensor maps (the encoder is the driver's, fetched once through the runtime) ----
+PFN_cuTensorMapEncodeTiled_v12000 encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, []() {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+// bf16 tensor [depth][rows][128], boxes of 64 columns x box_rows rows x 1, 128-byte swizzle,
+// rows past `rows` zero-filled
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t depth, int box_rows) {
+    auto enc = encoder();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)rows, (cuuint64_t)depth};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * (cuuint64_t)rows};
+    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -372,6 +541,11 @@ bool output_tc_supported(const Dims& d) { return d.dtype == LOLA_BF16 && d.D == 
 
 cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K, const void* V,
                              void* Y, char* state, int64_t head_bytes, cudaStream_t st) {
+    TcMaps maps;
+    if (!make_map(&maps.q, Q, n, d.BH, kTM) || !make_map(&maps.pq, ws.phiQb, n, d.BH, kTM) ||
+        !make_map(&maps.k, K, n, d.BH, kBN) || !make_map(&maps.pk, ws.phiKb, n, d.BH, kBN) ||
+        !make_map(&maps.v, V, n, d.BH, kBN) || !make_map(&maps.h, ws.snapHb, kD, (int64_t)d.BH * ws.nck, kD))
+        return cudaErrorInvalidValue;
     TcArgs a;
     a.n = n;
     a.eta = d.eta;
@@ -379,14 +553,11 @@ cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const vo
     a.chunk = ws.snap_interval;
     a.nck = ws.nck;
     a.read_mask = d.read_mask;
-    a.Q = static_cast<const __nv_bfloat16*>(Q);
     a.K = static_cast<const __nv_bfloat16*>(K);
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.Y = static_cast<__nv_bfloat16*>(Y);
-    a.phiQb = ws.phiQb;
     a.phiKb = ws.phiKb;
     a.wstep = ws.wstep;
-    a.snapHb = ws.snapHb;
     a.snapS = ws.snapS;
     a.snapC = ws.snapC;
     a.state = state;
@@ -395,7 +566,7 @@ cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const vo
     const size_t smem = SEND + 1024;
     cudaError_t e = cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    output_tc_kernel<<<dim3((n + kTM - 1) / kTM, d.BH), kThreadsTc, smem, st>>>(a);
+    output_tc_kernel<<<dim3((n + kTM - 1) / kTM, d.BH), kThreadsTc, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 
