@@ -58,6 +58,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", default="lola", choices=["lola", "reference"])
     p.add_argument("--workload", default=PREFILL, help="prefill workload of the headline value")
+    p.add_argument("--n", type=int, default=None,
+                   help="override the prefill workload's sequence length (profiling captures of the same kernels "
+                        "on a shorter sequence; the line then names the shortened workload)")
     p.add_argument("--decode-passes", type=int, default=2,
                    help="timed decode passes (each: every decode step of the workload from the post-prefix state)")
     p.add_argument("--no-decode", action="store_true")
@@ -245,11 +248,24 @@ class Clocks:
 # the digest of those files must match, otherwise the traffic is reported as null.
 CSRC = os.path.join(ROOT, "sparse_exact_kv_gb300", "csrc")
 NCU_TRAFFIC = {
+    # long prefill (8 heads): captured on the same configuration at n = 32768 (one launch each) and
+    # scaled x4 to n = 131072 -- every kernel's traffic grows in proportion to the tokens (the
+    # chain streams each key's rows once, the output pass reads one pool per 128-query tile)
+    ("select", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"],
+                                           "digest": "c3da4ad1ac597ac3", "bytes_per_launch": 4 * (208.9e6 + 27.81e6)},
+    ("output", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
+                                           "digest": "33f7134677057231", "bytes_per_launch": 4 * (372.8e6 + 52.93e6)},
+    ("phi", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_internal.cuh"], "digest": "528531d23d367e4a",
+                                        "bytes_per_launch": 4 * (67.21e6 + 140.8e6)},
+    ("phi_q", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_internal.cuh"], "digest": "528531d23d367e4a",
+                                          "bytes_per_launch": 4 * (67.26e6 + 20.33e6)},
+    # 4 x 32 heads, n = 4096: the output pass, one launch (--set full capture)
+    ("output", "w2_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
+                                        "digest": "33f7134677057231", "bytes_per_launch": 810.65e6 + 122.78e6},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
     ("decode", "w4_bf16_decode_b64h32"): {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                          "digest": "850fe64c2562ac87",
-                                          "bytes_per_launch": 2 * (206851584 + 56466483)},
+                                          "digest": "d8033cdd804a5454", "bytes_per_launch": 2 * (206.9e6 + 56.47e6)},
 }
 
 
@@ -528,10 +544,12 @@ def e2e_prefill(L, R, lay, w, Q, K, V, Y, W, wpos, ws, stream, steps):
 PREFILL_KERNELS = ["state_init", "phi", "phi_q", "select", "output"]
 
 
-def run_prefill(L, R, args, pk, name, steps, warmup, e2e=True, sre_map=False):
+def run_prefill(L, R, args, pk, name, steps, warmup, e2e=True, sre_map=False, n=None):
     import torch
     import synth
     w = synth.WORKLOADS[name]
+    if n:
+        w = dataclasses.replace(w, n=n, name=f"{w.name}[n={n}]")
     x = rank_inputs(w, R.rank)
     dev = torch.device("cuda", R.local)
     Q, K, V = (dev_tensor(getattr(x, a), w.dtype, dev) for a in "qkv")
@@ -778,7 +796,7 @@ def main(argv=None):
         R.close()
         return 0
     pre = run_prefill(L, R, args, pk, args.workload, args.steps, args.warmup, e2e=not args.no_e2e,
-                      sre_map=args.sre_map)
+                      sre_map=args.sre_map, n=args.n)
     w = pre["workload"]
     x = pre.pop("x")
     cpu = None
