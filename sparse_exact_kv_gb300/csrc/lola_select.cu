@@ -21,10 +21,11 @@
 //   * per step: apply the previous write; every warp scores its slots and takes its
 //     packed-key minimum with two redux.sync; after the step's single barrier every warp
 //     takes the CTA minimum itself and keeps the decision in registers; with CL > 1 each
-//     CTA pushes its best key and that candidate's phi / v row into every peer's shared
-//     memory with st.async, completing on the peer's exchange mbarrier, so the winner's
-//     row is local whatever CTA owns it (one thread waits on the mbarrier, bounded by 1 s,
-//     and a CTA barrier hands the result to the others);
+//     CTA pushes its best key into every peer's shared memory with st.async, completing on
+//     the peer's exchange mbarrier (one thread waits, bounded by 1 s, and a CTA barrier
+//     hands the keys to the others); when the winner is a cached key, its owner CTA then
+//     pushes its phi / v row the same way to every peer (the evictee, the usual winner, is
+//     held by every CTA, so most steps move no row);
 //   * evictee rows (phi(k_e), v_e) arrive by cp.async four steps ahead.
 // At every chunk start it stores H, s and the cache positions, from which the parallel
 // output kernel rebuilds every query's exact set and linear state.
@@ -175,7 +176,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     __shared__ float zbuf[2], gbuf[2], zpbuf[2], vvbuf[4];
     __shared__ uint2 wkey[2][kSelWarps + 1];         // per-warp minima; [16] = the evictee
     __shared__ uint2 exch[2][kMaxCluster];
-    __shared__ __align__(8) uint64_t xbar[2];        // exchange mbarriers (clusters)
+    __shared__ __align__(8) uint64_t xbar[2];        // key exchange mbarriers (clusters)
+    __shared__ __align__(8) uint64_t rbar[2];        // winner-row mbarriers (clusters)
     __shared__ int x_abort;
     __shared__ __align__(16) float s_sm[D];          // s, written only by the evictee warp's lanes 0-7
 
@@ -215,14 +217,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
     for (int r = 0; r < HR * HC; ++r) h[r] = 0.f;
     if (tid < D) s_sm[tid] = 0.f;
     if (tid < 2) zpbuf[tid] = 0.f;    // z' against the empty memory
-    const uint32_t xbar0 = smem_addr(&xbar[0]);
+    const uint32_t xbar0 = smem_addr(&xbar[0]), rbar0 = smem_addr(&rbar[0]);
     if (tid == 0) {
         x_abort = 0;
         if (CLUSTER) {
             tc::mbar_init(xbar0, 1);
             tc::mbar_init(xbar0 + 8, 1);
+            tc::mbar_init(rbar0, 1);
+            tc::mbar_init(rbar0 + 8, 1);
         }
     }
+    uint32_t rphase = 0u;   // completed phases of rbar[0] (bit 0) and rbar[1] (bit 1) in this CTA
 
     const float* phiK = a.phiK + (int64_t)bh * n * D;
     const int64_t vrow0 = (int64_t)bh * n;
@@ -421,38 +426,14 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
         warp_min_key(k.x, k.y);
         int bc = 0;
         if constexpr (CLUSTER) {
-            // push this CTA's best key (warp 0) and its candidate's row (warps 1..4) to every
-            // peer; the exchange mbarrier of step parity b completes once all CL - 1 peers'
-            // keys and rows have landed here
+            // push this CTA's best key (warp 0) to every peer; the exchange mbarrier of step
+            // parity b completes once all CL - 1 peers' keys have landed here
             const int b = t & 1;
             const uint32_t xb = xbar0 + 8 * b;
-            if (warp == 0 && lane < CL && lane != rank) {
+            if (warp == 0 && lane < CL && lane != rank)
                 st_async_v2(map_rank(smem_addr(&exch[b][rank]), lane), k.x, k.y, map_rank(xb, lane));
-            } else if (warp >= 1 && warp <= 4) {
-                const int code = (int)(k.y & 127u);
-                const unsigned char* sphi_;
-                const unsigned char* sv_;
-                if (k.y == kNoKey) {
-                    sphi_ = reinterpret_cast<const unsigned char*>(zero_phi);
-                    sv_ = reinterpret_cast<const unsigned char*>(zero_v);
-                } else if (code == kEvCode) {
-                    sphi_ = reinterpret_cast<const unsigned char*>(ebuf[t & (kNEB - 1)]);
-                    sv_ = reinterpret_cast<const unsigned char*>(evraw[t & (kNEB - 1)]);
-                } else {
-                    sphi_ = reinterpret_cast<const unsigned char*>(xphi[b][code / kSPW]);
-                    sv_ = reinterpret_cast<const unsigned char*>(xv[b][code / kSPW]);
-                }
-                const uint32_t dst0 = smem_addr(rows + ((size_t)b * CL + rank) * M::kRowBytes);
-                for (int i = tid - kWarp; i < (CL - 1) * RCH; i += 4 * kWarp) {
-                    const int pr = i / RCH, ch = i % RCH;
-                    const int peer = pr < rank ? pr : pr + 1;
-                    const uint4 v = ch < D / 4 ? reinterpret_cast<const uint4*>(sphi_)[ch]
-                                               : reinterpret_cast<const uint4*>(sv_)[ch - D / 4];
-                    st_async_v4(map_rank(dst0 + 16 * ch, peer), v, map_rank(xb, peer));
-                }
-            }
             if (tid == kThreads - 1) {
-                mbar_arrive_expect_tx(xb, (uint32_t)((CL - 1) * (8 + M::kRowBytes)));
+                mbar_arrive_expect_tx(xb, (uint32_t)((CL - 1) * 8));
                 if (!xbar_wait(xb, (uint32_t)(t >> 1) & 1u)) x_abort = 1;
             }
             __syncthreads();
@@ -467,6 +448,37 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             const unsigned hold = __ballot_sync(kFull, lane < CL && c.x == hi && c.y == lo);
             bc = __ffs(hold) - 1;
             k = make_uint2(hi, lo);
+            // a cached key of another CTA is written: its owner pushes the key's phi / v row
+            // (warps 1..4) into rows[b][owner] of every peer, completing on the peer's rbar[b]
+            const int wcode = (int)(k.y & 127u);
+            if (ev && (n_cached + 1 > lam) && wcode != kEvCode) {
+                const uint32_t rb = rbar0 + 8 * b;
+                if (bc == rank) {
+                    if (warp >= 1 && warp <= 4) {
+                        const unsigned char* sphi_ = reinterpret_cast<const unsigned char*>(xphi[b][wcode / kSPW]);
+                        const unsigned char* sv_ = reinterpret_cast<const unsigned char*>(xv[b][wcode / kSPW]);
+                        const uint32_t dst0 = smem_addr(rows + ((size_t)b * CL + rank) * M::kRowBytes);
+                        for (int i = tid - kWarp; i < (CL - 1) * RCH; i += 4 * kWarp) {
+                            const int pr = i / RCH, ch = i % RCH;
+                            const int peer = pr < rank ? pr : pr + 1;
+                            const uint4 v = ch < D / 4 ? reinterpret_cast<const uint4*>(sphi_)[ch]
+                                                       : reinterpret_cast<const uint4*>(sv_)[ch - D / 4];
+                            st_async_v4(map_rank(dst0 + 16 * ch, peer), v, map_rank(rb, peer));
+                        }
+                    }
+                } else {
+                    if (tid == kThreads - 1) {
+                        mbar_arrive_expect_tx(rb, (uint32_t)M::kRowBytes);
+                        if (!xbar_wait(rb, (rphase >> b) & 1u)) x_abort = 1;
+                    }
+                    rphase ^= 1u << b;
+                    __syncthreads();
+                    if (x_abort) {
+                        aborted = true;
+                        break;
+                    }
+                }
+            }
         }
         const int code = (int)(k.y & 127u);
         const int pos = (int)(k.y >> 7);
