@@ -305,13 +305,13 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
     e = cudaMemsetAsync(ws.abort_flag, 0, sizeof(int), st);
     if (e != cudaSuccess) return cuda_fail(e, "workspace flag");
     e = traced(LOLA_KERNEL_PHI, st,
-               [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, ws.phiKb, st); });
+               [&]() { return launch_phi(d, n, K, W, w_head_stride, ws.phiK, ws.phiKb, static_cast<char*>(state), L.head_bytes, ws.abort_flag, st); });
     if (e != cudaSuccess) return cuda_fail(e, "phi(K)");
     if (d.score != LOLA_SCORE_SRE) {
         // query-dependent scores: phi(Q) first (the scores read it in float32), then the
         // chain-free allocation
         e = traced(LOLA_KERNEL_PHI_Q, st,
-                   [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, st); });
+                   [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, static_cast<char*>(state), L.head_bytes, ws.abort_flag, st); });
         if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
         e = traced(LOLA_KERNEL_SELECT, st, [&]() {
             return launch_fixed_select(d, n, ws, Q, K, V, static_cast<char*>(state), L, st);
@@ -334,7 +334,7 @@ int32_t lola_prefill(const lola_config* cfg, int32_t n, const void* Q, const voi
         e = cudaStreamWaitEvent(side->st, side->fork, 0);
         if (e != cudaSuccess) return cuda_fail(e, "fork wait");
         e = traced(LOLA_KERNEL_PHI_Q, side->st,
-                   [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, side->st); });
+                   [&]() { return launch_phi(d, n, Q, W, w_head_stride, ws.phiQ, ws.phiQb, static_cast<char*>(state), L.head_bytes, ws.abort_flag, side->st); });
         if (e != cudaSuccess) return cuda_fail(e, "phi(Q)");
         e = cudaEventRecord(side->join, side->st);
         if (e != cudaSuccess) return cuda_fail(e, "join");
@@ -365,7 +365,7 @@ int32_t lola_decode_step(const lola_config* cfg, void* state, const float* W, in
     if (written_pos && (reinterpret_cast<uintptr_t>(written_pos) & 3)) return LOLA_ERR_INVALID_ARG;
     cudaStream_t st = (cudaStream_t)stream;
     const Layout L = make_layout(d);
-    if (decode_uses_tok_phi(d)) {
+    if (decode_uses_tok_phi(d, w_head_stride)) {
         const cudaError_t e = traced(LOLA_KERNEL_PHI, st, [&]() {
             return launch_tok_phi(d, static_cast<char*>(state), L, W, w_head_stride, q, k, st);
         });

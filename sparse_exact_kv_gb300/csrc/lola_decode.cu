@@ -18,6 +18,7 @@
 #include <climits>
 
 #include "lola_chain.cuh"
+#include "lola_phi_tc.cuh"
 #include "lola_tc.cuh"
 
 namespace lola {
@@ -44,6 +45,7 @@ struct DecArgs {
     int BH;
     int prefetch_ahead;   // heads ahead of this one whose state is prefetched into L2 (0: none)
     int read_mask;        // lola_read_flags: memories left out of the read (the update is unchanged)
+    int tok_phi_ready;    // decode_kernel: phi(q), phi(k) of the token are in tok_phi already
 };
 
 // Ask L2 to fetch [p, p + bytes) with bulk prefetches of at most 16 KB each, issued by
@@ -122,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
 
     // ---- 1. loads: W, tokens, H (H role), s (evictee warp) ----
     const float* Wh = a.W + (int64_t)h * a.w_head_stride;
-    stage_w<DK, D, kThreads>(Ws, Wh, tid);
+    if (!a.tok_phi_ready) stage_w<DK, D, kThreads>(Ws, Wh, tid);
     if (tid < DK) {
         xq[tid] = IO<T>::ld(qin, tid);
         xk[tid] = IO<T>::ld(kin, tid);
@@ -147,7 +149,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_kernel(const DecArgs a) {
     if (ev && eta > 0 && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
 
     // ---- 2. phi(q), phi(k_e), phi(k_{e+1}) ----
-    if (warp == 0) {
+    if (a.tok_phi_ready) {
+        // mapped by the token feature-map kernel that ran before this one
+        const float* tphi = reinterpret_cast<const float*>(rec + a.L.tok_phi);
+        if (tid < D) {
+            phq[tid] = tphi[tid];
+            nk[tid] = tphi[D + tid];
+            if (eta == 0) phe[tid] = tphi[D + tid];
+        }
+    } else if (warp == 0) {
         float ph[D / 32];
         phi_warp<DK, D>(xq, Ws, lane, ph);
 #pragma unroll
@@ -998,11 +1008,120 @@ __global__ void __launch_bounds__(kTokPhiWarps * kWarp) tok_phi_kernel(const Dec
     }
 }
 
+// phi(q) and phi(k) of the token of every head on the tensor cores (phi_uses_tc: bf16,
+// d_k = D = 128, one W for every head), with the arithmetic of the prefill's feature map
+// (lola_phi_tc.cuh), so a decode step continues a prefill bit for bit.  The rows are q of
+// heads 0 .. BH-1, then k of heads 0 .. BH-1; CTA g maps rows 128 g .. + 127: its threads
+// gather the row tile and split W, one thread issues the 24 MMAs, and warp w forms half w / 4
+// of the phi of rows 32 (w % 4) .. + 31 and writes it into each row's tok_phi scratch.
+constexpr int kTokTcThreads = 256;
+constexpr uint32_t kTokSW = 0;
+constexpr uint32_t kTokSX = phitc::kWSplitBytes;
+constexpr uint32_t kTokSEnd = kTokSX + phitc::kXBytes;
+__global__ void __launch_bounds__(kTokTcThreads) tok_phi_tc_kernel(const DecArgs a) {
+    using namespace tc;
+    constexpr int D = phitc::kD;
+    extern __shared__ __align__(1024) uint8_t smraw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sb = smem_u32(sm);
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ uint32_t tmem_base;
+    grid_dep_launch();   // decode_fast_kernel may start its burst now; it waits for this grid
+                         // before it reads tok_phi
+    const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
+    const int BH = a.BH;
+    const int r0 = blockIdx.x * 128;
+    if (tid == 0) mbar_init(smem_u32(&mbar), 1);
+    if (warp == 0) tmem_alloc<phitc::kN>(smem_u32(&tmem_base));
+    // the row tile: 16-byte chunks into the K-major swizzled layout, rows past 2 BH zero (all
+    // of the thread's loads in flight before its first store; W's loads follow)
+    constexpr int kXPer = 128 * 16 / kTokTcThreads;
+    uint4 xv[kXPer];
+#pragma unroll
+    for (int u = 0; u < kXPer; ++u) {
+        const int i = tid + u * kTokTcThreads;
+        const int r = i >> 4, c16 = i & 15, j = r0 + r;
+        xv[u] = make_uint4(0u, 0u, 0u, 0u);
+        if (j < 2 * BH) {
+            const __nv_bfloat16* src = static_cast<const __nv_bfloat16*>(j < BH ? a.q : a.k) +
+                                       (int64_t)(j < BH ? j : j - BH) * phitc::kDK + 8 * c16;
+            xv[u] = *reinterpret_cast<const uint4*>(src);
+        }
+    }
+    phitc::stage_w_split<kTokTcThreads>(sm + kTokSW, a.W, tid);
+#pragma unroll
+    for (int u = 0; u < kXPer; ++u) {
+        const int i = tid + u * kTokTcThreads;
+        const int r = i >> 4, c16 = i & 15;
+        *reinterpret_cast<uint4*>(sm + kTokSX + (c16 >> 3) * phitc::kXAtom + kmaj_chunk(r, c16 & 7)) = xv[u];
+    }
+    fence_async_smem();
+    fence_before();
+    __syncthreads();
+    fence_after();
+    const uint32_t tb = tmem_base;
+    if (tid == 0) {
+        phitc::issue_mma(tb, sb + kTokSX, sb + kTokSW);
+        mma_commit(smem_u32(&mbar));
+    }
+    // with this CTA's own loads in: the state of decode_fast_kernel's first wave (heads
+    // 0 .. prefetch_ahead - 1) into L2, shared among this grid's CTAs; of the window phi ring
+    // only the two rows the step reads (the evictee's and the next one's)
+    if (a.prefetch_ahead > 0 && a.eta > 0) {
+        const int t = reinterpret_cast<const int32_t*>(a.state)[HDR_T];   // all heads are at step t
+        const int wave = a.prefetch_ahead < BH ? a.prefetch_ahead : BH;
+        const int64_t p0 = (int64_t)(t % a.eta) * 4 * D, p1 = (int64_t)((t + 1) % a.eta) * 4 * D;
+        for (int hb = blockIdx.x; hb < wave; hb += gridDim.x) {
+            const char* nr = a.state + (int64_t)hb * a.L.head_bytes;
+            prefetch_l2(nr, a.L.win_phi, tid, kTokTcThreads);
+            prefetch_l2(nr + a.L.c_pos, a.L.head_bytes - a.L.c_pos, tid, kTokTcThreads, 1);
+            prefetch_l2(nr + a.L.win_phi + p0, 4 * D, tid, kTokTcThreads, 2);
+            prefetch_l2(nr + a.L.win_phi + p1, 4 * D, tid, kTokTcThreads, 3);
+        }
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&mbar), 0, kBurstWaitNs));
+    fence_after();
+    const int quarter = warp & 3;
+    const bool neg = warp >= 4;
+    const int j = r0 + 32 * quarter + lane;
+    const int hb = j < BH ? j : j - BH;
+    if (ok) {
+        float z[phitc::kN], e[phitc::kN];
+        phitc::load_z(tb + ((uint32_t)(quarter * 32) << 16), z);
+        phitc::half_phi(z, neg, e);
+        if (j < 2 * BH) {
+            float* out = reinterpret_cast<float*>(a.state + (int64_t)hb * a.L.head_bytes + a.L.tok_phi) +
+                         (j < BH ? 0 : D) + (neg ? phitc::kN : 0);
+#pragma unroll
+            for (int c = 0; c < phitc::kN; c += 4)
+                *reinterpret_cast<float4*>(out + c) = make_float4(e[c], e[c + 1], e[c + 2], e[c + 3]);
+        }
+    } else if (j < 2 * BH && !neg) {
+        atomicOr(reinterpret_cast<int32_t*>(a.state + (int64_t)hb * a.L.head_bytes) + HDR_STATUS, (int)ST_TIMEOUT);
+    }
+    fence_before();
+    __syncthreads();
+    // TMEM is released only after the product has landed (a second, longer bounded wait when
+    // the first one gave up)
+    if (tid == 0 && !ok) mbar_wait(smem_u32(&mbar), 0, 20ull * kBurstWaitNs);
+    __syncthreads();
+    fence_after();
+    if (warp == 0) tmem_dealloc<phitc::kN>(tb);
+}
+
 // the fast path's limits (float32 KV at D = 128 does not fit one CTA's shared memory: the
 // general kernel runs it)
 template <int D, int DV, typename T>
 bool fast_fits(const Dims& d) {
     return d.eta >= 1 && d.eta <= kFastEta && d.lam <= kFastLam && FastSmem<D, DV, T>::TOTAL <= kMaxSmemPerCta;
+}
+
+cudaError_t launch_tok_phi_tc(const Dims& d, const DecArgs& a, cudaStream_t st) {
+    const size_t smem = kTokSEnd + 1024;
+    cudaError_t e = cudaFuncSetAttribute(tok_phi_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    tok_phi_tc_kernel<<<(2 * d.BH + 127) / 128, kTokTcThreads, smem, st>>>(a);
+    return cudaGetLastError();
 }
 
 template <int D, typename T>
@@ -1074,6 +1193,7 @@ DecArgs make_args(const Dims& d, char* state, const Layout& L, const float* W, i
     a.written_pos = written_pos;
     a.BH = d.BH;
     a.read_mask = d.read_mask;
+    a.tok_phi_ready = 0;
     a.prefetch_ahead = 0;
     {
         int dev = 0, sms = 0;
@@ -1085,16 +1205,24 @@ DecArgs make_args(const Dims& d, char* state, const Layout& L, const float* W, i
 }
 }  // namespace
 
-bool decode_uses_tok_phi(const Dims& d) {
+namespace {
+bool decode_is_fast(const Dims& d) {
     const bool bf = d.dtype == LOLA_BF16;
     if (d.D == 128 && d.dv == 128) return bf ? fast_fits<128, 128, __nv_bfloat16>(d) : fast_fits<128, 128, float>(d);
     if (d.D == 64 && d.dv == 64) return bf ? fast_fits<64, 64, __nv_bfloat16>(d) : fast_fits<64, 64, float>(d);
     return false;
 }
+}  // namespace
+
+bool decode_uses_tok_phi(const Dims& d, int64_t w_head_stride) {
+    return decode_is_fast(d) || phi_uses_tc(d, w_head_stride);
+}
 
 cudaError_t launch_tok_phi(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
                            const void* q, const void* k, cudaStream_t st) {
-    const DecArgs a = make_args(d, state, L, W, w_head_stride, q, k, nullptr, nullptr, nullptr);
+    DecArgs a = make_args(d, state, L, W, w_head_stride, q, k, nullptr, nullptr, nullptr);
+    if (!decode_is_fast(d)) a.prefetch_ahead = 0;   // the L2 prefetch serves the fast kernel's layout
+    if (phi_uses_tc(d, w_head_stride)) return launch_tok_phi_tc(d, a, st);
     const bool bf = d.dtype == LOLA_BF16;
     if (d.D == 128 && d.dk == 128)
         return bf ? launch_tok_phi_t<128, __nv_bfloat16>(d, a, st) : launch_tok_phi_t<128, float>(d, a, st);
@@ -1106,7 +1234,8 @@ cudaError_t launch_tok_phi(const Dims& d, char* state, const Layout& L, const fl
 cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
                           const void* q, const void* k, const void* v, void* y, int32_t* written_pos,
                           cudaStream_t st) {
-    const DecArgs a = make_args(d, state, L, W, w_head_stride, q, k, v, y, written_pos);
+    DecArgs a = make_args(d, state, L, W, w_head_stride, q, k, v, y, written_pos);
+    a.tok_phi_ready = phi_uses_tc(d, w_head_stride) ? 1 : 0;
     const bool bf = d.dtype == LOLA_BF16;
     if (d.D == 128 && d.dv == 128)
         return bf ? launch_decode_t<128, 128, __nv_bfloat16>(d, a, st) : launch_decode_t<128, 128, float>(d, a, st);

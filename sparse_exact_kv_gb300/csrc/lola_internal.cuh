@@ -218,8 +218,14 @@ int32_t cuda_fail(cudaError_t e, const char* where);
 // ---------------------------------------------------------------------------------
 // Launchers (each returns the launch's cudaError_t)
 // ---------------------------------------------------------------------------------
+// phi of every row of X ([BH][n][d_k]) into out (float32) and/or out_bf16 ([BH][n][D]); a wait
+// that times out sets ST_TIMEOUT in a head's status word (state, head_bytes) and *abort_flag
 cudaError_t launch_phi(const Dims& d, int n, const void* X, const float* W, int64_t w_head_stride,
-                       float* out, __nv_bfloat16* out_bf16, cudaStream_t st);
+                       float* out, __nv_bfloat16* out_bf16, char* state, int64_t head_bytes, int* abort_flag,
+                       cudaStream_t st);
+// bf16 rows, d_k = D = 128 and one W for every head: phi runs on the tensor cores (the
+// arithmetic of lola_phi_tc.cuh), in the prefill and in the decode step alike
+bool phi_uses_tc(const Dims& d, int64_t w_head_stride);
 cudaError_t launch_select(const Dims& d, int n, const Workspace& ws, const void* K, const void* V,
                           char* state, const Layout& L, cudaStream_t st);
 // the chunk-granular allocation (alloc = LOLA_ALLOC_CHUNK); chunk_mode_fits: its shared
@@ -240,9 +246,10 @@ cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void*
 bool output_tc_supported(const Dims& d);
 cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                              const void* V, void* Y, char* state, int64_t head_bytes, cudaStream_t st);
-// The fast decode kernel reads phi(q), phi(k) of the token from the state's tok_phi scratch:
-// when decode_uses_tok_phi(d), launch_tok_phi must run on the stream first.
-bool decode_uses_tok_phi(const Dims& d);
+// The decode step reads phi(q), phi(k) of the token from the state's tok_phi scratch (the
+// fast kernel always; the general kernel when phi_uses_tc): when decode_uses_tok_phi(d,
+// w_head_stride), launch_tok_phi must run on the stream first.
+bool decode_uses_tok_phi(const Dims& d, int64_t w_head_stride);
 cudaError_t launch_tok_phi(const Dims& d, char* state, const Layout& L, const float* W, int64_t w_head_stride,
                            const void* q, const void* k, cudaStream_t st);
 cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const float* W,

@@ -114,20 +114,6 @@ __device__ __forceinline__ bool loaders_or(bool x) {
         : "memory");
     return r != 0;
 }
-__device__ __forceinline__ void mbar_arrive1(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void mbar_expect(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-// TMA: box (x, y, z) of a 3-D tensor map into shared memory, completing on `bar`
-__device__ __forceinline__ void tma_load3(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-            dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
-        : "memory");
-}
 // 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective)
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
     uint32_t r[16];
@@ -508,7 +494,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
     if (warp == kMmaWarp) tmem_dealloc<512>(tb);
 }
 
-// ---- tensor maps (the encoder is the driver's, fetched once through the runtime) ----
+// bf16 tensor [depth][rows][128], boxes of 64 columns x box_rows rows x 1, 128-byte swizzle,
+// rows past `rows` zero-filled
+bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t depth, int box_rows) {
+    return make_tmap3(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, kD, rows, depth, 64, box_rows);
+}
+
+}  // namespace
+
+namespace tc {
+namespace {
 PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -521,21 +516,21 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
     });
     return fn;
 }
-// bf16 tensor [depth][rows][128], boxes of 64 columns x box_rows rows x 1, 128-byte swizzle,
-// rows past `rows` zero-filled
-bool make_map(CUtensorMap* m, const void* base, int64_t rows, int64_t depth, int box_rows) {
+}  // namespace
+
+bool make_tmap3(CUtensorMap* m, CUtensorMapDataType type, int elem_bytes, const void* base, int64_t inner,
+                int64_t rows, int64_t depth, int box_inner, int box_rows) {
     auto enc = encoder();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)rows, (cuuint64_t)depth};
-    const cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)kD * 2 * (cuuint64_t)rows};
-    const cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    const cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)depth};
+    const cuuint64_t strides[2] = {(cuuint64_t)(inner * elem_bytes), (cuuint64_t)(inner * elem_bytes * rows)};
+    const cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+    return enc(m, type, 3, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
-
-}  // namespace
+}  // namespace tc
 
 bool output_tc_supported(const Dims& d) { return d.dtype == LOLA_BF16 && d.D == kD && d.dk == kD && d.dv == kD; }
 
