@@ -556,6 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     int32_t* hdr = reinterpret_cast<int32_t*>(rec);
     const int t = hdr[HDR_T];
     const int nc = hdr[HDR_NCACHE];
+    const int nwr = hdr[HDR_NWRITTEN];
     float* Hg = reinterpret_cast<float*>(rec + a.L.H);
     float* sg = reinterpret_cast<float*>(rec + a.L.s);
     int32_t* winpos = reinterpret_cast<int32_t*>(rec + a.L.win_pos);
@@ -575,6 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const int ring = t % eta;
     const bool nxt = t + 1 - eta >= 0;
     const int nring = (t + 1) % eta;
+    const int wpr = (ev && tid == 0) ? winpos[ring] : e;   // checked once the burst is in
 
     // ---- 1. one burst of bulk copies issued by lanes of warp 0 (the TMA engine moves them
     //         while the threads load): the exact KV of cache and window, the slots' phi, the
@@ -638,7 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         }
         return;
     }
-    if (ev && tid == 0 && winpos[ring] != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
+    if (wpr != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
     // the state of the head one wave ahead, into L2 (all heads step together, so its window
     // ring rows for this step are ring and nring as here); the window phi ring is skipped
     // but for those two rows
@@ -934,7 +936,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         winpos[ring] = t;
         hdr[HDR_T] = t + 1;
         hdr[HDR_NCACHE] = nc_after;
-        if (write) hdr[HDR_NWRITTEN] += 1;
+        if (write) hdr[HDR_NWRITTEN] = nwr + 1;
         if (a.written_pos) a.written_pos[bh] = wposn;
         bulk_wait_read();   // the bulk stores' shared-memory sources are read before the CTA ends
     }

@@ -60,23 +60,32 @@ constexpr int kRing = 8;                 // blocks of key positions / row bounds
 constexpr int kAhead = 4;                // blocks of row bounds computed ahead of the loads
 constexpr uint64_t kWaitNs = 1000000000ull;  // a stage not reached within 1 s is an error
 
-// shared-memory map (bytes from a 1024-aligned base).  Stage 1's K and phi(K) tiles reuse
-// the H_c tile once phi(Q) H_c has completed.
+// shared-memory map (bytes from a 1024-aligned base): Q, phi(Q), then three stages of a pool
+// block (K, phi(K) K-major [64 x 64] atoms; V MN-major [64 x d_v]).  Stage 1's K and phi(K)
+// tiles reuse the H_c tile once phi(Q) H_c has completed.
+constexpr int kStages = 3;
 constexpr uint32_t SQ = 0;               // Q tile      K-major, 2 atoms x [128 x 64]
 constexpr uint32_t SPQ = 32768;          // phi(Q) tile K-major
 constexpr uint32_t SH = 98304;           // H_c         MN-major [K = D x N = d_v], 2 atoms
-__device__ __forceinline__ uint32_t SK(int st) { return st ? 98304u : 65536u; }    // K block, 2 atoms x [64 x 64]
-__device__ __forceinline__ uint32_t SPK(int st) { return st ? 114688u : 81920u; }  // phi(K) block
-__device__ __forceinline__ uint32_t SV(int st) { return st ? 147456u : 131072u; }  // V block MN-major [64 x d_v]
-__device__ __forceinline__ uint32_t SP(int st) { return st ? 180224u : 163840u; }  // P K-major [128 x 64]
-constexpr uint32_t SEND = 196608;
-// TMEM columns: S and L double-buffered, then O
+__device__ __forceinline__ uint32_t SK(int st) { return st == 0 ? 65536u : (st == 1 ? 98304u : 180224u); }
+__device__ __forceinline__ uint32_t SPK(int st) { return st == 0 ? 81920u : (st == 1 ? 114688u : 196608u); }
+__device__ __forceinline__ uint32_t SV(int st) { return 131072u + 16384u * (uint32_t)st; }
+constexpr uint32_t SEND = 212992;
+// TMEM columns: S and L double-buffered, O, then the bf16 weights P (two buffers of 128 x 64,
+// two per 32-bit column): the P V product reads its A operand from TMEM
 __device__ __forceinline__ uint32_t TS(int st) { return st ? 64u : 0u; }
 __device__ __forceinline__ uint32_t TL(int st) { return st ? 192u : 128u; }
 constexpr uint32_t TO = 256;
+__device__ __forceinline__ uint32_t TP(int st) { return st ? 416u : 384u; }
 
 // barrier slots
-enum { B_Q = 0, B_H = 1, B_O = 2, B_KVFULL = 3, B_KVEMPTY = 5, B_SFULL = 7, B_SFREE = 9, B_PFULL = 11, B_NBARS = 13 };
+enum {
+    B_Q = 0, B_H = 1, B_O = 2, B_KVFULL = 3, B_KVEMPTY = B_KVFULL + kStages, B_SFULL = B_KVEMPTY + kStages,
+    B_SFREE = B_SFULL + 2, B_PFULL = B_SFREE + 2, B_NBARS = B_PFULL + 2
+};
+// a pool block's stage is full after kLoadThreads + 1 arrivals: every loader thread's (its
+// cp.async gathers landed, or a plain arrival for a TMA block), and loader 0's after the
+// row bounds written ahead are in
 
 struct TcMaps {
     CUtensorMap q, pq, k, pk, v, h;      // 3-D bf16 maps, 64-column boxes, 128-byte swizzle
@@ -155,9 +164,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
         mbar_init(bar(B_Q), 1);
         mbar_init(bar(B_H), 1);
         mbar_init(bar(B_O), 1);
-        for (int s = 0; s < 2; ++s) {
-            mbar_init(bar(B_KVFULL + s), 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bar(B_KVFULL + s), kLoadThreads + 1);
             mbar_init(bar(B_KVEMPTY + s), 1);
+        }
+        for (int s = 0; s < 2; ++s) {
             mbar_init(bar(B_SFULL + s), 1);
             mbar_init(bar(B_SFREE + s), kWeightWarps);
             mbar_init(bar(B_PFULL + s), kWeightWarps);
@@ -230,11 +241,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
         ok = !loaders_or(!ok);
         int issued = 0;
         for (int b = 0; b < nblk && ok; ++b) {
-            const int st = b & 1, u0 = b * kBN, sl = b & (kRing - 1);
+            const int st = b % kStages, u0 = b * kBN, sl = b & (kRing - 1);
             bool fail = false;
             if (ltid == 0) {
                 if (b == 1) fail = !wait(B_H, 0);                      // stage 1 overlaps H_c
-                if (!fail && b >= 2) fail = !wait(B_KVEMPTY + st, ((b - 2) >> 1) & 1);
+                if (!fail && b >= kStages) fail = !wait(B_KVEMPTY + st, ((b - kStages) / kStages) & 1);
             }
             if (loaders_or(fail)) {
                 ok = false;
@@ -250,38 +261,37 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                         tma_load3(sb + SPK(st) + 8192 * x, &maps.pk, 64 * x, r0, bh, bar(B_KVFULL + st));
                         tma_load3(sb + SV(st) + 8192 * x, &maps.v, 64 * x, r0, bh, bar(B_KVFULL + st));
                     }
+                } else {
+                    mbar_arrive1(bar(B_KVFULL + st));
                 }
             } else {
-                // cache (or mixed) block: gathered rows, zero rows for empty slots
+                // cache (or mixed) block: gathered rows, zero rows for empty slots; each thread's
+                // arrival waits for its own copies, so the loaders move on at once
                 for (int i = ltid; i < kBN * 16; i += kLoadThreads) {
                     const int r = i >> 4, c16 = i & 15;
                     const int p = kpos[sl][r];
                     const uint32_t off = (c16 >> 3) * 8192 + kmaj_chunk(r, c16 & 7);
                     const uint32_t voff = mnmaj_chunk(r, c16 * 8, kBN);
-                    if (p >= 0) {
-                        cp_async16(sb + SK(st) + off, a.K + (row0 + p) * kD + c16 * 8);
-                        cp_async16(sb + SPK(st) + off, a.phiKb + (row0 + p) * kD + c16 * 8);
-                        cp_async16(sb + SV(st) + voff, a.V + (row0 + p) * kD + c16 * 8);
-                    } else {
-                        *reinterpret_cast<uint4*>(sm + SK(st) + off) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(sm + SPK(st) + off) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(sm + SV(st) + voff) = make_uint4(0, 0, 0, 0);
-                    }
+                    const int64_t g = (row0 + (p >= 0 ? p : 0)) * kD + c16 * 8;
+                    const uint32_t nb = p >= 0 ? 16u : 0u;
+                    cp_async16_z(sb + SK(st) + off, a.K + g, nb);
+                    cp_async16_z(sb + SPK(st) + off, a.phiKb + g, nb);
+                    cp_async16_z(sb + SV(st) + voff, a.V + g, nb);
                 }
-                cp_async_wait_all();
-                fence_async_smem();
-                loaders_or(false);                               // every loader's rows have landed
-                if (ltid == 0) mbar_arrive1(bar(B_KVFULL + st));
+                cp_async_arrive_noinc(bar(B_KVFULL + st));
             }
             if (b + kAhead < nblk) bounds(b + kAhead);   // its slot's block (b - 4) is long weighted
             loaders_or(false);                           // the ring slot is written before it is read
+            if (ltid == 0) mbar_arrive1(bar(B_KVFULL + st));   // (releases the ring slots written so far)
             issued = b + 1;
         }
-        // leave no copy in flight: wait for the stages the loaders filled (bounded)
+        // leave no copy in flight: this thread's gathers, then the stages the loaders filled
+        // (bounded)
+        cp_async_wait_all();
         if (ltid == 0 && issued > 0) {
             const uint64_t t_start = globaltimer_ns();
-            for (int b = max(0, issued - 2); b < issued; ++b)
-                while (!mbar_wait(bar(B_KVFULL + (b & 1)), (b >> 1) & 1, 1000000ull))
+            for (int b = max(0, issued - kStages); b < issued; ++b)
+                while (!mbar_wait(bar(B_KVFULL + b % kStages), (b / kStages) & 1, 1000000ull))
                     if (globaltimer_ns() - t_start > kWaitNs) break;
         }
     } else if (warp == kMmaWarp) {
@@ -299,28 +309,29 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
             }
             mma_commit(bar(B_H));
             auto pv = [&](int j) -> bool {
-                const int sj = j & 1;
+                const int sj = j & 1, kv = j % kStages;
                 if (!wait(B_PFULL + sj, (j >> 1) & 1)) return false;
                 fence_after();
                 constexpr uint32_t id = idesc_bf16(kTM, kD, 1);
                 for (int k = 0; k < kBN / 16; ++k) {
-                    const uint64_t vd = sdesc(sb + SV(sj) + k * 2048, 8192, 1024);
-                    mma_bf16(tb + TO, sdesc(sb + SP(sj) + k * 32, 16, 1024), vd, id, !(hide_state && j == 0 && k == 0));
+                    const uint64_t vd = sdesc(sb + SV(kv) + k * 2048, 8192, 1024);
+                    mma_bf16_ts(tb + TO, tb + TP(sj) + 8 * k, vd, id, !(hide_state && j == 0 && k == 0));
                 }
-                mma_commit(bar(B_KVEMPTY + sj));
+                mma_commit(bar(B_KVEMPTY + kv));
                 return true;
             };
             for (int b = 0; b < nblk && ok; ++b) {
-                const int st = b & 1;
-                ok = wait(B_KVFULL + st, (b >> 1) & 1);
+                const int st = b & 1, kv = b % kStages;
+                ok = wait(B_KVFULL + kv, (b / kStages) & 1);
                 if (ok && b >= 2) ok = wait(B_SFREE + st, ((b - 2) >> 1) & 1);
                 if (!ok) break;
                 fence_after();
+                fence_async_smem();   // rows gathered by cp.async (generic proxy) before the MMA reads them
                 constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
-                    mma_bf16(tb + TS(st), sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK(st) + bo, 16, 1024), id, k > 0);
-                    mma_bf16(tb + TL(st), sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(st) + bo, 16, 1024), id, k > 0);
+                    mma_bf16(tb + TS(st), sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK(kv) + bo, 16, 1024), id, k > 0);
+                    mma_bf16(tb + TL(st), sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(kv) + bo, 16, 1024), id, k > 0);
                 }
                 mma_commit(bar(B_SFULL + st));
                 if (b >= 1) ok = pv(b - 1);
@@ -358,7 +369,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
         }
         for (int b = 0; b < nblk; ++b) {
             const int st = b & 1;
-            if (ok) ok = wwait(B_SFULL + st, (b >> 1) & 1) && wwait(B_KVFULL + st, (b >> 1) & 1);
+            if (ok) ok = wwait(B_SFULL + st, (b >> 1) & 1) && wwait(B_KVFULL + b % kStages, (b / kStages) & 1);
             float sv[32];
             uint32_t vis = 0u;
             float bm = -INFINITY;
@@ -388,7 +399,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                     if (need) m_run = bm;                  // O holds nothing yet
                 } else {
                     // O is quiescent once the product before this block has completed
-                    ok = b >= 1 ? wwait(B_KVEMPTY + ((b - 1) & 1), ((b - 1) >> 1) & 1) : wwait(B_H, 0);
+                    ok = b >= 1 ? wwait(B_KVEMPTY + (b - 1) % kStages, ((b - 1) / kStages) & 1) : wwait(B_H, 0);
                     if (!ok) continue;
                     fence_after();
                     const float f = need ? ex2(m_run - bm) : 1.f;
@@ -411,9 +422,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
             float lnext[8];
             // P[st] is free once the product of block b - 2 has completed
             if (b >= 2) {
-                ok = wwait(B_KVEMPTY + st, ((b - 2) >> 1) & 1);
+                ok = wwait(B_KVEMPTY + (b - 2) % kStages, ((b - 2) / kStages) & 1);
                 if (!ok) continue;
             }
+            uint32_t pw[16];   // this thread's 32 weights, bf16 pairs
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 float lv[8];
@@ -429,7 +441,6 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
 #pragma unroll
                     for (int j = 0; j < 8; ++j) lv[j] = lnext[j];
                 }
-                uint32_t pk[4];
 #pragma unroll
                 for (int hh = 0; hh < 4; ++hh) {
                     float e[2];
@@ -443,17 +454,19 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                     const __nv_bfloat162 bp = __floats2bfloat162_rn(e[0], e[1]);
                     const float2 fp = __bfloat1622float2(bp);
                     lp += fp.x + fp.y;
-                    pk[hh] = *reinterpret_cast<const uint32_t*>(&bp);
+                    pw[4 * c4 + hh] = *reinterpret_cast<const uint32_t*>(&bp);
                 }
-                *reinterpret_cast<uint4*>(sm + SP(st) + kmaj_chunk(row, 4 * hf + c4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            // S[st], L[st] are read: the MMA may overwrite them with block b + 2's products
+            tmem_st16(tb + lane_off + TP(st) + 16 * hf, pw);
+            tmem_wait_st();
+            // S[st], L[st] are read and P[st] is written: the MMA may overwrite S, L with block
+            // b + 2's products and read P
             fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive1(bar(B_SFREE + st));
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive1(bar(B_PFULL + st));
+            if (lane == 0) {
+                mbar_arrive1(bar(B_SFREE + st));
+                mbar_arrive1(bar(B_PFULL + st));
+            }
         }
         // ---- epilogue: y = O / l; thread (row, hf) writes output columns 64 hf .. 64 hf + 63 ----
         if (ok) ok = wwait(B_O, 0);
