@@ -144,6 +144,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
     __shared__ int abort_sm;
     __shared__ int kpos[kRing][kBN];
     __shared__ __align__(16) uint32_t kinfo[kRing][kBN];   // per key: soft rows [lo, hi), linear rows >= llo
+    __shared__ uint32_t kfull[kRing][2];   // per half block: max lo | min hi << 8 over its 32 keys
     __shared__ float sS[kD];
     __shared__ float bmx[2][2][kTM];     // per block parity, the two half-block maxima of each row
     __shared__ float lpart[2][kTM];      // the two partial normalisers of each row
@@ -235,6 +236,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 const int llo = (p < 0 || w < c0 || hide_state) ? 255 : min(max(w - t0, 0), 255);
                 kpos[sl][ltid] = p;
                 kinfo[sl][ltid] = (uint32_t)lo | ((uint32_t)hi << 8) | ((uint32_t)llo << 16);
+                // the rows for which every key of this half block is exact: [max lo, min hi)
+                const uint32_t mlo = __reduce_max_sync(0xffffffffu, (uint32_t)lo);
+                const uint32_t mhi = __reduce_min_sync(0xffffffffu, (uint32_t)hi);
+                if ((ltid & 31) == 0) kfull[sl][ltid >> 5] = mlo | (mhi << 8);
             }
         };
         for (int bb = 0; bb < min(nblk, kAhead); ++bb) bounds(bb);
@@ -374,17 +379,32 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
             uint32_t vis = 0u;
             float bm = -INFINITY;
             const uint32_t* ki = kinfo[b & (kRing - 1)] + 32 * hf;
+            // every key of this half block exact for all 32 rows of the warp: no masks, no L
+            const uint32_t kf = kfull[b & (kRing - 1)][hf];
+            const int rbase = (warp & 3) * 32;
+            const bool full = (int)(kf & 255u) <= rbase && (int)((kf >> 8) & 255u) >= rbase + 32;
             if (ok) {
                 fence_after();
                 tmem_ld32(tb + lane_off + TS(st) + 32 * hf, sv);
                 tmem_wait_ld();
                 // ---- masks and this half's maximum ----
+                if (full) {
+                    vis = 0xffffffffu;
 #pragma unroll
-                for (int jj = 0; jj < 32; ++jj) {
-                    const uint32_t info = ki[jj];
-                    const bool vs = row >= (int)(info & 255u) && row < (int)((info >> 8) & 255u);
-                    vis |= (uint32_t)vs << jj;
-                    bm = vs ? fmaxf(bm, sv[jj]) : bm;
+                    for (int jj = 0; jj < 32; ++jj) bm = fmaxf(bm, sv[jj]);
+                } else {
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const uint4 in4 = reinterpret_cast<const uint4*>(ki)[j4];
+                        const uint32_t iv[4] = {in4.x, in4.y, in4.z, in4.w};
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int jj = 4 * j4 + q;
+                            const bool vs = row >= (int)(iv[q] & 255u) && row < (int)((iv[q] >> 8) & 255u);
+                            vis |= (uint32_t)vs << jj;
+                            bm = vs ? fmaxf(bm, sv[jj]) : bm;
+                        }
+                    }
                 }
             }
             bmx[st][hf][row] = bm;
@@ -426,6 +446,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 if (!ok) continue;
             }
             uint32_t pw[16];   // this thread's 32 weights, bf16 pairs
+            if (full) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float e0 = ex2(fmaf(sv[2 * i], c2, -mr)), e1 = ex2(fmaf(sv[2 * i + 1], c2, -mr));
+                    const __nv_bfloat162 bp = __floats2bfloat162_rn(e0, e1);
+                    const float2 fp = __bfloat1622float2(bp);
+                    lp += fp.x + fp.y;
+                    pw[i] = *reinterpret_cast<const uint32_t*>(&bp);
+                }
+            } else
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 float lv[8];
