@@ -202,6 +202,13 @@ class Clocks:
                                          stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+        # the timed region starts once nvidia-smi has written its first sample: its start-up
+        # (NVML initialisation) can hold the driver for seconds and stall the launches
+        t0 = time.time()
+        while self.proc is not None and time.time() - t0 < 15.0:
+            if os.path.getsize(self.path) > 0 or self.proc.poll() is not None:
+                break
+            time.sleep(0.05)
         time.sleep(0.3)
         return self
 

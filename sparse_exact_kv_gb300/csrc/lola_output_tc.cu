@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
     __shared__ int abort_sm;
     __shared__ int kpos[kRing][kBN];
     __shared__ __align__(16) uint32_t kinfo[kRing][kBN];   // per key: soft rows [lo, hi), linear rows >= llo
-    __shared__ uint32_t kfull[kRing][2];   // per half block: max lo | min hi << 8 over its 32 keys
+    __shared__ uint32_t kfull[kRing][2];   // per half block: max lo | min hi << 8 | min llo << 16 over its 32 keys
     __shared__ float sS[kD];
     __shared__ float bmx[2][2][kTM];     // per block parity, the two half-block maxima of each row
     __shared__ float lpart[2][kTM];      // the two partial normalisers of each row
@@ -239,7 +239,8 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 // the rows for which every key of this half block is exact: [max lo, min hi)
                 const uint32_t mlo = __reduce_max_sync(0xffffffffu, (uint32_t)lo);
                 const uint32_t mhi = __reduce_min_sync(0xffffffffu, (uint32_t)hi);
-                if ((ltid & 31) == 0) kfull[sl][ltid >> 5] = mlo | (mhi << 8);
+                const uint32_t mll = __reduce_min_sync(0xffffffffu, (uint32_t)llo);
+                if ((ltid & 31) == 0) kfull[sl][ltid >> 5] = mlo | (mhi << 8) | (mll << 16);
             }
         };
         for (int bb = 0; bb < min(nblk, kAhead); ++bb) bounds(bb);
@@ -332,11 +333,15 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 if (!ok) break;
                 fence_after();
                 fence_async_smem();   // rows gathered by cp.async (generic proxy) before the MMA reads them
+                // L only when some key of the block is linear for some row of the tile
+                const uint32_t f0 = kfull[b & (kRing - 1)][0], f1 = kfull[b & (kRing - 1)][1];
+                const bool need_l = min((f0 >> 16) & 255u, (f1 >> 16) & 255u) < (uint32_t)kTM;
                 constexpr uint32_t id = idesc_bf16(kTM, kBN, 0);
                 for (int k = 0; k < kD / 16; ++k) {
                     const uint32_t ao = (k >> 2) * 16384 + (k & 3) * 32, bo = (k >> 2) * 8192 + (k & 3) * 32;
                     mma_bf16(tb + TS(st), sdesc(sb + SQ + ao, 16, 1024), sdesc(sb + SK(kv) + bo, 16, 1024), id, k > 0);
-                    mma_bf16(tb + TL(st), sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(kv) + bo, 16, 1024), id, k > 0);
+                    if (need_l)
+                        mma_bf16(tb + TL(st), sdesc(sb + SPQ + ao, 16, 1024), sdesc(sb + SPK(kv) + bo, 16, 1024), id, k > 0);
                 }
                 mma_commit(bar(B_SFULL + st));
                 if (b >= 1) ok = pv(b - 1);
