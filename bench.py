@@ -259,13 +259,13 @@ NCU_TRAFFIC = {
     # scaled x4 to n = 131072 -- every kernel's traffic grows in proportion to the tokens (the
     # chain streams each key's rows once, the output pass reads one pool per 128-query tile)
     ("select", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                           "digest": "c3da4ad1ac597ac3", "bytes_per_launch": 4 * (208.9e6 + 27.81e6)},
+                                           "digest": "942e14a39edfba5c", "bytes_per_launch": 4 * (207.43e6 + 27.64e6)},
     ("output", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                           "digest": "33f7134677057231", "bytes_per_launch": 4 * (372.8e6 + 52.93e6)},
-    ("phi", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_internal.cuh"], "digest": "528531d23d367e4a",
-                                        "bytes_per_launch": 4 * (67.21e6 + 140.8e6)},
-    ("phi_q", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_internal.cuh"], "digest": "528531d23d367e4a",
-                                          "bytes_per_launch": 4 * (67.26e6 + 20.33e6)},
+                                           "digest": "dc476ed3069109fa", "bytes_per_launch": 4 * (372.91e6 + 53.16e6)},
+    ("phi", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
+                                        "digest": "45133dcab50d1c6f", "bytes_per_launch": 4 * (67.20e6 + 140.72e6)},
+    ("phi_q", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
+                                          "digest": "45133dcab50d1c6f", "bytes_per_launch": 4 * (67.19e6 + 12.99e6)},
     # 4 x 32 heads, n = 4096: the output pass, one launch (--set full capture)
     ("output", "w2_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
                                         "digest": "33f7134677057231", "bytes_per_launch": 810.65e6 + 122.78e6},
