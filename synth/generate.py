@@ -263,3 +263,69 @@ def gauss_inputs(B: int, Hh: int, n: int, d: int, D: int, dtype: str = "f32", se
     v = normal(seed, _S_V, B * Hh * n * dv, out=dtype).reshape(B, Hh, n, dv)
     W = feature_weight(seed, D, d)
     return Inputs(w, n, q, k, v, W)
+
+
+# ---------------------------------------------------------------------------
+# The write-magnitude cache on a gated delta-rule state: per-token gates and the
+# cache path's scales, drawn like every other input
+# ---------------------------------------------------------------------------
+
+_S_ALPHA, _S_BETA, _S_GQ, _S_GK, _S_SINK, _S_GATE = 5, 6, 7, 8, 9, 10
+
+
+def uniform(seed: int, stream: int, count: int) -> np.ndarray:
+    """``count`` values uniform in [0, 1) of stream (seed, stream): (word >> 11) 2^-53, float64."""
+    return (uniform_bits(seed, stream, count) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+
+
+@dataclasses.dataclass
+class HolaInputs:
+    """Inputs of one delta-rule-state layer with a write-magnitude cache.  ``q``, ``k``, ``v``
+    hold the storage dtype (as in ``Inputs``); the gates and scales are float32:
+    ``alpha`` (decay) in (0.9, 1] and ``beta`` (write strength) in [0, 1) per (b, h, t),
+    ``gamma_q``, ``gamma_k`` (cache-path scales, 1 + 0.1 N(0,1)) per channel, ``sink`` (the
+    null entry's logit, N(0,1)) and ``gate`` (the cache read's weight, in [0.5, 1.5)) per head."""
+    B: int
+    Hh: int
+    n: int
+    d: int
+    w: int
+    chunk: int
+    dtype: str
+    q: np.ndarray
+    k: np.ndarray
+    v: np.ndarray
+    alpha: np.ndarray
+    beta: np.ndarray
+    gamma_q: np.ndarray
+    gamma_k: np.ndarray
+    sink: np.ndarray
+    gate: np.ndarray
+
+    def widened(self, name: str) -> np.ndarray:
+        """Exact float64 copy of q, k or v."""
+        a = getattr(self, name)
+        if self.dtype == "bf16":
+            return bf16_bits_to_f32(a).astype(np.float64)
+        return a.astype(np.float64)
+
+
+def hola_inputs(B: int, Hh: int, n: int, d: int, w: int = 64, chunk: int = 256, dtype: str = "bf16",
+                seed: int = 0) -> HolaInputs:
+    """Gaussian q, k, v and the gate / scale recipe above (no row normalisation: the layer
+    normalises its keys and queries itself)."""
+    cnt = B * Hh * n * d
+    q = normal(seed, _S_Q, cnt, out=dtype).reshape(B, Hh, n, d)
+    k = normal(seed, _S_K, cnt, out=dtype).reshape(B, Hh, n, d)
+    v = normal(seed, _S_V, cnt, out=dtype).reshape(B, Hh, n, d)
+    alpha = (1.0 - 0.1 * uniform(seed, _S_ALPHA, B * Hh * n)).astype(np.float32).reshape(B, Hh, n)
+    beta = uniform(seed, _S_BETA, B * Hh * n).astype(np.float32).reshape(B, Hh, n)
+    gamma_q = (1.0 + 0.1 * normal(seed, _S_GQ, d)).astype(np.float32)
+    gamma_k = (1.0 + 0.1 * normal(seed, _S_GK, d)).astype(np.float32)
+    sink = normal(seed, _S_SINK, Hh).astype(np.float32)
+    gate = (0.5 + uniform(seed, _S_GATE, Hh)).astype(np.float32)
+    return HolaInputs(B, Hh, n, d, w, chunk, dtype, q, k, v, alpha, beta, gamma_q, gamma_k, sink, gate)
+
+
+# the write-magnitude cache workload: 4 x 32 heads, n = 4096, d = 128, cache w = 64, chunk 256
+HOLA_WORKLOAD = dict(name="hola_bf16_b4h32_n4096", B=4, Hh=32, n=4096, d=128, w=64, chunk=256, dtype="bf16")
