@@ -256,7 +256,11 @@ typedef enum {
     LOLA_KERNEL_OUTPUT = 3,      /* co-normalised output of every query */
     LOLA_KERNEL_DECODE = 4,      /* one decode step */
     LOLA_KERNEL_PHI_Q = 5,       /* prefill: feature map of Q (on the side stream) */
-    LOLA_KERNEL_COUNT = 6
+    LOLA_KERNEL_HOLA_PREP = 6,   /* write-magnitude cache layer: unit and RMS-scaled q, k rows */
+    LOLA_KERNEL_HOLA_STATE = 7,  /* ... the sequential delta-rule state path and the scores */
+    LOLA_KERNEL_HOLA_CACHE = 8,  /* ... the persistent cache at every chunk start */
+    LOLA_KERNEL_HOLA_READ = 9,   /* ... the cache read and the gated sum */
+    LOLA_KERNEL_COUNT = 10
 } lola_kernel_id;
 
 /* enable != 0: clear the totals and start recording (process-wide); 0: stop recording. */
@@ -298,6 +302,60 @@ int32_t lola_sre_map(const lola_config* cfg, int32_t n, const void* V, const voi
  * Stream-ordered; validation errors return before anything is enqueued. */
 int32_t lola_sre_map_relative(const lola_config* cfg, int32_t n, const void* V, const void* workspace,
                               size_t workspace_bytes, float* out, float* base, void* stream);
+
+/* ---- the write-magnitude exact cache on a gated delta-rule state --------------------------
+ * "A Hippocampus for Linear Attention" (arXiv 2607.02303v1), reading notes, method sections
+ * 3.1-3.5.  A sibling of the LoLA layer above with its own state: per head (b, h), S (d_k x d_v,
+ * float32) starts at 0 and for t = 0 .. n-1
+ *   k^ = k_t / ||k_t||, q^ = q_t / ||q_t||                          (state path: unit rows)
+ *   e_t = v_t - alpha_t S^T k^,   S <- alpha_t S + beta_t k^ e_t^T    (Eq. 1, gated form of 3.5)
+ *   m_t = beta_t ||e_t||                                             (Eqs. 5-6: write magnitude,
+ *                                                                     fixed at the write)
+ * The persistent cache of chunk c (queries [cC, cC + C)) is the w tokens j < cC with the
+ * highest m_j (ties: the older token stays); the query reads it with its chunk's tokens up to
+ * t and a null sink (logit sink[h], value 0):
+ *   q~ = gamma_q * q / rms(q), k~ = gamma_k * k / rms(k), rms(x) = sqrt(mean(x^2) + 1e-6),
+ *   o_t = softmax over {cache, chunk tokens <= t, sink} of q~ . k~ / sqrt(d_k), times v  (Eq. 7)
+ *   y_t = S_t^T q^ + gate[h] * o_t                                   (section 3.2, Eq. 3)
+ * Shapes this build compiles: bf16 Q, K, V, d_k = d_v = 128, 0 <= w <= 128, chunk a positive
+ * multiple of 128 (at most 1024); else LOLA_ERR_UNSUPPORTED. */
+typedef struct {
+    int32_t B;       /* sequences */
+    int32_t Hh;      /* heads per sequence */
+    int32_t d_k;
+    int32_t d_v;
+    int32_t w;       /* persistent cache capacity */
+    int32_t chunk;   /* C: the cache changes at multiples of C */
+    int32_t dtype;   /* LOLA_BF16 */
+} lola_hola_config;
+
+/* Workspace bytes of one lola_hola_prefill over n tokens (negative: an invalid or
+ * unsupported cfg, the lola_status code). */
+int64_t lola_hola_workspace_bytes(const lola_hola_config* cfg, int32_t n);
+
+/* One layer over n tokens of every head.  Device pointers, 16-byte aligned, caller-owned:
+ *   Q, K, V   bf16 [B, Hh, n, d]            alpha, beta  float32 [B, Hh, n]  (decay in (0, 1],
+ *                                                        write strength in [0, 1])
+ *   gamma_q, gamma_k  float32 [d_k]         sink, gate   float32 [Hh]
+ *   Y         bf16 [B, Hh, n, d_v] (out)
+ *   S_out     float32 [B, Hh, d_k, d_v] (out, nullable): the state after token n - 1
+ *   scores    float32 [B, Hh, n] (out, nullable): m_t
+ *   cache     int32 [B, Hh, ceil(n / C), w] (out, nullable): the persistent cache's positions
+ *             at every chunk start (unordered, -1 for empty entries)
+ *   workspace at least lola_hola_workspace_bytes(cfg, n) bytes (it holds the same scores and
+ *             cache lists when those outputs are null, and the per-head status words).
+ * Stream-ordered on `stream`; validation errors return before anything is enqueued.  A wait
+ * of the read kernel that gives up sets ST-timeout bits readable with lola_hola_status. */
+int32_t lola_hola_prefill(const lola_hola_config* cfg, int32_t n, const void* Q, const void* K, const void* V,
+                          const float* alpha, const float* beta, const float* gamma_q, const float* gamma_k,
+                          const float* sink, const float* gate, void* Y, float* S_out, float* scores,
+                          int32_t* cache, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Synchronises `stream` and copies the per-head status words of the last lola_hola_prefill
+ * in `workspace` (same cfg, n) to host_status (int32 [B * Hh], nullable).  LOLA_OK if every
+ * head is 0, else LOLA_ERR_DEVICE. */
+int32_t lola_hola_status(const lola_hola_config* cfg, int32_t n, const void* workspace, int32_t* host_status,
+                         void* stream);
 
 /* ---- self-test of the bounded waits -----------------------------------------------------
  * No counterpart in the LoLA paper.  Every wait of the library's kernels on an mbarrier (the

@@ -41,10 +41,11 @@ EXPORTS = ("lola_version", "lola_status_string", "lola_last_cuda_error", "lola_c
            "lola_state_layout_of", "lola_state_bytes", "lola_prefill_workspace_bytes", "lola_state_init",
            "lola_prefill", "lola_decode_step", "lola_read_status", "lola_kernel_timing", "lola_kernel_time",
            "lola_kernel_name", "lola_prefill_noalloc", "lola_selftest_bounded_wait", "lola_sre_map",
-           "lola_sre_map_relative")
+           "lola_sre_map_relative", "lola_hola_workspace_bytes", "lola_hola_prefill", "lola_hola_status")
 # size of the fixed scratch array behind lola_prefill_noalloc (include/lola.h)
 LOLA_NOALLOC_SCRATCH_BYTES = 32 << 20
-KERNELS = ("state_init", "phi", "select", "output", "decode", "phi_q")
+KERNELS = ("state_init", "phi", "select", "output", "decode", "phi_q", "hola_prep", "hola_state", "hola_cache",
+           "hola_read")
 
 
 class lola_config(ctypes.Structure):
@@ -52,6 +53,11 @@ class lola_config(ctypes.Structure):
                 ("d_v", ctypes.c_int32), ("D", ctypes.c_int32), ("eta", ctypes.c_int32),
                 ("lambda_", ctypes.c_int32), ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32),
                 ("read_mask", ctypes.c_int32), ("alloc", ctypes.c_int32), ("score", ctypes.c_int32)]
+
+
+class lola_hola_config(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int32), ("Hh", ctypes.c_int32), ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32),
+                ("w", ctypes.c_int32), ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32)]
 
 
 class lola_state_layout(ctypes.Structure):
@@ -76,6 +82,7 @@ def _load():
     lib = ctypes.CDLL(LIB_PATH)
     P = ctypes.c_void_p
     C = ctypes.POINTER(lola_config)
+    HC = ctypes.POINTER(lola_hola_config)
     sig = {
         "lola_version": ([], ctypes.c_int32),
         "lola_status_string": ([ctypes.c_int32], ctypes.c_char_p),
@@ -97,6 +104,9 @@ def _load():
         "lola_selftest_bounded_wait": ([ctypes.c_int64, ctypes.POINTER(ctypes.c_int64), P], ctypes.c_int32),
         "lola_sre_map": ([C, ctypes.c_int32, P, P, ctypes.c_size_t, P, P], ctypes.c_int32),
         "lola_sre_map_relative": ([C, ctypes.c_int32, P, P, ctypes.c_size_t, P, P, P], ctypes.c_int32),
+        "lola_hola_workspace_bytes": ([HC, ctypes.c_int32], ctypes.c_int64),
+        "lola_hola_prefill": ([HC, ctypes.c_int32] + [P] * 14 + [ctypes.c_size_t, P], ctypes.c_int32),
+        "lola_hola_status": ([HC, ctypes.c_int32, P, P, P], ctypes.c_int32),
     }
     for name, (args, res) in sig.items():
         f = getattr(lib, name)
@@ -236,6 +246,37 @@ def lola_selftest_bounded_wait(limit_ns: int, stream=None):
     ns = ctypes.c_int64(0)
     st = _lib.lola_selftest_bounded_wait(int(limit_ns), ctypes.byref(ns), _stream(stream))
     return st, ns.value
+
+
+# ---------------------------------------------------------------------------------------
+# The write-magnitude exact cache on a gated delta-rule state (include/lola.h)
+# ---------------------------------------------------------------------------------------
+
+def make_hola_config(B, Hh, d, w, chunk, dtype=LOLA_BF16) -> lola_hola_config:
+    return lola_hola_config(B, Hh, d, d, w, chunk, dtype)
+
+
+def lola_hola_workspace_bytes(cfg: lola_hola_config, n: int) -> int:
+    b = _lib.lola_hola_workspace_bytes(ctypes.byref(cfg), n)
+    if b < 0:
+        raise LolaError(int(b), "lola_hola_workspace_bytes")
+    return int(b)
+
+
+def lola_hola_prefill(cfg: lola_hola_config, n: int, Q, K, V, alpha, beta, gamma_q, gamma_k, sink, gate, Y,
+                      workspace, S_out=None, scores=None, cache=None, stream=None) -> None:
+    _check(_lib.lola_hola_prefill(ctypes.byref(cfg), n, _ptr(Q), _ptr(K), _ptr(V), _ptr(alpha), _ptr(beta),
+                                  _ptr(gamma_q), _ptr(gamma_k), _ptr(sink), _ptr(gate), _ptr(Y), _ptr(S_out),
+                                  _ptr(scores), _ptr(cache), _ptr(workspace),
+                                  workspace.numel() * workspace.element_size(), _stream(stream)),
+           "lola_hola_prefill")
+
+
+def lola_hola_status(cfg: lola_hola_config, n: int, workspace, stream=None):
+    """Synchronises the stream and returns (status, per-head status words as a list)."""
+    buf = (ctypes.c_int32 * (cfg.B * cfg.Hh))()
+    st = _lib.lola_hola_status(ctypes.byref(cfg), n, _ptr(workspace), buf, _stream(stream))
+    return st, list(buf)
 
 
 # ---------------------------------------------------------------------------------------

@@ -209,6 +209,67 @@ cudaError_t launch_state_init(const Dims& d, char* state, const Layout& L, cudaS
     });
 }
 
+// ---- the write-magnitude cache layer: shapes and workspace ----
+namespace {
+struct HolaDims {
+    int B, Hh, BH, w, chunk, nck;
+};
+struct HolaWs {
+    float* qh;            // [BH][n][d_k] unit rows (state path)
+    float* kh;
+    __nv_bfloat16* qt;    // [BH][n][d_k] RMS-scaled rows (cache path)
+    __nv_bfloat16* kt;
+    float* ystate;        // [BH][n][d_v]
+    float* scores;        // [BH][n]
+    int32_t* cache;       // [BH][nck][w]
+    int32_t* status;      // [BH][4], word 3 the status bits
+    int* abort_flag;
+    size_t bytes;
+};
+constexpr int kHolaD = 128;
+
+int32_t hola_dims(const lola_hola_config* c, int n, HolaDims* d) {
+    if (!c || n < 1) return LOLA_ERR_INVALID_ARG;
+    if (c->B < 1 || c->Hh < 1 || c->d_k < 1 || c->d_v < 1 || c->w < 0 || c->chunk < 1 ||
+        (c->dtype != LOLA_F32 && c->dtype != LOLA_BF16))
+        return LOLA_ERR_INVALID_ARG;
+    if (c->d_k != kHolaD || c->d_v != kHolaD || c->dtype != LOLA_BF16) return LOLA_ERR_UNSUPPORTED;
+    if (c->w > hola_max_cache() || c->chunk % 128 != 0 || c->chunk > 1024) return LOLA_ERR_UNSUPPORTED;
+    if ((int64_t)c->B * c->Hh > (1 << 24) || (int64_t)n * c->B * c->Hh * kHolaD > ((int64_t)1 << 40))
+        return LOLA_ERR_UNSUPPORTED;
+    d->B = c->B;
+    d->Hh = c->Hh;
+    d->BH = c->B * c->Hh;
+    d->w = c->w;
+    d->chunk = c->chunk;
+    d->nck = (n + c->chunk - 1) / c->chunk;
+    return LOLA_OK;
+}
+
+HolaWs hola_carve(const HolaDims& d, int n, void* base) {
+    HolaWs w;
+    char* p = static_cast<char*>(base);
+    int64_t o = 0;
+    auto take = [&](int64_t bytes) {
+        char* r = p ? p + o : nullptr;
+        o = align256(o + bytes);
+        return r;
+    };
+    const int64_t rows = (int64_t)d.BH * n;
+    w.qh = reinterpret_cast<float*>(take(4 * rows * kHolaD));
+    w.kh = reinterpret_cast<float*>(take(4 * rows * kHolaD));
+    w.qt = reinterpret_cast<__nv_bfloat16*>(take(2 * rows * kHolaD));
+    w.kt = reinterpret_cast<__nv_bfloat16*>(take(2 * rows * kHolaD));
+    w.ystate = reinterpret_cast<float*>(take(4 * rows * kHolaD));
+    w.scores = reinterpret_cast<float*>(take(4 * rows));
+    w.cache = reinterpret_cast<int32_t*>(take(4 * (int64_t)d.BH * d.nck * (d.w > 0 ? d.w : 1)));
+    w.status = reinterpret_cast<int32_t*>(take(16 * (int64_t)d.BH));
+    w.abort_flag = reinterpret_cast<int*>(take(4));
+    w.bytes = (size_t)o;
+    return w;
+}
+}  // namespace
+
 }  // namespace lola
 
 using namespace lola;
@@ -421,8 +482,8 @@ int32_t lola_kernel_time(int32_t id, double* total_ms, int64_t* launches) {
 }
 
 const char* lola_kernel_name(int32_t id) {
-    static const char* names[LOLA_KERNEL_COUNT] = {"state_init", "phi", "select", "output", "decode",
-                                                        "phi_q"};
+    static const char* names[LOLA_KERNEL_COUNT] = {"state_init", "phi",        "select",     "output",     "decode",
+                                                        "phi_q",      "hola_prep",  "hola_state", "hola_cache", "hola_read"};
     return (id >= 0 && id < LOLA_KERNEL_COUNT) ? names[id] : "";
 }
 
@@ -467,6 +528,72 @@ int32_t lola_selftest_bounded_wait(int64_t limit_ns, int64_t* host_elapsed_ns, v
     if (e != cudaSuccess) return cuda_fail(e, "lola_selftest_bounded_wait");
     if (host_elapsed_ns) *host_elapsed_ns = out[1];
     return out[0] ? LOLA_OK : LOLA_ERR_DEVICE;
+}
+
+int64_t lola_hola_workspace_bytes(const lola_hola_config* cfg, int32_t n) {
+    HolaDims d;
+    const int32_t s = hola_dims(cfg, n, &d);
+    if (s != LOLA_OK) return s;
+    return (int64_t)hola_carve(d, n, nullptr).bytes;
+}
+
+int32_t lola_hola_prefill(const lola_hola_config* cfg, int32_t n, const void* Q, const void* K, const void* V,
+                          const float* alpha, const float* beta, const float* gamma_q, const float* gamma_k,
+                          const float* sink, const float* gate, void* Y, float* S_out, float* scores,
+                          int32_t* cache, void* workspace, size_t workspace_bytes, void* stream) {
+    HolaDims d;
+    const int32_t s = hola_dims(cfg, n, &d);
+    if (s != LOLA_OK) return s;
+    const void* need[] = {Q, K, V, alpha, beta, gamma_q, gamma_k, sink, gate, Y, workspace};
+    for (const void* p : need)
+        if (!p || !aligned16(p)) return LOLA_ERR_INVALID_ARG;
+    const void* opt[] = {S_out, scores, cache};
+    for (const void* p : opt)
+        if (p && !aligned16(p)) return LOLA_ERR_INVALID_ARG;
+    HolaWs ws = hola_carve(d, n, workspace);
+    if (workspace_bytes < ws.bytes) return LOLA_ERR_WORKSPACE;
+    float* sc = scores ? scores : ws.scores;
+    int32_t* cl = cache ? cache : ws.cache;
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaMemsetAsync(ws.status, 0, 16 * (size_t)d.BH, st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(ws.abort_flag, 0, sizeof(int), st);
+    if (e != cudaSuccess) return cuda_fail(e, "workspace status");
+    const int64_t rows = (int64_t)d.BH * n;
+    e = traced(LOLA_KERNEL_HOLA_PREP, st, [&]() {
+        return launch_hola_prep(rows, Q, K, gamma_q, gamma_k, ws.qh, ws.kh, ws.qt, ws.kt, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "rows");
+    e = traced(LOLA_KERNEL_HOLA_STATE, st, [&]() {
+        return launch_hola_state(d.BH, n, ws.qh, ws.kh, V, alpha, beta, ws.ystate, sc, S_out, st);
+    });
+    if (e != cudaSuccess) return cuda_fail(e, "delta-rule state");
+    e = traced(LOLA_KERNEL_HOLA_CACHE, st, [&]() { return launch_hola_cache(d.BH, n, d.w, d.chunk, d.nck, sc, cl, st); });
+    if (e != cudaSuccess) return cuda_fail(e, "persistent cache");
+    e = traced(LOLA_KERNEL_HOLA_READ, st, [&]() {
+        return launch_output_tc_hola(d.BH, d.Hh, n, d.w, d.chunk, ws.qt, ws.kt, V, Y, cl, d.nck, ws.ystate, sink, gate,
+                                     ws.status, ws.abort_flag, st);
+    });
+    return e == cudaSuccess ? LOLA_OK : cuda_fail(e, "cache read");
+}
+
+int32_t lola_hola_status(const lola_hola_config* cfg, int32_t n, const void* workspace, int32_t* host_status,
+                         void* stream) {
+    HolaDims d;
+    const int32_t s = hola_dims(cfg, n, &d);
+    if (s != LOLA_OK) return s;
+    if (!workspace) return LOLA_ERR_INVALID_ARG;
+    const HolaWs ws = hola_carve(d, n, const_cast<void*>(workspace));
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "lola_hola_status sync");
+    std::vector<int32_t> words(4 * (size_t)d.BH);
+    e = cudaMemcpy(words.data(), ws.status, 16 * (size_t)d.BH, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "lola_hola_status copy");
+    int32_t bad = 0;
+    for (int i = 0; i < d.BH; ++i) {
+        if (host_status) host_status[i] = words[4 * (size_t)i + HDR_STATUS];
+        bad |= words[4 * (size_t)i + HDR_STATUS];
+    }
+    return bad ? LOLA_ERR_DEVICE : LOLA_OK;
 }
 
 }  // extern "C"

@@ -244,6 +244,11 @@ cudaError_t launch_fixed_select(const Dims& d, int n, const Workspace& ws, const
 cudaError_t launch_output(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                           const void* V, void* Y, cudaStream_t st);
 bool output_tc_supported(const Dims& d);
+// the cache read of the write-magnitude cache layer (d_k = d_v = 128, bf16): see lola_output_tc.cu
+cudaError_t launch_output_tc_hola(int BH, int Hh, int n, int w, int chunk, const void* Qt, const void* Kt,
+                                  const void* V, void* Y, const int32_t* snapC, int nck, const float* ystate,
+                                  const float* sink, const float* gate, int32_t* status, int* abort_flag,
+                                  cudaStream_t st);
 cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const void* Q, const void* K,
                              const void* V, void* Y, char* state, int64_t head_bytes, cudaStream_t st);
 // The decode step reads phi(q), phi(k) of the token from the state's tok_phi scratch (the
@@ -256,5 +261,13 @@ cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const flo
                           int64_t w_head_stride, const void* q, const void* k, const void* v, void* y,
                           int32_t* written_pos, cudaStream_t st);
 cudaError_t launch_state_init(const Dims& d, char* state, const Layout& L, cudaStream_t st);
+// the write-magnitude cache layer (lola_hola.cu; d_k = d_v = 128, bf16 rows)
+cudaError_t launch_hola_prep(int64_t rows, const void* Q, const void* K, const float* gq, const float* gk, float* qh,
+                             float* kh, __nv_bfloat16* qt, __nv_bfloat16* kt, cudaStream_t st);
+cudaError_t launch_hola_state(int BH, int n, const float* qh, const float* kh, const void* V, const float* alpha,
+                              const float* beta, float* ystate, float* scores, float* S_out, cudaStream_t st);
+cudaError_t launch_hola_cache(int BH, int n, int w, int chunk, int nck, const float* scores, int32_t* cache,
+                              cudaStream_t st);
+int hola_max_cache();
 
 }  // namespace lola

@@ -103,6 +103,13 @@ struct TcArgs {
     char* state;                 // per-head status words (timeouts)
     int64_t head_bytes;
     int* abort_flag;             // set by any CTA whose wait timed out; later CTAs skip their work
+    // cache-read mode (the write-magnitude cache on a delta-rule state): Q and K are the
+    // RMS-scaled rows, the pool has no linear part, a null sink joins the softmax and
+    // y = ystate + gate_h * (the softmax read)
+    int hola, Hh;
+    const float* sink;           // [Hh] the sink's logit
+    const float* gate;           // [Hh] the cache read's weight
+    const float* ystate;         // [BH][n][d_v] float32 state read-out
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -158,7 +165,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
     const int P = a.lam + (t1 - wlo);
     const int nblk = (P + kBN - 1) / kBN;
     const int64_t row0 = (int64_t)bh * n;
-    const bool hide_state = (a.read_mask & LOLA_READ_HIDE_STATE) != 0;
+    const bool hide_state = (a.read_mask & LOLA_READ_HIDE_STATE) != 0 || a.hola;
     auto bar = [&](int i) { return smem_u32(&bars[i]); };
 
     if (tid == 0) {
@@ -176,7 +183,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
         }
         abort_sm = *reinterpret_cast<volatile int*>(a.abort_flag) != 0;
     }
-    if (tid < kD) sS[tid] = a.snapS[((int64_t)bh * a.nck + c) * kD + tid];
+    if (tid < kD) sS[tid] = a.hola ? 0.f : a.snapS[((int64_t)bh * a.nck + c) * kD + tid];
     if (warp == kMmaWarp) tmem_alloc<512>(smem_u32(&tmem_base));
     fence_before();
     __syncthreads();
@@ -210,14 +217,16 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
         // ================================ loaders ================================
         const int ltid = tid - kLoadWarp0 * kWarp;
         const int32_t* cpos = a.snapC + ((int64_t)bh * a.nck + c) * a.lam;
-        const int32_t* wst = a.wstep + row0;
+        const int32_t* wst = a.wstep ? a.wstep + row0 : nullptr;
         bool ok = !abort_sm;
         if (ok && ltid == 0) {
-            mbar_expect(bar(B_Q), 3 * 32768);
+            mbar_expect(bar(B_Q), (a.hola ? 1 : 3) * 32768);
             for (int x = 0; x < 2; ++x) {
                 tma_load3(sb + SQ + 16384 * x, &maps.q, 64 * x, t0, bh, bar(B_Q));
-                tma_load3(sb + SPQ + 16384 * x, &maps.pq, 64 * x, t0, bh, bar(B_Q));
-                tma_load3(sb + SH + 16384 * x, &maps.h, 64 * x, 0, bh * a.nck + c, bar(B_Q));
+                if (!a.hola) {
+                    tma_load3(sb + SPQ + 16384 * x, &maps.pq, 64 * x, t0, bh, bar(B_Q));
+                    tma_load3(sb + SH + 16384 * x, &maps.h, 64 * x, 0, bh * a.nck + c, bar(B_Q));
+                }
             }
         }
         // positions and row bounds of block bb into ring slot bb % kRing (threads 0..63)
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 const int u = bb * kBN + ltid;
                 int p = -1;
                 if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
-                const int w = p >= 0 ? wst[p] : -1;
+                const int w = (p >= 0 && !a.hola) ? wst[p] : -1;   // (cache read: never written)
                 // row r = t - t0 sees key p exactly iff lo <= r < hi, linearly iff r >= llo
                 const int lo = p < 0 ? 255 : min(max(p - t0, 0), 255);
                 int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
@@ -261,10 +270,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 // window block: consecutive positions wlo + u - lam (rows past the pool are masked)
                 if (ltid == 0) {
                     const int r0 = wlo + (u0 - a.lam);
-                    mbar_expect(bar(B_KVFULL + st), 3 * 16384);
+                    mbar_expect(bar(B_KVFULL + st), (a.hola ? 2 : 3) * 16384);
                     for (int x = 0; x < 2; ++x) {
                         tma_load3(sb + SK(st) + 8192 * x, &maps.k, 64 * x, r0, bh, bar(B_KVFULL + st));
-                        tma_load3(sb + SPK(st) + 8192 * x, &maps.pk, 64 * x, r0, bh, bar(B_KVFULL + st));
+                        if (!a.hola) tma_load3(sb + SPK(st) + 8192 * x, &maps.pk, 64 * x, r0, bh, bar(B_KVFULL + st));
                         tma_load3(sb + SV(st) + 8192 * x, &maps.v, 64 * x, r0, bh, bar(B_KVFULL + st));
                     }
                 } else {
@@ -281,7 +290,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                     const int64_t g = (row0 + (p >= 0 ? p : 0)) * kD + c16 * 8;
                     const uint32_t nb = p >= 0 ? 16u : 0u;
                     cp_async16_z(sb + SK(st) + off, a.K + g, nb);
-                    cp_async16_z(sb + SPK(st) + off, a.phiKb + g, nb);
+                    if (!a.hola) cp_async16_z(sb + SPK(st) + off, a.phiKb + g, nb);
                     cp_async16_z(sb + SV(st) + voff, a.V + g, nb);
                 }
                 cp_async_arrive_noinc(bar(B_KVFULL + st));
@@ -509,17 +518,39 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
         lpart[hf][row] = lp;
         weight_sync();
         if (ok) {
-            const float l = lpart[0][row] + lpart[1][row];
-            const float inv = t < n ? 1.0f / l : 0.f;
+            float l = lpart[0][row] + lpart[1][row];
+            float gh = 1.f;
+            if (a.hola) {
+                // the null sink (value 0) joins the normaliser at the row's scale 2^-m
+                const int h = bh % a.Hh;
+                l += ex2(a.sink[h] * kLog2e - m_run);
+                gh = a.gate[h];
+            }
+            const float inv = t < n ? gh / l : 0.f;
 #pragma unroll
             for (int cc = 0; cc < kD / 2; cc += 32) {
                 float o[32];
                 tmem_ld32(tb + lane_off + TO + 64 * hf + cc, o);
                 tmem_wait_ld();
+                if (a.hola && t < n) {
+                    // y = the state read-out + gate * the cache read
+                    const float4* ys = reinterpret_cast<const float4*>(a.ystate + (row0 + t) * kD + 64 * hf + cc);
+#pragma unroll
+                    for (int j4 = 0; j4 < 8; ++j4) {
+                        const float4 y4 = ys[j4];
+                        o[4 * j4] = fmaf(o[4 * j4], inv, y4.x);
+                        o[4 * j4 + 1] = fmaf(o[4 * j4 + 1], inv, y4.y);
+                        o[4 * j4 + 2] = fmaf(o[4 * j4 + 2], inv, y4.z);
+                        o[4 * j4 + 3] = fmaf(o[4 * j4 + 3], inv, y4.w);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) o[j] *= inv;
+                }
                 uint32_t pk[16];
 #pragma unroll
                 for (int j = 0; j < 32; j += 2) {
-                    const __nv_bfloat162 bv = __floats2bfloat162_rn(o[j] * inv, o[j + 1] * inv);
+                    const __nv_bfloat162 bv = __floats2bfloat162_rn(o[j], o[j + 1]);
                     pk[j / 2] = *reinterpret_cast<const uint32_t*>(&bv);
                 }
                 if (t < n) {
@@ -606,10 +637,55 @@ cudaError_t launch_output_tc(const Dims& d, int n, const Workspace& ws, const vo
     a.state = state;
     a.head_bytes = head_bytes;
     a.abort_flag = ws.abort_flag;
+    a.hola = 0;
+    a.Hh = d.Hh;
+    a.sink = a.gate = a.ystate = nullptr;
     const size_t smem = SEND + 1024;
     cudaError_t e = cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     output_tc_kernel<<<dim3((n + kTM - 1) / kTM, d.BH), kThreadsTc, smem, st>>>(maps, a);
+    return cudaGetLastError();
+}
+
+// The cache read of the write-magnitude cache layer: Qt, Kt the RMS-scaled rows (bf16), pool =
+// the persistent cache listed per chunk in snapC ([BH][nck][w], -1 empty) and the chunk's own
+// tokens up to the query (eta = 0, never written); y = ystate + gate_h * softmax read with a
+// null sink of logit sink_h.  status: [BH][4] int32 (ST_TIMEOUT in word 3 of a head).
+cudaError_t launch_output_tc_hola(int BH, int Hh, int n, int w, int chunk, const void* Qt, const void* Kt,
+                                  const void* V, void* Y, const int32_t* snapC, int nck, const float* ystate,
+                                  const float* sink, const float* gate, int32_t* status, int* abort_flag,
+                                  cudaStream_t st) {
+    TcMaps maps;
+    // the phi(Q), phi(K) and H_c maps are never used in this mode: any valid tensor serves
+    if (!make_map(&maps.q, Qt, n, BH, kTM) || !make_map(&maps.pq, Qt, n, BH, kTM) || !make_map(&maps.k, Kt, n, BH, kBN) ||
+        !make_map(&maps.pk, Kt, n, BH, kBN) || !make_map(&maps.v, V, n, BH, kBN) || !make_map(&maps.h, Qt, n, BH, kD))
+        return cudaErrorInvalidValue;
+    TcArgs a;
+    a.n = n;
+    a.eta = 0;
+    a.lam = w;
+    a.chunk = chunk;
+    a.nck = nck;
+    a.read_mask = 0;
+    a.K = static_cast<const __nv_bfloat16*>(Kt);
+    a.V = static_cast<const __nv_bfloat16*>(V);
+    a.Y = static_cast<__nv_bfloat16*>(Y);
+    a.phiKb = nullptr;
+    a.wstep = nullptr;
+    a.snapS = nullptr;
+    a.snapC = snapC;
+    a.state = reinterpret_cast<char*>(status);
+    a.head_bytes = 4 * sizeof(int32_t);
+    a.abort_flag = abort_flag;
+    a.hola = 1;
+    a.Hh = Hh;
+    a.sink = sink;
+    a.gate = gate;
+    a.ystate = ystate;
+    const size_t smem = SEND + 1024;
+    cudaError_t e = cudaFuncSetAttribute(output_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    output_tc_kernel<<<dim3((n + kTM - 1) / kTM, BH), kThreadsTc, smem, st>>>(maps, a);
     return cudaGetLastError();
 }
 

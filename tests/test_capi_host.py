@@ -203,3 +203,40 @@ def test_query_dependent_score_validation(lib):
     assert st == lib.LOLA_ERR_UNSUPPORTED
     # the float32 phi(Q) the scores read, the scores and the interval sums make the workspace larger
     assert lib.lola_prefill_workspace_bytes(cfg, 100) > lib.lola_prefill_workspace_bytes(mk(score=0), 100)
+
+
+def test_write_magnitude_cache_layer_validation(lib):
+    """The delta-rule cache layer's shapes and pointers are checked before anything is
+    enqueued: bf16 rows of 128, w <= 128, chunk a multiple of 128; null or misaligned
+    buffers are invalid; the optional outputs may be null."""
+    P = ctypes.c_void_p
+    ok = lib.make_hola_config(2, 3, 128, 64, 256)
+    base = lib.lola_hola_workspace_bytes(ok, 1000)
+    assert base > 0
+    # the workspace grows with n and with the cache
+    assert lib.lola_hola_workspace_bytes(ok, 2000) > base
+    assert lib.lola_hola_workspace_bytes(lib.make_hola_config(2, 3, 128, 128, 256), 1000) > base
+    for cfg, want in [(lib.make_hola_config(1, 1, 64, 16, 128), lib.LOLA_ERR_UNSUPPORTED),
+                      (lib.make_hola_config(1, 1, 128, 129, 128), lib.LOLA_ERR_UNSUPPORTED),
+                      (lib.make_hola_config(1, 1, 128, 16, 64), lib.LOLA_ERR_UNSUPPORTED),
+                      (lib.make_hola_config(1, 1, 128, 16, 2048), lib.LOLA_ERR_UNSUPPORTED),
+                      (lib.make_hola_config(1, 1, 128, 16, 128, lib.LOLA_F32), lib.LOLA_ERR_UNSUPPORTED),
+                      (lib.make_hola_config(1, 1, 128, -1, 128), lib.LOLA_ERR_INVALID_ARG),
+                      (lib.make_hola_config(0, 1, 128, 16, 128), lib.LOLA_ERR_INVALID_ARG),
+                      (lib.make_hola_config(1, 1, 128, 16, 0), lib.LOLA_ERR_INVALID_ARG),
+                      (lib.make_hola_config(1, 1, 128, 16, 128, 7), lib.LOLA_ERR_INVALID_ARG)]:
+        assert lib._lib.lola_hola_workspace_bytes(ctypes.byref(cfg), 100) == want
+    assert lib._lib.lola_hola_workspace_bytes(ctypes.byref(ok), 0) == lib.LOLA_ERR_INVALID_ARG
+    bufs = [P(256)] * 10
+    call = lambda b, ws=P(256), nbytes=base, n=1000, opt=(None, None, None): lib._lib.lola_hola_prefill(  # noqa: E731
+        ctypes.byref(ok), n, *b, *opt, ws, nbytes, None)
+    assert call(bufs, nbytes=base - 1) == lib.LOLA_ERR_WORKSPACE
+    for i in range(10):
+        b = list(bufs)
+        b[i] = None
+        assert call(b) == lib.LOLA_ERR_INVALID_ARG
+        b[i] = P(258)
+        assert call(b) == lib.LOLA_ERR_INVALID_ARG
+    assert call(bufs, ws=None) == lib.LOLA_ERR_INVALID_ARG
+    assert call(bufs, opt=(P(260), None, None)) == lib.LOLA_ERR_INVALID_ARG
+    assert call(bufs, n=0) == lib.LOLA_ERR_INVALID_ARG
