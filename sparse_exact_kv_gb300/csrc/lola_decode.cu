@@ -485,8 +485,7 @@ struct FastSmem {
     static constexpr size_t MISC = WKEY + 8 * 18;                          // [8] f32
     static_assert(DV <= D, "the N rows are staged in the slot phi rows");
     static constexpr size_t MBAR = a16(MISC + 4 * 8);                      // u64 burst barrier
-    static constexpr size_t MBAR2 = MBAR + 8;                              // u64 barrier of the slots' phi rows
-    static constexpr size_t TOTAL = MBAR2 + 8;
+    static constexpr size_t TOTAL = MBAR + 8;
 };
 
 // bulk copies (TMA engine) of the burst, completing on an mbarrier
@@ -580,28 +579,23 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     const int wpr = (ev && tid == 0) ? winpos[ring] : e;   // checked once the burst is in
 
     // ---- 1. one burst of bulk copies issued by lanes of warp 0 (the TMA engine moves them
-    //         while the threads load): the exact KV of cache and window, the two evictees'
-    //         phi, s and the evictee's N, z on one mbarrier; the slots' phi rows, needed only
-    //         after the decision, on a second one.  The new token and the slots' N, z,
-    //         positions come by plain loads meanwhile; H once the first part has landed, so
-    //         that it arrives while the scores are formed ----
+    //         while the threads load): the exact KV of cache and window, the slots' phi, the
+    //         two evictees' phi, s and the evictee's N, z.  The new token, H and the slots'
+    //         N, z, positions come by plain loads meanwhile ----
     const uint32_t bar = (uint32_t)__cvta_generic_to_shared(smb + M::MBAR);
-    const uint32_t barB = (uint32_t)__cvta_generic_to_shared(smb + M::MBAR2);
     int* fail = reinterpret_cast<int*>(misc + 7);
     if (warp == 0) {
         constexpr uint32_t kPhiB = 4 * D, kKB = sizeof(T) * DK, kVB = sizeof(T) * DV;
-        const uint32_t bytes = (uint32_t)nc * (kVB + kKB) + (uint32_t)eta * (kKB + kVB) +
+        const uint32_t bytes = (uint32_t)nc * (kPhiB + kVB + kKB) + (uint32_t)eta * (kKB + kVB) +
                                (ev ? kPhiB + 4 * (DV + 4) : 0) + (nxt ? kPhiB : 0) + kPhiB;
         if (lane == 0) {
             *fail = 0;
             mbar_init(bar, 1);
-            mbar_init(barB, 1);
             mbar_expect(bar, bytes);
-            mbar_expect(barB, (uint32_t)nc * kPhiB);
         }
         __syncwarp();
         switch (lane) {
-            case 0: if (nc > 0) bulk_g2s(cphi_s, cphi, nc * kPhiB, barB); break;
+            case 0: if (nc > 0) bulk_g2s(cphi_s, cphi, nc * kPhiB, bar); break;
             case 1: bulk_g2s(rk_s, wk, eta * kKB, bar); break;
             case 2: if (nc > 0) bulk_g2s(cv_s, cv, nc * kVB, bar); break;
             case 3: bulk_g2s(rv_s, wvv, eta * kVB, bar); break;
@@ -619,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     }
     if (tid < DV) nv_s[tid] = static_cast<const T*>(a.v)[(int64_t)bh * DV + tid];
     float hreg[HR * HC];
+    h_load<D, DV>(hreg, Hg, warp, lane);
     // slot role (one pass: lambda <= 64)
     const int sl = tid / kSG, sub = tid % kSG;
     const bool live = sl < nc;
@@ -642,11 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         if (tid == 0) {
             atomicOr(&hdr[HDR_STATUS], (int)ST_TIMEOUT);
             mbar_wait(bar, 0, 20ull * kBurstWaitNs);
-            mbar_wait(barB, 0, 20ull * kBurstWaitNs);
         }
         return;
     }
-    h_load<D, DV>(hreg, Hg, warp, lane);   // first used by the next evictee's partials, after the scores
     if (wpr != e) atomicOr(&hdr[HDR_STATUS], (int)ST_BAD_STATE);
     // the state of the head one wave ahead, into L2 (all heads step together, so its window
     // ring rows for this step are ring and nring as here); the window phi ring is skipped
@@ -661,7 +654,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         prefetch_l2(nr + a.L.c_pos, a.L.head_bytes - a.L.c_pos, tid, kThreads, 8);
     }
 
-    // ---- 2b. evictee and slot SREs (the next evictee's partials follow the scores) ----
+    // ---- 2b. next evictee's partials; evictee and slot SREs ----
+    if (nxt) h_partial_store<D, DV>(red, phn, hreg, warp, lane);
     float zn_prev = 0.f;
     if (warp == kEvWarp) {
         uint32_t ehi = kNoKey, elo = kNoKey;
@@ -743,8 +737,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
         for (int q = 0; q < DK / kWarp; ++q) acc = fmaf(qv[q], kv[q], acc);
         sc_e = warp_sum(acc) * scale;
     }
-    // the next evictee's partials against the memory before this step's write
-    if (nxt) h_partial_store<D, DV>(red, phn, hreg, warp, lane);
     __syncthreads();
 
     // ---- 3. decision (every warp) and write ----
@@ -767,14 +759,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_fast_kernel(const DecArgs 
     // the moved evictee (written slot) and the appended one (no write)
     const int slot_new = (ev && !write) ? nc : (wsel >= 0 ? wsel : -1);
     const int nc_after = (ev && !write) ? nc + 1 : nc;
-    // the slots' phi rows (the written key's, the slot update's, then the N rows' staging)
-    if (!__syncthreads_and(mbar_wait(barB, 0, kBurstWaitNs))) {
-        if (tid == 0) {
-            atomicOr(&hdr[HDR_STATUS], (int)ST_TIMEOUT);
-            mbar_wait(barB, 0, 20ull * kBurstWaitNs);
-        }
-        return;
-    }
     if (write) {
         float vh[HC];
         h_cols<DV, T>(wvT, lane, vh);
