@@ -67,6 +67,9 @@ def parse_args(argv=None):
     p.add_argument("--no-more", action="store_true", help="skip the other prefill workloads")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-hola", action="store_true",
+                   help="skip the write-magnitude cache layer (delta-rule state) line")
+    p.add_argument("--hola-only", action="store_true", help="only the write-magnitude cache layer line (profiling)")
     p.add_argument("--decode-only", action="store_true", help="skip the prefill measurement")
     p.add_argument("--decode-batch", type=int, default=None, help="batch of the decode workload (profiling)")
     p.add_argument("--decode-steps", type=int, default=None, help="decode steps per pass (profiling)")
@@ -607,6 +610,110 @@ def summarize_prefill(p):
             "clocks": p["clocks"], **({"e2e": p["e2e"]} if p.get("e2e") else {})}
 
 
+def hola_flops(d, w, chunk):
+    """Per head-token: the delta-rule state path's three d_k x d_v products (the prediction
+    S^T k, the rank-one write, the read-out S^T q: 6 d^2, float32 CUDA cores) and the cache
+    read's two products over its visible keys (w cached plus (C + 1) / 2 chunk tokens on
+    average: 2 (w + (C + 1)/2)(d_k + d_v), bf16 tensor cores)."""
+    return {"state": 6 * d * d, "read": 2 * (w + (chunk + 1) / 2) * (2 * d)}
+
+
+def hola_prep_bytes_per_row(d):
+    """HBM bytes of the row kernel per token and head: q, k in (bf16), unit q, k out (float32),
+    RMS-scaled q, k out (bf16)."""
+    return 2 * (2 * d) + 2 * (4 * d) + 2 * (2 * d)
+
+
+def cpu_baseline_hola(x, tokens):
+    """The float64 oracle on the first `tokens` tokens of every head of one sequence, threads
+    over heads (spawned workers)."""
+    import multiprocessing as mp
+    import numpy as np
+    heads = [(0, h) for h in range(x.Hh)]
+    threads = min(len(heads), os.cpu_count() or 1)
+    sub = dataclasses.replace(x, n=tokens, q=np.ascontiguousarray(x.q[:, :, :tokens]),
+                              k=np.ascontiguousarray(x.k[:, :, :tokens]), v=np.ascontiguousarray(x.v[:, :, :tokens]),
+                              alpha=np.ascontiguousarray(x.alpha[:, :, :tokens]),
+                              beta=np.ascontiguousarray(x.beta[:, :, :tokens]))
+    t0 = time.time()
+    with mp.get_context("spawn").Pool(threads) as pool:
+        pool.starmap(_hola_oracle_head, [(sub, bh) for bh in heads])
+    el = time.time() - t0
+    return {"value": tokens / el, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{x.Hh} heads of one sequence, first {tokens} tokens ({tokens} token-equivalents in {el:.2f} s)"}
+
+
+def _hola_oracle_head(x, bh):
+    from oracle import hola_ref
+    hola_ref.hola_run(x, heads=[bh])
+
+
+def run_hola(L, R, args, pk, steps=10):
+    """The write-magnitude cache layer (a gated delta-rule state with a persistent top-w exact
+    cache, B x Hh heads, n tokens, w, C as synth.HOLA_WORKLOAD): lola_hola_prefill steps."""
+    import numpy as np
+    import torch
+    import synth
+    wl = synth.HOLA_WORKLOAD
+    x = synth.hola_inputs(wl["B"], wl["Hh"], wl["n"], wl["d"], w=wl["w"], chunk=wl["chunk"], dtype=wl["dtype"],
+                          seed=R.rank)
+    dev = torch.device("cuda", R.local)
+    b16 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).view(torch.bfloat16).to(dev)  # noqa: E731
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    n, d = x.n, x.d
+    cfg = L.make_hola_config(x.B, x.Hh, d, x.w, x.chunk)
+    Q, K, V = b16(x.q), b16(x.k), b16(x.v)
+    rest = [f32(x.alpha), f32(x.beta), f32(x.gamma_q), f32(x.gamma_k), f32(x.sink), f32(x.gate)]
+    ws = torch.empty(L.lola_hola_workspace_bytes(cfg, n), dtype=torch.uint8, device=dev)
+    Y = torch.empty(x.B, x.Hh, n, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    step = lambda: L.lola_hola_prefill(cfg, n, Q, K, V, *rest, Y, ws, stream=stream)  # noqa: E731
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    with Clocks(R.local) as clk:
+        R.barrier()
+        ms = time_loop(step, steps, stream) / steps
+        R.barrier()
+    ms = R.max(ms)
+    names = ["hola_prep", "hola_state", "hola_cache", "hola_read"]
+    kt = traced_kernel_times(L, R, step, steps, stream, names)
+    st, _ = L.lola_hola_status(cfg, n, ws, stream=stream)
+    ht = x.B * x.Hh * n
+    fl = hola_flops(d, x.w, x.chunk)
+    kr = {}
+    if "hola_state" in kt:
+        t = kt["hola_state"]["avg_ms"]
+        a = fl["state"] * ht / (t * 1e-3) / 1e12
+        kr["hola_state"] = {"bound": "alu", "achieved": a, "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
+                            "frac": a / pk["fp32_tflops"], "flop_per_head_token": fl["state"], "traffic": None,
+                            "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
+    if "hola_read" in kt:
+        t = kt["hola_read"]["avg_ms"]
+        a = fl["read"] * ht / (t * 1e-3) / 1e12
+        kr["hola_read"] = {"bound": "tensor", "achieved": a, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                           "frac": a / pk["bf16_tflops"], "flop_per_head_token": fl["read"], "traffic": None}
+    if "hola_prep" in kt:
+        t = kt["hola_prep"]["avg_ms"]
+        a = hola_prep_bytes_per_row(d) * ht / (t * 1e-3) / 1e9
+        kr["hola_prep"] = {"bound": "hbm", "achieved": a, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                           "frac": a / pk["hbm_gbs"], "bytes_per_row": hola_prep_bytes_per_row(d), "traffic": None}
+    per_ht = fl["state"] + fl["read"]
+    step_tf = per_ht * ht / (ms * 1e-3) / 1e12
+    out = {"metric": "prefill tokens/s per layer (write-magnitude cache on a delta-rule state)",
+           "value": R.world * x.B * n / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
+           "status": int(st), "dtype": "bf16",
+           "config": {"workload": wl["name"], "B": x.B, "Hh": x.Hh, "n": n, "d": d, "w": x.w, "chunk": x.chunk,
+                      "inputs": "gauss q, k, v; alpha in (0.9, 1], beta in [0, 1)"},
+           "roofline": {"kernel": "layer step (all kernels)", "bound": "tensor", "achieved": step_tf,
+                        "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": step_tf / pk["bf16_tflops"],
+                        "flop_per_head_token": per_ht, "flop_terms": fl, "traffic": None},
+           "kernels": {k: {**v, **kr.get(k, {})} for k, v in kt.items()}, "clocks": clk.summary()}
+    if R.rank == 0 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline_hola(x, n)
+    return out
+
+
 def workload_config(w):
     return {"workload": w.name, "B": w.B, "Hh": w.Hh, "n": w.n, "d": w.d, "D": w.D, "eta": w.eta, "lambda": w.lam,
             "chunk": w.chunk, "inputs": w.kind}
@@ -796,6 +903,12 @@ def main(argv=None):
     R.init_gpu()
     props = torch.cuda.get_device_properties(R.local)
     pk = peaks(props.multi_processor_count)
+    if args.hola_only:
+        hol = run_hola(L, R, args, pk)
+        if R.rank == 0:
+            print(json.dumps(hol))
+        R.close()
+        return 0
     if args.decode_only:
         dec = run_decode(L, R, args, pk)
         if R.rank == 0:
@@ -828,6 +941,7 @@ def main(argv=None):
             more.append({**summarize_prefill(p), "steps": k})
             torch.cuda.empty_cache()
     dec = None if args.no_decode or args.alloc == "chunk" or args.score != "sre" else run_decode(L, R, args, pk)
+    hol = None if args.no_hola or args.n is not None else run_hola(L, R, args, pk)
     if R.rank == 0:
         kt = pre["kernels"]
         launches = int(round(pre["launches_per_step"] * args.steps))
@@ -846,6 +960,7 @@ def main(argv=None):
             "peaks": {k: pk[k] for k in ("hbm_gbs", "bf16_tflops", "fp32_tflops", "source")},
             "prefill_more": more,
             "decode": dec,
+            "hola": hol,
         }
         print(json.dumps(line))
     R.close()

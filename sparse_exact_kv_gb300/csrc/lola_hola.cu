@@ -18,8 +18,8 @@
 //                          prediction's and the previous read-out's row-group partials, then
 //                          the residual e (one column per thread), then the rank-one write;
 //   K7c hola_cache_kernel  the persistent cache at every chunk start from the fixed scores, one
-//                          warp per head (a new token replaces the worst entry -- lowest score,
-//                          newest among equals -- only with a strictly larger score);
+//                          CTA per head: per chunk, the w best of the cache and the chunk's
+//                          tokens by (higher score, older position), ranked by counting;
 //   K7d the output pass (lola_output_tc.cu) in its cache-read mode: the pool is the chunk's
 //       persistent cache plus the chunk's tokens, on tcgen05, with the sink and the gated sum
 //       in its epilogue.
@@ -197,79 +197,46 @@ __global__ void __launch_bounds__(kThreads, 1) hola_state_kernel(const StateArgs
 }
 
 // ---------------------------------------------------------------------------------------
-// K7c: entry i of the cache is held by lane i % 32 (its slot i / 32), w <= 32 * kCacheSlots
+// K7c: one CTA per head walks the chunks; the cache after chunk c is the w best, by (higher
+// score, older position), of the cache before it and the chunk's tokens -- each candidate's rank
+// is the number of candidates that beat it.  New tokens are always younger than the cached ones,
+// so this is the token-by-token rule (a strictly larger score replaces the worst entry) applied a
+// chunk at a time.
 // ---------------------------------------------------------------------------------------
-constexpr int kCacheSlots = 4;
-constexpr int kCacheWarps = 4;
-__global__ void __launch_bounds__(kCacheWarps * kWarp) hola_cache_kernel(const float* __restrict__ scores, int n,
-                                                                          int BH, int w, int chunk, int nck,
-                                                                          int32_t* __restrict__ cache) {
-    const int lane = threadIdx.x % kWarp;
-    const int bh = blockIdx.x * kCacheWarps + threadIdx.x / kWarp;
-    if (bh >= BH) return;
+constexpr int kMaxCache = 128;
+constexpr int kMaxChunk = 1024;
+constexpr int kCacheThreads = 256;
+__global__ void __launch_bounds__(kCacheThreads) hola_cache_kernel(const float* __restrict__ scores, int n, int w,
+                                                                   int chunk, int nck, int32_t* __restrict__ cache) {
+    __shared__ float cs[kMaxCache + kMaxChunk];
+    __shared__ int cp[kMaxCache + kMaxChunk];
+    __shared__ float hs[kMaxCache];
+    __shared__ int hp[kMaxCache];
+    const int tid = threadIdx.x, bh = blockIdx.x;
     const float* sc = scores + (int64_t)bh * n;
     int32_t* out = cache + (int64_t)bh * nck * w;
-    float cs[kCacheSlots];
-    int cp[kCacheSlots];
-#pragma unroll
-    for (int i = 0; i < kCacheSlots; ++i) {
-        cs[i] = 0.f;
-        cp[i] = -1;
-    }
     int count = 0;
-    uint32_t worst_hi = 0u, worst_lo = 0u;   // the worst entry's key once the cache is full
-    auto find_worst = [&]() {
-        // lowest score first (non-negative floats order as their bits), then the newest position
-        uint32_t hi = kNoKey, lo = kNoKey;
-#pragma unroll
-        for (int i = 0; i < kCacheSlots; ++i) {
-            if (cp[i] < 0) continue;
-            const uint32_t kh = __float_as_uint(cs[i]), kl = 0x7fffffffu - (uint32_t)cp[i];
-            if (kh < hi || (kh == hi && kl < lo)) {
-                hi = kh;
-                lo = kl;
+    for (int c = 0; c < nck; ++c) {
+        for (int i = tid; i < w; i += kCacheThreads) out[(int64_t)c * w + i] = i < count ? hp[i] : -1;
+        if (c == nck - 1) break;
+        const int c0 = c * chunk, m = min(chunk, n - c0), N = count + m;
+        for (int i = tid; i < N; i += kCacheThreads) {
+            cs[i] = i < count ? hs[i] : sc[c0 + i - count];
+            cp[i] = i < count ? hp[i] : c0 + i - count;
+        }
+        __syncthreads();
+        for (int i = tid; i < N; i += kCacheThreads) {
+            const float si = cs[i];
+            const int pi = cp[i];
+            int rank = 0;
+            for (int j = 0; j < N; ++j) rank += (cs[j] > si || (cs[j] == si && cp[j] < pi)) ? 1 : 0;
+            if (rank < w) {
+                hs[rank] = si;
+                hp[rank] = pi;
             }
         }
-        warp_min_key(hi, lo);
-        worst_hi = hi;
-        worst_lo = lo;
-    };
-    float next = lane < n ? sc[lane] : 0.f;   // scores arrive 32 at a time, one batch ahead
-    for (int t0 = 0; t0 < n; t0 += kWarp) {
-        const float cur = next;
-        next = t0 + kWarp + lane < n ? sc[t0 + kWarp + lane] : 0.f;
-        const int t1 = min(n, t0 + kWarp);
-        for (int t = t0; t < t1; ++t) {
-            if (t % chunk == 0) {
-#pragma unroll
-                for (int i = 0; i < kCacheSlots; ++i)
-                    if (lane + kWarp * i < w) out[(int64_t)(t / chunk) * w + lane + kWarp * i] = cp[i];
-            }
-            const float s = __shfl_sync(kFull, cur, t - t0);
-            if (w == 0) continue;
-            if (count < w) {
-                if (lane == count % kWarp) {
-#pragma unroll
-                    for (int i = 0; i < kCacheSlots; ++i)
-                        if (i == count / kWarp) {
-                            cs[i] = s;
-                            cp[i] = t;
-                        }
-                }
-                if (++count == w) find_worst();
-                continue;
-            }
-            if (__float_as_uint(s) > worst_hi) {
-                const int pos = (int)(0x7fffffffu - worst_lo);
-#pragma unroll
-                for (int i = 0; i < kCacheSlots; ++i)
-                    if (cp[i] == pos) {
-                        cs[i] = s;
-                        cp[i] = t;
-                    }
-                find_worst();
-            }
-        }
+        __syncthreads();
+        count = min(w, N);
     }
 }
 
@@ -302,11 +269,11 @@ cudaError_t launch_hola_state(int BH, int n, const float* qh, const float* kh, c
 
 cudaError_t launch_hola_cache(int BH, int n, int w, int chunk, int nck, const float* scores, int32_t* cache,
                               cudaStream_t st) {
-    hola_cache_kernel<<<(BH + kCacheWarps - 1) / kCacheWarps, kCacheWarps * kWarp, 0, st>>>(scores, n, BH, w, chunk,
-                                                                                          nck, cache);
+    if (w > kMaxCache || chunk > kMaxChunk) return cudaErrorInvalidValue;
+    hola_cache_kernel<<<BH, kCacheThreads, 0, st>>>(scores, n, w, chunk, nck, cache);
     return cudaGetLastError();
 }
 
-int hola_max_cache() { return kCacheSlots * kWarp; }
+int hola_max_cache() { return kMaxCache; }
 
 }  // namespace lola
