@@ -13,10 +13,11 @@
 // Four launches:
 //   K7a hola_prep_kernel   every row's q^, k^ (float32) and q~, k~ (bf16), one warp per row;
 //   K7b hola_state_kernel  the sequential state path, one CTA of 512 threads per head, S in
-//                          registers with the prefill chain's H layout (warp w: rows 8w..8w+7,
-//                          lane l: columns 4l..4l+3); per token two CTA barriers: the
-//                          prediction's and the previous read-out's row-group partials, then
-//                          the residual e (one column per thread), then the rank-one write;
+//                          registers by columns (warp w: columns 8w..8w+7, lane l: rows
+//                          4l..4l+3), so a token needs no CTA barrier: the prediction's and the
+//                          read-out's column sums are lane reductions, the residual is shuffled
+//                          across the warp's columns, the write is local; one barrier per block
+//                          of 8 tokens publishes the next block's rows;
 //   K7c hola_cache_kernel  the persistent cache at every chunk start from the fixed scores, one
 //                          CTA per head: per chunk, the w best of the cache and the chunk's
 //                          tokens by (higher score, older position), ranked by counting;
@@ -87,8 +88,15 @@ struct StateArgs {
     float* S_out;                  // [BH][d_k][d_v] or null
 };
 
-constexpr int kSPF = 4;            // token rows prefetched ahead
-constexpr int kSRing = 8;          // ring of token rows (> kSPF + 1)
+// Warp w owns columns 8w .. 8w+7 of S and lane l its rows 4l .. 4l+3 (32 registers), so a token
+// needs no CTA barrier: the column sums of S^T k^ and S^T q^ are lane reductions inside the warp.
+// The decay is kept as a scalar: S_t = G_t R_t with G_t = alpha_0 ... alpha_t (renormalised into
+// R when it falls below 2^-40), so the write is R += (beta_t / G_t) k^ e^T and the prediction and
+// read-out take G times R's products -- equal to the recurrence in exact arithmetic.
+// Token rows arrive in blocks of kBlk tokens by cp.async, one block ahead; a CTA barrier per
+// block publishes the next block and the score partials of the last one.
+constexpr int kBlk = 8;
+constexpr int kTRing = 2 * kBlk;   // token row slots: the block in use and the one arriving
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
@@ -102,98 +110,175 @@ __device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_grou
 template <int N>
 __device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
+// The sums over the warp's 32 lanes of 8 per-lane values x[0..7] (one per column): after
+// three halving exchanges and two butterflies, lane l holds the sum of column l >> 2.
+__device__ __forceinline__ float col_reduce8(const float (&x)[8], int lane) {
+    const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4;
+    float q[4], r[2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float send = b4 ? x[i] : x[i + 4];
+        q[i] = (b4 ? x[i + 4] : x[i]) + __shfl_xor_sync(kFull, send, 16);
+    }
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const float send = b3 ? q[i] : q[i + 2];
+        r[i] = (b3 ? q[i + 2] : q[i]) + __shfl_xor_sync(kFull, send, 8);
+    }
+    float s = (b2 ? r[1] : r[0]) + __shfl_xor_sync(kFull, b2 ? r[0] : r[1], 4);
+    s += __shfl_xor_sync(kFull, s, 2);
+    s += __shfl_xor_sync(kFull, s, 1);
+    return s;
+}
+
 __global__ void __launch_bounds__(kThreads, 1) hola_state_kernel(const StateArgs a) {
-    using Sh = Shape<kHD, kHD>;
-    constexpr int HR = Sh::HR, HC = Sh::HC;
-    __shared__ __align__(16) float kr[kSRing][kHD];
-    __shared__ __align__(16) float qr[kSRing][kHD];
-    __shared__ __align__(16) __nv_bfloat16 vr[kSRing][kHD];
-    __shared__ float ar[kSRing], br[kSRing];
-    __shared__ __align__(16) float redk[Sh::NRG][kHD];
-    __shared__ __align__(16) float redq[Sh::NRG][kHD];
-    __shared__ __align__(16) float es[kHD];
-    __shared__ float esq[kHD / kWarp];
+    constexpr int kCols = kHD / (kThreads / kWarp);   // 8 columns per warp
+    constexpr int kRows = kHD / kWarp;                // 4 rows per lane
+    static_assert(kCols == 8 && kRows == 4, "layout");
+    __shared__ __align__(16) float kr[kTRing][kHD];
+    __shared__ __align__(16) float qr[kTRing][kHD];
+    __shared__ __align__(16) __nv_bfloat16 vr[kTRing][kHD];
+    __shared__ float ar[kTRing], br[kTRing];
+    __shared__ float esq[kTRing][kThreads / kWarp];   // per token and warp: sum of e^2 over the warp's columns
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int bh = blockIdx.x, n = a.n;
+    const int col = warp * kCols + (lane >> 2);       // the column this lane's reductions end in
     const float* qh = a.qh + (int64_t)bh * n * kHD;
     const float* kh = a.kh + (int64_t)bh * n * kHD;
     const __nv_bfloat16* V = a.V + (int64_t)bh * n * kHD;
     const float* al = a.alpha + (int64_t)bh * n;
     const float* be = a.beta + (int64_t)bh * n;
     float* ys = a.ystate + (int64_t)bh * n * kHD;
+    float* scores = a.scores + (int64_t)bh * n;
 
-    // token `step`'s rows into ring slot step % kSRing (one commit group per call, every thread)
-    auto prefetch = [&](int step) {
-        if (step < n) {
-            const int sl = step % kSRing;
-            if (tid < 32) cp_async16g(&kr[sl][4 * tid], kh + (int64_t)step * kHD + 4 * tid);
-            else if (tid < 64) cp_async16g(&qr[sl][4 * (tid - 32)], qh + (int64_t)step * kHD + 4 * (tid - 32));
-            else if (tid < 80) cp_async16g(&vr[sl][8 * (tid - 64)], V + (int64_t)step * kHD + 8 * (tid - 64));
-            else if (tid == 80) cp_async4(&ar[sl], al + step);
-            else if (tid == 81) cp_async4(&br[sl], be + step);
+    // the rows of tokens [t0, t0 + kBlk) into their slots (one commit group per call, every thread)
+    auto prefetch_block = [&](int t0) {
+        for (int i = tid; i < kBlk * 82; i += kThreads) {
+            const int j = i / 82, part = i % 82, t = t0 + j;
+            if (t >= n) continue;
+            const int sl = t % kTRing;
+            if (part < 32) cp_async16g(&kr[sl][4 * part], kh + (int64_t)t * kHD + 4 * part);
+            else if (part < 64) cp_async16g(&qr[sl][4 * (part - 32)], qh + (int64_t)t * kHD + 4 * (part - 32));
+            else if (part < 80) cp_async16g(&vr[sl][8 * (part - 64)], V + (int64_t)t * kHD + 8 * (part - 64));
+            else if (part == 80) cp_async4(&ar[sl], al + t);
+            else cp_async4(&br[sl], be + t);
         }
         cp_commit();
     };
-    float h[HR * HC];
-#pragma unroll
-    for (int i = 0; i < HR * HC; ++i) h[i] = 0.f;
-    for (int st = 0; st < kSPF; ++st) prefetch(st);
-    cp_wait<0>();
-    __syncthreads();
-
-    for (int t = 0; t < n; ++t) {
-        const int sl = t % kSRing, ps = (t + kSRing - 1) % kSRing;
-        // ---- the prediction's partials S_{t-1}^T k^_t, and the read-out of token t - 1 ----
-        h_partial_store<kHD, kHD>(&redk[0][0], kr[sl], h, warp, lane);
-        if (t >= 1) h_partial_store<kHD, kHD>(&redq[0][0], qr[ps], h, warp, lane);
-        __syncthreads();
-        // ---- the residual (one column per thread of warps 0-3), the read-out's columns ----
-        if (tid < kHD) {
-            const float pred = reduce_partials_col<kHD, kHD>(&redk[0][0], tid);
-            const float v = __bfloat162float(vr[sl][tid]);
-            const float e = fmaf(-ar[sl], pred, v);
-            es[tid] = e;
-            float e2 = e * e;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) e2 += __shfl_xor_sync(kFull, e2, o);
-            if (lane == 0) esq[warp] = e2;
-        } else if (tid < 2 * kHD && t >= 1) {
-            const int c = tid - kHD;
-            ys[(int64_t)(t - 1) * kHD + c] = reduce_partials_col<kHD, kHD>(&redq[0][0], c);
-        }
-        prefetch(t + kSPF);
-        cp_wait<kSPF - 1>();   // this thread's copies of token t + 1 have landed
-        __syncthreads();
-        // ---- the write S = alpha S + beta k^ e^T; the score beta ||e|| ----
-        const float a_t = ar[sl], b_t = br[sl];
-        float ec[HC];
-        h_vec_load<HC>(es + lane * HC, ec);
-#pragma unroll
-        for (int r4 = 0; r4 < HR / 4; ++r4) {
-            const float4 k4 = *reinterpret_cast<const float4*>(&kr[sl][warp * HR + 4 * r4]);
-            const float kk[4] = {k4.x, k4.y, k4.z, k4.w};
-#pragma unroll
-            for (int rr = 0; rr < 4; ++rr) {
-                const float kb = b_t * kk[rr];
-#pragma unroll
-                for (int c = 0; c < HC; ++c) {
-                    float& x = h[(4 * r4 + rr) * HC + c];
-                    x = fmaf(kb, ec[c], a_t * x);
-                }
-            }
-        }
-        if (tid == 0) {
+    // the scores of tokens [t0, t1) from the warps' partials (beta from global memory: its ring
+    // slot may already be receiving the next block)
+    auto emit_scores = [&](int t0, int t1) {
+        if (tid < t1 - t0) {
+            const int t = t0 + tid, sl = t % kTRing;
             float s2 = 0.f;
 #pragma unroll
-            for (int w = 0; w < kHD / kWarp; ++w) s2 += esq[w];
-            a.scores[(int64_t)bh * n + t] = b_t * sqrtf(s2);
+            for (int w = 0; w < kThreads / kWarp; ++w) s2 += esq[sl][w];
+            scores[t] = be[t] * sqrtf(s2);
+        }
+    };
+
+    float S[kRows][kCols];
+#pragma unroll
+    for (int r = 0; r < kRows; ++r)
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) S[r][c] = 0.f;
+    float qprev[kRows] = {0.f, 0.f, 0.f, 0.f};
+    float G = 1.f;   // the decay so far, S = G R (R is held in S[][])
+
+    prefetch_block(0);
+    for (int t0 = 0; t0 < n; t0 += kBlk) {
+        cp_wait<0>();            // this thread's copies of block t0 have landed
+        __syncthreads();         // ... and everyone's; every warp is done with block t0 - kBlk
+        if (t0 > 0) emit_scores(t0 - kBlk, t0);
+        prefetch_block(t0 + kBlk);   // into block t0 - kBlk's slots
+        const int t1 = min(n, t0 + kBlk);
+        for (int t = t0; t < t1; ++t) {
+            const int sl = t % kTRing;
+            const float4 k4 = *reinterpret_cast<const float4*>(&kr[sl][4 * lane]);
+            const float kv[kRows] = {k4.x, k4.y, k4.z, k4.w};
+            // ---- R^T k^_t (the prediction / G_{t-1}) and R^T q^_{t-1} (the last read-out / G_{t-1}),
+            //      column pairs with paired FMAs ----
+            float pk[kCols], pq[kCols];
+#pragma unroll
+            for (int c = 0; c < kCols; c += 2) {
+                float2 ak = __fmul2_rn(make_float2(kv[0], kv[0]), make_float2(S[0][c], S[0][c + 1]));
+                float2 aq = __fmul2_rn(make_float2(qprev[0], qprev[0]), make_float2(S[0][c], S[0][c + 1]));
+#pragma unroll
+                for (int r = 1; r < kRows; ++r) {
+                    ak = __ffma2_rn(make_float2(kv[r], kv[r]), make_float2(S[r][c], S[r][c + 1]), ak);
+                    aq = __ffma2_rn(make_float2(qprev[r], qprev[r]), make_float2(S[r][c], S[r][c + 1]), aq);
+                }
+                pk[c] = ak.x;
+                pk[c + 1] = ak.y;
+                pq[c] = aq.x;
+                pq[c + 1] = aq.y;
+            }
+            const float pred = col_reduce8(pk, lane);
+            const float outp = col_reduce8(pq, lane);
+            if (t >= 1 && (lane & 3) == 0) ys[(int64_t)(t - 1) * kHD + col] = G * outp;
+            // ---- the residual of this lane's column, then every column of the warp ----
+            const float a_t = ar[sl], b_t = br[sl];
+            G *= a_t;                                         // G_t
+            const float e_mine = fmaf(-G, pred, __bfloat162float(vr[sl][col]));
+            float e[kCols], e2 = 0.f;
+#pragma unroll
+            for (int c = 0; c < kCols; ++c) {
+                e[c] = __shfl_sync(kFull, e_mine, 4 * c);
+                e2 = fmaf(e[c], e[c], e2);
+            }
+            if (lane == 0) esq[sl][warp] = e2;
+            // ---- the write R += (beta / G) k^ e^T (S = alpha S + beta k^ e^T) ----
+            const float bg = b_t / G;
+#pragma unroll
+            for (int r = 0; r < kRows; ++r) {
+                const float kb = bg * kv[r];
+#pragma unroll
+                for (int c = 0; c < kCols; c += 2) {
+                    const float2 y = __ffma2_rn(make_float2(kb, kb), make_float2(e[c], e[c + 1]),
+                                                make_float2(S[r][c], S[r][c + 1]));
+                    S[r][c] = y.x;
+                    S[r][c + 1] = y.y;
+                }
+            }
+            if (G < 0x1p-40f) {   // fold the decay back into R (the same G in every thread)
+#pragma unroll
+                for (int r = 0; r < kRows; ++r)
+#pragma unroll
+                    for (int c = 0; c < kCols; ++c) S[r][c] *= G;
+                G = 1.f;
+            }
+            const float4 q4 = *reinterpret_cast<const float4*>(&qr[sl][4 * lane]);
+            qprev[0] = q4.x;
+            qprev[1] = q4.y;
+            qprev[2] = q4.z;
+            qprev[3] = q4.w;
         }
     }
-    // ---- the last token's read-out; the final state ----
-    h_partial_store<kHD, kHD>(&redq[0][0], qr[(n - 1) % kSRing], h, warp, lane);
+    // ---- the last token's read-out, the last block's scores, the final state ----
+    {
+        float pq[kCols];
+#pragma unroll
+        for (int c = 0; c < kCols; ++c) {
+            pq[c] = qprev[0] * S[0][c];
+#pragma unroll
+            for (int r = 1; r < kRows; ++r) pq[c] = fmaf(qprev[r], S[r][c], pq[c]);
+        }
+        const float outp = col_reduce8(pq, lane);
+        if ((lane & 3) == 0) ys[(int64_t)(n - 1) * kHD + col] = G * outp;
+    }
+    cp_wait<0>();
     __syncthreads();
-    if (tid < kHD) ys[(int64_t)(n - 1) * kHD + tid] = reduce_partials_col<kHD, kHD>(&redq[0][0], tid);
-    if (a.S_out) h_store<kHD, kHD>(a.S_out + (int64_t)bh * kHD * kHD, h, warp, lane);
+    const int last0 = ((n - 1) / kBlk) * kBlk;
+    emit_scores(last0, n);
+    if (a.S_out) {
+        float* So = a.S_out + (int64_t)bh * kHD * kHD;
+#pragma unroll
+        for (int r = 0; r < kRows; ++r) {
+            float4* dst = reinterpret_cast<float4*>(So + (int64_t)(4 * lane + r) * kHD + warp * kCols);
+            dst[0] = make_float4(G * S[r][0], G * S[r][1], G * S[r][2], G * S[r][3]);
+            dst[1] = make_float4(G * S[r][4], G * S[r][5], G * S[r][6], G * S[r][7]);
+        }
+    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -206,34 +291,31 @@ __global__ void __launch_bounds__(kThreads, 1) hola_state_kernel(const StateArgs
 constexpr int kMaxCache = 128;
 constexpr int kMaxChunk = 1024;
 constexpr int kCacheThreads = 256;
+// rank key: a larger key is better (higher score, then the older position)
+__device__ __forceinline__ uint64_t cache_key(float score, int pos) {
+    return ((uint64_t)__float_as_uint(score) << 32) | (uint64_t)(0xffffffffu - (uint32_t)pos);
+}
 __global__ void __launch_bounds__(kCacheThreads) hola_cache_kernel(const float* __restrict__ scores, int n, int w,
                                                                    int chunk, int nck, int32_t* __restrict__ cache) {
-    __shared__ float cs[kMaxCache + kMaxChunk];
-    __shared__ int cp[kMaxCache + kMaxChunk];
-    __shared__ float hs[kMaxCache];
-    __shared__ int hp[kMaxCache];
+    __shared__ uint64_t ck[kMaxCache + kMaxChunk];   // the candidates of one merge
+    __shared__ uint64_t hk[kMaxCache];               // the cache, best first
     const int tid = threadIdx.x, bh = blockIdx.x;
     const float* sc = scores + (int64_t)bh * n;
     int32_t* out = cache + (int64_t)bh * nck * w;
     int count = 0;
     for (int c = 0; c < nck; ++c) {
-        for (int i = tid; i < w; i += kCacheThreads) out[(int64_t)c * w + i] = i < count ? hp[i] : -1;
+        for (int i = tid; i < w; i += kCacheThreads)
+            out[(int64_t)c * w + i] = i < count ? (int32_t)(0xffffffffu - (uint32_t)(hk[i] & 0xffffffffu)) : -1;
         if (c == nck - 1) break;
         const int c0 = c * chunk, m = min(chunk, n - c0), N = count + m;
-        for (int i = tid; i < N; i += kCacheThreads) {
-            cs[i] = i < count ? hs[i] : sc[c0 + i - count];
-            cp[i] = i < count ? hp[i] : c0 + i - count;
-        }
+        for (int i = tid; i < N; i += kCacheThreads) ck[i] = i < count ? hk[i] : cache_key(sc[c0 + i - count], c0 + i - count);
         __syncthreads();
         for (int i = tid; i < N; i += kCacheThreads) {
-            const float si = cs[i];
-            const int pi = cp[i];
+            const uint64_t ki = ck[i];
             int rank = 0;
-            for (int j = 0; j < N; ++j) rank += (cs[j] > si || (cs[j] == si && cp[j] < pi)) ? 1 : 0;
-            if (rank < w) {
-                hs[rank] = si;
-                hp[rank] = pi;
-            }
+#pragma unroll 8
+            for (int j = 0; j < N; ++j) rank += ck[j] > ki ? 1 : 0;
+            if (rank < w) hk[rank] = ki;
         }
         __syncthreads();
         count = min(w, N);
