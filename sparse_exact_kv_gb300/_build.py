@@ -15,7 +15,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "liblola.so")
 SOURCES = ["lola_capi.cu", "lola_phi.cu", "lola_select.cu", "lola_chunk.cu", "lola_output.cu", "lola_output_tc.cu",
            "lola_decode.cu", "lola_noalloc.cu", "lola_relsre.cu",
-           "lola_fixed.cu", "lola_hola.cu"]
+           "lola_fixed.cu", "lola_hola.cu", "lola_hola_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

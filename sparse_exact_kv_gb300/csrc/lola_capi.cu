@@ -564,7 +564,7 @@ int32_t lola_hola_prefill(const lola_hola_config* cfg, int32_t n, const void* Q,
     });
     if (e != cudaSuccess) return cuda_fail(e, "rows");
     e = traced(LOLA_KERNEL_HOLA_STATE, st, [&]() {
-        return launch_hola_state(d.BH, n, ws.qh, ws.kh, V, alpha, beta, ws.ystate, sc, S_out, st);
+        return launch_hola_state_tc(d.BH, n, ws.qh, ws.kh, V, alpha, beta, ws.ystate, sc, S_out, ws.status, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "delta-rule state");
     e = traced(LOLA_KERNEL_HOLA_CACHE, st, [&]() { return launch_hola_cache(d.BH, n, d.w, d.chunk, d.nck, sc, cl, st); });

@@ -269,5 +269,9 @@ cudaError_t launch_hola_state(int BH, int n, const float* qh, const float* kh, c
 cudaError_t launch_hola_cache(int BH, int n, int w, int chunk, int nck, const float* scores, int32_t* cache,
                               cudaStream_t st);
 int hola_max_cache();
+// the chunked tensor-core form of the same state path (lola_hola_tc.cu); status: [BH][4]
+cudaError_t launch_hola_state_tc(int BH, int n, const float* qh, const float* kh, const void* V, const float* alpha,
+                                 const float* beta, float* ystate, float* scores, float* S_out, int32_t* status,
+                                 cudaStream_t st);
 
 }  // namespace lola
