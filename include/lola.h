@@ -335,7 +335,8 @@ int64_t lola_hola_workspace_bytes(const lola_hola_config* cfg, int32_t n);
 
 /* One layer over n tokens of every head.  Device pointers, 16-byte aligned, caller-owned:
  *   Q, K, V   bf16 [B, Hh, n, d]            alpha, beta  float32 [B, Hh, n]  (decay in (0, 1],
- *                                                        write strength in [0, 1])
+ *                                                        write strength in [0, 1]; a decay
+ *                                                        below 2^-100 is taken as 2^-100)
  *   gamma_q, gamma_k  float32 [d_k]         sink, gate   float32 [Hh]
  *   Y         bf16 [B, Hh, n, d_v] (out)
  *   S_out     float32 [B, Hh, d_k, d_v] (out, nullable): the state after token n - 1

@@ -215,8 +215,7 @@ struct HolaDims {
     int B, Hh, BH, w, chunk, nck;
 };
 struct HolaWs {
-    float* qh;            // [BH][n][d_k] unit rows (state path)
-    float* kh;
+    uint8_t* xtile;       // [BH][ceil(n / 64)][64 KB] unit rows, split, in the state path's tiles
     __nv_bfloat16* qt;    // [BH][n][d_k] RMS-scaled rows (cache path)
     __nv_bfloat16* kt;
     float* ystate;        // [BH][n][d_v]
@@ -256,8 +255,7 @@ HolaWs hola_carve(const HolaDims& d, int n, void* base) {
         return r;
     };
     const int64_t rows = (int64_t)d.BH * n;
-    w.qh = reinterpret_cast<float*>(take(4 * rows * kHolaD));
-    w.kh = reinterpret_cast<float*>(take(4 * rows * kHolaD));
+    w.xtile = reinterpret_cast<uint8_t*>(take((int64_t)d.BH * ((n + 63) / 64) * kHolaXTile));
     w.qt = reinterpret_cast<__nv_bfloat16*>(take(2 * rows * kHolaD));
     w.kt = reinterpret_cast<__nv_bfloat16*>(take(2 * rows * kHolaD));
     w.ystate = reinterpret_cast<float*>(take(4 * rows * kHolaD));
@@ -558,13 +556,12 @@ int32_t lola_hola_prefill(const lola_hola_config* cfg, int32_t n, const void* Q,
     cudaError_t e = cudaMemsetAsync(ws.status, 0, 16 * (size_t)d.BH, st);
     if (e == cudaSuccess) e = cudaMemsetAsync(ws.abort_flag, 0, sizeof(int), st);
     if (e != cudaSuccess) return cuda_fail(e, "workspace status");
-    const int64_t rows = (int64_t)d.BH * n;
     e = traced(LOLA_KERNEL_HOLA_PREP, st, [&]() {
-        return launch_hola_prep(rows, Q, K, gamma_q, gamma_k, ws.qh, ws.kh, ws.qt, ws.kt, st);
+        return launch_hola_prep(d.BH, n, Q, K, gamma_q, gamma_k, ws.xtile, ws.qt, ws.kt, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "rows");
     e = traced(LOLA_KERNEL_HOLA_STATE, st, [&]() {
-        return launch_hola_state_tc(d.BH, n, ws.qh, ws.kh, V, alpha, beta, ws.ystate, sc, S_out, ws.status, st);
+        return launch_hola_state_tc(d.BH, n, ws.xtile, V, alpha, beta, ws.ystate, sc, S_out, ws.status, st);
     });
     if (e != cudaSuccess) return cuda_fail(e, "delta-rule state");
     e = traced(LOLA_KERNEL_HOLA_CACHE, st, [&]() { return launch_hola_cache(d.BH, n, d.w, d.chunk, d.nck, sc, cl, st); });

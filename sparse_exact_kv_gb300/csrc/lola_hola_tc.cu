@@ -1,21 +1,33 @@
-// K7b (tensor cores): the gated delta-rule state path of the write-magnitude cache layer in
-// its chunked form.
+// K7b: the gated delta-rule state path of the write-magnitude cache layer in its chunked
+// form, on tcgen05.
 //
 // "A Hippocampus for Linear Attention" (arXiv 2607.02303v1), reading notes, sections 3.1 and
 // 3.5: e_t = v_t - alpha_t S_{t-1}^T k^_t, S_t = alpha_t S_{t-1} + beta_t k^_t e_t^T, read-out
-// S_t^T q^_t, score m_t = beta_t ||e_t||.  With u_t = beta_t e_t, the decay kept as a scalar
-// (S_t = G_t R_t, G_t = alpha_0 ... alpha_t) and, inside a chunk of 64 tokens starting from R_0
-// and G (the decay before it), c_t = the product of the chunk's alphas up to t and
-// g_t = G c_t, the recurrence unrolls exactly into
-//   (I + A) U = W,  A_tj = beta_t (c_t / c_j) (k^_t . k^_j)  (j < t),
-//                   W_t  = beta_t (v_t - g_t R_0^T k^_t),
-//   o_t  = g_t R_0^T q^_t + sum_{j <= t} (c_t / c_j) (q^_t . k^_j) u_j,
-//   R_end = R_0 + sum_j (k^_j / g_j) u_j^T,   m_t = ||u_t||.
-// The dense products -- [K^; Q^] R_0, [K^; Q^] K^^T, the read-out's (c-masked QK^T) U and the
-// state update K'^T U -- run on tcgen05 with every float32 operand split into two bf16 terms
-// (hi + lo; three partial products hi.hi + hi.lo + lo.hi, float32 accumulation); the triangular
-// solve for U runs on CUDA cores (one column per thread, forward substitution in float32).
-// R lives in TMEM for the whole sequence.  One CTA of 256 threads per head.
+// S_t^T q^_t, score m_t = beta_t ||e_t||.
+//
+// A pass covers tokens [s0, s1) of a 64-token chunk and starts from S = R_0 (the decay before
+// it folded into R).  With c_t = alpha_{s0} ... alpha_t and u'_t = beta_t e_t / c_t, the
+// recurrence unrolls exactly into
+//   (I + A') U' = W',   A'_tj = beta_t (k^_t . k^_j)  (j < t),
+//                       W'_t  = beta_t (v_t / c_t - R_0^T k^_t),
+//   y_t  = c_t (R_0^T q^_t + sum_{j <= t} (q^_t . k^_j) u'_j),
+//   R_end = R_0 + sum_j k^_j u'_j^T,   m_t = c_t ||u'_t||,   S_end = c_{s1-1} R_end
+// (S_t = c_t R_t with R_t = R_0 + sum_{j <= t} k^_j u'_j^T).  A pass ends before the token whose
+// c_t would fall below 2^-100, so 1 / c_t stays far inside float32; with the notes' decays
+// (close to 1) every chunk is one pass.
+//
+// The state is kept transposed in TMEM (lane = value column c, columns = key index), so every
+// product comes out with the value column on the lane and the solve needs no transposition:
+//   P1  D1 = R_0^T [K^; Q^]^T   (128 x 128: columns 0-63 the keys' predictions, 64-127 the
+//                                queries' read-outs)       and   GM = [K^; Q^] K^^T (128 x 64);
+//   the solve: thread c holds column c of W' in registers and runs a right-looking forward
+//   substitution with A' read from shared memory (broadcast), float32;
+//   P3  D1[:, 64..] += U'^T A_read^T (the chunk's read-out; A_read = masked Q^ K^^T)  and
+//       R^T += U'^T K^ (the state update; K^ read from the same tile as X, MN-major).
+// Float32 operands are split into bf16 hi + lo; each product is hi.hi + hi.lo + lo.hi with
+// float32 accumulation.  The unit rows arrive pre-split in the tile layout the descriptors read
+// (written by the row kernel, 64 KB per chunk, one bulk copy, two chunks in flight); the chunk's
+// value rows by a bulk copy one chunk ahead.  One CTA of 256 threads per head.
 #include "lola_internal.cuh"
 #include "lola_tc.cuh"
 
@@ -28,29 +40,27 @@ constexpr int kD = 128;          // d_k = d_v
 constexpr int kC = 64;           // tokens per chunk
 constexpr int kThr = 256;
 constexpr uint64_t kWaitNs = 1000000000ull;
+constexpr float kMinC = 0x1p-100f;   // a pass ends before its decay falls below this
 
-// TMEM columns (128 lanes): R [d_k x d_v], P = [K^; Q^] R_0, G = [K^; Q^] K^^T, O = read-out
-constexpr uint32_t TR = 0, TP = 128, TG = 256, TO = 320;
+// TMEM columns (128 lanes, lane = value column c): R^T, D1 = R_0^T X^T, GM = X K^^T (lane = X row)
+constexpr uint32_t TRT = 0, TD1 = 128, TGM = 256;
 
 // shared memory (bytes from a 1024-aligned base)
-constexpr uint32_t SX = 0;                 // [K^; Q^] hi, lo: K-major 128 x 128, 2 atoms each (32 KB)
-constexpr uint32_t kXB = 32768;
-constexpr uint32_t SR = 65536;             // R_0 hi, lo: MN-major [K = 128 x N = 128] (32 KB each)
-constexpr uint32_t kRB = 32768;
-constexpr uint32_t SA = 65536;             // (after P1, over SR) read-out A hi, lo: K-major 128 x 64 (16 KB each)
-constexpr uint32_t kAB = 16384;
-constexpr uint32_t SU = 98304;             // (after P1, over SR) U hi, lo: MN-major [K = 64 x N = 128] (16 KB each)
+constexpr uint32_t SX = 0;                     // two chunk tiles X = [K^; Q^] (hi, lo), kHolaXTile each
+constexpr uint32_t SRT = 2 * kHolaXTile;       // R_0^T hi, lo: K-major 128 x 128 (32 KB each)
+constexpr uint32_t kRTB = 32768;
+constexpr uint32_t SU = SRT;                   // (after P1, over R_0^T) U'^T hi, lo: K-major 128 x 64
 constexpr uint32_t kUB = 16384;
-constexpr uint32_t SK = 131072;            // K' = k^ / g hi, lo: MN-major A [K = 64 x M = 128] (16 KB each)
-constexpr uint32_t kKB = 16384;
-constexpr uint32_t SW = 163840;            // W, then U, then g_t Q R_0 rows: float32 [64][128]
-constexpr uint32_t SAm = SW + 4 * kC * kD; // A: float32 [64][64]
-constexpr uint32_t SEND = SAm + 4 * kC * kC;
+constexpr uint32_t SAR = SRT + 32768;          // (after P1) A_read hi, lo: K-major 64 x 64
+constexpr uint32_t kARB = 8192;
+constexpr uint32_t SAm = SRT + 2 * kRTB;       // A' float32, transposed: [j][t]
+constexpr uint32_t SV = SAm + 4 * kC * kC;     // the chunk's value rows, bf16 [64][128]
+constexpr uint32_t SEND = SV + 2 * kC * kD;
+static_assert(SEND + 1024 + 2048 <= 232448, "shared memory plan exceeds 227 KB");
 
 struct TcStateArgs {
-    int n;
-    const float* qh;            // [BH][n][d] unit rows
-    const float* kh;
+    int n, nck;                 // tokens, 64-token chunks
+    const uint8_t* xtile;       // [BH][nck][kHolaXTile]
     const __nv_bfloat16* V;     // [BH][n][d]
     const float* alpha;         // [BH][n]
     const float* beta;
@@ -92,330 +102,380 @@ __device__ __forceinline__ void mma_split(uint32_t d, uint32_t idesc, int ksteps
         for (int k = 0; k < ksteps; ++k)
             mma_bf16(d, ad(ta[p], k), bd(tb[p], k), idesc, (accumulate || p > 0 || k > 0) ? 1 : 0);
 }
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+// Right-looking forward substitution of (I + A') u = w for one column held in registers:
+// after u_j is final it is taken out of every later row.  A' is read from shared memory,
+// transposed (Am[j * 64 + t] = A'_tj), four rows per load; entries with t <= j are never used.
+__device__ __forceinline__ void solve_column(float (&acc)[kC], const float* Am) {
+#pragma unroll
+    for (int j = 0; j < kC - 1; ++j) {
+        const float uj = acc[j];
+        const float* col = Am + j * kC;
+#pragma unroll
+        for (int t4 = (j + 1) & ~3; t4 < kC; t4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(col + t4);
+            if (t4 + 0 > j) acc[t4 + 0] = fmaf(-a4.x, uj, acc[t4 + 0]);
+            if (t4 + 1 > j) acc[t4 + 1] = fmaf(-a4.y, uj, acc[t4 + 1]);
+            if (t4 + 2 > j) acc[t4 + 2] = fmaf(-a4.z, uj, acc[t4 + 2]);
+            if (t4 + 3 > j) acc[t4 + 3] = fmaf(-a4.w, uj, acc[t4 + 3]);
+        }
+    }
+}
+
+// The sums over the warp's lanes of 64 per-lane values: after five halving exchanges lane l
+// holds the sums for tokens T(l) and T(l) + 1, T(l) = 32 b4 + 16 b3 + 8 b2 + 4 b1 + 2 b0 (b the
+// bits of l).  v is consumed.
+__device__ __forceinline__ void token_sums(float (&v)[kC], int lane) {
+#pragma unroll
+    for (int o = 16, cnt = kC; o > 0; o >>= 1, cnt >>= 1) {
+        const bool up = lane & o;
+        const int h = cnt / 2;
+#pragma unroll
+        for (int i = 0; i < h; ++i) {
+            const float send = up ? v[i] : v[h + i];
+            const float keep = up ? v[h + i] : v[i];
+            v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+    }
+}
+__device__ __forceinline__ int token_of_lane(int lane) {
+    return 32 * ((lane >> 4) & 1) + 16 * ((lane >> 3) & 1) + 8 * ((lane >> 2) & 1) + 4 * ((lane >> 1) & 1) +
+           2 * (lane & 1);
+}
 
 __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArgs a) {
     extern __shared__ __align__(1024) uint8_t smraw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smraw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = smem_u32(sm);
-    float* Wm = reinterpret_cast<float*>(sm + SW);
     float* Am = reinterpret_cast<float*>(sm + SAm);
-    __shared__ __align__(8) uint64_t mbar;
+    const __nv_bfloat16* Vs = reinterpret_cast<const __nv_bfloat16*>(sm + SV);
+    __shared__ __align__(8) uint64_t bars[4];     // 0: MMA commits, 1-2: the X tiles, 3: value rows
     __shared__ uint32_t tmem_base;
-    __shared__ float cs[kC], gs[kC], bs[kC];
-    __shared__ int fail;
+    __shared__ float cs[kC], ics[kC], bs[kC];     // the pass's c_t, 1 / c_t, beta_t (1, 1, 0 outside it)
+    __shared__ float sp[4][kC];                   // per-warp partial sums of ||u'_t||^2
+    __shared__ int pass_end;
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
-    const int bh = blockIdx.x, n = a.n;
-    const float* qh = a.qh + (int64_t)bh * n * kD;
-    const float* kh = a.kh + (int64_t)bh * n * kD;
+    const int bh = blockIdx.x, n = a.n, nck = a.nck;
+    const uint8_t* xg = a.xtile + (int64_t)bh * nck * kHolaXTile;
     const __nv_bfloat16* V = a.V + (int64_t)bh * n * kD;
     const float* al = a.alpha + (int64_t)bh * n;
     const float* be = a.beta + (int64_t)bh * n;
     float* ys = a.ystate + (int64_t)bh * n * kD;
     float* scores = a.scores + (int64_t)bh * n;
-    const uint32_t bar = smem_u32(&mbar);
+    const uint32_t bar_mma = smem_u32(&bars[0]), bar_v = smem_u32(&bars[3]);
+    const uint32_t bar_x0 = smem_u32(&bars[1]);
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // this warp's TMEM lane quarter
     const int row = (warp & 3) * 32 + lane;                         // its TMEM lane
-    const int chalf = warp >> 2;                                     // warps 4-7: the second half of the columns
+    const int half = warp >> 2;
 
+    // bulk loads in flight (thread 0's bookkeeping, for the abort path)
+    int x_issued[2] = {0, 0}, x_done[2] = {0, 0}, v_issued = 0, v_done = 0;
+    bool mma_pending = false;
     if (tid == 0) {
-        mbar_init(bar, 1);
-        fail = 0;
+        mbar_init(bar_mma, 1);
+        mbar_init(bar_x0, 1);
+        mbar_init(bar_x0 + 8, 1);
+        mbar_init(bar_v, 1);
+        for (int c = 0; c < 2 && c < nck; ++c) {
+            mbar_expect(bar_x0 + 8 * c, kHolaXTile);
+            bulk_load(sb + SX + c * kHolaXTile, xg + (int64_t)c * kHolaXTile, kHolaXTile, bar_x0 + 8 * c);
+            ++x_issued[c];
+        }
+        const uint32_t vb = (uint32_t)min(kC, n) * kD * 2;
+        mbar_expect(bar_v, vb);
+        bulk_load(sb + SV, V, vb, bar_v);
+        ++v_issued;
     }
     if (warp == 0) tmem_alloc<512>(smem_u32(&tmem_base));
     fence_before();
     __syncthreads();
     fence_after();
     const uint32_t tb = tmem_base;
-    // R = 0
-    {
+    {   // R = 0
         float z[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) z[i] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 64; c += 32) tmem_st32(tb + lane_base + TR + 64 * chalf + c, z);
+        for (int c = 0; c < 64; c += 32) tmem_st32(tb + lane_base + TRT + 64 * half + c, z);
         tmem_wait_st();
     }
-    uint32_t phase = 0;
-    float G = 1.f;
-    auto wait_mma = [&]() -> bool {
-        const bool ok = __syncthreads_and(mbar_wait(bar, phase, kWaitNs));
-        phase ^= 1u;
-        fence_after();
-        return ok;
+    // warp 0: this chunk's and the next chunk's alpha, beta at tokens 2 lane, 2 lane + 1
+    float na0 = 1.f, na1 = 1.f, nb0 = 0.f, nb1 = 0.f;
+    auto fetch_ab = [&](int c0) {
+        const int t0 = c0 + 2 * lane;
+        na0 = t0 < n ? al[t0] : 1.f;
+        na1 = t0 + 1 < n ? al[t0 + 1] : 1.f;
+        nb0 = t0 < n ? be[t0] : 0.f;
+        nb1 = t0 + 1 < n ? be[t0 + 1] : 0.f;
     };
-
-    for (int c0 = 0; c0 < n && !fail; c0 += kC) {
-        const int m = min(kC, n - c0);
-        // ---- P0: the chunk's decays (prefix products of alpha; padding tokens: alpha 1, beta 0) ----
+    if (warp == 0) fetch_ab(0);
+    uint32_t ph_mma = 0;
+    float G = 1.f;          // the decay not yet folded into R
+    bool bad = false;       // uniform: set after a barrier reports a failed wait
+    for (int i = 0; i < nck && !bad; ++i) {
+        const int c0 = i * kC, m = min(kC, n - c0), b = i & 1;
+        const uint32_t sx = sb + SX + b * kHolaXTile;
+        float ca0 = 1.f, ca1 = 1.f, cb0 = 0.f, cb1 = 0.f;
         if (warp == 0) {
-            const int t0 = 2 * lane, t1 = 2 * lane + 1;
-            const float a0 = t0 < m ? al[c0 + t0] : 1.f, a1 = t1 < m ? al[c0 + t1] : 1.f;
-            float p = a0 * a1, incl = p;
-#pragma unroll
-            for (int o = 1; o < kWarp; o <<= 1) {
-                const float x = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl *= x;
-            }
-            float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-            if (lane == 0) excl = 1.f;
-            cs[t0] = excl * a0;
-            cs[t1] = excl * p;
-            gs[t0] = G * (excl * a0);
-            gs[t1] = G * (excl * p);
-            bs[t0] = t0 < m ? be[c0 + t0] : 0.f;
-            bs[t1] = t1 < m ? be[c0 + t1] : 0.f;
+            ca0 = na0; ca1 = na1; cb0 = nb0; cb1 = nb1;
+            if (i + 1 < nck) fetch_ab(c0 + kC);
         }
-        __syncthreads();
-        // ---- P0: X = [K^; Q^] (rows 0-63 keys, 64-127 queries) and K' = K^ / g, split ----
-        for (int i = tid; i < 128 * 16; i += kThr) {
-            const int r = i >> 4, c8 = i & 15, t = r & 63;
-            float v[8];
-            if (t < m) {
-                const float* src = (r < 64 ? kh : qh) + (int64_t)(c0 + t) * kD + 8 * c8;
-                const float4 x0 = *reinterpret_cast<const float4*>(src), x1 = *reinterpret_cast<const float4*>(src + 4);
-                v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+        // GM = X K^^T needs only the tile: issued first, it runs under the first pass's split
+        bool xfail = false;
+        if (tid == 0) {
+            if (mbar_wait(bar_x0 + 8 * b, (uint32_t)(x_done[b] & 1), kWaitNs)) {
+                ++x_done[b];
+                mma_split(tb + TGM, idesc_ab(128, 64, 0, 0), kD / 16, false,
+                          [&](int h, int k) { return sdesc(sx + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
+                          [&](int h, int k) { return sdesc(sx + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); });
             } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] = 0.f;
-            }
-            uint4 hi, lo;
-            split8(v, hi, lo);
-            const uint32_t off = (uint32_t)(c8 >> 3) * 16384u + kmaj_chunk(r, c8 & 7);
-            *reinterpret_cast<uint4*>(sm + SX + off) = hi;
-            *reinterpret_cast<uint4*>(sm + SX + kXB + off) = lo;
-            if (r < 64) {
-                const float ig = 1.0f / gs[t];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) v[j] *= ig;
-                split8(v, hi, lo);
-                const uint32_t ko = mnmaj_chunk(t, 8 * c8, kC);
-                *reinterpret_cast<uint4*>(sm + SK + ko) = hi;
-                *reinterpret_cast<uint4*>(sm + SK + kKB + ko) = lo;
+                xfail = true;
             }
         }
-        // R_0 from TMEM (lane = row of R, warps 4-7 the second half of the columns), split, MN-major
-        {
+        for (int s0 = 0; s0 < m && !bad;) {
+            // ---- the pass's decays (warp 0): c_t from s0, the pass ends before c_t < 2^-100 ----
+            if (warp == 0) {
+                const int t0 = 2 * lane, t1 = t0 + 1;
+                const bool in0 = t0 >= s0 && t0 < m, in1 = t1 >= s0 && t1 < m;
+                const float a0 = in0 ? fmaxf(ca0, kMinC) : 1.f, a1 = in1 ? fmaxf(ca1, kMinC) : 1.f;
+                const float p = a0 * a1;
+                float incl = p;
+#pragma unroll
+                for (int o = 1; o < kWarp; o <<= 1) {
+                    const float x = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl *= x;
+                }
+                float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+                if (lane == 0) excl = 1.f;
+                const float c0v = excl * a0, c1v = excl * p;
+                const unsigned f0 = __ballot_sync(0xffffffffu, in0 && c0v < kMinC);
+                const unsigned f1 = __ballot_sync(0xffffffffu, in1 && c1v < kMinC);
+                int s1 = m;
+                if (f0) s1 = min(s1, 2 * (__ffs(f0) - 1));
+                if (f1) s1 = min(s1, 2 * (__ffs(f1) - 1) + 1);
+                const bool on0 = in0 && t0 < s1, on1 = in1 && t1 < s1;
+                cs[t0] = on0 ? c0v : 1.f;
+                cs[t1] = on1 ? c1v : 1.f;
+                ics[t0] = on0 ? 1.0f / c0v : 1.f;
+                ics[t1] = on1 ? 1.0f / c1v : 1.f;
+                bs[t0] = on0 ? cb0 : 0.f;
+                bs[t1] = on1 ? cb1 : 0.f;
+                if (lane == 0) pass_end = s1;
+            }
+            // ---- R_0 = G R (written back when G != 1), split into R_0^T hi, lo (K-major) ----
 #pragma unroll
             for (int cc = 0; cc < 64; cc += 32) {
                 float x[32];
-                tmem_ld32(tb + lane_base + TR + 64 * chalf + cc, x);
+                tmem_ld32(tb + lane_base + TRT + 64 * half + cc, x);
                 tmem_wait_ld();
+                if (G != 1.f) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) x[j] *= G;
+                    tmem_st32(tb + lane_base + TRT + 64 * half + cc, x);
+                }
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
                     uint4 hi, lo;
                     split8(x + j, hi, lo);
-                    const uint32_t ro = mnmaj_chunk(row, 64 * chalf + cc + j, kD);
-                    *reinterpret_cast<uint4*>(sm + SR + ro) = hi;
-                    *reinterpret_cast<uint4*>(sm + SR + kRB + ro) = lo;
+                    const uint32_t off = (uint32_t)half * 16384u + kmaj_chunk(row, (cc + j) >> 3);
+                    *reinterpret_cast<uint4*>(sm + SRT + off) = hi;
+                    *reinterpret_cast<uint4*>(sm + SRT + kRTB + off) = lo;
                 }
             }
-        }
-        fence_async_smem();
-        fence_before();
-        __syncthreads();
-        fence_after();
-        // ---- P1: P = X R_0 (128 x 128), Gm = X K^^T (128 x 64) ----
-        if (tid == 0) {
-            mma_split(tb + TP, idesc_ab(128, 128, 0, 1), kD / 16, false,
-                      [&](int h, int k) { return sdesc(sb + SX + h * kXB + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
-                      [&](int h, int k) { return sdesc(sb + SR + h * kRB + k * 2048, 16384, 1024); });
-            mma_split(tb + TG, idesc_ab(128, 64, 0, 0), kD / 16, false,
-                      [&](int h, int k) { return sdesc(sb + SX + h * kXB + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
-                      [&](int h, int k) { return sdesc(sb + SX + h * kXB + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); });
-            mma_commit(bar);
-        }
-        if (!wait_mma()) {
-            if (tid == 0) fail = 1;
-            break;
-        }
-        // ---- P2: W, A (key rows: warps 0, 1 and 4, 5), the read-out's A (query rows: warps 2, 3) ----
-        if ((warp & 3) < 2) {
-            const int t = row;   // 0 .. 63
-            const float bt = bs[t], gt = gs[t], ct = cs[t];
-            // W_t = beta_t (v_t - g_t R_0^T k^_t): this warp's half of the columns
+            if (G != 1.f) tmem_wait_st();
+            G = 1.f;
+            fence_async_smem();
+            fence_before();
+            __syncthreads();
+            fence_after();
+            const int s1 = pass_end;
+            const bool last = s1 >= m;
+            // ---- P1: D1 = R_0^T X^T (GM was issued with the tile) ----
+            if (tid == 0) {
+                if (!xfail) {
+                    mma_split(tb + TD1, idesc_ab(128, 128, 0, 0), kD / 16, false,
+                              [&](int h, int k) { return sdesc(sb + SRT + h * kRTB + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
+                              [&](int h, int k) { return sdesc(sx + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); });
+                    mma_commit(bar_mma);
+                    mma_pending = true;
+                } else {
+                    mbar_arrive1(bar_mma);   // nothing issued: complete the phase so no thread waits
+                }
+            }
+            {
+                const bool ok = mbar_wait(bar_mma, ph_mma, kWaitNs) && !xfail;
+                if (tid == 0 && ok) mma_pending = false;
+                ph_mma ^= 1u;
+                fence_after();
+                if (!__syncthreads_and(ok)) {
+                    bad = true;
+                    break;
+                }
+            }
+            // ---- A' (warps 4, 5: key rows), A_read (warps 6, 7: query rows), W' (warps 0-3) ----
+            float acc[kC];
+            bool vok = true;
+            if (warp >= 4 && warp < 6) {
+                // A'_tj = beta_t (k^_t . k^_j) for j < t, stored transposed
+                const int t = row;
+                const float bt = bs[t];
 #pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                float x[32];
-                tmem_ld32(tb + lane_base + TP + 64 * chalf + cc, x);
-                tmem_wait_ld();
-                const int col0 = 64 * chalf + cc;
+                for (int cc = 0; cc < 64; cc += 32) {
+                    float x[32];
+                    tmem_ld32(tb + lane_base + TGM + cc, x);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    float v8[8];
-                    if (t < m) {
-                        const uint4 raw = *reinterpret_cast<const uint4*>(V + (int64_t)(c0 + t) * kD + col0 + j);
-                        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+                    for (int j = 0; j < 32; ++j) Am[(cc + j) * kC + t] = cc + j < t ? bt * x[j] : 0.f;
+                }
+            } else if (warp >= 6) {
+                // A_read_tj = q^_t . k^_j for j <= t, split (K-major, row t)
+                const int t = row - 64;
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            v8[2 * q] = __uint_as_float(w4[q] << 16);
-                            v8[2 * q + 1] = __uint_as_float(w4[q] & 0xffff0000u);
-                        }
-                    } else {
+                for (int cc = 0; cc < 64; cc += 32) {
+                    float x[32];
+                    tmem_ld32(tb + lane_base + TGM + cc, x);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) v8[q] = 0.f;
+                    for (int j = 0; j < 32; j += 8) {
+                        float v8[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) v8[q] = cc + j + q <= t ? x[j + q] : 0.f;
+                        uint4 hi, lo;
+                        split8(v8, hi, lo);
+                        const uint32_t off = kmaj_chunk(t, (cc + j) >> 3);
+                        *reinterpret_cast<uint4*>(sm + SAR + off) = hi;
+                        *reinterpret_cast<uint4*>(sm + SAR + kARB + off) = lo;
                     }
-                    float4* dst = reinterpret_cast<float4*>(Wm + t * kD + col0 + j);
-                    dst[0] = make_float4(bt * fmaf(-gt, x[j], v8[0]), bt * fmaf(-gt, x[j + 1], v8[1]),
-                                         bt * fmaf(-gt, x[j + 2], v8[2]), bt * fmaf(-gt, x[j + 3], v8[3]));
-                    dst[1] = make_float4(bt * fmaf(-gt, x[j + 4], v8[4]), bt * fmaf(-gt, x[j + 5], v8[5]),
-                                         bt * fmaf(-gt, x[j + 6], v8[6]), bt * fmaf(-gt, x[j + 7], v8[7]));
+                }
+            } else {
+                // W'_t = beta_t (v_t / c_t - R_0^T k^_t) for column c = row, tokens of the pass only
+                vok = mbar_wait(bar_v, (uint32_t)(i & 1), kWaitNs);
+                const int c = row;
+#pragma unroll
+                for (int cc = 0; cc < 64; cc += 32) {
+                    float x[32];
+                    tmem_ld32(tb + lane_base + TD1 + cc, x);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int t = cc + j;
+                        const float v = __bfloat162float(Vs[t * kD + c]);
+                        acc[t] = (t >= s0 && t < s1) ? bs[t] * fmaf(v, ics[t], -x[j]) : 0.f;
+                    }
                 }
             }
-            // A_tj = beta_t (c_t / c_j) (k^_t . k^_j), j < t: this warp's half of the 64 keys
+            if (!__syncthreads_and(vok)) {
+                bad = true;
+                break;
+            }
+            if (tid == 0 && s0 == 0) ++v_done;   // (thread 0 waited for the rows and got them)
+            // ---- U' by forward substitution (warps 0-3), split into U'^T (K-major, row c) ----
+            if (warp < 4) {
+                solve_column(acc, Am);
+#pragma unroll
+                for (int t = 0; t < kC; t += 8) {
+                    uint4 hi, lo;
+                    split8(acc + t, hi, lo);
+                    const uint32_t off = kmaj_chunk(row, t >> 3);
+                    *reinterpret_cast<uint4*>(sm + SU + off) = hi;
+                    *reinterpret_cast<uint4*>(sm + SU + kUB + off) = lo;
+                }
+                // ||u_t||^2 = ||c_t u'_t||^2 (scaled before squaring: u' alone may be near 2^100)
+#pragma unroll
+                for (int t = 0; t < kC; ++t) {
+                    const float ut = cs[t] * acc[t];
+                    acc[t] = ut * ut;
+                }
+                token_sums(acc, lane);
+                const int t = token_of_lane(lane);
+                sp[warp][t] = acc[0];
+                sp[warp][t + 1] = acc[1];
+            }
+            fence_async_smem();
+            fence_before();
+            __syncthreads();
+            fence_after();
+            // ---- P3: D1[:, 64..] += U'^T A_read^T, R^T += U'^T K^ ----
+            if (tid == 0) {
+                mma_split(tb + TD1 + 64, idesc_ab(128, 64, 0, 0), kC / 16, true,
+                          [&](int h, int k) { return sdesc(sb + SU + h * kUB + k * 32, 16, 1024); },
+                          [&](int h, int k) { return sdesc(sb + SAR + h * kARB + k * 32, 16, 1024); });
+                mma_split(tb + TRT, idesc_ab(128, 128, 0, 1), kC / 16, true,
+                          [&](int h, int k) { return sdesc(sb + SU + h * kUB + k * 32, 16, 1024); },
+                          [&](int h, int k) { return sdesc(sx + h * 32768 + k * 2048, 16384, 1024); });
+                mma_commit(bar_mma);
+                mma_pending = true;
+                if (last && i + 1 < nck) {
+                    // the value rows were read before the last barrier: bring in the next chunk's
+                    const int mn = min(kC, n - c0 - kC);
+                    fence_async_smem();
+                    mbar_expect(bar_v, (uint32_t)mn * kD * 2);
+                    bulk_load(sb + SV, V + (int64_t)(c0 + kC) * kD, (uint32_t)mn * kD * 2, bar_v);
+                    ++v_issued;
+                }
+            }
+            // scores m_t = ||c_t u'_t|| of the pass's tokens
+            if (tid < kC && tid >= s0 && tid < s1)
+                scores[c0 + tid] = sqrtf((sp[0][tid] + sp[1][tid]) + (sp[2][tid] + sp[3][tid]));
+            {
+                const bool ok = mbar_wait(bar_mma, ph_mma, kWaitNs);
+                if (tid == 0 && ok) mma_pending = false;
+                ph_mma ^= 1u;
+                fence_after();
+                if (!__syncthreads_and(ok)) {
+                    bad = true;
+                    break;
+                }
+            }
+            if (tid == 0 && last && i + 2 < nck) {
+                // P3 has read this tile: bring in chunk i + 2
+                mbar_expect(bar_x0 + 8 * b, kHolaXTile);
+                bulk_load(sx, xg + (int64_t)(i + 2) * kHolaXTile, kHolaXTile, bar_x0 + 8 * b);
+                ++x_issued[b];
+            }
+            // ---- the read-outs y_t = c_t D1[c][64 + t] (warp w: tokens 32 (w >> 2) + 0..31) ----
             {
                 float x[32];
-                tmem_ld32(tb + lane_base + TG + 32 * chalf, x);
+                tmem_ld32(tb + lane_base + TD1 + 64 + 32 * half, x);
                 tmem_wait_ld();
+                float* y = ys + (int64_t)c0 * kD + row;
 #pragma unroll
                 for (int j = 0; j < 32; ++j) {
-                    const int jj = 32 * chalf + j;
-                    Am[t * kC + jj] = jj < t ? bt * (ct / cs[jj]) * x[j] : 0.f;
+                    const int t = 32 * half + j;
+                    if (t >= s0 && t < s1) y[(int64_t)t * kD] = cs[t] * x[j];
                 }
             }
-        } else {
-            // query rows: the read-out's A_tj = (c_t / c_j) (q^_t . k^_j), j <= t, split (rows 64+ stay 0)
-            const int t = row - 64;
-            const float ct = cs[t];
-            float x[32];
-            tmem_ld32(tb + lane_base + TG + 32 * chalf, x);
-            tmem_wait_ld();
-#pragma unroll
-            for (int j = 0; j < 32; j += 8) {
-                float v8[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int jj = 32 * chalf + j + q;
-                    v8[q] = jj <= t ? (ct / cs[jj]) * x[j + q] : 0.f;
-                }
-                uint4 hi, lo;
-                split8(v8, hi, lo);
-                const uint32_t off = kmaj_chunk(t, (32 * chalf + j) >> 3);
-                *reinterpret_cast<uint4*>(sm + SA + off) = hi;
-                *reinterpret_cast<uint4*>(sm + SA + kAB + off) = lo;
-            }
-            // rows 64 .. 127 of the read-out's A are zero (the MMA is M = 128)
-            const int r2 = row;   // 64 .. 127
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const uint32_t off = kmaj_chunk(r2, 4 * chalf + j);
-                *reinterpret_cast<uint4*>(sm + SA + off) = make_uint4(0u, 0u, 0u, 0u);
-                *reinterpret_cast<uint4*>(sm + SA + kAB + off) = make_uint4(0u, 0u, 0u, 0u);
-            }
+            G = cs[s1 - 1];
+            fence_before();
+            __syncthreads();
+            fence_after();
+            s0 = s1;
         }
-        __syncthreads();
-        // ---- P2b: U = (I + A)^{-1} W by forward substitution, one column per thread ----
-        if (tid < kD) {
-            const int c = tid;
-            float u[kC];
-#pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                float acc = Wm[t * kD + c];
-#pragma unroll
-                for (int j = 0; j < t; ++j) acc = fmaf(-Am[t * kC + j], u[j], acc);
-                u[t] = acc;
-            }
-#pragma unroll
-            for (int t = 0; t < kC; ++t) {
-                Wm[t * kD + c] = u[t];
-                __nv_bfloat16 h, l;
-                split2(u[t], h, l);
-                const uint32_t off = mnmaj_chunk(t, c, kC) + 2 * (c & 7);
-                *reinterpret_cast<__nv_bfloat16*>(sm + SU + off) = h;
-                *reinterpret_cast<__nv_bfloat16*>(sm + SU + kUB + off) = l;
-            }
-        }
-        fence_async_smem();
-        fence_before();
-        __syncthreads();
-        fence_after();
-        // ---- P3: O = A_read U (128 x 128; rows 0-63 used), R += K'^T U ----
-        if (tid == 0) {
-            mma_split(tb + TO, idesc_ab(128, 128, 0, 1), kC / 16, false,
-                      [&](int h, int k) { return sdesc(sb + SA + h * kAB + k * 32, 16, 1024); },
-                      [&](int h, int k) { return sdesc(sb + SU + h * kUB + k * 2048, 8192, 1024); });
-            mma_split(tb + TR, idesc_ab(128, 128, 1, 1), kC / 16, true,
-                      [&](int h, int k) { return sdesc(sb + SK + h * kKB + k * 2048, 8192, 1024); },
-                      [&](int h, int k) { return sdesc(sb + SU + h * kUB + k * 2048, 8192, 1024); });
-            mma_commit(bar);
-        }
-        // scores m_t = ||u_t|| (warps 4-7: two lanes per token... 16 tokens per warp, 2 lanes each)
-        if (warp >= 4) {
-            const int t = (warp - 4) * 16 + (lane >> 1), h = lane & 1;
-            float s = 0.f;
-            for (int c = 64 * h; c < 64 * h + 64; ++c) s = fmaf(Wm[t * kD + c], Wm[t * kD + c], s);
-            s += __shfl_xor_sync(0xffffffffu, s, 1);
-            if (h == 0 && t < m) scores[c0 + t] = sqrtf(s);
-        }
-        if (!wait_mma()) {
-            if (tid == 0) fail = 1;
-            break;
-        }
-        // ---- P4: the read-outs y_t = O_t + g_t R_0^T q^_t ----
-        if ((warp & 3) >= 2) {
-            const int t = row - 64;
-            const float gt = gs[t];
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                float x[32];
-                tmem_ld32(tb + lane_base + TP + 64 * chalf + cc, x);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4*>(Wm + t * kD + 64 * chalf + cc + j) =
-                        make_float4(gt * x[j], gt * x[j + 1], gt * x[j + 2], gt * x[j + 3]);
-            }
-        }
-        __syncthreads();
-        if ((warp & 3) < 2) {
-            const int t = row;
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                float x[32];
-                tmem_ld32(tb + lane_base + TO + 64 * chalf + cc, x);
-                tmem_wait_ld();
-                if (t < m) {
-                    float* y = ys + (int64_t)(c0 + t) * kD + 64 * chalf + cc;
-                    const float* qr = Wm + t * kD + 64 * chalf + cc;
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4*>(y + j) =
-                            make_float4(x[j] + qr[j], x[j + 1] + qr[j + 1], x[j + 2] + qr[j + 2], x[j + 3] + qr[j + 3]);
-                }
-            }
-        }
-        // ---- the decay after the chunk; fold it into R when it gets small ----
-        G = gs[kC - 1];
-        if (G < 0x1p-40f) {
-            float x[32];
-#pragma unroll
-            for (int cc = 0; cc < 64; cc += 32) {
-                tmem_ld32(tb + lane_base + TR + 64 * chalf + cc, x);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] *= G;
-                tmem_st32(tb + lane_base + TR + 64 * chalf + cc, x);
-            }
-            tmem_wait_st();
-            G = 1.f;
-        }
-        fence_before();
-        __syncthreads();
-        fence_after();
     }
-    if (fail) {
-        if (tid == 0) atomicOr(a.status + 4 * bh + HDR_STATUS, (int)ST_TIMEOUT);
-        // no MMA may still be writing TMEM when it is released
-        if (tid == 0) mbar_wait(bar, phase, 20ull * kWaitNs);
+    if (bad) {
+        if (tid == 0) {
+            atomicOr(a.status + 4 * bh + HDR_STATUS, (int)ST_TIMEOUT);
+            // nothing asynchronous may still be writing TMEM or shared memory when the CTA ends
+            if (mma_pending) mbar_wait(bar_mma, ph_mma ^ 1u, 20ull * kWaitNs);
+            for (int c = 0; c < 2; ++c)
+                if (x_issued[c] > x_done[c]) mbar_wait(bar_x0 + 8 * c, (uint32_t)(x_done[c] & 1), 20ull * kWaitNs);
+            if (v_issued > v_done) mbar_wait(bar_v, (uint32_t)(v_done & 1), 20ull * kWaitNs);
+        }
     } else if (a.S_out) {
-        float* So = a.S_out + (int64_t)bh * kD * kD + (int64_t)row * kD + 64 * chalf;
+        // S = G R: thread (c, half) writes S[k][c] for its 64 keys k
+        float* So = a.S_out + (int64_t)bh * kD * kD + (int64_t)(64 * half) * kD + row;
 #pragma unroll
         for (int cc = 0; cc < 64; cc += 32) {
             float x[32];
-            tmem_ld32(tb + lane_base + TR + 64 * chalf + cc, x);
+            tmem_ld32(tb + lane_base + TRT + 64 * half + cc, x);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; j += 4)
-                *reinterpret_cast<float4*>(So + cc + j) = make_float4(G * x[j], G * x[j + 1], G * x[j + 2], G * x[j + 3]);
+            for (int j = 0; j < 32; ++j) So[(int64_t)(cc + j) * kD] = G * x[j];
         }
     }
     fence_before();
@@ -426,13 +486,13 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
 
 }  // namespace
 
-cudaError_t launch_hola_state_tc(int BH, int n, const float* qh, const float* kh, const void* V, const float* alpha,
+cudaError_t launch_hola_state_tc(int BH, int n, const uint8_t* xtile, const void* V, const float* alpha,
                                  const float* beta, float* ystate, float* scores, float* S_out, int32_t* status,
                                  cudaStream_t st) {
     TcStateArgs a;
     a.n = n;
-    a.qh = qh;
-    a.kh = kh;
+    a.nck = (n + kC - 1) / kC;
+    a.xtile = xtile;
     a.V = static_cast<const __nv_bfloat16*>(V);
     a.alpha = alpha;
     a.beta = beta;

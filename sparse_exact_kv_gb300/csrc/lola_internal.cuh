@@ -261,16 +261,25 @@ cudaError_t launch_decode(const Dims& d, char* state, const Layout& L, const flo
                           int64_t w_head_stride, const void* q, const void* k, const void* v, void* y,
                           int32_t* written_pos, cudaStream_t st);
 cudaError_t launch_state_init(const Dims& d, char* state, const Layout& L, cudaStream_t st);
-// the write-magnitude cache layer (lola_hola.cu; d_k = d_v = 128, bf16 rows)
-cudaError_t launch_hola_prep(int64_t rows, const void* Q, const void* K, const float* gq, const float* gk, float* qh,
-                             float* kh, __nv_bfloat16* qt, __nv_bfloat16* kt, cudaStream_t st);
-cudaError_t launch_hola_state(int BH, int n, const float* qh, const float* kh, const void* V, const float* alpha,
-                              const float* beta, float* ystate, float* scores, float* S_out, cudaStream_t st);
+// the write-magnitude cache layer (lola_hola.cu, lola_hola_tc.cu; d_k = d_v = 128, bf16 rows)
+// The state path's chunk tile: 64 tokens' unit keys (rows 0-63) and unit queries (rows
+// 64-127), every float32 entry split into bf16 hi + lo, in the 128-byte-swizzled K-major layout
+// the tensor-core descriptors read: term h (0 hi, 1 lo) at h * 32 KB; entries 64 e .. 64 e + 63
+// of every row in atom column e (16 KB: 128 rows of 128 B, the 16-byte chunk index XORed with
+// the row mod 8).  Byte offset of entry d of row r, term h.
+constexpr uint32_t kHolaXTile = 65536;
+__host__ __device__ __forceinline__ uint32_t hola_xtile_off(int r, int d, int h) {
+    return (uint32_t)h * 32768u + (uint32_t)(d >> 6) * 16384u + (uint32_t)r * 128u +
+           ((((uint32_t)(d & 63) >> 3) ^ (uint32_t)r) & 7u) * 16u + (uint32_t)(d & 7) * 2u;
+}
+// rows: BH x (64-token chunks x 64); tile: [BH][nck64][kHolaXTile] (rows past n are zero)
+cudaError_t launch_hola_prep(int BH, int n, const void* Q, const void* K, const float* gq, const float* gk,
+                             uint8_t* xtile, __nv_bfloat16* qt, __nv_bfloat16* kt, cudaStream_t st);
 cudaError_t launch_hola_cache(int BH, int n, int w, int chunk, int nck, const float* scores, int32_t* cache,
                               cudaStream_t st);
 int hola_max_cache();
-// the chunked tensor-core form of the same state path (lola_hola_tc.cu); status: [BH][4]
-cudaError_t launch_hola_state_tc(int BH, int n, const float* qh, const float* kh, const void* V, const float* alpha,
+// the state path in chunked form on tcgen05 (lola_hola_tc.cu); status: [BH][4]
+cudaError_t launch_hola_state_tc(int BH, int n, const uint8_t* xtile, const void* V, const float* alpha,
                                  const float* beta, float* ystate, float* scores, float* S_out, int32_t* status,
                                  cudaStream_t st);
 

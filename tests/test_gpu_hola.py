@@ -128,3 +128,17 @@ def test_workload_sampled_heads(L):
     assert np.isfinite(res["Y"]).all()
     for b, h in [(0, 0), (3, 31)]:
         check_head(x, res, b, h, wl["n"])
+
+
+def test_small_decays_split_a_chunk(L):
+    """Decays far below 1 inside a chunk: the state path splits the chunk into passes wherever
+    the running decay would fall below 2^-100 (and takes a decay below 2^-100 as 2^-100, a
+    change of the state far below float32 resolution).  Scores, final state and outputs still
+    follow the oracle's exact recurrence."""
+    x = synth.hola_inputs(1, 2, 300, 128, w=16, chunk=128, dtype="bf16", seed=11)
+    x.alpha[0, 0, [5, 9, 20, 70, 71, 72, 200]] = [1e-20, 1e-20, 1e-20, 1e-30, 1e-30, 1e-30, 1e-35]
+    x.alpha[0, 1, 64:128] = 0.25                 # 0.25^64 = 2^-128: one chunk in two passes or more
+    x.alpha[0, 1, 130] = 1e-40                   # below 2^-100 (taken as 2^-100)
+    res = run_hola(L, x)
+    for h in range(2):
+        check_head(x, res, 0, h, 300)
