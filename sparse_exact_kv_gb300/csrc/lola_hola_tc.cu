@@ -110,21 +110,37 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 
 // Right-looking forward substitution of (I + A') u = w for one column held in registers:
 // after u_j is final it is taken out of every later row.  A' is read from shared memory,
-// transposed (Am[j * 64 + t] = A'_tj), four rows per load; entries with t <= j are never used.
-__device__ __forceinline__ void solve_column(float (&acc)[kC], const float* Am) {
+// transposed (Am[j * 64 + t] = A'_tj), four rows per load (entries with t <= j are not used);
+// column j + 1 is loaded while column j is applied.
+template <int J>
+__device__ __forceinline__ void load_col(float4 (&c)[kC / 4], const float* Am) {
 #pragma unroll
-    for (int j = 0; j < kC - 1; ++j) {
-        const float uj = acc[j];
-        const float* col = Am + j * kC;
+    for (int g = (J + 1) / 4; g < kC / 4; ++g) c[g] = *reinterpret_cast<const float4*>(Am + J * kC + 4 * g);
+}
+template <int J>
+__device__ __forceinline__ void solve_from(float (&acc)[kC], const float* Am, const float4 (&cur)[kC / 4]) {
+    float4 nxt[kC / 4];
+    if constexpr (J + 1 < kC - 1) load_col<J + 1>(nxt, Am);
+    const float uj = acc[J];
 #pragma unroll
-        for (int t4 = (j + 1) & ~3; t4 < kC; t4 += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(col + t4);
-            if (t4 + 0 > j) acc[t4 + 0] = fmaf(-a4.x, uj, acc[t4 + 0]);
-            if (t4 + 1 > j) acc[t4 + 1] = fmaf(-a4.y, uj, acc[t4 + 1]);
-            if (t4 + 2 > j) acc[t4 + 2] = fmaf(-a4.z, uj, acc[t4 + 2]);
-            if (t4 + 3 > j) acc[t4 + 3] = fmaf(-a4.w, uj, acc[t4 + 3]);
-        }
+    for (int g = (J + 1) / 4; g < kC / 4; ++g) {
+        if (4 * g + 0 > J) acc[4 * g + 0] = fmaf(-cur[g].x, uj, acc[4 * g + 0]);
+        if (4 * g + 1 > J) acc[4 * g + 1] = fmaf(-cur[g].y, uj, acc[4 * g + 1]);
+        if (4 * g + 2 > J) acc[4 * g + 2] = fmaf(-cur[g].z, uj, acc[4 * g + 2]);
+        if (4 * g + 3 > J) acc[4 * g + 3] = fmaf(-cur[g].w, uj, acc[4 * g + 3]);
     }
+    if constexpr (J + 1 < kC - 1) solve_from<J + 1>(acc, Am, nxt);
+}
+__device__ __forceinline__ void solve_column(float (&acc)[kC], const float* Am) {
+    float4 c0[kC / 4];
+    load_col<0>(c0, Am);
+    solve_from<0>(acc, Am, c0);
+}
+// a load the compiler keeps where it is written (issued a chunk before its use)
+__device__ __forceinline__ float ld_early(const float* p) {
+    float v;
+    asm volatile("ld.global.nc.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
 }
 
 // The sums over the warp's lanes of 64 per-lane values: after five halving exchanges lane l
@@ -208,12 +224,28 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
     float na0 = 1.f, na1 = 1.f, nb0 = 0.f, nb1 = 0.f;
     auto fetch_ab = [&](int c0) {
         const int t0 = c0 + 2 * lane;
-        na0 = t0 < n ? al[t0] : 1.f;
-        na1 = t0 + 1 < n ? al[t0 + 1] : 1.f;
-        nb0 = t0 < n ? be[t0] : 0.f;
-        nb1 = t0 + 1 < n ? be[t0 + 1] : 0.f;
+        na0 = t0 < n ? ld_early(al + t0) : 1.f;
+        na1 = t0 + 1 < n ? ld_early(al + t0 + 1) : 1.f;
+        nb0 = t0 < n ? ld_early(be + t0) : 0.f;
+        nb1 = t0 + 1 < n ? ld_early(be + t0 + 1) : 0.f;
     };
     if (warp == 0) fetch_ab(0);
+    // GM = X K^^T of a chunk needs only its tile: issued as soon as the tile is in (for chunk
+    // i + 1 right after chunk i's last products), it completes under the commit of the next D1
+    bool xfail_next = false;
+    auto issue_gm = [&](int c) {
+        const int bb = c & 1;
+        const uint32_t sxc = sb + SX + bb * kHolaXTile;
+        if (mbar_wait(bar_x0 + 8 * bb, (uint32_t)(x_done[bb] & 1), kWaitNs)) {
+            ++x_done[bb];
+            mma_split(tb + TGM, idesc_ab(128, 64, 0, 0), kD / 16, false,
+                      [&](int h, int k) { return sdesc(sxc + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
+                      [&](int h, int k) { return sdesc(sxc + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); });
+        } else {
+            xfail_next = true;
+        }
+    };
+    if (tid == 0) issue_gm(0);
     uint32_t ph_mma = 0;
     float G = 1.f;          // the decay not yet folded into R
     bool bad = false;       // uniform: set after a barrier reports a failed wait
@@ -225,18 +257,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
             ca0 = na0; ca1 = na1; cb0 = nb0; cb1 = nb1;
             if (i + 1 < nck) fetch_ab(c0 + kC);
         }
-        // GM = X K^^T needs only the tile: issued first, it runs under the first pass's split
-        bool xfail = false;
-        if (tid == 0) {
-            if (mbar_wait(bar_x0 + 8 * b, (uint32_t)(x_done[b] & 1), kWaitNs)) {
-                ++x_done[b];
-                mma_split(tb + TGM, idesc_ab(128, 64, 0, 0), kD / 16, false,
-                          [&](int h, int k) { return sdesc(sx + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
-                          [&](int h, int k) { return sdesc(sx + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); });
-            } else {
-                xfail = true;
-            }
-        }
+        const bool xfail = xfail_next;   // (thread 0's: its GM issue found no tile)
         for (int s0 = 0; s0 < m && !bad;) {
             // ---- the pass's decays (warp 0): c_t from s0, the pass ends before c_t < 2^-100 ----
             if (warp == 0) {
@@ -410,6 +431,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                           [&](int h, int k) { return sdesc(sx + h * 32768 + k * 2048, 16384, 1024); });
                 mma_commit(bar_mma);
                 mma_pending = true;
+                if (last && i + 1 < nck) issue_gm(i + 1);
                 if (last && i + 1 < nck) {
                     // the value rows were read before the last barrier: bring in the next chunk's
                     const int mn = min(kC, n - c0 - kC);
