@@ -338,8 +338,11 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
                 const float g = prev_write ? warp_dot<D>(W.phi, ebuf[t & (kNEB - 1)], lane) : 0.f;
                 if (lane == 0) gbuf[t & 1] = g;
             }
-            const int j = hidx * kWarp + lane;
-            npart[t & 1][j] = reduce_partials_col<D, DV>(&red[t & 1][0][0], j);
+            // (clusters: summed in the previous step's key exchange, except for step 0)
+            if (!CLUSTER || t == 0) {
+                const int j = hidx * kWarp + lane;
+                npart[t & 1][j] = reduce_partials_col<D, DV>(&red[t & 1][0][0], j);
+            }
             named_arrive(kHandoff);
         }
 
@@ -432,6 +435,12 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const SelArgs a) {
             const uint32_t xb = xbar0 + 8 * b;
             if (warp == 0 && lane < CL && lane != rank)
                 st_async_v2(map_rank(smem_addr(&exch[b][rank]), lane), k.x, k.y, map_rank(xb, lane));
+            // while the peers' keys travel: the helpers sum the next evictee's H^T phi partials
+            // (complete since the barrier above), which the next step would otherwise start with
+            if (hidx < kHelp && t + 1 >= eta) {
+                const int j = hidx * kWarp + lane;
+                npart[(t + 1) & 1][j] = reduce_partials_col<D, DV>(&red[(t + 1) & 1][0][0], j);
+            }
             if (tid == kThreads - 1) {
                 mbar_arrive_expect_tx(xb, (uint32_t)((CL - 1) * 8));
                 if (!xbar_wait(xb, (uint32_t)(t >> 1) & 1u)) x_abort = 1;
