@@ -28,6 +28,8 @@
 // float32 accumulation.  The unit rows arrive pre-split in the tile layout the descriptors read
 // (written by the row kernel, 64 KB per chunk, one bulk copy, two chunks in flight); the chunk's
 // value rows by a bulk copy one chunk ahead.  One CTA of 256 threads per head.
+#include <utility>
+
 #include "lola_internal.cuh"
 #include "lola_tc.cuh"
 
@@ -44,6 +46,7 @@ constexpr float kMinC = 0x1p-100f;   // a pass ends before its decay falls below
 
 // TMEM columns (128 lanes, lane = value column c): R^T, D1 = R_0^T X^T, GM = X K^^T (lane = X row)
 constexpr uint32_t TRT = 0, TD1 = 128, TGM = 256;
+constexpr uint32_t TZ = 320;   // the substitution's off-diagonal sums: lane c, column t - 16 (t = 16 .. 63)
 
 // shared memory (bytes from a 1024-aligned base)
 constexpr uint32_t SX = 0;                     // two chunk tiles X = [K^; Q^] (hi, lo), kHolaXTile each
@@ -53,6 +56,8 @@ constexpr uint32_t SU = SRT;                   // (after P1, over R_0^T) U'^T hi
 constexpr uint32_t kUB = 16384;
 constexpr uint32_t SAR = SRT + 32768;          // (after P1) A_read hi, lo: K-major 64 x 64
 constexpr uint32_t kARB = 8192;
+constexpr uint32_t SAB = SRT + 49152;          // (after P1) A' hi, lo: K-major 64 x 64 (row t, K = j)
+constexpr uint32_t kABB = 8192;
 constexpr uint32_t SAm = SRT + 2 * kRTB;       // A' float32, transposed: [j][t]
 constexpr uint32_t SV = SAm + 4 * kC * kC;     // the chunk's value rows, bf16 [64][128]
 constexpr uint32_t SEND = SV + 2 * kC * kD;
@@ -108,34 +113,38 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  : "memory");
 }
 
-// Right-looking forward substitution of (I + A') u = w for one column held in registers:
-// after u_j is final it is taken out of every later row.  A' is read from shared memory,
-// transposed (Am[j * 64 + t] = A'_tj), four rows per load (entries with t <= j are not used);
-// column j + 1 is loaded while column j is applied.
-template <int J>
-__device__ __forceinline__ void load_col(float4 (&c)[kC / 4], const float* Am) {
+// The substitution (I + A') u = w in four blocks of 16 rows.  A diagonal block is solved from
+// registers (right-looking, A' transposed in shared memory: Am[j * 64 + t] = A'_tj, four rows per
+// load); the rows below take the block's u through a split product on tcgen05 (see the kernel).
+template <int B>
+__device__ __forceinline__ void solve_diag(float (&acc)[kC], const float* Am) {
 #pragma unroll
-    for (int g = (J + 1) / 4; g < kC / 4; ++g) c[g] = *reinterpret_cast<const float4*>(Am + J * kC + 4 * g);
-}
-template <int J>
-__device__ __forceinline__ void solve_from(float (&acc)[kC], const float* Am, const float4 (&cur)[kC / 4]) {
-    float4 nxt[kC / 4];
-    if constexpr (J + 1 < kC - 1) load_col<J + 1>(nxt, Am);
-    const float uj = acc[J];
+    for (int j = 16 * B; j < 16 * B + 15; ++j) {
+        const float uj = acc[j];
 #pragma unroll
-    for (int g = (J + 1) / 4; g < kC / 4; ++g) {
-        if (4 * g + 0 > J) acc[4 * g + 0] = fmaf(-cur[g].x, uj, acc[4 * g + 0]);
-        if (4 * g + 1 > J) acc[4 * g + 1] = fmaf(-cur[g].y, uj, acc[4 * g + 1]);
-        if (4 * g + 2 > J) acc[4 * g + 2] = fmaf(-cur[g].z, uj, acc[4 * g + 2]);
-        if (4 * g + 3 > J) acc[4 * g + 3] = fmaf(-cur[g].w, uj, acc[4 * g + 3]);
+        for (int t4 = (j + 1) & ~3; t4 < 16 * B + 16; t4 += 4) {
+            const float4 a4 = *reinterpret_cast<const float4*>(Am + j * kC + t4);
+            if (t4 + 0 > j) acc[t4 + 0] = fmaf(-a4.x, uj, acc[t4 + 0]);
+            if (t4 + 1 > j) acc[t4 + 1] = fmaf(-a4.y, uj, acc[t4 + 1]);
+            if (t4 + 2 > j) acc[t4 + 2] = fmaf(-a4.z, uj, acc[t4 + 2]);
+            if (t4 + 3 > j) acc[t4 + 3] = fmaf(-a4.w, uj, acc[t4 + 3]);
+        }
     }
-    if constexpr (J + 1 < kC - 1) solve_from<J + 1>(acc, Am, nxt);
 }
-__device__ __forceinline__ void solve_column(float (&acc)[kC], const float* Am) {
-    float4 c0[kC / 4];
-    load_col<0>(c0, Am);
-    solve_from<0>(acc, Am, c0);
+// 16 consecutive fp32 columns of this thread's TMEM lane (warp-collective)
+__device__ __forceinline__ void tmem_ld16f(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// the solve warps (0-3) only
+__device__ __forceinline__ void solve_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 // a load the compiler keeps where it is written (issued a chunk before its use)
 __device__ __forceinline__ float ld_early(const float* p) {
     float v;
@@ -170,7 +179,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
     const uint32_t sb = smem_u32(sm);
     float* Am = reinterpret_cast<float*>(sm + SAm);
     const __nv_bfloat16* Vs = reinterpret_cast<const __nv_bfloat16*>(sm + SV);
-    __shared__ __align__(8) uint64_t bars[4];     // 0: MMA commits, 1-2: the X tiles, 3: value rows
+    __shared__ __align__(8) uint64_t bars[5];     // 0: MMA commits, 1-2: the X tiles, 3: value rows, 4: solve products
     __shared__ uint32_t tmem_base;
     __shared__ float cs[kC], ics[kC], bs[kC];     // the pass's c_t, 1 / c_t, beta_t (1, 1, 0 outside it)
     __shared__ float sp[4][kC];                   // per-warp partial sums of ||u'_t||^2
@@ -184,19 +193,20 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
     float* ys = a.ystate + (int64_t)bh * n * kD;
     float* scores = a.scores + (int64_t)bh * n;
     const uint32_t bar_mma = smem_u32(&bars[0]), bar_v = smem_u32(&bars[3]);
-    const uint32_t bar_x0 = smem_u32(&bars[1]);
+    const uint32_t bar_x0 = smem_u32(&bars[1]), bar_z = smem_u32(&bars[4]);
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // this warp's TMEM lane quarter
     const int row = (warp & 3) * 32 + lane;                         // its TMEM lane
     const int half = warp >> 2;
 
     // bulk loads in flight (thread 0's bookkeeping, for the abort path)
     int x_issued[2] = {0, 0}, x_done[2] = {0, 0}, v_issued = 0, v_done = 0;
-    bool mma_pending = false;
+    bool mma_pending = false, z_pending = false;
     if (tid == 0) {
         mbar_init(bar_mma, 1);
         mbar_init(bar_x0, 1);
         mbar_init(bar_x0 + 8, 1);
         mbar_init(bar_v, 1);
+        mbar_init(bar_z, 1);
         for (int c = 0; c < 2 && c < nck; ++c) {
             mbar_expect(bar_x0 + 8 * c, kHolaXTile);
             bulk_load(sb + SX + c * kHolaXTile, xg + (int64_t)c * kHolaXTile, kHolaXTile, bar_x0 + 8 * c);
@@ -246,7 +256,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
         }
     };
     if (tid == 0) issue_gm(0);
-    uint32_t ph_mma = 0;
+    uint32_t ph_mma = 0, ph_z = 0;
     float G = 1.f;          // the decay not yet folded into R
     bool bad = false;       // uniform: set after a barrier reports a failed wait
     for (int i = 0; i < nck && !bad; ++i) {
@@ -351,7 +361,19 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                     tmem_ld32(tb + lane_base + TGM + cc, x);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) Am[(cc + j) * kC + t] = cc + j < t ? bt * x[j] : 0.f;
+                    for (int j = 0; j < 32; ++j) {
+                        x[j] = cc + j < t ? bt * x[j] : 0.f;
+                        Am[(cc + j) * kC + t] = x[j];
+                    }
+                    // and row-major, split (K-major, row t): the B operand of the block products
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 hi, lo;
+                        split8(x + j, hi, lo);
+                        const uint32_t off = kmaj_chunk(t, (cc + j) >> 3);
+                        *reinterpret_cast<uint4*>(sm + SAB + off) = hi;
+                        *reinterpret_cast<uint4*>(sm + SAB + kABB + off) = lo;
+                    }
                 }
             } else if (warp >= 6) {
                 // A_read_tj = q^_t . k^_j for j <= t, split (K-major, row t)
@@ -390,22 +412,55 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                     }
                 }
             }
+            fence_async_smem();   // A' and A_read tiles are read by the tensor core
             if (!__syncthreads_and(vok)) {
                 bad = true;
                 break;
             }
             if (tid == 0 && s0 == 0) ++v_done;   // (thread 0 waited for the rows and got them)
-            // ---- U' by forward substitution (warps 0-3), split into U'^T (K-major, row c) ----
+            // ---- U' by blocks of 16 rows (warps 0-3): block b solved from registers and split into
+            //      U'^T (K-major, row c); the rows below it take TZ[:, 16 b ..] (+)= U'_b^T A'_b^T
+            //      (M = 128, N = 48 - 16 b, K = 16) on tcgen05, read back before their own block ----
+            bool zok = true;
             if (warp < 4) {
-                solve_column(acc, Am);
+                auto block_done = [&](auto bc) {
+                    constexpr int B = decltype(bc)::value;
+                    solve_diag<B>(acc, Am);
 #pragma unroll
-                for (int t = 0; t < kC; t += 8) {
-                    uint4 hi, lo;
-                    split8(acc + t, hi, lo);
-                    const uint32_t off = kmaj_chunk(row, t >> 3);
-                    *reinterpret_cast<uint4*>(sm + SU + off) = hi;
-                    *reinterpret_cast<uint4*>(sm + SU + kUB + off) = lo;
-                }
+                    for (int t = 16 * B; t < 16 * B + 16; t += 8) {
+                        uint4 hi, lo;
+                        split8(acc + t, hi, lo);
+                        const uint32_t off = kmaj_chunk(row, t >> 3);
+                        *reinterpret_cast<uint4*>(sm + SU + off) = hi;
+                        *reinterpret_cast<uint4*>(sm + SU + kUB + off) = lo;
+                    }
+                    if constexpr (B < 3) {
+                        fence_async_smem();
+                        fence_before();
+                        solve_sync();
+                        fence_after();
+                        if (tid == 0) {
+                            mma_split(tb + TZ + 16 * B, idesc_ab(128, 48 - 16 * B, 0, 0), 1, B > 0,
+                                      [&](int h, int k) { return sdesc(sb + SU + h * kUB + 32 * B, 16, 1024); },
+                                      [&](int h, int k) {
+                                          return sdesc(sb + SAB + h * kABB + 2048 * (B + 1) + 32 * B, 16, 1024);
+                                      });
+                            mma_commit(bar_z);
+                        }
+                        zok = mbar_wait(bar_z, ph_z, kWaitNs) && zok;
+                        ph_z ^= 1u;
+                        fence_after();
+                        float z[16];
+                        tmem_ld16f(tb + lane_base + TZ + 16 * B, z);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q) acc[16 * (B + 1) + q] -= z[q];
+                    }
+                };
+                block_done(std::integral_constant<int, 0>{});
+                block_done(std::integral_constant<int, 1>{});
+                block_done(std::integral_constant<int, 2>{});
+                block_done(std::integral_constant<int, 3>{});
                 // ||u_t||^2 = ||c_t u'_t||^2 (scaled before squaring: u' alone may be near 2^100)
 #pragma unroll
                 for (int t = 0; t < kC; ++t) {
@@ -417,9 +472,13 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                 sp[warp][t] = acc[0];
                 sp[warp][t + 1] = acc[1];
             }
+            if (tid == 0 && !zok) z_pending = true;
             fence_async_smem();
             fence_before();
-            __syncthreads();
+            if (!__syncthreads_and(zok)) {
+                bad = true;
+                break;
+            }
             fence_after();
             // ---- P3: D1[:, 64..] += U'^T A_read^T, R^T += U'^T K^ ----
             if (tid == 0) {
@@ -484,6 +543,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
             atomicOr(a.status + 4 * bh + HDR_STATUS, (int)ST_TIMEOUT);
             // nothing asynchronous may still be writing TMEM or shared memory when the CTA ends
             if (mma_pending) mbar_wait(bar_mma, ph_mma ^ 1u, 20ull * kWaitNs);
+            if (z_pending) mbar_wait(bar_z, ph_z ^ 1u, 20ull * kWaitNs);
             for (int c = 0; c < 2; ++c)
                 if (x_issued[c] > x_done[c]) mbar_wait(bar_x0 + 8 * c, (uint32_t)(x_done[c] & 1), 20ull * kWaitNs);
             if (v_issued > v_done) mbar_wait(bar_v, (uint32_t)(v_done & 1), 20ull * kWaitNs);
