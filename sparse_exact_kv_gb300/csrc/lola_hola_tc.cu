@@ -58,10 +58,12 @@ constexpr uint32_t SAR = SRT + 32768;          // (after P1) A_read hi, lo: K-ma
 constexpr uint32_t kARB = 8192;
 constexpr uint32_t SAB = SRT + 49152;          // (after P1) A' hi, lo: K-major 64 x 64 (row t, K = j)
 constexpr uint32_t kABB = 8192;
-constexpr uint32_t SAm = SRT + 2 * kRTB;       // A' float32, transposed: [j][t]
+constexpr uint32_t SAm = SRT + 2 * kRTB;       // A''s four diagonal 16 x 16 blocks, float32, [block][j][t]
+constexpr uint32_t SVEC = SAm + 4 * 16 * 16 * 4;   // per-pass vectors (float32 [64] each): see the kernel
 constexpr uint32_t SV = SAm + 4 * kC * kC;     // the chunk's value rows, bf16 [64][128]
 constexpr uint32_t SEND = SV + 2 * kC * kD;
 static_assert(SEND + 1024 + 2048 <= 232448, "shared memory plan exceeds 227 KB");
+static_assert(SVEC + 4 * kC * 8 <= SV, "per-pass vectors overlap the value rows");
 
 struct TcStateArgs {
     int n, nck;                 // tokens, 64-token chunks
@@ -114,8 +116,9 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 }
 
 // The substitution (I + A') u = w in four blocks of 16 rows.  A diagonal block is solved from
-// registers (right-looking, A' transposed in shared memory: Am[j * 64 + t] = A'_tj, four rows per
-// load); the rows below take the block's u through a split product on tcgen05 (see the kernel).
+// registers (right-looking, the block of A' transposed in shared memory:
+// Am[256 B' + 16 (j - 16 B') + (t - 16 B')] = A'_tj, four rows per load); the rows below take the
+// block's u through a split product on tcgen05 (see the kernel).
 template <int B>
 __device__ __forceinline__ void solve_diag(float (&acc)[kC], const float* Am) {
 #pragma unroll
@@ -123,7 +126,7 @@ __device__ __forceinline__ void solve_diag(float (&acc)[kC], const float* Am) {
         const float uj = acc[j];
 #pragma unroll
         for (int t4 = (j + 1) & ~3; t4 < 16 * B + 16; t4 += 4) {
-            const float4 a4 = *reinterpret_cast<const float4*>(Am + j * kC + t4);
+            const float4 a4 = *reinterpret_cast<const float4*>(Am + 256 * B + 16 * (j - 16 * B) + (t4 - 16 * B));
             if (t4 + 0 > j) acc[t4 + 0] = fmaf(-a4.x, uj, acc[t4 + 0]);
             if (t4 + 1 > j) acc[t4 + 1] = fmaf(-a4.y, uj, acc[t4 + 1]);
             if (t4 + 2 > j) acc[t4 + 2] = fmaf(-a4.z, uj, acc[t4 + 2]);
@@ -179,11 +182,18 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
     const uint32_t sb = smem_u32(sm);
     float* Am = reinterpret_cast<float*>(sm + SAm);
     const __nv_bfloat16* Vs = reinterpret_cast<const __nv_bfloat16*>(sm + SV);
-    __shared__ __align__(8) uint64_t bars[5];     // 0: MMA commits, 1-2: the X tiles, 3: value rows, 4: solve products
+    // mbarriers: 0 MMA commits (thread 0), 1-2 the X tiles, 3 value rows, 4 solve products,
+    // 5 X K^T (thread 128)
+    __shared__ __align__(8) uint64_t bars[6];
     __shared__ uint32_t tmem_base;
-    __shared__ float cs[kC], ics[kC], bs[kC];     // the pass's c_t, 1 / c_t, beta_t (1, 1, 0 outside it)
-    __shared__ float sp[4][kC];                   // per-warp partial sums of ||u'_t||^2
-    __shared__ int pass_end;
+    __shared__ int pass_end, gm_bad;
+    // per-pass vectors: c_t by pass parity (the read-outs of a pass are stored during the next
+    // pass's first phase), 1 / c_t, beta_t (1, 1, 0 outside the pass), and the per-warp partial
+    // sums of ||u_t||^2
+    float (*cs2)[kC] = reinterpret_cast<float (*)[kC]>(sm + SVEC);
+    float* ics = reinterpret_cast<float*>(sm + SVEC + 2 * 4 * kC);
+    float* bs = reinterpret_cast<float*>(sm + SVEC + 3 * 4 * kC);
+    float (*sp)[kC] = reinterpret_cast<float (*)[kC]>(sm + SVEC + 4 * 4 * kC);
     const int tid = threadIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const int bh = blockIdx.x, n = a.n, nck = a.nck;
     const uint8_t* xg = a.xtile + (int64_t)bh * nck * kHolaXTile;
@@ -193,20 +203,24 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
     float* ys = a.ystate + (int64_t)bh * n * kD;
     float* scores = a.scores + (int64_t)bh * n;
     const uint32_t bar_mma = smem_u32(&bars[0]), bar_v = smem_u32(&bars[3]);
-    const uint32_t bar_x0 = smem_u32(&bars[1]), bar_z = smem_u32(&bars[4]);
+    const uint32_t bar_x0 = smem_u32(&bars[1]), bar_z = smem_u32(&bars[4]), bar_gm = smem_u32(&bars[5]);
+    constexpr int kGmThread = 128;   // issues X K^T (a lane of warp 4, which reads it first)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;   // this warp's TMEM lane quarter
     const int row = (warp & 3) * 32 + lane;                         // its TMEM lane
     const int half = warp >> 2;
 
-    // bulk loads in flight (thread 0's bookkeeping, for the abort path)
+    // bulk loads and products in flight (for the abort path): thread 0 issues the loads, D1, the
+    // solve products and P3; thread kGmThread X K^T; each waits once on every phase it needs
     int x_issued[2] = {0, 0}, x_done[2] = {0, 0}, v_issued = 0, v_done = 0;
-    bool mma_pending = false, z_pending = false;
+    bool mma_pending = false, z_pending = false, gm_pending = false;
     if (tid == 0) {
         mbar_init(bar_mma, 1);
         mbar_init(bar_x0, 1);
         mbar_init(bar_x0 + 8, 1);
         mbar_init(bar_v, 1);
         mbar_init(bar_z, 1);
+        mbar_init(bar_gm, 1);
+        gm_bad = 0;
         for (int c = 0; c < 2 && c < nck; ++c) {
             mbar_expect(bar_x0 + 8 * c, kHolaXTile);
             bulk_load(sb + SX + c * kHolaXTile, xg + (int64_t)c * kHolaXTile, kHolaXTile, bar_x0 + 8 * c);
@@ -240,25 +254,45 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
         nb1 = t0 + 1 < n ? ld_early(be + t0 + 1) : 0.f;
     };
     if (warp == 0) fetch_ab(0);
-    // GM = X K^^T of a chunk needs only its tile: issued as soon as the tile is in (for chunk
-    // i + 1 right after chunk i's last products), it completes under the commit of the next D1
-    bool xfail_next = false;
+    // GM = X K^^T of a chunk needs only its tile: thread kGmThread issues it as soon as the tile is
+    // in (for chunk i + 1 right after chunk i's last products) and commits it to bar_gm; the
+    // warps that read GM wait there (chunk i: parity i & 1).  A tile that never lands sets gm_bad
+    // and completes the phase without products.
+    int gx_done[2] = {0, 0};
     auto issue_gm = [&](int c) {
         const int bb = c & 1;
         const uint32_t sxc = sb + SX + bb * kHolaXTile;
-        if (mbar_wait(bar_x0 + 8 * bb, (uint32_t)(x_done[bb] & 1), kWaitNs)) {
-            ++x_done[bb];
+        if (mbar_wait(bar_x0 + 8 * bb, (uint32_t)(gx_done[bb] & 1), kWaitNs)) {
+            ++gx_done[bb];
             mma_split(tb + TGM, idesc_ab(128, 64, 0, 0), kD / 16, false,
                       [&](int h, int k) { return sdesc(sxc + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); },
                       [&](int h, int k) { return sdesc(sxc + h * 32768 + (k >> 2) * 16384 + (k & 3) * 32, 16, 1024); });
+            mma_commit(bar_gm);
+            gm_pending = true;
         } else {
-            xfail_next = true;
+            gm_bad = 1;
+            mbar_arrive1(bar_gm);
         }
     };
-    if (tid == 0) issue_gm(0);
+    if (tid == kGmThread) issue_gm(0);
     uint32_t ph_mma = 0, ph_z = 0;
     float G = 1.f;          // the decay not yet folded into R
     bool bad = false;       // uniform: set after a barrier reports a failed wait
+    // the read-outs of a pass are stored while the next pass splits R_0: y_t = c_t D1[c][64 + t]
+    // (warp w: tokens 32 (w >> 2) + 0..31 of the pass [y_s0, y_s1) of the chunk at y_c0)
+    int pb = 0, y_c0 = -1, y_s0 = 0, y_s1 = 0;
+    auto store_readouts = [&]() {
+        float x[32];
+        tmem_ld32(tb + lane_base + TD1 + 64 + 32 * half, x);
+        tmem_wait_ld();
+        float* y = ys + (int64_t)y_c0 * kD + row;
+        const float* cp = cs2[pb ^ 1];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int t = 32 * half + j;
+            if (t >= y_s0 && t < y_s1) y[(int64_t)t * kD] = cp[t] * x[j];
+        }
+    };
     for (int i = 0; i < nck && !bad; ++i) {
         const int c0 = i * kC, m = min(kC, n - c0), b = i & 1;
         const uint32_t sx = sb + SX + b * kHolaXTile;
@@ -267,7 +301,12 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
             ca0 = na0; ca1 = na1; cb0 = nb0; cb1 = nb1;
             if (i + 1 < nck) fetch_ab(c0 + kC);
         }
-        const bool xfail = xfail_next;   // (thread 0's: its GM issue found no tile)
+        // thread 0 reads the tile in D1 and P3: it waits for it too (normally long landed)
+        bool xfail = false;
+        if (tid == 0) {
+            if (mbar_wait(bar_x0 + 8 * b, (uint32_t)(x_done[b] & 1), kWaitNs)) ++x_done[b];
+            else xfail = true;
+        }
         for (int s0 = 0; s0 < m && !bad;) {
             // ---- the pass's decays (warp 0): c_t from s0, the pass ends before c_t < 2^-100 ----
             if (warp == 0) {
@@ -290,8 +329,8 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                 if (f0) s1 = min(s1, 2 * (__ffs(f0) - 1));
                 if (f1) s1 = min(s1, 2 * (__ffs(f1) - 1) + 1);
                 const bool on0 = in0 && t0 < s1, on1 = in1 && t1 < s1;
-                cs[t0] = on0 ? c0v : 1.f;
-                cs[t1] = on1 ? c1v : 1.f;
+                cs2[pb][t0] = on0 ? c0v : 1.f;
+                cs2[pb][t1] = on1 ? c1v : 1.f;
                 ics[t0] = on0 ? 1.0f / c0v : 1.f;
                 ics[t1] = on1 ? 1.0f / c1v : 1.f;
                 bs[t0] = on0 ? cb0 : 0.f;
@@ -320,12 +359,15 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
             }
             if (G != 1.f) tmem_wait_st();
             G = 1.f;
+            if (y_c0 >= 0) store_readouts();   // the previous pass's (D1 is rewritten after the barrier)
             fence_async_smem();
             fence_before();
             __syncthreads();
             fence_after();
             const int s1 = pass_end;
             const bool last = s1 >= m;
+            const float* cs = cs2[pb];
+            if (tid == 0) xfail = xfail || gm_bad;
             // ---- P1: D1 = R_0^T X^T (GM was issued with the tile) ----
             if (tid == 0) {
                 if (!xfail) {
@@ -351,8 +393,14 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
             // ---- A' (warps 4, 5: key rows), A_read (warps 6, 7: query rows), W' (warps 0-3) ----
             float acc[kC];
             bool vok = true;
+            bool gok = true;
+            if (warp >= 4) {   // GM of this chunk (issued a chunk ahead)
+                gok = mbar_wait(bar_gm, (uint32_t)(i & 1), kWaitNs);
+                if (tid == kGmThread && gok) gm_pending = false;
+                fence_after();
+            }
             if (warp >= 4 && warp < 6) {
-                // A'_tj = beta_t (k^_t . k^_j) for j < t, stored transposed
+                // A'_tj = beta_t (k^_t . k^_j) for j < t: the diagonal blocks transposed
                 const int t = row;
                 const float bt = bs[t];
 #pragma unroll
@@ -363,7 +411,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         x[j] = cc + j < t ? bt * x[j] : 0.f;
-                        Am[(cc + j) * kC + t] = x[j];
+                        if (((cc + j) >> 4) == (t >> 4)) Am[256 * (t >> 4) + 16 * ((cc + j) & 15) + (t & 15)] = x[j];
                     }
                     // and row-major, split (K-major, row t): the B operand of the block products
 #pragma unroll
@@ -413,7 +461,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                 }
             }
             fence_async_smem();   // A' and A_read tiles are read by the tensor core
-            if (!__syncthreads_and(vok)) {
+            if (!__syncthreads_and(vok && gok)) {
                 bad = true;
                 break;
             }
@@ -490,7 +538,6 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                           [&](int h, int k) { return sdesc(sx + h * 32768 + k * 2048, 16384, 1024); });
                 mma_commit(bar_mma);
                 mma_pending = true;
-                if (last && i + 1 < nck) issue_gm(i + 1);
                 if (last && i + 1 < nck) {
                     // the value rows were read before the last barrier: bring in the next chunk's
                     const int mn = min(kC, n - c0 - kC);
@@ -500,6 +547,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                     ++v_issued;
                 }
             }
+            if (tid == kGmThread && last && i + 1 < nck) issue_gm(i + 1);
             // scores m_t = ||c_t u'_t|| of the pass's tokens
             if (tid < kC && tid >= s0 && tid < s1)
                 scores[c0 + tid] = sqrtf((sp[0][tid] + sp[1][tid]) + (sp[2][tid] + sp[3][tid]));
@@ -519,25 +567,15 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                 bulk_load(sx, xg + (int64_t)(i + 2) * kHolaXTile, kHolaXTile, bar_x0 + 8 * b);
                 ++x_issued[b];
             }
-            // ---- the read-outs y_t = c_t D1[c][64 + t] (warp w: tokens 32 (w >> 2) + 0..31) ----
-            {
-                float x[32];
-                tmem_ld32(tb + lane_base + TD1 + 64 + 32 * half, x);
-                tmem_wait_ld();
-                float* y = ys + (int64_t)c0 * kD + row;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int t = 32 * half + j;
-                    if (t >= s0 && t < s1) y[(int64_t)t * kD] = cs[t] * x[j];
-                }
-            }
             G = cs[s1 - 1];
-            fence_before();
-            __syncthreads();
-            fence_after();
+            y_c0 = c0;
+            y_s0 = s0;
+            y_s1 = s1;
+            pb ^= 1;
             s0 = s1;
         }
     }
+    if (!bad) store_readouts();
     if (bad) {
         if (tid == 0) {
             atomicOr(a.status + 4 * bh + HDR_STATUS, (int)ST_TIMEOUT);
@@ -548,6 +586,7 @@ __global__ void __launch_bounds__(kThr, 1) hola_state_tc_kernel(const TcStateArg
                 if (x_issued[c] > x_done[c]) mbar_wait(bar_x0 + 8 * c, (uint32_t)(x_done[c] & 1), 20ull * kWaitNs);
             if (v_issued > v_done) mbar_wait(bar_v, (uint32_t)(v_done & 1), 20ull * kWaitNs);
         }
+        if (tid == kGmThread && gm_pending) mbar_wait(bar_gm, (uint32_t)((gx_done[0] + gx_done[1] - 1) & 1), 20ull * kWaitNs);
     } else if (a.S_out) {
         // S = G R: thread (c, half) writes S[k][c] for its 64 keys k
         float* So = a.S_out + (int64_t)bh * kD * kD + (int64_t)(64 * half) * kD + row;
