@@ -262,20 +262,27 @@ NCU_TRAFFIC = {
     # scaled x4 to n = 131072 -- every kernel's traffic grows in proportion to the tokens (the
     # chain streams each key's rows once, the output pass reads one pool per 128-query tile)
     ("select", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                           "digest": "942e14a39edfba5c", "bytes_per_launch": 4 * (207.43e6 + 27.64e6)},
+                                           "digest": "bbeedb523c50d005", "bytes_per_launch": 4 * (207.87e6 + 27.81e6)},
     ("output", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                           "digest": "dc476ed3069109fa", "bytes_per_launch": 4 * (372.91e6 + 53.16e6)},
+                                           "digest": "a760322973f38312", "bytes_per_launch": 4 * (373.03e6 + 52.85e6)},
     ("phi", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
-                                        "digest": "45133dcab50d1c6f", "bytes_per_launch": 4 * (67.20e6 + 140.72e6)},
+                                        "digest": "2bf9c2757e9b5350", "bytes_per_launch": 4 * (67.20e6 + 140.94e6)},
     ("phi_q", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
-                                          "digest": "45133dcab50d1c6f", "bytes_per_launch": 4 * (67.19e6 + 12.99e6)},
-    # 4 x 32 heads, n = 4096: the output pass, one launch (--set full capture)
+                                          "digest": "2bf9c2757e9b5350", "bytes_per_launch": 4 * (67.19e6 + 13.51e6)},
+    # 4 x 32 heads, n = 4096: the output pass, one launch
     ("output", "w2_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                        "digest": "33f7134677057231", "bytes_per_launch": 810.65e6 + 122.78e6},
+                                        "digest": "a760322973f38312", "bytes_per_launch": 810.64e6 + 121.70e6},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
     ("decode", "w4_bf16_decode_b64h32"): {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                          "digest": "d8033cdd804a5454", "bytes_per_launch": 2 * (206.9e6 + 56.47e6)},
+                                          "digest": "13caa70b16a03ee3", "bytes_per_launch": 2 * (206.91e6 + 56.62e6)},
+    # the write-magnitude cache layer, 4 x 32 heads, n = 4096: one launch of each kernel
+    ("hola_prep", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola.cu", "lola_chain.cuh", "lola_internal.cuh"],
+                                             "digest": "3bdf5dec22f2559f", "bytes_per_launch": 268.47e6 + 744.45e6},
+    ("hola_state", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
+                                              "digest": "b1b344890c04080a", "bytes_per_launch": 675.40e6 + 240.09e6},
+    ("hola_read", "hola_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
+                                             "digest": "a760322973f38312", "bytes_per_launch": 671.69e6 + 118.10e6},
 }
 
 
@@ -686,18 +693,21 @@ def run_hola(L, R, args, pk, steps=10):
         t = kt["hola_state"]["avg_ms"]
         a = fl["state"] * ht / (t * 1e-3) / 1e12
         kr["hola_state"] = {"bound": "alu", "achieved": a, "peak": pk["fp32_tflops"], "unit": "TFLOP/s",
-                            "frac": a / pk["fp32_tflops"], "flop_per_head_token": fl["state"], "traffic": None,
+                            "frac": a / pk["fp32_tflops"], "flop_per_head_token": fl["state"],
+                            "traffic": traffic("hola_state", wl["name"]),
                             "peak_source": "derived: SMs x 128 FP32 lanes x 2 x max SM clock"}
     if "hola_read" in kt:
         t = kt["hola_read"]["avg_ms"]
         a = fl["read"] * ht / (t * 1e-3) / 1e12
         kr["hola_read"] = {"bound": "tensor", "achieved": a, "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
-                           "frac": a / pk["bf16_tflops"], "flop_per_head_token": fl["read"], "traffic": None}
+                           "frac": a / pk["bf16_tflops"], "flop_per_head_token": fl["read"],
+                           "traffic": traffic("hola_read", wl["name"])}
     if "hola_prep" in kt:
         t = kt["hola_prep"]["avg_ms"]
         a = hola_prep_bytes_per_row(d) * ht / (t * 1e-3) / 1e9
         kr["hola_prep"] = {"bound": "hbm", "achieved": a, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                           "frac": a / pk["hbm_gbs"], "bytes_per_row": hola_prep_bytes_per_row(d), "traffic": None}
+                           "frac": a / pk["hbm_gbs"], "bytes_per_row": hola_prep_bytes_per_row(d),
+                           "traffic": traffic("hola_prep", wl["name"])}
     per_ht = fl["state"] + fl["read"]
     step_tf = per_ht * ht / (ms * 1e-3) / 1e12
     out = {"metric": "prefill tokens/s per layer (write-magnitude cache on a delta-rule state)",
