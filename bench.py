@@ -279,6 +279,8 @@ NCU_TRAFFIC = {
     # the write-magnitude cache layer, 4 x 32 heads, n = 4096: one launch of each kernel
     ("hola_prep", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola.cu", "lola_chain.cuh", "lola_internal.cuh"],
                                              "digest": "3bdf5dec22f2559f", "bytes_per_launch": 268.47e6 + 744.45e6},
+    ("hola_cache", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola.cu", "lola_chain.cuh", "lola_internal.cuh"],
+                                              "digest": "3bdf5dec22f2559f", "bytes_per_launch": 1.98e6 + 0.0},
     ("hola_state", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
                                               "digest": "b1b344890c04080a", "bytes_per_launch": 675.40e6 + 240.09e6},
     ("hola_read", "hola_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
@@ -710,6 +712,8 @@ def run_hola(L, R, args, pk, steps=10):
                            "traffic": traffic("hola_prep", wl["name"])}
     per_ht = fl["state"] + fl["read"]
     step_tf = per_ht * ht / (ms * 1e-3) / 1e12
+    tr = [traffic(k, wl["name"]) for k in names]
+    step_traffic = sum(tr) if all(t is not None for t in tr) else None
     out = {"metric": "prefill tokens/s per layer (write-magnitude cache on a delta-rule state)",
            "value": R.world * x.B * n / (ms * 1e-3), "unit": "tokens/s", "ms_per_step": ms, "steps": steps,
            "status": int(st), "dtype": "bf16",
@@ -717,7 +721,7 @@ def run_hola(L, R, args, pk, steps=10):
                       "inputs": "gauss q, k, v; alpha in (0.9, 1], beta in [0, 1)"},
            "roofline": {"kernel": "layer step (all kernels)", "bound": "tensor", "achieved": step_tf,
                         "peak": pk["bf16_tflops"], "unit": "TFLOP/s", "frac": step_tf / pk["bf16_tflops"],
-                        "flop_per_head_token": per_ht, "flop_terms": fl, "traffic": None},
+                        "flop_per_head_token": per_ht, "flop_terms": fl, "traffic": step_traffic},
            "kernels": {k: {**v, **kr.get(k, {})} for k, v in kt.items()}, "clocks": clk.summary()}
     if R.rank == 0 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline_hola(x, n)
