@@ -16,7 +16,8 @@
 //   K7b hola_state_tc_kernel the state path in chunked form on tcgen05 (lola_hola_tc.cu);
 //   K7c hola_cache_kernel    the persistent cache at every chunk start from the fixed scores, one
 //                            CTA per head: per chunk, the w best of the cache and the chunk's
-//                            tokens by (higher score, older position), ranked by counting;
+//                            tokens by (higher score, older position), ranked by counting among
+//                            the cache and the tokens that beat a full cache's w-th key;
 //   K7d the output pass (lola_output_tc.cu) in its cache-read mode: the pool is the chunk's
 //       persistent cache plus the chunk's tokens, on tcgen05, with the sink and the gated sum
 //       in its epilogue.
@@ -110,7 +111,8 @@ __global__ void __launch_bounds__(kCacheThreads) hola_cache_kernel(const float* 
                                                                    int chunk, int nck, int32_t* __restrict__ cache) {
     __shared__ uint64_t ck[kMaxCache + kMaxChunk];   // the candidates of one merge
     __shared__ uint64_t hk[kMaxCache];               // the cache, best first
-    const int tid = threadIdx.x, bh = blockIdx.x;
+    __shared__ int wsum[kCacheThreads / kWarp + 1];
+    const int tid = threadIdx.x, bh = blockIdx.x, warp = tid / kWarp, lane = tid % kWarp;
     const float* sc = scores + (int64_t)bh * n;
     int32_t* out = cache + (int64_t)bh * nck * w;
     int count = 0;
@@ -118,9 +120,27 @@ __global__ void __launch_bounds__(kCacheThreads) hola_cache_kernel(const float* 
         for (int i = tid; i < w; i += kCacheThreads)
             out[(int64_t)c * w + i] = i < count ? (int32_t)(0xffffffffu - (uint32_t)(hk[i] & 0xffffffffu)) : -1;
         if (c == nck - 1) break;
-        const int c0 = c * chunk, m = min(chunk, n - c0), N = count + m;
-        for (int i = tid; i < N; i += kCacheThreads) ck[i] = i < count ? hk[i] : cache_key(sc[c0 + i - count], c0 + i - count);
-        __syncthreads();
+        const int c0 = c * chunk, m = min(chunk, n - c0);
+        // A full cache keeps its w-th best key unless a new key beats it (keys are unique: score
+        // bits, then the inverted position), so only the chunk's tokens above that key compete.
+        const uint64_t floor_key = count == w && w > 0 ? hk[w - 1] : 0ull;
+        for (int i = tid; i < count; i += kCacheThreads) ck[i] = hk[i];
+        int N = count;
+        for (int base = 0; base < m; base += kCacheThreads) {
+            const int i = base + tid;
+            const uint64_t key = i < m ? cache_key(sc[c0 + i], c0 + i) : 0ull;
+            const bool in = i < m && key > floor_key;
+            const unsigned bal = __ballot_sync(0xffffffffu, in);
+            if (lane == 0) wsum[warp] = __popc(bal);
+            __syncthreads();
+            int off = N;
+            for (int q = 0; q < warp; ++q) off += wsum[q];
+            int tot = 0;
+            for (int q = 0; q < kCacheThreads / kWarp; ++q) tot += wsum[q];
+            if (in) ck[off + __popc(bal & ((1u << lane) - 1u))] = key;
+            N += tot;
+            __syncthreads();
+        }
         for (int i = tid; i < N; i += kCacheThreads) {
             const uint64_t ki = ck[i];
             int rank = 0;
