@@ -142,3 +142,18 @@ def test_small_decays_split_a_chunk(L):
     res = run_hola(L, x)
     for h in range(2):
         check_head(x, res, 0, h, 300)
+
+
+def test_tied_scores_keep_the_older_tokens(L):
+    """Many tokens with beta = 0 write nothing and score exactly 0: the cache decisions among
+    those ties (older token stays) and against the rest follow the oracle's rule exactly."""
+    x = synth.hola_inputs(1, 2, 700, 128, w=32, chunk=128, dtype="bf16", seed=12)
+    r = np.random.default_rng(12)
+    x.beta[0, 0, r.random(700) < 0.6] = 0.0      # most of head 0's tokens tie at score 0
+    x.beta[0, 1, :] = 0.0                        # head 1: every score ties, the oldest w stay
+    res = run_hola(L, x)
+    for h in range(2):
+        check_head(x, res, 0, h, 700)
+    caches = _gpu_caches(res, 0, 1, (700 + 127) // 128, 32)
+    for c, got in enumerate(caches):
+        np.testing.assert_array_equal(got, np.arange(min(32, c * 128)))
