@@ -229,14 +229,20 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 }
             }
         }
-        // positions and row bounds of block bb into ring slot bb % kRing (threads 0..63)
-        auto bounds = [&](int bb) {
+        // Positions and row bounds of block bb into ring slot bb % kRing (threads 0..63, one key
+        // each).  A key's position (a cache list entry or a window index) and its write step are
+        // two dependent global loads; they are issued ahead (the prologue batches blocks 0..5, the
+        // loop issues block b + 6's position and block b + 5's write step while it finishes block
+        // b + 4), so no block's bounds wait for memory on the loaders' path.
+        auto load_p = [&](int bb) -> int {
+            const int u = bb * kBN + ltid;
+            if (ltid >= kBN || u >= P) return -1;
+            return u < a.lam ? cpos[u] : wlo + (u - a.lam);
+        };
+        auto load_w = [&](int p) -> int { return (p >= 0 && !a.hola) ? wst[p] : -1; };   // (cache read: never written)
+        auto finish = [&](int bb, int p, int w) {
             const int sl = bb & (kRing - 1);
             if (ltid < kBN) {
-                const int u = bb * kBN + ltid;
-                int p = -1;
-                if (u < P) p = u < a.lam ? cpos[u] : wlo + (u - a.lam);
-                const int w = (p >= 0 && !a.hola) ? wst[p] : -1;   // (cache read: never written)
                 // row r = t - t0 sees key p exactly iff lo <= r < hi, linearly iff r >= llo
                 const int lo = p < 0 ? 255 : min(max(p - t0, 0), 255);
                 int hi = p < 0 ? 0 : (w < 0 ? 255 : min(max(w - t0, 0), 255));
@@ -252,11 +258,22 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 if ((ltid & 31) == 0) kfull[sl][ltid >> 5] = mlo | (mhi << 8) | (mll << 16);
             }
         };
-        for (int bb = 0; bb < min(nblk, kAhead); ++bb) bounds(bb);
+        int pq[kAhead + 2], wq[kAhead + 1];
+#pragma unroll
+        for (int bb = 0; bb < kAhead + 2; ++bb) pq[bb] = load_p(bb);
+#pragma unroll
+        for (int bb = 0; bb < kAhead + 1; ++bb) wq[bb] = load_w(pq[bb]);
+#pragma unroll
+        for (int bb = 0; bb < kAhead; ++bb)
+            if (bb < nblk) finish(bb, pq[bb], wq[bb]);
+        // the pipeline: block b + 4's (position, write step), block b + 5's position
+        int p4 = pq[kAhead], w4 = wq[kAhead], p5 = pq[kAhead + 1];
         ok = !loaders_or(!ok);
         int issued = 0;
         for (int b = 0; b < nblk && ok; ++b) {
             const int st = b % kStages, u0 = b * kBN, sl = b & (kRing - 1);
+            // block b + 5's write step and block b + 6's position, a whole iteration ahead of use
+            const int w5 = load_w(p5), p6 = load_p(b + kAhead + 2);
             bool fail = false;
             if (ltid == 0) {
                 if (b == 1) fail = !wait(B_H, 0);                      // stage 1 overlaps H_c
@@ -295,7 +312,10 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 }
                 cp_async_arrive_noinc(bar(B_KVFULL + st));
             }
-            if (b + kAhead < nblk) bounds(b + kAhead);   // its slot's block (b - 4) is long weighted
+            if (b + kAhead < nblk) finish(b + kAhead, p4, w4);   // its slot's block (b - 4) is long weighted
+            p4 = p5;
+            w4 = w5;
+            p5 = p6;
             loaders_or(false);                           // the ring slot is written before it is read
             if (ltid == 0) mbar_arrive1(bar(B_KVFULL + st));   // (releases the ring slots written so far)
             issued = b + 1;
