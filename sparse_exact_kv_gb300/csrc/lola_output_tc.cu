@@ -493,7 +493,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4) {
                 float lv[8];
-                if ((c4 & 1) == 0) {
+                if (hide_state) {
+                    // no key is linear for any row (llo = 255) and L was never computed
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) lv[j] = 0.f;
+                } else if ((c4 & 1) == 0) {
                     float l16[16];
                     tmem_ld16(tb + lane_off + TL(st) + 32 * hf + 8 * c4, l16);
                     tmem_wait_ld();
@@ -533,19 +537,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
             }
         }
         // ---- epilogue: y = O / l; thread (row, hf) writes output columns 64 hf .. 64 hf + 63 ----
+        // (cache read: the head's sink and gate and this thread's 64 state read-out values are
+        // fetched before the last product is waited for)
+        float sink_l2 = 0.f, gh = 1.f;
+        float4 yst[16];
+        if (a.hola) {
+            const int h = bh % a.Hh;
+            sink_l2 = a.sink[h] * kLog2e;
+            gh = a.gate[h];
+            if (t < n) {
+                const float4* ys = reinterpret_cast<const float4*>(a.ystate + (row0 + t) * kD + 64 * hf);
+#pragma unroll
+                for (int j4 = 0; j4 < 16; ++j4) yst[j4] = ys[j4];
+            }
+        }
         if (ok) ok = wwait(B_O, 0);
         fence_after();
         lpart[hf][row] = lp;
         weight_sync();
         if (ok) {
             float l = lpart[0][row] + lpart[1][row];
-            float gh = 1.f;
-            if (a.hola) {
-                // the null sink (value 0) joins the normaliser at the row's scale 2^-m
-                const int h = bh % a.Hh;
-                l += ex2(a.sink[h] * kLog2e - m_run);
-                gh = a.gate[h];
-            }
+            // the null sink (value 0) joins the normaliser at the row's scale 2^-m
+            if (a.hola) l += ex2(sink_l2 - m_run);
             const float inv = t < n ? gh / l : 0.f;
 #pragma unroll
             for (int cc = 0; cc < kD / 2; cc += 32) {
@@ -554,10 +567,9 @@ __global__ void __launch_bounds__(kThreadsTc, 1) output_tc_kernel(const __grid_c
                 tmem_wait_ld();
                 if (a.hola && t < n) {
                     // y = the state read-out + gate * the cache read
-                    const float4* ys = reinterpret_cast<const float4*>(a.ystate + (row0 + t) * kD + 64 * hf + cc);
 #pragma unroll
                     for (int j4 = 0; j4 < 8; ++j4) {
-                        const float4 y4 = ys[j4];
+                        const float4 y4 = yst[cc / 4 + j4];
                         o[4 * j4] = fmaf(o[4 * j4], inv, y4.x);
                         o[4 * j4 + 1] = fmaf(o[4 * j4 + 1], inv, y4.y);
                         o[4 * j4 + 2] = fmaf(o[4 * j4 + 2], inv, y4.z);
