@@ -141,3 +141,16 @@ def test_sharded_heads_reassemble_in_order():
     for _, _, Y, wpos in got:
         np.testing.assert_array_equal(Y, whole["Y"])
         np.testing.assert_array_equal(wpos, whole["write_pos"])
+
+
+def test_traffic_figures_bind_to_the_kernel_sources(monkeypatch):
+    """A DRAM-traffic figure is reported only for the kernel sources it was captured on: the
+    digest of the named files must match, else the figure is null."""
+    import bench
+    files = ["lola_hola.cu", "lola_internal.cuh"]
+    good = bench.sources_digest(files)
+    monkeypatch.setitem(bench.NCU_TRAFFIC, ("k", "w"), {"sources": files, "digest": good, "bytes_per_launch": 5.0})
+    assert bench.traffic("k", "w") == 5.0
+    monkeypatch.setitem(bench.NCU_TRAFFIC, ("k", "w"), {"sources": files, "digest": "0" * 16, "bytes_per_launch": 5.0})
+    assert bench.traffic("k", "w") is None
+    assert bench.traffic("no such kernel", "w") is None
