@@ -345,8 +345,9 @@ int64_t lola_hola_workspace_bytes(const lola_hola_config* cfg, int32_t n);
  *             at every chunk start (unordered, -1 for empty entries)
  *   workspace at least lola_hola_workspace_bytes(cfg, n) bytes (it holds the same scores and
  *             cache lists when those outputs are null, and the per-head status words).
- * Stream-ordered on `stream`; validation errors return before anything is enqueued.  A wait
- * of the read kernel that gives up sets ST-timeout bits readable with lola_hola_status. */
+ * Stream-ordered on `stream`; validation errors return before anything is enqueued.  A bounded
+ * wait of the state or read kernel that gives up sets ST-timeout bits readable with
+ * lola_hola_status. */
 int32_t lola_hola_prefill(const lola_hola_config* cfg, int32_t n, const void* Q, const void* K, const void* V,
                           const float* alpha, const float* beta, const float* gamma_q, const float* gamma_k,
                           const float* sink, const float* gate, void* Y, float* S_out, float* scores,
