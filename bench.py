@@ -264,14 +264,14 @@ NCU_TRAFFIC = {
     ("select", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"],
                                            "digest": "bbeedb523c50d005", "bytes_per_launch": 4 * (207.87e6 + 27.81e6)},
     ("output", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                           "digest": "2c867ed0c8ed977d", "bytes_per_launch": 4 * (372.92e6 + 56.13e6)},
+                                           "digest": "1804e703ccb01a83", "bytes_per_launch": 4 * (372.92e6 + 56.13e6)},
     ("phi", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
                                         "digest": "2bf9c2757e9b5350", "bytes_per_launch": 4 * (67.20e6 + 140.94e6)},
     ("phi_q", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
                                           "digest": "2bf9c2757e9b5350", "bytes_per_launch": 4 * (67.19e6 + 13.51e6)},
     # 4 x 32 heads, n = 4096: the output pass, one launch
     ("output", "w2_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                        "digest": "2c867ed0c8ed977d", "bytes_per_launch": 810.63e6 + 121.14e6},
+                                        "digest": "1804e703ccb01a83", "bytes_per_launch": 810.63e6 + 121.14e6},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
     ("decode", "w4_bf16_decode_b64h32"): {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"],
@@ -284,7 +284,7 @@ NCU_TRAFFIC = {
     ("hola_state", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
                                               "digest": "b1b344890c04080a", "bytes_per_launch": 675.40e6 + 240.09e6},
     ("hola_read", "hola_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                             "digest": "2c867ed0c8ed977d", "bytes_per_launch": 671.73e6 + 118.11e6},
+                                             "digest": "1804e703ccb01a83", "bytes_per_launch": 671.73e6 + 118.11e6},
 }
 
 

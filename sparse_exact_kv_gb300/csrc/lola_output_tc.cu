@@ -21,16 +21,18 @@
 // Roles (416 threads):
 //   * warps 9-12 (loaders): Q, phi(Q) and H_c tiles by TMA (cp.async.bulk.tensor, 128-byte
 //     swizzle, rows past n zero-filled); per 64-key pool block the keys' positions and row
-//     bounds (four blocks ahead, into a ring), then its K, phi(K), V rows into one of two
+//     bounds (four blocks ahead, into a ring; the positions and write steps they need are
+//     loaded an iteration earlier still), then its K, phi(K), V rows into one of three
 //     stages -- a window block (consecutive positions) as TMA tiles, a cache block
 //     (scattered positions) as 16-byte cp.async gathers from all 128 loader threads (many
 //     requests in flight);
 //   * warp 8 (MMA, one thread): O = phi(Q) H_c, then per block S = Q K^T and
-//     L = phi(Q) phi(K)^T into one of two TMEM buffers, and O += P V of the block before,
-//     each group committed to an mbarrier;
+//     L = phi(Q) phi(K)^T into one of two TMEM buffers, and O += P V of the block before
+//     with P read from TMEM, each group committed to an mbarrier;
 //   * warps 0-7 (weighting): two threads per query row (TMEM lane = row; warp w takes keys
 //     32 (w / 4) .. + 31 of every block) read S and L, apply the masks, agree on the row
-//     maximum, write bf16 P to shared memory and keep the row's partial normaliser.
+//     maximum, write bf16 P into one of two TMEM buffers and keep the row's partial
+//     normaliser.
 // Double buffers let block b + 1's S, L products and block b - 1's P V product run while
 // block b is weighted.  Every wait is bounded by %globaltimer (1 s, then a status bit in
 // the head's state and a per-launch abort flag).
