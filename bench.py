@@ -17,7 +17,10 @@ Beside it, in the same line:
   * `decode`: 64 x 32 heads whose state was prefilled from a 4096-token prefix, then all
     1024 single-token steps, timed as whole passes from the restored post-prefix state;
   * `e2e`: the same prefill through the C ABI from pinned host buffers, copies included;
-  * `cpu_baseline`: the float64 C oracle on a stated sample of the workload.
+  * `cpu_baseline`: the float64 C oracle on a stated sample of the workload;
+  * `hola`: the write-magnitude exact cache on a gated delta-rule state (4 x 32 heads,
+    n = 4096, w = 64, C = 256, bf16), one lola_hola_prefill per step, with each of its four
+    kernels' rooflines and its own float64 oracle baseline.
 
 With N processes (torchrun) the global batch is N blocks of B sequences, block r drawn with
 seed + r; rank r takes the contiguous slice of heads [r B Hh, (r + 1) B Hh) -- its block -- so
