@@ -285,7 +285,7 @@ NCU_TRAFFIC = {
     ("hola_cache", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola.cu", "lola_chain.cuh", "lola_internal.cuh"],
                                               "digest": "4ed204a47283df44", "bytes_per_launch": 1.98e6 + 0.0},
     ("hola_state", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                              "digest": "b1b344890c04080a", "bytes_per_launch": 675.40e6 + 240.09e6},
+                                              "digest": "1db7cad6ea083c46", "bytes_per_launch": 675.40e6 + 240.09e6},
     ("hola_read", "hola_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
                                              "digest": "1804e703ccb01a83", "bytes_per_launch": 671.73e6 + 118.11e6},
 }

@@ -20,14 +20,18 @@
 // product comes out with the value column on the lane and the solve needs no transposition:
 //   P1  D1 = R_0^T [K^; Q^]^T   (128 x 128: columns 0-63 the keys' predictions, 64-127 the
 //                                queries' read-outs)       and   GM = [K^; Q^] K^^T (128 x 64);
-//   the solve: thread c holds column c of W' in registers and runs a right-looking forward
-//   substitution with A' read from shared memory (broadcast), float32;
+//   the solve: thread c holds column c of W' in registers; the substitution runs in four blocks
+//   of 16 rows -- a diagonal block right-looking from registers with its A' entries read from
+//   shared memory (broadcast, float32), the rows below it updated by the split product
+//   TZ[:, 16 b ..] += U'_b^T A'_b^T (tcgen05, TMEM on the same lanes) -- so a thread loads the
+//   480 entries of the diagonal blocks instead of all 2,016 of A';
 //   P3  D1[:, 64..] += U'^T A_read^T (the chunk's read-out; A_read = masked Q^ K^^T)  and
 //       R^T += U'^T K^ (the state update; K^ read from the same tile as X, MN-major).
 // Float32 operands are split into bf16 hi + lo; each product is hi.hi + hi.lo + lo.hi with
 // float32 accumulation.  The unit rows arrive pre-split in the tile layout the descriptors read
 // (written by the row kernel, 64 KB per chunk, one bulk copy, two chunks in flight); the chunk's
-// value rows by a bulk copy one chunk ahead.  One CTA of 256 threads per head.
+// value rows by a bulk copy one chunk ahead; X K^^T of the next chunk is issued by a second
+// thread as soon as the current chunk's last products are.  One CTA of 256 threads per head.
 #include <utility>
 
 #include "lola_internal.cuh"
