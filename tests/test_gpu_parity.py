@@ -38,6 +38,7 @@ def _final_state_matches(lay, ref, eta, n, dtype):
     (128, 40, 100, 32, 500),   # lambda > 64: a 2-CTA cluster per head
     (128, 20, 300, 64, 700),   # 8-CTA cluster
     (128, 20, 1000, 64, 1200), # 16-CTA cluster (a non-portable size): the largest cache supported
+    (64, 8192, 16, 256, 8300), # the largest window supported
     (64, 200, 0, 64, 150),     # eta >= n: nothing written, full causal softmax
     (64, 8, 8, 16, 1),         # a single token
 ])
