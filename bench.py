@@ -265,29 +265,29 @@ NCU_TRAFFIC = {
     # scaled x4 to n = 131072 -- every kernel's traffic grows in proportion to the tokens (the
     # chain streams each key's rows once, the output pass reads one pool per 128-query tile)
     ("select", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_select.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                           "digest": "bbeedb523c50d005", "bytes_per_launch": 4 * (207.87e6 + 27.81e6)},
+                                           "digest": "745c94b1a3f6faf1", "bytes_per_launch": 4 * (207.87e6 + 27.81e6)},
     ("output", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                           "digest": "1804e703ccb01a83", "bytes_per_launch": 4 * (372.92e6 + 56.13e6)},
+                                           "digest": "012ab2a4689683b4", "bytes_per_launch": 4 * (372.92e6 + 56.13e6)},
     ("phi", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
-                                        "digest": "2bf9c2757e9b5350", "bytes_per_launch": 4 * (67.20e6 + 140.94e6)},
+                                        "digest": "e53710d10f162473", "bytes_per_launch": 4 * (67.20e6 + 140.94e6)},
     ("phi_q", "w5_bf16_h8_n131072_ar1"): {"sources": ["lola_phi.cu", "lola_phi_tc.cuh", "lola_tc.cuh", "lola_internal.cuh"],
-                                          "digest": "2bf9c2757e9b5350", "bytes_per_launch": 4 * (67.19e6 + 13.51e6)},
+                                          "digest": "e53710d10f162473", "bytes_per_launch": 4 * (67.19e6 + 13.51e6)},
     # 4 x 32 heads, n = 4096: the output pass, one launch
     ("output", "w2_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                        "digest": "1804e703ccb01a83", "bytes_per_launch": 810.63e6 + 121.14e6},
+                                        "digest": "012ab2a4689683b4", "bytes_per_launch": 810.63e6 + 121.14e6},
     # w4 decode captured at B = 32 (1024 heads, mean of 5 launches), scaled x2 to the B = 64 launch
     # (every byte is per head)
     ("decode", "w4_bf16_decode_b64h32"): {"sources": ["lola_decode.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                          "digest": "13caa70b16a03ee3", "bytes_per_launch": 2 * (206.91e6 + 56.62e6)},
+                                          "digest": "3f2a4be8572b1122", "bytes_per_launch": 2 * (206.91e6 + 56.62e6)},
     # the write-magnitude cache layer, 4 x 32 heads, n = 4096: one launch of each kernel
     ("hola_prep", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                             "digest": "4ed204a47283df44", "bytes_per_launch": 268.53e6 + 744.45e6},
+                                             "digest": "2816d23cf95ee96f", "bytes_per_launch": 268.53e6 + 744.45e6},
     ("hola_cache", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola.cu", "lola_chain.cuh", "lola_internal.cuh"],
-                                              "digest": "4ed204a47283df44", "bytes_per_launch": 1.98e6 + 0.0},
+                                              "digest": "2816d23cf95ee96f", "bytes_per_launch": 1.98e6 + 0.0},
     ("hola_state", "hola_bf16_b4h32_n4096"): {"sources": ["lola_hola_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                              "digest": "1db7cad6ea083c46", "bytes_per_launch": 675.40e6 + 240.09e6},
+                                              "digest": "5cb3c1dd5116a066", "bytes_per_launch": 675.40e6 + 240.09e6},
     ("hola_read", "hola_bf16_b4h32_n4096"): {"sources": ["lola_output_tc.cu", "lola_tc.cuh", "lola_internal.cuh"],
-                                             "digest": "1804e703ccb01a83", "bytes_per_launch": 671.73e6 + 118.11e6},
+                                             "digest": "012ab2a4689683b4", "bytes_per_launch": 671.73e6 + 118.11e6},
 }
 
 

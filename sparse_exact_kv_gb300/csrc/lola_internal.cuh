@@ -108,11 +108,6 @@ __device__ __forceinline__ float warp_max(float x) {
     return x;
 }
 
-// Candidate order of the allocation rule: smaller SRE^2 first, then the older position.
-__device__ __forceinline__ bool key_less(float a, int pa, float b, int pb) {
-    return a < b || (a == b && pa < pb);
-}
-
 // ---------------------------------------------------------------------------------
 // phi(x) = [softmax(W x), softmax(-W x)] for R rows at a time, computed by one warp.
 //   xs: the R rows x (d_k floats each, row stride DK) in shared memory;  Ws: W in shared

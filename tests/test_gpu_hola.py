@@ -86,7 +86,7 @@ def check_head(x, res, b, h, n):
     assert err.max() <= 2e-2, err.max()
     # rel-L2 against the two branches' magnitudes: y is a sum of the state read-out and the
     # gated cache read, each carrying its own rounding (the cache read's bf16 operands), so a
-    # near-cancelling sum (a single token, say) is judged by the size of its terms
+    # near-cancelling sum (a single token, say) is measured against the size of its terms
     scale = np.linalg.norm(np.abs(ys) + abs(float(x.gate[h])) * np.abs(oc))
     assert np.linalg.norm(got - want) <= 1e-2 * scale
 
