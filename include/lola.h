@@ -256,8 +256,8 @@ typedef enum {
     LOLA_KERNEL_OUTPUT = 3,      /* co-normalised output of every query */
     LOLA_KERNEL_DECODE = 4,      /* one decode step */
     LOLA_KERNEL_PHI_Q = 5,       /* prefill: feature map of Q (on the side stream) */
-    LOLA_KERNEL_HOLA_PREP = 6,   /* write-magnitude cache layer: unit and RMS-scaled q, k rows */
-    LOLA_KERNEL_HOLA_STATE = 7,  /* ... the sequential delta-rule state path and the scores */
+    LOLA_KERNEL_HOLA_PREP = 6,   /* write-magnitude cache layer: unit q, k tiles, RMS-scaled rows */
+    LOLA_KERNEL_HOLA_STATE = 7,  /* ... the delta-rule state path (chunked, tensor cores), scores */
     LOLA_KERNEL_HOLA_CACHE = 8,  /* ... the persistent cache at every chunk start */
     LOLA_KERNEL_HOLA_READ = 9,   /* ... the cache read and the gated sum */
     LOLA_KERNEL_COUNT = 10
