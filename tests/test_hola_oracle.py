@@ -151,3 +151,21 @@ def test_gate_zero_leaves_the_state_read_out():
     x.gate[:] = 0.0
     for (b, h), r in HR.hola_run(x).items():
         np.testing.assert_array_equal(r["Y"], r["y_state"])
+
+
+def test_hand_derived_worked_example():
+    """Six tokens on two axes, derived by hand in tests/golden/hola_worked_example.json: the
+    delta rule's residuals, decays and write strengths in exact fractions, a score tie at a chunk
+    start (the older token stays), RMS-scaled logits with per-channel query scales, the sink and
+    the gate."""
+    import json
+    import os
+    with open(os.path.join(os.path.dirname(__file__), "golden", "hola_worked_example.json")) as f:
+        g = json.load(f)
+    a = lambda key: np.asarray(g[key], dtype=np.float64)  # noqa: E731
+    out = HR.hola_head(a("q"), a("k"), a("v"), a("alpha"), a("beta"), a("gamma_q"), a("gamma_k"),
+                       float(g["sink"]), float(g["gate"]), int(g["w"]), int(g["chunk"]))
+    for key in ("scores", "S", "y_state", "o_cache", "Y"):
+        np.testing.assert_allclose(out[key], a(key), rtol=1e-13, atol=1e-15, err_msg=key)
+    for caches in (out["caches"], HR.topw_sorted(out["scores"], int(g["w"]), int(g["chunk"]))):
+        assert [list(map(int, c)) for c in caches] == g["caches"]
