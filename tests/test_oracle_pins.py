@@ -400,6 +400,29 @@ def test_chunk_mode_without_writes_is_causal_softmax(C, eta):
     np.testing.assert_allclose(o["Y"], R.causal_softmax_attention(q, k, v), rtol=1e-11, atol=1e-12)
 
 
+def test_chunk_mode_golden_worked_example():
+    """Hand-derived in tests/golden/chunk_allocation_mean_memory.json: with W = 0 the memory
+    read-out is the mean of the written values, so every SRE is worked out by hand; the first
+    scored start meets the empty-memory rule and a tie at the cut (the older token is written),
+    the second a key the memory recalls exactly.  Every read weight is 1, so y_t is the running
+    mean (each token read exactly once)."""
+    with open(os.path.join(GOLDEN, "chunk_allocation_mean_memory.json")) as f:
+        g = json.load(f)
+    a = lambda key: np.asarray(g[key], dtype=np.float64)  # noqa: E731
+    tr = []
+    o = R.lola_chunk_run(a("q"), a("k"), a("v"), a("W"), g["eta"], g["lambda"], g["C"], trace=tr)
+    assert len(tr) == len(g["decisions"])
+    for (c0, sq, written, kept), want in zip(tr, g["decisions"]):
+        assert c0 == want["start"]
+        assert {int(j): x for j, x in want["sre_sq"].items()} == pytest.approx(sq, rel=1e-15, abs=1e-15)
+        assert list(written) == want["written"] and sorted(kept) == want["kept"]
+    assert o["write_step"].tolist() == g["write_step"]
+    assert o["cache"].tolist() == g["final_cache"] and o["window"].tolist() == g["final_window"]
+    np.testing.assert_allclose(o["H"], a("H"), rtol=1e-15)
+    np.testing.assert_allclose(o["s"], a("s"), rtol=1e-15)
+    np.testing.assert_allclose(o["Y"], a("y"), rtol=1e-14, atol=1e-15)
+
+
 @pytest.mark.parametrize("C,eta,lam", [(4, 8, 6), (8, 8, 5), (8, 16, 12)])
 def test_chunk_mode_keeps_the_highest_sre_and_writes_each_key_once(C, eta, lam):
     """Every scored decision keeps exactly lambda candidates, all with larger (SRE, position)
