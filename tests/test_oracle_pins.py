@@ -681,6 +681,25 @@ def test_window_scores_of_a_key_seen_by_one_query():
     np.testing.assert_allclose(R.window_scores(q, k, W, 1, "kernel_ratio"), 2.0 / e, rtol=1e-15)
 
 
+def test_fixed_score_golden_worked_example():
+    """Hand-derived in tests/golden/query_scores_two_axes.json: queries and keys on two axes
+    make every softmax weight 1 or 2 and (W = 0) every linear weight 1, so the four scores,
+    each kind's decisions (a tie between a cached key and the evictee included) and the reads
+    are worked out by hand."""
+    with open(os.path.join(GOLDEN, "query_scores_two_axes.json")) as f:
+        g = json.load(f)
+    a = lambda key: np.asarray(g[key], dtype=np.float64)  # noqa: E731
+    for kind, want in g["kinds"].items():
+        np.testing.assert_allclose(R.window_scores(a("q"), a("k"), a("W"), g["eta"], kind), want["score"],
+                                   rtol=1e-15, atol=1e-15)
+        o = R.lola_run_fixed_score(a("q"), a("k"), a("v"), a("W"), g["eta"], g["lambda"], kind)
+        np.testing.assert_allclose(o["score"], want["score"], rtol=1e-15, atol=1e-15)
+        assert o["write_pos"].tolist() == want["write_pos"], kind
+        assert o["cache"].tolist() == want["final_cache"], kind
+        assert sorted(o["window"].tolist()) == g["final_window"]
+        np.testing.assert_allclose(o["Y"], a("y"), rtol=1e-14, atol=1e-15)
+
+
 def test_fixed_score_replay_of_own_and_of_a_swapped_log():
     """Replaying the own log reproduces it with no gap; writing, at one decision, the lowest
     kept key instead of the written one is followed and reported as their relative score
