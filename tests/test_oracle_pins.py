@@ -550,6 +550,21 @@ def test_sre_at_first_write_is_the_rank_one_shrink_of_the_score():
     assert (base[o["write_step"] < 0] == 0).all()
 
 
+def test_sre_maps_golden_worked_example():
+    """Hand-derived in tests/golden/sre_maps_mean_memory.json: with W = 0 the memory read-out
+    is the mean of the held values, so the SRE map (Fig. 3), the first-write baseline (two keys
+    written at one chunk start share their first memory) and the relative map (Fig. 10,
+    Eq. 26) are worked out by hand."""
+    with open(os.path.join(GOLDEN, "sre_maps_mean_memory.json")) as f:
+        g = json.load(f)
+    a = lambda key: np.asarray(g[key], dtype=np.float64)  # noqa: E731
+    k, v, W, ws, times = a("k"), a("v"), a("W"), g["write_step"], g["times"]
+    np.testing.assert_allclose(R.sre_map(k, v, W, ws, times), a("sre_map"), rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(R.sre_at_first_write(k, v, W, ws), a("sre_at_first_write"), rtol=1e-15, atol=1e-15)
+    np.testing.assert_allclose(R.sre_map_relative(k, v, W, ws, times), a("sre_map_relative"), rtol=1e-14,
+                               atol=1e-15)
+
+
 def test_sre_map_relative_is_zero_right_after_the_write_and_tracks_later_writes():
     """Per token: at the time right after its write the relative SRE of a key is 0; later it
     is the map's SRE minus that baseline.  Chunk mode: the keys written at one chunk start
