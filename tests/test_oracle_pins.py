@@ -117,6 +117,10 @@ def test_golden_worked_examples(name):
         if "H" in g and "H" in out:
             np.testing.assert_allclose(out["H"], g["H"], rtol=1e-13)
             np.testing.assert_allclose(out["s"], g["s"], rtol=1e-13)
+    for mask, want in g.get("y_read_mask", {}).items():
+        for out in _all_forms(g["q"], g["k"], g["v"], g["W"], eta, lam, read_mask=int(mask)):
+            assert list(out["write_pos"]) == [int(x) for x in g["write_pos"]]
+            np.testing.assert_allclose(out["Y"], want, rtol=1e-13, atol=1e-13)
 
 
 # ---------------------------------------------------------------------------
